@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs for the gated delta rule workloads.
+
+This module only draws random tensors; it contains none of the recurrence's
+arithmetic, so both the CUDA path's tests and the float64 oracle can consume
+what it returns.
+
+Recipe (the same for every workload):
+  * a CPU ``torch.Generator`` seeded with the workload's seed;
+  * draws, in float32 and in this order: q, k, v, alpha-logits, beta-logits,
+    initial state, d_o, d_final_state (all drawn every time, so the stream of
+    random numbers does not depend on which are used);
+  * q, k ~ N(0,1) then divided by their L2 norm over the key dimension, per
+    (b, t, h); v ~ N(0,1); alpha = exp(-softplus(x)); beta = sigmoid(x);
+  * initial state ~ N(0, init_std^2) (zero state when init_std == 0);
+    d_o ~ N(0,1); d_final_state ~ N(0, dfinal_std^2) (absent when 0);
+  * finally every tensor except the fp32 states is cast to the run dtype.
+    The oracle receives exactly these cast values (upcast to float64).
+
+The workloads are the five problem shapes the method is measured on: a tiny
+fp32 case, a small bf16 forward, a medium and a large bf16 training shape, and a
+long-context bf16 stream processed in four calls.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+
+import torch
+import torch.nn.functional as F
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int
+    H: int
+    K: int
+    V: int
+    chunk: int
+    dtype: str            # "f32" or "bf16"
+    seed: int
+    init_std: float = 0.0
+    dfinal_std: float = 0.0
+    backward: bool = False
+    calls: int = 1        # streaming: the sequence is processed in this many calls
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def token_heads(self) -> int:
+        return self.B * self.T * self.H
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_f32_B1_T64_H2_K16_V16", 1, 64, 2, 16, 16, 16, "f32", seed=0,
+                 backward=True),
+        Workload("fwd_bf16_B2_T1024_H4_K64_V64", 2, 1024, 4, 64, 64, 64, "bf16", seed=1,
+                 init_std=0.1),
+        Workload("train_bf16_B4_T2048_H6_K128_V128", 4, 2048, 6, 128, 128, 64, "bf16",
+                 seed=2, backward=True),
+        Workload("train_bf16_B8_T4096_H6_K128_V128", 8, 4096, 6, 128, 128, 64, "bf16",
+                 seed=3, dfinal_std=0.01, backward=True),
+        Workload("stream_bf16_B1_T32768_H16_K128_V128_4calls", 1, 32768, 16, 128, 128, 64,
+                 "bf16", seed=4, init_std=0.1, calls=4),
+    ]
+}
+
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+
+
+def make_inputs(w: Workload, device="cpu") -> dict:
+    """Draw the inputs of workload ``w`` (see the module docstring for the recipe).
+
+    Returns a dict with q, k, v, alpha, beta in the run dtype, and
+    initial_state, d_o (run dtype), d_final_state (fp32 or None)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed))
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    f32 = torch.float32
+    q = torch.randn(B, T, H, K, generator=g, dtype=f32)
+    k = torch.randn(B, T, H, K, generator=g, dtype=f32)
+    v = torch.randn(B, T, H, V, generator=g, dtype=f32)
+    a_logit = torch.randn(B, T, H, generator=g, dtype=f32)
+    b_logit = torch.randn(B, T, H, generator=g, dtype=f32)
+    s0 = torch.randn(B, H, V, K, generator=g, dtype=f32)
+    d_o = torch.randn(B, T, H, V, generator=g, dtype=f32)
+    dsT = torch.randn(B, H, V, K, generator=g, dtype=f32)
+
+    q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    alpha = torch.exp(-F.softplus(a_logit))
+    beta = torch.sigmoid(b_logit)
+    dt = torch_dtype(w.dtype)
+    out = dict(
+        q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=alpha.to(dt), beta=beta.to(dt),
+        initial_state=(s0 * w.init_std) if w.init_std > 0 else None,
+        d_o=d_o.to(dt),
+        d_final_state=(dsT * w.dfinal_std) if w.dfinal_std > 0 else None,
+    )
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def custom(name="custom", B=1, T=64, H=2, K=16, V=16, chunk=16, dtype="f32", seed=0,
+           init_std=0.0, dfinal_std=0.0, backward=True) -> Workload:
+    """A workload of any shape with the same recipe (for edge-case tests)."""
+    return Workload(name, B, T, H, K, V, chunk, dtype, seed, init_std, dfinal_std, backward)
