@@ -1,0 +1,312 @@
+// api.cu -- the C ABI of libgdn.so (declared in include/gdn.h).
+//
+// Host-side only: argument checks (before any launch), workspace carving, and
+// the launch sequence on the caller's stream.  Nothing here allocates device
+// memory or synchronises.
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool supported_dim(int64_t x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+
+// Checks the problem and fills Dims.  Returns GDN_OK or an error status.
+gdn_status check_problem(const gdn_problem* p, gdn::Dims* d) {
+    if (!p) return fail(GDN_ERR_INVALID_ARG, "problem pointer is NULL");
+    if (p->B < 0 || p->T < 0 || p->H < 0)
+        return fail(GDN_ERR_INVALID_ARG, "negative size (B=%lld T=%lld H=%lld)",
+                    (long long)p->B, (long long)p->T, (long long)p->H);
+    if (p->dtype != GDN_F32 && p->dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "dtype %d is not GDN_F32 or GDN_BF16", (int)p->dtype);
+    if (!supported_dim(p->K) || !supported_dim(p->V))
+        return fail(GDN_ERR_UNSUPPORTED, "K=%lld V=%lld: each must be 16, 32, 64 or 128",
+                    (long long)p->K, (long long)p->V);
+    if (p->chunk != 16 && p->chunk != 32 && p->chunk != 64)
+        return fail(GDN_ERR_UNSUPPORTED, "chunk=%d: must be 16, 32 or 64", (int)p->chunk);
+    if (p->B > 65535 || p->H > 65535)
+        return fail(GDN_ERR_UNSUPPORTED, "B=%lld H=%lld: each must be <= 65535",
+                    (long long)p->B, (long long)p->H);
+    if (p->T > (int64_t)1 << 30)
+        return fail(GDN_ERR_UNSUPPORTED, "T=%lld exceeds 2^30", (long long)p->T);
+    d->B = (int)p->B;
+    d->T = (int)p->T;
+    d->H = (int)p->H;
+    d->K = (int)p->K;
+    d->V = (int)p->V;
+    d->C = p->chunk;
+    d->NC = (int)((p->T + p->chunk - 1) / p->chunk);
+    return GDN_OK;
+}
+
+// Workspace carving.  With base == nullptr only the size is computed.
+struct Carver {
+    char* base;
+    size_t off = 0;
+    template <typename T>
+    T* take(size_t count) {
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += round_up(count * sizeof(T));
+        return p;
+    }
+};
+
+size_t carve_chunk(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, bool with_T) {
+    const size_t nchunks = (size_t)d.NS() * d.NC;
+    const size_t C = d.C;
+    cb->G = cv.take<float>(nchunks * C);
+    cb->W = cv.take<float>(nchunks * C * d.K);
+    cb->Ut = cv.take<float>(nchunks * C * d.V);
+    cb->Mqk = cv.take<float>(nchunks * C * C);
+    cb->Tm = with_T ? cv.take<float>(nchunks * C * C) : nullptr;
+    return cv.off;
+}
+
+size_t carve_bwd(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, gdn::BwdBufs* bb,
+                 bool need_states) {
+    carve_chunk(d, cv, cb, true);
+    const size_t nchunks = (size_t)d.NS() * d.NC;
+    const size_t C = d.C, VK = (size_t)d.V * d.K;
+    bb->states = need_states ? cv.take<float>(nchunks * VK) : nullptr;
+    bb->U = cv.take<float>(nchunks * C * d.V);
+    bb->dU = cv.take<float>(nchunks * C * d.V);
+    bb->dS1 = cv.take<float>(nchunks * VK);
+    bb->dW = cv.take<float>(nchunks * C * d.K);
+    bb->dQ1 = cv.take<float>(nchunks * C * d.K);
+    bb->dKh = cv.take<float>(nchunks * C * d.K);
+    return cv.off;
+}
+
+struct Span {
+    const void* p;
+    size_t n;
+    const char* name;
+};
+
+bool overlap(const Span& a, const Span& b) {
+    if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+    const char* a0 = (const char*)a.p;
+    const char* b0 = (const char*)b.p;
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+gdn_status check_ptr(const Span& s, bool required) {
+    if (!s.p) {
+        if (required && s.n > 0) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", s.name);
+        return GDN_OK;
+    }
+    if (((uintptr_t)s.p) % 16 != 0)
+        return fail(GDN_ERR_INVALID_ARG, "%s is not 16-byte aligned", s.name);
+    return GDN_OK;
+}
+
+// Every output must be disjoint from every input and from every other output;
+// `allow_same` lists (output, input) pairs that may be the identical buffer.
+gdn_status check_overlaps(const Span* ins, int nin, const Span* outs, int nout,
+                          const void* same_out, const void* same_in) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j) {
+            if (outs[i].p && outs[i].p == same_out && ins[j].p == same_in) continue;
+            if (overlap(outs[i], ins[j]))
+                return fail(GDN_ERR_INVALID_ARG, "output %s overlaps input %s", outs[i].name,
+                            ins[j].name);
+        }
+        for (int j = i + 1; j < nout; ++j)
+            if (overlap(outs[i], outs[j]))
+                return fail(GDN_ERR_INVALID_ARG, "outputs %s and %s overlap", outs[i].name,
+                            outs[j].name);
+    }
+    return GDN_OK;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported problem";
+        case GDN_ERR_WORKSPACE: return "workspace too small";
+        case GDN_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+const char* gdn_last_error(void) { return g_err; }
+
+size_t gdn_fwd_workspace_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    Carver cv{nullptr};
+    gdn::ChunkBufs cb;
+    return carve_chunk(d, cv, &cb, false);
+}
+
+size_t gdn_saved_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    return (size_t)d.NS() * d.NC * d.V * d.K * sizeof(float);
+}
+
+size_t gdn_bwd_workspace_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    Carver cv{nullptr};
+    gdn::ChunkBufs cb;
+    gdn::BwdBufs bb;
+    return carve_bwd(d, cv, &cb, &bb, true);
+}
+
+gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* alpha, const void* beta, const float* initial_state,
+                   void* o, float* final_state, void* saved, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const size_t need = gdn_fwd_workspace_bytes(p);
+    const Span ins[] = {{q, BTH * d.K * es, "q"},       {k, BTH * d.K * es, "k"},
+                        {v, BTH * d.V * es, "v"},       {alpha, BTH * es, "alpha"},
+                        {beta, BTH * es, "beta"},       {initial_state, nstate, "initial_state"}};
+    const Span outs[] = {{o, BTH * d.V * es, "o"},
+                         {final_state, nstate, "final_state"},
+                         {saved, gdn_saved_bytes(p), "saved"},
+                         {workspace, need, "workspace"}};
+    for (int i = 0; i < 6; ++i)  // initial_state is optional
+        if ((st = check_ptr(ins[i], i != 5)) != GDN_OK) return st;
+    for (int i = 0; i < 4; ++i)  // final_state and saved are optional
+        if ((st = check_ptr(outs[i], i == 0 || i == 3)) != GDN_OK) return st;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                    need);
+    if ((st = check_overlaps(ins, 6, outs, 4, final_state, initial_state)) != GDN_OK) return st;
+
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (d.NS() == 0) return GDN_OK;
+    if (d.T == 0) {  // empty sequence: the final state is the initial state
+        cudaError_t e = cudaSuccess;
+        if (final_state && final_state != initial_state)
+            e = initial_state ? cudaMemcpyAsync(final_state, initial_state, nstate,
+                                                cudaMemcpyDeviceToDevice, cs)
+                              : cudaMemsetAsync(final_state, 0, nstate, cs);
+        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "empty-sequence state copy");
+    }
+    const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    Carver cv{(char*)workspace};
+    gdn::ChunkBufs cb;
+    carve_chunk(d, cv, &cb, false);
+    cudaError_t e = gdn::launch_prep(d, ty, k, q, v, alpha, beta, cb, false, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "chunk kernel");
+    e = gdn::launch_scan_fwd(d, ty, q, k, cb, initial_state, o, final_state, (float*)saved,
+                             true, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "scan kernel");
+    return GDN_OK;
+}
+
+gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* alpha, const void* beta, const float* initial_state,
+                   const void* saved, const void* d_o, const float* d_final_state,
+                   void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
+                   float* d_initial_state, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const size_t need = gdn_bwd_workspace_bytes(p);
+    const Span ins[] = {{q, BTH * d.K * es, "q"},
+                        {k, BTH * d.K * es, "k"},
+                        {v, BTH * d.V * es, "v"},
+                        {alpha, BTH * es, "alpha"},
+                        {beta, BTH * es, "beta"},
+                        {initial_state, nstate, "initial_state"},
+                        {saved, gdn_saved_bytes(p), "saved"},
+                        {d_o, BTH * d.V * es, "d_o"},
+                        {d_final_state, nstate, "d_final_state"}};
+    const Span outs[] = {{dq, BTH * d.K * es, "dq"},
+                         {dk, BTH * d.K * es, "dk"},
+                         {dv, BTH * d.V * es, "dv"},
+                         {dalpha, BTH * es, "dalpha"},
+                         {dbeta, BTH * es, "dbeta"},
+                         {d_initial_state, nstate, "d_initial_state"},
+                         {workspace, need, "workspace"}};
+    for (int i = 0; i < 9; ++i) {
+        const bool req = !(i == 5 || i == 6 || i == 8);
+        if ((st = check_ptr(ins[i], req)) != GDN_OK) return st;
+    }
+    for (int i = 0; i < 7; ++i)
+        if ((st = check_ptr(outs[i], i != 5)) != GDN_OK) return st;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                    need);
+    if ((st = check_overlaps(ins, 9, outs, 7, d_initial_state, d_final_state)) != GDN_OK)
+        return st;
+
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (d.NS() == 0) return GDN_OK;
+    if (d.T == 0) {  // empty sequence: d(initial state) = d(final state)
+        cudaError_t e = cudaSuccess;
+        if (d_initial_state && d_initial_state != d_final_state)
+            e = d_final_state ? cudaMemcpyAsync(d_initial_state, d_final_state, nstate,
+                                                cudaMemcpyDeviceToDevice, cs)
+                              : cudaMemsetAsync(d_initial_state, 0, nstate, cs);
+        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "empty-sequence state copy");
+    }
+    const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    Carver cv{(char*)workspace};
+    gdn::ChunkBufs cb;
+    gdn::BwdBufs bb;
+    carve_bwd(d, cv, &cb, &bb, saved == nullptr);
+    const float* states = saved ? (const float*)saved : bb.states;
+    cudaError_t e = gdn::launch_prep(d, ty, k, q, v, alpha, beta, cb, true, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "chunk kernel");
+    if (!saved) {
+        e = gdn::launch_scan_fwd(d, ty, q, k, cb, initial_state, nullptr, nullptr, bb.states,
+                                 false, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "state recompute kernel");
+    }
+    e = gdn::launch_scan_bwd(d, ty, q, k, d_o, cb, states, d_final_state, bb, d_initial_state,
+                             cs);
+    if (e != cudaSuccess) return cuda_fail(e, "reverse scan kernel");
+    e = gdn::launch_grad(d, ty, q, k, v, alpha, beta, d_o, cb, states, bb, dq, dk, dv, dalpha,
+                         dbeta, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "chunk gradient kernel");
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// gdn_internal.h -- shapes, workspace layout and kernel launchers shared by the
+// translation units of libgdn.so (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Problem dimensions as the kernels see them.  NC = ceil(T / C) chunks per
+// (b, h) stream; NS = B * H streams.  All index arithmetic that can exceed 2^31
+// is done in int64.
+struct Dims {
+    int B, T, H, K, V, C, NC;
+    int64_t NS() const { return (int64_t)B * H; }
+};
+
+// Per-chunk results of the chunk-parallel step (Phase 1 + solve + recompute),
+// float32, indexed [stream][chunk][...]:
+//   G   [C]     within-chunk cumulative log alpha
+//   W   [C,K]   T diag(beta*gamma) K
+//   Ut  [C,V]   T diag(beta) V
+//   Mqk [C,C]   lower(Gamma .* Q K^T)
+//   Tm  [C,C]   (I + A)^-1   (backward only)
+struct ChunkBufs {
+    float* G;
+    float* W;
+    float* Ut;
+    float* Mqk;
+    float* Tm;
+};
+
+// Backward-only buffers, float32:
+//   states [NS,NC,V,K] chunk-start states (when the caller passed no `saved`)
+//   U, dU  [NS,NC,C,V] corrected writes and their gradient
+//   dS1    [NS,NC,V,K] gradient of each chunk's end state
+//   dW, dQ1, dKh [NS,NC,C,K] chunk-local gradient scratch
+struct BwdBufs {
+    float* states;
+    float* U;
+    float* dU;
+    float* dS1;
+    float* dW;
+    float* dQ1;
+    float* dKh;
+};
+
+enum class InType { F32 = 0, BF16 = 1 };
+
+// Launchers of the SIMT (CUDA-core, float32) kernels.  Each returns the
+// cudaError_t of its launch.
+cudaError_t launch_prep(const Dims& d, InType ty, const void* k, const void* q,
+                        const void* v, const void* alpha, const void* beta,
+                        const ChunkBufs& cb, bool write_T, cudaStream_t st);
+cudaError_t launch_scan_fwd(const Dims& d, InType ty, const void* q, const void* k,
+                            const ChunkBufs& cb, const float* s0, void* o, float* sT,
+                            float* states, bool write_o, cudaStream_t st);
+cudaError_t launch_scan_bwd(const Dims& d, InType ty, const void* q, const void* k,
+                            const void* d_o, const ChunkBufs& cb, const float* states,
+                            const float* dsT, const BwdBufs& bb, float* ds0,
+                            cudaStream_t st);
+cudaError_t launch_grad(const Dims& d, InType ty, const void* q, const void* k,
+                        const void* v, const void* alpha, const void* beta,
+                        const void* d_o, const ChunkBufs& cb, const float* states,
+                        const BwdBufs& bb, void* dq, void* dk, void* dv, void* dalpha,
+                        void* dbeta, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,227 @@
+"""Python binding of libgdn.so (the C ABI declared in include/gdn.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, device buffers (outputs, workspace, saved states) are allocated with
+torch, and the call goes through ctypes to the C entry point of the same name on
+torch's current CUDA stream.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or Python fallback -- if the library is
+missing, importing or calling raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = range(5)
+GDN_F32, GDN_BF16 = 0, 1
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"gdn status {status}: {message}")
+        self.status = status
+
+
+class gdn_problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("V", ctypes.c_int64), ("chunk", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def load_library():
+    """Load libgdn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(gdn_problem)
+    lib.gdn_version.restype = ctypes.c_int
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    for fn in ("gdn_fwd_workspace_bytes", "gdn_saved_bytes", "gdn_bwd_workspace_bytes"):
+        getattr(lib, fn).argtypes = [P]
+        getattr(lib, fn).restype = ctypes.c_size_t
+    lib.gdn_fwd.argtypes = [P] + [_vp] * 10 + [ctypes.c_size_t, _vp]
+    lib.gdn_fwd.restype = ctypes.c_int
+    lib.gdn_bwd.argtypes = [P] + [_vp] * 16 + [ctypes.c_size_t, _vp]
+    lib.gdn_bwd.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_workspace_bytes",
+            "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd")
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return GDN_F32
+    if dt == torch.bfloat16:
+        return GDN_BF16
+    raise GdnError(GDN_ERR_UNSUPPORTED, f"dtype {dt} (use float32 or bfloat16)")
+
+
+def make_problem(B, T, H, K, V, chunk=64, dtype=torch.bfloat16) -> gdn_problem:
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return gdn_problem(int(B), int(T), int(H), int(K), int(V), int(chunk), int(code))
+
+
+def gdn_version() -> int:
+    return int(load_library().gdn_version())
+
+
+def gdn_status_string(status: int) -> str:
+    return load_library().gdn_status_string(int(status)).decode()
+
+
+def gdn_last_error() -> str:
+    return load_library().gdn_last_error().decode()
+
+
+def gdn_fwd_workspace_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_fwd_workspace_bytes(ctypes.byref(p)))
+
+
+def gdn_saved_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_saved_bytes(ctypes.byref(p)))
+
+
+def gdn_bwd_workspace_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GdnError(status, gdn_last_error() or gdn_status_string(status))
+
+
+def _need(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    if t.dtype != dtype:
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise GdnError(GDN_ERR_INVALID_ARG, f"{name} must be contiguous")
+
+
+def _stream_handle(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def gdn_fwd(q, k, v, alpha, beta, initial_state=None, *, chunk: int = 64, o=None,
+            final_state=True, saved=False, workspace=None, stream=None):
+    """Chunkwise gated delta rule forward.
+
+    q, k [B,T,H,K]; v [B,T,H,V]; alpha, beta [B,T,H] (all float32 or all bf16,
+    contiguous, on one CUDA device); initial_state float32 [B,H,V,K] or None.
+    ``final_state``: True (allocate), a float32 tensor to fill (may be
+    initial_state itself), or False/None (not written).  ``saved``: True to
+    allocate and return the chunk-boundary states for :func:`gdn_bwd`, or a
+    uint8/float tensor of at least gdn_saved_bytes() bytes.
+    Returns ``(o, final_state or None, saved or None)``.
+    """
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dt = q.dtype
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    _need(k, "k", (B, T, H, K), dt, dev)
+    _need(v, "v", (B, T, H, V), dt, dev)
+    _need(q, "q", (B, T, H, K), dt, dev)
+    _need(alpha, "alpha", (B, T, H), dt, dev)
+    _need(beta, "beta", (B, T, H), dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=dt, device=dev)
+    _need(o, "o", (B, T, H, V), dt, dev)
+    if final_state is True:
+        final_state = torch.empty((B, H, V, K), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", (B, H, V, K), torch.float32, dev)
+    if saved is True:
+        saved = torch.empty(max(gdn_saved_bytes(p), 1), dtype=torch.uint8, device=dev)
+    elif saved is False:
+        saved = None
+    ws_need = gdn_fwd_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                     _ptr(initial_state), _ptr(o), _ptr(final_state), _ptr(saved),
+                     _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
+    _check(st)
+    return o, final_state, saved
+
+
+def gdn_bwd(q, k, v, alpha, beta, initial_state, d_o, d_final_state=None, *, saved=None,
+            chunk: int = 64, grads=None, d_initial_state=True, workspace=None, stream=None):
+    """Gradients of ``sum(d_o * o) + sum(d_final_state * final_state)``.
+
+    ``saved`` is the buffer returned by ``gdn_fwd(..., saved=True)`` with the same
+    inputs, or None (the chunk-boundary states are then recomputed).
+    Returns ``(dq, dk, dv, dalpha, dbeta, d_initial_state or None)``.
+    """
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dt = q.dtype
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    for t, n, s in ((k, "k", (B, T, H, K)), (v, "v", (B, T, H, V)), (q, "q", (B, T, H, K)),
+                    (alpha, "alpha", (B, T, H)), (beta, "beta", (B, T, H)),
+                    (d_o, "d_o", (B, T, H, V))):
+        _need(t, n, s, dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    _need(d_final_state, "d_final_state", (B, H, V, K), torch.float32, dev)
+    if saved is not None and saved.numel() * saved.element_size() < gdn_saved_bytes(p):
+        raise GdnError(GDN_ERR_INVALID_ARG, "saved buffer is smaller than gdn_saved_bytes()")
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.empty_like(alpha), torch.empty_like(beta))
+    dq, dk, dv, da, db = grads
+    if d_initial_state is True:
+        d_initial_state = torch.empty((B, H, V, K), dtype=torch.float32, device=dev)
+    elif d_initial_state is False:
+        d_initial_state = None
+    ws_need = gdn_bwd_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                     _ptr(initial_state), _ptr(saved), _ptr(d_o), _ptr(d_final_state),
+                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(db), _ptr(d_initial_state),
+                     _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
+    _check(st)
+    return dq, dk, dv, da, db, d_initial_state

@@ -1,0 +1,128 @@
+/*
+ * gdn.h -- C ABI of the GB300 chunkwise gated delta rule library (libgdn.so).
+ *
+ * The operation ("Sparse Delta Memory: layer and kernels", "What the layer
+ * computes" and its dense-limit paragraph; "OpenGDN", "Core operator reference"):
+ *
+ *     S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t                      (read after the write, no scale on q)
+ *
+ * per (batch b, head h) stream, computed chunkwise with the extended-WY
+ * decomposition: per chunk of `chunk` tokens the decay-weighted Gram matrices,
+ * the solve T = (I + strict_lower(diag(beta) (Gamma .* K K^T)))^-1, the
+ * recompute W = T diag(beta gamma) K and U~ = T diag(beta) V, then a sequential
+ * scan over chunks that keeps the state on chip ("Sparse Delta Memory", "What
+ * the layer computes": Phase 1, Solve, Phase 2; "OpenGDN", "Core operator
+ * reference": the 64-token extended-WY chunk form with FP32 state).
+ *
+ * Layouts (all dense, row-major, no strides):
+ *   q, k            [B, T, H, K]   dtype
+ *   v, o            [B, T, H, V]   dtype
+ *   alpha, beta     [B, T, H]      dtype   (linear gates; precondition 0 < alpha <= 1)
+ *   states          [B, H, V, K]   float32 (initial/final state and their gradients)
+ *   gradients       same shape and dtype as the input they belong to
+ * dtype is GDN_F32 or GDN_BF16 (bf16 results are rounded to nearest even); every
+ * accumulation, the gates, the solve and the state are float32 in both cases.
+ *
+ * Ownership and execution: the caller owns every buffer (device memory).  The
+ * library allocates nothing, never synchronises, and enqueues all work on
+ * `stream` (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ * Results are ready when the stream reaches that point.
+ *
+ * Errors: every argument check happens on the host before any launch and returns
+ * a status (nothing is enqueued then); gdn_last_error() gives a message for the
+ * last failure on the calling thread.  GDN_ERR_CUDA reports a failed launch.
+ *
+ * Requirements: B, H >= 0, T >= 0; K, V in {16, 32, 64, 128}; chunk in
+ * {16, 32, 64}; every pointer 16-byte aligned; outputs must not overlap inputs
+ * or each other.  T need not be a multiple of chunk (the tail chunk is padded
+ * inside the kernels with alpha = 1, beta = 0, which leaves the state unchanged).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size   */
+    GDN_ERR_UNSUPPORTED = 2, /* K, V, chunk or dtype outside the supported set  */
+    GDN_ERR_WORKSPACE = 3,   /* workspace smaller than the *_workspace_bytes()  */
+    GDN_ERR_CUDA = 4         /* a kernel launch failed (cudaGetLastError)        */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Problem description.  `dtype` holds a gdn_dtype value. */
+typedef struct {
+    int64_t B, T, H, K, V;
+    int32_t chunk;
+    int32_t dtype;
+} gdn_problem;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int gdn_version(void);
+
+/* Message for a status code (static storage). */
+const char* gdn_status_string(gdn_status s);
+
+/* Message describing the last failed call on the calling thread ("" if none). */
+const char* gdn_last_error(void);
+
+/* Bytes of device workspace gdn_fwd needs (the per-chunk Phase-1/solve results
+ * handed to the scan).  Returns 0 for an invalid problem. */
+size_t gdn_fwd_workspace_bytes(const gdn_problem* p);
+
+/* Bytes of the `saved` buffer: the float32 state at the start of every chunk,
+ * [B, H, NC, V, K] with NC = ceil(T / chunk) ("OpenGDN", "Core operator
+ * reference": the reverse retains FP32 chunk boundaries). */
+size_t gdn_saved_bytes(const gdn_problem* p);
+
+/* Bytes of device workspace gdn_bwd needs. */
+size_t gdn_bwd_workspace_bytes(const gdn_problem* p);
+
+/*
+ * Forward.
+ *   q, k, v, alpha, beta : inputs (device, dtype), layouts above.
+ *   initial_state        : float32 [B,H,V,K] or NULL (= zeros).
+ *   o                    : output [B,T,H,V] (device, dtype).
+ *   final_state          : float32 [B,H,V,K] or NULL (= not written).  Passing it as
+ *                          the next call's initial_state continues the stream exactly.
+ *   saved                : NULL, or gdn_saved_bytes(p) bytes that receive the chunk
+ *                          boundary states for gdn_bwd.
+ *   workspace            : gdn_fwd_workspace_bytes(p) bytes (contents are scratch).
+ * May be called with initial_state == final_state (in-place stream update).
+ */
+gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* alpha, const void* beta, const float* initial_state,
+                   void* o, float* final_state, void* saved, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: gradients of L = sum(d_o * o) + sum(d_final_state * final_state)
+ * with respect to q, k, v, alpha, beta and initial_state.
+ *   saved          : the buffer a gdn_fwd call with the same inputs filled, or NULL
+ *                    (the boundary states are then recomputed into the workspace).
+ *   d_o            : [B,T,H,V] dtype.
+ *   d_final_state  : float32 [B,H,V,K] or NULL (= zeros).
+ *   dq, dk, dv, dalpha, dbeta : outputs in dtype, shapes of their inputs.
+ *   d_initial_state: float32 [B,H,V,K] or NULL (= not written).
+ *   workspace      : gdn_bwd_workspace_bytes(p) bytes.
+ */
+gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                   const void* alpha, const void* beta, const float* initial_state,
+                   const void* saved, const void* d_o, const float* d_final_state,
+                   void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
+                   float* d_initial_state, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

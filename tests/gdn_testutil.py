@@ -1,0 +1,106 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path (through the C ABI
+binding) and the float64 oracle on the same seeded inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from gated_delta_rule_19_gb300 import gdn
+from gated_delta_rule_19_gb300.inputs import Workload, custom, make_inputs
+
+# Tolerances on relative L2 error, per output tensor: fp32 inputs 1e-5; bf16
+# inputs with fp32 state and accumulation: 2e-2 for outputs / final state, 3e-2
+# for gradients.
+TOL = {"f32": dict(out=1e-5, grad=1e-5), "bf16": dict(out=2e-2, grad=3e-2)}
+
+
+def rel_l2(x, ref) -> float:
+    x = np.asarray(x, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    den = np.linalg.norm(ref)
+    num = np.linalg.norm(x - ref)
+    if den == 0.0:
+        return float(num)
+    return float(num / den)
+
+
+def to_np(t):
+    return None if t is None else t.detach().float().cpu().double().numpy()
+
+
+def gpu_run(w: Workload, inp: dict, backward: bool, saved_mode: str = "saved",
+            device="cuda"):
+    """Runs the CUDA path.  Returns a dict of numpy float64 arrays."""
+    d = {n: (t.to(device) if t is not None else None) for n, t in inp.items()}
+    o, sT, saved = gdn.gdn_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"],
+                               d["initial_state"], chunk=w.chunk,
+                               saved=(backward and saved_mode == "saved"))
+    out = dict(o=to_np(o), final_state=to_np(sT))
+    if backward:
+        g = gdn.gdn_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"],
+                        d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk)
+        for n, t in zip(("dq", "dk", "dv", "dalpha", "dbeta", "d_initial_state"), g):
+            out[n] = to_np(t)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_run(oracle, inp: dict, backward: bool, streams=None):
+    """Runs the oracle on the (optionally sampled) streams.  `streams` is a list
+    of (b, h) pairs; the returned arrays then have B'=1, H'=len(streams) layout
+    [1, T, n, ...]."""
+    q, k, v, a, be = (to_np(inp[n]) for n in ("q", "k", "v", "alpha", "beta"))
+    s0 = to_np(inp["initial_state"])
+    do = to_np(inp["d_o"])
+    dsT = to_np(inp["d_final_state"])
+    if streams is not None:
+        q, k, v, a, be, do = (select_streams(x, streams) for x in (q, k, v, a, be, do))
+        s0 = select_states(s0, streams) if s0 is not None else None
+        dsT = select_states(dsT, streams) if dsT is not None else None
+    o, sT = oracle.gated_delta_fwd(q, k, v, a, be, s0)
+    out = dict(o=o, final_state=sT)
+    if backward:
+        out.update(oracle.gated_delta_bwd(q, k, v, a, be, s0, do, dsT))
+    return out
+
+
+def select_streams(x, streams):
+    """[B,T,H,...] -> [1,T,n,...] for the listed (b,h) streams."""
+    return np.stack([x[b, :, h] for b, h in streams], axis=1)[None]
+
+
+def select_states(x, streams):
+    """[B,H,...] -> [1,n,...]."""
+    return np.stack([x[b, h] for b, h in streams], axis=0)[None]
+
+
+def sample_gpu(out: dict, streams):
+    res = {}
+    for n, x in out.items():
+        if x is None:
+            continue
+        if n in ("final_state", "d_initial_state"):
+            res[n] = select_states(x, streams)
+        else:
+            res[n] = select_streams(x, streams)
+    return res
+
+
+def compare(got: dict, ref: dict, dtype: str, names=None):
+    """Returns {name: rel_l2} and raises AssertionError listing failures."""
+    tol = TOL[dtype]
+    errs, bad = {}, []
+    for n in (names or ref.keys()):
+        if n not in got or got[n] is None:
+            continue
+        e = rel_l2(got[n], ref[n])
+        errs[n] = e
+        lim = tol["out"] if n in ("o", "final_state") else tol["grad"]
+        if not (e <= lim):
+            bad.append(f"{n}: rel_l2={e:.3e} > {lim:.0e}")
+    assert not bad, "; ".join(bad) + f" (all: {errs})"
+    return errs
+
+
+__all__ = ["TOL", "rel_l2", "gpu_run", "oracle_run", "compare", "custom", "make_inputs",
+           "sample_gpu", "select_streams", "select_states", "to_np"]

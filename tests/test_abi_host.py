@@ -1,0 +1,134 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/gdn.h declares, sizes its buffers, and rejects
+bad arguments with the right status before touching the device.  No call here
+reaches a kernel launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_19_gb300 import _build, gdn
+
+    _build.build()
+    return gdn
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("gdn_fwd", "gdn_bwd", "gdn_fwd_workspace_bytes", "gdn_saved_bytes",
+              "gdn_bwd_workspace_bytes", "gdn_status_string", "gdn_last_error", "gdn_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    missing = [n for n in _declared_functions() if n not in exported]
+    assert not missing, missing
+    handle = lib.load_library()
+    for n in _declared_functions():
+        assert hasattr(handle, n)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "gdn.h"\nint main(void){gdn_problem p={1,2,3,16,16,16,GDN_F32};'
+                   'return (int)p.B - 1;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gdn_version() >= 100
+    assert lib.gdn_status_string(0) == "ok"
+    assert "workspace" in lib.gdn_status_string(3)
+
+
+def test_sizes(lib):
+    p = lib.make_problem(8, 4096, 6, 128, 128, 64, 1)
+    NC = 64
+    assert lib.gdn_saved_bytes(p) == 8 * 6 * NC * 128 * 128 * 4
+    assert lib.gdn_fwd_workspace_bytes(p) > 0
+    assert lib.gdn_bwd_workspace_bytes(p) > lib.gdn_fwd_workspace_bytes(p)
+    # ragged T rounds up to whole chunks
+    p2 = lib.make_problem(1, 65, 1, 16, 16, 64, 0)
+    assert lib.gdn_saved_bytes(p2) == 2 * 16 * 16 * 4
+    # invalid problems size to 0
+    assert lib.gdn_fwd_workspace_bytes(lib.make_problem(1, 8, 1, 24, 16, 16, 0)) == 0
+    assert lib.gdn_saved_bytes(lib.make_problem(1, 8, 1, 16, 16, 48, 0)) == 0
+
+
+FAKE = 1 << 40  # a 16-byte aligned address that is never dereferenced
+
+
+def _fwd(lib, p, **over):
+    h = lib.load_library()
+    args = dict(q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), alpha=FAKE + (3 << 30),
+                beta=FAKE + (4 << 30), s0=None, o=FAKE + (5 << 30), sT=None, saved=None,
+                ws=FAKE + (6 << 30), ws_bytes=1 << 40)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return h.gdn_fwd(ctypes.byref(p), vp(args["q"]), vp(args["k"]), vp(args["v"]),
+                     vp(args["alpha"]), vp(args["beta"]), vp(args["s0"]), vp(args["o"]),
+                     vp(args["sT"]), vp(args["saved"]), vp(args["ws"]), args["ws_bytes"],
+                     vp(None))
+
+
+def _bwd(lib, p, **over):
+    h = lib.load_library()
+    base = dict(q=0, k=1, v=2, alpha=3, beta=4, s0=None, saved=None, do=5, dsT=None, dq=6,
+                dk=7, dv=8, da=9, db=10, ds0=None, ws=11)
+    args = {n: (None if x is None else FAKE + (x << 30)) for n, x in base.items()}
+    args["ws_bytes"] = 1 << 40
+    args.update(over)
+    vp = ctypes.c_void_p
+    order = ("q", "k", "v", "alpha", "beta", "s0", "saved", "do", "dsT", "dq", "dk", "dv",
+             "da", "db", "ds0", "ws")
+    return h.gdn_bwd(ctypes.byref(p), *[vp(args[n]) for n in order], args["ws_bytes"], vp(None))
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    ok = lib.make_problem(2, 100, 3, 64, 32, 32, 1)
+    INVALID, UNSUP, WS = 1, 2, 3
+    assert _fwd(lib, lib.make_problem(1, 8, 1, 24, 16, 16, 1)) == UNSUP
+    assert "K=24" in lib.gdn_last_error()
+    assert _fwd(lib, lib.make_problem(1, 8, 1, 16, 16, 8, 1)) == UNSUP
+    assert _fwd(lib, lib.make_problem(1, 8, 1, 16, 16, 16, 7)) == UNSUP
+    assert _fwd(lib, lib.make_problem(-1, 8, 1, 16, 16, 16, 1)) == INVALID
+    assert _fwd(lib, ok, q=None) == INVALID
+    assert "q is NULL" in lib.gdn_last_error()
+    assert _fwd(lib, ok, beta=FAKE + (4 << 30) + 8) == INVALID
+    assert "aligned" in lib.gdn_last_error()
+    assert _fwd(lib, ok, ws_bytes=16) == WS
+    assert _fwd(lib, ok, o=FAKE + 64) == INVALID  # o overlaps q
+    assert "overlaps" in lib.gdn_last_error()
+    assert _fwd(lib, ok, sT=FAKE + (5 << 30) + 4096) == INVALID  # final_state inside o
+    # bwd
+    assert _bwd(lib, ok, do=None) == INVALID
+    assert _bwd(lib, ok, dq=None) == INVALID
+    assert _bwd(lib, ok, ws_bytes=0) == WS
+    assert _bwd(lib, ok, dk=FAKE + (6 << 30) + 256) == INVALID  # dk overlaps dq
+    assert _bwd(lib, ok, dv=FAKE) == INVALID  # dv overlaps q
+    assert _bwd(lib, lib.make_problem(1, 8, 1, 16, 256, 16, 1)) == UNSUP
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    q = torch.zeros(1, 4, 1, 16)
+    with pytest.raises(lib.GdnError):
+        lib.gdn_fwd(q, q, q, torch.ones(1, 4, 1), torch.zeros(1, 4, 1), chunk=16)
