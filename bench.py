@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunkwise gated delta rule on one GB300 (or N replicas).
+
+A step is one pass of the whole path over one batch: gdn_fwd (keeping the chunk
+boundary states) followed by gdn_bwd, on the training shape B=8, T=4096, H=6,
+K=V=128, chunk 64, bf16 inputs with float32 state.  The headline value is
+fwd+bwd token*heads per second with every input resident in HBM; the forward
+alone is reported beside it.  Inputs (about 200 MB) and workspace exceed the
+129 MB L2, so no L2 flush is needed between steps.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs its own batch on its own GPU (the (b,h)
+streams are independent; no collective on the data path) and rank 0 prints the
+whole-job throughput, timed as the max over ranks.
+
+The float64 CPU oracle is timed on a bounded sample of the same workload
+(cpu_baseline) and also gates the run: the GPU results on the sampled streams
+must match it within the tolerances before anything is timed.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from gated_delta_rule_19_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "gated-delta fwd & fwd+bwd tokens*heads/s at 1 GB300; % of bf16 TC roofline"
+UNIT = "tokens*heads/s"
+DEFAULT_WORKLOAD = "train_bf16_B8_T4096_H6_K128_V128"
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+# ----------------------------------------------------------------- arguments
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if (args.impl == "gdn" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def sample_streams(w, n):
+    """n (b, h) streams spread over the batch and the heads."""
+    all_s = [(b, h) for b in range(w.B) for h in range(w.H)]
+    if n >= len(all_s):
+        return all_s
+    idx = np.linspace(0, len(all_s) - 1, n).round().astype(int)
+    return [all_s[i] for i in idx]
+
+
+def oracle_step(oracle, np_in, streams, threads):
+    from_s = lambda x: np.stack([x[b, :, h] for b, h in streams], axis=1)[None]  # noqa: E731
+    st = lambda x: None if x is None else np.stack([x[b, h] for b, h in streams])[None]  # noqa
+    q, k, v, a, be, do = (from_s(np_in[n]) for n in ("q", "k", "v", "alpha", "beta", "d_o"))
+    s0, dsT = st(np_in["initial_state"]), st(np_in["d_final_state"])
+    t0 = time.perf_counter()
+    o, sT = oracle.gated_delta_fwd(q, k, v, a, be, s0, threads=threads)
+    g = oracle.gated_delta_bwd(q, k, v, a, be, s0, do, dsT, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, dict(o=o, final_state=sT, **g)
+
+
+def np_inputs(inp):
+    return {n: (t.double().numpy() if t is not None else None) for n, t in inp.items()}
+
+
+def n_sample_streams(w, threads):
+    return max(1, min(w.B * w.H, threads))
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the float64 CPU oracle, timed as it stands on the
+    host cores, each step a bounded sample (as many full-length streams as
+    there are cores) of the workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    threads = oracle.threads(0)
+    streams = sample_streams(w, n_sample_streams(w, threads))
+    np_in = np_inputs(make_inputs(w))
+    for _ in range(args.warmup):
+        oracle_step(oracle, np_in, streams, threads)
+    total = 0.0
+    for _ in range(args.steps):
+        dt, _ = oracle_step(oracle, np_in, streams, threads)
+        total += dt
+    units = len(streams) * w.T
+    value = units * args.steps / total
+    sample = (f"{len(streams)} of {w.B * w.H} (b,h) streams, full T={w.T}, fwd+bwd, "
+              "float64 token recurrence")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
+                   "chunk": w.chunk, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxs, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxs.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxs) if maxs else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sms), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- roofline
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm_gbs=float(pk["hbm_gbs"]), bf16_tflops=float(pk["bf16_tflops"]),
+                    bf16_tflops_sustained=float(pk.get("bf16_tflops_sustained",
+                                                       pk["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_work(name, w):
+    """Algorithmic flops and bytes per token*head of each kernel: the per-unit
+    counts of the whole path (fwd flops 2C(3K+2V)+6KV, bwd flops
+    14KV+10CV+18CK+4C^2; bytes = the path's own inputs and outputs in the run
+    dtype) split by the step each kernel performs."""
+    C, K, V = w.chunk, w.K, w.V
+    es = 2 if w.dtype == "bf16" else 4
+    read_inputs = es * (2 * K + V) + 2 * es
+    table = {
+        "prep_kernel(fwd)": (6 * C * K + 2 * C * V, read_inputs),
+        "scan_fwd_kernel": (6 * K * V + 2 * C * V, es * V),
+        "prep_kernel(bwd)": (6 * C * K + 2 * C * V, read_inputs),
+        "scan_fwd_kernel(state-only)": (4 * K * V, 0),
+        "scan_bwd_kernel": (8 * K * V + 2 * C * V, es * V),
+        "grad_kernel": (6 * K * V + 6 * C * V + 12 * C * K + 4 * C * C, es * (2 * K + V) + 2 * es),
+    }
+    return table.get(name, (0, 0))
+
+
+def traffic_for(name):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if
+    that summary was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    ent = t.get("kernels", {}).get(name)
+    if not ent or ent.get("source_hash") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch_full_workload")
+
+
+def source_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_19_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def roofline(summary, w, peaks):
+    units = w.token_heads
+    rows = []
+    for name, (n, ms) in summary.items():
+        flops, byts = kernel_work(name, w)
+        avg_s = ms / n / 1e3
+        t_f = flops * units / (peaks["bf16_tflops_sustained"] * 1e12)
+        t_b = byts * units / (peaks["hbm_gbs"] * 1e9)
+        if t_f >= t_b:
+            ach = flops * units / avg_s / 1e12
+            row = dict(bound="tensor", achieved=ach, peak=peaks["bf16_tflops_sustained"],
+                       unit="TFLOP/s")
+        else:
+            ach = byts * units / avg_s / 1e9
+            row = dict(bound="hbm", achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s")
+        row.update(frac=row["achieved"] / row["peak"], kernel=name, launches=n,
+                   avg_ms=ms / n, share=0.0, traffic=traffic_for(name),
+                   peak_source=peaks["source"] + (" sustained bf16" if row["bound"] == "tensor"
+                                                  else " hbm copy"))
+        rows.append(row)
+    tot = sum(r["avg_ms"] * r["launches"] for r in rows) or 1.0
+    for r in rows:
+        r["share"] = r["avg_ms"] * r["launches"] / tot
+    rows.sort(key=lambda r: -r["share"])
+    return rows
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gdn(args, world, rank, local):
+    from gated_delta_rule_19_gb300 import _build, gdn
+
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    if w.calls != 1 or not w.backward:
+        raise SystemExit(f"{w.name} is not a single-call training workload")
+    inp_cpu = make_inputs(w.with_(seed=w.seed + 1000 * rank) if rank else w)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in inp_cpu.items()}
+    p = gdn.make_problem(w.B, w.T, w.H, w.K, w.V, w.chunk, d["q"].dtype)
+    ws_f = torch.empty(gdn.gdn_fwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(gdn.gdn_bwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    saved = torch.empty(gdn.gdn_saved_bytes(p), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(d["v"])
+    sT = torch.empty(w.B, w.H, w.V, w.K, dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+             torch.empty_like(d["alpha"]), torch.empty_like(d["beta"]))
+    ds0 = torch.empty_like(sT)
+    args_in = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"])
+
+    def step():
+        gdn.gdn_fwd(*args_in, chunk=w.chunk, o=o, final_state=sT, saved=saved, workspace=ws_f)
+        gdn.gdn_bwd(*args_in, d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk,
+                    grads=grads, d_initial_state=ds0, workspace=ws_b)
+
+    def fwd_only():
+        gdn.gdn_fwd(*args_in, chunk=w.chunk, o=o, final_state=sT, workspace=ws_f)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # correctness gate + cpu baseline (rank 0): the oracle on sampled streams
+    cpu = None
+    parity = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        threads = oracle.threads(0)
+        streams = sample_streams(w, n_sample_streams(w, threads))
+        dt, ref = oracle_step(oracle, np_inputs(inp_cpu), streams, threads)
+        got = dict(o=o, final_state=sT, dq=grads[0], dk=grads[1], dv=grads[2],
+                   dalpha=grads[3], dbeta=grads[4], d_initial_state=ds0)
+        parity = {}
+        for n, t in got.items():
+            x = t.detach().double().cpu().numpy()
+            if n in ("final_state", "d_initial_state"):
+                x = np.stack([x[b, h] for b, h in streams])[None]
+            else:
+                x = np.stack([x[b, :, h] for b, h in streams], axis=1)[None]
+            r = ref[n]
+            parity[n] = float(np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-300))
+        tol = {"o": 2e-2, "final_state": 2e-2}
+        bad = {n: e for n, e in parity.items() if not e <= tol.get(n, 3e-2)}
+        if bad:
+            print(json.dumps({"error": "parity gate failed", "parity": parity}), flush=True)
+            raise SystemExit(3)
+        cpu = {"value": len(streams) * w.T / dt, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"{len(streams)} of {w.B * w.H} (b,h) streams at full T={w.T}, "
+                         f"fwd+bwd float64, {dt:.2f} s"}
+
+    # ---- timed region: fwd+bwd steps, inputs resident in HBM
+    stream = torch.cuda.current_stream(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev)
+    time.sleep(0.3)
+    gdn.gdn_profiler_start(16 * args.steps + 16)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    gdn.gdn_profiler_stop()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    summary = gdn.gdn_profiler_summary()
+    launches = sum(n for n, _ in summary.values())
+    ms_max = max_over_ranks(ms, world, dev)
+    barrier(world)
+
+    # ---- forward only
+    torch.cuda.synchronize(dev)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        fwd_only()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world, dev)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        names_in = ("q", "k", "v", "alpha", "beta", "initial_state", "d_o", "d_final_state")
+        host_in = {n: inp_cpu[n].pin_memory() for n in names_in if inp_cpu[n] is not None}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        outs_dev = [o, sT] + list(grads) + [ds0]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            dd = {n: t.to(dev, non_blocking=True) for n, t in host_in.items()}
+            a_in = (dd["q"], dd["k"], dd["v"], dd["alpha"], dd["beta"], dd.get("initial_state"))
+            gdn.gdn_fwd(*a_in, chunk=w.chunk, o=o, final_state=sT, saved=saved, workspace=ws_f)
+            gdn.gdn_bwd(*a_in, dd["d_o"], dd.get("d_final_state"), saved=saved,
+                        chunk=w.chunk, grads=grads, d_initial_state=ds0, workspace=ws_b)
+            for src, dst in zip(outs_dev, host_out):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, dev)
+        e2e = {"value": world * w.token_heads / (e2e_ms / 1e3), "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    rows = roofline(summary, w, peaks)
+    dom = rows[0]
+    rl = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    rl.update(kernel=dom["kernel"], avg_ms=dom["avg_ms"], share=dom["share"],
+              peak_source=dom["peak_source"])
+    value = world * w.token_heads / (ms_max / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
+                   "chunk": w.chunk, "state": "f32", "step": "gdn_fwd(saved) + gdn_bwd",
+                   "l2": "inputs and workspace larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "fwd": {"value": world * w.token_heads / (fwd_ms / 1e3), "unit": UNIT,
+                "ms_per_step": fwd_ms},
+        "roofline": rl,
+        "kernels": [{k: r[k] for k in ("kernel", "launches", "avg_ms", "share", "bound",
+                                       "achieved", "unit", "frac")} for r in rows],
+        "cpu_baseline": cpu,
+        "parity_sampled": parity,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gdn(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

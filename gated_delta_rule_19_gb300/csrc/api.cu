@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "gdn.h"
 #include "gdn_internal.h"
@@ -143,6 +144,31 @@ gdn_status cuda_fail(cudaError_t e, const char* what) {
     return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Optional launch timer: while on, each launch is bracketed by two CUDA events
+// recorded on the launch's own stream.
+struct Profiler {
+    bool on = false;
+    int n = 0;
+    std::vector<cudaEvent_t> ev;  // 2 per record
+    std::vector<int> kid;
+};
+Profiler g_prof;
+
+const char* const kKernelNames[gdn::KID_COUNT] = {
+    "prep_kernel(fwd)", "scan_fwd_kernel", "prep_kernel(bwd)",
+    "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel"};
+
+template <typename F>
+cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
+    if (!g_prof.on || g_prof.n >= (int)g_prof.kid.size()) return launch();
+    const int i = g_prof.n++;
+    g_prof.kid[i] = kid;
+    cudaEventRecord(g_prof.ev[2 * i], st);
+    cudaError_t e = launch();
+    cudaEventRecord(g_prof.ev[2 * i + 1], st);
+    return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -227,10 +253,14 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
     Carver cv{(char*)workspace};
     gdn::ChunkBufs cb;
     carve_chunk(d, cv, &cb, false);
-    cudaError_t e = gdn::launch_prep(d, ty, k, q, v, alpha, beta, cb, false, cs);
+    cudaError_t e = timed(gdn::KID_PREP_FWD, cs, [&] {
+        return gdn::launch_prep(d, ty, k, q, v, alpha, beta, cb, false, cs);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "chunk kernel");
-    e = gdn::launch_scan_fwd(d, ty, q, k, cb, initial_state, o, final_state, (float*)saved,
-                             true, cs);
+    e = timed(gdn::KID_SCAN_FWD, cs, [&] {
+        return gdn::launch_scan_fwd(d, ty, q, k, cb, initial_state, o, final_state,
+                                    (float*)saved, true, cs);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "scan kernel");
     return GDN_OK;
 }
@@ -293,20 +323,80 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
     gdn::BwdBufs bb;
     carve_bwd(d, cv, &cb, &bb, saved == nullptr);
     const float* states = saved ? (const float*)saved : bb.states;
-    cudaError_t e = gdn::launch_prep(d, ty, k, q, v, alpha, beta, cb, true, cs);
+    cudaError_t e = timed(gdn::KID_PREP_BWD, cs, [&] {
+        return gdn::launch_prep(d, ty, k, q, v, alpha, beta, cb, true, cs);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "chunk kernel");
     if (!saved) {
-        e = gdn::launch_scan_fwd(d, ty, q, k, cb, initial_state, nullptr, nullptr, bb.states,
-                                 false, cs);
+        e = timed(gdn::KID_STATE_RECOMPUTE, cs, [&] {
+            return gdn::launch_scan_fwd(d, ty, q, k, cb, initial_state, nullptr, nullptr,
+                                        bb.states, false, cs);
+        });
         if (e != cudaSuccess) return cuda_fail(e, "state recompute kernel");
     }
-    e = gdn::launch_scan_bwd(d, ty, q, k, d_o, cb, states, d_final_state, bb, d_initial_state,
-                             cs);
+    e = timed(gdn::KID_SCAN_BWD, cs, [&] {
+        return gdn::launch_scan_bwd(d, ty, q, k, d_o, cb, states, d_final_state, bb,
+                                    d_initial_state, cs);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "reverse scan kernel");
-    e = gdn::launch_grad(d, ty, q, k, v, alpha, beta, d_o, cb, states, bb, dq, dk, dv, dalpha,
-                         dbeta, cs);
+    e = timed(gdn::KID_GRAD, cs, [&] {
+        return gdn::launch_grad(d, ty, q, k, v, alpha, beta, d_o, cb, states, bb, dq, dk, dv,
+                                dalpha, dbeta, cs);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "chunk gradient kernel");
     return GDN_OK;
+}
+
+int gdn_num_kernels(void) { return gdn::KID_COUNT; }
+
+const char* gdn_kernel_name(int id) {
+    return (id >= 0 && id < gdn::KID_COUNT) ? kKernelNames[id] : "";
+}
+
+gdn_status gdn_profiler_start(int capacity) {
+    if (capacity < 0) return fail(GDN_ERR_INVALID_ARG, "negative profiler capacity");
+    if ((int)g_prof.kid.size() < capacity) {
+        const size_t have = g_prof.ev.size();
+        g_prof.ev.resize(2 * (size_t)capacity);
+        for (size_t i = have; i < g_prof.ev.size(); ++i) {
+            cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+            if (e != cudaSuccess) {
+                g_prof.ev.resize(i);
+                g_prof.kid.resize(i / 2);
+                return cuda_fail(e, "cudaEventCreate");
+            }
+        }
+        g_prof.kid.resize(capacity);
+    }
+    g_prof.n = 0;
+    g_prof.on = true;
+    return GDN_OK;
+}
+
+gdn_status gdn_profiler_stop(void) {
+    g_prof.on = false;
+    return GDN_OK;
+}
+
+gdn_status gdn_profiler_summary(int id, int* launches, double* total_ms) {
+    if (!launches || !total_ms) return fail(GDN_ERR_INVALID_ARG, "NULL output pointer");
+    *launches = 0;
+    *total_ms = 0.0;
+    for (int i = 0; i < g_prof.n; ++i) {
+        if (g_prof.kid[i] != id) continue;
+        cudaError_t e = cudaEventSynchronize(g_prof.ev[2 * i + 1]);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "profiler event");
+        *launches += 1;
+        *total_ms += ms;
+    }
+    return GDN_OK;
+}
+
+void gdn_profiler_release(void) {
+    for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+    g_prof = Profiler();
 }
 
 }  // extern "C"

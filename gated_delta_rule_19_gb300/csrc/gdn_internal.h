@@ -48,6 +48,18 @@ struct BwdBufs {
 
 enum class InType { F32 = 0, BF16 = 1 };
 
+// Kernel identities for the optional launch timer (gdn_profiler_*).  The names
+// are the CUDA kernel names, so they match the entries of an ncu launch list.
+enum KernelId {
+    KID_PREP_FWD = 0,    // prep_kernel, forward
+    KID_SCAN_FWD,        // scan_fwd_kernel
+    KID_PREP_BWD,        // prep_kernel, backward (also writes T)
+    KID_STATE_RECOMPUTE, // scan_fwd_kernel in state-only mode (backward without saved)
+    KID_SCAN_BWD,        // scan_bwd_kernel
+    KID_GRAD,            // grad_kernel
+    KID_COUNT
+};
+
 // Launchers of the SIMT (CUDA-core, float32) kernels.  Each returns the
 // cudaError_t of its launch.
 cudaError_t launch_prep(const Dims& d, InType ty, const void* k, const void* q,

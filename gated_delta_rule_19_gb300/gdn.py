@@ -59,12 +59,24 @@ def load_library():
     lib.gdn_fwd.restype = ctypes.c_int
     lib.gdn_bwd.argtypes = [P] + [_vp] * 16 + [ctypes.c_size_t, _vp]
     lib.gdn_bwd.restype = ctypes.c_int
+    lib.gdn_num_kernels.restype = ctypes.c_int
+    lib.gdn_kernel_name.argtypes = [ctypes.c_int]
+    lib.gdn_kernel_name.restype = ctypes.c_char_p
+    lib.gdn_profiler_start.argtypes = [ctypes.c_int]
+    lib.gdn_profiler_start.restype = ctypes.c_int
+    lib.gdn_profiler_stop.restype = ctypes.c_int
+    lib.gdn_profiler_summary.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_double)]
+    lib.gdn_profiler_summary.restype = ctypes.c_int
+    lib.gdn_profiler_release.restype = None
     _lib = lib
     return lib
 
 
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_workspace_bytes",
-            "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd")
+            "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd",
+            "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
+            "gdn_profiler_summary", "gdn_profiler_release")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -225,3 +237,36 @@ def gdn_bwd(q, k, v, alpha, beta, initial_state, d_o, d_final_state=None, *, sav
                      _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
     _check(st)
     return dq, dk, dv, da, db, d_initial_state
+
+
+def gdn_num_kernels() -> int:
+    return int(load_library().gdn_num_kernels())
+
+
+def gdn_kernel_name(i: int) -> str:
+    return load_library().gdn_kernel_name(int(i)).decode()
+
+
+def gdn_profiler_start(capacity: int) -> None:
+    _check(load_library().gdn_profiler_start(int(capacity)))
+
+
+def gdn_profiler_stop() -> None:
+    _check(load_library().gdn_profiler_stop())
+
+
+def gdn_profiler_summary() -> dict:
+    """{kernel name: (launches, total ms)} for the launches timed since start."""
+    lib = load_library()
+    out = {}
+    for i in range(gdn_num_kernels()):
+        n = ctypes.c_int(0)
+        ms = ctypes.c_double(0.0)
+        _check(lib.gdn_profiler_summary(i, ctypes.byref(n), ctypes.byref(ms)))
+        if n.value:
+            out[gdn_kernel_name(i)] = (n.value, ms.value)
+    return out
+
+
+def gdn_profiler_release() -> None:
+    load_library().gdn_profiler_release()

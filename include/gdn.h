@@ -121,6 +121,23 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
                    float* d_initial_state, void* workspace, size_t workspace_bytes,
                    void* stream);
 
+/*
+ * Optional launch timer, for benchmarks.  While started, every kernel launch of
+ * gdn_fwd/gdn_bwd is bracketed by two CUDA events recorded on the call's stream
+ * (up to `capacity` launches; later launches are not timed).  The events are
+ * host-side driver objects created once by gdn_profiler_start; no device memory
+ * is allocated.  Kernel ids run from 0 to gdn_num_kernels()-1; gdn_kernel_name
+ * gives the CUDA kernel's name (as an ncu launch list shows it).
+ * gdn_profiler_summary waits for the recorded events of kernel `id` and returns
+ * their count and summed duration in milliseconds.  Not thread-safe.
+ */
+int gdn_num_kernels(void);
+const char* gdn_kernel_name(int id);
+gdn_status gdn_profiler_start(int capacity);
+gdn_status gdn_profiler_stop(void);
+gdn_status gdn_profiler_summary(int id, int* launches, double* total_ms);
+void gdn_profiler_release(void);
+
 #ifdef __cplusplus
 }
 #endif
