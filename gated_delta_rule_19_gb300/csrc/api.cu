@@ -171,6 +171,12 @@ cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
 
 }  // namespace
 
+namespace gdn {
+// Lets other translation units of the library report a message through
+// gdn_last_error().
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_version(void) { return 100; }

@@ -60,6 +60,9 @@ enum KernelId {
     KID_COUNT
 };
 
+// Sets the message gdn_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 // Launchers of the SIMT (CUDA-core, float32) kernels.  Each returns the
 // cudaError_t of its launch.
 cudaError_t launch_prep(const Dims& d, InType ty, const void* k, const void* q,

@@ -59,6 +59,8 @@ def load_library():
     lib.gdn_fwd.restype = ctypes.c_int
     lib.gdn_bwd.argtypes = [P] + [_vp] * 16 + [ctypes.c_size_t, _vp]
     lib.gdn_bwd.restype = ctypes.c_int
+    lib.gdn_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
+    lib.gdn_fwd_noalloc.restype = ctypes.c_int
     lib.gdn_num_kernels.restype = ctypes.c_int
     lib.gdn_kernel_name.argtypes = [ctypes.c_int]
     lib.gdn_kernel_name.restype = ctypes.c_char_p
@@ -76,7 +78,7 @@ def load_library():
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_workspace_bytes",
             "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd",
             "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
-            "gdn_profiler_summary", "gdn_profiler_release")
+            "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -270,3 +272,37 @@ def gdn_profiler_summary() -> dict:
 
 def gdn_profiler_release() -> None:
     load_library().gdn_profiler_release()
+
+
+def gdn_fwd_noalloc(q, k, v, alpha, beta, initial_state, o, final_state=None, *,
+                    chunk: int = 64, stream=None):
+    """Forward through ``gdn_fwd_noalloc``: the same result as :func:`gdn_fwd`,
+    for callers that cannot allocate device memory (a host framework that owns
+    every byte of device memory, or a latency-critical path where cudaMalloc's
+    device-wide synchronisation is not acceptable).  Its scratch is a fixed
+    array in the library (``GDN_FWD_NOALLOC_SCRATCH_BYTES`` = 32 MiB per device);
+    larger problems raise.  This wrapper allocates nothing either: the caller
+    passes ``o`` and, optionally, ``final_state``.  Calls that overlap on the GPU
+    share the array and race; the first call on a device must not be inside a
+    stream capture.  Returns ``(o, final_state)``."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dt = q.dtype
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    for t, n, s in ((k, "k", (B, T, H, K)), (v, "v", (B, T, H, V)), (q, "q", (B, T, H, K)),
+                    (alpha, "alpha", (B, T, H)), (beta, "beta", (B, T, H)),
+                    (o, "o", (B, T, H, V))):
+        if t is None:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"{n} is required")
+        _need(t, n, s, dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    _need(final_state, "final_state", (B, H, V, K), torch.float32, dev)
+    st = lib.gdn_fwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                             _ptr(beta), _ptr(initial_state), _ptr(o), _ptr(final_state),
+                             _stream_handle(dev, stream))
+    _check(st)
+    return o, final_state

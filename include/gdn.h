@@ -122,6 +122,36 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
                    void* stream);
 
 /*
+ * Forward for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it is a convenience of this library.
+ *
+ * gdn_fwd needs a caller-owned workspace.  Some callers cannot provide one: code
+ * running inside a host framework that owns all device memory (a plugin, or an
+ * inference runtime whose memory pool is fixed and fully committed, where a
+ * cudaMalloc fails or is not allowed), and code on a latency-critical path where
+ * cudaMalloc/cudaFree would synchronise the device and stall concurrent work.
+ * gdn_fwd_noalloc computes exactly what gdn_fwd computes (same kernels, no
+ * `saved` output) with its scratch in a fixed array inside the library's device
+ * memory: GDN_FWD_NOALLOC_SCRATCH_BYTES on every device that loads the library,
+ * held until the process exits.  It calls no allocating routine.
+ *   - Problems whose gdn_fwd_workspace_bytes(p) exceeds that size are rejected
+ *     with GDN_ERR_UNSUPPORTED before anything is enqueued (e.g. K=V=128,
+ *     chunk 64 needs 80.25 KiB per (b, h, chunk), so B*H*ceil(T/64) <= 408).
+ *   - The first call on a device looks up the array's address there
+ *     (cudaGetSymbolAddress, with the stream's device current): make that
+ *     first call outside any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; calls that overlap on the GPU (e.g. on two streams) race and
+ *     corrupt each other's results, so order them on one stream.  Each call
+ *     writes every scratch element before reading it, so nothing is cleared.
+ * Arguments are those of gdn_fwd without saved/workspace; `o` is required.
+ */
+#define GDN_FWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const void* alpha, const void* beta, const float* initial_state,
+                           void* o, float* final_state, void* stream);
+
+/*
  * Optional launch timer, for benchmarks.  While started, every kernel launch of
  * gdn_fwd/gdn_bwd is bracketed by two CUDA events recorded on the call's stream
  * (up to `capacity` launches; later launches are not timed).  The events are
