@@ -234,6 +234,8 @@ def kernel_work(name, w):
     read_inputs = es * (2 * K + V) + 2 * es
     table = {
         "prep_kernel(fwd)": (6 * C * K + 2 * C * V, read_inputs),
+        "prep_fwd_tc": (6 * C * K + 2 * C * V, read_inputs),
+        "scan_fwd_tc": (6 * K * V + 2 * C * V, es * V),
         "scan_fwd_kernel": (6 * K * V + 2 * C * V, es * V),
         "prep_kernel(bwd)": (6 * C * K + 2 * C * V, read_inputs),
         "scan_fwd_kernel(state-only)": (4 * K * V, 0),

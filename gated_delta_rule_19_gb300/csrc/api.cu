@@ -83,6 +83,16 @@ size_t carve_chunk(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, bool with
     return cv.off;
 }
 
+size_t carve_tc(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb) {
+    const size_t rows = (size_t)d.NS() * d.NC * d.C;
+    tb->err = cv.take<int>(64);
+    tb->G = cv.take<float>(rows);
+    tb->W = cv.take<__nv_bfloat16>(rows * d.K);
+    tb->Ut = cv.take<__nv_bfloat16>(rows * d.V);
+    tb->Mqk = cv.take<__nv_bfloat16>(rows * d.C);
+    return cv.off;
+}
+
 size_t carve_bwd(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, gdn::BwdBufs* bb,
                  bool need_states) {
     carve_chunk(d, cv, cb, true);
@@ -156,7 +166,8 @@ Profiler g_prof;
 
 const char* const kKernelNames[gdn::KID_COUNT] = {
     "prep_kernel(fwd)", "scan_fwd_kernel", "prep_kernel(bwd)",
-    "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel"};
+    "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel",
+    "prep_fwd_tc", "scan_fwd_tc"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -198,6 +209,11 @@ size_t gdn_fwd_workspace_bytes(const gdn_problem* p) {
     gdn::Dims d{};
     if (check_problem(p, &d) != GDN_OK) return 0;
     Carver cv{nullptr};
+    if (d.NS() * d.NC == 0) return 0;
+    if (gdn::tc_fwd_supported(d, p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32)) {
+        gdn::TcBufs tb;
+        return carve_tc(d, cv, &tb);
+    }
     gdn::ChunkBufs cb;
     return carve_chunk(d, cv, &cb, false);
 }
@@ -257,6 +273,22 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
     }
     const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
     Carver cv{(char*)workspace};
+    if (gdn::tc_fwd_supported(d, ty)) {
+        gdn::TcBufs tb;
+        carve_tc(d, cv, &tb);
+        cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
+        if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
+        e = timed(gdn::KID_PREP_TC, cs, [&] {
+            return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
+        e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
+            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state,
+                                           (float*)saved, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
+        return GDN_OK;
+    }
     gdn::ChunkBufs cb;
     carve_chunk(d, cv, &cb, false);
     cudaError_t e = timed(gdn::KID_PREP_FWD, cs, [&] {

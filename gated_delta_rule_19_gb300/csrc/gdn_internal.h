@@ -2,6 +2,7 @@
 // translation units of libgdn.so (not part of the public ABI).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -48,6 +49,18 @@ struct BwdBufs {
 
 enum class InType { F32 = 0, BF16 = 1 };
 
+// Chunk results of the tensor-core forward (bf16 inputs, K = V = 128, chunk 64),
+// rows indexed chunk * 64 + r with chunk = stream * NC + c:
+//   W [rows, K], Ut [rows, V], Mqk [rows, 64] (bf16); G [rows] (fp32).
+// err: an int the kernels set (bitwise) when a bounded wait gives up.
+struct TcBufs {
+    __nv_bfloat16* W;
+    __nv_bfloat16* Ut;
+    __nv_bfloat16* Mqk;
+    float* G;
+    int* err;
+};
+
 // Kernel identities for the optional launch timer (gdn_profiler_*).  The names
 // are the CUDA kernel names, so they match the entries of an ncu launch list.
 enum KernelId {
@@ -57,6 +70,8 @@ enum KernelId {
     KID_STATE_RECOMPUTE, // scan_fwd_kernel in state-only mode (backward without saved)
     KID_SCAN_BWD,        // scan_bwd_kernel
     KID_GRAD,            // grad_kernel
+    KID_PREP_TC,         // prep_fwd_tc
+    KID_SCAN_FWD_TC,     // scan_fwd_tc
     KID_COUNT
 };
 
@@ -80,5 +95,15 @@ cudaError_t launch_grad(const Dims& d, InType ty, const void* q, const void* k,
                         const void* d_o, const ChunkBufs& cb, const float* states,
                         const BwdBufs& bb, void* dq, void* dk, void* dv, void* dalpha,
                         void* dbeta, cudaStream_t st);
+
+// Tensor-core forward (tc_fwd.cu).  tc_fwd_supported: shape/dtype test only.
+bool tc_fwd_supported(const Dims& d, InType ty);
+int tc_scan_vt(const Dims& d);
+cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v,
+                           const void* alpha, const void* beta, const TcBufs& tb,
+                           cudaStream_t st);
+cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb,
+                               const float* s0, void* o, float* sT, float* states,
+                               cudaStream_t st);
 
 }  // namespace gdn
