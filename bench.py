@@ -236,6 +236,11 @@ def kernel_work(name, w):
         "prep_kernel(fwd)": (6 * C * K + 2 * C * V, read_inputs),
         "prep_fwd_tc": (6 * C * K + 2 * C * V, read_inputs),
         "scan_fwd_tc": (6 * K * V + 2 * C * V, es * V),
+        "prep_fwd_tc(bwd)": (6 * C * K + 2 * C * V, read_inputs),
+        "scan_fwd_tc(state-only)": (4 * K * V, 0),
+        "scan_bwd_tc": (8 * K * V + 2 * C * V, es * V),
+        "grad_qk_tc": (6 * K * V + 2 * C * V + 4 * C * K, es * K),
+        "grad_wy_tc": (8 * C * K + 4 * C * V + 4 * C * C, es * (K + V) + 2 * es),
         "scan_fwd_kernel": (6 * K * V + 2 * C * V, es * V),
         "prep_kernel(bwd)": (6 * C * K + 2 * C * V, read_inputs),
         "scan_fwd_kernel(state-only)": (4 * K * V, 0),

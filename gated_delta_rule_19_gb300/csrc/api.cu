@@ -83,14 +83,33 @@ size_t carve_chunk(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, bool with
     return cv.off;
 }
 
-size_t carve_tc(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb) {
+size_t carve_tc(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with_T = false) {
     const size_t rows = (size_t)d.NS() * d.NC * d.C;
     tb->err = cv.take<int>(64);
     tb->G = cv.take<float>(rows);
     tb->W = cv.take<__nv_bfloat16>(rows * d.K);
     tb->Ut = cv.take<__nv_bfloat16>(rows * d.V);
     tb->Mqk = cv.take<__nv_bfloat16>(rows * d.C);
+    tb->T = with_T ? cv.take<__nv_bfloat16>(rows * d.C) : nullptr;
     return cv.off;
+}
+
+size_t carve_tc_bwd(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, gdn::TcBwdBufs* bb,
+                    bool need_states) {
+    carve_tc(d, cv, tb, true);
+    const size_t nchunks = (size_t)d.NS() * d.NC;
+    const size_t rows = nchunks * d.C;
+    bb->dU = cv.take<__nv_bfloat16>(rows * d.V);
+    bb->dS1 = cv.take<__nv_bfloat16>(nchunks * d.K * d.V);
+    bb->dKp = cv.take<float>(nchunks * d.K * d.C);
+    bb->dWt = cv.take<__nv_bfloat16>(nchunks * d.K * d.C);
+    bb->dGp = cv.take<float>(rows);
+    bb->states = need_states ? cv.take<__nv_bfloat16>(nchunks * d.K * d.V) : nullptr;
+    return cv.off;
+}
+
+gdn::InType in_type(const gdn_problem* p) {
+    return p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
 }
 
 size_t carve_bwd(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, gdn::BwdBufs* bb,
@@ -167,7 +186,8 @@ Profiler g_prof;
 const char* const kKernelNames[gdn::KID_COUNT] = {
     "prep_kernel(fwd)", "scan_fwd_kernel", "prep_kernel(bwd)",
     "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel",
-    "prep_fwd_tc", "scan_fwd_tc"};
+    "prep_fwd_tc", "scan_fwd_tc", "prep_fwd_tc(bwd)", "scan_fwd_tc(state-only)",
+    "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -221,13 +241,20 @@ size_t gdn_fwd_workspace_bytes(const gdn_problem* p) {
 size_t gdn_saved_bytes(const gdn_problem* p) {
     gdn::Dims d{};
     if (check_problem(p, &d) != GDN_OK) return 0;
-    return (size_t)d.NS() * d.NC * d.V * d.K * sizeof(float);
+    const size_t elem = gdn::tc_fwd_supported(d, in_type(p)) ? 2 : sizeof(float);
+    return (size_t)d.NS() * d.NC * d.V * d.K * elem;
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_problem* p) {
     gdn::Dims d{};
     if (check_problem(p, &d) != GDN_OK) return 0;
     Carver cv{nullptr};
+    if (d.NS() * d.NC == 0) return 0;
+    if (gdn::tc_fwd_supported(d, in_type(p))) {
+        gdn::TcBufs tb;
+        gdn::TcBwdBufs tbb;
+        return carve_tc_bwd(d, cv, &tb, &tbb, true);
+    }
     gdn::ChunkBufs cb;
     gdn::BwdBufs bb;
     return carve_bwd(d, cv, &cb, &bb, true);
@@ -284,7 +311,7 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
         e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
             return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state,
-                                           (float*)saved, cs);
+                                           (__nv_bfloat16*)saved, cs);
         });
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
         return GDN_OK;
@@ -357,6 +384,40 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
     }
     const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
     Carver cv{(char*)workspace};
+    if (gdn::tc_fwd_supported(d, ty)) {
+        gdn::TcBufs tb;
+        gdn::TcBwdBufs tbb;
+        carve_tc_bwd(d, cv, &tb, &tbb, saved == nullptr);
+        const __nv_bfloat16* states = saved ? (const __nv_bfloat16*)saved : tbb.states;
+        cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
+        if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
+        e = timed(gdn::KID_PREP_TC_BWD, cs, [&] {
+            return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
+        if (!saved) {
+            e = timed(gdn::KID_STATE_TC, cs, [&] {
+                return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, nullptr, nullptr,
+                                               tbb.states, cs);
+            });
+            if (e != cudaSuccess) return cuda_fail(e, "tensor-core state recompute");
+        }
+        e = timed(gdn::KID_SCAN_BWD_TC, cs, [&] {
+            return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, d_final_state, tbb,
+                                           d_initial_state, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core reverse scan");
+        e = timed(gdn::KID_GRAD_QK_TC, cs, [&] {
+            return gdn::launch_grad_qk_tc(d, q, k, d_o, tb, states, tbb, dq, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (q, k)");
+        e = timed(gdn::KID_GRAD_WY_TC, cs, [&] {
+            return gdn::launch_grad_wy_tc(d, k, v, alpha, beta, tb, tbb, dk, dv, dalpha, dbeta,
+                                          cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (WY)");
+        return GDN_OK;
+    }
     gdn::ChunkBufs cb;
     gdn::BwdBufs bb;
     carve_bwd(d, cv, &cb, &bb, saved == nullptr);

@@ -2,6 +2,7 @@
 // translation units of libgdn.so (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -53,12 +54,30 @@ enum class InType { F32 = 0, BF16 = 1 };
 // rows indexed chunk * 64 + r with chunk = stream * NC + c:
 //   W [rows, K], Ut [rows, V], Mqk [rows, 64] (bf16); G [rows] (fp32).
 // err: an int the kernels set (bitwise) when a bounded wait gives up.
+//   T [rows, 64] (bf16, (I + A)^-1; written only when non-null, for the backward).
 struct TcBufs {
     __nv_bfloat16* W;
     __nv_bfloat16* Ut;
     __nv_bfloat16* Mqk;
     float* G;
+    __nv_bfloat16* T;
     int* err;
+};
+
+// Backward buffers of the tensor-core path:
+//   dU   [rows, V] bf16            gradient of the corrected writes U
+//   dS1  [chunks * K, V] bf16      gradient of each chunk's end state, transposed
+//   dKp  [chunks * K, 64] fp32     dK^T from the Mqk and state-update terms
+//   dWt  [chunks * K, 64] bf16     dW^T
+//   dGp  [rows] fp32               dG from the output, Mqk and state-update terms
+//   states [chunks * K, V] bf16    chunk-start states when no saved buffer is given
+struct TcBwdBufs {
+    __nv_bfloat16* dU;
+    __nv_bfloat16* dS1;
+    float* dKp;
+    __nv_bfloat16* dWt;
+    float* dGp;
+    __nv_bfloat16* states;
 };
 
 // Kernel identities for the optional launch timer (gdn_profiler_*).  The names
@@ -72,6 +91,11 @@ enum KernelId {
     KID_GRAD,            // grad_kernel
     KID_PREP_TC,         // prep_fwd_tc
     KID_SCAN_FWD_TC,     // scan_fwd_tc
+    KID_PREP_TC_BWD,     // prep_fwd_tc, backward recompute (also writes T)
+    KID_STATE_TC,        // scan_fwd_tc in state-only mode
+    KID_SCAN_BWD_TC,     // scan_bwd_tc
+    KID_GRAD_QK_TC,      // grad_qk_tc
+    KID_GRAD_WY_TC,      // grad_wy_tc
     KID_COUNT
 };
 
@@ -96,6 +120,14 @@ cudaError_t launch_grad(const Dims& d, InType ty, const void* q, const void* k,
                         const BwdBufs& bb, void* dq, void* dk, void* dv, void* dalpha,
                         void* dbeta, cudaStream_t st);
 
+// Host helpers of the tensor-core path (tmap.cu).
+// [B, T, H, D] bf16 -> 4D TMA map (D, H, T, B), box 64 x 1 x 64 x 1, 128B swizzle.
+bool tmap_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D);
+// [rows, cols] bf16 row-major -> 2D TMA map, box 64 x 64, 128B swizzle.
+bool tmap_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols);
+bool tma_available();
+int sm_count();
+
 // Tensor-core forward (tc_fwd.cu).  tc_fwd_supported: shape/dtype test only.
 bool tc_fwd_supported(const Dims& d, InType ty);
 int tc_scan_vt(const Dims& d);
@@ -103,7 +135,17 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
                            const void* alpha, const void* beta, const TcBufs& tb,
                            cudaStream_t st);
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb,
-                               const float* s0, void* o, float* sT, float* states,
+                               const float* s0, void* o, float* sT, __nv_bfloat16* states,
                                cudaStream_t st);
+// Tensor-core backward (tc_bwd.cu).
+cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, const void* d_o,
+                               const TcBufs& tb, const float* dsT, const TcBwdBufs& bb,
+                               float* ds0, cudaStream_t st);
+cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const void* d_o,
+                              const TcBufs& tb, const __nv_bfloat16* states,
+                              const TcBwdBufs& bb, void* dq, cudaStream_t st);
+cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const void* alpha,
+                              const void* beta, const TcBufs& tb, const TcBwdBufs& bb,
+                              void* dk, void* dv, void* dalpha, void* dbeta, cudaStream_t st);
 
 }  // namespace gdn

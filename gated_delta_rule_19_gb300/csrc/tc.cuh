@@ -101,6 +101,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
         "r"(smem_u32(src)), "r"(c0), "r"(c1)
         : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -231,9 +239,57 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t co
     return row * 128u + ((((col >> 3) ^ (row & 7u)) & 7u) << 4) + ((col & 7u) << 1);
 }
 
+// bf16 matrix tiles in shared memory: a [R rows x C cols] matrix (R <= 128) is
+// stored as C/64 column blocks of [R rows x 64 cols], each 128B-swizzled, blocks
+// R*128 bytes apart, base 1024-byte aligned.  The same tile serves as a K-major
+// operand (rows = M or N, columns = K) and as an MN-major operand (rows = K,
+// columns = M or N).  s = index of the 16-element K step.
+__host__ __device__ __forceinline__ uint32_t tile_off(int R, int row, int col) {
+    return (uint32_t)(col >> 6) * (uint32_t)R * 128u + sw128_off(row, col & 63);
+}
+__device__ __forceinline__ uint64_t desc_kmaj(uint32_t base, int R, int s) {
+    return sdesc(base + (uint32_t)(s >> 2) * (uint32_t)R * 128u + (uint32_t)(s & 3) * 32u, 16, 1024,
+                 SW_128B);
+}
+__device__ __forceinline__ uint64_t desc_mnmaj(uint32_t base, int R, int s) {
+    return sdesc(base + (uint32_t)s * 2048u, (uint32_t)R * 128u, 1024, SW_128B);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Reads 16 fp32 TMEM columns of this thread's lane and waits for them.
+__device__ __forceinline__ void tmem_load16f(uint32_t taddr, float (&f)[16]) {
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld(r);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+}
+
+// Writes 16 values as bf16 into row `row`, columns col0..col0+15 of a tile.
+__device__ __forceinline__ void tile_put16(unsigned char* base, int R, int row, int col0,
+                                           const float (&f)[16]) {
+    uint4 a = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                         pack_bf16(f[6], f[7]));
+    uint4 b = make_uint4(pack_bf16(f[8], f[9]), pack_bf16(f[10], f[11]), pack_bf16(f[12], f[13]),
+                         pack_bf16(f[14], f[15]));
+    *(uint4*)(base + tile_off(R, row, col0)) = a;
+    *(uint4*)(base + tile_off(R, row, col0 + 8)) = b;
+}
+
+// Reads 8 bf16 (one 16-byte chunk) of a tile row as floats.
+__device__ __forceinline__ void tile_get8(const unsigned char* base, int R, int row, int col0,
+                                          float (&f)[8]) {
+    uint4 x = *(const uint4*)(base + tile_off(R, row, col0));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
 }
 
 }  // namespace tc

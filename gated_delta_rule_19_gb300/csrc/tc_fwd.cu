@@ -121,7 +121,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_W,
             const __grid_constant__ CUtensorMap tm_U, const __grid_constant__ CUtensorMap tm_M,
             const bf16* __restrict__ alpha, const bf16* __restrict__ beta, float* __restrict__ Gout,
-            int* err) {
+            bf16* __restrict__ Tout, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* Af = (float*)(sm + P_AF);
@@ -239,15 +239,18 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int r = tid >> 1, i0 = (tid & 1) * 32;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint32_t p1[4], p2[4];
+            uint32_t p0[4], p1[4], p2[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int i = i0 + q * 8 + 2 * e;
                 const float ta = (i <= r) ? Tf[r * 65 + i] : 0.f;
                 const float tb = (i + 1 <= r) ? Tf[r * 65 + i + 1] : 0.f;
+                p0[e] = pack_bf16(ta, tb);
                 p1[e] = pack_bf16(ta * bs[i] * gs[i], tb * bs[i + 1] * gs[i + 1]);
                 p2[e] = pack_bf16(ta * bs[i], tb * bs[i + 1]);
             }
+            if (Tout)
+                *(uint4*)(Tout + ((int64_t)row0 + r) * kC + i0 + q * 8) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
             *(uint4*)(sm + P_T1 + sw128_off(r, i0 + q * 8)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
             *(uint4*)(sm + P_T2 + sw128_off(r, i0 + q * 8)) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
         }
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(128, 1)
 scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const bf16* __restrict__ Ut, const float* __restrict__ G, const float* s0,
-            bf16* __restrict__ o, float* sT, float* __restrict__ states, int* err) {
+            bf16* __restrict__ o, float* sT, bf16* __restrict__ states, int* err) {
     using P = ScanPlan<Vt>;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -403,10 +406,12 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int64_t chunk = strm * NC + c;
         const int t0 = c * kC;
         // chunk-start state -> saved boundary states
-        if (states) {
-            float* St = states + (chunk * d.V + v0) * kD + k;
+        if (states) {  // bf16, [chunk][k][v]: this thread's row k, columns v0 .. v0+Vt
+            uint4* St = (uint4*)(states + (chunk * kD + k) * d.V + v0);
 #pragma unroll
-            for (int v = 0; v < Vt; ++v) St[(int64_t)v * kD] = s[v];
+            for (int g = 0; g < Vt / 8; ++g)
+                St[g] = make_uint4(pack_bf16(s[8 * g + 0], s[8 * g + 1]), pack_bf16(s[8 * g + 2], s[8 * g + 3]),
+                                   pack_bf16(s[8 * g + 4], s[8 * g + 5]), pack_bf16(s[8 * g + 6], s[8 * g + 7]));
         }
         if (tid == 0) {
             bool okt = mbar_wait(&tbar[stg], (c >> 1) & 1, err, 8);
@@ -498,7 +503,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             uint32_t ov[16];
             tmem_ld16(tO + lanebase + c0, ov);
             tmem_wait_ld(ov);
-            if (rowthr && t0 + r < d.T) {
+            if (o && rowthr && t0 + r < d.T) {
                 uint32_t po[8];
 #pragma unroll
                 for (int j = 0; j < 16; j += 2)
@@ -538,60 +543,10 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, P::TMEM_COLS);
 }
 
-// ----------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return (PFN_cuTensorMapEncodeTiled_v12000)p;
-    }();
-    return fn;
-}
-
-// [B, T, H, D] bf16 -> 4D map (D, H, T, B); box 64 x 1 x 64 x 1, 128B swizzle.
-bool tmap_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
-    cuuint32_t box[4] = {64, 1, 64, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, str, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// [rows, cols] bf16 row-major -> 2D map; box 64 x 64, 128B swizzle.
-bool tmap_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t str[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, str, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-    static int n = [] {
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        return v > 0 ? v : 148;
-    }();
-    return n;
-}
-
 template <int Vt>
 cudaError_t launch_scan_vt(const Dims& d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mW,
                            const CUtensorMap& mM, const TcBufs& tb, const float* s0, void* o, float* sT,
-                           float* states, cudaStream_t st) {
+                           bf16* states, cudaStream_t st) {
     using P = ScanPlan<Vt>;
     auto kern = scan_fwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
@@ -626,12 +581,12 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
     if (e != cudaSuccess) return e;
     dim3 grid(d.NC, d.H, d.B);
     prep_fwd_tc<<<grid, 128, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
-                                              tb.G, tb.err);
+                                              tb.G, tb.T, tb.err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
-                               void* o, float* sT, float* states, cudaStream_t st) {
+                               void* o, float* sT, __nv_bfloat16* states, cudaStream_t st) {
     CUtensorMap mq, mk, mW, mM;
     const int64_t rows = d.NS() * d.NC * kC;
     if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||

@@ -78,9 +78,12 @@ const char* gdn_last_error(void);
  * handed to the scan).  Returns 0 for an invalid problem. */
 size_t gdn_fwd_workspace_bytes(const gdn_problem* p);
 
-/* Bytes of the `saved` buffer: the float32 state at the start of every chunk,
- * [B, H, NC, V, K] with NC = ceil(T / chunk) ("OpenGDN", "Core operator
- * reference": the reverse retains FP32 chunk boundaries). */
+/* Bytes of the `saved` buffer: the state at the start of every chunk, NC =
+ * ceil(T / chunk) per stream ("OpenGDN", "Core operator reference": the reverse
+ * keeps chunk boundaries instead of a token history).  Its contents are private
+ * to gdn_fwd/gdn_bwd: float32 [B, H, NC, V, K] in general; bf16 [B, H, NC, K, V]
+ * on the tensor-core path (bf16 inputs, K = V = 128, chunk 64), where the states
+ * only feed bf16 tensor-core products. */
 size_t gdn_saved_bytes(const gdn_problem* p);
 
 /* Bytes of device workspace gdn_bwd needs. */

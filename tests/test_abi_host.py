@@ -61,7 +61,10 @@ def test_version_and_status_strings(lib):
 def test_sizes(lib):
     p = lib.make_problem(8, 4096, 6, 128, 128, 64, 1)
     NC = 64
-    assert lib.gdn_saved_bytes(p) == 8 * 6 * NC * 128 * 128 * 4
+    # bf16 K=V=128 chunk 64 runs on tensor cores and keeps bf16 boundary states
+    assert lib.gdn_saved_bytes(p) == 8 * 6 * NC * 128 * 128 * 2
+    # other shapes keep float32 boundary states
+    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 1)) == 8 * 6 * NC * 64 * 64 * 4
     assert lib.gdn_fwd_workspace_bytes(p) > 0
     assert lib.gdn_bwd_workspace_bytes(p) > lib.gdn_fwd_workspace_bytes(p)
     # ragged T rounds up to whole chunks
