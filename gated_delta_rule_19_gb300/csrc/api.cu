@@ -83,6 +83,25 @@ size_t carve_chunk(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, bool with
     return cv.off;
 }
 
+// Chunk results of the tensor-core path.  err is carved separately (it always
+// lives in the workspace, even when the chunk results live in `saved`).
+size_t carve_tc_chunk(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with_T) {
+    const size_t rows = (size_t)d.NS() * d.NC * d.C;
+    tb->G = cv.take<float>(rows);
+    tb->W = cv.take<__nv_bfloat16>(rows * d.K);
+    tb->Ut = cv.take<__nv_bfloat16>(rows * d.V);
+    tb->Mqk = cv.take<__nv_bfloat16>(rows * d.C);
+    tb->T = with_T ? cv.take<__nv_bfloat16>(rows * d.C) : nullptr;
+    return cv.off;
+}
+
+// `saved` of the tensor-core path: bf16 chunk-start states [chunks*K, V] followed
+// by the forward's chunk results (reused by the backward instead of recomputed).
+size_t carve_tc_saved(const gdn::Dims& d, Carver& cv, __nv_bfloat16** states, gdn::TcBufs* tb) {
+    *states = cv.take<__nv_bfloat16>((size_t)d.NS() * d.NC * d.K * d.V);
+    return carve_tc_chunk(d, cv, tb, true);
+}
+
 size_t carve_tc(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with_T = false) {
     const size_t rows = (size_t)d.NS() * d.NC * d.C;
     tb->err = cv.take<int>(64);
@@ -95,8 +114,13 @@ size_t carve_tc(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with_T = f
 }
 
 size_t carve_tc_bwd(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, gdn::TcBwdBufs* bb,
-                    bool need_states) {
-    carve_tc(d, cv, tb, true);
+                    bool need_recompute) {
+    if (need_recompute) {
+        carve_tc(d, cv, tb, true);
+    } else {
+        tb->err = cv.take<int>(64);
+    }
+    const bool need_states = need_recompute;
     const size_t nchunks = (size_t)d.NS() * d.NC;
     const size_t rows = nchunks * d.C;
     bb->dU = cv.take<__nv_bfloat16>(rows * d.V);
@@ -241,8 +265,13 @@ size_t gdn_fwd_workspace_bytes(const gdn_problem* p) {
 size_t gdn_saved_bytes(const gdn_problem* p) {
     gdn::Dims d{};
     if (check_problem(p, &d) != GDN_OK) return 0;
-    const size_t elem = gdn::tc_fwd_supported(d, in_type(p)) ? 2 : sizeof(float);
-    return (size_t)d.NS() * d.NC * d.V * d.K * elem;
+    if (gdn::tc_fwd_supported(d, in_type(p))) {
+        Carver cv{nullptr};
+        __nv_bfloat16* st;
+        gdn::TcBufs tb;
+        return carve_tc_saved(d, cv, &st, &tb);
+    }
+    return (size_t)d.NS() * d.NC * d.V * d.K * sizeof(float);
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_problem* p) {
@@ -302,7 +331,12 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
     Carver cv{(char*)workspace};
     if (gdn::tc_fwd_supported(d, ty)) {
         gdn::TcBufs tb;
+        __nv_bfloat16* states = nullptr;
         carve_tc(d, cv, &tb);
+        if (saved) {  // keep the chunk results for the backward
+            Carver sv{(char*)saved};
+            carve_tc_saved(d, sv, &states, &tb);
+        }
         cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
         if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
         e = timed(gdn::KID_PREP_TC, cs, [&] {
@@ -310,8 +344,8 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
         });
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
         e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
-            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state,
-                                           (__nv_bfloat16*)saved, cs);
+            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state, states,
+                                           cs);
         });
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
         return GDN_OK;
@@ -388,14 +422,22 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
         gdn::TcBufs tb;
         gdn::TcBwdBufs tbb;
         carve_tc_bwd(d, cv, &tb, &tbb, saved == nullptr);
-        const __nv_bfloat16* states = saved ? (const __nv_bfloat16*)saved : tbb.states;
+        const __nv_bfloat16* states = tbb.states;
+        if (saved) {  // reuse the forward's states and chunk results
+            Carver sv{(char*)const_cast<void*>(saved)};
+            __nv_bfloat16* st = nullptr;
+            int* err = tb.err;
+            carve_tc_saved(d, sv, &st, &tb);
+            tb.err = err;
+            states = st;
+        }
         cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
         if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
-        e = timed(gdn::KID_PREP_TC_BWD, cs, [&] {
-            return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
         if (!saved) {
+            e = timed(gdn::KID_PREP_TC_BWD, cs, [&] {
+                return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs);
+            });
+            if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
             e = timed(gdn::KID_STATE_TC, cs, [&] {
                 return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, nullptr, nullptr,
                                                tbb.states, cs);

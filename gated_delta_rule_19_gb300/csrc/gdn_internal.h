@@ -125,6 +125,12 @@ cudaError_t launch_grad(const Dims& d, InType ty, const void* q, const void* k,
 bool tmap_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D);
 // [rows, cols] bf16 row-major -> 2D TMA map, box 64 x 64, 128B swizzle.
 bool tmap_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols);
+// [rows, cols] bf16 as 3D (8, rows, cols/8); box (8, box_rows, box_groups), no swizzle:
+// lands as the MN-major no-swizzle operand layout [group][row][8].
+bool tmap_core8_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols, int box_rows,
+                     int box_groups);
+// [B, T, H, D] bf16 as 5D (8, T, D/8, H, B); box (8, 64, box_groups, 1, 1), no swizzle.
+bool tmap_core8_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D, int box_groups);
 bool tma_available();
 int sm_count();
 

@@ -109,6 +109,35 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "r"(c4)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_nb(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                               int c0, int c1, int c2) {
+    tma_load_3d(dst, map, bar, c0, c1, c2);
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -188,6 +217,26 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
+// 32 lanes x 32-bit, 32 consecutive columns (one instruction).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]),"+r"(r[16]),"+r"(r[17]),"+r"(r[18]),"+r"(r[19]),"+r"(r[20]),"+r"(r[21]),"+r"(r[22]),"+r"(r[23]),"+r"(r[24]),"+r"(r[25]),"+r"(r[26]),"+r"(r[27]),"+r"(r[28]),"+r"(r[29]),"+r"(r[30]),"+r"(r[31])
+                 :
+                 : "memory");
+}
+// Two 32-column loads in flight, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32], uint32_t (&b)[32]) {
+    tmem_ld32(ta, a);
+    tmem_ld32(tb, b);
+    tmem_wait_ld(a);
+    tmem_wait_ld(b);
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -232,6 +281,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
 }
 
+// A descriptor moved by `bytes` (the start-address field is the low 14 bits, in
+// 16-byte units; operands never cross a 256 KB boundary, so no carry is lost).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+    return desc + (uint64_t)(bytes >> 4);
+}
+
 // Byte offset of element (row, col) inside a [rows x 64] bf16 block stored with
 // the 128-byte swizzle (block base 1024-byte aligned): the 16-byte chunk index
 // is XORed with row % 8.
@@ -267,6 +322,37 @@ __device__ __forceinline__ void tmem_load16f(uint32_t taddr, float (&f)[16]) {
     tmem_wait_ld(r);
 #pragma unroll
     for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+}
+
+// Two / three 16-column loads in flight, one wait.
+__device__ __forceinline__ void tmem_load16f2(uint32_t ta, uint32_t tb, float (&fa)[16],
+                                              float (&fb)[16]) {
+    uint32_t a[16], b[16];
+    tmem_ld16(ta, a);
+    tmem_ld16(tb, b);
+    tmem_wait_ld(a);
+    tmem_wait_ld(b);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        fa[j] = __uint_as_float(a[j]);
+        fb[j] = __uint_as_float(b[j]);
+    }
+}
+__device__ __forceinline__ void tmem_load16f3(uint32_t ta, uint32_t tb, uint32_t tc,
+                                              float (&fa)[16], float (&fb)[16], float (&fc)[16]) {
+    uint32_t a[16], b[16], c[16];
+    tmem_ld16(ta, a);
+    tmem_ld16(tb, b);
+    tmem_ld16(tc, c);
+    tmem_wait_ld(a);
+    tmem_wait_ld(b);
+    tmem_wait_ld(c);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        fa[j] = __uint_as_float(a[j]);
+        fb[j] = __uint_as_float(b[j]);
+        fc[j] = __uint_as_float(c[j]);
+    }
 }
 
 // Writes 16 values as bf16 into row `row`, columns col0..col0+15 of a tile.

@@ -46,27 +46,72 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
                       pack_bf16(f[6], f[7]));
 }
 
+template <int W>
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, float* f) {
+    if constexpr (W == 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+    } else {
+        uint32_t r[32];
+        tmem_ld32(taddr, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+    }
+}
+template <int W>
+__device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, float* fb) {
+    if constexpr (W == 16) {
+        uint32_t a[16], b2[16];
+        tmem_ld16(ta, a);
+        tmem_ld16(tb, b2);
+        tmem_wait_ld(a);
+        tmem_wait_ld(b2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            fa[j] = __uint_as_float(a[j]);
+            fb[j] = __uint_as_float(b2[j]);
+        }
+    } else {
+        uint32_t a[32], b2[32];
+        tmem_ld32x2(ta, tb, a, b2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            fa[j] = __uint_as_float(a[j]);
+            fb[j] = __uint_as_float(b2[j]);
+        }
+    }
+}
+
 // ============================================================ reverse scan
 template <int Vt>
 struct BScan {
-    static constexpr int STAGE = 57344;              // Mqk 8K | K 16K | Q 16K | W 16K
-    static constexpr int OFF_M = 0, OFF_K = 8192, OFF_Q = 24576, OFF_W = 40960;
-    static constexpr int DS_OP = 2 * STAGE;          // dS1^T [128 k][Vt], MN-major, no swizzle
-    static constexpr int DO_OP = DS_OP + kD * Vt * 2;  // dO [64 s][Vt]
-    static constexpr int GDO_OP = DO_OP + kC * Vt * 2; // gamma dO
-    static constexpr int DU_OP = GDO_OP + kC * Vt * 2; // dU
+    // stage: Mqk 8K | K_0 | K_1 | Q_0 | Q_1 | W_0 | W_1 (8K each) | dO slice [Vt/8][64][8]
+    static constexpr int OFF_M = 0, OFF_K = 8192, OFF_Q = 24576, OFF_W = 40960, OFF_DO = 57344;
+    static constexpr int STAGE = 57344 + kC * Vt * 2;
+    static constexpr int DS_OP = 2 * STAGE;            // dS1^T [Vt/8][128 k][8], MN-major, no swizzle
+    static constexpr int GDO_OP = DS_OP + kD * Vt * 2;  // gamma dO, two buffers [Vt/8][64][8]
+    static constexpr int DU_OP = GDO_OP + 2 * kC * Vt * 2;
     static constexpr int BAR = DU_OP + kC * Vt * 2;
     static constexpr size_t SMEM = BAR + 64 + 1024;
     static constexpr uint32_t TMEM_COLS = (3 * Vt <= 64) ? 64 : (3 * Vt <= 128 ? 128 : 256);
 };
 
+// 256 threads; warps w and w+4 split the columns of TMEM lanes 32*(w%4) ...
+// Lanes 0-63: rows of dU (critical); lanes 64-127 prepare the next chunk's
+// gamma dO operand; all lanes update dS^T (rows k).
 template <int Vt>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
 scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
-            const bf16* __restrict__ d_o, const float* __restrict__ G, const float* dsT,
-            bf16* __restrict__ dU_out, bf16* __restrict__ dS1_out, float* ds0, int* err) {
+            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dU,
+            const __grid_constant__ CUtensorMap tm_dS1, const float* __restrict__ G, const float* dsT,
+            float* ds0, int* err) {
     using P = BScan<Vt>;
+    constexpr int HV = Vt / 2;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     uint64_t* tbar = (uint64_t*)(sm + P::BAR);
@@ -75,6 +120,12 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint32_t* tslot = (uint32_t*)(sm + P::BAR + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sub = warp & 3, half = warp >> 2;
+    const int lanerow = 32 * sub + lane;
+    const int cb = half * HV;
+    const bool issuer = tid == 96;
+    const bool urow = sub < 2;
+    const int r = urow ? lanerow : lanerow - 64;
     const int v0 = blockIdx.x * Vt, h = blockIdx.y, b = blockIdx.z;
     const int64_t strm = (int64_t)b * d.H + h;
     const int NC = d.NC;
@@ -84,20 +135,18 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         unsigned char* st = sm + (it & 1) * P::STAGE;
         uint64_t* bar = &tbar[it & 1];
         const int row = (int)((strm * NC + c) * kC);
-        mbar_arrive_expect_tx(bar, 7 * 8192);
+        mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         tma_load_2d(st + P::OFF_M, &tm_M, bar, 0, row);
         for (int j = 0; j < 2; ++j) {
             tma_load_4d(st + P::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, c * kC, b);
             tma_load_4d(st + P::OFF_Q + j * 8192, &tm_q, bar, 64 * j, h, c * kC, b);
             tma_load_2d(st + P::OFF_W + j * 8192, &tm_W, bar, 64 * j, row);
         }
+        tma_load_5d(st + P::OFF_DO, &tm_do, bar, 0, c * kC, v0 / 8, h, b);
     };
 
-    if (tid == 0) {
-        mbar_init(&tbar[0], 1);
-        mbar_init(&tbar[1], 1);
-        mbar_init(bar1, 1);
-        mbar_init(bar2, 1);
+    if (issuer) {
+        for (int i = 0; i < 4; ++i) mbar_init(&tbar[i], 1);
         fence_mbar_init();
         issue_loads(0);
         if (NC > 1) issue_loads(1);
@@ -106,159 +155,175 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_alloc(tslot, P::TMEM_COLS);
         tmem_relinquish();
     }
-    const int k = tid;
-    float ds[Vt];
+    const int k = lanerow;
+    float ds[HV];
 #pragma unroll
-    for (int v = 0; v < Vt; ++v) ds[v] = dsT ? dsT[(strm * d.V + v0 + v) * kD + k] : 0.f;
+    for (int j = 0; j < HV; ++j) ds[j] = dsT ? dsT[(strm * d.V + v0 + cb + j) * kD + k] : 0.f;
     auto write_ds_operand = [&]() {
 #pragma unroll
-        for (int g = 0; g < Vt / 8; ++g) *(uint4*)(sm + P::DS_OP + g * 2048 + k * 16) = pack8(&ds[8 * g]);
+        for (int g = 0; g < HV / 8; ++g)
+            *(uint4*)(sm + P::DS_OP + (cb / 8 + g) * 2048 + k * 16) = pack8(&ds[8 * g]);
     };
     write_ds_operand();
+    // G of a chunk is fetched one chunk ahead.
+    float GC_n = G[(strm * NC + NC - 1) * kC + kC - 1], Gr_n = G[(strm * NC + NC - 1) * kC + r];
+    // gamma dO operand (buffer it2 & 1) of the chunk held in stage it2 & 1; rows of
+    // lanes 64-127; uses gamma_r = exp(Gr_n) of that chunk.
+    auto write_gdo_operand = [&](int it2, bool& okk) {
+        okk = mbar_wait(&tbar[it2 & 1], (it2 >> 1) & 1, err, 8) && okk;
+        const float gr = expf(Gr_n);
+        const unsigned char* dsrc = sm + (it2 & 1) * P::STAGE + P::OFF_DO;
+        unsigned char* ddst = sm + P::GDO_OP + (it2 & 1) * (kC * Vt * 2);
+#pragma unroll
+        for (int g = 0; g < HV / 8; ++g) {
+            const int gg = cb / 8 + g;
+            const uint4 x = *(const uint4*)(dsrc + gg * 1024 + r * 16);
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = gr * bf_lo(w4[e]);
+                f[2 * e + 1] = gr * bf_hi(w4[e]);
+            }
+            *(uint4*)(ddst + gg * 1024 + r * 16) = pack8(f);
+        }
+    };
+    bool ok = true;
+    if (!urow) write_gdo_operand(0, ok);
     fence_proxy_async();
     fence_before_sync();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t tA = tmem, tB = tmem + Vt, tCc = tmem + 2 * Vt;
-    const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
-    const int r = warp * 16 + (lane & 15);
-    const bool rowthr = lane < 16;
+    const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
+    const uint64_t dDS = sdesc(smem_u32(sm + P::DS_OP), 128, 2048, SW_NONE);
+    const uint64_t dDU = sdesc(smem_u32(sm + P::DU_OP), 128, 1024, SW_NONE);
+    const uint32_t idn = idesc_bf16(128, Vt, false, true);
+    const uint32_t idm = idesc_bf16(128, Vt, true, true);
+    const uint32_t idneg = idesc_bf16(128, Vt, true, true, true);  // -W^T dU
 
-    bool ok = true;
     int it = 0;
 #pragma unroll 1
-    for (; it < NC; ++it) {
+    for (; ok && it < NC; ++it) {
         const int c = NC - 1 - it;
         const int stg = it & 1;
         unsigned char* st = sm + stg * P::STAGE;
         const int64_t chunk = strm * NC + c;
-        const int t0 = c * kC;
-        const float* Gc = G + chunk * kC;
-        const float GC = Gc[kC - 1];
+        const float GC = GC_n;
         const float gC = expf(GC);
-        const float Gr = Gc[r];
-        const float gr = expf(Gr), er = expf(GC - Gr);
-        // dO row r of this slice -> operands dO and gamma dO (MN-major, no swizzle)
-        {
-            uint32_t dor[Vt / 2];
-            if (t0 + r < d.T) {
-                const uint4* p = (const uint4*)(d_o + (((int64_t)b * d.T + t0 + r) * d.H + h) * d.V + v0);
-#pragma unroll
-                for (int q = 0; q < Vt / 8; ++q) {
-                    uint4 x = p[q];
-                    dor[4 * q] = x.x; dor[4 * q + 1] = x.y; dor[4 * q + 2] = x.z; dor[4 * q + 3] = x.w;
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < Vt / 2; ++q) dor[q] = 0u;
-            }
-            if (rowthr) {
-#pragma unroll
-                for (int g = 0; g < Vt / 8; ++g) {
-                    *(uint4*)(sm + P::DO_OP + g * 1024 + r * 16) =
-                        make_uint4(dor[4 * g], dor[4 * g + 1], dor[4 * g + 2], dor[4 * g + 3]);
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        f[2 * e] = gr * bf_lo(dor[4 * g + e]);
-                        f[2 * e + 1] = gr * bf_hi(dor[4 * g + e]);
-                    }
-                    *(uint4*)(sm + P::GDO_OP + g * 1024 + r * 16) = pack8(f);
-                }
-            }
-        }
-        // the gradient of this chunk's end state, for the chunk-local gradients
-        {
-            uint4* dst = (uint4*)(dS1_out + (chunk * kD + k) * d.V + v0);
-#pragma unroll
-            for (int g = 0; g < Vt / 8; ++g) dst[g] = pack8(&ds[8 * g]);
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-        if (tid == 0) {
+        const float er = expf(GC - Gr_n);
+        if (issuer) {
+            // the gradient of this chunk's end state, for the chunk-local gradients
+            tma_store_3d(&tm_dS1, sm + P::DS_OP, 0, (int)(chunk * kD), v0 / 8);
+            bulk_commit();
             const bool okt = mbar_wait(&tbar[stg], (it >> 1) & 1, err, 8);
             if (okt) {
-                const uint32_t mb = smem_u32(st + P::OFF_M), kb = smem_u32(st + P::OFF_K);
-                const uint32_t qb = smem_u32(st + P::OFF_Q);
-                const uint32_t dob = smem_u32(sm + P::DO_OP), gdob = smem_u32(sm + P::GDO_OP);
-                const uint32_t dsb = smem_u32(sm + P::DS_OP);
-                const uint32_t ida = idesc_bf16(64, Vt, true, true);
-                const uint32_t idb = idesc_bf16(64, Vt, false, true);
-                const uint32_t idc = idesc_bf16(128, Vt, true, true);
+                // rows 64-127 of the first two A operands are neighbouring tiles (unused)
+                const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 16, 1024, SW_128B);
+                const uint64_t dM = sdesc(smem_u32(st + P::OFF_M), 8192, 1024, SW_128B);
+                const uint64_t dQ = sdesc(smem_u32(st + P::OFF_Q), 8192, 1024, SW_128B);
+                const uint64_t dDO = sdesc(smem_u32(st + P::OFF_DO), 128, 1024, SW_NONE);
+                const uint64_t dG = sdesc(smem_u32(sm + P::GDO_OP + stg * (kC * Vt * 2)), 128, 1024, SW_NONE);
 #pragma unroll
                 for (int s2 = 0; s2 < 8; ++s2)
-                    mma_bf16_ss(tB, desc_kmaj(kb, 64, s2), sdesc(dsb + s2 * 256, 128, 2048, SW_NONE), idb, s2 > 0);
-#pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2) {
-                    mma_bf16_ss(tA, desc_mnmaj(mb, 64, s2), sdesc(dob + s2 * 256, 128, 1024, SW_NONE), ida, s2 > 0);
-                    mma_bf16_ss(tCc, desc_mnmaj(qb, 64, s2), sdesc(gdob + s2 * 256, 128, 1024, SW_NONE), idc,
+                    mma_bf16_ss(tB, desc_add(dK, (s2 >> 2) * 8192 + (s2 & 3) * 32), desc_add(dDS, s2 * 256), idn,
                                 s2 > 0);
-                }
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_bf16_ss(tA, desc_add(dM, s2 * 2048), desc_add(dDO, s2 * 256), idm, s2 > 0);
                 mma_commit(bar1);
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_bf16_ss(tCc, desc_add(dQ, s2 * 2048), desc_add(dG, s2 * 256), idm, s2 > 0);
             }
         }
-        ok = mbar_wait(bar1, it & 1, err, 16) && ok;
-        __syncwarp();
-        fence_after_sync();
-        // dU = Mqk^T dO + e_r (K dS1^T)
+        if (c > 0) {
+            GC_n = G[(chunk - 1) * kC + kC - 1];
+            Gr_n = G[(chunk - 1) * kC + r];
+        }
+        if (urow) {
+            ok = mbar_wait(bar1, it & 1, err, 16) && ok;
+            __syncwarp();
+            fence_after_sync();
+            // dU = Mqk^T dO + e_r (K dS1^T)  (row r, columns cb .. cb+HV)
+            float a[HV], bb[HV];
+            if constexpr (HV == 8) {
+                uint32_t wa[16], wb[16];
+                tmem_ld16(tA + lanebase, wa);
+                tmem_ld16(tB + lanebase, wb);
+                tmem_wait_ld(wa);
+                tmem_wait_ld(wb);
 #pragma unroll
-        for (int c0 = 0; c0 < Vt; c0 += 16) {
-            float a[16], bb[16], u[16];
-            tmem_load16f(tA + lanebase + c0, a);
-            tmem_load16f(tB + lanebase + c0, bb);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) u[j] = a[j] + er * bb[j];
-            if (rowthr) {
-                const uint4 lo = pack8(u), hi = pack8(u + 8);
-                *(uint4*)(sm + P::DU_OP + (c0 >> 3) * 1024 + r * 16) = lo;
-                *(uint4*)(sm + P::DU_OP + ((c0 >> 3) + 1) * 1024 + r * 16) = hi;
-                uint4* gp = (uint4*)(dU_out + (chunk * kC + r) * d.V + v0 + c0);
-                gp[0] = lo;
-                gp[1] = hi;
+                for (int j = 0; j < 8; ++j) {
+                    a[j] = __uint_as_float(half ? wa[8 + j] : wa[j]);
+                    bb[j] = __uint_as_float(half ? wb[8 + j] : wb[j]);
+                }
+            } else {
+                tmem_cols2<HV>(tA + lanebase + cb, tB + lanebase + cb, a, bb);
             }
+#pragma unroll
+            for (int g = 0; g < HV / 8; ++g) {
+                float u[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) u[j] = a[8 * g + j] + er * bb[8 * g + j];
+                *(uint4*)(sm + P::DU_OP + (cb / 8 + g) * 1024 + r * 16) = pack8(u);
+            }
+        } else if (c > 0) {
+            write_gdo_operand(it + 1, ok);  // operand of the next chunk (c - 1)
         }
         fence_proxy_async();
         fence_before_sync();
+        if (issuer) bulk_wait_read0();  // the dS1 store no longer reads dS1^T
         ok = __syncthreads_and(ok);
         if (!ok) break;
         fence_after_sync();
-        if (tid == 0) {
-            const uint32_t wb = smem_u32(st + P::OFF_W), dub = smem_u32(sm + P::DU_OP);
-            const uint32_t idd = idesc_bf16(128, Vt, true, true, true);  // -W^T dU
+        if (issuer) {
+            tma_store_3d(&tm_dU, sm + P::DU_OP, 0, (int)(chunk * kC), v0 / 8);
+            bulk_commit();
+            const uint64_t dW = sdesc(smem_u32(st + P::OFF_W), 8192, 1024, SW_128B);
 #pragma unroll
             for (int s2 = 0; s2 < 4; ++s2)
-                mma_bf16_ss(tCc, desc_mnmaj(wb, 64, s2), sdesc(dub + s2 * 256, 128, 1024, SW_NONE), idd, 1u);
+                mma_bf16_ss(tCc, desc_add(dW, s2 * 2048), desc_add(dDU, s2 * 256), idneg, 1u);
             mma_commit(bar2);
         }
         ok = mbar_wait(bar2, it & 1, err, 32) && ok;
         __syncwarp();
         fence_after_sync();
-        if (tid == 0 && ok && it + 2 < NC) issue_loads(it + 2);
+        if (issuer && ok && it + 2 < NC) issue_loads(it + 2);
         __syncwarp();
+        {
+            float x[HV];
+            if constexpr (HV == 8) {
+                uint32_t w16[16];
+                tmem_ld16(tCc + lanebase, w16);
+                tmem_wait_ld(w16);
 #pragma unroll
-        for (int c0 = 0; c0 < Vt; c0 += 16) {
-            float x[16];
-            tmem_load16f(tCc + lanebase + c0, x);
+                for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
+            } else {
+                tmem_cols<HV>(tCc + lanebase + cb, x);
+            }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ds[c0 + j] = gC * ds[c0 + j] + x[j];
+            for (int j = 0; j < HV; ++j) ds[j] = gC * ds[j] + x[j];
         }
         write_ds_operand();
         fence_proxy_async();
         fence_before_sync();
+        if (issuer) bulk_wait_read0();  // the dU store no longer reads the dU tile
         ok = __syncthreads_and(ok);
         if (!ok) break;
         fence_after_sync();
     }
     if (ok && ds0) {
 #pragma unroll
-        for (int v = 0; v < Vt; ++v) ds0[(strm * d.V + v0 + v) * kD + k] = ds[v];
+        for (int j = 0; j < HV; ++j) ds0[(strm * d.V + v0 + cb + j) * kD + k] = ds[j];
     }
-    if (!ok && tid == 0) {
-        for (int i2 = it; i2 < NC && i2 < it + 2; ++i2) mbar_wait(&tbar[i2 & 1], (i2 >> 1) & 1, nullptr, 0);
+    if (issuer) {
+        if (!ok)
+            for (int i2 = it; i2 < NC && i2 < it + 2; ++i2) mbar_wait(&tbar[i2 & 1], (i2 >> 1) & 1, nullptr, 0);
+        bulk_wait0();
     }
+    __syncwarp();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -368,9 +433,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 16) {
             float x[16], y[16], z[16], u[16], eu[16], dd[8], de[8];
-            tmem_load16f(tmem + 0 + lanebase + c0, x);
-            tmem_load16f(tmem + 128 + lanebase + c0, y);
-            tmem_load16f(tmem + 256 + lanebase + c0, z);
+            tmem_load16f3(tmem + 0 + lanebase + c0, tmem + 128 + lanebase + c0, tmem + 256 + lanebase + c0, x,
+                          y, z);
             const uint4 ua = up[c0 / 8], ub = up[c0 / 8 + 1];
             const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
@@ -417,12 +481,12 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mma_commit(&bars[1]);
     }
     {   // <dS1, S0> over the chunk (both tiles share one layout)
-        const uint4* a = (const uint4*)(sm + qk::S0) + tid * 16;
-        const uint4* bq = (const uint4*)(sm + qk::DS1) + tid * 16;
+        const uint4* a = (const uint4*)(sm + qk::S0) + tid;
+        const uint4* bq = (const uint4*)(sm + qk::DS1) + tid;
         float acc = 0.f;
 #pragma unroll 4
         for (int i = 0; i < 16; ++i) {
-            const uint4 x = a[i], y = bq[i];
+            const uint4 x = a[i * 128], y = bq[i * 128];
             const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc += bf_lo(xw[e]) * bf_lo(yw[e]) + bf_hi(xw[e]) * bf_hi(yw[e]);
@@ -452,11 +516,13 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // dW^T row k -> scratch
         uint4* wp = (uint4*)(dWt + ((int64_t)krow0 + tid) * kC);
 #pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            float w[16];
-            tmem_load16f(tmem + 128 + lanebase + c0, w);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            float w[16], w2[16];
+            tmem_load16f2(tmem + 128 + lanebase + c0, tmem + 128 + lanebase + c0 + 16, w, w2);
             wp[c0 / 8] = pack8(w);
             wp[c0 / 8 + 1] = pack8(w + 8);
+            wp[c0 / 8 + 2] = pack8(w2);
+            wp[c0 / 8 + 3] = pack8(w2 + 8);
         }
     }
     fence_proxy_async();
@@ -492,9 +558,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 16) {
             float q1[16], q2[16], kk[16];
-            tmem_load16f(tmem + 64 + lanebase + c0, q1);
-            tmem_load16f(tmem + 256 + lanebase + c0, q2);
-            tmem_load16f(tmem + 192 + lanebase + c0, kk);
+            tmem_load16f3(tmem + 64 + lanebase + c0, tmem + 256 + lanebase + c0, tmem + 192 + lanebase + c0, q1,
+                          q2, kk);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 *(bf16*)(dqt + tile_off(64, c0 + j, tid)) = __float2bfloat16_rn(gs[c0 + j] * q1[j] + q2[j]);
@@ -651,9 +716,8 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 16) {
         float qm[16], p[16], kk[16], t8a[8], t8b[8], dt[16];
-        tmem_load16f(tmem + 0 + lanebase + c0, qm);
-        tmem_load16f(tmem + 64 + lanebase + c0, p);
-        tmem_load16f(tmem + 128 + lanebase + c0, kk);
+        tmem_load16f3(tmem + 0 + lanebase + c0, tmem + 64 + lanebase + c0, tmem + 128 + lanebase + c0, qm, p,
+                      kk);
         tile_get8(sm + wy::T, 64, r, c0, t8a);
         tile_get8(sm + wy::T, 64, r, c0 + 8, t8b);
 #pragma unroll
@@ -793,16 +857,30 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (int s = 0; s < 4; ++s) mma_bf16_ss(tmem + 256, desc_mnmaj(sK, 64, s), desc_kmaj(sE, 64, s), id2, 1u);
         mma_commit(&bars[1]);
     }
-    if (tid == 0) {
-        // dG, then dlog alpha = reverse within-chunk cumsum, dalpha = dlog alpha / alpha
-        float run = 0.f;
-        for (int rr = 63; rr >= 0; --rr) {
-            run += dGq[rr] + dGw[rr] + rE2[rr] - cE2[rr];
-            const int t = t0 + rr;
+    if (warp == 0) {
+        // dG, then dlog alpha = reverse within-chunk cumsum (warp scan, lane l holds
+        // positions 63-2l and 62-2l), dalpha = dlog alpha / alpha
+        const int p1 = 63 - 2 * lane, p0 = 62 - 2 * lane;
+        const float g1 = dGq[p1] + dGw[p1] + rE2[p1] - cE2[p1];
+        const float g0 = dGq[p0] + dGw[p0] + rE2[p0] - cE2[p0];
+        const float pair = g1 + g0;
+        float incl = pair;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const float before = incl - pair;  // sum over positions > p1
+        const float run1 = before + g1, run0 = run1 + g0;
+        const int pos[2] = {p1, p0};
+        const float run[2] = {run1, run0};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + pos[e];
             if (t < d.T) {
                 const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-                dalpha[gi] = __float2bfloat16_rn(run / as_[rr]);
-                dbeta[gi] = __float2bfloat16_rn(dB12[rr] + dB3[rr]);
+                dalpha[gi] = __float2bfloat16_rn(run[e] / as_[pos[e]]);
+                dbeta[gi] = __float2bfloat16_rn(dB12[pos[e]] + dB3[pos[e]]);
             }
         }
     }
@@ -842,15 +920,22 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 }
 
 template <int Vt>
-cudaError_t launch_scan_bwd_vt(const Dims& d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mW,
-                               const CUtensorMap& mM, const void* d_o, const TcBufs& tb, const float* dsT,
-                               const TcBwdBufs& bb, float* ds0, cudaStream_t st) {
+cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
+                               const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st) {
     using P = BScan<Vt>;
+    CUtensorMap mq, mk, mW, mM, mdo, mdU, mdS1;
+    const int64_t rows = d.NS() * d.NC * kC;
+    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
+        !tmap_rows(&mW, tb.W, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC) ||
+        !tmap_core8_bthd(&mdo, d_o, d.B, d.T, d.H, kD, Vt / 8) ||
+        !tmap_core8_rows(&mdU, bb.dU, rows, kD, kC, Vt / 8) ||
+        !tmap_core8_rows(&mdS1, bb.dS1, d.NS() * d.NC * kD, kD, kD, Vt / 8))
+        return cudaErrorInvalidValue;
     auto kern = scan_bwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(kD / Vt, d.H, d.B);
-    kern<<<grid, 128, P::SMEM, st>>>(d, mq, mk, mW, mM, (const bf16*)d_o, tb.G, dsT, bb.dU, bb.dS1, ds0, tb.err);
+    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0, tb.err);
     return cudaGetLastError();
 }
 
@@ -858,15 +943,10 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const CUtensorMap& mq, const CUten
 
 cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
                                const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st) {
-    CUtensorMap mq, mk, mW, mM;
-    const int64_t rows = d.NS() * d.NC * kC;
-    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
-        !tmap_rows(&mW, tb.W, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC))
-        return cudaErrorInvalidValue;
     switch (tc_scan_vt(d)) {
-        case 16: return launch_scan_bwd_vt<16>(d, mq, mk, mW, mM, d_o, tb, dsT, bb, ds0, st);
-        case 32: return launch_scan_bwd_vt<32>(d, mq, mk, mW, mM, d_o, tb, dsT, bb, ds0, st);
-        default: return launch_scan_bwd_vt<64>(d, mq, mk, mW, mM, d_o, tb, dsT, bb, ds0, st);
+        case 16: return launch_scan_bwd_vt<16>(d, q, k, d_o, tb, dsT, bb, ds0, st);
+        case 32: return launch_scan_bwd_vt<32>(d, q, k, d_o, tb, dsT, bb, ds0, st);
+        default: return launch_scan_bwd_vt<64>(d, q, k, d_o, tb, dsT, bb, ds0, st);
     }
 }
 

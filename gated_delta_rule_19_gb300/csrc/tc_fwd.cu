@@ -26,6 +26,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "gdn_internal.h"
 #include "tc.cuh"
 
@@ -318,31 +320,87 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 // ---------------------------------------------------------------------------
 template <int Vt>
 struct ScanPlan {
-    static constexpr int STAGE = 57344;         // Q 16K | W 16K | K 16K | Mqk 8K
-    static constexpr int S_OP = 2 * STAGE;      // S0^T operand [128 k][Vt] bf16, MN-major, no swizzle
-    static constexpr int U_OP = S_OP + kD * Vt * 2;  // U  [64 tok][Vt]
-    static constexpr int UH_OP = U_OP + kC * Vt * 2; // Uh [64 tok][Vt]
-    static constexpr int BAR = UH_OP + kC * Vt * 2;  // tma[2], mma1, mma2
+    // stage: [W_0 | Q_0 | W_1 | Q_1] (stacked A of one M=128 MMA) | K_0 | K_1 | Mqk | Ut slice
+    static constexpr int OFF_WQ = 0, OFF_K = 32768, OFF_M = 49152, OFF_UT = 57344;
+    static constexpr int STAGE = 57344 + kC * Vt * 2;
+    static constexpr int S_OP = 2 * STAGE;           // S0^T [Vt/8][128 k][8] (MN-major, no swizzle)
+    static constexpr int U_OP = S_OP + kD * Vt * 2;  // U  [Vt/8][64 tok][8]
+    static constexpr int UH_OP = U_OP + kC * Vt * 2; // Uh
+    static constexpr int O_OP = UH_OP + kC * Vt * 2; // output tile, same layout
+    static constexpr int BAR = O_OP + kC * Vt * 2;   // tma[2], XY, S, O
     static constexpr int END = BAR + 64;
     static constexpr size_t SMEM = END + 1024;
+    // TMEM: [X;Y] (two buffers), O2, DS, each Vt columns
     static constexpr uint32_t TMEM_COLS = (4 * Vt <= 32) ? 32 : (4 * Vt <= 64 ? 64 : (4 * Vt <= 128 ? 128 : 256));
 };
 
+// Loads W consecutive fp32 TMEM columns (W = 16 or 32) of this thread's lane.
+template <int W>
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, float* f) {
+    if constexpr (W == 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+    } else {
+        uint32_t r[32];
+        tmem_ld32(taddr, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+    }
+}
+// Two W-column groups, one wait.
+template <int W>
+__device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, float* fb) {
+    if constexpr (W == 16) {
+        uint32_t a[16], b2[16];
+        tmem_ld16(ta, a);
+        tmem_ld16(tb, b2);
+        tmem_wait_ld(a);
+        tmem_wait_ld(b2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            fa[j] = __uint_as_float(a[j]);
+            fb[j] = __uint_as_float(b2[j]);
+        }
+    } else {
+        uint32_t a[32], b2[32];
+        tmem_ld32x2(ta, tb, a, b2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            fa[j] = __uint_as_float(a[j]);
+            fb[j] = __uint_as_float(b2[j]);
+        }
+    }
+}
+
+// 256 threads.  Warp w reaches TMEM lanes 32*(w%4) ..; warps w and w+4 split the
+// columns.  Lanes 0-63 hold X = W S0^T (rows of U), lanes 64-127 hold Y = Q S0^T
+// and the output term; the state update uses all 128 lanes (rows k).
 template <int Vt>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
 scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
-            const bf16* __restrict__ Ut, const float* __restrict__ G, const float* s0,
-            bf16* __restrict__ o, float* sT, bf16* __restrict__ states, int* err) {
+            const __grid_constant__ CUtensorMap tm_Ut, const __grid_constant__ CUtensorMap tm_o,
+            const __grid_constant__ CUtensorMap tm_st, const float* __restrict__ G, const float* s0,
+            float* sT, int write_o, int write_states, int* err) {
     using P = ScanPlan<Vt>;
+    constexpr int HV = Vt / 2;  // columns per thread
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     uint64_t* tbar = (uint64_t*)(sm + P::BAR);
-    uint64_t* bar1 = tbar + 2;
-    uint64_t* bar2 = tbar + 3;
-    uint32_t* tslot = (uint32_t*)(sm + P::BAR + 32);
+    uint64_t* barXY = tbar + 2;
+    uint64_t* barS = tbar + 3;
+    uint64_t* barO = tbar + 4;
+    uint32_t* tslot = (uint32_t*)(sm + P::BAR + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sub = warp & 3, half = warp >> 2;
+    const int lanerow = 32 * sub + lane;  // TMEM lane of this thread
+    const int cb = half * HV;             // first column of this thread
+    const bool issuer = tid == 96;        // warp 3 (output side) issues MMAs and copies
     const int v0 = blockIdx.x * Vt, h = blockIdx.y, b = blockIdx.z;
     const int64_t strm = (int64_t)b * d.H + h;
     const int NC = d.NC;
@@ -350,20 +408,19 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     auto issue_loads = [&](int c) {
         unsigned char* st = sm + (c & 1) * P::STAGE;
         const int row = (int)((strm * NC + c) * kC);
-        mbar_arrive_expect_tx(&tbar[c & 1], 7 * 8192);
+        uint64_t* bar = &tbar[c & 1];
+        mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(st + j * 8192, &tm_q, &tbar[c & 1], 64 * j, h, c * kC, b);
-            tma_load_2d(st + 16384 + j * 8192, &tm_W, &tbar[c & 1], 64 * j, row);
-            tma_load_4d(st + 32768 + j * 8192, &tm_k, &tbar[c & 1], 64 * j, h, c * kC, b);
+            tma_load_2d(st + P::OFF_WQ + j * 16384, &tm_W, bar, 64 * j, row);
+            tma_load_4d(st + P::OFF_WQ + j * 16384 + 8192, &tm_q, bar, 64 * j, h, c * kC, b);
+            tma_load_4d(st + P::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, c * kC, b);
         }
-        tma_load_2d(st + 49152, &tm_M, &tbar[c & 1], 0, row);
+        tma_load_2d(st + P::OFF_M, &tm_M, bar, 0, row);
+        tma_load_3d(st + P::OFF_UT, &tm_Ut, bar, 0, row, v0 / 8);
     };
 
-    if (tid == 0) {
-        mbar_init(&tbar[0], 1);
-        mbar_init(&tbar[1], 1);
-        mbar_init(bar1, 1);
-        mbar_init(bar2, 1);
+    if (issuer) {
+        for (int i = 0; i < 5; ++i) mbar_init(&tbar[i], 1);
         fence_mbar_init();
         issue_loads(0);
         if (NC > 1) issue_loads(1);
@@ -372,19 +429,18 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_alloc(tslot, P::TMEM_COLS);
         tmem_relinquish();
     }
-    // State slice: thread k holds S[v0 + v][k], v < Vt.
-    const int k = tid;
-    float s[Vt];
+    // State: thread holds S[v0 + cb + j][k = lanerow], j < HV.
+    const int k = lanerow;
+    float s[HV];
 #pragma unroll
-    for (int v = 0; v < Vt; ++v) s[v] = s0 ? s0[(strm * d.V + v0 + v) * kD + k] : 0.f;
+    for (int j = 0; j < HV; ++j) s[j] = s0 ? s0[(strm * d.V + v0 + cb + j) * kD + k] : 0.f;
     auto write_state_operand = [&]() {
         // MN-major, no swizzle: element (v, k) at (v/8)*2048 + k*16 + (v%8)*2
 #pragma unroll
-        for (int g = 0; g < Vt / 8; ++g) {
-            uint4 pk = make_uint4(pack_bf16(s[8 * g + 0], s[8 * g + 1]), pack_bf16(s[8 * g + 2], s[8 * g + 3]),
-                                  pack_bf16(s[8 * g + 4], s[8 * g + 5]), pack_bf16(s[8 * g + 6], s[8 * g + 7]));
-            *(uint4*)(sm + P::S_OP + g * 2048 + k * 16) = pk;
-        }
+        for (int g = 0; g < HV / 8; ++g)
+            *(uint4*)(sm + P::S_OP + (cb / 8 + g) * 2048 + k * 16) =
+                make_uint4(pack_bf16(s[8 * g + 0], s[8 * g + 1]), pack_bf16(s[8 * g + 2], s[8 * g + 3]),
+                           pack_bf16(s[8 * g + 4], s[8 * g + 5]), pack_bf16(s[8 * g + 6], s[8 * g + 7]));
     };
     write_state_operand();
     fence_proxy_async();
@@ -392,10 +448,60 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tY = tmem, tX = tmem + Vt, tO = tmem + 2 * Vt, tS = tmem + 3 * Vt;
-    const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
-    const int r = warp * 16 + (lane & 15);  // token row of this thread in the M=64 results
-    const bool rowthr = lane < 16;
+    const uint32_t tXY0 = tmem, tO = tmem + 2 * Vt, tS = tmem + 3 * Vt;
+    const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
+    const bool urow = sub < 2;            // lanes 0-63: rows of U (r = lanerow)
+    const int r = urow ? lanerow : lanerow - 64;  // token row (both sides)
+
+    const uint64_t dS = sdesc(smem_u32(sm + P::S_OP), 128, 2048, SW_NONE);
+    const uint64_t dU = sdesc(smem_u32(sm + P::U_OP), 128, 1024, SW_NONE);
+    const uint64_t dUh = sdesc(smem_u32(sm + P::UH_OP), 128, 1024, SW_NONE);
+    const uint32_t id = idesc_bf16(128, Vt, false, true);
+    const uint32_t idmn = idesc_bf16(128, Vt, true, true);
+
+    float GC_n = G[strm * NC * kC + kC - 1], Gr_n = G[strm * NC * kC + r];
+    float gr_prev = 0.f;
+
+    // Output of chunk cc (threads on lanes 64-127): O = gamma Y + Mqk U.
+    auto output_epilogue = [&](int cc, bool& okk) {
+        okk = mbar_wait(barO, cc & 1, err, 64) && okk;
+        __syncwarp();
+        fence_after_sync();
+        if (issuer && okk && cc + 2 < NC) issue_loads(cc + 2);
+        __syncwarp();
+        float y[HV], ov[HV];
+        if constexpr (HV == 8) {
+            uint32_t a[8], b2[8];
+            // two 8-column halves through the x16 loader would over-read; use the
+            // x16 load on a 16-column window and keep our half
+            uint32_t wa[16], wb[16];
+            tmem_ld16(tXY0 + (uint32_t)((cc & 1) * Vt) + lanebase, wa);
+            tmem_ld16(tO + lanebase, wb);
+            tmem_wait_ld(wa);
+            tmem_wait_ld(wb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                a[j] = half ? wa[8 + j] : wa[j];
+                b2[j] = half ? wb[8 + j] : wb[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                y[j] = __uint_as_float(a[j]);
+                ov[j] = __uint_as_float(b2[j]);
+            }
+        } else {
+            tmem_cols2<HV>(tXY0 + (uint32_t)((cc & 1) * Vt) + lanebase + cb, tO + lanebase + cb, y, ov);
+        }
+#pragma unroll
+        for (int g = 0; g < HV / 8; ++g) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = gr_prev * y[8 * g + j] + ov[8 * g + j];
+            *(uint4*)(sm + P::O_OP + (cb / 8 + g) * 1024 + r * 16) =
+                make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                           pack_bf16(f[6], f[7]));
+        }
+    };
 
     bool ok = true;
     int c = 0;
@@ -404,139 +510,141 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int stg = c & 1;
         unsigned char* st = sm + stg * P::STAGE;
         const int64_t chunk = strm * NC + c;
-        const int t0 = c * kC;
-        // chunk-start state -> saved boundary states
-        if (states) {  // bf16, [chunk][k][v]: this thread's row k, columns v0 .. v0+Vt
-            uint4* St = (uint4*)(states + (chunk * kD + k) * d.V + v0);
-#pragma unroll
-            for (int g = 0; g < Vt / 8; ++g)
-                St[g] = make_uint4(pack_bf16(s[8 * g + 0], s[8 * g + 1]), pack_bf16(s[8 * g + 2], s[8 * g + 3]),
-                                   pack_bf16(s[8 * g + 4], s[8 * g + 5]), pack_bf16(s[8 * g + 6], s[8 * g + 7]));
-        }
-        if (tid == 0) {
-            bool okt = mbar_wait(&tbar[stg], (c >> 1) & 1, err, 8);
+        if (issuer) {
+            if (write_states) {  // chunk-start state -> saved boundary states, by TMA
+                tma_store_3d(&tm_st, sm + P::S_OP, 0, (int)(chunk * kD), v0 / 8);
+                bulk_commit();
+            }
+            const bool okt = mbar_wait(&tbar[stg], (c >> 1) & 1, err, 8);
             if (okt) {
-                const uint32_t id = idesc_bf16(64, Vt, false, true);
-                const uint32_t qb = smem_u32(st), wb = smem_u32(st + 16384), sb = smem_u32(sm + P::S_OP);
+                // [X; Y] = [W; Q] S0^T in one M=128 MMA chain
+                const uint64_t dWQ = sdesc(smem_u32(st + P::OFF_WQ), 16, 1024, SW_128B);
 #pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) {
-                    const uint64_t bd = sdesc(sb + s2 * 256, 128, 2048, SW_NONE);
-                    const uint32_t ao = (s2 >> 2) * 8192 + (s2 & 3) * 32;
-                    mma_bf16_ss(tY, sdesc(qb + ao, 16, 1024, SW_128B), bd, id, s2 > 0);
-                    mma_bf16_ss(tX, sdesc(wb + ao, 16, 1024, SW_128B), bd, id, s2 > 0);
-                }
-                mma_commit(bar1);
+                for (int s2 = 0; s2 < 8; ++s2)
+                    mma_bf16_ss(tXY0 + (uint32_t)(stg * Vt), desc_add(dWQ, (s2 >> 2) * 16384 + (s2 & 3) * 32),
+                                desc_add(dS, s2 * 256), id, s2 > 0);
+                mma_commit(barXY);
             }
         }
-        // per-row inputs of this chunk (overlap with the MMA)
-        const float* Gc = G + chunk * kC;
-        const float GC = Gc[kC - 1];
+        const float GC = GC_n;
         const float gC = expf(GC);
-        const float Gr = Gc[r];
+        const float Gr = Gr_n;
         const float gr = expf(Gr), er = expf(GC - Gr);
-        uint32_t utr[Vt / 2];
-        {
-            const uint4* up = (const uint4*)(Ut + (chunk * kC + r) * (int64_t)d.V + v0);
-#pragma unroll
-            for (int q = 0; q < Vt / 8; ++q) {
-                uint4 x = up[q];
-                utr[4 * q + 0] = x.x; utr[4 * q + 1] = x.y; utr[4 * q + 2] = x.z; utr[4 * q + 3] = x.w;
-            }
+        if (c + 1 < NC) {
+            GC_n = G[(chunk + 1) * kC + kC - 1];
+            Gr_n = G[(chunk + 1) * kC + r];
         }
-        ok = mbar_wait(bar1, c & 1, err, 16) && ok;
-        __syncwarp();
-        fence_after_sync();
-        // U = Ut - X, Uh = e_r U  (row r, threads with lane < 16); Y kept as gamma_r Y.
-        float y[Vt];
+        if (!urow && c > 0) output_epilogue(c - 1, ok);  // overlaps this chunk's first MMAs
+        gr_prev = gr;
+        if (urow) {
+            ok = mbar_wait(&tbar[stg], (c >> 1) & 1, err, 8) && ok;  // Ut slice is read below
+            ok = mbar_wait(barXY, c & 1, err, 16) && ok;
+            __syncwarp();
+            fence_after_sync();
+            // U = Ut - X, Uh = e_r U  (row r, columns cb .. cb+HV)
+            float xg[HV];
+            if constexpr (HV == 8) {
+                uint32_t w16[16];
+                tmem_ld16(tXY0 + (uint32_t)(stg * Vt) + lanebase, w16);
+                tmem_wait_ld(w16);
 #pragma unroll
-        for (int c0 = 0; c0 < Vt; c0 += 16) {
-            uint32_t xv[16], yv[16];
-            tmem_ld16(tX + lanebase + c0, xv);
-            tmem_ld16(tY + lanebase + c0, yv);
-            tmem_wait_ld(xv);
-            tmem_wait_ld(yv);
-            uint32_t pu[8], ph[8];
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-                const uint32_t uw = utr[(c0 + j) >> 1];
-                const float u0 = bf_lo(uw) - __uint_as_float(xv[j]);
-                const float u1 = bf_hi(uw) - __uint_as_float(xv[j + 1]);
-                pu[j >> 1] = pack_bf16(u0, u1);
-                ph[j >> 1] = pack_bf16(er * u0, er * u1);
-                y[c0 + j] = gr * __uint_as_float(yv[j]);
-                y[c0 + j + 1] = gr * __uint_as_float(yv[j + 1]);
+                for (int j = 0; j < 8; ++j) xg[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
+            } else {
+                tmem_cols<HV>(tXY0 + (uint32_t)(stg * Vt) + lanebase + cb, xg);
             }
-            if (rowthr) {
+#pragma unroll
+            for (int g = 0; g < HV / 8; ++g) {
+                const int gg = cb / 8 + g;
+                const uint4 uq = *(const uint4*)(st + P::OFF_UT + gg * 1024 + r * 16);
+                const uint32_t uw4[4] = {uq.x, uq.y, uq.z, uq.w};
+                float u[8], uh[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    u[2 * e] = bf_lo(uw4[e]) - xg[8 * g + 2 * e];
+                    u[2 * e + 1] = bf_hi(uw4[e]) - xg[8 * g + 2 * e + 1];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) uh[j] = er * u[j];
                 // MN-major, no swizzle: element (v, r) at (v/8)*1024 + r*16 + (v%8)*2
-                *(uint4*)(sm + P::U_OP + ((c0 >> 3) + 0) * 1024 + r * 16) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
-                *(uint4*)(sm + P::U_OP + ((c0 >> 3) + 1) * 1024 + r * 16) = make_uint4(pu[4], pu[5], pu[6], pu[7]);
-                *(uint4*)(sm + P::UH_OP + ((c0 >> 3) + 0) * 1024 + r * 16) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                *(uint4*)(sm + P::UH_OP + ((c0 >> 3) + 1) * 1024 + r * 16) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+                *(uint4*)(sm + P::U_OP + gg * 1024 + r * 16) =
+                    make_uint4(pack_bf16(u[0], u[1]), pack_bf16(u[2], u[3]), pack_bf16(u[4], u[5]), pack_bf16(u[6], u[7]));
+                *(uint4*)(sm + P::UH_OP + gg * 1024 + r * 16) =
+                    make_uint4(pack_bf16(uh[0], uh[1]), pack_bf16(uh[2], uh[3]), pack_bf16(uh[4], uh[5]), pack_bf16(uh[6], uh[7]));
             }
         }
         fence_proxy_async();
         fence_before_sync();
+        if (issuer) bulk_wait_read0();  // the states store no longer reads S0^T
         ok = __syncthreads_and(ok);
         if (!ok) break;
         fence_after_sync();
-        if (tid == 0) {
-            const uint32_t ub = smem_u32(sm + P::U_OP), uhb = smem_u32(sm + P::UH_OP);
-            const uint32_t mb = smem_u32(st + 49152), kb = smem_u32(st + 32768);
-            const uint32_t id2 = idesc_bf16(64, Vt, false, true);
-            const uint32_t id3 = idesc_bf16(128, Vt, true, true);
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                mma_bf16_ss(tO, sdesc(mb + s2 * 32, 16, 1024, SW_128B), sdesc(ub + s2 * 256, 128, 1024, SW_NONE),
-                            id2, s2 > 0);
-                mma_bf16_ss(tS, sdesc(kb + s2 * 2048, 8192, 1024, SW_128B),
-                            sdesc(uhb + s2 * 256, 128, 1024, SW_NONE), id3, s2 > 0);
+        if (issuer) {
+            if (c > 0 && write_o) {  // output tile of the previous chunk
+                tma_store_5d(&tm_o, sm + P::O_OP, 0, (c - 1) * kC, v0 / 8, h, b);
+                bulk_commit();
             }
-            mma_commit(bar2);
+            const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 8192, 1024, SW_128B);
+            // rows 0-63 of this A are the K_1 block (unused rows), rows 64-127 are Mqk
+            const uint64_t dM = sdesc(smem_u32(st + P::OFF_K + 8192), 16, 1024, SW_128B);
+            // S1^T update first (critical), then the output term
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+                mma_bf16_ss(tS, desc_add(dK, s2 * 2048), desc_add(dUh, s2 * 256), idmn, s2 > 0);
+            mma_commit(barS);
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+                mma_bf16_ss(tO, desc_add(dM, s2 * 32), desc_add(dU, s2 * 256), id, s2 > 0);
+            mma_commit(barO);
         }
-        ok = mbar_wait(bar2, c & 1, err, 32) && ok;
-        fence_after_sync();
-        if (tid == 0 && ok && c + 2 < NC) issue_loads(c + 2);
+        ok = mbar_wait(barS, c & 1, err, 32) && ok;
         __syncwarp();
-        // O = gamma Y + Mqk U
+        fence_after_sync();
+        // S1^T = gamma_C S0^T + K^T Uh
+        {
+            float sv[HV];
+            if constexpr (HV == 8) {
+                uint32_t w16[16];
+                tmem_ld16(tS + lanebase, w16);
+                tmem_wait_ld(w16);
 #pragma unroll
-        for (int c0 = 0; c0 < Vt; c0 += 16) {
-            uint32_t ov[16];
-            tmem_ld16(tO + lanebase + c0, ov);
-            tmem_wait_ld(ov);
-            if (o && rowthr && t0 + r < d.T) {
-                uint32_t po[8];
-#pragma unroll
-                for (int j = 0; j < 16; j += 2)
-                    po[j >> 1] = pack_bf16(y[c0 + j] + __uint_as_float(ov[j]), y[c0 + j + 1] + __uint_as_float(ov[j + 1]));
-                uint4* op = (uint4*)(o + (((int64_t)b * d.T + t0 + r) * d.H + h) * d.V + v0 + c0);
-                op[0] = make_uint4(po[0], po[1], po[2], po[3]);
-                op[1] = make_uint4(po[4], po[5], po[6], po[7]);
+                for (int j = 0; j < 8; ++j) sv[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
+            } else {
+                tmem_cols<HV>(tS + lanebase + cb, sv);
             }
-        }
-        // S1^T = gamma_C S0^T + K^T Uh  (thread k = lane of the M=128 result)
 #pragma unroll
-        for (int c0 = 0; c0 < Vt; c0 += 16) {
-            uint32_t sv[16];
-            tmem_ld16(tS + lanebase + c0, sv);
-            tmem_wait_ld(sv);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) s[c0 + j] = gC * s[c0 + j] + __uint_as_float(sv[j]);
+            for (int j = 0; j < HV; ++j) s[j] = gC * s[j] + sv[j];
         }
         write_state_operand();
         fence_proxy_async();
         fence_before_sync();
+        if (issuer) bulk_wait_read0();  // the output store no longer reads the O tile
         ok = __syncthreads_and(ok);
         if (!ok) break;
         fence_after_sync();
     }
+    if (ok && NC > 0) {
+        if (!urow) output_epilogue(NC - 1, ok);
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        if (issuer && ok && write_o) {
+            tma_store_5d(&tm_o, sm + P::O_OP, 0, (NC - 1) * kC, v0 / 8, h, b);
+            bulk_commit();
+        }
+    }
     if (ok && sT) {
 #pragma unroll
-        for (int v = 0; v < Vt; ++v) sT[(strm * d.V + v0 + v) * kD + k] = s[v];
+        for (int j = 0; j < HV; ++j) sT[(strm * d.V + v0 + cb + j) * kD + k] = s[j];
     }
-    if (!ok && tid == 0) {
-        // drain the loads still in flight (bounded) before leaving
-        for (int cc = c; cc < NC && cc < c + 2; ++cc) mbar_wait(&tbar[cc & 1], (cc >> 1) & 1, nullptr, 0);
+    if (issuer) {
+        if (!ok) {
+            // drain what may still be in flight (bounded) before leaving
+            for (int cc = c; cc < NC && cc < c + 2; ++cc) mbar_wait(&tbar[cc & 1], (cc >> 1) & 1, nullptr, 0);
+            mbar_wait(barO, (c > 0 ? c - 1 : 0) & 1, nullptr, 0);
+        }
+        bulk_wait0();
     }
+    __syncwarp();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -544,15 +652,26 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }
 
 template <int Vt>
-cudaError_t launch_scan_vt(const Dims& d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mW,
-                           const CUtensorMap& mM, const TcBufs& tb, const float* s0, void* o, float* sT,
-                           bf16* states, cudaStream_t st) {
+cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
+                           void* o, float* sT, bf16* states, cudaStream_t st) {
     using P = ScanPlan<Vt>;
+    CUtensorMap mq, mk, mW, mM, mUt, mo, mst;
+    const int64_t rows = d.NS() * d.NC * kC;
+    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
+        !tmap_rows(&mW, tb.W, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC) ||
+        !tmap_core8_rows(&mUt, tb.Ut, rows, kD, kC, Vt / 8))
+        return cudaErrorInvalidValue;
+    memset(&mo, 0, sizeof(mo));
+    memset(&mst, 0, sizeof(mst));
+    if (o && !tmap_core8_bthd(&mo, o, d.B, d.T, d.H, kD, Vt / 8)) return cudaErrorInvalidValue;
+    if (states && !tmap_core8_rows(&mst, states, d.NS() * d.NC * kD, kD, kD, Vt / 8))
+        return cudaErrorInvalidValue;
     auto kern = scan_fwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(kD / Vt, d.H, d.B);
-    kern<<<grid, 128, P::SMEM, st>>>(d, mq, mk, mW, mM, tb.Ut, tb.G, s0, (bf16*)o, sT, states, tb.err);
+    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, o != nullptr,
+                                     states != nullptr, tb.err);
     return cudaGetLastError();
 }
 
@@ -587,15 +706,10 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
 
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
                                void* o, float* sT, __nv_bfloat16* states, cudaStream_t st) {
-    CUtensorMap mq, mk, mW, mM;
-    const int64_t rows = d.NS() * d.NC * kC;
-    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
-        !tmap_rows(&mW, tb.W, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC))
-        return cudaErrorInvalidValue;
     switch (tc_scan_vt(d)) {
-        case 16: return launch_scan_vt<16>(d, mq, mk, mW, mM, tb, s0, o, sT, states, st);
-        case 32: return launch_scan_vt<32>(d, mq, mk, mW, mM, tb, s0, o, sT, states, st);
-        default: return launch_scan_vt<64>(d, mq, mk, mW, mM, tb, s0, o, sT, states, st);
+        case 16: return launch_scan_vt<16>(d, q, k, tb, s0, o, sT, states, st);
+        case 32: return launch_scan_vt<32>(d, q, k, tb, s0, o, sT, states, st);
+        default: return launch_scan_vt<64>(d, q, k, tb, s0, o, sT, states, st);
     }
 }
 

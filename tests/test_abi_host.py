@@ -61,8 +61,11 @@ def test_version_and_status_strings(lib):
 def test_sizes(lib):
     p = lib.make_problem(8, 4096, 6, 128, 128, 64, 1)
     NC = 64
-    # bf16 K=V=128 chunk 64 runs on tensor cores and keeps bf16 boundary states
-    assert lib.gdn_saved_bytes(p) == 8 * 6 * NC * 128 * 128 * 2
+    # bf16 K=V=128 chunk 64 runs on tensor cores: bf16 boundary states followed by
+    # the forward's chunk results (G f32; W, Ut, Mqk, T bf16), each region 256-aligned
+    rows = 8 * 6 * NC * 64
+    expect = 8 * 6 * NC * 128 * 128 * 2 + rows * 4 + rows * 128 * 2 * 2 + rows * 64 * 2 * 2
+    assert lib.gdn_saved_bytes(p) == expect
     # other shapes keep float32 boundary states
     assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 1)) == 8 * 6 * NC * 64 * 64 * 4
     assert lib.gdn_fwd_workspace_bytes(p) > 0

@@ -164,3 +164,52 @@ def test_null_update_and_exact_write_on_gpu():
     assert rel_l2(to_np(sT), to_np(d["initial_state"])) < 1e-6
     o, _, _ = gdn.gdn_fwd(d["k"], d["k"], d["v"], d["alpha"], ones, d["initial_state"], chunk=64)
     assert rel_l2(to_np(o), to_np(d["v"])) < 1e-5
+
+
+# ------------------------------------------------ tensor-core path (bf16, K=V=128, C=64)
+
+@pytest.mark.parametrize("T", [1, 63, 65, 200])
+def test_tc_path_ragged_lengths(oracle_mod, T):
+    w = custom(B=2, T=T, H=3, K=128, V=128, chunk=64, dtype="bf16", seed=300 + T, init_std=0.1,
+               dfinal_std=0.01)
+    inp = make_inputs(w)
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16")
+
+
+def test_tc_path_many_streams_multiple_waves(oracle_mod):
+    """B*H above the SM count: the scans run in several waves of CTAs."""
+    w = custom(B=4, T=128, H=40, K=128, V=128, chunk=64, dtype="bf16", seed=77, init_std=0.1,
+               dfinal_std=0.01)
+    inp = make_inputs(w)
+    got = gpu_run(w, inp, True)
+    streams = [(0, 0), (1, 17), (2, 33), (3, 39)]
+    ref = oracle_run(oracle_mod, inp, True, streams=streams)
+    compare(sample_gpu(got, streams), ref, "bf16")
+
+
+def test_tc_backward_recompute_equals_saved():
+    w = custom(B=2, T=300, H=2, K=128, V=128, chunk=64, dtype="bf16", seed=8, init_std=0.1,
+               dfinal_std=0.01)
+    inp = make_inputs(w)
+    a = gpu_run(w, inp, True, saved_mode="saved")
+    b = gpu_run(w, inp, True, saved_mode="recompute")
+    for n in a:
+        np.testing.assert_array_equal(a[n], b[n], err_msg=n)
+
+
+def test_tc_error_flag_stays_clear():
+    """The tensor-core kernels' bounded waits never give up in a normal run: the
+    error word at the start of the caller's workspace stays 0."""
+    w = custom(B=2, T=256, H=2, K=128, V=128, chunk=64, dtype="bf16", seed=9, init_std=0.1,
+               dfinal_std=0.01)
+    inp = make_inputs(w)
+    d = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+    args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"])
+    p = gdn.make_problem(w.B, w.T, w.H, w.K, w.V, w.chunk, torch.bfloat16)
+    wsf = torch.full((gdn.gdn_fwd_workspace_bytes(p),), 0x5A, dtype=torch.uint8, device="cuda")
+    wsb = torch.full((gdn.gdn_bwd_workspace_bytes(p),), 0x5A, dtype=torch.uint8, device="cuda")
+    _, _, saved = gdn.gdn_fwd(*args, chunk=w.chunk, saved=True, workspace=wsf)
+    gdn.gdn_bwd(*args, d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk, workspace=wsb)
+    torch.cuda.synchronize()
+    assert int(wsf[:4].view(torch.int32).item()) == 0
+    assert int(wsb[:4].view(torch.int32).item()) == 0
