@@ -15,7 +15,7 @@ namespace gdn {
 // is done in int64.
 struct Dims {
     int B, T, H, K, V, C, NC;
-    int64_t NS() const { return (int64_t)B * H; }
+    __host__ __device__ int64_t NS() const { return (int64_t)B * H; }
 };
 
 // Per-chunk results of the chunk-parallel step (Phase 1 + solve + recompute),

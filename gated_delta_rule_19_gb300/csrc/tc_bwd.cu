@@ -26,6 +26,8 @@
 //
 // Every wait is bounded (2 s) and raises the error flag when it gives up.
 
+#include <algorithm>
+
 #include "gdn_internal.h"
 #include "tc.cuh"
 
@@ -84,6 +86,25 @@ __device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, 
             fb[j] = __uint_as_float(b2[j]);
         }
     }
+}
+
+// Column sums of a 32 x 32 block held one row per lane: on entry lane l holds
+// v[0..31] (row l); on return lane l holds the sum over the 32 rows of column l.
+// Butterfly reduce-scatter, 31 shuffles.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = lane & w;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            // keep the half of the columns this lane is responsible for, send the other
+            const float send = upper ? v[j] : v[j + w];
+            const float keep = upper ? v[j + w] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
 }
 
 // ============================================================ reverse scan
@@ -332,17 +353,24 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 // ====================================================== chunk gradients (1)
 namespace qk {
-constexpr int Q = 0, K = 16384, DO = 32768, W = 49152, DU = 65536;  // [64 x 128] tiles
-constexpr int S0 = 81920, DS1 = 114688;                              // [128 x 128] tiles
-constexpr int U = 147456, EU = 163840;                               // [64 x 128]
-constexpr int DQK = 180224;                                          // [64 x 64]
-constexpr int E1 = 188416;                                           // fp32 [64][65]
-constexpr int VEC = E1 + 64 * 65 * 4;                                // 8 x 64 floats + 128
-constexpr int BAR = VEC + (8 * 64 + 128) * 4;
+constexpr int WQ = 0;                  // [W_0 | Q_0 | W_1 | Q_1]: stacked [W;Q] and Q (MN-major)
+constexpr int K = 32768;               // [K_0 | K_1]
+constexpr int DO = 49152;              // [dO_0 | dO_1]
+constexpr int DU = 65536;              // [64 x 128]
+constexpr int S0 = 81920, DS1 = 114688;  // [128 x 128]
+constexpr int U = 147456, EU = 163840;   // [64 x 128]
+constexpr int DQK = 180224;              // [64 x 64]
+constexpr int DQ = 188416;               // dq output tile [64 x 128]
+constexpr int E1 = 204800;               // fp32 [64][65]
+constexpr int VEC = E1 + 64 * 65 * 4;    // Gs gs eRp[2] dG1p[2] rE1 cE1 (8 x 64) + red (256)
+constexpr int BAR = VEC + (8 * 64 + 256) * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
 }  // namespace qk
 
-__global__ void __launch_bounds__(128, 1)
+// Persistent: CTA i handles chunks i, i + gridDim.x, ...  256 threads; warps w and
+// w+4 split the columns of TMEM lanes 32*(w%4) ..  The next chunk's tiles are
+// requested as soon as their buffers are free (after phase 2 / phase 3).
+__global__ void __launch_bounds__(256, 1)
 grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_W,
            const __grid_constant__ CUtensorMap tm_dU, const __grid_constant__ CUtensorMap tm_S0,
@@ -354,245 +382,322 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     float* E1f = (float*)(sm + qk::E1);
     float* Gs = (float*)(sm + qk::VEC);
     float* gs = Gs + 64;
-    float* eR = gs + 64;
-    float* dG1 = eR + 64;
-    float* rE1 = dG1 + 64;
+    float* eRp = gs + 64;    // [2][64]
+    float* dG1p = eRp + 128; // [2][64]
+    float* rE1 = dG1p + 128;
     float* cE1 = rE1 + 64;
-    float* red = cE1 + 128;  // 128
-    uint64_t* bars = (uint64_t*)(sm + qk::BAR);  // [0] TMA, [1] MMA
-    uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 16);
+    float* red = cE1 + 64;   // 256
+    uint64_t* bars = (uint64_t*)(sm + qk::BAR);  // [0] loads A, [1] loads B, [2..4] MMA phases
+    uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int t0 = c * kC;
-    const int64_t chunk = ((int64_t)b * d.H + h) * d.NC + c;
-    const int row0 = (int)(chunk * kC);
-    const int krow0 = (int)(chunk * kD);
+    const int sub = warp & 3, half = warp >> 2;
+    const int lanerow = 32 * sub + lane;
+    const bool urow = sub < 2;
+    const int r = urow ? lanerow : lanerow - 64;
+    const int64_t nchunks = d.NS() * d.NC;
 
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bars[0], 18 * 8192);
+    auto decode = [&](int64_t ch, int& b, int& h, int& c) {
+        c = (int)(ch % d.NC);
+        const int64_t bh = ch / d.NC;
+        h = (int)(bh % d.H);
+        b = (int)(bh / d.H);
+    };
+    // group A: W, dU, dO, S0^T, dS1^T (free after phase 2); group B: Q, K (after phase 3)
+    auto load_A = [&](int64_t ch) {
+        int b, h, c;
+        decode(ch, b, h, c);
+        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
+        mbar_arrive_expect_tx(&bars[0], 14 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + qk::Q + j * 8192, &tm_q, &bars[0], 64 * j, h, t0, b);
-            tma_load_4d(sm + qk::K + j * 8192, &tm_k, &bars[0], 64 * j, h, t0, b);
-            tma_load_4d(sm + qk::DO + j * 8192, &tm_do, &bars[0], 64 * j, h, t0, b);
-            tma_load_2d(sm + qk::W + j * 8192, &tm_W, &bars[0], 64 * j, row0);
+            tma_load_2d(sm + qk::WQ + j * 16384, &tm_W, &bars[0], 64 * j, row0);
+            tma_load_4d(sm + qk::DO + j * 8192, &tm_do, &bars[0], 64 * j, h, c * kC, b);
             tma_load_2d(sm + qk::DU + j * 8192, &tm_dU, &bars[0], 64 * j, row0);
             for (int i = 0; i < 2; ++i) {
                 tma_load_2d(sm + qk::S0 + j * 16384 + i * 8192, &tm_S0, &bars[0], 64 * j, krow0 + 64 * i);
                 tma_load_2d(sm + qk::DS1 + j * 16384 + i * 8192, &tm_dS1, &bars[0], 64 * j, krow0 + 64 * i);
             }
         }
+    };
+    auto load_B = [&](int64_t ch) {
+        int b, h, c;
+        decode(ch, b, h, c);
+        mbar_arrive_expect_tx(&bars[1], 4 * 8192);
+        for (int j = 0; j < 2; ++j) {
+            tma_load_4d(sm + qk::WQ + j * 16384 + 8192, &tm_q, &bars[1], 64 * j, h, c * kC, b);
+            tma_load_4d(sm + qk::K + j * 8192, &tm_k, &bars[1], 64 * j, h, c * kC, b);
+        }
+    };
+
+    const int64_t first = blockIdx.x;
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        if (first < nchunks) {
+            load_A(first);
+            load_B(first);
+        }
     }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    if (tid < 64) {
-        Gs[tid] = G[(int64_t)row0 + tid];
-        gs[tid] = expf(Gs[tid]);
-    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
-    const int r = warp * 16 + (lane & 15);
-    const bool rowthr = lane < 16;
-    const float GC = Gs[63], gC = gs[63];
-    const float Gr = Gs[r], gr = gs[r], er = expf(GC - Gr);
-    const uint32_t sQ = smem_u32(sm + qk::Q), sK = smem_u32(sm + qk::K), sDO = smem_u32(sm + qk::DO);
-    const uint32_t sW = smem_u32(sm + qk::W), sDU = smem_u32(sm + qk::DU);
-    const uint32_t sS0 = smem_u32(sm + qk::S0), sDS1 = smem_u32(sm + qk::DS1);
+    const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
+    const uint32_t tXY = tmem, tZ = tmem + 128, tDM = tmem + 256, tQ1 = tmem + 320, tDW = tmem + 384,
+                   tDK = tmem + 448, tQ2 = tmem + 0;
+    const uint32_t sWQ = smem_u32(sm + qk::WQ), sK = smem_u32(sm + qk::K), sDO = smem_u32(sm + qk::DO);
+    const uint32_t sDU = smem_u32(sm + qk::DU), sS0 = smem_u32(sm + qk::S0), sDS1 = smem_u32(sm + qk::DS1);
     const uint32_t sU = smem_u32(sm + qk::U), sEU = smem_u32(sm + qk::EU), sDQK = smem_u32(sm + qk::DQK);
 
     bool ok = true;
-    // ---- phase 1: X = W S0^T, Y = Q S0^T, Z = K dS1^T   (M=64, N=128, K over k)
-    if (tid == 0) {
-        ok = mbar_wait(&bars[0], 0, err, 1);
-        if (ok) {
-            const uint32_t id = idesc_bf16(64, 128, false, true);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                mma_bf16_ss(tmem + 0, desc_kmaj(sW, 64, s), desc_mnmaj(sS0, 128, s), id, s > 0);
-                mma_bf16_ss(tmem + 128, desc_kmaj(sQ, 64, s), desc_mnmaj(sS0, 128, s), id, s > 0);
-                mma_bf16_ss(tmem + 256, desc_kmaj(sK, 64, s), desc_mnmaj(sDS1, 128, s), id, s > 0);
-            }
-            mma_commit(&bars[1]);
-        }
-    }
-    ok = mbar_wait(&bars[0], 0, err, 1) && ok;  // every thread reads the dO tile below
-    ok = mbar_wait(&bars[1], 0, err, 2) && ok;
-    __syncwarp();
-    fence_after_sync();
-    {
-        float eacc = 0.f, gacc = 0.f;
-        const uint4* up = (const uint4*)(Ut + ((int64_t)row0 + r) * kD);
+    int n = 0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-            float x[16], y[16], z[16], u[16], eu[16], dd[8], de[8];
-            tmem_load16f3(tmem + 0 + lanebase + c0, tmem + 128 + lanebase + c0, tmem + 256 + lanebase + c0, x,
-                          y, z);
-            const uint4 ua = up[c0 / 8], ub = up[c0 / 8 + 1];
-            const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+    for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
+        int b, h, c;
+        decode(ch, b, h, c);
+        const int t0 = c * kC;
+        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
+        const int ph = n & 1;
+        if (tid < 64) {
+            Gs[tid] = G[(int64_t)row0 + tid];
+            gs[tid] = expf(Gs[tid]);
+        }
+        // rows of Ut (64 columns) and Mqk (32 columns) this thread needs, fetched early
+        uint4 utv[8], mqv[4];
+        if (urow) {
+            const uint4* up = (const uint4*)(Ut + ((int64_t)row0 + r) * kD + half * 64);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                u[2 * j] = bf_lo(uw[j]) - x[2 * j];
-                u[2 * j + 1] = bf_hi(uw[j]) - x[2 * j + 1];
-            }
+            for (int q = 0; q < 8; ++q) utv[q] = up[q];
+            const uint4* mp = (const uint4*)(Mqk + ((int64_t)row0 + r) * kC + half * 32);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                eu[j] = er * u[j];
-                eacc += u[j] * z[j];
-            }
-            tile_get8(sm + qk::DO, 64, r, c0, dd);
-            tile_get8(sm + qk::DO, 64, r, c0 + 8, de);
+            for (int q = 0; q < 4; ++q) mqv[q] = mp[q];
+        }
+        // ---- phase 1 (K over k): [X; Y] = [W; Q] S0^T, Z = [K; -] dS1^T  (M=128, N=128)
+        if (tid == 0) {
+            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[1], ph, err, 1) && ok;
+            if (ok) {
+                const uint32_t id = idesc_bf16(128, 128, false, true);
+                const uint64_t dwq = sdesc(sWQ, 16, 1024, SW_128B), dk = sdesc(sK, 16, 1024, SW_128B);
+                const uint64_t ds0 = sdesc(sS0, 16384, 1024, SW_128B), dds1 = sdesc(sDS1, 16384, 1024, SW_128B);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) gacc += dd[j] * y[j] + de[j] * y[8 + j];
-            if (rowthr) {
-                tile_put16(sm + qk::U, 64, r, c0, u);
-                tile_put16(sm + qk::EU, 64, r, c0, eu);
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    mma_bf16_ss(tXY, desc_add(dwq, (s2 >> 2) * 16384 + (s2 & 3) * 32), desc_add(ds0, s2 * 2048), id,
+                                s2 > 0);
+                    mma_bf16_ss(tZ, desc_add(dk, (s2 >> 2) * 8192 + (s2 & 3) * 32), desc_add(dds1, s2 * 2048), id,
+                                s2 > 0);
+                }
+                mma_commit(&bars[2]);
             }
         }
-        if (rowthr) {
-            eR[r] = er * eacc;
-            dG1[r] = gr * gacc;
-        }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    // ---- phase 2 (K over v): dMqk = dO U^T (M=64); dQ1^T = S0^T dO^T, dW^T = -S0^T dU^T,
-    //      dK^T = dS1^T (eU)^T (M=128)
-    if (tid == 0 && ok) {
-        const uint32_t id64 = idesc_bf16(64, 64, false, false);
-        const uint32_t id128 = idesc_bf16(128, 64, false, false);
-        const uint32_t id128n = idesc_bf16(128, 64, false, false, true);
+        ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // dO and S0 tiles are read by every thread
+        ok = mbar_wait(&bars[2], ph, err, 2) && ok;
+        __syncthreads();  // Gs / gs
+        fence_after_sync();
+        const float GC = Gs[63], gC = gs[63];
+        const float Gr = Gs[r], er = expf(GC - Gr);
+        {
+            const int cb = half * 64;
+            float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            mma_bf16_ss(tmem + 0, desc_kmaj(sDO, 64, s), desc_kmaj(sU, 64, s), id64, s > 0);
-            mma_bf16_ss(tmem + 64, desc_kmaj(sS0, 128, s), desc_kmaj(sDO, 64, s), id128, s > 0);
-            mma_bf16_ss(tmem + 128, desc_kmaj(sS0, 128, s), desc_kmaj(sDU, 64, s), id128n, s > 0);
-            mma_bf16_ss(tmem + 192, desc_kmaj(sDS1, 128, s), desc_kmaj(sEU, 64, s), id128, s > 0);
+            for (int c0 = cb; c0 < cb + 64; c0 += 16) {
+                if (urow) {
+                    float x[16], z[16], u[16], eu[16];
+                    tmem_load16f2(tXY + lanebase + c0, tZ + lanebase + c0, x, z);
+                    const uint4 ua = utv[(c0 - cb) / 8], ub = utv[(c0 - cb) / 8 + 1];
+                    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        u[2 * j] = bf_lo(uw[j]) - x[2 * j];
+                        u[2 * j + 1] = bf_hi(uw[j]) - x[2 * j + 1];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        eu[j] = er * u[j];
+                        acc += u[j] * z[j];
+                    }
+                    tile_put16(sm + qk::U, 64, r, c0, u);
+                    tile_put16(sm + qk::EU, 64, r, c0, eu);
+                } else {
+                    float y[16], dd[8], de[8];
+                    tmem_load16f(tXY + lanebase + c0, y);
+                    tile_get8(sm + qk::DO, 64, r, c0, dd);
+                    tile_get8(sm + qk::DO, 64, r, c0 + 8, de);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc += dd[j] * y[j] + de[j] * y[8 + j];
+                }
+            }
+            if (urow) eRp[half * 64 + r] = acc;
+            else dG1p[half * 64 + r] = acc;
         }
-        mma_commit(&bars[1]);
-    }
-    {   // <dS1, S0> over the chunk (both tiles share one layout)
-        const uint4* a = (const uint4*)(sm + qk::S0) + tid;
-        const uint4* bq = (const uint4*)(sm + qk::DS1) + tid;
-        float acc = 0.f;
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        // ---- phase 2 (K over v): dMqk = [dO; -] U^T, dQ1^T = S0^T dO^T, dW^T = -S0^T dU^T,
+        //      dK^T = dS1^T (eU)^T   (M=128, N=64)
+        if (tid == 0 && ok) {
+            const uint32_t id = idesc_bf16(128, 64, false, false);
+            const uint32_t idn = idesc_bf16(128, 64, false, false, true);
+            const uint64_t ddo = sdesc(sDO, 16, 1024, SW_128B), du = sdesc(sU, 16, 1024, SW_128B);
+            const uint64_t ds0 = sdesc(sS0, 16, 1024, SW_128B), ddu = sdesc(sDU, 16, 1024, SW_128B);
+            const uint64_t dds1 = sdesc(sDS1, 16, 1024, SW_128B), deu = sdesc(sEU, 16, 1024, SW_128B);
+#pragma unroll
+            for (int s2 = 0; s2 < 8; ++s2) {
+                const uint32_t o64 = (s2 >> 2) * 8192 + (s2 & 3) * 32, o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
+                mma_bf16_ss(tDM, desc_add(ddo, o64), desc_add(du, o64), id, s2 > 0);
+                mma_bf16_ss(tQ1, desc_add(ds0, o128), desc_add(ddo, o64), id, s2 > 0);
+                mma_bf16_ss(tDW, desc_add(ds0, o128), desc_add(ddu, o64), idn, s2 > 0);
+                mma_bf16_ss(tDK, desc_add(dds1, o128), desc_add(deu, o64), id, s2 > 0);
+            }
+            mma_commit(&bars[3]);
+        }
+        {   // <dS1, S0> over the chunk (both tiles share one layout), coalesced
+            const uint4* a = (const uint4*)(sm + qk::S0) + tid;
+            const uint4* bq = (const uint4*)(sm + qk::DS1) + tid;
+            float acc = 0.f;
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-            const uint4 x = a[i * 128], y = bq[i * 128];
-            const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+            for (int i = 0; i < 8; ++i) {
+                const uint4 x = a[i * 256], y = bq[i * 256];
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc += bf_lo(xw[e]) * bf_lo(yw[e]) + bf_hi(xw[e]) * bf_hi(yw[e]);
-        }
-        red[tid] = acc;
-    }
-    if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
-    __syncwarp();
-    fence_after_sync();
-    {
-        const uint4* mp = (const uint4*)(Mqk + ((int64_t)row0 + r) * kC);
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            float dm[16], dq[16];
-            tmem_load16f(tmem + 0 + lanebase + c0, dm);
-            const uint4 ma = mp[c0 / 8], mb = mp[c0 / 8 + 1];
-            const uint32_t mw[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = c0 + j;
-                const float mq = (j & 1) ? bf_hi(mw[j >> 1]) : bf_lo(mw[j >> 1]);
-                if (rowthr) E1f[r * 65 + i] = dm[j] * mq;
-                dq[j] = (i <= r) ? expf(Gr - Gs[i]) * dm[j] : 0.f;
+                for (int e = 0; e < 4; ++e) acc += bf_lo(xw[e]) * bf_lo(yw[e]) + bf_hi(xw[e]) * bf_hi(yw[e]);
             }
-            if (rowthr) tile_put16(sm + qk::DQK, 64, r, c0, dq);
+            red[tid] = acc;
         }
-        // dW^T row k -> scratch
-        uint4* wp = (uint4*)(dWt + ((int64_t)krow0 + tid) * kC);
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        if (ok) ok = mbar_wait(&bars[3], ph, err, 4);
+        __syncwarp();
+        fence_after_sync();
+        // W, dU, dO, S0^T, dS1^T are free: request the next chunk's
+        __syncthreads();  // every thread is past its reads of those tiles
+        if (tid == 0 && ok && ch + gridDim.x < nchunks) load_A(ch + gridDim.x);
+        {
+            if (urow) {  // dMqk row r, columns half*32 .. +32 -> E1 row/column sums, dQK
+                const int cb = half * 32;
+                float e1[32];
+                float rsum = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < 32; c0 += 16) {
+                    float dm[16], dq[16];
+                    tmem_load16f(tDM + lanebase + cb + c0, dm);
+                    const uint4 ma = mqv[c0 / 8], mb = mqv[c0 / 8 + 1];
+                    const uint32_t mw[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = cb + c0 + j;
+                        const float mq = (j & 1) ? bf_hi(mw[j >> 1]) : bf_lo(mw[j >> 1]);
+                        e1[c0 + j] = dm[j] * mq;
+                        rsum += e1[c0 + j];
+                        dq[j] = (i <= r) ? __expf(Gr - Gs[i]) * dm[j] : 0.f;
+                    }
+                    tile_put16(sm + qk::DQK, 64, r, cb + c0, dq);
+                }
+                // row sums (this half of the columns) and column sums (these 32 rows)
+                E1f[half * 64 + r] = rsum;
+                E1f[128 + (sub * 2 + half) * 32 + lane] = warp_colsum32(e1);
+            }
+            // dW^T row k (= lanerow), columns half*32 .. +32 -> scratch
+            const int cb = half * 32;
+            uint4* wp = (uint4*)(dWt + ((int64_t)krow0 + lanerow) * kC + cb);
             float w[16], w2[16];
-            tmem_load16f2(tmem + 128 + lanebase + c0, tmem + 128 + lanebase + c0 + 16, w, w2);
-            wp[c0 / 8] = pack8(w);
-            wp[c0 / 8 + 1] = pack8(w + 8);
-            wp[c0 / 8 + 2] = pack8(w2);
-            wp[c0 / 8 + 3] = pack8(w2 + 8);
+            tmem_load16f2(tDW + lanebase + cb, tDW + lanebase + cb + 16, w, w2);
+            wp[0] = pack8(w);
+            wp[1] = pack8(w + 8);
+            wp[2] = pack8(w2);
+            wp[3] = pack8(w2 + 8);
         }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    // ---- phase 3 (K over tokens): dQ2^T = K^T dQK^T;  dK^T += Q^T dQK
-    if (tid == 0 && ok) {
-        const uint32_t idq = idesc_bf16(128, 64, true, false);
-        const uint32_t idk = idesc_bf16(128, 64, true, true);
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        // ---- phase 3 (K over tokens): dQ2^T = K^T dQK^T;  dK^T += Q^T dQK  (M=128, N=64)
+        if (tid == 0 && ok) {
+            const uint32_t idq = idesc_bf16(128, 64, true, false);
+            const uint32_t idk = idesc_bf16(128, 64, true, true);
+            const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
+            const uint64_t dqm = sdesc(sWQ + 8192, 16384, 1024, SW_128B);  // Q blocks 16 KB apart
+            const uint64_t dqk = sdesc(sDQK, 16, 1024, SW_128B), dqkm = sdesc(sDQK, 8192, 1024, SW_128B);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            mma_bf16_ss(tmem + 256, desc_mnmaj(sK, 64, s), desc_kmaj(sDQK, 64, s), idq, s > 0);
-            mma_bf16_ss(tmem + 192, desc_mnmaj(sQ, 64, s), desc_mnmaj(sDQK, 64, s), idk, 1u);
+            for (int s2 = 0; s2 < 4; ++s2) {
+                mma_bf16_ss(tQ2, desc_add(dkm, s2 * 2048), desc_add(dqk, s2 * 32), idq, s2 > 0);
+                mma_bf16_ss(tDK, desc_add(dqm, s2 * 2048), desc_add(dqkm, s2 * 2048), idk, 1u);
+            }
+            mma_commit(&bars[4]);
         }
-        mma_commit(&bars[1]);
-    }
-    if (tid < 64) {
-        float re = 0.f, ce = 0.f;
-        for (int i = 0; i < 64; ++i) {
-            re += E1f[tid * 65 + i];
-            ce += E1f[i * 65 + tid];
-        }
-        rE1[tid] = re;
-        cE1[tid] = ce;
-    }
-    if (ok) ok = mbar_wait(&bars[1], 0, err, 4);
-    __syncwarp();
-    fence_after_sync();
-    {
-        unsigned char* dqt = sm + qk::S0;  // the S0 tile is dead: dq tile [64 r x 128 k]
-        float* kp = dKp + ((int64_t)krow0 + tid) * kC;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            float q1[16], q2[16], kk[16];
-            tmem_load16f3(tmem + 64 + lanebase + c0, tmem + 256 + lanebase + c0, tmem + 192 + lanebase + c0, q1,
-                          q2, kk);
+        if (tid < 64) {
+            // E1f[0..127]: row sums per column half; E1f[128 + (sub*2+half)*32 + col]:
+            // column sums over rows 32*sub .. +31 of columns half*32 + col
+            rE1[tid] = E1f[tid] + E1f[64 + tid];
+            const int hh = tid >> 5, col = tid & 31;
+            cE1[tid] = E1f[128 + (0 * 2 + hh) * 32 + col] + E1f[128 + (1 * 2 + hh) * 32 + col];
+        } else if (warp == 2) {
+            float ip = 0.f;
+            for (int i = lane; i < 256; i += 32) ip += red[i];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *(bf16*)(dqt + tile_off(64, c0 + j, tid)) = __float2bfloat16_rn(gs[c0 + j] * q1[j] + q2[j]);
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) *(float4*)(kp + c0 + j) = make_float4(kk[j], kk[j + 1], kk[j + 2], kk[j + 3]);
+            for (int off = 16; off > 0; off >>= 1) ip += __shfl_xor_sync(0xffffffffu, ip, off);
+            if (lane == 0) red[0] = ip;  // read after the next barrier
         }
+        if (ok) ok = mbar_wait(&bars[4], ph, err, 8);
+        __syncwarp();
+        fence_after_sync();
+        if (tid == 0) bulk_wait_read0();  // the previous dq store no longer reads the dq tile
+        __syncthreads();                  // Q, K, dQK free; dq tile writable
+        if (tid == 0 && ok && ch + gridDim.x < nchunks) load_B(ch + gridDim.x);
+        {
+            const int cb = half * 32;
+            unsigned char* dqt = sm + qk::DQ;
+            float* kp = dKp + ((int64_t)krow0 + lanerow) * kC + cb;
+#pragma unroll
+            for (int c0 = 0; c0 < 32; c0 += 16) {
+                float q1[16], q2[16], kk[16];
+                tmem_load16f3(tQ1 + lanebase + cb + c0, tQ2 + lanebase + cb + c0, tDK + lanebase + cb + c0, q1,
+                              q2, kk);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    *(bf16*)(dqt + tile_off(64, cb + c0 + j, lanerow)) =
+                        __float2bfloat16_rn(gs[cb + c0 + j] * q1[j] + q2[j]);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *(float4*)(kp + c0 + j) = make_float4(kk[j], kk[j + 1], kk[j + 2], kk[j + 3]);
+            }
+        }
+        if (tid < 64) {
+            const float eR = eRp[tid] + eRp[64 + tid];
+            float g = gs[tid] * (dG1p[tid] + dG1p[64 + tid]) + rE1[tid] - cE1[tid] - expf(GC - Gs[tid]) * eR;
+            if (tid == 63) {
+                float es = 0.f;
+                for (int i = 0; i < 64; ++i) es += expf(GC - Gs[i]) * (eRp[i] + eRp[64 + i]);
+                g += gC * red[0] + es;
+            }
+            dGp[(int64_t)row0 + tid] = g;
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        if (tid == 0 && ok) {
+            for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
+            bulk_commit();
+        }
+        if (!ok) break;
     }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
     if (tid == 0) {
-        float ip = 0.f, es = 0.f;
-        for (int i = 0; i < 128; ++i) ip += red[i];
-        for (int i = 0; i < 64; ++i) es += eR[i];
-        red[0] = ip;
-        red[1] = es;
-    }
-    __syncthreads();
-    if (tid < 64) {
-        float g = dG1[tid] + rE1[tid] - cE1[tid] - eR[tid];
-        if (tid == 63) g += gC * red[0] + red[1];
-        dGp[(int64_t)row0 + tid] = g;
-    }
-    if (tid == 0) {
-        for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dq, sm + qk::S0 + j * 8192, 64 * j, h, t0, b);
-        bulk_commit();
+        if (!ok) {  // prefetches of the next chunk may still be in flight (bounded waits)
+            mbar_wait(&bars[0], (n + 1) & 1, nullptr, 0);
+            mbar_wait(&bars[1], (n + 1) & 1, nullptr, 0);
+        }
         bulk_wait0();
     }
     __syncwarp();
+    fence_before_sync();
+    __syncthreads();
     fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
-
 
 // ====================================================== chunk gradients (2)
 namespace wy {
@@ -962,8 +1067,9 @@ cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(grad_qk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(d.NC, d.H, d.B);
-    grad_qk_tc<<<grid, 128, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, tb.Ut, tb.Mqk, tb.G, bb.dKp,
+    const int64_t nchunks = d.NS() * d.NC;
+    dim3 grid((unsigned)std::min<int64_t>(nchunks, sm_count()));
+    grad_qk_tc<<<grid, 256, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, tb.Ut, tb.Mqk, tb.G, bb.dKp,
                                             bb.dWt, bb.dGp, tb.err);
     return cudaGetLastError();
 }
