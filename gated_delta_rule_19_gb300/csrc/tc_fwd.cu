@@ -59,66 +59,143 @@ __device__ __forceinline__ void warp_cumsum64(float* x) {
     x[2 * lane + 1] = b + excl;
 }
 
-// T = (I + A)^-1 for strictly lower A (64 x 64, row stride 65), fp32.  128 threads.
-// Diagonal 16x16 blocks: warp w solves block w, lane j < 16 carries column j in
-// registers (no synchronisation inside a block).  Then block rows I = 1..3:
-// T_IJ = -T_II * sum_{J<=L<I} A_IL T_LJ.  Only the lower blocks of Tf are written.
+constexpr int kAS = 68;  // fp32 row stride of A and T in shared memory (16-byte aligned rows)
+constexpr int kXS = 36;  // fp32 row stride of the solve's scratch block
+
+// T = (I + A)^-1 for strictly lower A (64 x 64 fp32, rows kAS floats apart), by
+// 256 threads in five steps separated by barriers:
+//   1. the four 16x16 diagonal blocks T_II by forward substitution, one column
+//      per thread (threads 0-63), zeros stored above their diagonals;
+//   2-3. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
+//   4-5. the lower-left 32x32 block -T_bb A_ba T_aa, where T_aa and T_bb are the
+//      two 32x32 diagonal blocks finished by steps 1-3.
+// Entries above the diagonal outside the 16x16 diagonal blocks stay unwritten.
 __device__ void solve_unit_lower_64(const float* A, float* Tf, float* X) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (lane < 16) {
-        const int base = warp * 16, j = lane;
+    if (tid < 64) {
+        const int bo = (tid >> 4) * 16, c = tid & 15;
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
+            const float* ar = A + (bo + r) * kAS + bo;
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < r; ++i) acc += A[(base + r) * 65 + base + i] * t[i];
-            t[r] = (r < j) ? 0.f : (r == j ? 1.f : -acc);
+            for (int i4 = 0; i4 < r; i4 += 4) {
+                const float4 a = *(const float4*)(ar + i4);
+                acc = fmaf(a.x, t[i4], acc);
+                if (i4 + 1 < r) acc = fmaf(a.y, t[i4 + 1], acc);
+                if (i4 + 2 < r) acc = fmaf(a.z, t[i4 + 2], acc);
+                if (i4 + 3 < r) acc = fmaf(a.w, t[i4 + 3], acc);
+            }
+            t[r] = (r == c) ? 1.f : ((r < c) ? 0.f : -acc);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(base + r) * 65 + base + j] = t[r];
+        for (int r = 0; r < 16; ++r) Tf[(bo + r) * kAS + bo + c] = t[r];
     }
     __syncthreads();
-#pragma unroll 1
-    for (int I = 1; I < 4; ++I) {
-        const int n = I * 256;
-        for (int idx = tid; idx < n; idx += 128) {
-            const int J = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-            float acc = 0.f;
-            for (int L = J; L < I; ++L) {
-                const float* ar = A + (I * 16 + r) * 65 + L * 16;
-                const float* tc_ = Tf + (L * 16) * 65 + J * 16 + c;
+    // steps 2-3: warps 0-3 block I = 1, warps 4-7 block I = 3; this warp's 4
+    // columns start at cq, lane -> row r and a column pair
+    const int blk = warp >> 2, I = 1 + 2 * blk, cq = (warp & 3) * 4;
+    const int r16 = lane & 15, cp = cq + 2 * (lane >> 4);
+    {
+        const float* ar = A + (16 * I + r16) * kAS + 16 * (I - 1);
+        const float* tc = Tf + 16 * (I - 1) * kAS + 16 * (I - 1) + cp;
+        float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc += ar[m] * tc_[m * 65];
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+            if (m4 + 3 < cq) continue;  // T_{I-1,I-1}[m][c] = 0 for m < c (warp-uniform)
+            const float4 a = *(const float4*)(ar + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 tv = *(const float2*)(tc + (m4 + e) * kAS);
+                x0 = fmaf(av[e], tv.x, x0);
+                x1 = fmaf(av[e], tv.y, x1);
             }
-            X[idx] = acc;
         }
-        __syncthreads();
-        for (int idx = tid; idx < n; idx += 128) {
-            const int J = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-            const float* tr = Tf + (I * 16 + r) * 65 + I * 16;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m) acc += tr[m] * X[(J << 8) + (m << 4) + c];
-            Tf[(I * 16 + r) * 65 + J * 16 + c] = -acc;
-        }
-        __syncthreads();
+        *(float2*)(X + (16 * blk + r16) * kXS + cp) = make_float2(x0, x1);
     }
+    __syncthreads();
+    {
+        const float* tr = Tf + (16 * I + r16) * kAS + 16 * I;  // zeros above the diagonal
+        const float* xc = X + 16 * blk * kXS + cp;
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+            const float4 a = *(const float4*)(tr + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 xv = *(const float2*)(xc + (m4 + e) * kXS);
+                y0 = fmaf(av[e], xv.x, y0);
+                y1 = fmaf(av[e], xv.y, y1);
+            }
+        }
+        *(float2*)(Tf + (16 * I + r16) * kAS + 16 * (I - 1) + cp) = make_float2(-y0, -y1);
+    }
+    __syncthreads();
+    // steps 4-5: lane -> row r of the lower-left block, warp -> 4 columns c0
+    const int r = lane, c0 = warp * 4;
+    {
+        const float* ar = A + (32 + r) * kAS;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+        for (int m4 = c0; m4 < 32; m4 += 4) {  // T_aa[m][c] = 0 for m < c
+            const float4 a = *(const float4*)(ar + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 tv = *(const float4*)(Tf + (m4 + e) * kAS + c0);
+                x[0] = fmaf(av[e], tv.x, x[0]);
+                x[1] = fmaf(av[e], tv.y, x[1]);
+                x[2] = fmaf(av[e], tv.z, x[2]);
+                x[3] = fmaf(av[e], tv.w, x[3]);
+            }
+        }
+        *(float4*)(X + r * kXS + c0) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+    __syncthreads();
+    {
+        const float* tr = Tf + (32 + r) * kAS + 32;
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+        for (int m4 = 0; m4 <= r; m4 += 4) {  // T_bb[r][m] = 0 for m > r; m4 + 3 stays in r's 16-block
+            const float4 a = *(const float4*)(tr + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 xv = *(const float4*)(X + (m4 + e) * kXS + c0);
+                y[0] = fmaf(av[e], xv.x, y[0]);
+                y[1] = fmaf(av[e], xv.y, y[1]);
+                y[2] = fmaf(av[e], xv.z, y[2]);
+                y[3] = fmaf(av[e], xv.w, y[3]);
+            }
+        }
+        *(float4*)(Tf + (32 + r) * kAS + c0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+    }
+    __syncthreads();
 }
 
-// Shared-memory plan of prep_fwd_tc (offsets from a 1024-aligned base).
-constexpr int P_QK = 0;           // [K_0 | Q_0 | K_1 | Q_1], 8 KB each (64 rows x 64 bf16)
-constexpr int P_V = 32768;        // V_0 | V_1
-constexpr int P_T1 = 49152;       // T diag(beta gamma), bf16 K-major
-constexpr int P_T2 = 57344;       // T diag(beta)
-constexpr int P_AF = 65536;       // fp32 A [64][65]
-constexpr int P_TF = P_AF + 64 * 65 * 4;
-constexpr int P_XF = P_TF + 64 * 65 * 4;
-constexpr int P_G = P_XF + 768 * 4;  // G, gamma, beta: 3 x 64 floats
-constexpr int P_BAR = P_G + 3 * 64 * 4;
+// Shared-memory plan of prep_fwd_tc (offsets from a 1024-aligned base).  The Gram
+// MMA reads [K_0; Q_0] and [K_1; Q_1] as M=128 K-major operands (rows 64-127 of a
+// K-major tile lie 8 KB after rows 0-63); the W / Ut MMA reads K_0, K_1, V_0, V_1
+// as one N=256 MN-major operand (64-wide blocks 16 KB apart).
+constexpr int P_K0 = 0, P_Q0 = 8192, P_K1 = 16384, P_Q1 = 24576;
+constexpr int P_V0 = 32768, P_M = 40960, P_V1 = 49152;  // P_M: the Mqk output tile
+constexpr int P_AF = 57344;                             // fp32 A [64][kAS], dead before T1 / T2 exist
+constexpr int P_T1 = 65536, P_T2 = 73728;               // [T1; T2]: one M=128 K-major operand
+constexpr int P_TF = 81920;                             // fp32 T [64][kAS]
+constexpr int P_X = P_Q0;                               // fp32 [32][kXS] scratch, Q_0 is dead by then
+constexpr int P_VEC = P_TF + 64 * kAS * 4;              // G (log2 units), gamma, beta
+constexpr int P_BAR = P_VEC + 3 * 64 * 4;
 constexpr int P_END = P_BAR + 64;
 constexpr size_t kPrepSmem = P_END + 1024;
+static_assert(P_AF + 64 * kAS * 4 <= P_T2 + 8192, "A overlaps only T1 / T2");
+static_assert(32 * kXS * 4 <= 8192, "solve scratch fits the Q_0 slot");
 
-__global__ void __launch_bounds__(128, 2)
+// One CTA per chunk, 256 threads, two CTAs per SM.  Warps w and w+4 read the same
+// TMEM lane quarter (w % 4) and split its columns.
+__global__ void __launch_bounds__(256, 2)
 prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_W,
             const __grid_constant__ CUtensorMap tm_U, const __grid_constant__ CUtensorMap tm_M,
@@ -128,14 +205,14 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* Af = (float*)(sm + P_AF);
     float* Tf = (float*)(sm + P_TF);
-    float* Xf = (float*)(sm + P_XF);
-    float* Gs = (float*)(sm + P_G);
-    float* gs = Gs + 64;
+    float* G2s = (float*)(sm + P_VEC);  // within-chunk cumsum of log2(alpha)
+    float* gs = G2s + 64;               // gamma = alpha_1 ... alpha_r
     float* bs = gs + 64;
     uint64_t* bars = (uint64_t*)(sm + P_BAR);  // [0] TMA, [1] MMA
     uint32_t* tslot = (uint32_t*)(sm + P_BAR + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sub = warp & 3, half = warp >> 2;
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int t0 = c * kC;
     const int64_t chunk = ((int64_t)b * d.H + h) * d.NC + c;
@@ -147,42 +224,58 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_mbar_init();
         mbar_arrive_expect_tx(&bars[0], 6 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + P_QK + j * 16384, &tm_k, &bars[0], 64 * j, h, t0, b);
-            tma_load_4d(sm + P_QK + j * 16384 + 8192, &tm_q, &bars[0], 64 * j, h, t0, b);
-            tma_load_4d(sm + P_V + j * 8192, &tm_v, &bars[0], 64 * j, h, t0, b);
+            tma_load_4d(sm + P_K0 + j * 16384, &tm_k, &bars[0], 64 * j, h, t0, b);
+            tma_load_4d(sm + P_Q0 + j * 16384, &tm_q, &bars[0], 64 * j, h, t0, b);
+            tma_load_4d(sm + P_V0 + j * 16384, &tm_v, &bars[0], 64 * j, h, t0, b);
         }
     }
-    if (warp == 0) {
-        tmem_alloc(tslot, 128);
+    if (warp == 1) {
+        tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
-    if (tid < 64) {
-        const int t = t0 + tid;
-        float a = 1.f, be = 0.f;  // padding: alpha = 1, beta = 0 leaves the state unchanged
-        if (t < d.T) {
-            const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-            a = __bfloat162float(alpha[gi]);
-            be = __bfloat162float(beta[gi]);
+    if (warp == 2) {
+        // lane -> tokens 2 lane, 2 lane + 1; padding (alpha = 1, beta = 0) leaves the state unchanged
+        float l[2], be[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + 2 * lane + e;
+            float a = 1.f, bb = 0.f;
+            if (t < d.T) {
+                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
+                a = __bfloat162float(alpha[gi]);
+                bb = __bfloat162float(beta[gi]);
+            }
+            l[e] = log2f(a);
+            be[e] = bb;
         }
-        Gs[tid] = logf(a);
-        bs[tid] = be;
+        const float pair = l[0] + l[1];
+        float incl = pair;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const float g0 = incl - pair + l[0], g1 = incl;
+        G2s[2 * lane] = g0;
+        G2s[2 * lane + 1] = g1;
+        gs[2 * lane] = exp2f(g0);
+        gs[2 * lane + 1] = exp2f(g1);
+        bs[2 * lane] = be[0];
+        bs[2 * lane + 1] = be[1];
+        constexpr float kLn2 = 0.693147180559945309f;
+        *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
-    if (warp == 0) {
-        warp_cumsum64(Gs);
-        __syncwarp();
-        gs[2 * lane] = expf(Gs[2 * lane]);
-        gs[2 * lane + 1] = expf(Gs[2 * lane + 1]);
-    }
     bool ok = true;
     if (tid == 0) {
         ok = mbar_wait(&bars[0], 0, err, 1);
         if (ok) {
+            // [K; Q] K^T = [K K^T ; Q K^T] into columns 0-63 (M=128, N=64, K over k)
             const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint32_t base = smem_u32(sm + P_QK);
+            const uint32_t base = smem_u32(sm + P_K0);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t a = base + (s >> 2) * 16384 + (s & 3) * 32;
@@ -191,130 +284,155 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mma_commit(&bars[1]);
         }
     }
-    __syncthreads();  // G, gamma, beta visible
     ok = mbar_wait(&bars[1], 0, err, 2) && ok;
     __syncwarp();
     fence_after_sync();
-    // Gram epilogue.  Warps 0-1: rows of K K^T -> A (fp32).  Warps 2-3: rows of
-    // Q K^T -> Mqk (bf16, into the dead Q_0 slot as a 128B-swizzled tile).
+    // Gram epilogue: lanes 0-63 hold rows of K K^T -> A (fp32), lanes 64-127 rows of
+    // Q K^T -> Mqk (bf16 tile); this warp takes columns cb .. cb+31.
     {
-        const int r = tid & 63;
-        const float Gr = Gs[r];
-        const float br = bs[r];
-        unsigned char* mt = sm + P_QK + 8192;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-            tmem_wait_ld(v);
-            if (warp < 2) {
+        const int rr = 32 * (sub & 1) + lane;
+        const int cb = 32 * half;
+        const bool any = cb <= 32 * (sub & 1) + 31;  // warp-uniform: some column on or below the diagonal
+        const float G2r = G2s[rr];
+        if (sub < 2) {
+            if (any) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + cb, v);
+                tmem_wait_ld(v);
+                const float br = bs[rr];
+                float* arow = Af + rr * kAS + cb;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int i = c0 + j;
-                    Af[r * 65 + i] = (i < r) ? br * expf(Gr - Gs[i]) * __uint_as_float(v[j]) : 0.f;
+                for (int q = 0; q < 8; ++q) {
+                    float f[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = cb + 4 * q + e;
+                        f[e] = (i < rr) ? br * exp2f(G2r - G2s[i]) * __uint_as_float(v[4 * q + e]) : 0.f;
+                    }
+                    *(float4*)(arow + 4 * q) = make_float4(f[0], f[1], f[2], f[3]);
+                }
+            }
+        } else {
+            unsigned char* mt = sm + P_M;
+            if (any) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + cb, v);
+                tmem_wait_ld(v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = cb + 8 * q + 2 * e;
+                        const float m0 = (i <= rr) ? exp2f(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
+                        const float m1 =
+                            (i + 1 <= rr) ? exp2f(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f;
+                        pk[e] = pack_bf16(m0, m1);
+                    }
+                    *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             } else {
-                uint32_t pk[8];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const int i = c0 + j;
-                    const float m0 = (i <= r) ? expf(Gr - Gs[i]) * __uint_as_float(v[j]) : 0.f;
-                    const float m1 = (i + 1 <= r) ? expf(Gr - Gs[i + 1]) * __uint_as_float(v[j + 1]) : 0.f;
-                    pk[j >> 1] = pack_bf16(m0, m1);
-                }
-                *(uint4*)(mt + sw128_off(r, c0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *(uint4*)(mt + sw128_off(r, c0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                for (int q = 0; q < 4; ++q) *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(0u, 0u, 0u, 0u);
             }
-        }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        tma_store_2d(&tm_M, sm + P_QK + 8192, 0, row0);
-        bulk_commit();
-    }
-    solve_unit_lower_64(Af, Tf, Xf);  // ends with __syncthreads
-    // B operands of the recompute: T1 = T diag(beta gamma), T2 = T diag(beta), bf16
-    // K-major [r][i], zero above the diagonal.
-    {
-        const int r = tid >> 1, i0 = (tid & 1) * 32;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t p0[4], p1[4], p2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = i0 + q * 8 + 2 * e;
-                const float ta = (i <= r) ? Tf[r * 65 + i] : 0.f;
-                const float tb = (i + 1 <= r) ? Tf[r * 65 + i + 1] : 0.f;
-                p0[e] = pack_bf16(ta, tb);
-                p1[e] = pack_bf16(ta * bs[i] * gs[i], tb * bs[i + 1] * gs[i + 1]);
-                p2[e] = pack_bf16(ta * bs[i], tb * bs[i + 1]);
-            }
-            if (Tout)
-                *(uint4*)(Tout + ((int64_t)row0 + r) * kC + i0 + q * 8) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            *(uint4*)(sm + P_T1 + sw128_off(r, i0 + q * 8)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-            *(uint4*)(sm + P_T2 + sw128_off(r, i0 + q * 8)) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
         }
     }
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (tid == 0 && ok) {
-        // W^T [k, r] = K^T T1^T and Ut^T [v, r] = V^T T2^T: A read MN-major from the
-        // K / V tiles (64-wide column blocks 16 KB / 8 KB apart), B = T1 / T2.
-        const uint32_t id = idesc_bf16(128, 64, true, false);
-        const uint32_t kb = smem_u32(sm + P_QK), vb = smem_u32(sm + P_V);
-        const uint32_t t1 = smem_u32(sm + P_T1), t2 = smem_u32(sm + P_T2);
+    if (tid == 0) {
+        tma_store_2d(&tm_M, sm + P_M, 0, row0);
+        bulk_commit();
+    }
+    solve_unit_lower_64(Af, Tf, (float*)(sm + P_X));  // ends with __syncthreads
+    // B operands of W / Ut: T1 = T diag(beta gamma), T2 = T diag(beta), bf16 K-major
+    // [r][i], zero above the diagonal; T itself to global memory when asked for.
+    {
+        const int r = tid >> 2, i0 = (tid & 3) * 16;
+        const float* trow = Tf + r * kAS + i0;
+        uint32_t p0[8], p1[8], p2[8];
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            mma_bf16_ss(tmem + 64, sdesc(kb + s * 2048, 16384, 1024, SW_128B),
-                        sdesc(t1 + s * 32, 16, 1024, SW_128B), id, s > 0);
-            mma_bf16_ss(tmem + 0, sdesc(vb + s * 2048, 8192, 1024, SW_128B),
-                        sdesc(t2 + s * 32, 16, 1024, SW_128B), id, s > 0);
+        for (int e4 = 0; e4 < 16; e4 += 4) {
+            const float4 t4 = *(const float4*)(trow + e4);
+            float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (i0 + e4 + e > r) tv[e] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const int i = i0 + e4 + e;
+                const float b0 = bs[i], b1 = bs[i + 1];
+                p0[(e4 + e) >> 1] = pack_bf16(tv[e], tv[e + 1]);
+                p1[(e4 + e) >> 1] = pack_bf16(tv[e] * b0 * gs[i], tv[e + 1] * b1 * gs[i + 1]);
+                p2[(e4 + e) >> 1] = pack_bf16(tv[e] * b0, tv[e + 1] * b1);
+            }
         }
+        if (Tout) {
+            uint4* tg = (uint4*)(Tout + ((int64_t)row0 + r) * kC + i0);
+            tg[0] = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+            tg[1] = make_uint4(p0[4], p0[5], p0[6], p0[7]);
+        }
+        *(uint4*)(sm + P_T1 + sw128_off(r, i0)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+        *(uint4*)(sm + P_T1 + sw128_off(r, i0 + 8)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
+        *(uint4*)(sm + P_T2 + sw128_off(r, i0)) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+        *(uint4*)(sm + P_T2 + sw128_off(r, i0 + 8)) = make_uint4(p2[4], p2[5], p2[6], p2[7]);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    if (tid == 0 && ok) {
+        // [T1; T2] [K | V] (M=128, N=256, K over tokens): rows 0-63 of columns 0-127
+        // are W = T1 K, rows 64-127 of columns 128-255 are Ut = T2 V.
+        const uint32_t id = idesc_bf16(128, 256, false, true);
+        const uint64_t da = sdesc(smem_u32(sm + P_T1), 16, 1024, SW_128B);
+        const uint64_t db = sdesc(smem_u32(sm + P_K0), 16384, 1024, SW_128B);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) mma_bf16_ss(tmem, desc_add(da, s * 32), desc_add(db, s * 2048), id, s > 0);
         mma_commit(&bars[1]);
     }
-    ok = __syncthreads_and(ok);
     if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
     __syncwarp();
     fence_after_sync();
-    // Epilogue: thread k holds row k of W^T / Ut^T -> write W[r][k], Ut[r][v] into
-    // the K / V tile slots (dead now) as 128B-swizzled K-major tiles.
+    // Epilogue: row rr of W (lanes 0-63) or Ut (lanes 64-127), 64 columns per warp,
+    // into the dead Q (W) and K (Ut) slots as 128B-swizzled K-major tiles.
     {
-        const int k = tid;
-        unsigned char* wt = sm + P_QK + (k >> 6) * 16384;
-        unsigned char* ut = sm + P_V + (k >> 6) * 8192;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            uint32_t w[16], u[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 64 + c0, w);
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, u);
-            tmem_wait_ld(w);
-            tmem_wait_ld(u);
+        const int rr = 32 * (sub & 1) + lane;
+        const bool isw = sub < 2;
+        unsigned char* dst = sm + (isw ? (half ? P_Q1 : P_Q0) : (half ? P_K1 : P_K0));
+        const uint32_t taddr = tmem + ((uint32_t)(32 * sub) << 16) + (isw ? 0 : 128) + 64 * half;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                *(bf16*)(wt + sw128_off(c0 + j, k & 63)) = __float2bfloat16_rn(__uint_as_float(w[j]));
-                *(bf16*)(ut + sw128_off(c0 + j, k & 63)) = __float2bfloat16_rn(__uint_as_float(u[j]));
+        for (int g = 0; g < 2; ++g) {
+            uint32_t v[32];
+            tmem_ld32(taddr + 32 * g, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pk[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]), __uint_as_float(v[8 * q + 2 * e + 1]));
+                *(uint4*)(dst + sw128_off(rr, 32 * g + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
     }
-    if (tid < 64) Gout[(int64_t)row0 + tid] = Gs[tid];
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
     if (tid == 0) {
-        for (int j = 0; j < 2; ++j) {
-            tma_store_2d(&tm_W, sm + P_QK + j * 16384, 64 * j, row0);
-            tma_store_2d(&tm_U, sm + P_V + j * 8192, 64 * j, row0);
+        if (ok) {
+            tma_store_2d(&tm_W, sm + P_Q0, 0, row0);
+            tma_store_2d(&tm_W, sm + P_Q1, 64, row0);
+            tma_store_2d(&tm_U, sm + P_K0, 0, row0);
+            tma_store_2d(&tm_U, sm + P_K1, 64, row0);
+            bulk_commit();
         }
-        bulk_commit();
         bulk_wait0();
     }
     __syncwarp();
     fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -699,7 +817,7 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(prep_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(d.NC, d.H, d.B);
-    prep_fwd_tc<<<grid, 128, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
+    prep_fwd_tc<<<grid, 256, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
                                               tb.G, tb.T, tb.err);
     return cudaGetLastError();
 }
