@@ -355,8 +355,8 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 namespace qk {
 constexpr int WQ = 0;                  // [W_0 | Q_0 | W_1 | Q_1]: stacked [W;Q] and Q (MN-major)
 constexpr int K = 32768;               // [K_0 | K_1]
-constexpr int DO = 49152;              // [dO_0 | dO_1]
-constexpr int DU = 65536;              // [64 x 128]
+constexpr int DO = 49152;              // [dO_0 | dU_0 | dO_1 | dU_1]: stacked [dO; dU] (N=128)
+constexpr int DU = DO + 8192;
 constexpr int S0 = 81920, DS1 = 114688;  // [128 x 128]
 constexpr int U = 147456, EU = 163840;   // [64 x 128]
 constexpr int DQK = 180224;              // [64 x 64]
@@ -411,8 +411,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_arrive_expect_tx(&bars[0], 14 * 8192);
         for (int j = 0; j < 2; ++j) {
             tma_load_2d(sm + qk::WQ + j * 16384, &tm_W, &bars[0], 64 * j, row0);
-            tma_load_4d(sm + qk::DO + j * 8192, &tm_do, &bars[0], 64 * j, h, c * kC, b);
-            tma_load_2d(sm + qk::DU + j * 8192, &tm_dU, &bars[0], 64 * j, row0);
+            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[0], 64 * j, h, c * kC, b);
+            tma_load_2d(sm + qk::DU + j * 16384, &tm_dU, &bars[0], 64 * j, row0);
             for (int i = 0; i < 2; ++i) {
                 tma_load_2d(sm + qk::S0 + j * 16384 + i * 8192, &tm_S0, &bars[0], 64 * j, krow0 + 64 * i);
                 tma_load_2d(sm + qk::DS1 + j * 16384 + i * 8192, &tm_dS1, &bars[0], 64 * j, krow0 + 64 * i);
@@ -430,6 +430,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     };
 
     const int64_t first = blockIdx.x;
+    // warp 3 keeps the next chunk's G (2 tokens per lane) in registers
+    float2 gnext = make_float2(0.f, 0.f);
+    if (warp == 3 && first < nchunks) gnext = *(const float2*)(G + first * kC + 2 * lane);
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -447,10 +450,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
-    const uint32_t tXY = tmem, tZ = tmem + 128, tDM = tmem + 256, tQ1 = tmem + 320, tDW = tmem + 384,
+    // tQW: columns 0-63 S0^T dO^T (dQ1^T), 64-127 S0^T dU^T (-dW^T)
+    const uint32_t tXY = tmem, tZ = tmem + 128, tDM = tmem + 256, tQW = tmem + 320, tQ1 = tQW, tDW = tQW + 64,
                    tDK = tmem + 448, tQ2 = tmem + 0;
     const uint32_t sWQ = smem_u32(sm + qk::WQ), sK = smem_u32(sm + qk::K), sDO = smem_u32(sm + qk::DO);
-    const uint32_t sDU = smem_u32(sm + qk::DU), sS0 = smem_u32(sm + qk::S0), sDS1 = smem_u32(sm + qk::DS1);
+    const uint32_t sS0 = smem_u32(sm + qk::S0), sDS1 = smem_u32(sm + qk::DS1);
     const uint32_t sU = smem_u32(sm + qk::U), sEU = smem_u32(sm + qk::EU), sDQK = smem_u32(sm + qk::DQK);
 
     bool ok = true;
@@ -462,9 +466,12 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int t0 = c * kC;
         const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
         const int ph = n & 1;
-        if (tid < 64) {
-            Gs[tid] = G[(int64_t)row0 + tid];
-            gs[tid] = expf(Gs[tid]);
+        if (warp == 3) {
+            Gs[2 * lane] = gnext.x;
+            Gs[2 * lane + 1] = gnext.y;
+            gs[2 * lane] = expf(gnext.x);
+            gs[2 * lane + 1] = expf(gnext.y);
+            if (ch + gridDim.x < nchunks) gnext = *(const float2*)(G + (ch + gridDim.x) * kC + 2 * lane);
         }
         // rows of Ut (64 columns) and Mqk (32 columns) this thread needs, fetched early
         uint4 utv[8], mqv[4];
@@ -525,8 +532,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 } else {
                     float y[16], dd[8], de[8];
                     tmem_load16f(tXY + lanebase + c0, y);
-                    tile_get8(sm + qk::DO, 64, r, c0, dd);
-                    tile_get8(sm + qk::DO, 64, r, c0 + 8, de);
+                    const unsigned char* dob = sm + qk::DO + (c0 >> 6) * 16384;
+                    tile_get8(dob, 64, r, c0 & 63, dd);
+                    tile_get8(dob, 64, r, (c0 & 63) + 8, de);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) acc += dd[j] * y[j] + de[j] * y[8 + j];
                 }
@@ -538,20 +546,19 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        // ---- phase 2 (K over v): dMqk = [dO; -] U^T, dQ1^T = S0^T dO^T, dW^T = -S0^T dU^T,
-        //      dK^T = dS1^T (eU)^T   (M=128, N=64)
+        // ---- phase 2 (K over v): dMqk = [dO; -] U^T (N=64), S0^T [dO; dU]^T (N=128),
+        //      dK^T = dS1^T (eU)^T (N=64)   (M=128)
         if (tid == 0 && ok) {
             const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint32_t idn = idesc_bf16(128, 64, false, false, true);
+            const uint32_t id128 = idesc_bf16(128, 128, false, false);
             const uint64_t ddo = sdesc(sDO, 16, 1024, SW_128B), du = sdesc(sU, 16, 1024, SW_128B);
-            const uint64_t ds0 = sdesc(sS0, 16, 1024, SW_128B), ddu = sdesc(sDU, 16, 1024, SW_128B);
+            const uint64_t ds0 = sdesc(sS0, 16, 1024, SW_128B);
             const uint64_t dds1 = sdesc(sDS1, 16, 1024, SW_128B), deu = sdesc(sEU, 16, 1024, SW_128B);
 #pragma unroll
             for (int s2 = 0; s2 < 8; ++s2) {
                 const uint32_t o64 = (s2 >> 2) * 8192 + (s2 & 3) * 32, o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-                mma_bf16_ss(tDM, desc_add(ddo, o64), desc_add(du, o64), id, s2 > 0);
-                mma_bf16_ss(tQ1, desc_add(ds0, o128), desc_add(ddo, o64), id, s2 > 0);
-                mma_bf16_ss(tDW, desc_add(ds0, o128), desc_add(ddu, o64), idn, s2 > 0);
+                mma_bf16_ss(tDM, desc_add(ddo, o128), desc_add(du, o64), id, s2 > 0);
+                mma_bf16_ss(tQW, desc_add(ds0, o128), desc_add(ddo, o128), id128, s2 > 0);
                 mma_bf16_ss(tDK, desc_add(dds1, o128), desc_add(deu, o64), id, s2 > 0);
             }
             mma_commit(&bars[3]);
@@ -605,6 +612,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint4* wp = (uint4*)(dWt + ((int64_t)krow0 + lanerow) * kC + cb);
             float w[16], w2[16];
             tmem_load16f2(tDW + lanebase + cb, tDW + lanebase + cb + 16, w, w2);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                w[j] = -w[j];
+                w2[j] = -w2[j];
+            }
             wp[0] = pack8(w);
             wp[1] = pack8(w + 8);
             wp[2] = pack8(w2);
@@ -637,9 +649,19 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         } else if (warp == 2) {
             float ip = 0.f;
             for (int i = lane; i < 256; i += 32) ip += red[i];
+            // sum_i exp(G_C - G_i) eR_i over the chunk's 64 tokens
+            float es = expf(GC - Gs[lane]) * (eRp[lane] + eRp[64 + lane]) +
+                       expf(GC - Gs[32 + lane]) * (eRp[32 + lane] + eRp[96 + lane]);
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ip += __shfl_xor_sync(0xffffffffu, ip, off);
-            if (lane == 0) red[0] = ip;  // read after the next barrier
+            for (int off = 16; off > 0; off >>= 1) {
+                ip += __shfl_xor_sync(0xffffffffu, ip, off);
+                es += __shfl_xor_sync(0xffffffffu, es, off);
+            }
+            __syncwarp();
+            if (lane == 0) {  // read after the next barrier
+                red[0] = ip;
+                red[1] = es;
+            }
         }
         if (ok) ok = mbar_wait(&bars[4], ph, err, 8);
         __syncwarp();
@@ -668,11 +690,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (tid < 64) {
             const float eR = eRp[tid] + eRp[64 + tid];
             float g = gs[tid] * (dG1p[tid] + dG1p[64 + tid]) + rE1[tid] - cE1[tid] - expf(GC - Gs[tid]) * eR;
-            if (tid == 63) {
-                float es = 0.f;
-                for (int i = 0; i < 64; ++i) es += expf(GC - Gs[i]) * (eRp[i] + eRp[64 + i]);
-                g += gC * red[0] + es;
-            }
+            if (tid == 63) g += gC * red[0] + red[1];
             dGp[(int64_t)row0 + tid] = g;
         }
         fence_proxy_async();
@@ -768,7 +786,29 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         tma_load_2d(st + wy::OFF_T, &tm_T, bar, 0, row0);
     };
 
+    // warp 3 keeps the next chunk's gates, G and dG partials (2 tokens per lane) in
+    // registers, raw, so that the loads complete while the current chunk runs
+    bf16 na[2], nb[2];
+    float2 ng = make_float2(0.f, 0.f), nq = make_float2(0.f, 0.f);
+    auto fetch_vec = [&](int64_t ch2) {
+        int b2, h2, c2;
+        decode(ch2, b2, h2, c2);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = c2 * kC + 2 * lane + e;
+            na[e] = __float2bfloat16_rn(1.f);
+            nb[e] = __float2bfloat16_rn(0.f);
+            if (t < d.T) {
+                const int64_t gi = ((int64_t)b2 * d.T + t) * d.H + h2;
+                na[e] = alpha[gi];
+                nb[e] = beta[gi];
+            }
+        }
+        ng = *(const float2*)(G + ch2 * kC + 2 * lane);
+        nq = *(const float2*)(dGp + ch2 * kC + 2 * lane);
+    };
     const int64_t first = blockIdx.x;
+    if (warp == 3 && first < nchunks) fetch_vec(first);
     if (tid == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -802,19 +842,18 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const uint32_t sDU = smem_u32(st + wy::OFF_DU), sDWT = smem_u32(st + wy::OFF_DWT);
         const uint32_t sT = smem_u32(st + wy::OFF_T);
         if (tid == 0 && ch + gridDim.x < nchunks) load_stage(ch + gridDim.x, stg ^ 1);
-        if (tid < 64) {
-            const int t = t0 + tid;
-            float a = 1.f, be = 0.f;
-            if (t < d.T) {
-                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-                a = __bfloat162float(alpha[gi]);
-                be = __bfloat162float(beta[gi]);
+        if (warp == 3) {
+            const float gv[2] = {ng.x, ng.y}, qv[2] = {nq.x, nq.y};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int p = 2 * lane + e;
+                Gs[p] = gv[e];
+                gs[p] = expf(gv[e]);
+                bs[p] = __bfloat162float(nb[e]);
+                as_[p] = __bfloat162float(na[e]);
+                dGq[p] = qv[e];
             }
-            Gs[tid] = G[(int64_t)row0 + tid];
-            gs[tid] = expf(Gs[tid]);
-            bs[tid] = be;
-            as_[tid] = a;
-            dGq[tid] = dGp[(int64_t)row0 + tid];
+            if (ch + gridDim.x < nchunks) fetch_vec(ch + gridDim.x);
         }
         // dK^T partial (row k = lanerow, this thread's 32 columns), fetched early
         float4 kpv[8];
