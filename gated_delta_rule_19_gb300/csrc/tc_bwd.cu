@@ -107,6 +107,23 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
     return v[0];
 }
 
+// Column sums of a 32 x 16 block held one row per lane: on return lanes l and l+16
+// hold the sum over the 32 rows of column l % 16.  15 + 1 shuffles.
+__device__ __forceinline__ float warp_colsum16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool upper = lane & w;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float send = upper ? v[j] : v[j + w];
+            const float keep = upper ? v[j + w] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
 // ============================================================ reverse scan
 template <int Vt>
 struct BScan {
@@ -719,22 +736,22 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 // ====================================================== chunk gradients (2)
 namespace wy {
-// input stage (double-buffered): K | V | dU ([64 x 128] each) | dW^T [128 x 64] | T [64 x 64]
-constexpr int OFF_K = 0, OFF_V = 16384, OFF_DU = 32768, OFF_DWT = 49152, OFF_T = 65536;
-constexpr int STAGE = 73728;
-constexpr int T1 = 2 * STAGE, T2 = T1 + 8192, DT = T2 + 8192, Y = DT + 8192, E = Y + 8192;  // [64 x 64]
-constexpr int DV = E + 8192, DK = DV + 16384;  // output tiles [64 x 128]
-constexpr int VEC = DK + 16384;                // per-token and partial-sum vectors
+// inputs: K | V | dU ([64 x 128] each) | dW^T [128 x 64] | T [64 x 64]
+constexpr int K = 0, V = 16384, DU = 32768, DWT = 49152, T = 65536;
+constexpr int T1 = 73728, T2 = 81920, DT = 90112, Y = 98304;  // [64 x 64]
+constexpr int E = DT;                  // dT is dead once Y is formed
+constexpr int DV = V, DK = K;          // outputs [64 x 128] into dead input slots
+constexpr int VEC = Y + 8192;          // per-token and partial-sum vectors
 constexpr int NVEC = 15 * 64;
 constexpr int BAR = VEC + NVEC * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
+static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 }  // namespace wy
 
-// Persistent: CTA i handles chunks i, i + gridDim.x, ...  256 threads; rows of the
-// M=64 products land in TMEM lanes 0-63 (threads with warp % 4 < 2), warps w and
-// w+4 split columns.  The next chunk's inputs load into the other stage while
-// this chunk runs.
-__global__ void __launch_bounds__(256, 1)
+// One CTA per chunk, 256 threads, two CTAs per SM (each one's epilogues overlap
+// the other's MMAs and loads).  Rows of the M=64 products land in TMEM lanes 0-63
+// (threads with warp % 4 < 2); warps w and w+4 split columns.
+__global__ void __launch_bounds__(256, 2)
 grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_dWt, const __grid_constant__ CUtensorMap tm_dU,
            const __grid_constant__ CUtensorMap tm_T, const __grid_constant__ CUtensorMap tm_dk,
@@ -751,358 +768,310 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     float* dGq = vec + 256;
     float* cB12 = vec + 320;    // [2 row groups][64]
     float* cGw = vec + 448;     // [2][64]
-    float* dB3p = vec + 576;    // [2 halves][64]
+    float* dB3p = vec + 576;    // [2 column halves][64]
     float* rE2p = vec + 704;    // [2][64]
     float* cE2 = vec + 832;     // [2][64]
-    uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0..1] loads per stage, [2..5] MMA phases
-    uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 56);
+    uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0] loads, [1] MMA
+    uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = warp & 3, half = warp >> 2;
     const int lanerow = 32 * sub + lane;
     const bool urow = sub < 2;
     const int r = urow ? lanerow : lanerow - 64;  // row of the M=64 results (urow threads)
-    const int64_t nchunks = d.NS() * d.NC;
+    const int cb = half * 32;                     // this warp's 32 columns of a 64-column result
+    const int64_t ch = blockIdx.x;
+    const int c = (int)(ch % d.NC);
+    const int h = (int)((ch / d.NC) % d.H);
+    const int b = (int)(ch / d.NC / d.H);
+    const int t0 = c * kC;
+    const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
 
-    auto decode = [&](int64_t ch, int& b, int& h, int& c) {
-        c = (int)(ch % d.NC);
-        const int64_t bh = ch / d.NC;
-        h = (int)(bh % d.H);
-        b = (int)(bh / d.H);
-    };
-    auto load_stage = [&](int64_t ch, int stg) {
-        int b, h, c;
-        decode(ch, b, h, c);
-        unsigned char* st = sm + stg * wy::STAGE;
-        uint64_t* bar = &bars[stg];
-        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
-        mbar_arrive_expect_tx(bar, 9 * 8192);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bars[0], 9 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(st + wy::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, c * kC, b);
-            tma_load_4d(st + wy::OFF_V + j * 8192, &tm_v, bar, 64 * j, h, c * kC, b);
-            tma_load_2d(st + wy::OFF_DU + j * 8192, &tm_dU, bar, 64 * j, row0);
-            tma_load_2d(st + wy::OFF_DWT + j * 8192, &tm_dWt, bar, 0, krow0 + 64 * j);
+            tma_load_4d(sm + wy::K + j * 8192, &tm_k, &bars[0], 64 * j, h, t0, b);
+            tma_load_4d(sm + wy::V + j * 8192, &tm_v, &bars[0], 64 * j, h, t0, b);
+            tma_load_2d(sm + wy::DU + j * 8192, &tm_dU, &bars[0], 64 * j, row0);
+            tma_load_2d(sm + wy::DWT + j * 8192, &tm_dWt, &bars[0], 0, krow0 + 64 * j);
         }
-        tma_load_2d(st + wy::OFF_T, &tm_T, bar, 0, row0);
-    };
-
-    // warp 3 keeps the next chunk's gates, G and dG partials (2 tokens per lane) in
-    // registers, raw, so that the loads complete while the current chunk runs
-    bf16 na[2], nb[2];
-    float2 ng = make_float2(0.f, 0.f), nq = make_float2(0.f, 0.f);
-    auto fetch_vec = [&](int64_t ch2) {
-        int b2, h2, c2;
-        decode(ch2, b2, h2, c2);
+        tma_load_2d(sm + wy::T, &tm_T, &bars[0], 0, row0);
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
+    if (warp == 3) {
+        const float2 gv = *(const float2*)(G + (int64_t)row0 + 2 * lane);
+        const float2 qv = *(const float2*)(dGp + (int64_t)row0 + 2 * lane);
+        const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int t = c2 * kC + 2 * lane + e;
-            na[e] = __float2bfloat16_rn(1.f);
-            nb[e] = __float2bfloat16_rn(0.f);
+            const int p = 2 * lane + e, t = t0 + p;
+            float a = 1.f, be = 0.f;  // padding: alpha = 1, beta = 0
             if (t < d.T) {
-                const int64_t gi = ((int64_t)b2 * d.T + t) * d.H + h2;
-                na[e] = alpha[gi];
-                nb[e] = beta[gi];
+                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
+                a = __bfloat162float(alpha[gi]);
+                be = __bfloat162float(beta[gi]);
             }
+            Gs[p] = g2[e];
+            gs[p] = expf(g2[e]);
+            bs[p] = be;
+            as_[p] = a;
+            dGq[p] = q2[e];
         }
-        ng = *(const float2*)(G + ch2 * kC + 2 * lane);
-        nq = *(const float2*)(dGp + ch2 * kC + 2 * lane);
-    };
-    const int64_t first = blockIdx.x;
-    if (warp == 3 && first < nchunks) fetch_vec(first);
-    if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-        if (first < nchunks) load_stage(first, 0);
-    }
-    if (warp == 0) {
-        tmem_alloc(tslot, 512);
-        tmem_relinquish();
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
-    const uint32_t tQm = tmem, tP = tmem + 64, tKK = tmem + 128, tY = tmem + 192, tDA = tmem + 0, tDV = tmem + 256,
-                   tDK = tmem + 320;
+    // TMEM columns: Qm, P, KK, Y; later dA over Qm, dV^T over P, dK^T over Y
+    const uint32_t tQm = tmem, tP = tmem + 64, tKK = tmem + 128, tY = tmem + 192;
+    const uint32_t tDA = tQm, tDV = tP, tDK = tY;
+    const uint32_t sK = smem_u32(sm + wy::K), sV = smem_u32(sm + wy::V), sDU = smem_u32(sm + wy::DU);
+    const uint32_t sDWT = smem_u32(sm + wy::DWT), sT = smem_u32(sm + wy::T);
     const uint32_t sT1 = smem_u32(sm + wy::T1), sT2 = smem_u32(sm + wy::T2), sDT = smem_u32(sm + wy::DT);
     const uint32_t sY = smem_u32(sm + wy::Y), sE = smem_u32(sm + wy::E);
 
-    bool ok = true;
-    int n = 0;
-#pragma unroll 1
-    for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
-        int b, h, c;
-        decode(ch, b, h, c);
-        const int t0 = c * kC;
-        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
-        const int stg = n & 1, sph = (n >> 1) & 1, ph = n & 1;  // stage parity, MMA parity
-        unsigned char* st = sm + stg * wy::STAGE;
-        const uint32_t sK = smem_u32(st + wy::OFF_K), sV = smem_u32(st + wy::OFF_V);
-        const uint32_t sDU = smem_u32(st + wy::OFF_DU), sDWT = smem_u32(st + wy::OFF_DWT);
-        const uint32_t sT = smem_u32(st + wy::OFF_T);
-        if (tid == 0 && ch + gridDim.x < nchunks) load_stage(ch + gridDim.x, stg ^ 1);
-        if (warp == 3) {
-            const float gv[2] = {ng.x, ng.y}, qv[2] = {nq.x, nq.y};
+    bool ok = mbar_wait(&bars[0], 0, err, 1);
+    // ---- phase 1: Qm = dW K^T (K over k), P = dU V^T (K over v), KK = K K^T   (M=128: rows 64-127 unused)
+    if (tid == 0 && ok) {
+        const uint32_t idq = idesc_bf16(128, 64, true, false);
+        const uint32_t id = idesc_bf16(128, 64, false, false);
+        const uint64_t ddw = sdesc(sDWT, 16384, 1024, SW_128B);
+        const uint64_t dk = sdesc(sK, 16, 1024, SW_128B), du = sdesc(sDU, 16, 1024, SW_128B);
+        const uint64_t dv = sdesc(sV, 16, 1024, SW_128B);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int p = 2 * lane + e;
-                Gs[p] = gv[e];
-                gs[p] = expf(gv[e]);
-                bs[p] = __bfloat162float(nb[e]);
-                as_[p] = __bfloat162float(na[e]);
-                dGq[p] = qv[e];
+        for (int s2 = 0; s2 < 8; ++s2) {
+            const uint32_t o = (s2 >> 2) * 8192 + (s2 & 3) * 32;
+            mma_bf16_ss(tQm, desc_add(ddw, s2 * 2048), desc_add(dk, o), idq, s2 > 0);
+            mma_bf16_ss(tP, desc_add(du, o), desc_add(dv, o), id, s2 > 0);
+            mma_bf16_ss(tKK, desc_add(dk, o), desc_add(dk, o), id, s2 > 0);
+        }
+        mma_commit(&bars[1]);
+    }
+    if (!urow) {
+        // T1 = T diag(beta gamma), T2 = T diag(beta): rows r, this half of the columns
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float f[8], f1[8], f2[8];
+            tile_get8(sm + wy::T, 64, r, cb + 8 * q, f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int cc = cb + 8 * q + j;
+                f2[j] = f[j] * bs[cc];
+                f1[j] = f2[j] * gs[cc];
             }
-            if (ch + gridDim.x < nchunks) fetch_vec(ch + gridDim.x);
+            *(uint4*)(sm + wy::T1 + tile_off(64, r, cb + 8 * q)) = pack8(f1);
+            *(uint4*)(sm + wy::T2 + tile_off(64, r, cb + 8 * q)) = pack8(f2);
         }
-        // dK^T partial (row k = lanerow, this thread's 32 columns), fetched early
-        float4 kpv[8];
-        {
-            const float4* kp = (const float4*)(dKp + ((int64_t)krow0 + lanerow) * kC + half * 32);
+    }
+    ok = mbar_wait(&bars[1], 0, err, 2) && ok;
+    __syncwarp();
+    fence_after_sync();
+    if (urow) {
+        // rows s = r: column sums of T (P + Qm diag(gamma)) and T Qm over this warp's 32
+        // rows; dT (strictly lower) for the Y product
 #pragma unroll
-            for (int q = 0; q < 8; ++q) kpv[q] = kp[q];
-        }
-        ok = mbar_wait(&bars[stg], sph, err, 1) && ok;
-        // ---- phase 1: Qm = dW K^T (K over k), P = dU V^T (K over v), KK = K K^T   (M=128: rows 64-127 unused)
-        if (tid == 0 && ok) {
-            const uint32_t idq = idesc_bf16(128, 64, true, false);
-            const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint64_t ddw = sdesc(sDWT, 16384, 1024, SW_128B);
-            const uint64_t dk = sdesc(sK, 16, 1024, SW_128B), du = sdesc(sDU, 16, 1024, SW_128B);
-            const uint64_t dv = sdesc(sV, 16, 1024, SW_128B);
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+            float qm[16], p[16], t8a[8], t8b[8], dt[16], c1[16], c2[16];
+            tmem_load16f2(tQm + lanebase + cb + c0, tP + lanebase + cb + c0, qm, p);
+            tile_get8(sm + wy::T, 64, r, cb + c0, t8a);
+            tile_get8(sm + wy::T, 64, r, cb + c0 + 8, t8b);
 #pragma unroll
-            for (int s2 = 0; s2 < 8; ++s2) {
-                const uint32_t o = (s2 >> 2) * 8192 + (s2 & 3) * 32;
-                mma_bf16_ss(tQm, desc_add(ddw, s2 * 2048), desc_add(dk, o), idq, s2 > 0);
-                mma_bf16_ss(tP, desc_add(du, o), desc_add(dv, o), id, s2 > 0);
-                mma_bf16_ss(tKK, desc_add(dk, o), desc_add(dk, o), id, s2 > 0);
+            for (int j = 0; j < 16; ++j) {
+                const int rc = cb + c0 + j;
+                const float tsr = j < 8 ? t8a[j] : t8b[j - 8];
+                const float pv = p[j] + gs[rc] * qm[j];
+                c1[j] = tsr * pv;
+                c2[j] = tsr * qm[j];
+                dt[j] = (rc < r) ? bs[rc] * pv : 0.f;
             }
-            mma_commit(&bars[2]);
-        }
-        __syncthreads();  // per-token vectors
-        if (!urow) {
-            // T1 = T diag(beta gamma), T2 = T diag(beta): rows r, this half of the columns
-            const int cb = half * 32;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float f[8], f1[8], f2[8];
-                tile_get8(st + wy::OFF_T, 64, r, cb + 8 * q, f);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int cc = cb + 8 * q + j;
-                    f2[j] = f[j] * bs[cc];
-                    f1[j] = f2[j] * gs[cc];
-                }
-                *(uint4*)(sm + wy::T1 + tile_off(64, r, cb + 8 * q)) = pack8(f1);
-                *(uint4*)(sm + wy::T2 + tile_off(64, r, cb + 8 * q)) = pack8(f2);
+            tile_put16(sm + wy::DT, 64, r, cb + c0, dt);
+            const float s1 = warp_colsum16(c1), s2 = warp_colsum16(c2);
+            if (lane < 16) {
+                cB12[sub * 64 + cb + c0 + lane] = s1;
+                cGw[sub * 64 + cb + c0 + lane] = s2;
             }
         }
-        ok = mbar_wait(&bars[2], ph, err, 2) && ok;
-        __syncwarp();
-        fence_after_sync();
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    // ---- phase 2: Y = dT T^T  (M=128, K over tokens)
+    if (tid == 0 && ok) {
+        const uint32_t id = idesc_bf16(128, 64, false, false);
+        const uint64_t ddt = sdesc(sDT, 16, 1024, SW_128B), dt = sdesc(sT, 16, 1024, SW_128B);
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) mma_bf16_ss(tY, desc_add(ddt, s2 * 32), desc_add(dt, s2 * 32), id, s2 > 0);
+        mma_commit(&bars[1]);
+    }
+    if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
+    __syncwarp();
+    fence_after_sync();
+    if (urow) {
+        float y[16], y2[16];
+        tmem_load16f2(tY + lanebase + cb, tY + lanebase + cb + 16, y, y2);
+        tile_put16(sm + wy::Y, 64, r, cb, y);
+        tile_put16(sm + wy::Y, 64, r, cb + 16, y2);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    // ---- phase 3: dA = -T^T Y (M=128, rows 64-127 unused), dV^T = dU^T T2 (M=128)
+    if (tid == 0 && ok) {
+        const uint32_t ida = idesc_bf16(128, 64, true, true, true);
+        const uint32_t idv = idesc_bf16(128, 64, true, true);
+        const uint64_t dtm = sdesc(sT, 8192, 1024, SW_128B), dym = sdesc(sY, 8192, 1024, SW_128B);
+        const uint64_t dum = sdesc(sDU, 8192, 1024, SW_128B), dt2m = sdesc(sT2, 8192, 1024, SW_128B);
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+            mma_bf16_ss(tDA, desc_add(dtm, s2 * 2048), desc_add(dym, s2 * 2048), ida, s2 > 0);
+            mma_bf16_ss(tDV, desc_add(dum, s2 * 2048), desc_add(dt2m, s2 * 2048), idv, s2 > 0);
+        }
+        mma_commit(&bars[1]);
+    }
+    if (ok) ok = mbar_wait(&bars[1], 0, err, 8);
+    __syncwarp();
+    fence_after_sync();
+    {
         if (urow) {
-            // rows s = r: column sums of T (P + Qm diag(gamma)) and T Qm over this warp's 32
-            // rows; dT (strictly lower) for the Y product
-            const int cb = half * 32;
-            float c1[32], c2[32];
+            // rows a = r: dbeta3, E = beta_a Gam .* dA (strictly lower) -> E tile, E2 = E .* KK
+            const float Ga = Gs[r], ba = bs[r];
+            float b3 = 0.f, re2 = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < 32; c0 += 16) {
-                float qm[16], p[16], t8a[8], t8b[8], dt[16];
-                tmem_load16f2(tQm + lanebase + cb + c0, tP + lanebase + cb + c0, qm, p);
-                tile_get8(st + wy::OFF_T, 64, r, cb + c0, t8a);
-                tile_get8(st + wy::OFF_T, 64, r, cb + c0 + 8, t8b);
+                float da[16], kk[16], ev[16], e2[16];
+                tmem_load16f2(tDA + lanebase + cb + c0, tKK + lanebase + cb + c0, da, kk);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int rc = cb + c0 + j;
-                    const float tsr = j < 8 ? t8a[j] : t8b[j - 8];
-                    const float pv = p[j] + gs[rc] * qm[j];
-                    c1[c0 + j] = tsr * pv;
-                    c2[c0 + j] = tsr * qm[j];
-                    dt[j] = (rc < r) ? bs[rc] * pv : 0.f;
+                    const int bc = cb + c0 + j;
+                    const float gam = (bc < r) ? expf(Ga - Gs[bc]) : 0.f;
+                    const float m = gam * da[j];
+                    b3 += m * kk[j];
+                    ev[j] = ba * m;
+                    e2[j] = ev[j] * kk[j];
+                    re2 += e2[j];
                 }
-                tile_put16(sm + wy::DT, 64, r, cb + c0, dt);
+                tile_put16(sm + wy::E, 64, r, cb + c0, ev);
+                const float s3 = warp_colsum16(e2);
+                if (lane < 16) cE2[sub * 64 + cb + c0 + lane] = s3;
             }
-            cB12[sub * 64 + cb + lane] = warp_colsum32(c1);
-            cGw[sub * 64 + cb + lane] = warp_colsum32(c2);
+            dB3p[half * 64 + r] = b3;
+            rE2p[half * 64 + r] = re2;
         }
-        fence_proxy_async();
-        fence_before_sync();
-        ok = __syncthreads_and(ok);
-        fence_after_sync();
-        // ---- phase 2: Y = dT T^T  (M=128, K over tokens)
-        if (tid == 0 && ok) {
-            const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint64_t ddt = sdesc(sDT, 16, 1024, SW_128B), dt = sdesc(sT, 16, 1024, SW_128B);
+        // dV^T row v = lanerow, columns cb .. +32 -> dv tile (rows r, column v) in the V slot
+        unsigned char* dvt = sm + wy::DV;
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) mma_bf16_ss(tY, desc_add(ddt, s2 * 32), desc_add(dt, s2 * 32), id, s2 > 0);
-            mma_commit(&bars[3]);
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+            float x[16];
+            tmem_load16f(tDV + lanebase + cb + c0, x);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *(bf16*)(dvt + tile_off(64, cb + c0 + j, lanerow)) = __float2bfloat16_rn(x[j]);
         }
-        if (ok) ok = mbar_wait(&bars[3], ph, err, 4);
-        __syncwarp();
-        fence_after_sync();
-        if (urow) {
-            const int cb = half * 32;
-            float y[16], y2[16];
-            tmem_load16f2(tY + lanebase + cb, tY + lanebase + cb + 16, y, y2);
-            tile_put16(sm + wy::Y, 64, r, cb, y);
-            tile_put16(sm + wy::Y, 64, r, cb + 16, y2);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    // ---- phase 4: dK^T = dW^T T1 + K^T E + K^T E^T   (M=128, K over tokens)
+    if (tid == 0 && ok) {
+        for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
+        bulk_commit();
+        const uint32_t id1 = idesc_bf16(128, 64, false, true);
+        const uint32_t id2 = idesc_bf16(128, 64, true, true);
+        const uint32_t id3 = idesc_bf16(128, 64, true, false);
+        const uint64_t ddw = sdesc(sDWT, 16, 1024, SW_128B), dt1m = sdesc(sT1, 8192, 1024, SW_128B);
+        const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
+        const uint64_t dem = sdesc(sE, 8192, 1024, SW_128B), dek = sdesc(sE, 16, 1024, SW_128B);
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+            mma_bf16_ss(tDK, desc_add(ddw, s2 * 32), desc_add(dt1m, s2 * 2048), id1, s2 > 0);
+            mma_bf16_ss(tDK, desc_add(dkm, s2 * 2048), desc_add(dem, s2 * 2048), id2, 1u);
+            mma_bf16_ss(tDK, desc_add(dkm, s2 * 2048), desc_add(dek, s2 * 32), id3, 1u);
         }
-        fence_proxy_async();
-        fence_before_sync();
-        ok = __syncthreads_and(ok);
-        fence_after_sync();
-        // ---- phase 3: dA = -T^T Y (M=128, rows 64-127 unused), dV^T = dU^T T2 (M=128)
-        if (tid == 0 && ok) {
-            const uint32_t ida = idesc_bf16(128, 64, true, true, true);
-            const uint32_t idv = idesc_bf16(128, 64, true, true);
-            const uint64_t dtm = sdesc(sT, 8192, 1024, SW_128B), dym = sdesc(sY, 8192, 1024, SW_128B);
-            const uint64_t dum = sdesc(sDU, 8192, 1024, SW_128B), dt2m = sdesc(sT2, 8192, 1024, SW_128B);
+        mma_commit(&bars[1]);
+    }
+    if (warp == 3) {
+        // dG, dlog alpha = reverse within-chunk cumsum (lane l holds positions 63-2l and
+        // 62-2l), dalpha = dlog alpha / alpha, dbeta = dbeta12 + dbeta3
+        auto dg = [&](int p) {
+            return dGq[p] + bs[p] * gs[p] * (cGw[p] + cGw[64 + p]) + (rE2p[p] + rE2p[64 + p]) -
+                   (cE2[p] + cE2[64 + p]);
+        };
+        const int p1 = 63 - 2 * lane, p0 = 62 - 2 * lane;
+        const float g1 = dg(p1), g0 = dg(p0);
+        const float pair = g1 + g0;
+        float incl = pair;
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                mma_bf16_ss(tDA, desc_add(dtm, s2 * 2048), desc_add(dym, s2 * 2048), ida, s2 > 0);
-                mma_bf16_ss(tDV, desc_add(dum, s2 * 2048), desc_add(dt2m, s2 * 2048), idv, s2 > 0);
-            }
-            mma_commit(&bars[4]);
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
         }
-        if (ok) ok = mbar_wait(&bars[4], ph, err, 8);
-        __syncwarp();
-        fence_after_sync();
-        if (tid == 0) bulk_wait_read0();  // previous dv / dk stores no longer read their tiles
-        __syncthreads();
-        {
-            const int cb = half * 32;
-            if (urow) {
-                // rows a = r: dbeta3, E = beta_a Gam .* dA (strictly lower) -> E tile, E2 = E .* KK
-                const float Ga = Gs[r], ba = bs[r];
-                float b3 = 0.f, re2 = 0.f, e2[32];
+        const float run1 = incl - pair + g1, run0 = run1 + g0;
+        const int pos[2] = {p1, p0};
+        const float run[2] = {run1, run0};
 #pragma unroll
-                for (int c0 = 0; c0 < 32; c0 += 16) {
-                    float da[16], kk[16], ev[16];
-                    tmem_load16f2(tDA + lanebase + cb + c0, tKK + lanebase + cb + c0, da, kk);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int bc = cb + c0 + j;
-                        const float gam = (bc < r) ? expf(Ga - Gs[bc]) : 0.f;
-                        const float m = gam * da[j];
-                        b3 += m * kk[j];
-                        ev[j] = ba * m;
-                        e2[c0 + j] = ev[j] * kk[j];
-                        re2 += e2[c0 + j];
-                    }
-                    tile_put16(sm + wy::E, 64, r, cb + c0, ev);
-                }
-                dB3p[half * 64 + r] = b3;
-                rE2p[half * 64 + r] = re2;
-                cE2[sub * 64 + cb + lane] = warp_colsum32(e2);
-            }
-            // dV^T row v = lanerow, columns cb .. +32 -> dv tile (rows r, column v)
-            unsigned char* dvt = sm + wy::DV;
-#pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
-                float x[16];
-                tmem_load16f(tDV + lanebase + cb + c0, x);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *(bf16*)(dvt + tile_off(64, cb + c0 + j, lanerow)) = __float2bfloat16_rn(x[j]);
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + pos[e];
+            if (t < d.T) {
+                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
+                const int p = pos[e];
+                dalpha[gi] = __float2bfloat16_rn(run[e] / as_[p]);
+                dbeta[gi] = __float2bfloat16_rn(cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p]);
             }
         }
-        fence_proxy_async();
-        fence_before_sync();
-        ok = __syncthreads_and(ok);
-        fence_after_sync();
-        // ---- phase 4: dK^T = dW^T T1 + K^T E + K^T E^T   (M=128, K over tokens)
-        if (tid == 0 && ok) {
-            for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
-            bulk_commit();
-            const uint32_t id1 = idesc_bf16(128, 64, false, true);
-            const uint32_t id2 = idesc_bf16(128, 64, true, true);
-            const uint32_t id3 = idesc_bf16(128, 64, true, false);
-            const uint64_t ddw = sdesc(sDWT, 16, 1024, SW_128B), dt1m = sdesc(sT1, 8192, 1024, SW_128B);
-            const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
-            const uint64_t dem = sdesc(sE, 8192, 1024, SW_128B), dek = sdesc(sE, 16, 1024, SW_128B);
+    }
+    // dK^T partial from the first gradient kernel (row k = lanerow, this thread's 32 columns)
+    float4 kpv[8];
+    {
+        const float4* kp = (const float4*)(dKp + ((int64_t)krow0 + lanerow) * kC + cb);
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                mma_bf16_ss(tDK, desc_add(ddw, s2 * 32), desc_add(dt1m, s2 * 2048), id1, s2 > 0);
-                mma_bf16_ss(tDK, desc_add(dkm, s2 * 2048), desc_add(dem, s2 * 2048), id2, 1u);
-                mma_bf16_ss(tDK, desc_add(dkm, s2 * 2048), desc_add(dek, s2 * 32), id3, 1u);
+        for (int q = 0; q < 8; ++q) kpv[q] = kp[q];
+    }
+    if (ok) ok = mbar_wait(&bars[1], 1, err, 16);
+    __syncwarp();
+    fence_after_sync();
+    {
+        unsigned char* out = sm + wy::DK;  // K is dead once the last MMA has completed
+#pragma unroll
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+            float x[16];
+            tmem_load16f(tDK + lanebase + cb + c0, x);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 pk = kpv[(c0 + j) / 4];
+                x[j] += pk.x;
+                x[j + 1] += pk.y;
+                x[j + 2] += pk.z;
+                x[j + 3] += pk.w;
             }
-            mma_commit(&bars[5]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *(bf16*)(out + tile_off(64, cb + c0 + j, lanerow)) = __float2bfloat16_rn(x[j]);
         }
-        if (warp == 1) {
-            // dG, dlog alpha = reverse within-chunk cumsum (lane l holds positions 63-2l and
-            // 62-2l), dalpha = dlog alpha / alpha, dbeta = dbeta12 + dbeta3
-            auto dg = [&](int p) {
-                return dGq[p] + bs[p] * gs[p] * (cGw[p] + cGw[64 + p]) + (rE2p[p] + rE2p[64 + p]) -
-                       (cE2[p] + cE2[64 + p]);
-            };
-            const int p1 = 63 - 2 * lane, p0 = 62 - 2 * lane;
-            const float g1 = dg(p1), g0 = dg(p0);
-            const float pair = g1 + g0;
-            float incl = pair;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += y;
-            }
-            const float run1 = incl - pair + g1, run0 = run1 + g0;
-            const int pos[2] = {p1, p0};
-            const float run[2] = {run1, run0};
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = t0 + pos[e];
-                if (t < d.T) {
-                    const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-                    const int p = pos[e];
-                    dalpha[gi] = __float2bfloat16_rn(run[e] / as_[p]);
-                    dbeta[gi] = __float2bfloat16_rn(cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p]);
-                }
-            }
-        }
-        if (ok) ok = mbar_wait(&bars[5], ph, err, 16);
-        __syncwarp();
-        fence_after_sync();
-        {
-            const int cb = half * 32;
-            unsigned char* out = sm + wy::DK;
-#pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
-                float x[16];
-                tmem_load16f(tDK + lanebase + cb + c0, x);
-#pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 pk = kpv[(c0 + j) / 4];
-                    x[j] += pk.x;
-                    x[j + 1] += pk.y;
-                    x[j + 2] += pk.z;
-                    x[j + 3] += pk.w;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *(bf16*)(out + tile_off(64, cb + c0 + j, lanerow)) = __float2bfloat16_rn(x[j]);
-            }
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        ok = __syncthreads_and(ok);
-        fence_after_sync();
-        if (tid == 0 && ok) {
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(ok);
+    fence_after_sync();
+    if (tid == 0) {
+        if (ok) {
             for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
-        }
-        if (!ok) break;
-    }
-    if (tid == 0) {
-        if (!ok) {  // loads of this chunk and the next may still be in flight (bounded waits)
-            mbar_wait(&bars[n & 1], (n >> 1) & 1, nullptr, 0);
-            mbar_wait(&bars[(n + 1) & 1], ((n + 1) >> 1) & 1, nullptr, 0);
         }
         bulk_wait0();
     }
     __syncwarp();
-    fence_before_sync();
-    __syncthreads();
     fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 template <int Vt>
@@ -1168,8 +1137,7 @@ cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(grad_wy_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wy::SMEM);
     if (e != cudaSuccess) return e;
-    const int64_t nchunks = d.NS() * d.NC;
-    dim3 grid((unsigned)std::min<int64_t>(nchunks, sm_count()));
+    dim3 grid((unsigned)(d.NS() * d.NC));
     grad_wy_tc<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, (const bf16*)alpha,
                                             (const bf16*)beta, tb.G, bb.dKp, bb.dGp, (bf16*)dalpha, (bf16*)dbeta,
                                             tb.err);
