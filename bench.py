@@ -250,6 +250,29 @@ def kernel_work(name, w):
     return table.get(name, (0, 0))
 
 
+def path_roofline(w, peaks, ms, fwd_ms):
+    """The whole path against its algorithmic bound: per token*head the forward
+    does 2C(3K+2V)+6KV flops and moves 2(2K+2V)+4 bytes at bf16 (es(2K+2V)+2es in
+    general); the backward 14KV+10CV+18CK+4C^2 flops and es(4K+3V)+4es bytes (reads
+    q,k,v,dO,alpha,beta; writes dq,dk,dv,dalpha,dbeta).  The bound time is the larger
+    of flops / sustained bf16 peak and bytes / HBM copy bandwidth."""
+    C, K, V = w.chunk, w.K, w.V
+    es = 2 if w.dtype == "bf16" else 4
+    f_fwd = 2 * C * (3 * K + 2 * V) + 6 * K * V
+    f_bwd = 14 * K * V + 10 * C * V + 18 * C * K + 4 * C * C
+    b_fwd = es * (2 * K + 2 * V) + 2 * es
+    b_bwd = es * (4 * K + 3 * V) + 4 * es
+    n = w.token_heads
+    def bound_ms(f, b):
+        return 1e3 * max(f * n / (peaks["bf16_tflops_sustained"] * 1e12), b * n / (peaks["hbm_gbs"] * 1e9))
+    step_ms = bound_ms(f_fwd + f_bwd, b_fwd + b_bwd)
+    fwd_bound = bound_ms(f_fwd, b_fwd)
+    return {"bound_ms": step_ms, "frac": step_ms / ms, "fwd_bound_ms": fwd_bound,
+            "fwd_frac": fwd_bound / fwd_ms if fwd_ms else None,
+            "tc_peak_frac": (f_fwd + f_bwd) * n / (ms / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12),
+            "per_token_head": {"fwd_flops": f_fwd, "bwd_flops": f_bwd, "fwd_bytes": b_fwd, "bwd_bytes": b_bwd}}
+
+
 def traffic_for(name):
     """Per-launch DRAM bytes of a kernel from the committed ncu summary, if
     that summary was taken on the current kernel sources; else None."""
@@ -458,6 +481,7 @@ def run_gdn(args, world, rank, local):
         "fwd": {"value": world * w.token_heads / (fwd_ms / 1e3), "unit": UNIT,
                 "ms_per_step": fwd_ms},
         "roofline": rl,
+        "path_roofline": path_roofline(w, peaks, ms_max, fwd_ms),
         "kernels": [{k: r[k] for k in ("kernel", "launches", "avg_ms", "share", "bound",
                                        "achieved", "unit", "frac")} for r in rows],
         "cpu_baseline": cpu,
