@@ -125,7 +125,7 @@ size_t carve_tc_bwd(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, gdn::TcBwdB
     const size_t rows = nchunks * d.C;
     bb->dU = cv.take<__nv_bfloat16>(rows * d.V);
     bb->dS1 = cv.take<__nv_bfloat16>(nchunks * d.K * d.V);
-    bb->dKp = cv.take<float>(nchunks * d.K * d.C);
+    bb->dKp = cv.take<__nv_bfloat16>(nchunks * d.K * d.C);
     bb->dWt = cv.take<__nv_bfloat16>(nchunks * d.K * d.C);
     bb->dGp = cv.take<float>(rows);
     bb->states = need_states ? cv.take<__nv_bfloat16>(nchunks * d.K * d.V) : nullptr;

@@ -67,14 +67,14 @@ struct TcBufs {
 // Backward buffers of the tensor-core path:
 //   dU   [rows, V] bf16            gradient of the corrected writes U
 //   dS1  [chunks * K, V] bf16      gradient of each chunk's end state, transposed
-//   dKp  [chunks * K, 64] fp32     dK^T from the Mqk and state-update terms
+//   dKp  [chunks * K, 64] bf16     dK^T from the Mqk and state-update terms
 //   dWt  [chunks * K, 64] bf16     dW^T
 //   dGp  [rows] fp32               dG from the output, Mqk and state-update terms
 //   states [chunks * K, V] bf16    chunk-start states when no saved buffer is given
 struct TcBwdBufs {
     __nv_bfloat16* dU;
     __nv_bfloat16* dS1;
-    float* dKp;
+    __nv_bfloat16* dKp;
     __nv_bfloat16* dWt;
     float* dGp;
     __nv_bfloat16* states;

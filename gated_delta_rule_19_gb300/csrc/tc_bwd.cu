@@ -393,7 +393,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
            const __grid_constant__ CUtensorMap tm_dU, const __grid_constant__ CUtensorMap tm_S0,
            const __grid_constant__ CUtensorMap tm_dS1, const __grid_constant__ CUtensorMap tm_dq,
            const bf16* __restrict__ Ut, const bf16* __restrict__ Mqk, const float* __restrict__ G,
-           float* __restrict__ dKp, bf16* __restrict__ dWt, float* __restrict__ dGp, int* err) {
+           bf16* __restrict__ dKp, bf16* __restrict__ dWt, float* __restrict__ dGp, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* E1f = (float*)(sm + qk::E1);
@@ -689,7 +689,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         {
             const int cb = half * 32;
             unsigned char* dqt = sm + qk::DQ;
-            float* kp = dKp + ((int64_t)krow0 + lanerow) * kC + cb;
+            uint4* kp = (uint4*)(dKp + ((int64_t)krow0 + lanerow) * kC + cb);
 #pragma unroll
             for (int c0 = 0; c0 < 32; c0 += 16) {
                 float q1[16], q2[16], kk[16];
@@ -699,9 +699,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int j = 0; j < 16; ++j)
                     *(bf16*)(dqt + tile_off(64, cb + c0 + j, lanerow)) =
                         __float2bfloat16_rn(gs[cb + c0 + j] * q1[j] + q2[j]);
-#pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *(float4*)(kp + c0 + j) = make_float4(kk[j], kk[j + 1], kk[j + 2], kk[j + 3]);
+                kp[c0 / 8] = pack8(kk);
+                kp[c0 / 8 + 1] = pack8(kk + 8);
             }
         }
         if (tid < 64) {
@@ -756,7 +755,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
            const __grid_constant__ CUtensorMap tm_dWt, const __grid_constant__ CUtensorMap tm_dU,
            const __grid_constant__ CUtensorMap tm_T, const __grid_constant__ CUtensorMap tm_dk,
            const __grid_constant__ CUtensorMap tm_dv, const bf16* __restrict__ alpha,
-           const bf16* __restrict__ beta, const float* __restrict__ G, const float* __restrict__ dKp,
+           const bf16* __restrict__ beta, const float* __restrict__ G, const bf16* __restrict__ dKp,
            const float* __restrict__ dGp, bf16* __restrict__ dalpha, bf16* __restrict__ dbeta, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -1030,11 +1029,11 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
     }
     // dK^T partial from the first gradient kernel (row k = lanerow, this thread's 32 columns)
-    float4 kpv[8];
+    uint4 kpv[4];
     {
-        const float4* kp = (const float4*)(dKp + ((int64_t)krow0 + lanerow) * kC + cb);
+        const uint4* kp = (const uint4*)(dKp + ((int64_t)krow0 + lanerow) * kC + cb);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) kpv[q] = kp[q];
+        for (int q = 0; q < 4; ++q) kpv[q] = kp[q];
     }
     if (ok) ok = mbar_wait(&bars[1], 1, err, 16);
     __syncwarp();
@@ -1046,12 +1045,14 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             float x[16];
             tmem_load16f(tDK + lanebase + cb + c0, x);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                const float4 pk = kpv[(c0 + j) / 4];
-                x[j] += pk.x;
-                x[j + 1] += pk.y;
-                x[j + 2] += pk.z;
-                x[j + 3] += pk.w;
+            for (int q = 0; q < 2; ++q) {
+                const uint4 pk = kpv[c0 / 8 + q];
+                const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[8 * q + 2 * e] += bf_lo(pw[e]);
+                    x[8 * q + 2 * e + 1] += bf_hi(pw[e]);
+                }
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j)

@@ -43,22 +43,6 @@ constexpr int kD = 128;  // K = V = 128
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-// In-place inclusive prefix sum of x[0..64) by one warp.
-__device__ __forceinline__ void warp_cumsum64(float* x) {
-    const int lane = threadIdx.x & 31;
-    float a = x[2 * lane], b = x[2 * lane + 1];
-    b += a;
-    float incl = b;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        float y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const float excl = incl - b;
-    x[2 * lane] = a + excl;
-    x[2 * lane + 1] = b + excl;
-}
-
 constexpr int kAS = 68;  // fp32 row stride of A and T in shared memory (16-byte aligned rows)
 constexpr int kXS = 36;  // fp32 row stride of the solve's scratch block
 
@@ -181,7 +165,7 @@ __device__ void solve_unit_lower_64(const float* A, float* Tf, float* X) {
 // K-major tile lie 8 KB after rows 0-63); the W / Ut MMA reads K_0, K_1, V_0, V_1
 // as one N=256 MN-major operand (64-wide blocks 16 KB apart).
 constexpr int P_K0 = 0, P_Q0 = 8192, P_K1 = 16384, P_Q1 = 24576;
-constexpr int P_V0 = 32768, P_M = 40960, P_V1 = 49152;  // P_M: the Mqk output tile
+constexpr int P_V0 = 32768, P_M = 40960;  // V_1 at P_V0 + 16384; P_M: the Mqk output tile
 constexpr int P_AF = 57344;                             // fp32 A [64][kAS], dead before T1 / T2 exist
 constexpr int P_T1 = 65536, P_T2 = 73728;               // [T1; T2]: one M=128 K-major operand
 constexpr int P_TF = 81920;                             // fp32 T [64][kAS]
