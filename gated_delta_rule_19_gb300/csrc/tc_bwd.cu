@@ -359,7 +359,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (issuer) {
         if (!ok)
             for (int i2 = it; i2 < NC && i2 < it + 2; ++i2) mbar_wait(&tbar[i2 & 1], (i2 >> 1) & 1, nullptr, 0);
-        bulk_wait0();
+        bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
     fence_before_sync();
@@ -724,7 +724,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_wait(&bars[0], (n + 1) & 1, nullptr, 0);
             mbar_wait(&bars[1], (n + 1) & 1, nullptr, 0);
         }
-        bulk_wait0();
+        bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
     fence_before_sync();
@@ -1068,7 +1068,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
         }
-        bulk_wait0();
+        bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
     fence_after_sync();

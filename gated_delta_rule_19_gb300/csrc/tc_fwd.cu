@@ -217,37 +217,21 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
+    // warp 2: gates of tokens 2 lane, 2 lane + 1, loaded now and used once the Gram MMA
+    // is issued; padding (alpha = 1, beta = 0) leaves the state unchanged
+    bf16 ga[2], gb[2];
     if (warp == 2) {
-        // lane -> tokens 2 lane, 2 lane + 1; padding (alpha = 1, beta = 0) leaves the state unchanged
-        float l[2], be[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * lane + e;
-            float a = 1.f, bb = 0.f;
+            ga[e] = __float2bfloat16_rn(1.f);
+            gb[e] = __float2bfloat16_rn(0.f);
             if (t < d.T) {
                 const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-                a = __bfloat162float(alpha[gi]);
-                bb = __bfloat162float(beta[gi]);
+                ga[e] = alpha[gi];
+                gb[e] = beta[gi];
             }
-            l[e] = log2f(a);
-            be[e] = bb;
         }
-        const float pair = l[0] + l[1];
-        float incl = pair;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        const float g0 = incl - pair + l[0], g1 = incl;
-        G2s[2 * lane] = g0;
-        G2s[2 * lane + 1] = g1;
-        gs[2 * lane] = exp2f(g0);
-        gs[2 * lane + 1] = exp2f(g1);
-        bs[2 * lane] = be[0];
-        bs[2 * lane + 1] = be[1];
-        constexpr float kLn2 = 0.693147180559945309f;
-        *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
     }
     fence_before_sync();
     __syncthreads();
@@ -268,6 +252,26 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mma_commit(&bars[1]);
         }
     }
+    if (warp == 2) {
+        const float l[2] = {log2f(__bfloat162float(ga[0])), log2f(__bfloat162float(ga[1]))};
+        const float pair = l[0] + l[1];
+        float incl = pair;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const float g0 = incl - pair + l[0], g1 = incl;
+        G2s[2 * lane] = g0;
+        G2s[2 * lane + 1] = g1;
+        gs[2 * lane] = exp2f(g0);
+        gs[2 * lane + 1] = exp2f(g1);
+        bs[2 * lane] = __bfloat162float(gb[0]);
+        bs[2 * lane + 1] = __bfloat162float(gb[1]);
+        constexpr float kLn2 = 0.693147180559945309f;
+        *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
+    }
+    __syncthreads();  // gates visible
     ok = mbar_wait(&bars[1], 0, err, 2) && ok;
     __syncwarp();
     fence_after_sync();
@@ -412,7 +416,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tma_store_2d(&tm_U, sm + P_K1, 64, row0);
             bulk_commit();
         }
-        bulk_wait0();
+        bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
     fence_after_sync();
@@ -744,7 +748,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int cc = c; cc < NC && cc < c + 2; ++cc) mbar_wait(&tbar[cc & 1], (cc >> 1) & 1, nullptr, 0);
             mbar_wait(barO, (c > 0 ? c - 1 : 0) & 1, nullptr, 0);
         }
-        bulk_wait0();
+        bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
     fence_before_sync();
