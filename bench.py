@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     return ap.parse_args()
 
 
@@ -329,6 +330,49 @@ def roofline(summary, w, peaks):
 
 # ------------------------------------------------------------------ GPU arm
 
+def measure_decode(gdn, dev, stream, args, world):
+    """Times gdn_decode on the decode workload (256 sequences x 16 heads, one
+    token, K=V=128 bf16): its 256 MB fp32 state is read and written once per
+    call, so the call is bound by that traffic; achieved bandwidth is taken
+    against the measured HBM copy rate.  Before timing, one call is checked
+    against the chunked forward (gdn_fwd) on the same token; the oracle checks
+    the decode step in the tests."""
+    from gated_delta_rule_19_gb300.inputs import DECODE_WORKLOADS
+
+    w = DECODE_WORKLOADS["decode_bf16_B256_T1_H16_K128_V128"]
+    inp = make_inputs(w)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
+    args_in = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
+    state = d["initial_state"].clone()
+    o = torch.empty_like(d["v"])
+    gdn.gdn_decode(*args_in, state, o=o)
+    of, sf, _ = gdn.gdn_fwd(*args_in, d["initial_state"], chunk=w.chunk)
+    torch.cuda.synchronize(dev)
+    rel = lambda a, b: float((a.float() - b.float()).norm() / b.float().norm())
+    consistency = {"o": rel(o, of), "state": rel(state, sf)}
+    del of, sf
+    for _ in range(max(3, args.warmup)):
+        gdn.gdn_decode(*args_in, state, o=o)
+    n = max(20, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n):
+        gdn.gdn_decode(*args_in, state, o=o)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+    BH = w.B * w.H
+    byts = BH * w.V * w.K * 4 * 2 + BH * w.T * (2 * w.K + 2 * w.V + 2) * 2
+    peaks = load_peaks()
+    return {"workload": w.name, "us_per_call": ms * 1e3,
+            "token_heads_per_s": world * BH * w.T / (ms / 1e3),
+            "bytes_per_call": byts, "achieved_GBs": byts / (ms / 1e3) / 1e9,
+            "frac_of_hbm": byts / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "l2": "state 256 MB > L2 (no flush)", "rel_l2_vs_gdn_fwd": consistency}
+
+
 def run_gdn(args, world, rank, local):
     from gated_delta_rule_19_gb300 import _build, gdn
 
@@ -509,6 +553,10 @@ def run_gdn(args, world, rank, local):
                "pipeline": "uploads and downloads on two copy streams overlap adjacent steps' compute",
                "results_match_resident_run": ok_e2e}
 
+    # ---- the decode step (a survey "next" row): one token per call, the state
+    # carried in place between calls
+    decode = None if args.no_decode else measure_decode(gdn, dev, stream, args, world)
+
     if rank != 0:
         return
     peaks = load_peaks()
@@ -536,6 +584,7 @@ def run_gdn(args, world, rank, local):
         "cpu_baseline": cpu,
         "parity_sampled": parity,
         "e2e": e2e,
+        "decode": decode,
         "gpu_launches": launches,
         "clocks": clk,
     }

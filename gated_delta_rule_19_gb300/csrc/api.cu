@@ -32,8 +32,9 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool supported_dim(int64_t x) { return x == 16 || x == 32 || x == 64 || x == 128; }
 
-// Checks the problem and fills Dims.  Returns GDN_OK or an error status.
-gdn_status check_problem(const gdn_problem* p, gdn::Dims* d) {
+// Checks the problem and fills Dims.  Returns GDN_OK or an error status.  With
+// need_chunk false the chunk field is not used (gdn_decode) and is not checked.
+gdn_status check_problem(const gdn_problem* p, gdn::Dims* d, bool need_chunk = true) {
     if (!p) return fail(GDN_ERR_INVALID_ARG, "problem pointer is NULL");
     if (p->B < 0 || p->T < 0 || p->H < 0)
         return fail(GDN_ERR_INVALID_ARG, "negative size (B=%lld T=%lld H=%lld)",
@@ -43,7 +44,7 @@ gdn_status check_problem(const gdn_problem* p, gdn::Dims* d) {
     if (!supported_dim(p->K) || !supported_dim(p->V))
         return fail(GDN_ERR_UNSUPPORTED, "K=%lld V=%lld: each must be 16, 32, 64 or 128",
                     (long long)p->K, (long long)p->V);
-    if (p->chunk != 16 && p->chunk != 32 && p->chunk != 64)
+    if (need_chunk && p->chunk != 16 && p->chunk != 32 && p->chunk != 64)
         return fail(GDN_ERR_UNSUPPORTED, "chunk=%d: must be 16, 32 or 64", (int)p->chunk);
     if (p->B > 65535 || p->H > 65535)
         return fail(GDN_ERR_UNSUPPORTED, "B=%lld H=%lld: each must be <= 65535",
@@ -55,8 +56,8 @@ gdn_status check_problem(const gdn_problem* p, gdn::Dims* d) {
     d->H = (int)p->H;
     d->K = (int)p->K;
     d->V = (int)p->V;
-    d->C = p->chunk;
-    d->NC = (int)((p->T + p->chunk - 1) / p->chunk);
+    d->C = need_chunk ? p->chunk : 64;
+    d->NC = (int)((p->T + d->C - 1) / d->C);
     return GDN_OK;
 }
 
@@ -211,7 +212,7 @@ const char* const kKernelNames[gdn::KID_COUNT] = {
     "prep_kernel(fwd)", "scan_fwd_kernel", "prep_kernel(bwd)",
     "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel",
     "prep_fwd_tc", "scan_fwd_tc", "prep_fwd_tc(bwd)", "scan_fwd_tc(state-only)",
-    "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc"};
+    "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc", "decode_kernel"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -362,6 +363,32 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
     });
     if (e != cudaSuccess) return cuda_fail(e, "scan kernel");
     return GDN_OK;
+}
+
+gdn_status gdn_decode(const gdn_problem* p, const void* q, const void* k, const void* v,
+                      const void* alpha, const void* beta, float* state, void* o, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d, false);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const Span ins[] = {{q, BTH * d.K * es, "q"},   {k, BTH * d.K * es, "k"}, {v, BTH * d.V * es, "v"},
+                        {alpha, BTH * es, "alpha"}, {beta, BTH * es, "beta"}};
+    const Span outs[] = {{o, BTH * d.V * es, "o"}, {state, nstate, "state"}};
+    for (int i = 0; i < 5; ++i)
+        if ((st = check_ptr(ins[i], true)) != GDN_OK) return st;
+    for (int i = 0; i < 2; ++i)
+        if ((st = check_ptr(outs[i], true)) != GDN_OK) return st;
+    if ((st = check_overlaps(ins, 5, outs, 2, nullptr, nullptr)) != GDN_OK) return st;
+    if (d.NS() == 0 || d.T == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    cudaError_t e = timed(gdn::KID_DECODE, cs, [&] {
+        return gdn::launch_decode(d, ty, q, k, v, alpha, beta, state, o, cs);
+    });
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "decode kernel");
 }
 
 gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,

@@ -96,6 +96,7 @@ enum KernelId {
     KID_SCAN_BWD_TC,     // scan_bwd_tc
     KID_GRAD_QK_TC,      // grad_qk_tc
     KID_GRAD_WY_TC,      // grad_wy_tc
+    KID_DECODE,          // decode_kernel
     KID_COUNT
 };
 
@@ -137,6 +138,11 @@ int sm_count();
 // Tensor-core forward (tc_fwd.cu).  tc_fwd_supported: shape/dtype test only.
 bool tc_fwd_supported(const Dims& d, InType ty);
 int tc_scan_vt(const Dims& d);
+// Recurrent step over the call's tokens, state [B,H,V,K] fp32 updated in place
+// (decode.cu).
+cudaError_t launch_decode(const Dims& d, InType ty, const void* q, const void* k, const void* v,
+                          const void* alpha, const void* beta, float* state, void* o, cudaStream_t st);
+
 cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v,
                            const void* alpha, const void* beta, const TcBufs& tb,
                            cudaStream_t st);

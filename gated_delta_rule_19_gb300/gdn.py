@@ -61,6 +61,8 @@ def load_library():
     lib.gdn_bwd.restype = ctypes.c_int
     lib.gdn_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
     lib.gdn_fwd_noalloc.restype = ctypes.c_int
+    lib.gdn_decode.argtypes = [P] + [_vp] * 7 + [_vp]
+    lib.gdn_decode.restype = ctypes.c_int
     lib.gdn_num_kernels.restype = ctypes.c_int
     lib.gdn_kernel_name.argtypes = [ctypes.c_int]
     lib.gdn_kernel_name.restype = ctypes.c_char_p
@@ -78,7 +80,7 @@ def load_library():
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_workspace_bytes",
             "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd",
             "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
-            "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc")
+            "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -272,6 +274,36 @@ def gdn_profiler_summary() -> dict:
 
 def gdn_profiler_release() -> None:
     load_library().gdn_profiler_release()
+
+
+def gdn_decode(q, k, v, alpha, beta, state, *, o=None, stream=None):
+    """Recurrent step through ``gdn_decode``: advances ``state`` ([B,H,V,K] fp32,
+    updated in place) through the T tokens of q, k, v, alpha, beta (usually T=1)
+    and writes their outputs.  Calls continue the stream exactly: T calls of one
+    token equal one call of T tokens bit for bit.  Returns ``(o, state)``."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dt = q.dtype
+    p = make_problem(B, T, H, K, V, 64, dt)
+    if o is None:
+        o = torch.empty(B, T, H, V, dtype=dt, device=dev)
+    for t, n, sh in ((k, "k", (B, T, H, K)), (v, "v", (B, T, H, V)), (q, "q", (B, T, H, K)),
+                     (alpha, "alpha", (B, T, H)), (beta, "beta", (B, T, H)),
+                     (o, "o", (B, T, H, V))):
+        if t is None:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"{n} is required")
+        _need(t, n, sh, dt, dev)
+    if state is None:
+        raise GdnError(GDN_ERR_INVALID_ARG, "state is required")
+    _need(state, "state", (B, H, V, K), torch.float32, dev)
+    st = lib.gdn_decode(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                        _ptr(state), _ptr(o), _stream_handle(dev, stream))
+    _check(st)
+    return o, state
 
 
 def gdn_fwd_noalloc(q, k, v, alpha, beta, initial_state, o, final_state=None, *,

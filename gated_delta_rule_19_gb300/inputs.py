@@ -71,6 +71,17 @@ WORKLOADS = {
 
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# The decode step (one token per call, the state carried between calls): a
+# serving batch of 256 sequences with the long-stream shape's 16 heads and a
+# warm state (256 MB of fp32 state, larger than L2).
+DECODE_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("decode_bf16_B256_T1_H16_K128_V128", 256, 1, 16, 128, 128, 64, "bf16", seed=5,
+                 init_std=0.1),
+    ]
+}
+
 
 def torch_dtype(dtype: str) -> torch.dtype:
     return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]

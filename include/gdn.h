@@ -157,6 +157,27 @@ gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, c
                            void* o, float* final_state, void* stream);
 
 /*
+ * gdn_decode -- the recurrent step, for decoding: advances `state` through the
+ * call's T tokens (usually 1) and writes their outputs.  It computes exactly the
+ * token recurrence of section 1 ("OpenGDN", Core operator reference: a stream
+ * continued through state=; "Sparse Delta Memory: layer and kernels",
+ * Execution: the single-token call), in fp32, token by token:
+ *     S <- alpha S (I - beta k k^T) + beta v k^T,   o = S q.
+ * It reads and writes the state once per call, so it is bound by that traffic;
+ * for long T, gdn_fwd's chunked kernels are faster.
+ *   q, k   [B,T,H,K] and v, o [B,T,H,V] in p->dtype; alpha, beta [B,T,H].
+ *   state  [B,H,V,K] fp32, required: read at entry, overwritten with the state
+ *          after the last token.  Calls on one stream continue the stream
+ *          exactly: T calls of one token equal one call of T tokens bit for bit.
+ *   p->chunk is not used (any value is accepted); K, V in {16, 32, 64, 128}.
+ * All pointers 16-byte aligned and required; o and state must not overlap each
+ * other or any input.  Errors are returned before any launch.  Allocates
+ * nothing; asynchronous on `stream`.
+ */
+gdn_status gdn_decode(const gdn_problem* p, const void* q, const void* k, const void* v,
+                      const void* alpha, const void* beta, float* state, void* o, void* stream);
+
+/*
  * Optional launch timer, for benchmarks.  While started, every kernel launch of
  * gdn_fwd/gdn_bwd is bracketed by two CUDA events recorded on the call's stream
  * (up to `capacity` launches; later launches are not timed).  The events are

@@ -138,3 +138,25 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 4, 1, 16)
     with pytest.raises(lib.GdnError):
         lib.gdn_fwd(q, q, q, torch.ones(1, 4, 1), torch.zeros(1, 4, 1), chunk=16)
+
+
+def _decode(lib, p, **over):
+    h = lib.load_library()
+    base = dict(q=0, k=1, v=2, alpha=3, beta=4, state=5, o=6)
+    args = {n: FAKE + (x << 30) for n, x in base.items()}
+    args.update(over)
+    vp = ctypes.c_void_p
+    order = ("q", "k", "v", "alpha", "beta", "state", "o")
+    return h.gdn_decode(ctypes.byref(p), *[vp(args[n]) for n in order], vp(None))
+
+
+def test_decode_arguments_rejected_before_launch(lib):
+    INVALID, UNSUP = 1, 2
+    ok = lib.make_problem(2, 1, 3, 64, 32, 64, 1)
+    assert _decode(lib, ok, state=None) == INVALID
+    assert "state is NULL" in lib.gdn_last_error()
+    assert _decode(lib, ok, o=FAKE + (5 << 30)) == INVALID  # o is the state
+    assert _decode(lib, ok, q=FAKE + 8) == INVALID          # misaligned
+    assert _decode(lib, lib.make_problem(1, 1, 1, 24, 16, 64, 1)) == UNSUP
+    # the chunk field is not used by the decode step: with T = 0 nothing launches
+    assert _decode(lib, lib.make_problem(1, 0, 1, 16, 16, 7, 1)) == 0
