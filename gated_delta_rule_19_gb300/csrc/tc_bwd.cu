@@ -392,8 +392,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_W,
            const __grid_constant__ CUtensorMap tm_dU, const __grid_constant__ CUtensorMap tm_S0,
            const __grid_constant__ CUtensorMap tm_dS1, const __grid_constant__ CUtensorMap tm_dq,
+           const __grid_constant__ CUtensorMap tm_dKp, const __grid_constant__ CUtensorMap tm_dWt,
            const bf16* __restrict__ Ut, const bf16* __restrict__ Mqk, const float* __restrict__ G,
-           bf16* __restrict__ dKp, bf16* __restrict__ dWt, float* __restrict__ dGp, int* err) {
+           float* __restrict__ dGp, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* E1f = (float*)(sm + qk::E1);
@@ -520,6 +521,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // dO and S0 tiles are read by every thread
         ok = mbar_wait(&bars[2], ph, err, 2) && ok;
+        if (tid == 0) bulk_wait_read0();  // the previous chunk's stores from the U / EU tiles are done
         __syncthreads();  // Gs / gs
         fence_after_sync();
         const float GC = Gs[63], gC = gs[63];
@@ -624,9 +626,10 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 E1f[half * 64 + r] = rsum;
                 E1f[128 + (sub * 2 + half) * 32 + lane] = warp_colsum32(e1);
             }
-            // dW^T row k (= lanerow), columns half*32 .. +32 -> scratch
+            // dW^T row k (= lanerow), columns half*32 .. +32 -> [128 x 64] tile in the EU
+            // slot (dead once phase 2 is done), stored to scratch by TMA
             const int cb = half * 32;
-            uint4* wp = (uint4*)(dWt + ((int64_t)krow0 + lanerow) * kC + cb);
+            unsigned char* wt = sm + qk::EU + (lanerow >> 6) * 8192;
             float w[16], w2[16];
             tmem_load16f2(tDW + lanebase + cb, tDW + lanebase + cb + 16, w, w2);
 #pragma unroll
@@ -634,10 +637,10 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 w[j] = -w[j];
                 w2[j] = -w2[j];
             }
-            wp[0] = pack8(w);
-            wp[1] = pack8(w + 8);
-            wp[2] = pack8(w2);
-            wp[3] = pack8(w2 + 8);
+            *(uint4*)(wt + sw128_off(lanerow & 63, cb)) = pack8(w);
+            *(uint4*)(wt + sw128_off(lanerow & 63, cb + 8)) = pack8(w + 8);
+            *(uint4*)(wt + sw128_off(lanerow & 63, cb + 16)) = pack8(w2);
+            *(uint4*)(wt + sw128_off(lanerow & 63, cb + 24)) = pack8(w2 + 8);
         }
         fence_proxy_async();
         fence_before_sync();
@@ -645,6 +648,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_after_sync();
         // ---- phase 3 (K over tokens): dQ2^T = K^T dQK^T;  dK^T += Q^T dQK  (M=128, N=64)
         if (tid == 0 && ok) {
+            for (int j = 0; j < 2; ++j) tma_store_2d(&tm_dWt, sm + qk::EU + j * 8192, 0, krow0 + 64 * j);
+            bulk_commit();
             const uint32_t idq = idesc_bf16(128, 64, true, false);
             const uint32_t idk = idesc_bf16(128, 64, true, true);
             const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
@@ -689,7 +694,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         {
             const int cb = half * 32;
             unsigned char* dqt = sm + qk::DQ;
-            uint4* kp = (uint4*)(dKp + ((int64_t)krow0 + lanerow) * kC + cb);
+            unsigned char* kt = sm + qk::U + (lanerow >> 6) * 8192;  // U is dead after phase 2
 #pragma unroll
             for (int c0 = 0; c0 < 32; c0 += 16) {
                 float q1[16], q2[16], kk[16];
@@ -699,8 +704,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 for (int j = 0; j < 16; ++j)
                     *(bf16*)(dqt + tile_off(64, cb + c0 + j, lanerow)) =
                         __float2bfloat16_rn(gs[cb + c0 + j] * q1[j] + q2[j]);
-                kp[c0 / 8] = pack8(kk);
-                kp[c0 / 8 + 1] = pack8(kk + 8);
+                *(uint4*)(kt + sw128_off(lanerow & 63, cb + c0)) = pack8(kk);
+                *(uint4*)(kt + sw128_off(lanerow & 63, cb + c0 + 8)) = pack8(kk + 8);
             }
         }
         if (tid < 64) {
@@ -714,7 +719,10 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ok = __syncthreads_and(ok);
         fence_after_sync();
         if (tid == 0 && ok) {
-            for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
+            for (int j = 0; j < 2; ++j) {
+                tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
+                tma_store_2d(&tm_dKp, sm + qk::U + j * 8192, 0, krow0 + 64 * j);
+            }
             bulk_commit();
         }
         if (!ok) break;
@@ -1108,20 +1116,21 @@ cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, cons
 
 cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
                               const __nv_bfloat16* states, const TcBwdBufs& bb, void* dq, cudaStream_t st) {
-    CUtensorMap mq, mk, mdo, mW, mdU, mS0, mdS1, mdq;
+    CUtensorMap mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, mdKp, mdWt;
     const int64_t rows = d.NS() * d.NC * kC;
     const int64_t krows = d.NS() * d.NC * kD;
     if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
         !tmap_bthd(&mdo, d_o, d.B, d.T, d.H, kD) || !tmap_rows(&mW, tb.W, rows, kD) ||
         !tmap_rows(&mdU, bb.dU, rows, kD) || !tmap_rows(&mS0, states, krows, kD) ||
-        !tmap_rows(&mdS1, bb.dS1, krows, kD) || !tmap_bthd(&mdq, dq, d.B, d.T, d.H, kD))
+        !tmap_rows(&mdS1, bb.dS1, krows, kD) || !tmap_bthd(&mdq, dq, d.B, d.T, d.H, kD) ||
+        !tmap_rows(&mdKp, bb.dKp, krows, kC) || !tmap_rows(&mdWt, bb.dWt, krows, kC))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(grad_qk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::SMEM);
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;
     dim3 grid((unsigned)std::min<int64_t>(nchunks, sm_count()));
-    grad_qk_tc<<<grid, 256, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, tb.Ut, tb.Mqk, tb.G, bb.dKp,
-                                            bb.dWt, bb.dGp, tb.err);
+    grad_qk_tc<<<grid, 256, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, mdKp, mdWt, tb.Ut, tb.Mqk,
+                                            tb.G, bb.dGp, tb.err);
     return cudaGetLastError();
 }
 
