@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step and prologue lines")
     return ap.parse_args()
 
 
@@ -330,6 +330,49 @@ def roofline(summary, w, peaks):
 
 # ------------------------------------------------------------------ GPU arm
 
+def measure_prologue(gdn, dev, stream, args, world, w):
+    """Times the fused prologue (q/k L2 normalisation and gate activations) and its
+    backward on the training shape: both are elementwise passes bound by HBM
+    traffic, taken against the measured HBM copy rate.  Property check: the
+    normalised rows have unit length up to the 1e-6 epsilon."""
+    from gated_delta_rule_19_gb300.inputs import make_prologue_inputs
+
+    x = {n: t.to(dev) for n, t in make_prologue_inputs(w.B, w.T, w.H, w.K, w.dtype, seed=w.seed).items()}
+    fwd_in = [x[n] for n in ("q_raw", "k_raw", "a_logit", "b_logit")]
+    bwd_in = fwd_in + [x[n] for n in ("dq", "dk", "dalpha", "dbeta")]
+    out_f = gdn.gdn_prologue_fwd(*fwd_in)
+    out_b = gdn.gdn_prologue_bwd(*bwd_in)
+    torch.cuda.synchronize(dev)
+    norm_err = float((out_f[0].float().norm(dim=-1) - 1).abs().max())
+
+    def timed(fn, n):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+
+    n = max(20, args.steps)
+    f_ms = timed(lambda: gdn.gdn_prologue_fwd(*fwd_in, out=out_f), n)
+    b_ms = timed(lambda: gdn.gdn_prologue_bwd(*bwd_in, out=out_b), n)
+    es = 2 if w.dtype == "bf16" else 4
+    rows = w.B * w.T * w.H
+    fb = rows * (4 * w.K + 4) * es
+    bb = rows * (6 * w.K + 6) * es
+    hbm = load_peaks()["hbm_gbs"]
+    return {"workload": w.name, "fwd_us": f_ms * 1e3, "bwd_us": b_ms * 1e3,
+            "fwd_bytes": fb, "bwd_bytes": bb,
+            "fwd_GBs": fb / (f_ms / 1e3) / 1e9, "bwd_GBs": bb / (b_ms / 1e3) / 1e9,
+            "fwd_frac_of_hbm": fb / (f_ms / 1e3) / 1e9 / hbm, "bwd_frac_of_hbm": bb / (b_ms / 1e3) / 1e9 / hbm,
+            "max_unit_norm_error": norm_err}
+
+
 def measure_decode(gdn, dev, stream, args, world):
     """Times gdn_decode on the decode workload (256 sequences x 16 heads, one
     token, K=V=128 bf16): its 256 MB fp32 state is read and written once per
@@ -556,6 +599,7 @@ def run_gdn(args, world, rank, local):
     # ---- the decode step (a survey "next" row): one token per call, the state
     # carried in place between calls
     decode = None if args.no_decode else measure_decode(gdn, dev, stream, args, world)
+    prologue = None if args.no_decode else measure_prologue(gdn, dev, stream, args, world, w)
 
     if rank != 0:
         return
@@ -585,6 +629,7 @@ def run_gdn(args, world, rank, local):
         "parity_sampled": parity,
         "e2e": e2e,
         "decode": decode,
+        "prologue": prologue,
         "gpu_launches": launches,
         "clocks": clk,
     }

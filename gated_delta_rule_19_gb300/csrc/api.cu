@@ -212,7 +212,8 @@ const char* const kKernelNames[gdn::KID_COUNT] = {
     "prep_kernel(fwd)", "scan_fwd_kernel", "prep_kernel(bwd)",
     "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel",
     "prep_fwd_tc", "scan_fwd_tc", "prep_fwd_tc(bwd)", "scan_fwd_tc(state-only)",
-    "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc", "decode_kernel"};
+    "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc", "decode_kernel", "prologue_fwd_kernel",
+    "prologue_bwd_kernel"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -363,6 +364,61 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
     });
     if (e != cudaSuccess) return cuda_fail(e, "scan kernel");
     return GDN_OK;
+}
+
+gdn_status gdn_prologue_fwd(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* a_logit,
+                            const void* b_logit, void* q, void* k, void* alpha, void* beta, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d, false);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const Span ins[] = {{q_raw, BTH * d.K * es, "q_raw"}, {k_raw, BTH * d.K * es, "k_raw"},
+                        {a_logit, BTH * es, "a_logit"},   {b_logit, BTH * es, "b_logit"}};
+    const Span outs[] = {{q, BTH * d.K * es, "q"}, {k, BTH * d.K * es, "k"}, {alpha, BTH * es, "alpha"},
+                         {beta, BTH * es, "beta"}};
+    for (int i = 0; i < 4; ++i)
+        if ((st = check_ptr(ins[i], true)) != GDN_OK || (st = check_ptr(outs[i], true)) != GDN_OK) return st;
+    if ((st = check_overlaps(ins, 4, outs, 4, nullptr, nullptr)) != GDN_OK) return st;
+    if (BTH == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    cudaError_t e = timed(gdn::KID_PROLOGUE_FWD, cs, [&] {
+        return gdn::launch_prologue_fwd(d, ty, q_raw, k_raw, a_logit, b_logit, q, k, alpha, beta, cs);
+    });
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "prologue kernel");
+}
+
+gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* a_logit,
+                            const void* b_logit, const void* dq, const void* dk, const void* dalpha,
+                            const void* dbeta, void* dq_raw, void* dk_raw, void* da_logit, void* db_logit,
+                            void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d, false);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const Span ins[] = {{q_raw, BTH * d.K * es, "q_raw"}, {k_raw, BTH * d.K * es, "k_raw"},
+                        {a_logit, BTH * es, "a_logit"},   {b_logit, BTH * es, "b_logit"},
+                        {dq, BTH * d.K * es, "dq"},       {dk, BTH * d.K * es, "dk"},
+                        {dalpha, BTH * es, "dalpha"},     {dbeta, BTH * es, "dbeta"}};
+    const Span outs[] = {{dq_raw, BTH * d.K * es, "dq_raw"}, {dk_raw, BTH * d.K * es, "dk_raw"},
+                         {da_logit, BTH * es, "da_logit"},   {db_logit, BTH * es, "db_logit"}};
+    for (int i = 0; i < 8; ++i)
+        if ((st = check_ptr(ins[i], true)) != GDN_OK) return st;
+    for (int i = 0; i < 4; ++i)
+        if ((st = check_ptr(outs[i], true)) != GDN_OK) return st;
+    if ((st = check_overlaps(ins, 8, outs, 4, nullptr, nullptr)) != GDN_OK) return st;
+    if (BTH == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    cudaError_t e = timed(gdn::KID_PROLOGUE_BWD, cs, [&] {
+        return gdn::launch_prologue_bwd(d, ty, q_raw, k_raw, a_logit, b_logit, dq, dk, dalpha, dbeta, dq_raw,
+                                        dk_raw, da_logit, db_logit, cs);
+    });
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "prologue backward kernel");
 }
 
 gdn_status gdn_decode(const gdn_problem* p, const void* q, const void* k, const void* v,

@@ -97,6 +97,8 @@ enum KernelId {
     KID_GRAD_QK_TC,      // grad_qk_tc
     KID_GRAD_WY_TC,      // grad_wy_tc
     KID_DECODE,          // decode_kernel
+    KID_PROLOGUE_FWD,    // prologue_fwd_kernel
+    KID_PROLOGUE_BWD,    // prologue_bwd_kernel
     KID_COUNT
 };
 
@@ -138,6 +140,13 @@ int sm_count();
 // Tensor-core forward (tc_fwd.cu).  tc_fwd_supported: shape/dtype test only.
 bool tc_fwd_supported(const Dims& d, InType ty);
 int tc_scan_vt(const Dims& d);
+// q/k L2 normalisation and gate activations, and their backward (prologue.cu).
+cudaError_t launch_prologue_fwd(const Dims& d, InType ty, const void* qr, const void* kr, const void* a,
+                                const void* b, void* q, void* k, void* alpha, void* beta, cudaStream_t st);
+cudaError_t launch_prologue_bwd(const Dims& d, InType ty, const void* qr, const void* kr, const void* a,
+                                const void* b, const void* dq, const void* dk, const void* dalpha, const void* dbeta,
+                                void* dqr, void* dkr, void* da, void* db, cudaStream_t st);
+
 // Recurrent step over the call's tokens, state [B,H,V,K] fp32 updated in place
 // (decode.cu).
 cudaError_t launch_decode(const Dims& d, InType ty, const void* q, const void* k, const void* v,

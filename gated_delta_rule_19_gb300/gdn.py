@@ -63,6 +63,10 @@ def load_library():
     lib.gdn_fwd_noalloc.restype = ctypes.c_int
     lib.gdn_decode.argtypes = [P] + [_vp] * 7 + [_vp]
     lib.gdn_decode.restype = ctypes.c_int
+    lib.gdn_prologue_fwd.argtypes = [P] + [_vp] * 8 + [_vp]
+    lib.gdn_prologue_fwd.restype = ctypes.c_int
+    lib.gdn_prologue_bwd.argtypes = [P] + [_vp] * 12 + [_vp]
+    lib.gdn_prologue_bwd.restype = ctypes.c_int
     lib.gdn_num_kernels.restype = ctypes.c_int
     lib.gdn_kernel_name.argtypes = [ctypes.c_int]
     lib.gdn_kernel_name.restype = ctypes.c_char_p
@@ -80,7 +84,8 @@ def load_library():
 EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_workspace_bytes",
             "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd",
             "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
-            "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode")
+            "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode",
+            "gdn_prologue_fwd", "gdn_prologue_bwd")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -274,6 +279,67 @@ def gdn_profiler_summary() -> dict:
 
 def gdn_profiler_release() -> None:
     load_library().gdn_profiler_release()
+
+
+def _prologue_problem(q_raw, v_dim):
+    B, T, H, K = q_raw.shape
+    return make_problem(B, T, H, K, v_dim, 64, q_raw.dtype), (B, T, H, K)
+
+
+def gdn_prologue_fwd(q_raw, k_raw, a_logit, b_logit, *, out=None, stream=None):
+    """q/k L2 normalisation and gate activations through ``gdn_prologue_fwd``:
+    returns ``(q, k, alpha, beta)`` with q = q_raw / sqrt(|q_raw|^2 + 1e-6) (same
+    for k), alpha = exp(-softplus(a_logit)), beta = sigmoid(b_logit).  ``out`` may
+    pass the four output tensors."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    p, (B, T, H, K) = _prologue_problem(q_raw, 16)
+    dt = q_raw.dtype
+    if out is None:
+        out = (torch.empty_like(q_raw), torch.empty_like(q_raw), torch.empty(B, T, H, dtype=dt, device=dev),
+               torch.empty(B, T, H, dtype=dt, device=dev))
+    q, k, alpha, beta = out
+    for t, n, sh in ((q_raw, "q_raw", (B, T, H, K)), (k_raw, "k_raw", (B, T, H, K)),
+                     (a_logit, "a_logit", (B, T, H)), (b_logit, "b_logit", (B, T, H)),
+                     (q, "q", (B, T, H, K)), (k, "k", (B, T, H, K)), (alpha, "alpha", (B, T, H)),
+                     (beta, "beta", (B, T, H))):
+        if t is None:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"{n} is required")
+        _need(t, n, sh, dt, dev)
+    st = lib.gdn_prologue_fwd(ctypes.byref(p), _ptr(q_raw), _ptr(k_raw), _ptr(a_logit), _ptr(b_logit),
+                              _ptr(q), _ptr(k), _ptr(alpha), _ptr(beta), _stream_handle(dev, stream))
+    _check(st)
+    return q, k, alpha, beta
+
+
+def gdn_prologue_bwd(q_raw, k_raw, a_logit, b_logit, dq, dk, dalpha, dbeta, *, out=None, stream=None):
+    """Backward of :func:`gdn_prologue_fwd` through ``gdn_prologue_bwd``: returns
+    ``(dq_raw, dk_raw, da_logit, db_logit)``."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    p, (B, T, H, K) = _prologue_problem(q_raw, 16)
+    dt = q_raw.dtype
+    if out is None:
+        out = (torch.empty_like(q_raw), torch.empty_like(q_raw), torch.empty(B, T, H, dtype=dt, device=dev),
+               torch.empty(B, T, H, dtype=dt, device=dev))
+    dqr, dkr, da, db = out
+    for t, n, sh in ((q_raw, "q_raw", (B, T, H, K)), (k_raw, "k_raw", (B, T, H, K)),
+                     (a_logit, "a_logit", (B, T, H)), (b_logit, "b_logit", (B, T, H)),
+                     (dq, "dq", (B, T, H, K)), (dk, "dk", (B, T, H, K)), (dalpha, "dalpha", (B, T, H)),
+                     (dbeta, "dbeta", (B, T, H)), (dqr, "dq_raw", (B, T, H, K)), (dkr, "dk_raw", (B, T, H, K)),
+                     (da, "da_logit", (B, T, H)), (db, "db_logit", (B, T, H))):
+        if t is None:
+            raise GdnError(GDN_ERR_INVALID_ARG, f"{n} is required")
+        _need(t, n, sh, dt, dev)
+    st = lib.gdn_prologue_bwd(ctypes.byref(p), _ptr(q_raw), _ptr(k_raw), _ptr(a_logit), _ptr(b_logit),
+                              _ptr(dq), _ptr(dk), _ptr(dalpha), _ptr(dbeta), _ptr(dqr), _ptr(dkr), _ptr(da),
+                              _ptr(db), _stream_handle(dev, stream))
+    _check(st)
+    return dqr, dkr, da, db
 
 
 def gdn_decode(q, k, v, alpha, beta, state, *, o=None, stream=None):

@@ -125,3 +125,27 @@ def custom(name="custom", B=1, T=64, H=2, K=16, V=16, chunk=16, dtype="f32", see
            init_std=0.0, dfinal_std=0.0, backward=True) -> Workload:
     """A workload of any shape with the same recipe (for edge-case tests)."""
     return Workload(name, B, T, H, K, V, chunk, dtype, seed, init_std, dfinal_std, backward)
+
+
+def make_prologue_inputs(B, T, H, K, dtype="f32", seed=0, scale=3.0, logit_scale=2.0) -> dict:
+    """Raw inputs of the prologue (before q/k normalisation and the gate
+    activations) and upstream gradients for its backward, drawn in this order
+    from a CPU generator seeded with ``seed``: q_raw, k_raw ~ N(0, scale^2);
+    a_logit, b_logit ~ N(0, logit_scale^2); dq, dk ~ N(0,1); dalpha, dbeta ~
+    N(0,1); all cast to the run dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    f32 = torch.float32
+    shape = (B, T, H, K)
+    out = dict(
+        q_raw=torch.randn(*shape, generator=g, dtype=f32) * scale,
+        k_raw=torch.randn(*shape, generator=g, dtype=f32) * scale,
+        a_logit=torch.randn(B, T, H, generator=g, dtype=f32) * logit_scale,
+        b_logit=torch.randn(B, T, H, generator=g, dtype=f32) * logit_scale,
+        dq=torch.randn(*shape, generator=g, dtype=f32),
+        dk=torch.randn(*shape, generator=g, dtype=f32),
+        dalpha=torch.randn(B, T, H, generator=g, dtype=f32),
+        dbeta=torch.randn(B, T, H, generator=g, dtype=f32),
+    )
+    dt = torch_dtype(dtype)
+    return {n: t.to(dt) for n, t in out.items()}

@@ -157,6 +157,31 @@ gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const void* k, c
                            void* o, float* final_state, void* stream);
 
 /*
+ * gdn_prologue_fwd / gdn_prologue_bwd -- the step in front of the recurrence in
+ * every mixer the pages show ("OpenGDN", Mixer: L2-normalized Q/K and per-head
+ * alpha/beta gates), fused into one pass each way.  Per row (b, t, h):
+ *     q = q_raw / sqrt(sum_K q_raw^2 + 1e-6)      (the same for k)
+ *     alpha = exp(-softplus(a_logit)) = 1 / (1 + e^a_logit)
+ *     beta  = sigmoid(b_logit)
+ * (a mixer whose gate is alpha = sigmoid(x) passes a_logit = -x).  The backward
+ * takes dL/dq, dL/dk, dL/dalpha, dL/dbeta (e.g. from gdn_bwd) and returns the
+ * gradients with respect to q_raw, k_raw, a_logit, b_logit, recomputing the
+ * norms and gates from the raw inputs (nothing is saved between the two calls).
+ *   q_raw, k_raw, q, k, dq, dk, dq_raw, dk_raw  [B,T,H,K] in p->dtype;
+ *   a_logit, b_logit, alpha, beta, dalpha, dbeta, da_logit, db_logit  [B,T,H].
+ *   p->V and p->chunk are not used (V must still be a supported size).
+ * All pointers 16-byte aligned and required; no output may overlap an input or
+ * another output.  Errors are returned before any launch.  Allocates nothing;
+ * asynchronous on `stream`.  Arithmetic in fp32.
+ */
+gdn_status gdn_prologue_fwd(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* a_logit,
+                            const void* b_logit, void* q, void* k, void* alpha, void* beta, void* stream);
+gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* a_logit,
+                            const void* b_logit, const void* dq, const void* dk, const void* dalpha,
+                            const void* dbeta, void* dq_raw, void* dk_raw, void* da_logit, void* db_logit,
+                            void* stream);
+
+/*
  * gdn_decode -- the recurrent step, for decoding: advances `state` through the
  * call's T tokens (usually 1) and writes their outputs.  It computes exactly the
  * token recurrence of section 1 ("OpenGDN", Core operator reference: a stream
