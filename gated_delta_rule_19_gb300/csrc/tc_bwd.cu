@@ -746,24 +746,31 @@ namespace wy {
 // inputs: K | V | dU ([64 x 128] each) | dW^T [128 x 64] | T [64 x 64]
 constexpr int K = 0, V = 16384, DU = 32768, DWT = 49152, T = 65536;
 constexpr int T1 = 73728, T2 = 81920, DT = 90112, Y = 98304;  // [64 x 64]
-constexpr int E = DT;                  // dT is dead once Y is formed
-constexpr int DV = V, DK = K;          // outputs [64 x 128] into dead input slots
-constexpr int VEC = Y + 8192;          // per-token and partial-sum vectors
+constexpr int E = DT;      // dT is dead once Y is formed
+constexpr int ID = Y;      // identity [64 x 64], written once Y has been read
+constexpr int KP = V;      // dK partial [128 x 64], loaded once V has been read
+constexpr int DV = DU;     // outputs [64 x 128] into dead input slots
+constexpr int DK = K;
+constexpr int VEC = Y + 8192;  // per-token and partial-sum vectors
 constexpr int NVEC = 15 * 64;
 constexpr int BAR = VEC + NVEC * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
+// the M=128 operands whose rows 0-63 are not used read the 8 KB before their tile
+static_assert(T1 - 8192 == T && T2 - 8192 == T1 && E - 8192 == T2 && ID - 8192 == DT, "tile order");
 }  // namespace wy
 
 // One CTA per chunk, 256 threads, two CTAs per SM (each one's epilogues overlap
-// the other's MMAs and loads).  Rows of the M=64 products land in TMEM lanes 0-63
-// (threads with warp % 4 < 2); warps w and w+4 split columns.
+// the other's MMAs and loads).  Warps w and w+4 reach TMEM lanes 32*(w%4) and
+// split columns.  Rows of the 64 x 64 products land in lanes 0-63 (threads with
+// warp % 4 < 2); dV and dK are formed with tokens on lanes 64-127 and 128
+// columns, so the other half of the threads writes them as whole rows.
 __global__ void __launch_bounds__(256, 2)
 grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_dWt, const __grid_constant__ CUtensorMap tm_dU,
            const __grid_constant__ CUtensorMap tm_T, const __grid_constant__ CUtensorMap tm_dk,
-           const __grid_constant__ CUtensorMap tm_dv, const bf16* __restrict__ alpha,
-           const bf16* __restrict__ beta, const float* __restrict__ G, const bf16* __restrict__ dKp,
+           const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dKp,
+           const bf16* __restrict__ alpha, const bf16* __restrict__ beta, const float* __restrict__ G,
            const float* __restrict__ dGp, bf16* __restrict__ dalpha, bf16* __restrict__ dbeta, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -778,14 +785,14 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     float* dB3p = vec + 576;    // [2 column halves][64]
     float* rE2p = vec + 704;    // [2][64]
     float* cE2 = vec + 832;     // [2][64]
-    uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0] loads, [1] MMA
-    uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 16);
+    uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0] loads, [1] MMA, [2] dK partial
+    uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = warp & 3, half = warp >> 2;
     const int lanerow = 32 * sub + lane;
     const bool urow = sub < 2;
-    const int r = urow ? lanerow : lanerow - 64;  // row of the M=64 results (urow threads)
+    const int r = urow ? lanerow : lanerow - 64;  // row of the 64-row results (both sides)
     const int cb = half * 32;                     // this warp's 32 columns of a 64-column result
     const int64_t ch = blockIdx.x;
     const int c = (int)(ch % d.NC);
@@ -795,8 +802,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(&bars[0], 9 * 8192);
         for (int j = 0; j < 2; ++j) {
@@ -836,13 +842,15 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
-    // TMEM columns: Qm, P, KK, Y; later dA over Qm, dV^T over P, dK^T over Y
-    const uint32_t tQm = tmem, tP = tmem + 64, tKK = tmem + 128, tY = tmem + 192;
-    const uint32_t tDA = tQm, tDV = tP, tDK = tY;
+    // TMEM columns: Qm 0-63, P 64-127, Y 128-191, KK 192-255; then dA over Y,
+    // dV over Qm/P (128 columns), dK over dV (128 columns)
+    const uint32_t tQm = tmem, tP = tmem + 64, tY = tmem + 128, tKK = tmem + 192;
+    const uint32_t tDA = tY, tDV = tmem, tDK = tmem;
     const uint32_t sK = smem_u32(sm + wy::K), sV = smem_u32(sm + wy::V), sDU = smem_u32(sm + wy::DU);
     const uint32_t sDWT = smem_u32(sm + wy::DWT), sT = smem_u32(sm + wy::T);
     const uint32_t sT1 = smem_u32(sm + wy::T1), sT2 = smem_u32(sm + wy::T2), sDT = smem_u32(sm + wy::DT);
-    const uint32_t sY = smem_u32(sm + wy::Y), sE = smem_u32(sm + wy::E);
+    const uint32_t sY = smem_u32(sm + wy::Y), sE = smem_u32(sm + wy::E), sID = smem_u32(sm + wy::ID);
+    const uint32_t sKP = smem_u32(sm + wy::KP);
 
     bool ok = mbar_wait(&bars[0], 0, err, 1);
     // ---- phase 1: Qm = dW K^T (K over k), P = dU V^T (K over v), KK = K K^T   (M=128: rows 64-127 unused)
@@ -880,6 +888,11 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     ok = mbar_wait(&bars[1], 0, err, 2) && ok;
     __syncwarp();
     fence_after_sync();
+    // V is dead: bring in the dK partial of the first gradient kernel for phase 4
+    if (tid == 0 && ok) {
+        mbar_arrive_expect_tx(&bars[2], 2 * 8192);
+        for (int j = 0; j < 2; ++j) tma_load_2d(sm + wy::KP + j * 8192, &tm_dKp, &bars[2], 0, krow0 + 64 * j);
+    }
     if (urow) {
         // rows s = r: column sums of T (P + Qm diag(gamma)) and T Qm over this warp's 32
         // rows; dT (strictly lower) for the Y product
@@ -931,82 +944,96 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     fence_before_sync();
     ok = __syncthreads_and(ok);
     fence_after_sync();
-    // ---- phase 3: dA = -T^T Y (M=128, rows 64-127 unused), dV^T = dU^T T2 (M=128)
+    // ---- phase 3: dA = -T^T Y (N=64, rows 0-63), dV = T2^T dU (N=128, tokens on rows 64-127)
     if (tid == 0 && ok) {
         const uint32_t ida = idesc_bf16(128, 64, true, true, true);
-        const uint32_t idv = idesc_bf16(128, 64, true, true);
+        const uint32_t idv = idesc_bf16(128, 128, true, true);
         const uint64_t dtm = sdesc(sT, 8192, 1024, SW_128B), dym = sdesc(sY, 8192, 1024, SW_128B);
-        const uint64_t dum = sdesc(sDU, 8192, 1024, SW_128B), dt2m = sdesc(sT2, 8192, 1024, SW_128B);
+        const uint64_t dt2m = sdesc(sT2 - 8192, 8192, 1024, SW_128B), dum = sdesc(sDU, 8192, 1024, SW_128B);
 #pragma unroll
         for (int s2 = 0; s2 < 4; ++s2) {
             mma_bf16_ss(tDA, desc_add(dtm, s2 * 2048), desc_add(dym, s2 * 2048), ida, s2 > 0);
-            mma_bf16_ss(tDV, desc_add(dum, s2 * 2048), desc_add(dt2m, s2 * 2048), idv, s2 > 0);
+            mma_bf16_ss(tDV, desc_add(dt2m, s2 * 2048), desc_add(dum, s2 * 2048), idv, s2 > 0);
         }
         mma_commit(&bars[1]);
     }
     if (ok) ok = mbar_wait(&bars[1], 0, err, 8);
     __syncwarp();
     fence_after_sync();
-    {
-        if (urow) {
-            // rows a = r: dbeta3, E = beta_a Gam .* dA (strictly lower) -> E tile, E2 = E .* KK
-            const float Ga = Gs[r], ba = bs[r];
-            float b3 = 0.f, re2 = 0.f;
-#pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
-                float da[16], kk[16], ev[16], e2[16];
-                tmem_load16f2(tDA + lanebase + cb + c0, tKK + lanebase + cb + c0, da, kk);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int bc = cb + c0 + j;
-                    const float gam = (bc < r) ? expf(Ga - Gs[bc]) : 0.f;
-                    const float m = gam * da[j];
-                    b3 += m * kk[j];
-                    ev[j] = ba * m;
-                    e2[j] = ev[j] * kk[j];
-                    re2 += e2[j];
-                }
-                tile_put16(sm + wy::E, 64, r, cb + c0, ev);
-                const float s3 = warp_colsum16(e2);
-                if (lane < 16) cE2[sub * 64 + cb + c0 + lane] = s3;
-            }
-            dB3p[half * 64 + r] = b3;
-            rE2p[half * 64 + r] = re2;
-        }
-        // dV^T row v = lanerow, columns cb .. +32 -> dv tile (rows r, column v) in the V slot
-        unsigned char* dvt = sm + wy::DV;
+    if (urow) {
+        // rows a = r: dbeta3, E = beta_a Gam .* dA (strictly lower) -> E tile, E2 = E .* KK
+        const float Ga = Gs[r], ba = bs[r];
+        float b3 = 0.f, re2 = 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < 32; c0 += 16) {
-            float x[16];
-            tmem_load16f(tDV + lanebase + cb + c0, x);
+            float da[16], kk[16], ev[16], e2[16];
+            tmem_load16f2(tDA + lanebase + cb + c0, tKK + lanebase + cb + c0, da, kk);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *(bf16*)(dvt + tile_off(64, cb + c0 + j, lanerow)) = __float2bfloat16_rn(x[j]);
+            for (int j = 0; j < 16; ++j) {
+                const int bc = cb + c0 + j;
+                const float gam = (bc < r) ? expf(Ga - Gs[bc]) : 0.f;
+                const float m = gam * da[j];
+                b3 += m * kk[j];
+                ev[j] = ba * m;
+                e2[j] = ev[j] * kk[j];
+                re2 += e2[j];
+            }
+            tile_put16(sm + wy::E, 64, r, cb + c0, ev);
+            const float s3 = warp_colsum16(e2);
+            if (lane < 16) cE2[sub * 64 + cb + c0 + lane] = s3;
+        }
+        dB3p[half * 64 + r] = b3;
+        rE2p[half * 64 + r] = re2;
+        // the identity for adding the dK partial by an MMA (Y is dead)
+        if (half == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = (8 * q + j == r) ? 1.f : 0.f;
+                *(uint4*)(sm + wy::ID + sw128_off(r, 8 * q)) = pack8(f);
+            }
+        }
+    } else {
+        // dV row a = r (token), columns 64*half .. +64 -> dv tile (dU is dead)
+        unsigned char* dvt = sm + wy::DV + half * 8192;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            float x[32];
+            tmem_cols<32>(tDV + lanebase + 64 * half + 32 * g, x);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *(uint4*)(dvt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
         }
     }
     fence_proxy_async();
     fence_before_sync();
     ok = __syncthreads_and(ok);
     fence_after_sync();
-    // ---- phase 4: dK^T = dW^T T1 + K^T E + K^T E^T   (M=128, K over tokens)
+    // ---- phase 4: dK = T1^T dW + E K + E^T K + dK_partial (N=128, tokens on rows 64-127)
     if (tid == 0 && ok) {
         for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
         bulk_commit();
-        const uint32_t id1 = idesc_bf16(128, 64, false, true);
-        const uint32_t id2 = idesc_bf16(128, 64, true, true);
-        const uint32_t id3 = idesc_bf16(128, 64, true, false);
-        const uint64_t ddw = sdesc(sDWT, 16, 1024, SW_128B), dt1m = sdesc(sT1, 8192, 1024, SW_128B);
-        const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
-        const uint64_t dem = sdesc(sE, 8192, 1024, SW_128B), dek = sdesc(sE, 16, 1024, SW_128B);
+        ok = mbar_wait(&bars[2], 0, err, 16);
+        if (ok) {
+            const uint32_t id_mk = idesc_bf16(128, 128, true, false);   // A MN-major, B K-major
+            const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
+            const uint32_t id_mm = idesc_bf16(128, 128, true, true);
+            const uint32_t id_kk = idesc_bf16(128, 128, false, false);
+            const uint64_t dt1m = sdesc(sT1 - 8192, 8192, 1024, SW_128B), ddw = sdesc(sDWT, 16, 1024, SW_128B);
+            const uint64_t dek = sdesc(sE - 8192, 16, 1024, SW_128B), dem = sdesc(sE - 8192, 8192, 1024, SW_128B);
+            const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
+            const uint64_t did = sdesc(sID - 8192, 16, 1024, SW_128B), dkp = sdesc(sKP, 16, 1024, SW_128B);
 #pragma unroll
-        for (int s2 = 0; s2 < 4; ++s2) {
-            mma_bf16_ss(tDK, desc_add(ddw, s2 * 32), desc_add(dt1m, s2 * 2048), id1, s2 > 0);
-            mma_bf16_ss(tDK, desc_add(dkm, s2 * 2048), desc_add(dem, s2 * 2048), id2, 1u);
-            mma_bf16_ss(tDK, desc_add(dkm, s2 * 2048), desc_add(dek, s2 * 32), id3, 1u);
+            for (int s2 = 0; s2 < 4; ++s2) {
+                mma_bf16_ss(tDK, desc_add(dt1m, s2 * 2048), desc_add(ddw, s2 * 32), id_mk, s2 > 0);
+                mma_bf16_ss(tDK, desc_add(dek, s2 * 32), desc_add(dkm, s2 * 2048), id_km, 1u);
+                mma_bf16_ss(tDK, desc_add(dem, s2 * 2048), desc_add(dkm, s2 * 2048), id_mm, 1u);
+                mma_bf16_ss(tDK, desc_add(did, s2 * 32), desc_add(dkp, s2 * 32), id_kk, 1u);
+            }
+            mma_commit(&bars[1]);
         }
-        mma_commit(&bars[1]);
     }
-    if (warp == 3) {
+    if (warp == 1) {
         // dG, dlog alpha = reverse within-chunk cumsum (lane l holds positions 63-2l and
         // 62-2l), dalpha = dlog alpha / alpha, dbeta = dbeta12 + dbeta3
         auto dg = [&](int p) {
@@ -1036,35 +1063,19 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             }
         }
     }
-    // dK^T partial from the first gradient kernel (row k = lanerow, this thread's 32 columns)
-    uint4 kpv[4];
-    {
-        const uint4* kp = (const uint4*)(dKp + ((int64_t)krow0 + lanerow) * kC + cb);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) kpv[q] = kp[q];
-    }
+    ok = __syncthreads_and(ok);  // the issuer's load wait is every thread's
     if (ok) ok = mbar_wait(&bars[1], 1, err, 16);
     __syncwarp();
     fence_after_sync();
-    {
-        unsigned char* out = sm + wy::DK;  // K is dead once the last MMA has completed
+    if (!urow) {
+        // dK row a = r (token), columns 64*half .. +64 -> dk tile (K is dead)
+        unsigned char* dkt = sm + wy::DK + half * 8192;
 #pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-            float x[16];
-            tmem_load16f(tDK + lanebase + cb + c0, x);
+        for (int g = 0; g < 2; ++g) {
+            float x[32];
+            tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint4 pk = kpv[c0 / 8 + q];
-                const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    x[8 * q + 2 * e] += bf_lo(pw[e]);
-                    x[8 * q + 2 * e + 1] += bf_hi(pw[e]);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *(bf16*)(out + tile_off(64, cb + c0 + j, lanerow)) = __float2bfloat16_rn(x[j]);
+            for (int q = 0; q < 4; ++q) *(uint4*)(dkt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
         }
     }
     fence_proxy_async();
@@ -1076,6 +1087,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
         }
+        if (!ok) mbar_wait(&bars[2], 0, nullptr, 0);  // the dK partial load may still be in flight
         bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
@@ -1137,20 +1149,19 @@ cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const
 cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const void* alpha, const void* beta,
                               const TcBufs& tb, const TcBwdBufs& bb, void* dk, void* dv, void* dalpha, void* dbeta,
                               cudaStream_t st) {
-    CUtensorMap mk, mv, mdWt, mdU, mT, mdk, mdv;
+    CUtensorMap mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp;
     const int64_t rows = d.NS() * d.NC * kC;
     const int64_t krows = d.NS() * d.NC * kD;
     if (!tmap_bthd(&mk, k, d.B, d.T, d.H, kD) || !tmap_bthd(&mv, v, d.B, d.T, d.H, kD) ||
         !tmap_rows(&mdWt, bb.dWt, krows, kC) || !tmap_rows(&mdU, bb.dU, rows, kD) ||
         !tmap_rows(&mT, tb.T, rows, kC) || !tmap_bthd(&mdk, dk, d.B, d.T, d.H, kD) ||
-        !tmap_bthd(&mdv, dv, d.B, d.T, d.H, kD))
+        !tmap_bthd(&mdv, dv, d.B, d.T, d.H, kD) || !tmap_rows(&mdKp, bb.dKp, krows, kC))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(grad_wy_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wy::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.NS() * d.NC));
-    grad_wy_tc<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, (const bf16*)alpha,
-                                            (const bf16*)beta, tb.G, bb.dKp, bb.dGp, (bf16*)dalpha, (bf16*)dbeta,
-                                            tb.err);
+    grad_wy_tc<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp, (const bf16*)alpha,
+                                            (const bf16*)beta, tb.G, bb.dGp, (bf16*)dalpha, (bf16*)dbeta, tb.err);
     return cudaGetLastError();
 }
 
