@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step and prologue lines")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step, prologue and varlen lines")
     return ap.parse_args()
 
 
@@ -416,6 +416,64 @@ def measure_decode(gdn, dev, stream, args, world):
             "l2": "state 256 MB > L2 (no flush)", "rel_l2_vs_gdn_fwd": consistency}
 
 
+def measure_varlen(gdn, dev, stream, args, world, dense_ms, dense_token_heads):
+    """Times one training step (gdn_varlen_fwd with saved states + gdn_varlen_bwd)
+    on a packed batch with the large training shape's 32768 tokens split into
+    sequences of log-uniform lengths in [128, 8192].  Throughput counts the real
+    tokens; the calls pad every sequence to the longest, so the kernels process
+    S * max_len token rows (reported as pad_factor).  Before timing, the error
+    word is checked and one sequence's output is compared with gdn_fwd on that
+    sequence alone; the oracle checks the varlen calls in the tests."""
+    from gated_delta_rule_19_gb300.inputs import VARLEN_WORKLOADS, make_varlen_inputs, varlen_lengths
+
+    name, spec = next(iter(VARLEN_WORKLOADS.items()))
+    lengths = varlen_lengths(spec["total"], spec["lo"], spec["hi"], spec["seed"])
+    inp = make_varlen_inputs(lengths, spec["H"], spec["K"], spec["V"], spec["dtype"], seed=spec["seed"])
+    d = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in inp.items()}
+    S, total, H = len(lengths), spec["total"], spec["H"]
+    max_len = max(lengths)
+    ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
+    p = gdn.make_problem(S, max_len, H, spec["K"], spec["V"], 64, d["q"].dtype)
+    ws_f = torch.empty(gdn.gdn_varlen_fwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(gdn.gdn_varlen_bwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    saved = torch.empty(gdn.gdn_saved_bytes(p), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(d["v"])
+    sT = torch.empty(S, H, spec["V"], spec["K"], dtype=torch.float32, device=dev)
+    grads = tuple(torch.empty_like(t) for t in ins)
+    ds0 = torch.empty_like(sT)
+
+    def step(check=False):
+        gdn.gdn_varlen_fwd(*ins, d["cu_seqlens"], max_len, None, o=o, final_state=sT, saved=saved,
+                           workspace=ws_f, check=check)
+        gdn.gdn_varlen_bwd(*ins, d["cu_seqlens"], max_len, None, d["d_o"], None, saved=saved, grads=grads,
+                           d_initial_state=ds0, workspace=ws_b, check=check)
+
+    step(check=True)
+    s = max(range(S), key=lambda i: lengths[i])
+    a, e = int(inp["cu_seqlens"][s]), int(inp["cu_seqlens"][s + 1])
+    o1, _, _ = gdn.gdn_fwd(*(t[a:e].unsqueeze(0).clone() for t in ins), None)  # clone: 16-byte aligned
+    torch.cuda.synchronize(dev)
+    rel = float((o[a:e].float() - o1[0].float()).norm() / o1.float().norm())
+    for _ in range(max(3, args.warmup)):
+        step()
+    n = max(10, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+    return {"workload": name, "sequences": S, "tokens": total, "max_len": max_len,
+            "pad_factor": S * max_len / total, "ms_per_step": ms,
+            "token_heads_per_s": world * total * H / (ms / 1e3),
+            "dense_same_tokens_token_heads_per_s": world * dense_token_heads / (dense_ms / 1e3),
+            "step": "gdn_varlen_fwd(saved) + gdn_varlen_bwd",
+            "rel_l2_longest_seq_vs_gdn_fwd": rel}
+
+
 def run_gdn(args, world, rank, local):
     from gated_delta_rule_19_gb300 import _build, gdn
 
@@ -600,6 +658,7 @@ def run_gdn(args, world, rank, local):
     # carried in place between calls
     decode = None if args.no_decode else measure_decode(gdn, dev, stream, args, world)
     prologue = None if args.no_decode else measure_prologue(gdn, dev, stream, args, world, w)
+    varlen = None if args.no_decode else measure_varlen(gdn, dev, stream, args, world, ms_max, w.token_heads)
 
     if rank != 0:
         return
@@ -630,6 +689,7 @@ def run_gdn(args, world, rank, local):
         "e2e": e2e,
         "decode": decode,
         "prologue": prologue,
+        "varlen": varlen,
         "gpu_launches": launches,
         "clocks": clk,
     }

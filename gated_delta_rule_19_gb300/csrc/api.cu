@@ -366,6 +366,201 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
     return GDN_OK;
 }
 
+// ---------------------------------------------------------------- varlen
+// Workspace of the varlen calls: the error word (256 bytes), the inner call's
+// workspace, then the padded tensors.
+namespace {
+struct VarlenLayout {
+    size_t inner, q, k, v, a, b, o, d_o, dq, dk, dv, da, db, total;
+};
+VarlenLayout varlen_layout(const gdn_problem* p, bool bwd) {
+    VarlenLayout L{};
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)p->B * p->T * p->H;
+    size_t off = kAlign;
+    L.inner = off;
+    off += round_up(bwd ? gdn_bwd_workspace_bytes(p) : gdn_fwd_workspace_bytes(p));
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += round_up(bytes);
+        return o;
+    };
+    L.q = take(BTH * p->K * es);
+    L.k = take(BTH * p->K * es);
+    L.v = take(BTH * p->V * es);
+    L.a = take(BTH * es);
+    L.b = take(BTH * es);
+    if (!bwd) {
+        L.o = take(BTH * p->V * es);
+    } else {
+        L.d_o = take(BTH * p->V * es);
+        L.dq = take(BTH * p->K * es);
+        L.dk = take(BTH * p->K * es);
+        L.dv = take(BTH * p->V * es);
+        L.da = take(BTH * es);
+        L.db = take(BTH * es);
+    }
+    L.total = off;
+    return L;
+}
+
+gdn_status check_varlen(const gdn_problem* p, int64_t total, const int32_t* cu, gdn::Dims* d) {
+    gdn_status st = check_problem(p, d);
+    if (st != GDN_OK) return st;
+    if (total < 0 || total > (int64_t)p->B * p->T)
+        return fail(GDN_ERR_INVALID_ARG, "total=%lld must be in [0, B*T] (B sequences of at most T tokens)",
+                    (long long)total);
+    if (!cu && p->B > 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (((uintptr_t)cu) % 4 != 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    return GDN_OK;
+}
+
+uint32_t one_bits(const gdn_problem* p) { return p->dtype == GDN_BF16 ? 0x3F80u : 0x3F800000u; }
+
+// The inner call's error word (bounded waits of the tensor-core kernels) sits at
+// the start of its workspace; the CUDA-core path has none.
+const int* inner_err(const gdn_problem* p, const gdn::Dims& d, const char* inner_ws) {
+    return gdn::tc_fwd_supported(d, in_type(p)) ? (const int*)inner_ws : nullptr;
+}
+}  // namespace
+
+size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    return varlen_layout(p, false).total;
+}
+
+size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    return varlen_layout(p, true).total;
+}
+
+gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu_seqlens, const void* q,
+                          const void* k, const void* v, const void* alpha, const void* beta,
+                          const float* initial_state, void* o, float* final_state, void* saved, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_varlen(p, total, cu_seqlens, &d);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t TH = (size_t)total * d.H;
+    const VarlenLayout L = varlen_layout(p, false);
+    const size_t nstate = (size_t)d.NS() * d.K * d.V * sizeof(float);
+    const Span ins[] = {{q, TH * d.K * es, "q"},         {k, TH * d.K * es, "k"},
+                        {v, TH * d.V * es, "v"},         {alpha, TH * es, "alpha"},
+                        {beta, TH * es, "beta"},         {initial_state, nstate, "initial_state"},
+                        {cu_seqlens, ((size_t)d.B + 1) * 4, "cu_seqlens"}};
+    const Span outs[] = {{o, TH * d.V * es, "o"},
+                         {workspace, L.total, "workspace"},
+                         {final_state, nstate, "final_state"},
+                         {saved, saved ? gdn_saved_bytes(p) : 0, "saved"}};
+    for (int i = 0; i < 5; ++i)
+        if ((st = check_ptr(ins[i], true)) != GDN_OK) return st;
+    for (int i = 0; i < 2; ++i)
+        if ((st = check_ptr(outs[i], true)) != GDN_OK) return st;
+    if (workspace_bytes < L.total)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+    if ((st = check_overlaps(ins, 7, outs, 4, final_state, initial_state)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    char* ws = (char*)workspace;
+    int* err = (int*)ws;
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "error-word reset");
+    if (d.NS() == 0) return GDN_OK;
+    const int kb = d.K * (int)es, vb = d.V * (int)es;
+    const void* srcs[3] = {q, k, v};
+    const size_t dsts[3] = {L.q, L.k, L.v};
+    const int widths[3] = {kb, kb, vb};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = gdn::launch_varlen_rows(d, total, cu_seqlens, widths[i], srcs[i], ws + dsts[i], 0u, false, err,
+                                    nullptr, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, alpha, ws + L.a, one_bits(p), false, err, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, beta, ws + L.b, 0u, false, err, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
+    st = gdn_fwd(p, ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.b, initial_state, ws + L.o, final_state, saved,
+                 ws + L.inner, L.total - L.inner, stream);
+    if (st != GDN_OK) return st;
+    e = gdn::launch_varlen_rows(d, total, cu_seqlens, vb, ws + L.o, o, 0u, true, err, inner_err(p, d, ws + L.inner),
+                                cs);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
+}
+
+gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu_seqlens, const void* q,
+                          const void* k, const void* v, const void* alpha, const void* beta,
+                          const float* initial_state, const void* saved, const void* d_o,
+                          const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
+                          float* d_initial_state, void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_varlen(p, total, cu_seqlens, &d);
+    if (st != GDN_OK) return st;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t TH = (size_t)total * d.H;
+    const VarlenLayout L = varlen_layout(p, true);
+    const size_t nstate = (size_t)d.NS() * d.K * d.V * sizeof(float);
+    const Span ins[] = {{q, TH * d.K * es, "q"},
+                        {k, TH * d.K * es, "k"},
+                        {v, TH * d.V * es, "v"},
+                        {alpha, TH * es, "alpha"},
+                        {beta, TH * es, "beta"},
+                        {d_o, TH * d.V * es, "d_o"},
+                        {initial_state, nstate, "initial_state"},
+                        {d_final_state, nstate, "d_final_state"},
+                        {saved, saved ? gdn_saved_bytes(p) : 0, "saved"},
+                        {cu_seqlens, ((size_t)d.B + 1) * 4, "cu_seqlens"}};
+    const Span outs[] = {{dq, TH * d.K * es, "dq"},
+                         {dk, TH * d.K * es, "dk"},
+                         {dv, TH * d.V * es, "dv"},
+                         {dalpha, TH * es, "dalpha"},
+                         {dbeta, TH * es, "dbeta"},
+                         {workspace, L.total, "workspace"},
+                         {d_initial_state, nstate, "d_initial_state"}};
+    for (int i = 0; i < 6; ++i)
+        if ((st = check_ptr(ins[i], true)) != GDN_OK) return st;
+    for (int i = 0; i < 6; ++i)
+        if ((st = check_ptr(outs[i], true)) != GDN_OK) return st;
+    if (workspace_bytes < L.total)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+    if ((st = check_overlaps(ins, 10, outs, 7, nullptr, nullptr)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    char* ws = (char*)workspace;
+    int* err = (int*)ws;
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "error-word reset");
+    if (d.NS() == 0) return GDN_OK;
+    const int kb = d.K * (int)es, vb = d.V * (int)es;
+    const void* srcs[4] = {q, k, v, d_o};
+    const size_t dsts[4] = {L.q, L.k, L.v, L.d_o};
+    const int widths[4] = {kb, kb, vb, vb};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+        e = gdn::launch_varlen_rows(d, total, cu_seqlens, widths[i], srcs[i], ws + dsts[i], 0u, false, err,
+                                    nullptr, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, alpha, ws + L.a, one_bits(p), false, err, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, beta, ws + L.b, 0u, false, err, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
+    st = gdn_bwd(p, ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.b, initial_state, saved, ws + L.d_o,
+                 d_final_state, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db, d_initial_state,
+                 ws + L.inner, L.total - L.inner, stream);
+    if (st != GDN_OK) return st;
+    const size_t srcs2[3] = {L.dq, L.dk, L.dv};
+    void* dsts2[3] = {dq, dk, dv};
+    const int widths2[3] = {kb, kb, vb};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = gdn::launch_varlen_rows(d, total, cu_seqlens, widths2[i], ws + srcs2[i], dsts2[i], 0u, true, err,
+                                    i == 0 ? inner_err(p, d, ws + L.inner) : nullptr, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, ws + L.da, dalpha, 0u, true, err, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, ws + L.db, dbeta, 0u, true, err, cs);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
+}
+
 gdn_status gdn_prologue_fwd(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* a_logit,
                             const void* b_logit, void* q, void* k, void* alpha, void* beta, void* stream) {
     g_err[0] = 0;

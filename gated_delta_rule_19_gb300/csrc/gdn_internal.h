@@ -140,6 +140,15 @@ int sm_count();
 // Tensor-core forward (tc_fwd.cu).  tc_fwd_supported: shape/dtype test only.
 bool tc_fwd_supported(const Dims& d, InType ty);
 int tc_scan_vt(const Dims& d);
+// Packed variable-length batches (varlen.cu): rows of packed [total, H, width]
+// tensors to and from the padded [S, T, H, width] layout.  `merge` (optional) is
+// ORed into `err` once.
+constexpr int kVarlenBadOffsets = 1 << 30;  // error-word bit: invalid cu_seqlens
+cudaError_t launch_varlen_rows(const Dims& d, int64_t total, const int32_t* cu, int width_bytes, const void* src,
+                               void* dst, uint32_t fill, bool scatter, int* err, const int* merge, cudaStream_t st);
+cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu, int elem_bytes, const void* src,
+                                void* dst, uint32_t fill, bool scatter, int* err, cudaStream_t st);
+
 // q/k L2 normalisation and gate activations, and their backward (prologue.cu).
 cudaError_t launch_prologue_fwd(const Dims& d, InType ty, const void* qr, const void* kr, const void* a,
                                 const void* b, void* q, void* k, void* alpha, void* beta, cudaStream_t st);

@@ -67,6 +67,13 @@ def load_library():
     lib.gdn_prologue_fwd.restype = ctypes.c_int
     lib.gdn_prologue_bwd.argtypes = [P] + [_vp] * 12 + [_vp]
     lib.gdn_prologue_bwd.restype = ctypes.c_int
+    for fn in ("gdn_varlen_fwd_workspace_bytes", "gdn_varlen_bwd_workspace_bytes"):
+        getattr(lib, fn).argtypes = [P]
+        getattr(lib, fn).restype = ctypes.c_size_t
+    lib.gdn_varlen_fwd.argtypes = [P, ctypes.c_int64] + [_vp] * 11 + [ctypes.c_size_t, _vp]
+    lib.gdn_varlen_fwd.restype = ctypes.c_int
+    lib.gdn_varlen_bwd.argtypes = [P, ctypes.c_int64] + [_vp] * 17 + [ctypes.c_size_t, _vp]
+    lib.gdn_varlen_bwd.restype = ctypes.c_int
     lib.gdn_num_kernels.restype = ctypes.c_int
     lib.gdn_kernel_name.argtypes = [ctypes.c_int]
     lib.gdn_kernel_name.restype = ctypes.c_char_p
@@ -85,7 +92,8 @@ EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_works
             "gdn_saved_bytes", "gdn_bwd_workspace_bytes", "gdn_fwd", "gdn_bwd",
             "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
             "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode",
-            "gdn_prologue_fwd", "gdn_prologue_bwd")
+            "gdn_prologue_fwd", "gdn_prologue_bwd", "gdn_varlen_fwd_workspace_bytes",
+            "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -340,6 +348,132 @@ def gdn_prologue_bwd(q_raw, k_raw, a_logit, b_logit, dq, dk, dalpha, dbeta, *, o
                               _ptr(db), _stream_handle(dev, stream))
     _check(st)
     return dqr, dkr, da, db
+
+
+VARLEN_BAD_OFFSETS = 1 << 30  # bit of the varlen workspace's error word
+
+
+def gdn_varlen_fwd_workspace_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_varlen_fwd_workspace_bytes(ctypes.byref(p)))
+
+
+def gdn_varlen_bwd_workspace_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_varlen_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def _varlen_problem(q, v, cu_seqlens, max_len, chunk):
+    if q.dim() != 3:
+        raise GdnError(GDN_ERR_INVALID_ARG, "packed q must be [total, H, K]")
+    total, H, K = q.shape
+    V = v.shape[-1]
+    if cu_seqlens is None or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise GdnError(GDN_ERR_INVALID_ARG, "cu_seqlens must be a 1-d int32 tensor of S+1 offsets")
+    _need(cu_seqlens, "cu_seqlens", tuple(cu_seqlens.shape), torch.int32, q.device)
+    S = cu_seqlens.numel() - 1
+    if max_len is None:  # one device-to-host read; pass max_len to avoid it
+        max_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if S > 0 else 0
+    return make_problem(S, max_len, H, K, V, chunk, q.dtype), (total, S, H, K, V)
+
+
+def _varlen_error(workspace, stream, dev):
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    stream.synchronize()
+    word = int(workspace[:4].view(torch.int32).item())
+    if word & VARLEN_BAD_OFFSETS:
+        raise GdnError(GDN_ERR_INVALID_ARG, "cu_seqlens is invalid (offsets must rise from 0 to total, "
+                       "each length at most max_len)")
+    if word:
+        raise GdnError(GDN_ERR_CUDA, f"kernel error word {word:#x} (a bounded wait gave up)")
+
+
+def gdn_varlen_fwd(q, k, v, alpha, beta, cu_seqlens, max_len=None, initial_state=None, *, chunk: int = 64,
+                   o=None, final_state=True, saved=False, workspace=None, check=False, stream=None):
+    """Forward over S packed sequences of different lengths (``gdn_varlen_fwd``).
+
+    q, k [total,H,K]; v [total,H,V]; alpha, beta [total,H]; sequence s is rows
+    ``cu_seqlens[s]:cu_seqlens[s+1]`` (int32 [S+1] on the device).  ``max_len``
+    bounds every length (computed from cu_seqlens with one device-to-host read
+    if None).  initial_state / final_state are float32 [S,H,V,K] as in
+    :func:`gdn_fwd`.  ``check=True`` synchronises and raises if the kernels
+    found cu_seqlens invalid.  Returns ``(o, final_state or None, saved or None)``;
+    ``saved`` feeds :func:`gdn_varlen_bwd` with the same cu_seqlens and max_len.
+    """
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    p, (total, S, H, K, V) = _varlen_problem(q, v, cu_seqlens, max_len, chunk)
+    dt = q.dtype
+    for t, n, sh in ((k, "k", (total, H, K)), (v, "v", (total, H, V)), (alpha, "alpha", (total, H)),
+                     (beta, "beta", (total, H))):
+        _need(t, n, sh, dt, dev)
+    _need(initial_state, "initial_state", (S, H, V, K), torch.float32, dev)
+    if o is None:
+        o = torch.empty((total, H, V), dtype=dt, device=dev)
+    _need(o, "o", (total, H, V), dt, dev)
+    if final_state is True:
+        final_state = torch.empty((S, H, V, K), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", (S, H, V, K), torch.float32, dev)
+    if saved is True:
+        saved = torch.empty(max(gdn_saved_bytes(p), 1), dtype=torch.uint8, device=dev)
+    elif saved is False:
+        saved = None
+    if workspace is None:
+        workspace = torch.empty(max(gdn_varlen_fwd_workspace_bytes(p), 4), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_varlen_fwd(ctypes.byref(p), total, _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                            _ptr(beta), _ptr(initial_state), _ptr(o), _ptr(final_state), _ptr(saved),
+                            _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
+    _check(st)
+    if check:
+        _varlen_error(workspace, stream, dev)
+    return o, final_state, saved
+
+
+def gdn_varlen_bwd(q, k, v, alpha, beta, cu_seqlens, max_len, initial_state, d_o, d_final_state=None, *,
+                   saved=None, chunk: int = 64, grads=None, d_initial_state=True, workspace=None,
+                   check=False, stream=None):
+    """Backward of :func:`gdn_varlen_fwd` (``gdn_varlen_bwd``), packed layouts as
+    there.  Returns ``(dq, dk, dv, dalpha, dbeta, d_initial_state or None)``."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    p, (total, S, H, K, V) = _varlen_problem(q, v, cu_seqlens, max_len, chunk)
+    dt = q.dtype
+    for t, n, sh in ((k, "k", (total, H, K)), (v, "v", (total, H, V)), (alpha, "alpha", (total, H)),
+                     (beta, "beta", (total, H)), (d_o, "d_o", (total, H, V))):
+        _need(t, n, sh, dt, dev)
+    _need(initial_state, "initial_state", (S, H, V, K), torch.float32, dev)
+    _need(d_final_state, "d_final_state", (S, H, V, K), torch.float32, dev)
+    if saved is not None and saved.numel() * saved.element_size() < gdn_saved_bytes(p):
+        raise GdnError(GDN_ERR_INVALID_ARG, "saved buffer is smaller than gdn_saved_bytes()")
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(alpha),
+                 torch.empty_like(beta))
+    dq, dk, dv, da, db = grads
+    for t, n, sh in ((dq, "dq", (total, H, K)), (dk, "dk", (total, H, K)), (dv, "dv", (total, H, V)),
+                     (da, "dalpha", (total, H)), (db, "dbeta", (total, H))):
+        _need(t, n, sh, dt, dev)
+    if d_initial_state is True:
+        d_initial_state = torch.empty((S, H, V, K), dtype=torch.float32, device=dev)
+    elif d_initial_state is False:
+        d_initial_state = None
+    _need(d_initial_state, "d_initial_state", (S, H, V, K), torch.float32, dev)
+    if workspace is None:
+        workspace = torch.empty(max(gdn_varlen_bwd_workspace_bytes(p), 4), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_varlen_bwd(ctypes.byref(p), total, _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                            _ptr(beta), _ptr(initial_state), _ptr(saved), _ptr(d_o), _ptr(d_final_state),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(db), _ptr(d_initial_state),
+                            _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
+    _check(st)
+    if check:
+        _varlen_error(workspace, stream, dev)
+    return dq, dk, dv, da, db, d_initial_state
 
 
 def gdn_decode(q, k, v, alpha, beta, state, *, o=None, stream=None):

@@ -149,3 +149,61 @@ def make_prologue_inputs(B, T, H, K, dtype="f32", seed=0, scale=3.0, logit_scale
     )
     dt = torch_dtype(dtype)
     return {n: t.to(dt) for n, t in out.items()}
+
+
+def varlen_lengths(total: int, lo: int, hi: int, seed: int) -> list:
+    """Sequence lengths of a packed batch: drawn log-uniformly in [lo, hi] from a
+    CPU generator seeded with ``seed`` until they sum to ``total`` (the last one
+    is cut to fit)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out, left = [], int(total)
+    while left > 0:
+        u = float(torch.rand(1, generator=g))
+        n = int(round(lo * (hi / lo) ** u))
+        n = max(1, min(n, left))
+        out.append(n)
+        left -= n
+    return out
+
+
+# Packed variable-length training batch: the large training shape's 32768 tokens
+# split into sequences whose lengths are drawn log-uniformly in [128, 8192].
+VARLEN_WORKLOADS = {
+    "varlen_bf16_T32768_H6_K128_V128": dict(total=32768, lo=128, hi=8192, seed=6, H=6, K=128, V=128,
+                                            dtype="bf16"),
+}
+
+
+def make_varlen_inputs(lengths, H, K, V, dtype="f32", seed=0, init_std=0.0, dfinal_std=0.0) -> dict:
+    """Packed inputs of len(lengths) sequences with the recipe of
+    :func:`make_inputs` (same distributions and draw order), but with q, k, v,
+    alpha, beta, d_o laid out [total, H, ...] and one initial state and
+    d_final_state per sequence ([S, H, V, K]).  ``cu_seqlens`` (int32 [S+1]) holds
+    the offsets of the sequences."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    S, total = len(lengths), int(sum(lengths))
+    f32 = torch.float32
+    q = torch.randn(total, H, K, generator=g, dtype=f32)
+    k = torch.randn(total, H, K, generator=g, dtype=f32)
+    v = torch.randn(total, H, V, generator=g, dtype=f32)
+    a_logit = torch.randn(total, H, generator=g, dtype=f32)
+    b_logit = torch.randn(total, H, generator=g, dtype=f32)
+    s0 = torch.randn(S, H, V, K, generator=g, dtype=f32)
+    d_o = torch.randn(total, H, V, generator=g, dtype=f32)
+    dsT = torch.randn(S, H, V, K, generator=g, dtype=f32)
+    q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    dt = torch_dtype(dtype)
+    cu = torch.zeros(S + 1, dtype=torch.int32)
+    if S:
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return dict(
+        q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=torch.exp(-F.softplus(a_logit)).to(dt),
+        beta=torch.sigmoid(b_logit).to(dt),
+        initial_state=(s0 * init_std) if init_std > 0 else None,
+        d_o=d_o.to(dt),
+        d_final_state=(dsT * dfinal_std) if dfinal_std > 0 else None,
+        cu_seqlens=cu, lengths=list(lengths),
+    )

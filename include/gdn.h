@@ -182,6 +182,54 @@ gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void*
                             void* stream);
 
 /*
+ * Packed variable-length batches.  "OpenGDN", Scope, lists ragged batches as not
+ * supported; "Sparse Delta Memory: layer and kernels", What the layer computes,
+ * masks the tokens past the end of a stream.  These calls run S = p->B
+ * independent sequences of different lengths stored back to back: sequence s
+ * is rows cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed tensors, and each
+ * sequence has its own initial and final state.  The result for each sequence
+ * equals gdn_fwd / gdn_bwd on that sequence alone (B = 1, T = its length).
+ *
+ *   p            : B = number of sequences S, T = an upper bound on every
+ *                  sequence length (the padded length the kernels run on), H, K,
+ *                  V, chunk, dtype as for gdn_fwd.
+ *   total        : packed rows, 0 <= total <= B*T.
+ *   cu_seqlens   : int32 [S+1] on the device, cu[0] = 0, non-decreasing,
+ *                  cu[S] = total, every length <= T.  It is read by the kernels,
+ *                  not on the host: a violation makes the offending sequences
+ *                  empty (their outputs are not written) and sets bit 30 of the
+ *                  int32 at the start of the workspace; the kernels never touch
+ *                  memory outside the buffers.  That word also carries the
+ *                  tensor-core kernels' bounded-wait bits (1..64); it is 0 when
+ *                  the call succeeded.
+ *   q, k         : packed [total, H, K] dtype;  v, o: [total, H, V];
+ *   alpha, beta  : packed [total, H];  d_o and the gradients: packed, shapes of
+ *                  their inputs.
+ *   initial_state, final_state, d_final_state, d_initial_state : float32
+ *                  [S, H, V, K] or NULL, as for gdn_fwd / gdn_bwd.
+ *   saved        : NULL or gdn_saved_bytes(p) bytes (p as above), filled by
+ *                  gdn_varlen_fwd and read by gdn_varlen_bwd.
+ *   workspace    : gdn_varlen_fwd_workspace_bytes(p) / gdn_varlen_bwd_
+ *                  workspace_bytes(p) bytes.
+ * Method: the sequences are copied into a padded [S, T, H, ...] layout inside the
+ * workspace (rows past a sequence's end get q = k = v = 0, alpha = 1, beta = 0,
+ * which leave the state unchanged and read nothing), the chunk kernels run on it,
+ * and the results are copied back.  Host-side checks as for gdn_fwd; every
+ * pointer 16-byte aligned except cu_seqlens (4 bytes).
+ */
+size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p);
+size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p);
+gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu_seqlens, const void* q,
+                          const void* k, const void* v, const void* alpha, const void* beta,
+                          const float* initial_state, void* o, float* final_state, void* saved, void* workspace,
+                          size_t workspace_bytes, void* stream);
+gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu_seqlens, const void* q,
+                          const void* k, const void* v, const void* alpha, const void* beta,
+                          const float* initial_state, const void* saved, const void* d_o,
+                          const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
+                          float* d_initial_state, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdn_decode -- the recurrent step, for decoding: advances `state` through the
  * call's T tokens (usually 1) and writes their outputs.  It computes exactly the
  * token recurrence of section 1 ("OpenGDN", Core operator reference: a stream

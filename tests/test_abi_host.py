@@ -160,3 +160,54 @@ def test_decode_arguments_rejected_before_launch(lib):
     assert _decode(lib, lib.make_problem(1, 1, 1, 24, 16, 64, 1)) == UNSUP
     # the chunk field is not used by the decode step: with T = 0 nothing launches
     assert _decode(lib, lib.make_problem(1, 0, 1, 16, 16, 7, 1)) == 0
+
+
+def _varlen_fwd(lib, p, total, **over):
+    h = lib.load_library()
+    base = dict(cu=12, q=0, k=1, v=2, alpha=3, beta=4, s0=None, o=5, sT=None, saved=None, ws=6)
+    args = {n: (None if x is None else FAKE + (x << 30)) for n, x in base.items()}
+    args["ws_bytes"] = 1 << 40
+    args.update(over)
+    vp = ctypes.c_void_p
+    order = ("cu", "q", "k", "v", "alpha", "beta", "s0", "o", "sT", "saved", "ws")
+    return h.gdn_varlen_fwd(ctypes.byref(p), total, *[vp(args[n]) for n in order], args["ws_bytes"],
+                            vp(None))
+
+
+def _varlen_bwd(lib, p, total, **over):
+    h = lib.load_library()
+    base = dict(cu=13, q=0, k=1, v=2, alpha=3, beta=4, s0=None, saved=None, do=5, dsT=None, dq=6,
+                dk=7, dv=8, da=9, db=10, ds0=None, ws=11)
+    args = {n: (None if x is None else FAKE + (x << 30)) for n, x in base.items()}
+    args["ws_bytes"] = 1 << 40
+    args.update(over)
+    vp = ctypes.c_void_p
+    order = ("cu", "q", "k", "v", "alpha", "beta", "s0", "saved", "do", "dsT", "dq", "dk", "dv",
+             "da", "db", "ds0", "ws")
+    return h.gdn_varlen_bwd(ctypes.byref(p), total, *[vp(args[n]) for n in order], args["ws_bytes"],
+                            vp(None))
+
+
+def test_varlen_arguments_rejected_before_launch(lib):
+    INVALID, UNSUP, WS = 1, 2, 3
+    p = lib.make_problem(3, 100, 2, 64, 64, 64, 1)  # 3 sequences of at most 100 tokens
+    assert _varlen_fwd(lib, p, 301) == INVALID  # more rows than 3 sequences can hold
+    assert "total" in lib.gdn_last_error()
+    assert _varlen_fwd(lib, p, -1) == INVALID
+    assert _varlen_fwd(lib, p, 200, cu=None) == INVALID
+    assert "cu_seqlens" in lib.gdn_last_error()
+    assert _varlen_fwd(lib, p, 200, cu=FAKE + (12 << 30) + 2) == INVALID  # not 4-byte aligned
+    assert _varlen_fwd(lib, p, 200, q=None) == INVALID
+    assert _varlen_fwd(lib, p, 200, ws_bytes=1024) == WS
+    need = lib.load_library().gdn_varlen_fwd_workspace_bytes(ctypes.byref(p))
+    assert need > lib.load_library().gdn_fwd_workspace_bytes(ctypes.byref(p))
+    assert _varlen_fwd(lib, p, 200, ws_bytes=need - 1) == WS
+    assert _varlen_fwd(lib, p, 200, o=FAKE + 256) == INVALID          # o overlaps q
+    assert _varlen_fwd(lib, p, 200, cu=FAKE + (5 << 30) + 64) == INVALID  # cu inside o
+    assert _varlen_fwd(lib, p, 200, sT=FAKE + (5 << 30)) == INVALID   # final state is o
+    assert _varlen_fwd(lib, lib.make_problem(3, 100, 2, 24, 64, 64, 1), 200) == UNSUP
+    assert _varlen_bwd(lib, p, 200, do=None) == INVALID
+    assert _varlen_bwd(lib, p, 200, dv=FAKE) == INVALID               # dv overlaps q
+    assert _varlen_bwd(lib, p, 200, ds0=FAKE + (6 << 30)) == INVALID  # d_initial_state is dq
+    assert _varlen_bwd(lib, p, 200, ws_bytes=0) == WS
+    assert _varlen_bwd(lib, p, 301) == INVALID

@@ -1,0 +1,181 @@
+"""GPU parity of the packed variable-length calls (gdn_varlen_fwd / gdn_varlen_bwd).
+
+Each sequence of a packed batch is an independent stream with its own initial
+state, so its outputs and gradients must equal the float64 oracle run on that
+sequence alone ("OpenGDN", Scope: ragged batches; "Sparse Delta Memory: layer and
+kernels", What the layer computes: tokens past the end of a stream are masked).
+Tolerances as for gdn_fwd / gdn_bwd: relative L2 1e-5 for fp32 inputs; 2e-2 for
+bf16 outputs and states, 3e-2 for bf16 gradients."""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_19_gb300 import gdn
+from gated_delta_rule_19_gb300.inputs import custom, make_inputs, make_varlen_inputs
+from gdn_testutil import TOL, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dq", "dk", "dv", "dalpha", "dbeta")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_delta_rule_19_gb300 import _build
+
+    _build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _cuda(inp):
+    return {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in inp.items()}
+
+
+def _run_varlen(d, chunk, max_len=None, backward=True):
+    o, sT, saved = gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], max_len,
+                                      d["initial_state"], chunk=chunk, saved=backward, check=True)
+    out = dict(o=o, final_state=sT)
+    if backward:
+        g = gdn.gdn_varlen_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], max_len,
+                               d["initial_state"], d["d_o"], d["d_final_state"], saved=saved, chunk=chunk,
+                               check=True)
+        out.update(zip(GRADS + ("d_initial_state",), g))
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_seq(oracle_mod, inp, s):
+    """The oracle on sequence s alone (B = 1, T = its length)."""
+    a, e = int(inp["cu_seqlens"][s]), int(inp["cu_seqlens"][s + 1])
+    seq = {n: to_np(inp[n][a:e])[None] for n in ("q", "k", "v", "alpha", "beta", "d_o")}
+    s0 = None if inp["initial_state"] is None else to_np(inp["initial_state"][s:s + 1])
+    dsT = None if inp["d_final_state"] is None else to_np(inp["d_final_state"][s:s + 1])
+    o, sT = oracle_mod.gated_delta_fwd(seq["q"], seq["k"], seq["v"], seq["alpha"], seq["beta"], s0)
+    g = oracle_mod.gated_delta_bwd(seq["q"], seq["k"], seq["v"], seq["alpha"], seq["beta"], s0, seq["d_o"], dsT)
+    return dict(o=o[0], final_state=sT[0], d_initial_state=g["d_initial_state"][0],
+                **{n: g[n][0] for n in GRADS})
+
+
+CASES = [
+    # lengths (one empty, ragged tails, exact chunks, several tiles), H, K, V, chunk, dtype
+    ([1, 63, 64, 65, 200, 0, 130], 2, 64, 64, 64, "bf16"),
+    ([64, 1, 128, 191], 2, 128, 128, 64, "bf16"),
+    ([5, 17, 33, 0, 48], 3, 32, 32, 16, "f32"),
+    ([70, 9, 100], 1, 16, 64, 32, "f32"),
+    ([129, 2], 2, 128, 128, 64, "f32"),
+]
+
+
+@pytest.mark.parametrize("lengths,H,K,V,chunk,dtype", CASES)
+def test_varlen_matches_oracle_per_sequence(oracle_mod, lengths, H, K, V, chunk, dtype):
+    inp = make_varlen_inputs(lengths, H, K, V, dtype, seed=700 + len(lengths) + K, init_std=0.3,
+                             dfinal_std=0.05)
+    got = _run_varlen(_cuda(inp), chunk)
+    tol = TOL[dtype]
+    cu = inp["cu_seqlens"].tolist()
+    bad = []
+    ref_all = {n: [] for n in ("o",) + GRADS}
+    for s in range(len(lengths)):
+        ref = _oracle_seq(oracle_mod, inp, s)
+        a, e = cu[s], cu[s + 1]
+        for n in ("final_state", "d_initial_state"):
+            err = rel_l2(to_np(got[n][s]), ref[n])
+            if err > tol["out" if n == "final_state" else "grad"]:
+                bad.append(f"seq {s} {n}: {err:.2e}")
+        for n in ("o",) + GRADS:
+            ref_all[n].append(ref[n])
+            # per sequence where the sequence has enough elements for a relative
+            # norm to mean something; the packed tensors are compared as a whole
+            if e - a >= 16:
+                err = rel_l2(to_np(got[n][a:e]), ref[n])
+                if err > tol["out" if n == "o" else "grad"]:
+                    bad.append(f"seq {s} {n}: {err:.2e}")
+    for n in ("o",) + GRADS:
+        err = rel_l2(to_np(got[n]), np.concatenate(ref_all[n], 0))
+        if err > tol["out" if n == "o" else "grad"]:
+            bad.append(f"packed {n}: {err:.2e}")
+    assert not bad, "; ".join(bad)
+
+
+def test_varlen_short_sequences_equal_their_own_dense_runs():
+    """Each sequence of a packed batch, run alone through gdn_fwd / gdn_bwd (B = 1,
+    T = its length), gives the same outputs and gradients: the varlen calls only
+    move rows, so short sequences whose gradients are too small for a relative
+    norm are checked against the dense path here."""
+    lengths = [1, 2, 3, 7, 15, 64, 65]
+    inp = make_varlen_inputs(lengths, 2, 64, 64, "f32", seed=41, init_std=0.3, dfinal_std=0.05)
+    d = _cuda(inp)
+    got = _run_varlen(d, 64)
+    cu = inp["cu_seqlens"].tolist()
+    for s in range(len(lengths)):
+        a, e = cu[s], cu[s + 1]
+        seq = {n: d[n][a:e].unsqueeze(0).clone() for n in ("q", "k", "v", "alpha", "beta", "d_o")}
+        s0 = d["initial_state"][s:s + 1].clone()
+        dsT = d["d_final_state"][s:s + 1].clone()
+        o, sT, saved = gdn.gdn_fwd(seq["q"], seq["k"], seq["v"], seq["alpha"], seq["beta"], s0, saved=True)
+        g = gdn.gdn_bwd(seq["q"], seq["k"], seq["v"], seq["alpha"], seq["beta"], s0, seq["d_o"], dsT,
+                        saved=saved)
+        torch.cuda.synchronize()
+        pairs = [(got["o"][a:e], o[0]), (got["final_state"][s], sT[0]),
+                 (got["d_initial_state"][s], g[5][0])]
+        pairs += [(got[n][a:e], g[i][0]) for i, n in enumerate(GRADS)]
+        for x, y in pairs:
+            torch.testing.assert_close(x, y, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_varlen_equal_lengths_bitwise_equal_to_dense(dtype):
+    """S sequences of one length T are the dense [S, T] batch: the padded layout
+    is then exactly the dense one, so every result is bit-identical."""
+    S, T, H, K, V = 3, 130, 2, 64, 64
+    w = custom(B=S, T=T, H=H, K=K, V=V, chunk=64, dtype=dtype, seed=42, init_std=0.2, dfinal_std=0.05)
+    dense = {n: (t.cuda() if t is not None else None) for n, t in make_inputs(w).items()}
+    o, sT, saved = gdn.gdn_fwd(dense["q"], dense["k"], dense["v"], dense["alpha"], dense["beta"],
+                               dense["initial_state"], saved=True)
+    g = gdn.gdn_bwd(dense["q"], dense["k"], dense["v"], dense["alpha"], dense["beta"], dense["initial_state"],
+                    dense["d_o"], dense["d_final_state"], saved=saved)
+    packed = {n: dense[n].reshape(S * T, *dense[n].shape[2:]) for n in ("q", "k", "v", "alpha", "beta", "d_o")}
+    packed.update(initial_state=dense["initial_state"], d_final_state=dense["d_final_state"],
+                  cu_seqlens=torch.arange(0, S * T + 1, T, dtype=torch.int32, device="cuda"))
+    got = _run_varlen(packed, 64, max_len=T)
+    assert torch.equal(got["o"], o.reshape(S * T, H, V))
+    assert torch.equal(got["final_state"], sT)
+    assert torch.equal(got["d_initial_state"], g[5])
+    for i, n in enumerate(GRADS):
+        assert torch.equal(got[n], g[i].reshape(got[n].shape)), n
+
+
+def test_varlen_empty_batch_and_empty_sequences():
+    """No tokens at all: outputs are empty, final state = initial state, and
+    d_initial_state = d_final_state."""
+    H, K, V = 2, 32, 32
+    inp = make_varlen_inputs([0, 0], H, K, V, "f32", seed=43, init_std=0.5, dfinal_std=0.5)
+    got = _run_varlen(_cuda(inp), 64, max_len=0)
+    assert got["o"].shape == (0, H, V)
+    assert torch.equal(got["final_state"].cpu(), inp["initial_state"])
+    assert torch.equal(got["d_initial_state"].cpu(), inp["d_final_state"])
+
+
+@pytest.mark.parametrize("cu,total,max_len", [
+    ([0, 50, 40, 100], 100, 64),   # decreasing offsets
+    ([0, 50, 100], 120, 64),       # the offsets do not reach total
+    ([0, 10, 100], 100, 64),       # a sequence longer than max_len
+    ([3, 50, 100], 100, 64),       # does not start at row 0
+])
+def test_varlen_invalid_offsets_are_flagged(cu, total, max_len):
+    """An invalid cu_seqlens (read only on the device) sets the error bit; the
+    kernels stay inside the buffers and the binding raises with check=True."""
+    H, K, V = 2, 32, 32
+    inp = make_varlen_inputs([total], H, K, V, "f32", seed=44)
+    d = _cuda(inp)
+    d["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    with pytest.raises(gdn.GdnError, match="cu_seqlens"):
+        gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], max_len,
+                           None, check=True)
+    with pytest.raises(gdn.GdnError, match="cu_seqlens"):
+        gdn.gdn_varlen_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], max_len, None,
+                           d["d_o"], None, check=True)
+    # the context is still usable: a valid call afterwards succeeds
+    d["cu_seqlens"] = torch.tensor([0, total], dtype=torch.int32, device="cuda")
+    gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], None, None, check=True)
+    torch.cuda.synchronize()
