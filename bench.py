@@ -420,8 +420,10 @@ def measure_varlen(gdn, dev, stream, args, world, dense_ms, dense_token_heads):
     """Times one training step (gdn_varlen_fwd with saved states + gdn_varlen_bwd)
     on a packed batch with the large training shape's 32768 tokens split into
     sequences of log-uniform lengths in [128, 8192].  Throughput counts the real
-    tokens; the calls pad every sequence to the longest, so the kernels process
-    S * max_len token rows (reported as pad_factor).  Before timing, the error
+    tokens; every sequence starts a new chunk, so the kernels process
+    sum(ceil(len / 64) * 64) token rows per head (rows_processed_per_token), and
+    each scan walks its own sequence's chunks, so the longest sequence is the
+    critical path.  Before timing, the error
     word is checked and one sequence's output is compared with gdn_fwd on that
     sequence alone; the oracle checks the varlen calls in the tests."""
     from gated_delta_rule_19_gb300.inputs import VARLEN_WORKLOADS, make_varlen_inputs, varlen_lengths
@@ -434,9 +436,9 @@ def measure_varlen(gdn, dev, stream, args, world, dense_ms, dense_token_heads):
     max_len = max(lengths)
     ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
     p = gdn.make_problem(S, max_len, H, spec["K"], spec["V"], 64, d["q"].dtype)
-    ws_f = torch.empty(gdn.gdn_varlen_fwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(gdn.gdn_varlen_bwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
-    saved = torch.empty(gdn.gdn_saved_bytes(p), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(gdn.gdn_varlen_fwd_workspace_bytes(p, total), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(gdn.gdn_varlen_bwd_workspace_bytes(p, total), dtype=torch.uint8, device=dev)
+    saved = torch.empty(gdn.gdn_varlen_saved_bytes(p, total), dtype=torch.uint8, device=dev)
     o = torch.empty_like(d["v"])
     sT = torch.empty(S, H, spec["V"], spec["K"], dtype=torch.float32, device=dev)
     grads = tuple(torch.empty_like(t) for t in ins)
@@ -460,17 +462,24 @@ def measure_varlen(gdn, dev, stream, args, world, dense_ms, dense_token_heads):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
+    gdn.gdn_profiler_start(32 * n + 32)
     e0.record(stream)
     for _ in range(n):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    gdn.gdn_profiler_stop()
+    split = {k: round(t / n * 1e3, 1) for k, (_, t) in gdn.gdn_profiler_summary().items()}
     ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+    C = 64
+    flat_rows = sum((L + C - 1) // C * C for L in lengths)
     return {"workload": name, "sequences": S, "tokens": total, "max_len": max_len,
-            "pad_factor": S * max_len / total, "ms_per_step": ms,
+            "layout": "flat chunk rows, each sequence starts a chunk",
+            "rows_processed_per_token": flat_rows / total, "ms_per_step": ms,
             "token_heads_per_s": world * total * H / (ms / 1e3),
             "dense_same_tokens_token_heads_per_s": world * dense_token_heads / (dense_ms / 1e3),
-            "step": "gdn_varlen_fwd(saved) + gdn_varlen_bwd",
+            "step": "gdn_varlen_fwd(saved) + gdn_varlen_bwd", "us_per_step_by_kernel": split,
+            "critical_path": f"the longest sequence's scan: {(max_len + C - 1) // C} chunks",
             "rel_l2_longest_seq_vs_gdn_fwd": rel}
 
 

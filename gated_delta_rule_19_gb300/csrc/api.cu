@@ -213,7 +213,7 @@ const char* const kKernelNames[gdn::KID_COUNT] = {
     "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel",
     "prep_fwd_tc", "scan_fwd_tc", "prep_fwd_tc(bwd)", "scan_fwd_tc(state-only)",
     "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc", "decode_kernel", "prologue_fwd_kernel",
-    "prologue_bwd_kernel"};
+    "prologue_bwd_kernel", "varlen_offsets", "varlen_gather", "varlen_scatter"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -224,6 +224,72 @@ cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
     cudaError_t e = launch();
     cudaEventRecord(g_prof.ev[2 * i + 1], st);
     return e;
+}
+
+// The tensor-core forward on dims d: the chunk kernel, then the scan.  The
+// workspace holds carve_tc(d) and `saved` (or NULL) carve_tc_saved(d); `sq`
+// (or NULL) runs packed sequences on the flat chunk layout.
+gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* alpha,
+                      const void* beta, const float* initial_state, void* o, float* final_state, void* saved,
+                      void* workspace, const gdn::SeqMap* sq, cudaStream_t cs) {
+    Carver cv{(char*)workspace};
+    gdn::TcBufs tb;
+    __nv_bfloat16* states = nullptr;
+    carve_tc(d, cv, &tb);
+    if (saved) {  // keep the chunk results for the backward
+        Carver sv{(char*)saved};
+        carve_tc_saved(d, sv, &states, &tb);
+    }
+    cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
+    e = timed(gdn::KID_PREP_TC, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
+    e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
+        return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state, states, cs, sq);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
+    return GDN_OK;
+}
+
+// The tensor-core backward on dims d (same conventions as run_fwd_tc).
+gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* alpha,
+                      const void* beta, const float* initial_state, const void* saved, const void* d_o,
+                      const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
+                      float* d_initial_state, void* workspace, const gdn::SeqMap* sq, cudaStream_t cs) {
+    Carver cv{(char*)workspace};
+    gdn::TcBufs tb;
+    gdn::TcBwdBufs tbb;
+    carve_tc_bwd(d, cv, &tb, &tbb, saved == nullptr);
+    const __nv_bfloat16* states = tbb.states;
+    if (saved) {  // reuse the forward's states and chunk results
+        Carver sv{(char*)const_cast<void*>(saved)};
+        __nv_bfloat16* st = nullptr;
+        int* err = tb.err;
+        carve_tc_saved(d, sv, &st, &tb);
+        tb.err = err;
+        states = st;
+    }
+    cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
+    if (!saved) {
+        e = timed(gdn::KID_PREP_TC_BWD, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
+        e = timed(gdn::KID_STATE_TC, cs, [&] {
+            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, nullptr, nullptr, tbb.states, cs, sq);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core state recompute");
+    }
+    e = timed(gdn::KID_SCAN_BWD_TC, cs, [&] {
+        return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, d_final_state, tbb, d_initial_state, cs, sq);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core reverse scan");
+    e = timed(gdn::KID_GRAD_QK_TC, cs, [&] { return gdn::launch_grad_qk_tc(d, q, k, d_o, tb, states, tbb, dq, cs); });
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (q, k)");
+    e = timed(gdn::KID_GRAD_WY_TC, cs, [&] {
+        return gdn::launch_grad_wy_tc(d, k, v, alpha, beta, tb, tbb, dk, dv, dalpha, dbeta, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (WY)");
+    return GDN_OK;
 }
 
 }  // namespace
@@ -330,28 +396,9 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
         return e == cudaSuccess ? GDN_OK : cuda_fail(e, "empty-sequence state copy");
     }
     const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    if (gdn::tc_fwd_supported(d, ty))
+        return run_fwd_tc(d, q, k, v, alpha, beta, initial_state, o, final_state, saved, workspace, nullptr, cs);
     Carver cv{(char*)workspace};
-    if (gdn::tc_fwd_supported(d, ty)) {
-        gdn::TcBufs tb;
-        __nv_bfloat16* states = nullptr;
-        carve_tc(d, cv, &tb);
-        if (saved) {  // keep the chunk results for the backward
-            Carver sv{(char*)saved};
-            carve_tc_saved(d, sv, &states, &tb);
-        }
-        cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
-        if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
-        e = timed(gdn::KID_PREP_TC, cs, [&] {
-            return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
-        e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
-            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state, states,
-                                           cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
-        return GDN_OK;
-    }
     gdn::ChunkBufs cb;
     carve_chunk(d, cv, &cb, false);
     cudaError_t e = timed(gdn::KID_PREP_FWD, cs, [&] {
@@ -367,73 +414,141 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
 }
 
 // ---------------------------------------------------------------- varlen
-// Workspace of the varlen calls: the error word (256 bytes), the inner call's
-// workspace, then the padded tensors.
+// Packed sequences run on one of two layouts inside the workspace:
+//  * flat (tensor-core path): one row of chunks per head (B = 1), every sequence
+//    starting a new chunk: nc_max = ceil(total / C) + S chunks bound the
+//    sum of ceil(len_s / C); the scans take a SeqMap;
+//  * padded (other shapes): [S, max_len] streams, gdn_fwd / gdn_bwd as they are.
+// Workspace: the error word, chunk_off, the inner workspace, the laid-out tensors.
 namespace {
-struct VarlenLayout {
-    size_t inner, q, k, v, a, b, o, d_o, dq, dk, dv, da, db, total;
+struct VarlenPlan {
+    bool flat;
+    gdn::Dims pd;  // the problem the chunk kernels run on
+    size_t off, inner, q, k, v, a, b, o, d_o, dq, dk, dv, da, db, total;
+    // `saved` of the flat layout: chunk_off and the laid-out inputs (the backward
+    // reads them instead of gathering again), then the chunk kernels' own.
+    size_t s_off, s_q, s_k, s_v, s_a, s_b, s_tc, saved;
 };
-VarlenLayout varlen_layout(const gdn_problem* p, bool bwd) {
-    VarlenLayout L{};
+
+gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan* L) {
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (total < 0 || total > (int64_t)p->B * p->T)
+        return fail(GDN_ERR_INVALID_ARG, "total=%lld must be in [0, B*T] (B sequences of at most T tokens)",
+                    (long long)total);
+    *L = VarlenPlan{};
+    L->flat = gdn::tc_fwd_supported(d, in_type(p));
+    L->pd = d;
+    if (L->flat) {
+        const int64_t nc_max = (total + d.C - 1) / d.C + d.B;
+        if (nc_max * d.C > ((int64_t)1 << 30))
+            return fail(GDN_ERR_UNSUPPORTED, "total=%lld with B=%d sequences exceeds 2^30 chunk rows",
+                        (long long)total, d.B);
+        L->pd.B = 1;
+        L->pd.NC = (int)nc_max;
+        L->pd.T = (int)(nc_max * d.C);
+    }
+    const gdn::Dims& q = L->pd;
     const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
-    const size_t BTH = (size_t)p->B * p->T * p->H;
+    const size_t BTH = (size_t)q.B * q.T * q.H;
+    size_t inner_bytes = 0;
+    Carver cv{nullptr};
+    if (q.NS() * q.NC > 0) {
+        if (L->flat) {
+            gdn::TcBufs tb;
+            gdn::TcBwdBufs tbb;
+            inner_bytes = bwd ? carve_tc_bwd(q, cv, &tb, &tbb, true) : carve_tc(q, cv, &tb);
+        } else {
+            inner_bytes = bwd ? gdn_bwd_workspace_bytes(p) : gdn_fwd_workspace_bytes(p);
+        }
+    }
+    if (L->flat) {
+        Carver sv{nullptr};
+        __nv_bfloat16* states;
+        gdn::TcBufs tb;
+        const size_t tc = q.NS() * q.NC > 0 ? carve_tc_saved(q, sv, &states, &tb) : 0;
+        size_t so = 0;
+        auto stake = [&](size_t bytes) {
+            const size_t o = so;
+            so += round_up(bytes);
+            return o;
+        };
+        L->s_off = stake(((size_t)d.B + 1) * sizeof(int));
+        L->s_q = stake(BTH * q.K * es);
+        L->s_k = stake(BTH * q.K * es);
+        L->s_v = stake(BTH * q.V * es);
+        L->s_a = stake(BTH * es);
+        L->s_b = stake(BTH * es);
+        L->s_tc = stake(tc);
+        L->saved = so;
+    } else {
+        L->saved = gdn_saved_bytes(p);
+    }
     size_t off = kAlign;
-    L.inner = off;
-    off += round_up(bwd ? gdn_bwd_workspace_bytes(p) : gdn_fwd_workspace_bytes(p));
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off += round_up(bytes);
         return o;
     };
-    L.q = take(BTH * p->K * es);
-    L.k = take(BTH * p->K * es);
-    L.v = take(BTH * p->V * es);
-    L.a = take(BTH * es);
-    L.b = take(BTH * es);
+    L->off = take(((size_t)d.B + 1) * sizeof(int));
+    L->inner = take(inner_bytes);
+    L->q = take(BTH * q.K * es);
+    L->k = take(BTH * q.K * es);
+    L->v = take(BTH * q.V * es);
+    L->a = take(BTH * es);
+    L->b = take(BTH * es);
     if (!bwd) {
-        L.o = take(BTH * p->V * es);
+        L->o = take(BTH * q.V * es);
     } else {
-        L.d_o = take(BTH * p->V * es);
-        L.dq = take(BTH * p->K * es);
-        L.dk = take(BTH * p->K * es);
-        L.dv = take(BTH * p->V * es);
-        L.da = take(BTH * es);
-        L.db = take(BTH * es);
+        L->d_o = take(BTH * q.V * es);
+        L->dq = take(BTH * q.K * es);
+        L->dk = take(BTH * q.K * es);
+        L->dv = take(BTH * q.V * es);
+        L->da = take(BTH * es);
+        L->db = take(BTH * es);
     }
-    L.total = off;
-    return L;
-}
-
-gdn_status check_varlen(const gdn_problem* p, int64_t total, const int32_t* cu, gdn::Dims* d) {
-    gdn_status st = check_problem(p, d);
-    if (st != GDN_OK) return st;
-    if (total < 0 || total > (int64_t)p->B * p->T)
-        return fail(GDN_ERR_INVALID_ARG, "total=%lld must be in [0, B*T] (B sequences of at most T tokens)",
-                    (long long)total);
-    if (!cu && p->B > 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
-    if (((uintptr_t)cu) % 4 != 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    L->total = off;
     return GDN_OK;
 }
 
 uint32_t one_bits(const gdn_problem* p) { return p->dtype == GDN_BF16 ? 0x3F80u : 0x3F800000u; }
 
-// The inner call's error word (bounded waits of the tensor-core kernels) sits at
-// the start of its workspace; the CUDA-core path has none.
-const int* inner_err(const gdn_problem* p, const gdn::Dims& d, const char* inner_ws) {
-    return gdn::tc_fwd_supported(d, in_type(p)) ? (const int*)inner_ws : nullptr;
+// The padded layout: packed -> laid out (gather) or back (scatter) for one tensor
+// of `width` bytes per (token, head).  `merge` (row moves only) is ORed into the
+// error word.
+cudaError_t varlen_move(const VarlenPlan& L, const gdn_problem* p, int64_t total, const int32_t* cu, char* ws,
+                        int width, const void* src, void* dst, uint32_t fill, bool scatter, const int* merge,
+                        cudaStream_t cs) {
+    int* err = (int*)ws;
+    const gdn::Dims& d = L.pd;
+    return timed(scatter ? gdn::KID_VARLEN_SCATTER : gdn::KID_VARLEN_GATHER, cs, [&] {
+        if (width % 16 == 0)
+            return gdn::launch_varlen_rows(d, total, cu, width, src, dst, fill, scatter, err, merge, cs);
+        return gdn::launch_varlen_elems(d, total, cu, width, src, dst, fill, scatter, err, cs);
+    });
+}
+
+gdn_status check_cu(const gdn_problem* p, const int32_t* cu) {
+    if (!cu && p->B > 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (((uintptr_t)cu) % 4 != 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    return GDN_OK;
 }
 }  // namespace
 
-size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p) {
-    gdn::Dims d{};
-    if (check_problem(p, &d) != GDN_OK) return 0;
-    return varlen_layout(p, false).total;
+size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p, int64_t total) {
+    VarlenPlan L;
+    return varlen_plan(p, total, false, &L) == GDN_OK ? L.total : 0;
 }
 
-size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p) {
-    gdn::Dims d{};
-    if (check_problem(p, &d) != GDN_OK) return 0;
-    return varlen_layout(p, true).total;
+size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p, int64_t total) {
+    VarlenPlan L;
+    return varlen_plan(p, total, true, &L) == GDN_OK ? L.total : 0;
+}
+
+size_t gdn_varlen_saved_bytes(const gdn_problem* p, int64_t total) {
+    VarlenPlan L;
+    return varlen_plan(p, total, false, &L) == GDN_OK ? L.saved : 0;
 }
 
 gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu_seqlens, const void* q,
@@ -441,51 +556,78 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu
                           const float* initial_state, void* o, float* final_state, void* saved, void* workspace,
                           size_t workspace_bytes, void* stream) {
     g_err[0] = 0;
-    gdn::Dims d{};
-    gdn_status st = check_varlen(p, total, cu_seqlens, &d);
+    VarlenPlan L;
+    gdn_status st = varlen_plan(p, total, false, &L);
     if (st != GDN_OK) return st;
+    if ((st = check_cu(p, cu_seqlens)) != GDN_OK) return st;
     const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
-    const size_t TH = (size_t)total * d.H;
-    const VarlenLayout L = varlen_layout(p, false);
-    const size_t nstate = (size_t)d.NS() * d.K * d.V * sizeof(float);
-    const Span ins[] = {{q, TH * d.K * es, "q"},         {k, TH * d.K * es, "k"},
-                        {v, TH * d.V * es, "v"},         {alpha, TH * es, "alpha"},
+    const size_t TH = (size_t)total * p->H;
+    const size_t nstate = (size_t)p->B * p->H * p->K * p->V * sizeof(float);
+    const Span ins[] = {{q, TH * p->K * es, "q"},         {k, TH * p->K * es, "k"},
+                        {v, TH * p->V * es, "v"},         {alpha, TH * es, "alpha"},
                         {beta, TH * es, "beta"},         {initial_state, nstate, "initial_state"},
-                        {cu_seqlens, ((size_t)d.B + 1) * 4, "cu_seqlens"}};
-    const Span outs[] = {{o, TH * d.V * es, "o"},
+                        {cu_seqlens, ((size_t)p->B + 1) * 4, "cu_seqlens"}};
+    const Span outs[] = {{o, TH * p->V * es, "o"},
                          {workspace, L.total, "workspace"},
                          {final_state, nstate, "final_state"},
-                         {saved, saved ? gdn_saved_bytes(p) : 0, "saved"}};
-    for (int i = 0; i < 5; ++i)
-        if ((st = check_ptr(ins[i], true)) != GDN_OK) return st;
-    for (int i = 0; i < 2; ++i)
-        if ((st = check_ptr(outs[i], true)) != GDN_OK) return st;
+                         {saved, L.saved, "saved"}};
+    for (int i = 0; i < 6; ++i)
+        if ((st = check_ptr(ins[i], i != 5)) != GDN_OK) return st;
+    for (int i = 0; i < 4; ++i)
+        if ((st = check_ptr(outs[i], i < 2)) != GDN_OK) return st;
     if (workspace_bytes < L.total)
         return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
     if ((st = check_overlaps(ins, 7, outs, 4, final_state, initial_state)) != GDN_OK) return st;
     cudaStream_t cs = (cudaStream_t)stream;
     char* ws = (char*)workspace;
-    int* err = (int*)ws;
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), cs);
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-word reset");
-    if (d.NS() == 0) return GDN_OK;
-    const int kb = d.K * (int)es, vb = d.V * (int)es;
-    const void* srcs[3] = {q, k, v};
-    const size_t dsts[3] = {L.q, L.k, L.v};
-    const int widths[3] = {kb, kb, vb};
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-        e = gdn::launch_varlen_rows(d, total, cu_seqlens, widths[i], srcs[i], ws + dsts[i], 0u, false, err,
-                                    nullptr, cs);
-    if (e == cudaSuccess)
-        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, alpha, ws + L.a, one_bits(p), false, err, cs);
-    if (e == cudaSuccess)
-        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, beta, ws + L.b, 0u, false, err, cs);
+    if (p->B * p->H == 0) return GDN_OK;
+    const int S = (int)p->B, kb = (int)(p->K * es), vb = (int)(p->V * es);
+    if (L.flat) {
+        // laid-out inputs and chunk_off go to `saved` when given (the backward reuses them)
+        char* in = saved ? (char*)saved : ws;
+        int* off = (int*)(saved ? in + L.s_off : ws + L.off);
+        char* lq = in + (saved ? L.s_q : L.q);
+        char* lk = in + (saved ? L.s_k : L.k);
+        char* lv = in + (saved ? L.s_v : L.v);
+        char* la = in + (saved ? L.s_a : L.a);
+        char* lb = in + (saved ? L.s_b : L.b);
+        const gdn::Dims& fd = L.pd;
+        e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
+            return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, off, (int*)ws, cs);
+        });
+        gdn::FlatMoves m{5, {q, k, v, alpha, beta}, {lq, lk, lv, la, lb},
+                         {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)(p->H * es), (int)(p->H * es)},
+                         {16, 16, 16, (int)es, (int)es}, {0u, 0u, 0u, one_bits(p), 0u}};
+        if (e == cudaSuccess)
+            e = timed(gdn::KID_VARLEN_GATHER, cs, [&] {
+                return gdn::launch_varlen_flat(m, S, fd.C, fd.NC, total, cu_seqlens, off, false, nullptr, (int*)ws,
+                                               cs);
+            });
+        if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
+        const gdn::SeqMap sq{off, S};
+        st = run_fwd_tc(fd, lq, lk, lv, la, lb, initial_state, ws + L.o, final_state,
+                        saved ? (char*)saved + L.s_tc : nullptr, ws + L.inner, &sq, cs);
+        if (st != GDN_OK) return st;
+        gdn::FlatMoves mo{1, {ws + L.o}, {o}, {(int)p->H * vb}, {16}, {0u}};
+        e = timed(gdn::KID_VARLEN_SCATTER, cs, [&] {
+            return gdn::launch_varlen_flat(mo, S, fd.C, fd.NC, total, cu_seqlens, off, true,
+                                           (const int*)(ws + L.inner), (int*)ws, cs);
+        });
+        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
+    }
+    const void* src[5] = {q, k, v, alpha, beta};
+    const size_t dst[5] = {L.q, L.k, L.v, L.a, L.b};
+    const int width[5] = {kb, kb, vb, (int)es, (int)es};
+    const uint32_t fill[5] = {0u, 0u, 0u, one_bits(p), 0u};
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+        e = varlen_move(L, p, total, cu_seqlens, ws, width[i], src[i], ws + dst[i], fill[i], false, nullptr, cs);
     if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
     st = gdn_fwd(p, ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.b, initial_state, ws + L.o, final_state, saved,
-                 ws + L.inner, L.total - L.inner, stream);
+                 ws + L.inner, L.q - L.inner, stream);
     if (st != GDN_OK) return st;
-    e = gdn::launch_varlen_rows(d, total, cu_seqlens, vb, ws + L.o, o, 0u, true, err, inner_err(p, d, ws + L.inner),
-                                cs);
+    e = varlen_move(L, p, total, cu_seqlens, ws, vb, ws + L.o, o, 0u, true, nullptr, cs);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
 }
 
@@ -495,69 +637,107 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
                           const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
                           float* d_initial_state, void* workspace, size_t workspace_bytes, void* stream) {
     g_err[0] = 0;
-    gdn::Dims d{};
-    gdn_status st = check_varlen(p, total, cu_seqlens, &d);
+    VarlenPlan L;
+    gdn_status st = varlen_plan(p, total, true, &L);
     if (st != GDN_OK) return st;
+    if ((st = check_cu(p, cu_seqlens)) != GDN_OK) return st;
     const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
-    const size_t TH = (size_t)total * d.H;
-    const VarlenLayout L = varlen_layout(p, true);
-    const size_t nstate = (size_t)d.NS() * d.K * d.V * sizeof(float);
-    const Span ins[] = {{q, TH * d.K * es, "q"},
-                        {k, TH * d.K * es, "k"},
-                        {v, TH * d.V * es, "v"},
+    const size_t TH = (size_t)total * p->H;
+    const size_t nstate = (size_t)p->B * p->H * p->K * p->V * sizeof(float);
+    const Span ins[] = {{q, TH * p->K * es, "q"},
+                        {k, TH * p->K * es, "k"},
+                        {v, TH * p->V * es, "v"},
                         {alpha, TH * es, "alpha"},
                         {beta, TH * es, "beta"},
-                        {d_o, TH * d.V * es, "d_o"},
+                        {d_o, TH * p->V * es, "d_o"},
                         {initial_state, nstate, "initial_state"},
                         {d_final_state, nstate, "d_final_state"},
-                        {saved, saved ? gdn_saved_bytes(p) : 0, "saved"},
-                        {cu_seqlens, ((size_t)d.B + 1) * 4, "cu_seqlens"}};
-    const Span outs[] = {{dq, TH * d.K * es, "dq"},
-                         {dk, TH * d.K * es, "dk"},
-                         {dv, TH * d.V * es, "dv"},
+                        {saved, L.saved, "saved"},
+                        {cu_seqlens, ((size_t)p->B + 1) * 4, "cu_seqlens"}};
+    const Span outs[] = {{dq, TH * p->K * es, "dq"},
+                         {dk, TH * p->K * es, "dk"},
+                         {dv, TH * p->V * es, "dv"},
                          {dalpha, TH * es, "dalpha"},
                          {dbeta, TH * es, "dbeta"},
                          {workspace, L.total, "workspace"},
                          {d_initial_state, nstate, "d_initial_state"}};
-    for (int i = 0; i < 6; ++i)
-        if ((st = check_ptr(ins[i], true)) != GDN_OK) return st;
-    for (int i = 0; i < 6; ++i)
-        if ((st = check_ptr(outs[i], true)) != GDN_OK) return st;
+    for (int i = 0; i < 9; ++i)
+        if ((st = check_ptr(ins[i], i < 6)) != GDN_OK) return st;
+    for (int i = 0; i < 7; ++i)
+        if ((st = check_ptr(outs[i], i < 6)) != GDN_OK) return st;
     if (workspace_bytes < L.total)
         return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
-    if ((st = check_overlaps(ins, 10, outs, 7, nullptr, nullptr)) != GDN_OK) return st;
+    if ((st = check_overlaps(ins, 10, outs, 7, d_initial_state, d_final_state)) != GDN_OK) return st;
     cudaStream_t cs = (cudaStream_t)stream;
     char* ws = (char*)workspace;
-    int* err = (int*)ws;
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), cs);
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-word reset");
-    if (d.NS() == 0) return GDN_OK;
-    const int kb = d.K * (int)es, vb = d.V * (int)es;
-    const void* srcs[4] = {q, k, v, d_o};
-    const size_t dsts[4] = {L.q, L.k, L.v, L.d_o};
-    const int widths[4] = {kb, kb, vb, vb};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-        e = gdn::launch_varlen_rows(d, total, cu_seqlens, widths[i], srcs[i], ws + dsts[i], 0u, false, err,
-                                    nullptr, cs);
-    if (e == cudaSuccess)
-        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, alpha, ws + L.a, one_bits(p), false, err, cs);
-    if (e == cudaSuccess)
-        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, beta, ws + L.b, 0u, false, err, cs);
+    if (p->B * p->H == 0) return GDN_OK;
+    const int S = (int)p->B, kb = (int)(p->K * es), vb = (int)(p->V * es);
+    if (L.flat) {
+        const gdn::Dims& fd = L.pd;
+        const char* in = saved ? (const char*)saved : ws;
+        const int* off = (const int*)(saved ? in + L.s_off : ws + L.off);
+        const char* lq = in + (saved ? L.s_q : L.q);
+        const char* lk = in + (saved ? L.s_k : L.k);
+        const char* lv = in + (saved ? L.s_v : L.v);
+        const char* la = in + (saved ? L.s_a : L.a);
+        const char* lb = in + (saved ? L.s_b : L.b);
+        gdn::FlatMoves m{};
+        if (saved) {  // the forward laid out the inputs and the offsets: only d_o is new
+            m = gdn::FlatMoves{1, {d_o}, {ws + L.d_o}, {(int)p->H * vb}, {16}, {0u}};
+        } else {
+            e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
+                return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, (int*)(ws + L.off),
+                                                  (int*)ws, cs);
+            });
+            m = gdn::FlatMoves{6,
+                               {q, k, v, d_o, alpha, beta},
+                               {ws + L.q, ws + L.k, ws + L.v, ws + L.d_o, ws + L.a, ws + L.b},
+                               {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)p->H * vb, (int)(p->H * es),
+                                (int)(p->H * es)},
+                               {16, 16, 16, 16, (int)es, (int)es},
+                               {0u, 0u, 0u, 0u, one_bits(p), 0u}};
+        }
+        if (e == cudaSuccess)
+            e = timed(gdn::KID_VARLEN_GATHER, cs, [&] {
+                return gdn::launch_varlen_flat(m, S, fd.C, fd.NC, total, cu_seqlens, off, false, nullptr, (int*)ws,
+                                               cs);
+            });
+        if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
+        const gdn::SeqMap sq{off, S};
+        st = run_bwd_tc(fd, lq, lk, lv, la, lb, initial_state, saved ? (const char*)saved + L.s_tc : nullptr,
+                        ws + L.d_o, d_final_state, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db,
+                        d_initial_state, ws + L.inner, &sq, cs);
+        if (st != GDN_OK) return st;
+        gdn::FlatMoves mg{5,
+                          {ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db},
+                          {dq, dk, dv, dalpha, dbeta},
+                          {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)(p->H * es), (int)(p->H * es)},
+                          {16, 16, 16, (int)es, (int)es},
+                          {0u, 0u, 0u, 0u, 0u}};
+        e = timed(gdn::KID_VARLEN_SCATTER, cs, [&] {
+            return gdn::launch_varlen_flat(mg, S, fd.C, fd.NC, total, cu_seqlens, off, true,
+                                           (const int*)(ws + L.inner), (int*)ws, cs);
+        });
+        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
+    }
+    const void* src[6] = {q, k, v, d_o, alpha, beta};
+    const size_t dst[6] = {L.q, L.k, L.v, L.d_o, L.a, L.b};
+    const int width[6] = {kb, kb, vb, vb, (int)es, (int)es};
+    const uint32_t fill[6] = {0u, 0u, 0u, 0u, one_bits(p), 0u};
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+        e = varlen_move(L, p, total, cu_seqlens, ws, width[i], src[i], ws + dst[i], fill[i], false, nullptr, cs);
     if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
     st = gdn_bwd(p, ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.b, initial_state, saved, ws + L.d_o,
                  d_final_state, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db, d_initial_state,
-                 ws + L.inner, L.total - L.inner, stream);
+                 ws + L.inner, L.q - L.inner, stream);
     if (st != GDN_OK) return st;
-    const size_t srcs2[3] = {L.dq, L.dk, L.dv};
-    void* dsts2[3] = {dq, dk, dv};
-    const int widths2[3] = {kb, kb, vb};
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-        e = gdn::launch_varlen_rows(d, total, cu_seqlens, widths2[i], ws + srcs2[i], dsts2[i], 0u, true, err,
-                                    i == 0 ? inner_err(p, d, ws + L.inner) : nullptr, cs);
-    if (e == cudaSuccess)
-        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, ws + L.da, dalpha, 0u, true, err, cs);
-    if (e == cudaSuccess)
-        e = gdn::launch_varlen_elems(d, total, cu_seqlens, (int)es, ws + L.db, dbeta, 0u, true, err, cs);
+    const size_t gsrc[5] = {L.dq, L.dk, L.dv, L.da, L.db};
+    void* gdst[5] = {dq, dk, dv, dalpha, dbeta};
+    const int gw[5] = {kb, kb, vb, (int)es, (int)es};
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+        e = varlen_move(L, p, total, cu_seqlens, ws, gw[i], ws + gsrc[i], gdst[i], 0u, true, nullptr, cs);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
 }
 
@@ -695,49 +875,10 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
         return e == cudaSuccess ? GDN_OK : cuda_fail(e, "empty-sequence state copy");
     }
     const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    if (gdn::tc_fwd_supported(d, ty))
+        return run_bwd_tc(d, q, k, v, alpha, beta, initial_state, saved, d_o, d_final_state, dq, dk, dv, dalpha,
+                          dbeta, d_initial_state, workspace, nullptr, cs);
     Carver cv{(char*)workspace};
-    if (gdn::tc_fwd_supported(d, ty)) {
-        gdn::TcBufs tb;
-        gdn::TcBwdBufs tbb;
-        carve_tc_bwd(d, cv, &tb, &tbb, saved == nullptr);
-        const __nv_bfloat16* states = tbb.states;
-        if (saved) {  // reuse the forward's states and chunk results
-            Carver sv{(char*)const_cast<void*>(saved)};
-            __nv_bfloat16* st = nullptr;
-            int* err = tb.err;
-            carve_tc_saved(d, sv, &st, &tb);
-            tb.err = err;
-            states = st;
-        }
-        cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
-        if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
-        if (!saved) {
-            e = timed(gdn::KID_PREP_TC_BWD, cs, [&] {
-                return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs);
-            });
-            if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
-            e = timed(gdn::KID_STATE_TC, cs, [&] {
-                return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, nullptr, nullptr,
-                                               tbb.states, cs);
-            });
-            if (e != cudaSuccess) return cuda_fail(e, "tensor-core state recompute");
-        }
-        e = timed(gdn::KID_SCAN_BWD_TC, cs, [&] {
-            return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, d_final_state, tbb,
-                                           d_initial_state, cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core reverse scan");
-        e = timed(gdn::KID_GRAD_QK_TC, cs, [&] {
-            return gdn::launch_grad_qk_tc(d, q, k, d_o, tb, states, tbb, dq, cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (q, k)");
-        e = timed(gdn::KID_GRAD_WY_TC, cs, [&] {
-            return gdn::launch_grad_wy_tc(d, k, v, alpha, beta, tb, tbb, dk, dv, dalpha, dbeta,
-                                          cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (WY)");
-        return GDN_OK;
-    }
     gdn::ChunkBufs cb;
     gdn::BwdBufs bb;
     carve_bwd(d, cv, &cb, &bb, saved == nullptr);

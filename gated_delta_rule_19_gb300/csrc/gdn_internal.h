@@ -99,6 +99,9 @@ enum KernelId {
     KID_DECODE,          // decode_kernel
     KID_PROLOGUE_FWD,    // prologue_fwd_kernel
     KID_PROLOGUE_BWD,    // prologue_bwd_kernel
+    KID_VARLEN_OFFSETS,  // offsets_kernel (chunk offsets of packed sequences)
+    KID_VARLEN_GATHER,   // flat_kernel / rows16_kernel / elems_kernel, packed -> laid out
+    KID_VARLEN_SCATTER,  // the same, laid out -> packed
     KID_COUNT
 };
 
@@ -139,7 +142,16 @@ int sm_count();
 
 // Tensor-core forward (tc_fwd.cu).  tc_fwd_supported: shape/dtype test only.
 bool tc_fwd_supported(const Dims& d, InType ty);
-int tc_scan_vt(const Dims& d);
+// Packed sequences on the flat chunk layout (B = 1; every sequence starts a new
+// chunk): sequence s owns chunks chunk_off[s] .. chunk_off[s+1]-1 of each head's
+// row of chunks and state slot s*H + h.  The scans take it to run one stream per
+// (sequence, head); the chunk-parallel kernels need nothing (their work is local
+// to a chunk).
+struct SeqMap {
+    const int* chunk_off;  // device, int32 [nseq + 1]
+    int nseq;
+};
+int tc_scan_vt(int64_t streams);
 // Packed variable-length batches (varlen.cu): rows of packed [total, H, width]
 // tensors to and from the padded [S, T, H, width] layout.  `merge` (optional) is
 // ORed into `err` once.
@@ -148,6 +160,24 @@ cudaError_t launch_varlen_rows(const Dims& d, int64_t total, const int32_t* cu, 
                                void* dst, uint32_t fill, bool scatter, int* err, const int* merge, cudaStream_t st);
 cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu, int elem_bytes, const void* src,
                                 void* dst, uint32_t fill, bool scatter, int* err, cudaStream_t st);
+// The flat chunk layout (SeqMap): chunk_off from cu (one block; lengths above
+// max_len or invalid pairs count as empty and set the error bit; the offsets
+// never pass nc_max), then rows and single elements to (gather) and from
+// (scatter) the flat [H rows of nc_max*C tokens] layout.
+cudaError_t launch_varlen_offsets(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* cu,
+                                  int* chunk_off, int* err, cudaStream_t st);
+// Up to 8 tensors moved by one launch; row_bytes = H * (bytes per token and head),
+// a multiple of 16 or, for the gates, H * 2 or H * 4 with elem_bytes 2 or 4.
+struct FlatMoves {
+    int n;
+    const void* src[8];
+    void* dst[8];
+    int row_bytes[8];
+    int elem_bytes[8];  // 16 for row tensors
+    uint32_t fill[8];
+};
+cudaError_t launch_varlen_flat(const FlatMoves& m, int S, int C, int nc_max, int64_t total, const int32_t* cu,
+                               const int* chunk_off, bool scatter, const int* merge, int* err, cudaStream_t st);
 
 // q/k L2 normalisation and gate activations, and their backward (prologue.cu).
 cudaError_t launch_prologue_fwd(const Dims& d, InType ty, const void* qr, const void* kr, const void* a,
@@ -166,11 +196,11 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
                            cudaStream_t st);
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb,
                                const float* s0, void* o, float* sT, __nv_bfloat16* states,
-                               cudaStream_t st);
+                               cudaStream_t st, const SeqMap* sq = nullptr);
 // Tensor-core backward (tc_bwd.cu).
 cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, const void* d_o,
                                const TcBufs& tb, const float* dsT, const TcBwdBufs& bb,
-                               float* ds0, cudaStream_t st);
+                               float* ds0, cudaStream_t st, const SeqMap* sq = nullptr);
 cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const void* d_o,
                               const TcBufs& tb, const __nv_bfloat16* states,
                               const TcBwdBufs& bb, void* dq, cudaStream_t st);

@@ -147,7 +147,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dU,
             const __grid_constant__ CUtensorMap tm_dS1, const float* __restrict__ G, const float* dsT,
-            float* ds0, int* err) {
+            float* ds0, const int* __restrict__ chunk_off, int* err) {
     using P = BScan<Vt>;
     constexpr int HV = Vt / 2;
     extern __shared__ unsigned char smraw[];
@@ -164,29 +164,40 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const bool issuer = tid == 96;
     const bool urow = sub < 2;
     const int r = urow ? lanerow : lanerow - 64;
-    const int v0 = blockIdx.x * Vt, h = blockIdx.y, b = blockIdx.z;
-    const int64_t strm = (int64_t)b * d.H + h;
-    const int NC = d.NC;
+    const int v0 = blockIdx.x * Vt, h = blockIdx.y;
+    // Stream (b = blockIdx.z, h) runs chunks d.NC-1 .. 0 of its row of chunks.  With
+    // packed sequences (chunk_off) the data is one row of chunks per head (B = 1):
+    // sequence s = blockIdx.z runs chunks chunk_off[s+1]-1 .. chunk_off[s] of it,
+    // with the state gradients in slot s*H + h.  c below counts this CTA's chunks.
+    int b = blockIdx.z, c0 = 0, NC = d.NC;
+    const int64_t sidx = (int64_t)blockIdx.z * d.H + h;  // state slot
+    if (chunk_off) {
+        c0 = chunk_off[blockIdx.z];
+        NC = chunk_off[blockIdx.z + 1] - c0;
+        b = 0;
+    }
+    const int64_t cbase = ((int64_t)b * d.H + h) * d.NC + c0;  // global index of chunk c = 0
 
     auto issue_loads = [&](int it) {
         const int c = NC - 1 - it;
         unsigned char* st = sm + (it & 1) * P::STAGE;
         uint64_t* bar = &tbar[it & 1];
-        const int row = (int)((strm * NC + c) * kC);
+        const int row = (int)((cbase + c) * kC);
+        const int t0 = (c0 + c) * kC;
         mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         tma_load_2d(st + P::OFF_M, &tm_M, bar, 0, row);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(st + P::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, c * kC, b);
-            tma_load_4d(st + P::OFF_Q + j * 8192, &tm_q, bar, 64 * j, h, c * kC, b);
+            tma_load_4d(st + P::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, t0, b);
+            tma_load_4d(st + P::OFF_Q + j * 8192, &tm_q, bar, 64 * j, h, t0, b);
             tma_load_2d(st + P::OFF_W + j * 8192, &tm_W, bar, 64 * j, row);
         }
-        tma_load_5d(st + P::OFF_DO, &tm_do, bar, 0, c * kC, v0 / 8, h, b);
+        tma_load_5d(st + P::OFF_DO, &tm_do, bar, 0, t0, v0 / 8, h, b);
     };
 
     if (issuer) {
         for (int i = 0; i < 4; ++i) mbar_init(&tbar[i], 1);
         fence_mbar_init();
-        issue_loads(0);
+        if (NC > 0) issue_loads(0);
         if (NC > 1) issue_loads(1);
     }
     if (warp == 0) {
@@ -196,7 +207,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int k = lanerow;
     float ds[HV];
 #pragma unroll
-    for (int j = 0; j < HV; ++j) ds[j] = dsT ? dsT[(strm * d.V + v0 + cb + j) * kD + k] : 0.f;
+    for (int j = 0; j < HV; ++j) ds[j] = dsT ? dsT[(sidx * d.V + v0 + cb + j) * kD + k] : 0.f;
     auto write_ds_operand = [&]() {
 #pragma unroll
         for (int g = 0; g < HV / 8; ++g)
@@ -204,7 +215,8 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     };
     write_ds_operand();
     // G of a chunk is fetched one chunk ahead.
-    float GC_n = G[(strm * NC + NC - 1) * kC + kC - 1], Gr_n = G[(strm * NC + NC - 1) * kC + r];
+    float GC_n = NC > 0 ? G[(cbase + NC - 1) * kC + kC - 1] : 0.f;
+    float Gr_n = NC > 0 ? G[(cbase + NC - 1) * kC + r] : 0.f;
     // gamma dO operand (buffer it2 & 1) of the chunk held in stage it2 & 1; rows of
     // lanes 64-127; uses gamma_r = exp(Gr_n) of that chunk.
     auto write_gdo_operand = [&](int it2, bool& okk) {
@@ -227,7 +239,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     };
     bool ok = true;
-    if (!urow) write_gdo_operand(0, ok);
+    if (!urow && NC > 0) write_gdo_operand(0, ok);
     fence_proxy_async();
     fence_before_sync();
     ok = __syncthreads_and(ok);
@@ -247,7 +259,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int c = NC - 1 - it;
         const int stg = it & 1;
         unsigned char* st = sm + stg * P::STAGE;
-        const int64_t chunk = strm * NC + c;
+        const int64_t chunk = cbase + c;
         const float GC = GC_n;
         const float gC = expf(GC);
         const float er = expf(GC - Gr_n);
@@ -354,7 +366,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     if (ok && ds0) {
 #pragma unroll
-        for (int j = 0; j < HV; ++j) ds0[(strm * d.V + v0 + cb + j) * kD + k] = ds[j];
+        for (int j = 0; j < HV; ++j) ds0[(sidx * d.V + v0 + cb + j) * kD + k] = ds[j];
     }
     if (issuer) {
         if (!ok)
@@ -1097,7 +1109,8 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
 template <int Vt>
 cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
-                               const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st) {
+                               const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st,
+                               const SeqMap* sq) {
     using P = BScan<Vt>;
     CUtensorMap mq, mk, mW, mM, mdo, mdU, mdS1;
     const int64_t rows = d.NS() * d.NC * kC;
@@ -1110,19 +1123,21 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
     auto kern = scan_bwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(kD / Vt, d.H, d.B);
-    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0, tb.err);
+    dim3 grid(kD / Vt, d.H, sq ? sq->nseq : d.B);
+    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0,
+                                     sq ? sq->chunk_off : nullptr, tb.err);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
-                               const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st) {
-    switch (tc_scan_vt(d)) {
-        case 16: return launch_scan_bwd_vt<16>(d, q, k, d_o, tb, dsT, bb, ds0, st);
-        case 32: return launch_scan_bwd_vt<32>(d, q, k, d_o, tb, dsT, bb, ds0, st);
-        default: return launch_scan_bwd_vt<64>(d, q, k, d_o, tb, dsT, bb, ds0, st);
+                               const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st,
+                               const SeqMap* sq) {
+    switch (tc_scan_vt(sq ? (int64_t)sq->nseq * d.H : d.NS())) {
+        case 16: return launch_scan_bwd_vt<16>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
+        case 32: return launch_scan_bwd_vt<32>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
+        default: return launch_scan_bwd_vt<64>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
     }
 }
 

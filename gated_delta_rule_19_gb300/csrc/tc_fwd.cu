@@ -491,7 +491,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_Ut, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_st, const float* __restrict__ G, const float* s0,
-            float* sT, int write_o, int write_states, int* err) {
+            float* sT, int write_o, int write_states, const int* __restrict__ chunk_off, int* err) {
     using P = ScanPlan<Vt>;
     constexpr int HV = Vt / 2;  // columns per thread
     extern __shared__ unsigned char smraw[];
@@ -507,19 +507,30 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int lanerow = 32 * sub + lane;  // TMEM lane of this thread
     const int cb = half * HV;             // first column of this thread
     const bool issuer = tid == 96;        // warp 3 (output side) issues MMAs and copies
-    const int v0 = blockIdx.x * Vt, h = blockIdx.y, b = blockIdx.z;
-    const int64_t strm = (int64_t)b * d.H + h;
-    const int NC = d.NC;
+    const int v0 = blockIdx.x * Vt, h = blockIdx.y;
+    // Stream (b = blockIdx.z, h) runs chunks 0 .. d.NC-1 of its row of chunks.  With
+    // packed sequences (chunk_off) the data is one row of chunks per head (B = 1):
+    // sequence s = blockIdx.z runs chunks chunk_off[s] .. chunk_off[s+1]-1 of it
+    // and keeps its state in slot s*H + h.  c below counts this CTA's chunks.
+    int b = blockIdx.z, c0 = 0, NC = d.NC;
+    const int64_t sidx = (int64_t)blockIdx.z * d.H + h;  // state slot
+    if (chunk_off) {
+        c0 = chunk_off[blockIdx.z];
+        NC = chunk_off[blockIdx.z + 1] - c0;
+        b = 0;
+    }
+    const int64_t cbase = ((int64_t)b * d.H + h) * d.NC + c0;  // global index of chunk c = 0
 
     auto issue_loads = [&](int c) {
         unsigned char* st = sm + (c & 1) * P::STAGE;
-        const int row = (int)((strm * NC + c) * kC);
+        const int row = (int)((cbase + c) * kC);
+        const int t0 = (c0 + c) * kC;
         uint64_t* bar = &tbar[c & 1];
         mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         for (int j = 0; j < 2; ++j) {
             tma_load_2d(st + P::OFF_WQ + j * 16384, &tm_W, bar, 64 * j, row);
-            tma_load_4d(st + P::OFF_WQ + j * 16384 + 8192, &tm_q, bar, 64 * j, h, c * kC, b);
-            tma_load_4d(st + P::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, c * kC, b);
+            tma_load_4d(st + P::OFF_WQ + j * 16384 + 8192, &tm_q, bar, 64 * j, h, t0, b);
+            tma_load_4d(st + P::OFF_K + j * 8192, &tm_k, bar, 64 * j, h, t0, b);
         }
         tma_load_2d(st + P::OFF_M, &tm_M, bar, 0, row);
         tma_load_3d(st + P::OFF_UT, &tm_Ut, bar, 0, row, v0 / 8);
@@ -528,7 +539,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (issuer) {
         for (int i = 0; i < 5; ++i) mbar_init(&tbar[i], 1);
         fence_mbar_init();
-        issue_loads(0);
+        if (NC > 0) issue_loads(0);
         if (NC > 1) issue_loads(1);
     }
     if (warp == 0) {
@@ -539,7 +550,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int k = lanerow;
     float s[HV];
 #pragma unroll
-    for (int j = 0; j < HV; ++j) s[j] = s0 ? s0[(strm * d.V + v0 + cb + j) * kD + k] : 0.f;
+    for (int j = 0; j < HV; ++j) s[j] = s0 ? s0[(sidx * d.V + v0 + cb + j) * kD + k] : 0.f;
     auto write_state_operand = [&]() {
         // MN-major, no swizzle: element (v, k) at (v/8)*2048 + k*16 + (v%8)*2
 #pragma unroll
@@ -565,7 +576,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t id = idesc_bf16(128, Vt, false, true);
     const uint32_t idmn = idesc_bf16(128, Vt, true, true);
 
-    float GC_n = G[strm * NC * kC + kC - 1], Gr_n = G[strm * NC * kC + r];
+    float GC_n = NC > 0 ? G[cbase * kC + kC - 1] : 0.f, Gr_n = NC > 0 ? G[cbase * kC + r] : 0.f;
     float gr_prev = 0.f;
 
     // Output of chunk cc (threads on lanes 64-127): O = gamma Y + Mqk U.
@@ -615,7 +626,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (; c < NC; ++c) {
         const int stg = c & 1;
         unsigned char* st = sm + stg * P::STAGE;
-        const int64_t chunk = strm * NC + c;
+        const int64_t chunk = cbase + c;
         if (issuer) {
             if (write_states) {  // chunk-start state -> saved boundary states, by TMA
                 tma_store_3d(&tm_st, sm + P::S_OP, 0, (int)(chunk * kD), v0 / 8);
@@ -686,7 +697,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_after_sync();
         if (issuer) {
             if (c > 0 && write_o) {  // output tile of the previous chunk
-                tma_store_5d(&tm_o, sm + P::O_OP, 0, (c - 1) * kC, v0 / 8, h, b);
+                tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + c - 1) * kC, v0 / 8, h, b);
                 bulk_commit();
             }
             const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 8192, 1024, SW_128B);
@@ -734,13 +745,13 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_before_sync();
         ok = __syncthreads_and(ok);
         if (issuer && ok && write_o) {
-            tma_store_5d(&tm_o, sm + P::O_OP, 0, (NC - 1) * kC, v0 / 8, h, b);
+            tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + NC - 1) * kC, v0 / 8, h, b);
             bulk_commit();
         }
     }
     if (ok && sT) {
 #pragma unroll
-        for (int j = 0; j < HV; ++j) sT[(strm * d.V + v0 + cb + j) * kD + k] = s[j];
+        for (int j = 0; j < HV; ++j) sT[(sidx * d.V + v0 + cb + j) * kD + k] = s[j];
     }
     if (issuer) {
         if (!ok) {
@@ -759,7 +770,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 template <int Vt>
 cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
-                           void* o, float* sT, bf16* states, cudaStream_t st) {
+                           void* o, float* sT, bf16* states, cudaStream_t st, const SeqMap* sq) {
     using P = ScanPlan<Vt>;
     CUtensorMap mq, mk, mW, mM, mUt, mo, mst;
     const int64_t rows = d.NS() * d.NC * kC;
@@ -775,9 +786,9 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     auto kern = scan_fwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(kD / Vt, d.H, d.B);
+    dim3 grid(kD / Vt, d.H, sq ? sq->nseq : d.B);
     kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, o != nullptr,
-                                     states != nullptr, tb.err);
+                                     states != nullptr, sq ? sq->chunk_off : nullptr, tb.err);
     return cudaGetLastError();
 }
 
@@ -787,10 +798,10 @@ bool tc_fwd_supported(const Dims& d, InType ty) {
     return ty == InType::BF16 && d.K == kD && d.V == kD && d.C == kC;
 }
 
-int tc_scan_vt(const Dims& d) {
+int tc_scan_vt(int64_t streams) {
     const int64_t sms = sm_count();
     for (int vt : {16, 32, 64})
-        if (d.NS() * (kD / vt) <= sms) return vt;
+        if (streams * (kD / vt) <= sms) return vt;
     return 64;
 }
 
@@ -811,11 +822,11 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
 }
 
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
-                               void* o, float* sT, __nv_bfloat16* states, cudaStream_t st) {
-    switch (tc_scan_vt(d)) {
-        case 16: return launch_scan_vt<16>(d, q, k, tb, s0, o, sT, states, st);
-        case 32: return launch_scan_vt<32>(d, q, k, tb, s0, o, sT, states, st);
-        default: return launch_scan_vt<64>(d, q, k, tb, s0, o, sT, states, st);
+                               void* o, float* sT, __nv_bfloat16* states, cudaStream_t st, const SeqMap* sq) {
+    switch (tc_scan_vt(sq ? (int64_t)sq->nseq * d.H : d.NS())) {
+        case 16: return launch_scan_vt<16>(d, q, k, tb, s0, o, sT, states, st, sq);
+        case 32: return launch_scan_vt<32>(d, q, k, tb, s0, o, sT, states, st, sq);
+        default: return launch_scan_vt<64>(d, q, k, tb, s0, o, sT, states, st, sq);
     }
 }
 

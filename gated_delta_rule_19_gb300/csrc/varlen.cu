@@ -79,6 +79,138 @@ __global__ void elems_kernel(int S, int T, int H, int64_t total, const int32_t* 
     }
 }
 
+// ------------------------------------------------ flat chunk layout (SeqMap)
+// chunk_off[s] = sum over j < s of ceil(len_j / C), capped at nc_max.  One block;
+// thread i sums a contiguous run of sequences, then the block scans the sums.
+__global__ void offsets_kernel(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* __restrict__ cu,
+                               int* __restrict__ chunk_off, int* err) {
+    __shared__ int64_t part[1024];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (S + nt - 1) / nt;
+    const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+    int64_t sum = 0;
+    for (int s = s0; s < s1; ++s) {
+        int64_t start;
+        int len;
+        seq_span(cu, s, total, max_len, start, len, err);
+        sum += (len + C - 1) / C;
+    }
+    part[tid] = sum;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {  // inclusive scan (Hillis-Steele)
+        const int64_t x = tid >= off ? part[tid - off] : 0;
+        __syncthreads();
+        part[tid] += x;
+        __syncthreads();
+    }
+    int64_t run = tid ? part[tid - 1] : 0;
+    for (int s = s0; s < s1; ++s) {
+        chunk_off[s] = (int)min(run, (int64_t)nc_max);
+        int64_t start;
+        int len;
+        seq_span(cu, s, total, max_len, start, len, nullptr);
+        run += (len + C - 1) / C;
+    }
+    if (tid == nt - 1) {
+        chunk_off[S] = (int)min(part[nt - 1], (int64_t)nc_max);
+        if (part[nt - 1] > nc_max || cu[0] != 0 || (int64_t)cu[S] != total) atomicOr(err, kVarlenBadOffsets);
+    }
+}
+
+// Rows of sequence s that reach the flat layout: its length, cut to its chunks.
+__device__ __forceinline__ int flat_len(const int32_t* cu, const int* chunk_off, int s, int64_t total, int C,
+                                        int64_t& start) {
+    int len;
+    seq_span(cu, s, total, 0x7fffffff, start, len, nullptr);
+    return (int)min((int64_t)len, (int64_t)(chunk_off[s + 1] - chunk_off[s]) * C);
+}
+
+// Largest s in [0, n) with a[s] <= x (a non-decreasing; 0 if none).
+__device__ __forceinline__ int last_le(const int* a, int n, int64_t x) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)a[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// One contiguous run: `nvalid` units copied, then (gather only) `ntotal - nvalid`
+// units of fill.  Four independent loads in flight per thread.
+template <typename U>
+__device__ __forceinline__ void move_run(const U* __restrict__ src, U* __restrict__ dst, int nvalid, int ntotal,
+                                         U fill, bool do_fill) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    int i = tid;
+    for (; i + 3 * nt < nvalid; i += 4 * nt) {
+        const U a = src[i], b = src[i + nt], c = src[i + 2 * nt], d = src[i + 3 * nt];
+        dst[i] = a;
+        dst[i + nt] = b;
+        dst[i + 2 * nt] = c;
+        dst[i + 3 * nt] = d;
+    }
+    for (; i < nvalid; i += nt) dst[i] = src[i];
+    if (do_fill)
+        for (int k = nvalid + tid; k < ntotal; k += nt) dst[k] = fill;
+}
+
+// Block per flat chunk c: the sequence s owning it (chunk_off[s] <= c <
+// chunk_off[s+1]) has n = min(C, len - j*C) valid rows there, j = c - chunk_off[s],
+// at packed rows start + j*C ...  Both sides are contiguous runs of rows, so each
+// tensor is one copy of n rows plus (gather) C - n rows of fill.
+__global__ void flat_move_kernel(FlatMoves m, int S, int C, int nc_max, int64_t total,
+                                 const int32_t* __restrict__ cu, const int* __restrict__ chunk_off, int dir,
+                                 const int* merge, int* err) {
+    if (merge && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, *merge);
+    __shared__ int64_t sh_row;
+    __shared__ int sh_n;
+    for (int c = blockIdx.x; c < nc_max; c += gridDim.x) {
+        if (threadIdx.x == 0) {
+            int n = 0;
+            int64_t prow = 0;
+            if (S > 0 && c < chunk_off[S]) {
+                const int s = last_le(chunk_off, S, c);
+                int64_t start;
+                const int len = flat_len(cu, chunk_off, s, total, C, start);
+                const int64_t j = c - chunk_off[s];
+                n = (int)max((int64_t)0, min((int64_t)C, (int64_t)len - j * C));
+                prow = start + j * C;
+            }
+            sh_n = n;
+            sh_row = prow;
+        }
+        __syncthreads();
+        const int n = sh_n;
+        const int64_t prow = sh_row;
+        if (dir == 0 || n > 0) {
+            for (int t = 0; t < m.n; ++t) {
+                const int rb = m.row_bytes[t], eb = m.elem_bytes[t];
+                const int per_row = rb / eb;
+                const int64_t fo = (int64_t)c * C * per_row, po = prow * per_row;
+                const int nv = n * per_row, nall = C * per_row;
+                const char* sb = (const char*)m.src[t];
+                char* db = (char*)m.dst[t];
+                const uint32_t f = m.fill[t];
+                if (eb == 16) {
+                    const uint4* sp = (const uint4*)sb + (dir == 0 ? po : fo);
+                    uint4* dp = (uint4*)db + (dir == 0 ? fo : po);
+                    move_run<uint4>(sp, dp, nv, nall, make_uint4(f, f, f, f), dir == 0);
+                } else if (eb == 4) {
+                    const uint32_t* sp = (const uint32_t*)sb + (dir == 0 ? po : fo);
+                    uint32_t* dp = (uint32_t*)db + (dir == 0 ? fo : po);
+                    move_run<uint32_t>(sp, dp, nv, nall, f, dir == 0);
+                } else {
+                    const uint16_t* sp = (const uint16_t*)sb + (dir == 0 ? po : fo);
+                    uint16_t* dp = (uint16_t*)db + (dir == 0 ? fo : po);
+                    move_run<uint16_t>(sp, dp, nv, nall, (uint16_t)f, dir == 0);
+                }
+            }
+        }
+        __syncthreads();  // sh_n / sh_row are rewritten for the next chunk
+    }
+}
+
 unsigned grid_for(int64_t n) {
     const int64_t want = (n + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -107,6 +239,27 @@ cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu,
     else
         elems_kernel<uint32_t><<<grid_for(n), 256, 0, st>>>(d.B, d.T, d.H, total, cu, (const uint32_t*)src,
                                                             (uint32_t*)dst, fill, scatter ? 1 : 0, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_offsets(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* cu,
+                                  int* chunk_off, int* err, cudaStream_t st) {
+    int nt = 32;  // a power of two for the block scan
+    while (nt < 1024 && nt < S) nt <<= 1;
+    offsets_kernel<<<1, nt, 0, st>>>(S, total, max_len, C, nc_max, cu, chunk_off, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_flat(const FlatMoves& m, int S, int C, int nc_max, int64_t total, const int32_t* cu,
+                               const int* chunk_off, bool scatter, const int* merge, int* err, cudaStream_t st) {
+    for (int t = 0; t < m.n; ++t)
+        if ((m.elem_bytes[t] != 16 && m.elem_bytes[t] != 4 && m.elem_bytes[t] != 2) ||
+            m.row_bytes[t] % m.elem_bytes[t] != 0)
+            return cudaErrorInvalidValue;
+    if (m.n < 0 || m.n > 8) return cudaErrorInvalidValue;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    const unsigned grid = (unsigned)max((int64_t)1, min((int64_t)nc_max, cap));
+    flat_move_kernel<<<grid, 256, 0, st>>>(m, S, C, nc_max, total, cu, chunk_off, scatter ? 1 : 0, merge, err);
     return cudaGetLastError();
 }
 

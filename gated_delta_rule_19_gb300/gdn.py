@@ -67,8 +67,8 @@ def load_library():
     lib.gdn_prologue_fwd.restype = ctypes.c_int
     lib.gdn_prologue_bwd.argtypes = [P] + [_vp] * 12 + [_vp]
     lib.gdn_prologue_bwd.restype = ctypes.c_int
-    for fn in ("gdn_varlen_fwd_workspace_bytes", "gdn_varlen_bwd_workspace_bytes"):
-        getattr(lib, fn).argtypes = [P]
+    for fn in ("gdn_varlen_fwd_workspace_bytes", "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_saved_bytes"):
+        getattr(lib, fn).argtypes = [P, ctypes.c_int64]
         getattr(lib, fn).restype = ctypes.c_size_t
     lib.gdn_varlen_fwd.argtypes = [P, ctypes.c_int64] + [_vp] * 11 + [ctypes.c_size_t, _vp]
     lib.gdn_varlen_fwd.restype = ctypes.c_int
@@ -93,7 +93,7 @@ EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_works
             "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
             "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode",
             "gdn_prologue_fwd", "gdn_prologue_bwd", "gdn_varlen_fwd_workspace_bytes",
-            "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd")
+            "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_saved_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -353,12 +353,16 @@ def gdn_prologue_bwd(q_raw, k_raw, a_logit, b_logit, dq, dk, dalpha, dbeta, *, o
 VARLEN_BAD_OFFSETS = 1 << 30  # bit of the varlen workspace's error word
 
 
-def gdn_varlen_fwd_workspace_bytes(p: gdn_problem) -> int:
-    return int(load_library().gdn_varlen_fwd_workspace_bytes(ctypes.byref(p)))
+def gdn_varlen_fwd_workspace_bytes(p: gdn_problem, total: int) -> int:
+    return int(load_library().gdn_varlen_fwd_workspace_bytes(ctypes.byref(p), int(total)))
 
 
-def gdn_varlen_bwd_workspace_bytes(p: gdn_problem) -> int:
-    return int(load_library().gdn_varlen_bwd_workspace_bytes(ctypes.byref(p)))
+def gdn_varlen_bwd_workspace_bytes(p: gdn_problem, total: int) -> int:
+    return int(load_library().gdn_varlen_bwd_workspace_bytes(ctypes.byref(p), int(total)))
+
+
+def gdn_varlen_saved_bytes(p: gdn_problem, total: int) -> int:
+    return int(load_library().gdn_varlen_saved_bytes(ctypes.byref(p), int(total)))
 
 
 def _varlen_problem(q, v, cu_seqlens, max_len, chunk):
@@ -418,11 +422,11 @@ def gdn_varlen_fwd(q, k, v, alpha, beta, cu_seqlens, max_len=None, initial_state
         final_state = None
     _need(final_state, "final_state", (S, H, V, K), torch.float32, dev)
     if saved is True:
-        saved = torch.empty(max(gdn_saved_bytes(p), 1), dtype=torch.uint8, device=dev)
+        saved = torch.empty(max(gdn_varlen_saved_bytes(p, total), 1), dtype=torch.uint8, device=dev)
     elif saved is False:
         saved = None
     if workspace is None:
-        workspace = torch.empty(max(gdn_varlen_fwd_workspace_bytes(p), 4), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(max(gdn_varlen_fwd_workspace_bytes(p, total), 4), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
     st = lib.gdn_varlen_fwd(ctypes.byref(p), total, _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                             _ptr(beta), _ptr(initial_state), _ptr(o), _ptr(final_state), _ptr(saved),
@@ -449,8 +453,8 @@ def gdn_varlen_bwd(q, k, v, alpha, beta, cu_seqlens, max_len, initial_state, d_o
         _need(t, n, sh, dt, dev)
     _need(initial_state, "initial_state", (S, H, V, K), torch.float32, dev)
     _need(d_final_state, "d_final_state", (S, H, V, K), torch.float32, dev)
-    if saved is not None and saved.numel() * saved.element_size() < gdn_saved_bytes(p):
-        raise GdnError(GDN_ERR_INVALID_ARG, "saved buffer is smaller than gdn_saved_bytes()")
+    if saved is not None and saved.numel() * saved.element_size() < gdn_varlen_saved_bytes(p, total):
+        raise GdnError(GDN_ERR_INVALID_ARG, "saved buffer is smaller than gdn_varlen_saved_bytes()")
     if grads is None:
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(alpha),
                  torch.empty_like(beta))
@@ -464,7 +468,7 @@ def gdn_varlen_bwd(q, k, v, alpha, beta, cu_seqlens, max_len, initial_state, d_o
         d_initial_state = None
     _need(d_initial_state, "d_initial_state", (S, H, V, K), torch.float32, dev)
     if workspace is None:
-        workspace = torch.empty(max(gdn_varlen_bwd_workspace_bytes(p), 4), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(max(gdn_varlen_bwd_workspace_bytes(p, total), 4), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
     st = lib.gdn_varlen_bwd(ctypes.byref(p), total, _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                             _ptr(beta), _ptr(initial_state), _ptr(saved), _ptr(d_o), _ptr(d_final_state),
@@ -474,6 +478,95 @@ def gdn_varlen_bwd(q, k, v, alpha, beta, cu_seqlens, max_len, initial_state, d_o
     if check:
         _varlen_error(workspace, stream, dev)
     return dq, dk, dv, da, db, d_initial_state
+
+
+class ResetSegments:
+    """A dense [B, T] batch with reset positions, as the packed sequences the
+    varlen calls run: a reset at (b, t) restarts row b's stream from the zero
+    state at token t, so every row splits into segments that start at t = 0 or
+    at a reset, laid back to back in the row-major token order of the batch.
+
+    ``cu_seqlens`` (int32 [S+1]) holds the segment offsets over the B*T tokens,
+    ``first`` / ``last`` (int64 [B]) the segment index of each row's first and
+    last segment, ``max_len`` the longest segment, ``carry`` (int64) the rows
+    without a reset at t = 0, whose first segment starts from the row's initial
+    state (a reset at t = 0 discards it).  Building it reads the mask once on the
+    host (the number of segments sizes the launch)."""
+
+    def __init__(self, reset):
+        if reset.dim() != 2:
+            raise GdnError(GDN_ERR_INVALID_ARG, "reset must be a [B, T] mask")
+        B, T = reset.shape
+        dev = reset.device
+        start = reset.to(torch.bool).clone()
+        if T:
+            start[:, 0] = True
+        pos = torch.nonzero(start.reshape(-1), as_tuple=False).reshape(-1)
+        self.B, self.T, self.S = B, T, int(pos.numel())
+        self.cu_seqlens = torch.cat([pos, torch.tensor([B * T], device=dev)]).to(torch.int32)
+        lens = self.cu_seqlens[1:] - self.cu_seqlens[:-1]
+        self.max_len = int(lens.max().item()) if self.S else 0
+        self.first = torch.nonzero(pos % max(T, 1) == 0, as_tuple=False).reshape(-1) if T else pos
+        self.last = torch.cat([self.first[1:] - 1, torch.tensor([self.S - 1], device=dev)]) if T else pos
+        self.carry = torch.nonzero(~reset[:, 0].to(torch.bool), as_tuple=False).reshape(-1) if T else pos
+
+
+def _rows_to_segments(x, seg: ResetSegments, at, rows):
+    """Per-row states [B,H,V,K] -> per-segment states [S,H,V,K]: row rows[i]'s
+    state at segment at[i], zero elsewhere."""
+    if x is None:
+        return None
+    out = torch.zeros((seg.S,) + tuple(x.shape[1:]), dtype=x.dtype, device=x.device)
+    out.index_copy_(0, at, x.index_select(0, rows))
+    return out
+
+
+def _all_rows(seg):
+    return torch.arange(seg.B, device=seg.cu_seqlens.device)
+
+
+def gdn_reset_fwd(q, k, v, alpha, beta, reset, initial_state=None, *, chunk: int = 64, segments=None,
+                  saved=False, check=False, stream=None):
+    """Forward over a dense batch (q, k [B,T,H,K]; v [B,T,H,V]; alpha, beta
+    [B,T,H]) whose streams restart from the zero state at every position where
+    ``reset`` ([B,T] bool) is set.  initial_state [B,H,V,K] feeds each row's
+    first segment.  Returns ``(o [B,T,H,V], final_state [B,H,V,K], saved,
+    segments)``; pass ``segments`` and ``saved`` on to :func:`gdn_reset_bwd`."""
+    seg = segments if segments is not None else ResetSegments(reset)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if seg.S == 0:  # no tokens: the state passes through
+        sT = (initial_state.clone() if initial_state is not None
+              else torch.zeros(B, H, V, K, dtype=torch.float32, device=q.device))
+        return torch.empty(B, T, H, V, dtype=q.dtype, device=q.device), sT, None, seg
+    flat = lambda x: x.reshape((B * T,) + tuple(x.shape[2:]))
+    s0 = _rows_to_segments(initial_state, seg, seg.first.index_select(0, seg.carry), seg.carry)
+    o, sT, sv = gdn_varlen_fwd(flat(q), flat(k), flat(v), flat(alpha), flat(beta), seg.cu_seqlens, seg.max_len,
+                               s0, chunk=chunk, saved=saved, check=check, stream=stream)
+    return o.reshape(B, T, H, V), sT.index_select(0, seg.last), sv, seg
+
+
+def gdn_reset_bwd(q, k, v, alpha, beta, reset, initial_state, d_o, d_final_state=None, *, chunk: int = 64,
+                  segments=None, saved=None, check=False, stream=None):
+    """Backward of :func:`gdn_reset_fwd`: returns ``(dq, dk, dv, dalpha, dbeta,
+    d_initial_state [B,H,V,K])``."""
+    seg = segments if segments is not None else ResetSegments(reset)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if seg.S == 0:  # no tokens: d(initial state) = d(final state)
+        ds0 = (d_final_state.clone() if d_final_state is not None
+               else torch.zeros(B, H, V, K, dtype=torch.float32, device=q.device))
+        return tuple(torch.empty_like(t) for t in (q, k, v, alpha, beta)) + (ds0,)
+    flat = lambda x: x.reshape((B * T,) + tuple(x.shape[2:]))
+    s0 = _rows_to_segments(initial_state, seg, seg.first.index_select(0, seg.carry), seg.carry)
+    dsT = _rows_to_segments(d_final_state, seg, seg.last, _all_rows(seg))
+    g = gdn_varlen_bwd(flat(q), flat(k), flat(v), flat(alpha), flat(beta), seg.cu_seqlens, seg.max_len, s0,
+                       flat(d_o), dsT, saved=saved, chunk=chunk, check=check, stream=stream)
+    grads = tuple(x.reshape(t.shape) for x, t in zip(g[:5], (q, k, v, alpha, beta)))
+    # a row whose stream was reset at t = 0 does not depend on its initial state
+    ds0 = torch.zeros(B, H, V, K, dtype=torch.float32, device=q.device)
+    ds0.index_copy_(0, seg.carry, g[5].index_select(0, seg.first.index_select(0, seg.carry)))
+    return grads + (ds0,)
 
 
 def gdn_decode(q, k, v, alpha, beta, state, *, o=None, stream=None):

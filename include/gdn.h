@@ -191,8 +191,7 @@ gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void*
  * equals gdn_fwd / gdn_bwd on that sequence alone (B = 1, T = its length).
  *
  *   p            : B = number of sequences S, T = an upper bound on every
- *                  sequence length (the padded length the kernels run on), H, K,
- *                  V, chunk, dtype as for gdn_fwd.
+ *                  sequence length, H, K, V, chunk, dtype as for gdn_fwd.
  *   total        : packed rows, 0 <= total <= B*T.
  *   cu_seqlens   : int32 [S+1] on the device, cu[0] = 0, non-decreasing,
  *                  cu[S] = total, every length <= T.  It is read by the kernels,
@@ -207,18 +206,26 @@ gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void*
  *                  their inputs.
  *   initial_state, final_state, d_final_state, d_initial_state : float32
  *                  [S, H, V, K] or NULL, as for gdn_fwd / gdn_bwd.
- *   saved        : NULL or gdn_saved_bytes(p) bytes (p as above), filled by
- *                  gdn_varlen_fwd and read by gdn_varlen_bwd.
- *   workspace    : gdn_varlen_fwd_workspace_bytes(p) / gdn_varlen_bwd_
- *                  workspace_bytes(p) bytes.
- * Method: the sequences are copied into a padded [S, T, H, ...] layout inside the
- * workspace (rows past a sequence's end get q = k = v = 0, alpha = 1, beta = 0,
- * which leave the state unchanged and read nothing), the chunk kernels run on it,
- * and the results are copied back.  Host-side checks as for gdn_fwd; every
- * pointer 16-byte aligned except cu_seqlens (4 bytes).
+ *   saved        : NULL or gdn_varlen_saved_bytes(p, total) bytes, filled by
+ *                  gdn_varlen_fwd and read by gdn_varlen_bwd with the same
+ *                  inputs and cu_seqlens.  On the tensor-core path it also keeps
+ *                  the laid-out inputs and the chunk offsets, so the backward
+ *                  then lays out only d_o (and does not re-check cu_seqlens).
+ *   workspace    : gdn_varlen_fwd_workspace_bytes(p, total) /
+ *                  gdn_varlen_bwd_workspace_bytes(p, total) bytes.
+ * Method: the sequences are copied into a chunk layout inside the workspace,
+ * the chunk kernels run on it, and the results are copied back.  Rows past a
+ * sequence's end get q = k = v = 0, alpha = 1, beta = 0, which leave the state
+ * unchanged and read nothing.  With bf16, K = V = 128 and chunk 64 (the
+ * tensor-core path) each sequence starts a new chunk of one row of chunks per
+ * head, and the scans run one stream per (sequence, head) over that
+ * sequence's chunks: at most chunk-1 padded rows per sequence.  Other shapes
+ * pad every sequence to T.  Host-side checks as for gdn_fwd; every pointer
+ * 16-byte aligned except cu_seqlens (4 bytes); S <= 65535.
  */
-size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p);
-size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p);
+size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p, int64_t total);
+size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p, int64_t total);
+size_t gdn_varlen_saved_bytes(const gdn_problem* p, int64_t total);
 gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu_seqlens, const void* q,
                           const void* k, const void* v, const void* alpha, const void* beta,
                           const float* initial_state, void* o, float* final_state, void* saved, void* workspace,

@@ -2,9 +2,10 @@
 (only the tests import it; the product path never does).
 
 Every mixer the pages show feeds the recurrence L2-normalised keys and queries
-and per-head gates ("OpenGDN", Mixer: "L2-normalized Q/K, per-head alpha/beta
-gates"; "Sparse Delta Memory: layer and kernels", What the layer computes:
-l2-normalised read and write weights in the dense limit).  This module writes
+and per-head gates ("OpenGDN", Mixer: the mixer normalises q and k to unit L2
+length and computes one alpha and one beta per head; "Sparse Delta Memory: layer
+and kernels", What the layer computes: l2-normalised read and write weights in
+the dense limit).  This module writes
 that step out in plain numpy:
 
 * ``q = q_raw / sqrt(sum_K q_raw^2 + eps)`` and the same for k, per (b, t, h),

@@ -199,8 +199,8 @@ def test_varlen_arguments_rejected_before_launch(lib):
     assert _varlen_fwd(lib, p, 200, cu=FAKE + (12 << 30) + 2) == INVALID  # not 4-byte aligned
     assert _varlen_fwd(lib, p, 200, q=None) == INVALID
     assert _varlen_fwd(lib, p, 200, ws_bytes=1024) == WS
-    need = lib.load_library().gdn_varlen_fwd_workspace_bytes(ctypes.byref(p))
-    assert need > lib.load_library().gdn_fwd_workspace_bytes(ctypes.byref(p))
+    need = lib.load_library().gdn_varlen_fwd_workspace_bytes(ctypes.byref(p), 200)
+    assert need > 0
     assert _varlen_fwd(lib, p, 200, ws_bytes=need - 1) == WS
     assert _varlen_fwd(lib, p, 200, o=FAKE + 256) == INVALID          # o overlaps q
     assert _varlen_fwd(lib, p, 200, cu=FAKE + (5 << 30) + 64) == INVALID  # cu inside o

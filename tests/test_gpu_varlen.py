@@ -56,10 +56,15 @@ def _oracle_seq(oracle_mod, inp, s):
                 **{n: g[n][0] for n in GRADS})
 
 
+# bf16 with K = V = 128 and chunk 64 runs the tensor-core kernels on the flat
+# chunk layout (each sequence starts a new chunk); other shapes pad to max_len.
 CASES = [
     # lengths (one empty, ragged tails, exact chunks, several tiles), H, K, V, chunk, dtype
     ([1, 63, 64, 65, 200, 0, 130], 2, 64, 64, 64, "bf16"),
     ([64, 1, 128, 191], 2, 128, 128, 64, "bf16"),
+    ([1, 63, 64, 65, 200, 0, 130, 0], 2, 128, 128, 64, "bf16"),
+    # 40 sequences x 4 heads: more (sequence, head) streams than one wave of SMs
+    ([(37 * i) % 150 + 1 for i in range(40)], 4, 128, 128, 64, "bf16"),
     ([5, 17, 33, 0, 48], 3, 32, 32, 16, "f32"),
     ([70, 9, 100], 1, 16, 64, 32, "f32"),
     ([129, 2], 2, 128, 128, 64, "f32"),
@@ -97,13 +102,16 @@ def test_varlen_matches_oracle_per_sequence(oracle_mod, lengths, H, K, V, chunk,
     assert not bad, "; ".join(bad)
 
 
-def test_varlen_short_sequences_equal_their_own_dense_runs():
+@pytest.mark.parametrize("dtype,K", [("f32", 64), ("bf16", 128)])
+def test_varlen_short_sequences_equal_their_own_dense_runs(dtype, K):
     """Each sequence of a packed batch, run alone through gdn_fwd / gdn_bwd (B = 1,
     T = its length), gives the same outputs and gradients: the varlen calls only
     move rows, so short sequences whose gradients are too small for a relative
-    norm are checked against the dense path here."""
+    norm are checked against the dense path here.  Both layouts pad a sequence's
+    last chunk exactly as the dense kernels pad a ragged tail, so the results are
+    bit-identical."""
     lengths = [1, 2, 3, 7, 15, 64, 65]
-    inp = make_varlen_inputs(lengths, 2, 64, 64, "f32", seed=41, init_std=0.3, dfinal_std=0.05)
+    inp = make_varlen_inputs(lengths, 2, K, K, dtype, seed=41, init_std=0.3, dfinal_std=0.05)
     d = _cuda(inp)
     got = _run_varlen(d, 64)
     cu = inp["cu_seqlens"].tolist()
@@ -120,14 +128,15 @@ def test_varlen_short_sequences_equal_their_own_dense_runs():
                  (got["d_initial_state"][s], g[5][0])]
         pairs += [(got[n][a:e], g[i][0]) for i, n in enumerate(GRADS)]
         for x, y in pairs:
-            torch.testing.assert_close(x, y, rtol=1e-5, atol=1e-6)
+            assert torch.equal(x, y), (s, float((x.float() - y.float()).abs().max()))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_varlen_equal_lengths_bitwise_equal_to_dense(dtype):
-    """S sequences of one length T are the dense [S, T] batch: the padded layout
-    is then exactly the dense one, so every result is bit-identical."""
-    S, T, H, K, V = 3, 130, 2, 64, 64
+@pytest.mark.parametrize("dtype,K", [("bf16", 64), ("f32", 64), ("bf16", 128)])
+def test_varlen_equal_lengths_bitwise_equal_to_dense(dtype, K):
+    """S sequences of one length T are the dense [S, T] batch: both layouts then
+    put the chunk boundaries where the dense batch has them, so every result is
+    bit-identical."""
+    S, T, H, V = 3, 130, 2, K
     w = custom(B=S, T=T, H=H, K=K, V=V, chunk=64, dtype=dtype, seed=42, init_std=0.2, dfinal_std=0.05)
     dense = {n: (t.cuda() if t is not None else None) for n, t in make_inputs(w).items()}
     o, sT, saved = gdn.gdn_fwd(dense["q"], dense["k"], dense["v"], dense["alpha"], dense["beta"],
@@ -146,10 +155,21 @@ def test_varlen_equal_lengths_bitwise_equal_to_dense(dtype):
 
 
 def test_varlen_empty_batch_and_empty_sequences():
-    """No tokens at all: outputs are empty, final state = initial state, and
-    d_initial_state = d_final_state."""
+    """No tokens at all (and an empty sequence among others): outputs are empty,
+    final state = initial state, and d_initial_state = d_final_state."""
     H, K, V = 2, 32, 32
     inp = make_varlen_inputs([0, 0], H, K, V, "f32", seed=43, init_std=0.5, dfinal_std=0.5)
+    got = _run_varlen(_cuda(inp), 64, max_len=0)
+    assert got["o"].shape == (0, H, V)
+    assert torch.equal(got["final_state"].cpu(), inp["initial_state"])
+    assert torch.equal(got["d_initial_state"].cpu(), inp["d_final_state"])
+    # the tensor-core layout, with one empty sequence between two short ones
+    H, K, V = 2, 128, 128
+    inp = make_varlen_inputs([3, 0, 5], H, K, V, "bf16", seed=45, init_std=0.5, dfinal_std=0.5)
+    got = _run_varlen(_cuda(inp), 64)
+    assert torch.equal(got["final_state"][1].cpu(), inp["initial_state"][1])
+    assert torch.equal(got["d_initial_state"][1].cpu(), inp["d_final_state"][1])
+    inp = make_varlen_inputs([0, 0], H, K, V, "bf16", seed=46, init_std=0.5, dfinal_std=0.5)
     got = _run_varlen(_cuda(inp), 64, max_len=0)
     assert got["o"].shape == (0, H, V)
     assert torch.equal(got["final_state"].cpu(), inp["initial_state"])
@@ -162,11 +182,12 @@ def test_varlen_empty_batch_and_empty_sequences():
     ([0, 10, 100], 100, 64),       # a sequence longer than max_len
     ([3, 50, 100], 100, 64),       # does not start at row 0
 ])
-def test_varlen_invalid_offsets_are_flagged(cu, total, max_len):
+@pytest.mark.parametrize("dtype,K", [("f32", 32), ("bf16", 128)])
+def test_varlen_invalid_offsets_are_flagged(cu, total, max_len, dtype, K):
     """An invalid cu_seqlens (read only on the device) sets the error bit; the
     kernels stay inside the buffers and the binding raises with check=True."""
-    H, K, V = 2, 32, 32
-    inp = make_varlen_inputs([total], H, K, V, "f32", seed=44)
+    H, V = 2, K
+    inp = make_varlen_inputs([total], H, K, V, dtype, seed=44)
     d = _cuda(inp)
     d["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32, device="cuda")
     with pytest.raises(gdn.GdnError, match="cu_seqlens"):
@@ -179,3 +200,35 @@ def test_varlen_invalid_offsets_are_flagged(cu, total, max_len):
     d["cu_seqlens"] = torch.tensor([0, total], dtype=torch.int32, device="cuda")
     gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], None, None, check=True)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype,K,chunk", [("bf16", 128, 64), ("f32", 32, 16)])
+def test_reset_mask_matches_oracle(oracle_mod, dtype, K, chunk):
+    """Streams with reset positions (the state is cleared just before a reset
+    token; a reset at t = 0 discards the initial state) against the segment-wise
+    float64 oracle.  Resets: adjacent, at t = 0, at a chunk boundary, at T - 1."""
+    from oracle import resets
+    from gdn_testutil import compare
+
+    B, T, H = 3, 150, 2
+    w = custom(B=B, T=T, H=H, K=K, V=K, chunk=chunk, dtype=dtype, seed=47, init_std=0.3, dfinal_std=0.05)
+    inp = make_inputs(w)
+    reset = torch.zeros(B, T, dtype=torch.bool)
+    for b, t in [(0, 1), (0, 2), (0, 64), (1, 0), (1, 100), (2, 70), (2, 149)]:
+        reset[b, t] = True
+    d = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
+    ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
+    o, sT, saved, seg = gdn.gdn_reset_fwd(*ins, reset.cuda(), d["initial_state"], chunk=chunk, saved=True,
+                                          check=True)
+    g = gdn.gdn_reset_bwd(*ins, reset.cuda(), d["initial_state"], d["d_o"], d["d_final_state"], chunk=chunk,
+                          segments=seg, saved=saved, check=True)
+    torch.cuda.synchronize()
+    assert seg.S == B + 6
+    got = dict(o=to_np(o), final_state=to_np(sT), **{n: to_np(x) for n, x in zip(GRADS + ("d_initial_state",), g)})
+    npi = {n: to_np(inp[n]) for n in ("q", "k", "v", "alpha", "beta", "initial_state", "d_o", "d_final_state")}
+    args = [npi[n] for n in ("q", "k", "v", "alpha", "beta")]
+    ref_o, ref_sT = resets.fwd_resets(*args, reset.numpy(), npi["initial_state"])
+    ref = dict(o=ref_o, final_state=ref_sT)
+    ref.update(resets.bwd_resets(*args, reset.numpy(), npi["initial_state"], npi["d_o"], npi["d_final_state"]))
+    compare(got, ref, dtype)
+    assert np.all(got["d_initial_state"][1] == 0.0)  # row 1 was reset at t = 0
