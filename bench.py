@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from gated_delta_rule_19_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+from gated_delta_rule_19_gb300.inputs import WORKLOADS, custom, make_inputs  # noqa: E402
 
 METRIC = "gated-delta fwd & fwd+bwd tokens*heads/s at 1 GB300; % of bf16 TC roofline"
 UNIT = "tokens*heads/s"
@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step, prologue and varlen lines")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step, prologue, varlen and sequence-split lines")
     return ap.parse_args()
 
 
@@ -483,6 +483,59 @@ def measure_varlen(gdn, dev, stream, args, world, dense_ms, dense_token_heads):
             "rel_l2_longest_seq_vs_gdn_fwd": rel}
 
 
+def measure_split(gdn, dev, stream, args, world):
+    """Times one training step (gdn_fwd with saved states + gdn_bwd) on a long
+    context with few streams (B=1, T=65536, H=4, K=V=128 bf16: 4 streams, 1024
+    chunks each) with the within-call sequence split off and automatic.  The
+    unsplit scans run 1024 chunks in a row on 32 CTAs; the split cuts each
+    stream into pieces that run side by side.  Before timing, the two results are
+    compared (they differ by the fp32 rounding of the piece chain only)."""
+    w = custom("long_bf16_B1_T65536_H4_K128_V128", B=1, T=65536, H=4, K=128, V=128, chunk=64, dtype="bf16",
+               seed=7, init_std=0.1)
+    d = {n: (t.to(dev) if t is not None else None) for n, t in make_inputs(w).items()}
+    ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
+    p = gdn.make_problem(w.B, w.T, w.H, w.K, w.V, w.chunk, d["q"].dtype)
+    res = {}
+    outs = {}
+    for name, policy in (("unsplit", 1), ("split", 0)):
+        gdn.gdn_set_sequence_split(policy)
+        ws_f = torch.empty(gdn.gdn_fwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(gdn.gdn_bwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+        saved = torch.empty(gdn.gdn_saved_bytes(p), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(d["v"])
+        sT = torch.empty(w.B, w.H, w.V, w.K, dtype=torch.float32, device=dev)
+        grads = tuple(torch.empty_like(t) for t in ins)
+
+        def step():
+            gdn.gdn_fwd(*ins, d["initial_state"], o=o, final_state=sT, saved=saved, workspace=ws_f)
+            gdn.gdn_bwd(*ins, d["initial_state"], d["d_o"], None, saved=saved, grads=grads, workspace=ws_b)
+
+        for _ in range(max(3, args.warmup)):
+            step()
+        n = max(5, args.steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        gdn.gdn_profiler_start(64 * n + 64)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        gdn.gdn_profiler_stop()
+        ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+        split = {k: round(t / n * 1e3, 1) for k, (_, t) in gdn.gdn_profiler_summary().items()}
+        res[name] = {"ms_per_step": ms, "token_heads_per_s": world * w.token_heads / (ms / 1e3),
+                     "us_per_step_by_kernel": split}
+        outs[name] = (o.float().clone(), grads[0].float().clone())
+    gdn.gdn_set_sequence_split(0)
+    rel = lambda a, b: float((a - b).norm() / b.norm())
+    return {"workload": w.name, "step": "gdn_fwd(saved) + gdn_bwd", **res,
+            "speedup": res["unsplit"]["ms_per_step"] / res["split"]["ms_per_step"],
+            "rel_l2_split_vs_unsplit": {"o": rel(outs["split"][0], outs["unsplit"][0]),
+                                        "dq": rel(outs["split"][1], outs["unsplit"][1])}}
+
+
 def run_gdn(args, world, rank, local):
     from gated_delta_rule_19_gb300 import _build, gdn
 
@@ -668,6 +721,7 @@ def run_gdn(args, world, rank, local):
     decode = None if args.no_decode else measure_decode(gdn, dev, stream, args, world)
     prologue = None if args.no_decode else measure_prologue(gdn, dev, stream, args, world, w)
     varlen = None if args.no_decode else measure_varlen(gdn, dev, stream, args, world, ms_max, w.token_heads)
+    split = None if args.no_decode else measure_split(gdn, dev, stream, args, world)
 
     if rank != 0:
         return
@@ -699,6 +753,7 @@ def run_gdn(args, world, rank, local):
         "decode": decode,
         "prologue": prologue,
         "varlen": varlen,
+        "sequence_split": split,
         "gpu_launches": launches,
         "clocks": clk,
     }

@@ -213,7 +213,8 @@ const char* const kKernelNames[gdn::KID_COUNT] = {
     "scan_fwd_kernel(state-only)", "scan_bwd_kernel", "grad_kernel",
     "prep_fwd_tc", "scan_fwd_tc", "prep_fwd_tc(bwd)", "scan_fwd_tc(state-only)",
     "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc", "decode_kernel", "prologue_fwd_kernel",
-    "prologue_bwd_kernel", "varlen_offsets", "varlen_gather", "varlen_scatter"};
+    "prologue_bwd_kernel", "varlen_offsets", "varlen_gather", "varlen_scatter", "scan_fwd_tc(split pass 1)",
+    "scan_bwd_tc(split pass 1)", "scan_fwd_tc(transitions)", "split_combine"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -226,12 +227,71 @@ cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
     return e;
 }
 
+// Within-call sequence split (split.cu): every sequence's chunks are cut into P
+// pieces whose scans run side by side; the pieces' affine maps are chained by
+// the combine kernels and a second scan runs each piece from its true state.
+struct SplitCfg {
+    int P = 1;                     // pieces per sequence (1: no split)
+    int nseq = 0;                  // sequences (dense: B)
+    const int* seq_off = nullptr;  // chunk offsets of packed sequences, or NULL: rows of nc chunks
+    int nc = 0;
+};
+struct SplitBufs {
+    int* piece_off;
+    float* R;  // zero-start final states (forward) / zero-start state gradients (backward)
+    float* T;  // transitions
+    float* X;  // piece input states (forward) / piece output state gradients (backward)
+};
+
+int g_split = 0;  // gdn_set_sequence_split: 0 automatic, 1 off, n >= 2 pieces
+
+void carve_split(const gdn::Dims& fd, const SplitCfg& sp, Carver& cv, SplitBufs* sb) {
+    const size_t slots = (size_t)sp.nseq * sp.P * fd.H;
+    sb->piece_off = cv.take<int>((size_t)sp.nseq * sp.P + 1);
+    sb->R = cv.take<float>(slots * fd.V * fd.K);
+    sb->T = cv.take<float>(slots * fd.K * fd.K);
+    sb->X = cv.take<float>(slots * fd.V * fd.K);
+}
+
+// Pieces per sequence: the knob, else (dense calls only) a power of two when the
+// streams would leave most SMs idle, keeping >= 4 chunks per piece and the first
+// pass (states and transitions, 64-column slices) within one wave.
+int split_pieces(int64_t streams, int nc, bool automatic) {
+    if (g_split == 1) return 1;
+    if (g_split >= 2) return g_split;
+    if (!automatic) return 1;
+    const int64_t sms = gdn::sm_count();
+    if (streams * 8 > sms / 2) return 1;
+    int P = 1;
+    while (2 * P <= nc / 4 && 4 * (2 * P) * streams <= sms) P *= 2;
+    return P;
+}
+
+// The dims the tensor-core kernels run on, and the split of a dense call: a
+// split needs one row of chunks per head (B = 1, or T a multiple of the chunk so
+// that the batch rows lie back to back as whole chunks).
+SplitCfg dense_split(const gdn::Dims& d, gdn::Dims* fd) {
+    *fd = d;
+    SplitCfg sp;
+    if (d.B != 1 && d.T % d.C != 0) return sp;
+    const int P = split_pieces(d.NS(), d.NC, true);
+    if (P < 2) return sp;
+    fd->B = 1;
+    fd->T = d.B * d.T;
+    fd->NC = d.B * d.NC;
+    sp.P = P;
+    sp.nseq = d.B;
+    sp.nc = d.NC;
+    return sp;
+}
+
 // The tensor-core forward on dims d: the chunk kernel, then the scan.  The
-// workspace holds carve_tc(d) and `saved` (or NULL) carve_tc_saved(d); `sq`
-// (or NULL) runs packed sequences on the flat chunk layout.
+// workspace holds carve_tc(d) (then carve_split with a split) and `saved` (or
+// NULL) carve_tc_saved(d); `sq` (or NULL) runs packed sequences on the flat
+// chunk layout; `sp` (or NULL, or P = 1) splits every sequence into pieces.
 gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* alpha,
                       const void* beta, const float* initial_state, void* o, float* final_state, void* saved,
-                      void* workspace, const gdn::SeqMap* sq, cudaStream_t cs) {
+                      void* workspace, const gdn::SeqMap* sq, const SplitCfg* sp, cudaStream_t cs) {
     Carver cv{(char*)workspace};
     gdn::TcBufs tb;
     __nv_bfloat16* states = nullptr;
@@ -244,18 +304,44 @@ gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
     if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
     e = timed(gdn::KID_PREP_TC, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
+    if (!sp || sp->P < 2) {
+        e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
+            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state, states, cs, sq);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
+        return GDN_OK;
+    }
+    SplitBufs sb;
+    carve_split(d, *sp, cv, &sb);
+    const int npieces = sp->nseq * sp->P;
+    e = timed(gdn::KID_SPLIT_COMBINE, cs, [&] {
+        return gdn::launch_split_pieces(sp->nseq, sp->P, sp->nc, sp->seq_off, sb.piece_off, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "split pieces");
+    const gdn::SeqMap both{sb.piece_off, npieces, 1, sb.T};
+    e = timed(gdn::KID_SPLIT_FWD_P1, cs, [&] {
+        return gdn::launch_scan_fwd_tc(d, q, k, tb, nullptr, nullptr, sb.R, nullptr, cs, &both);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "split pass 1");
+    e = timed(gdn::KID_SPLIT_COMBINE, cs, [&] {
+        return gdn::launch_combine_fwd(sp->nseq, sp->P, d.H, initial_state, sb.R, sb.T, sb.X, final_state, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "split combine");
+    const gdn::SeqMap pieces{sb.piece_off, npieces};
     e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
-        return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, o, final_state, states, cs, sq);
+        return gdn::launch_scan_fwd_tc(d, q, k, tb, sb.X, o, nullptr, states, cs, &pieces);
     });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan kernel");
     return GDN_OK;
 }
 
-// The tensor-core backward on dims d (same conventions as run_fwd_tc).
+// The tensor-core backward on dims d (same conventions as run_fwd_tc; the
+// workspace holds carve_tc_bwd(d), then carve_split with a split).
 gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* alpha,
                       const void* beta, const float* initial_state, const void* saved, const void* d_o,
                       const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
-                      float* d_initial_state, void* workspace, const gdn::SeqMap* sq, cudaStream_t cs) {
+                      float* d_initial_state, void* workspace, const gdn::SeqMap* sq, const SplitCfg* sp,
+                      cudaStream_t cs) {
     Carver cv{(char*)workspace};
     gdn::TcBufs tb;
     gdn::TcBwdBufs tbb;
@@ -269,19 +355,69 @@ gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
         tb.err = err;
         states = st;
     }
+    const bool split = sp && sp->P >= 2;
+    SplitBufs sb{};
+    if (split) carve_split(d, *sp, cv, &sb);
+    const int npieces = split ? sp->nseq * sp->P : 0;
     cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
+    if (split) {
+        e = timed(gdn::KID_SPLIT_COMBINE, cs, [&] {
+            return gdn::launch_split_pieces(sp->nseq, sp->P, sp->nc, sp->seq_off, sb.piece_off, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "split pieces");
+    }
     if (!saved) {
         e = timed(gdn::KID_PREP_TC_BWD, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
-        e = timed(gdn::KID_STATE_TC, cs, [&] {
-            return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, nullptr, nullptr, tbb.states, cs, sq);
-        });
+        if (!split) {
+            e = timed(gdn::KID_STATE_TC, cs, [&] {
+                return gdn::launch_scan_fwd_tc(d, q, k, tb, initial_state, nullptr, nullptr, tbb.states, cs, sq);
+            });
+        } else {  // the chunk-start states by the split forward, states only
+            const gdn::SeqMap both{sb.piece_off, npieces, 1, sb.T};
+            e = timed(gdn::KID_SPLIT_FWD_P1, cs, [&] {
+                return gdn::launch_scan_fwd_tc(d, q, k, tb, nullptr, nullptr, sb.R, nullptr, cs, &both);
+            });
+            if (e == cudaSuccess)
+                e = timed(gdn::KID_SPLIT_COMBINE, cs, [&] {
+                    return gdn::launch_combine_fwd(sp->nseq, sp->P, d.H, initial_state, sb.R, sb.T, sb.X, nullptr,
+                                                   cs);
+                });
+            const gdn::SeqMap pieces{sb.piece_off, npieces};
+            if (e == cudaSuccess)
+                e = timed(gdn::KID_STATE_TC, cs, [&] {
+                    return gdn::launch_scan_fwd_tc(d, q, k, tb, sb.X, nullptr, nullptr, tbb.states, cs, &pieces);
+                });
+        }
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core state recompute");
+    } else if (split) {  // the pieces' transitions (the forward did not keep them)
+        const gdn::SeqMap trans{sb.piece_off, npieces, 2, sb.T};
+        e = timed(gdn::KID_SPLIT_TRANS, cs, [&] {
+            return gdn::launch_scan_fwd_tc(d, q, k, tb, nullptr, nullptr, nullptr, nullptr, cs, &trans);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "split transitions");
     }
-    e = timed(gdn::KID_SCAN_BWD_TC, cs, [&] {
-        return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, d_final_state, tbb, d_initial_state, cs, sq);
-    });
+    if (!split) {
+        e = timed(gdn::KID_SCAN_BWD_TC, cs, [&] {
+            return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, d_final_state, tbb, d_initial_state, cs, sq);
+        });
+    } else {
+        // pass 1: every piece from a zero end gradient; its dU, dS1 are rewritten by pass 2
+        const gdn::SeqMap pieces{sb.piece_off, npieces};
+        e = timed(gdn::KID_SPLIT_BWD_P1, cs, [&] {
+            return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, nullptr, tbb, sb.R, cs, &pieces);
+        });
+        if (e == cudaSuccess)
+            e = timed(gdn::KID_SPLIT_COMBINE, cs, [&] {
+                return gdn::launch_combine_bwd(sp->nseq, sp->P, d.H, d_final_state, sb.R, sb.T, sb.X,
+                                               d_initial_state, cs);
+            });
+        if (e == cudaSuccess)
+            e = timed(gdn::KID_SCAN_BWD_TC, cs, [&] {
+                return gdn::launch_scan_bwd_tc(d, q, k, d_o, tb, sb.X, tbb, nullptr, cs, &pieces);
+            });
+    }
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core reverse scan");
     e = timed(gdn::KID_GRAD_QK_TC, cs, [&] { return gdn::launch_grad_qk_tc(d, q, k, d_o, tb, states, tbb, dq, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (q, k)");
@@ -324,7 +460,12 @@ size_t gdn_fwd_workspace_bytes(const gdn_problem* p) {
     if (d.NS() * d.NC == 0) return 0;
     if (gdn::tc_fwd_supported(d, p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32)) {
         gdn::TcBufs tb;
-        return carve_tc(d, cv, &tb);
+        gdn::Dims fd;
+        const SplitCfg sp = dense_split(d, &fd);
+        carve_tc(fd, cv, &tb);
+        SplitBufs sb;
+        if (sp.P >= 2) carve_split(fd, sp, cv, &sb);
+        return cv.off;
     }
     gdn::ChunkBufs cb;
     return carve_chunk(d, cv, &cb, false);
@@ -350,7 +491,12 @@ size_t gdn_bwd_workspace_bytes(const gdn_problem* p) {
     if (gdn::tc_fwd_supported(d, in_type(p))) {
         gdn::TcBufs tb;
         gdn::TcBwdBufs tbb;
-        return carve_tc_bwd(d, cv, &tb, &tbb, true);
+        gdn::Dims fd;
+        const SplitCfg sp = dense_split(d, &fd);
+        carve_tc_bwd(fd, cv, &tb, &tbb, true);
+        SplitBufs sb;
+        if (sp.P >= 2) carve_split(fd, sp, cv, &sb);
+        return cv.off;
     }
     gdn::ChunkBufs cb;
     gdn::BwdBufs bb;
@@ -396,8 +542,12 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
         return e == cudaSuccess ? GDN_OK : cuda_fail(e, "empty-sequence state copy");
     }
     const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
-    if (gdn::tc_fwd_supported(d, ty))
-        return run_fwd_tc(d, q, k, v, alpha, beta, initial_state, o, final_state, saved, workspace, nullptr, cs);
+    if (gdn::tc_fwd_supported(d, ty)) {
+        gdn::Dims fd;
+        const SplitCfg sp = dense_split(d, &fd);
+        return run_fwd_tc(fd, q, k, v, alpha, beta, initial_state, o, final_state, saved, workspace, nullptr, &sp,
+                          cs);
+    }
     Carver cv{(char*)workspace};
     gdn::ChunkBufs cb;
     carve_chunk(d, cv, &cb, false);
@@ -423,6 +573,7 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
 namespace {
 struct VarlenPlan {
     bool flat;
+    int pieces;    // within-call split of every sequence (flat layout; 1: none)
     gdn::Dims pd;  // the problem the chunk kernels run on
     size_t off, inner, q, k, v, a, b, o, d_o, dq, dk, dv, da, db, total;
     // `saved` of the flat layout: chunk_off and the laid-out inputs (the backward
@@ -454,11 +605,20 @@ gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan
     const size_t BTH = (size_t)q.B * q.T * q.H;
     size_t inner_bytes = 0;
     Carver cv{nullptr};
+    L->pieces = L->flat ? split_pieces((int64_t)d.B * d.H, 0, false) : 1;
     if (q.NS() * q.NC > 0) {
         if (L->flat) {
             gdn::TcBufs tb;
             gdn::TcBwdBufs tbb;
             inner_bytes = bwd ? carve_tc_bwd(q, cv, &tb, &tbb, true) : carve_tc(q, cv, &tb);
+            if (L->pieces >= 2) {
+                SplitBufs sb;
+                SplitCfg sp;
+                sp.P = L->pieces;
+                sp.nseq = d.B;
+                carve_split(q, sp, cv, &sb);
+                inner_bytes = cv.off;
+            }
         } else {
             inner_bytes = bwd ? gdn_bwd_workspace_bytes(p) : gdn_fwd_workspace_bytes(p);
         }
@@ -607,8 +767,12 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu
             });
         if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
         const gdn::SeqMap sq{off, S};
+        SplitCfg sp;
+        sp.P = L.pieces;
+        sp.nseq = S;
+        sp.seq_off = off;
         st = run_fwd_tc(fd, lq, lk, lv, la, lb, initial_state, ws + L.o, final_state,
-                        saved ? (char*)saved + L.s_tc : nullptr, ws + L.inner, &sq, cs);
+                        saved ? (char*)saved + L.s_tc : nullptr, ws + L.inner, &sq, &sp, cs);
         if (st != GDN_OK) return st;
         gdn::FlatMoves mo{1, {ws + L.o}, {o}, {(int)p->H * vb}, {16}, {0u}};
         e = timed(gdn::KID_VARLEN_SCATTER, cs, [&] {
@@ -706,9 +870,13 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
             });
         if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
         const gdn::SeqMap sq{off, S};
+        SplitCfg sp;
+        sp.P = L.pieces;
+        sp.nseq = S;
+        sp.seq_off = off;
         st = run_bwd_tc(fd, lq, lk, lv, la, lb, initial_state, saved ? (const char*)saved + L.s_tc : nullptr,
                         ws + L.d_o, d_final_state, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db,
-                        d_initial_state, ws + L.inner, &sq, cs);
+                        d_initial_state, ws + L.inner, &sq, &sp, cs);
         if (st != GDN_OK) return st;
         gdn::FlatMoves mg{5,
                           {ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db},
@@ -875,9 +1043,12 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
         return e == cudaSuccess ? GDN_OK : cuda_fail(e, "empty-sequence state copy");
     }
     const gdn::InType ty = p->dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
-    if (gdn::tc_fwd_supported(d, ty))
-        return run_bwd_tc(d, q, k, v, alpha, beta, initial_state, saved, d_o, d_final_state, dq, dk, dv, dalpha,
-                          dbeta, d_initial_state, workspace, nullptr, cs);
+    if (gdn::tc_fwd_supported(d, ty)) {
+        gdn::Dims fd;
+        const SplitCfg sp = dense_split(d, &fd);
+        return run_bwd_tc(fd, q, k, v, alpha, beta, initial_state, saved, d_o, d_final_state, dq, dk, dv, dalpha,
+                          dbeta, d_initial_state, workspace, nullptr, &sp, cs);
+    }
     Carver cv{(char*)workspace};
     gdn::ChunkBufs cb;
     gdn::BwdBufs bb;
@@ -906,6 +1077,14 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
     if (e != cudaSuccess) return cuda_fail(e, "chunk gradient kernel");
     return GDN_OK;
 }
+
+gdn_status gdn_set_sequence_split(int pieces) {
+    if (pieces < 0 || pieces > 1024) return fail(GDN_ERR_INVALID_ARG, "pieces=%d must be in [0, 1024]", pieces);
+    g_split = pieces;
+    return GDN_OK;
+}
+
+int gdn_get_sequence_split(void) { return g_split; }
 
 int gdn_num_kernels(void) { return gdn::KID_COUNT; }
 

@@ -102,6 +102,10 @@ enum KernelId {
     KID_VARLEN_OFFSETS,  // offsets_kernel (chunk offsets of packed sequences)
     KID_VARLEN_GATHER,   // flat_kernel / rows16_kernel / elems_kernel, packed -> laid out
     KID_VARLEN_SCATTER,  // the same, laid out -> packed
+    KID_SPLIT_FWD_P1,    // scan_fwd_tc, split pass 1 (zero-start states and transitions of the pieces)
+    KID_SPLIT_BWD_P1,    // scan_bwd_tc, split pass 1 (zero-start state gradients of the pieces)
+    KID_SPLIT_TRANS,     // scan_fwd_tc, transitions only (backward with saved)
+    KID_SPLIT_COMBINE,   // pieces_kernel, combine_fwd_kernel, combine_bwd_kernel
     KID_COUNT
 };
 
@@ -147,11 +151,26 @@ bool tc_fwd_supported(const Dims& d, InType ty);
 // row of chunks and state slot s*H + h.  The scans take it to run one stream per
 // (sequence, head); the chunk-parallel kernels need nothing (their work is local
 // to a chunk).
+// The forward scan can also run the transition of a run of chunks: from S0 = I
+// with U~ read as 0 its final state is the product of the chunks' maps (the
+// within-call sequence split).  mode 0: the sequences only; 1: the sequences
+// (CTAs z < nseq) and their transitions (z >= nseq, final states to `trans`);
+// 2: the transitions only.
 struct SeqMap {
     const int* chunk_off;  // device, int32 [nseq + 1]
     int nseq;
+    int mode = 0;
+    float* trans = nullptr;  // [nseq * H, K, K] fp32, slot s*H + h
 };
 int tc_scan_vt(int64_t streams);
+
+// Within-call sequence split (split.cu): piece offsets, and the chains of the
+// pieces' affine maps forward (states) and backward (state gradients).
+cudaError_t launch_split_pieces(int S, int P, int nc, const int* chunk_off, int* piece_off, cudaStream_t st);
+cudaError_t launch_combine_fwd(int S, int P, int H, const float* s0, const float* R, const float* trans, float* s_in,
+                               float* sT, cudaStream_t st);
+cudaError_t launch_combine_bwd(int S, int P, int H, const float* dsT, const float* D, const float* trans,
+                               float* ds_out, float* ds0, cudaStream_t st);
 // Packed variable-length batches (varlen.cu): rows of packed [total, H, width]
 // tensors to and from the padded [S, T, H, width] layout.  `merge` (optional) is
 // ORed into `err` once.

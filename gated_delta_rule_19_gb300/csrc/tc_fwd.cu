@@ -491,7 +491,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_Ut, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_st, const float* __restrict__ G, const float* s0,
-            float* sT, int write_o, int write_states, const int* __restrict__ chunk_off, int* err) {
+            float* sT, int write_o, int write_states, const int* __restrict__ chunk_off, int nseq, int tmode,
+            float* trans, int* err) {
     using P = ScanPlan<Vt>;
     constexpr int HV = Vt / 2;  // columns per thread
     extern __shared__ unsigned char smraw[];
@@ -512,14 +513,24 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // packed sequences (chunk_off) the data is one row of chunks per head (B = 1):
     // sequence s = blockIdx.z runs chunks chunk_off[s] .. chunk_off[s+1]-1 of it
     // and keeps its state in slot s*H + h.  c below counts this CTA's chunks.
+    // A transition CTA (tmode) starts from S0 = I, reads U~ as 0 and writes its
+    // final state, the product of its chunks' maps, to `trans`.
     int b = blockIdx.z, c0 = 0, NC = d.NC;
-    const int64_t sidx = (int64_t)blockIdx.z * d.H + h;  // state slot
+    bool tr = tmode == 2;
+    if (tmode == 1 && b >= nseq) {
+        tr = true;
+        b -= nseq;
+    }
+    const int64_t sidx = (int64_t)b * d.H + h;  // state slot
     if (chunk_off) {
-        c0 = chunk_off[blockIdx.z];
-        NC = chunk_off[blockIdx.z + 1] - c0;
+        c0 = chunk_off[b];
+        NC = chunk_off[b + 1] - c0;
         b = 0;
     }
     const int64_t cbase = ((int64_t)b * d.H + h) * d.NC + c0;  // global index of chunk c = 0
+    const float ut_w = tr ? 0.f : 1.f;
+    float* const s_out = tr ? trans : sT;
+    const bool wr_o = write_o && !tr, wr_states = write_states && !tr;
 
     auto issue_loads = [&](int c) {
         unsigned char* st = sm + (c & 1) * P::STAGE;
@@ -550,7 +561,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int k = lanerow;
     float s[HV];
 #pragma unroll
-    for (int j = 0; j < HV; ++j) s[j] = s0 ? s0[(sidx * d.V + v0 + cb + j) * kD + k] : 0.f;
+    for (int j = 0; j < HV; ++j)
+        s[j] = tr ? (v0 + cb + j == k ? 1.f : 0.f) : (s0 ? s0[(sidx * d.V + v0 + cb + j) * kD + k] : 0.f);
     auto write_state_operand = [&]() {
         // MN-major, no swizzle: element (v, k) at (v/8)*2048 + k*16 + (v%8)*2
 #pragma unroll
@@ -628,7 +640,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         unsigned char* st = sm + stg * P::STAGE;
         const int64_t chunk = cbase + c;
         if (issuer) {
-            if (write_states) {  // chunk-start state -> saved boundary states, by TMA
+            if (wr_states) {  // chunk-start state -> saved boundary states, by TMA
                 tma_store_3d(&tm_st, sm + P::S_OP, 0, (int)(chunk * kD), v0 / 8);
                 bulk_commit();
             }
@@ -676,9 +688,9 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const uint32_t uw4[4] = {uq.x, uq.y, uq.z, uq.w};
                 float u[8], uh[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    u[2 * e] = bf_lo(uw4[e]) - xg[8 * g + 2 * e];
-                    u[2 * e + 1] = bf_hi(uw4[e]) - xg[8 * g + 2 * e + 1];
+                for (int e = 0; e < 4; ++e) {  // ut_w = 1 gives exactly Ut - X
+                    u[2 * e] = fmaf(ut_w, bf_lo(uw4[e]), -xg[8 * g + 2 * e]);
+                    u[2 * e + 1] = fmaf(ut_w, bf_hi(uw4[e]), -xg[8 * g + 2 * e + 1]);
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) uh[j] = er * u[j];
@@ -696,7 +708,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!ok) break;
         fence_after_sync();
         if (issuer) {
-            if (c > 0 && write_o) {  // output tile of the previous chunk
+            if (c > 0 && wr_o) {  // output tile of the previous chunk
                 tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + c - 1) * kC, v0 / 8, h, b);
                 bulk_commit();
             }
@@ -744,14 +756,14 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_proxy_async();
         fence_before_sync();
         ok = __syncthreads_and(ok);
-        if (issuer && ok && write_o) {
+        if (issuer && ok && wr_o) {
             tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + NC - 1) * kC, v0 / 8, h, b);
             bulk_commit();
         }
     }
-    if (ok && sT) {
+    if (ok && s_out) {
 #pragma unroll
-        for (int j = 0; j < HV; ++j) sT[(sidx * d.V + v0 + cb + j) * kD + k] = s[j];
+        for (int j = 0; j < HV; ++j) s_out[(sidx * d.V + v0 + cb + j) * kD + k] = s[j];
     }
     if (issuer) {
         if (!ok) {
@@ -786,9 +798,13 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     auto kern = scan_fwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(kD / Vt, d.H, sq ? sq->nseq : d.B);
-    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, o != nullptr,
-                                     states != nullptr, sq ? sq->chunk_off : nullptr, tb.err);
+    const int mode = sq ? sq->mode : 0;
+    const int nseq = sq ? sq->nseq : d.B;
+    dim3 grid(kD / Vt, d.H, mode == 1 ? 2 * nseq : nseq);
+    const bool tr_only = mode == 2;
+    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, (o != nullptr && !tr_only),
+                                     (states != nullptr && !tr_only), sq ? sq->chunk_off : nullptr, nseq, mode,
+                                     sq ? sq->trans : nullptr, tb.err);
     return cudaGetLastError();
 }
 
@@ -823,7 +839,8 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
 
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
                                void* o, float* sT, __nv_bfloat16* states, cudaStream_t st, const SeqMap* sq) {
-    switch (tc_scan_vt(sq ? (int64_t)sq->nseq * d.H : d.NS())) {
+    const int64_t streams = sq ? (int64_t)sq->nseq * d.H * (sq->mode == 1 ? 2 : 1) : d.NS();
+    switch (tc_scan_vt(streams)) {
         case 16: return launch_scan_vt<16>(d, q, k, tb, s0, o, sT, states, st, sq);
         case 32: return launch_scan_vt<32>(d, q, k, tb, s0, o, sT, states, st, sq);
         default: return launch_scan_vt<64>(d, q, k, tb, s0, o, sT, states, st, sq);

@@ -74,6 +74,9 @@ def load_library():
     lib.gdn_varlen_fwd.restype = ctypes.c_int
     lib.gdn_varlen_bwd.argtypes = [P, ctypes.c_int64] + [_vp] * 17 + [ctypes.c_size_t, _vp]
     lib.gdn_varlen_bwd.restype = ctypes.c_int
+    lib.gdn_set_sequence_split.argtypes = [ctypes.c_int]
+    lib.gdn_set_sequence_split.restype = ctypes.c_int
+    lib.gdn_get_sequence_split.restype = ctypes.c_int
     lib.gdn_num_kernels.restype = ctypes.c_int
     lib.gdn_kernel_name.argtypes = [ctypes.c_int]
     lib.gdn_kernel_name.restype = ctypes.c_char_p
@@ -93,7 +96,8 @@ EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_works
             "gdn_num_kernels", "gdn_kernel_name", "gdn_profiler_start", "gdn_profiler_stop",
             "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode",
             "gdn_prologue_fwd", "gdn_prologue_bwd", "gdn_varlen_fwd_workspace_bytes",
-            "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_saved_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd")
+            "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_saved_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd",
+            "gdn_set_sequence_split", "gdn_get_sequence_split")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -254,6 +258,16 @@ def gdn_bwd(q, k, v, alpha, beta, initial_state, d_o, d_final_state=None, *, sav
                      _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
     _check(st)
     return dq, dk, dv, da, db, d_initial_state
+
+
+def gdn_set_sequence_split(pieces: int) -> None:
+    """Within-call sequence split policy for the calls that follow: 0 automatic
+    (default), 1 never, n >= 2 pieces per sequence (see include/gdn.h)."""
+    _check(load_library().gdn_set_sequence_split(int(pieces)))
+
+
+def gdn_get_sequence_split() -> int:
+    return int(load_library().gdn_get_sequence_split())
 
 
 def gdn_num_kernels() -> int:

@@ -11,6 +11,9 @@ Recipe (the same for every workload):
     random numbers does not depend on which are used);
   * q, k ~ N(0,1) then divided by their L2 norm over the key dimension, per
     (b, t, h); v ~ N(0,1); alpha = exp(-softplus(x)); beta = sigmoid(x);
+  * slow decay (``alpha_lo`` > 0): alpha = alpha_lo + (1 - alpha_lo) * alpha,
+    gates in (alpha_lo, 1) whose state survives many chunks (with the default
+    gates, about 0.5 on average, a chunk's decay is below float32 resolution);
   * initial state ~ N(0, init_std^2) (zero state when init_std == 0);
     d_o ~ N(0,1); d_final_state ~ N(0, dfinal_std^2) (absent when 0);
   * finally every tensor except the fp32 states is cast to the run dtype.
@@ -44,6 +47,7 @@ class Workload:
     backward: bool = False
     calls: int = 1        # streaming: the sequence is processed in this many calls
     extra: dict = field(default_factory=dict)
+    alpha_lo: float = 0.0  # slow decay: alpha in (alpha_lo, 1)
 
     @property
     def token_heads(self) -> int:
@@ -108,6 +112,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-30)
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
     alpha = torch.exp(-F.softplus(a_logit))
+    if w.alpha_lo > 0:
+        alpha = w.alpha_lo + (1.0 - w.alpha_lo) * alpha
     beta = torch.sigmoid(b_logit)
     dt = torch_dtype(w.dtype)
     out = dict(
@@ -122,9 +128,10 @@ def make_inputs(w: Workload, device="cpu") -> dict:
 
 
 def custom(name="custom", B=1, T=64, H=2, K=16, V=16, chunk=16, dtype="f32", seed=0,
-           init_std=0.0, dfinal_std=0.0, backward=True) -> Workload:
+           init_std=0.0, dfinal_std=0.0, backward=True, alpha_lo=0.0) -> Workload:
     """A workload of any shape with the same recipe (for edge-case tests)."""
-    return Workload(name, B, T, H, K, V, chunk, dtype, seed, init_std, dfinal_std, backward)
+    return Workload(name, B, T, H, K, V, chunk, dtype, seed, init_std, dfinal_std, backward,
+                    alpha_lo=alpha_lo)
 
 
 def make_prologue_inputs(B, T, H, K, dtype="f32", seed=0, scale=3.0, logit_scale=2.0) -> dict:
@@ -175,7 +182,8 @@ VARLEN_WORKLOADS = {
 }
 
 
-def make_varlen_inputs(lengths, H, K, V, dtype="f32", seed=0, init_std=0.0, dfinal_std=0.0) -> dict:
+def make_varlen_inputs(lengths, H, K, V, dtype="f32", seed=0, init_std=0.0, dfinal_std=0.0,
+                       alpha_lo=0.0) -> dict:
     """Packed inputs of len(lengths) sequences with the recipe of
     :func:`make_inputs` (same distributions and draw order), but with q, k, v,
     alpha, beta, d_o laid out [total, H, ...] and one initial state and
@@ -196,11 +204,14 @@ def make_varlen_inputs(lengths, H, K, V, dtype="f32", seed=0, init_std=0.0, dfin
     q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-30)
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
     dt = torch_dtype(dtype)
+    alpha = torch.exp(-F.softplus(a_logit))
+    if alpha_lo > 0:
+        alpha = alpha_lo + (1.0 - alpha_lo) * alpha
     cu = torch.zeros(S + 1, dtype=torch.int32)
     if S:
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
     return dict(
-        q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=torch.exp(-F.softplus(a_logit)).to(dt),
+        q=q.to(dt), k=k.to(dt), v=v.to(dt), alpha=alpha.to(dt),
         beta=torch.sigmoid(b_logit).to(dt),
         initial_state=(s0 * init_std) if init_std > 0 else None,
         d_o=d_o.to(dt),

@@ -237,6 +237,32 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
                           float* d_initial_state, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Within-call sequence split (two-level scan) of the tensor-core path.  The
+ * chunk scans are sequential over a stream's chunks; with few streams most SMs
+ * would idle, so each stream's chunks are cut into pieces that run side by side:
+ * over a run of chunks the state map is affine, S_out = S_in P^T + R ("Sparse
+ * Delta Memory: layer and kernels", What the layer computes: Phase 2 applies the
+ * corrected writes to the chunk-start state), so a first pass computes every
+ * piece's R (zero start) and P (its chunks' transition), a short chain links the
+ * pieces, and a second pass runs every piece from its true start state.  The
+ * backward does the same with the transposed maps.  The results equal the
+ * unsplit scan's up to float32 rounding of the chain.
+ *
+ * gdn_set_sequence_split sets the policy for the calls that follow (process-wide):
+ *   0 (default): automatic for gdn_fwd / gdn_bwd on the tensor-core path when
+ *      the streams (B*H) would leave most SMs idle and the batch rows are whole
+ *      chunks apart (B = 1 or T a multiple of the chunk); none for varlen calls;
+ *   1: never;
+ *   n >= 2: n pieces per sequence wherever the layout allows it (dense calls as
+ *      above, and every varlen call on the tensor-core path).
+ * The workspace sizes depend on it: query them under the policy of the calls,
+ * and run a backward under the policy of its forward (their `saved` layouts
+ * differ).  Returns GDN_ERR_INVALID_ARG outside [0, 1024].
+ */
+gdn_status gdn_set_sequence_split(int pieces);
+int gdn_get_sequence_split(void);
+
+/*
  * gdn_decode -- the recurrent step, for decoding: advances `state` through the
  * call's T tokens (usually 1) and writes their outputs.  It computes exactly the
  * token recurrence of section 1 ("OpenGDN", Core operator reference: a stream

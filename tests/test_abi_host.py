@@ -211,3 +211,31 @@ def test_varlen_arguments_rejected_before_launch(lib):
     assert _varlen_bwd(lib, p, 200, ds0=FAKE + (6 << 30)) == INVALID  # d_initial_state is dq
     assert _varlen_bwd(lib, p, 200, ws_bytes=0) == WS
     assert _varlen_bwd(lib, p, 301) == INVALID
+
+
+def test_sequence_split_policy(lib):
+    h = lib.load_library()
+    INVALID = 1
+    assert h.gdn_set_sequence_split(-1) == INVALID
+    assert h.gdn_set_sequence_split(2000) == INVALID
+    few = lib.make_problem(1, 2048, 2, 128, 128, 64, 1)   # 2 streams: the automatic policy splits
+    many = lib.make_problem(8, 4096, 6, 128, 128, 64, 1)  # 48 streams: it does not
+    try:
+        assert h.gdn_set_sequence_split(1) == 0 and h.gdn_get_sequence_split() == 1
+        off_f = h.gdn_fwd_workspace_bytes(ctypes.byref(few))
+        off_b = h.gdn_bwd_workspace_bytes(ctypes.byref(few))
+        off_many = h.gdn_fwd_workspace_bytes(ctypes.byref(many))
+        assert h.gdn_set_sequence_split(0) == 0
+        assert h.gdn_fwd_workspace_bytes(ctypes.byref(few)) > off_f  # piece states and transitions
+        assert h.gdn_bwd_workspace_bytes(ctypes.byref(few)) > off_b
+        assert h.gdn_fwd_workspace_bytes(ctypes.byref(many)) == off_many
+        saved = h.gdn_saved_bytes(ctypes.byref(few))
+        assert h.gdn_set_sequence_split(5) == 0
+        assert h.gdn_saved_bytes(ctypes.byref(few)) == saved  # the split keeps nothing extra
+        # B > 1 with T not a multiple of the chunk: the rows are not whole chunks apart, no split
+        ragged = lib.make_problem(2, 100, 2, 128, 128, 64, 1)
+        w5 = h.gdn_fwd_workspace_bytes(ctypes.byref(ragged))
+        assert h.gdn_set_sequence_split(1) == 0
+        assert h.gdn_fwd_workspace_bytes(ctypes.byref(ragged)) == w5
+    finally:
+        h.gdn_set_sequence_split(0)

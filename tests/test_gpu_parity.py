@@ -197,6 +197,18 @@ def test_tc_backward_recompute_equals_saved():
         np.testing.assert_array_equal(a[n], b[n], err_msg=n)
 
 
+@pytest.mark.parametrize("dtype,K,V,C", [("bf16", 128, 128, 64), ("f32", 32, 64, 32), ("bf16", 64, 64, 64)])
+def test_slow_decay_long_range(oracle_mod, dtype, K, V, C):
+    """Gates in (0.97, 1): the state carries across many chunks (about 40% of it
+    survives a 64-token chunk), so cross-chunk propagation, the initial state and
+    the final-state gradient all reach far; forward and backward against the
+    oracle on every stream."""
+    w = custom(B=2, T=1000, H=2, K=K, V=V, chunk=C, dtype=dtype, seed=600 + K + C, init_std=0.3, dfinal_std=0.05,
+               alpha_lo=0.97)
+    inp = make_inputs(w)
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), dtype)
+
+
 def test_tc_error_flag_stays_clear():
     """The tensor-core kernels' bounded waits never give up in a normal run: the
     error word at the start of the caller's workspace stays 0."""

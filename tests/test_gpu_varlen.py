@@ -71,10 +71,13 @@ CASES = [
 ]
 
 
+# alpha_lo = 0.97: slow decay, each sequence's initial state and the state
+# carried across its chunks reach far (with the default gates a chunk forgets).
+@pytest.mark.parametrize("alpha_lo", [0.0, 0.97])
 @pytest.mark.parametrize("lengths,H,K,V,chunk,dtype", CASES)
-def test_varlen_matches_oracle_per_sequence(oracle_mod, lengths, H, K, V, chunk, dtype):
+def test_varlen_matches_oracle_per_sequence(oracle_mod, lengths, H, K, V, chunk, dtype, alpha_lo):
     inp = make_varlen_inputs(lengths, H, K, V, dtype, seed=700 + len(lengths) + K, init_std=0.3,
-                             dfinal_std=0.05)
+                             dfinal_std=0.05, alpha_lo=alpha_lo)
     got = _run_varlen(_cuda(inp), chunk)
     tol = TOL[dtype]
     cu = inp["cu_seqlens"].tolist()
@@ -211,7 +214,9 @@ def test_reset_mask_matches_oracle(oracle_mod, dtype, K, chunk):
     from gdn_testutil import compare
 
     B, T, H = 3, 150, 2
-    w = custom(B=B, T=T, H=H, K=K, V=K, chunk=chunk, dtype=dtype, seed=47, init_std=0.3, dfinal_std=0.05)
+    # slow decay: without a reset the state would carry across the reset points
+    w = custom(B=B, T=T, H=H, K=K, V=K, chunk=chunk, dtype=dtype, seed=47, init_std=0.3, dfinal_std=0.05,
+               alpha_lo=0.97)
     inp = make_inputs(w)
     reset = torch.zeros(B, T, dtype=torch.bool)
     for b, t in [(0, 1), (0, 2), (0, 64), (1, 0), (1, 100), (2, 70), (2, 149)]:
