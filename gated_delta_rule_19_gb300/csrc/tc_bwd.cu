@@ -50,7 +50,21 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 
 template <int W>
 __device__ __forceinline__ void tmem_cols(uint32_t taddr, float* f) {
-    if constexpr (W == 16) {
+    if constexpr (W == 24) {
+        uint32_t a[8], b[8], c[8];
+        tmem_ld8(taddr, a);
+        tmem_ld8(taddr + 8, b);
+        tmem_ld8(taddr + 16, c);
+        tmem_wait_ld(a);
+        tmem_wait_ld(b);
+        tmem_wait_ld(c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            f[j] = __uint_as_float(a[j]);
+            f[8 + j] = __uint_as_float(b[j]);
+            f[16 + j] = __uint_as_float(c[j]);
+        }
+    } else if constexpr (W == 16) {
         uint32_t r[16];
         tmem_ld16(taddr, r);
         tmem_wait_ld(r);
@@ -66,7 +80,30 @@ __device__ __forceinline__ void tmem_cols(uint32_t taddr, float* f) {
 }
 template <int W>
 __device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, float* fb) {
-    if constexpr (W == 16) {
+    if constexpr (W == 24) {
+        uint32_t a0[8], a1[8], a2[8], b0[8], b1[8], b2[8];
+        tmem_ld8(ta, a0);
+        tmem_ld8(ta + 8, a1);
+        tmem_ld8(ta + 16, a2);
+        tmem_ld8(tb, b0);
+        tmem_ld8(tb + 8, b1);
+        tmem_ld8(tb + 16, b2);
+        tmem_wait_ld(a0);
+        tmem_wait_ld(a1);
+        tmem_wait_ld(a2);
+        tmem_wait_ld(b0);
+        tmem_wait_ld(b1);
+        tmem_wait_ld(b2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            fa[j] = __uint_as_float(a0[j]);
+            fa[8 + j] = __uint_as_float(a1[j]);
+            fa[16 + j] = __uint_as_float(a2[j]);
+            fb[j] = __uint_as_float(b0[j]);
+            fb[8 + j] = __uint_as_float(b1[j]);
+            fb[16 + j] = __uint_as_float(b2[j]);
+        }
+    } else if constexpr (W == 16) {
         uint32_t a[16], b2[16];
         tmem_ld16(ta, a);
         tmem_ld16(tb, b2);
@@ -207,7 +244,10 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int k = lanerow;
     float ds[HV];
 #pragma unroll
-    for (int j = 0; j < HV; ++j) ds[j] = dsT ? dsT[(sidx * d.V + v0 + cb + j) * kD + k] : 0.f;
+    for (int j = 0; j < HV; ++j) {
+        const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
+        ds[j] = (dsT && ((kD % Vt == 0) || v < kD)) ? dsT[(sidx * d.V + v) * kD + k] : 0.f;
+    }
     auto write_ds_operand = [&]() {
 #pragma unroll
         for (int g = 0; g < HV / 8; ++g)
@@ -366,7 +406,8 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     if (ok && ds0) {
 #pragma unroll
-        for (int j = 0; j < HV; ++j) ds0[(sidx * d.V + v0 + cb + j) * kD + k] = ds[j];
+        for (int j = 0; j < HV; ++j)
+            if ((kD % Vt == 0) || v0 + cb + j < kD) ds0[(sidx * d.V + v0 + cb + j) * kD + k] = ds[j];
     }
     if (issuer) {
         if (!ok)
@@ -1123,7 +1164,7 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
     auto kern = scan_bwd_tc<Vt>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(kD / Vt, d.H, sq ? sq->nseq : d.B);
+    dim3 grid((kD + Vt - 1) / Vt, d.H, sq ? sq->nseq : d.B);
     kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0,
                                      sq ? sq->chunk_off : nullptr, tb.err);
     return cudaGetLastError();
@@ -1137,6 +1178,7 @@ cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, cons
     switch (tc_scan_vt(sq ? (int64_t)sq->nseq * d.H : d.NS())) {
         case 16: return launch_scan_bwd_vt<16>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
         case 32: return launch_scan_bwd_vt<32>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
+        case 48: return launch_scan_bwd_vt<48>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
         default: return launch_scan_bwd_vt<64>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
     }
 }

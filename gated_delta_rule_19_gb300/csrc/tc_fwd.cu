@@ -426,24 +426,41 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 // ---------------------------------------------------------------------------
 template <int Vt>
 struct ScanPlan {
+    // TMA stages: three (two chunks of lead) where they fit, up to 48-column slices
+    static constexpr int NS = Vt <= 48 ? 3 : 2;
     // stage: [W_0 | Q_0 | W_1 | Q_1] (stacked A of one M=128 MMA) | K_0 | K_1 | Mqk | Ut slice
     static constexpr int OFF_WQ = 0, OFF_K = 32768, OFF_M = 49152, OFF_UT = 57344;
-    static constexpr int STAGE = 57344 + kC * Vt * 2;
-    static constexpr int S_OP = 2 * STAGE;           // S0^T [Vt/8][128 k][8] (MN-major, no swizzle)
+    static constexpr int STAGE = 57344 + kC * Vt * 2;  // a multiple of 1024 (swizzled operands)
+    static constexpr int S_OP = NS * STAGE;          // S0^T [Vt/8][128 k][8] (MN-major, no swizzle)
     static constexpr int U_OP = S_OP + kD * Vt * 2;  // U  [Vt/8][64 tok][8]
     static constexpr int UH_OP = U_OP + kC * Vt * 2; // Uh
     static constexpr int O_OP = UH_OP + kC * Vt * 2; // output tile, same layout
-    static constexpr int BAR = O_OP + kC * Vt * 2;   // tma[2], XY, S, O
+    static constexpr int BAR = O_OP + kC * Vt * 2;   // tma[NS], XY, S, O, then the TMEM slot at +48
     static constexpr int END = BAR + 64;
     static constexpr size_t SMEM = END + 1024;
     // TMEM: [X;Y] (two buffers), O2, DS, each Vt columns
     static constexpr uint32_t TMEM_COLS = (4 * Vt <= 32) ? 32 : (4 * Vt <= 64 ? 64 : (4 * Vt <= 128 ? 128 : 256));
 };
 
-// Loads W consecutive fp32 TMEM columns (W = 16 or 32) of this thread's lane.
+// Loads W consecutive fp32 TMEM columns (W = 16, 24 or 32) of this thread's lane;
+// 24 columns are three 8-column loads (each starting on a multiple of 8).
 template <int W>
 __device__ __forceinline__ void tmem_cols(uint32_t taddr, float* f) {
-    if constexpr (W == 16) {
+    if constexpr (W == 24) {
+        uint32_t a[8], b[8], c[8];
+        tmem_ld8(taddr, a);
+        tmem_ld8(taddr + 8, b);
+        tmem_ld8(taddr + 16, c);
+        tmem_wait_ld(a);
+        tmem_wait_ld(b);
+        tmem_wait_ld(c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            f[j] = __uint_as_float(a[j]);
+            f[8 + j] = __uint_as_float(b[j]);
+            f[16 + j] = __uint_as_float(c[j]);
+        }
+    } else if constexpr (W == 16) {
         uint32_t r[16];
         tmem_ld16(taddr, r);
         tmem_wait_ld(r);
@@ -460,7 +477,30 @@ __device__ __forceinline__ void tmem_cols(uint32_t taddr, float* f) {
 // Two W-column groups, one wait.
 template <int W>
 __device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, float* fb) {
-    if constexpr (W == 16) {
+    if constexpr (W == 24) {
+        uint32_t a0[8], a1[8], a2[8], b0[8], b1[8], b2[8];
+        tmem_ld8(ta, a0);
+        tmem_ld8(ta + 8, a1);
+        tmem_ld8(ta + 16, a2);
+        tmem_ld8(tb, b0);
+        tmem_ld8(tb + 8, b1);
+        tmem_ld8(tb + 16, b2);
+        tmem_wait_ld(a0);
+        tmem_wait_ld(a1);
+        tmem_wait_ld(a2);
+        tmem_wait_ld(b0);
+        tmem_wait_ld(b1);
+        tmem_wait_ld(b2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            fa[j] = __uint_as_float(a0[j]);
+            fa[8 + j] = __uint_as_float(a1[j]);
+            fa[16 + j] = __uint_as_float(a2[j]);
+            fb[j] = __uint_as_float(b0[j]);
+            fb[8 + j] = __uint_as_float(b1[j]);
+            fb[16 + j] = __uint_as_float(b2[j]);
+        }
+    } else if constexpr (W == 16) {
         uint32_t a[16], b2[16];
         tmem_ld16(ta, a);
         tmem_ld16(tb, b2);
@@ -482,11 +522,15 @@ __device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, 
     }
 }
 
-// 256 threads.  Warp w reaches TMEM lanes 32*(w%4) ..; warps w and w+4 split the
-// columns.  Lanes 0-63 hold X = W S0^T (rows of U), lanes 64-127 hold Y = Q S0^T
-// and the output term; the state update uses all 128 lanes (rows k).
+// 320 threads: warps 0-7 run the epilogues, warp 8 issues the MMAs and warp 9 the
+// TMA copies (lane 0 of each), so no epilogue waits behind an instruction issue
+// and the two issue streams run side by side.  Warp w < 8 reaches TMEM lanes
+// 32*(w%4) ..; warps w and w+4 split the columns.  Lanes 0-63 hold X = W S0^T
+// (rows of U), lanes 64-127 hold Y = Q S0^T and the output term; the state update
+// uses all 128 lanes (rows k).  The three roles run separate loops with the same
+// two block-wide barriers per chunk.
 template <int Vt>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(320, 1)
 scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_Ut, const __grid_constant__ CUtensorMap tm_o,
@@ -495,19 +539,21 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             float* trans, int* err) {
     using P = ScanPlan<Vt>;
     constexpr int HV = Vt / 2;  // columns per thread
+    constexpr int NS = P::NS;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     uint64_t* tbar = (uint64_t*)(sm + P::BAR);
-    uint64_t* barXY = tbar + 2;
-    uint64_t* barS = tbar + 3;
-    uint64_t* barO = tbar + 4;
+    uint64_t* barXY = tbar + NS;
+    uint64_t* barS = tbar + NS + 1;
+    uint64_t* barO = tbar + NS + 2;
     uint32_t* tslot = (uint32_t*)(sm + P::BAR + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int sub = warp & 3, half = warp >> 2;
-    const int lanerow = 32 * sub + lane;  // TMEM lane of this thread
+    const bool mma_warp = warp == 8, tma_warp = warp == 9, epi = warp < 8;
+    const bool mma_issuer = tid == 256, tma_issuer = tid == 288;
+    const int sub = warp & 3, half = (warp >> 2) & 1;
+    const int lanerow = 32 * sub + lane;  // TMEM lane of this thread (epilogue warps)
     const int cb = half * HV;             // first column of this thread
-    const bool issuer = tid == 96;        // warp 3 (output side) issues MMAs and copies
     const int v0 = blockIdx.x * Vt, h = blockIdx.y;
     // Stream (b = blockIdx.z, h) runs chunks 0 .. d.NC-1 of its row of chunks.  With
     // packed sequences (chunk_off) the data is one row of chunks per head (B = 1):
@@ -532,11 +578,12 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     float* const s_out = tr ? trans : sT;
     const bool wr_o = write_o && !tr, wr_states = write_states && !tr;
 
+    // Chunk c's tiles into stage c % NS (the n-th use of a stage completes phase n & 1).
     auto issue_loads = [&](int c) {
-        unsigned char* st = sm + (c & 1) * P::STAGE;
+        unsigned char* st = sm + (c % NS) * P::STAGE;
         const int row = (int)((cbase + c) * kC);
         const int t0 = (c0 + c) * kC;
-        uint64_t* bar = &tbar[c & 1];
+        uint64_t* bar = &tbar[c % NS];
         mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         for (int j = 0; j < 2; ++j) {
             tma_load_2d(st + P::OFF_WQ + j * 16384, &tm_W, bar, 64 * j, row);
@@ -547,11 +594,11 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tma_load_3d(st + P::OFF_UT, &tm_Ut, bar, 0, row, v0 / 8);
     };
 
-    if (issuer) {
-        for (int i = 0; i < 5; ++i) mbar_init(&tbar[i], 1);
+    int issued = 0;  // chunks whose loads were issued (TMA issuer)
+    if (tma_issuer) {
+        for (int i = 0; i < NS + 3; ++i) mbar_init(&tbar[i], 1);
         fence_mbar_init();
-        if (NC > 0) issue_loads(0);
-        if (NC > 1) issue_loads(1);
+        for (; issued < NS - 1 && issued < NC; ++issued) issue_loads(issued);
     }
     if (warp == 0) {
         tmem_alloc(tslot, P::TMEM_COLS);
@@ -561,8 +608,11 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int k = lanerow;
     float s[HV];
 #pragma unroll
-    for (int j = 0; j < HV; ++j)
-        s[j] = tr ? (v0 + cb + j == k ? 1.f : 0.f) : (s0 ? s0[(sidx * d.V + v0 + cb + j) * kD + k] : 0.f);
+    for (int j = 0; j < HV; ++j) {
+        const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
+        const bool vok = (kD % Vt == 0) || v < kD;
+        s[j] = (!epi || !vok) ? 0.f : (tr ? (v == k ? 1.f : 0.f) : (s0 ? s0[(sidx * d.V + v) * kD + k] : 0.f));
+    }
     auto write_state_operand = [&]() {
         // MN-major, no swizzle: element (v, k) at (v/8)*2048 + k*16 + (v%8)*2
 #pragma unroll
@@ -571,7 +621,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 make_uint4(pack_bf16(s[8 * g + 0], s[8 * g + 1]), pack_bf16(s[8 * g + 2], s[8 * g + 3]),
                            pack_bf16(s[8 * g + 4], s[8 * g + 5]), pack_bf16(s[8 * g + 6], s[8 * g + 7]));
     };
-    write_state_operand();
+    if (epi) write_state_operand();
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
@@ -588,7 +638,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t id = idesc_bf16(128, Vt, false, true);
     const uint32_t idmn = idesc_bf16(128, Vt, true, true);
 
-    float GC_n = NC > 0 ? G[cbase * kC + kC - 1] : 0.f, Gr_n = NC > 0 ? G[cbase * kC + r] : 0.f;
+    float GC_n = (NC > 0 && epi) ? G[cbase * kC + kC - 1] : 0.f;
+    float Gr_n = (NC > 0 && epi) ? G[cbase * kC + r] : 0.f;
     float gr_prev = 0.f;
 
     // Output of chunk cc (threads on lanes 64-127): O = gamma Y + Mqk U.
@@ -596,11 +647,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         okk = mbar_wait(barO, cc & 1, err, 64) && okk;
         __syncwarp();
         fence_after_sync();
-        if (issuer && okk && cc + 2 < NC) issue_loads(cc + 2);
-        __syncwarp();
         float y[HV], ov[HV];
         if constexpr (HV == 8) {
-            uint32_t a[8], b2[8];
             // two 8-column halves through the x16 loader would over-read; use the
             // x16 load on a 16-column window and keep our half
             uint32_t wa[16], wb[16];
@@ -610,13 +658,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tmem_wait_ld(wb);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                a[j] = half ? wa[8 + j] : wa[j];
-                b2[j] = half ? wb[8 + j] : wb[j];
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                y[j] = __uint_as_float(a[j]);
-                ov[j] = __uint_as_float(b2[j]);
+                y[j] = __uint_as_float(half ? wa[8 + j] : wa[j]);
+                ov[j] = __uint_as_float(half ? wb[8 + j] : wb[j]);
             }
         } else {
             tmem_cols2<HV>(tXY0 + (uint32_t)((cc & 1) * Vt) + lanebase + cb, tO + lanebase + cb, y, ov);
@@ -634,144 +677,195 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     bool ok = true;
     int c = 0;
+    int xy_last = -1, o_last = -1;  // last chunk whose [X;Y] / output MMAs were committed (MMA issuer)
+    if (mma_warp) {
 #pragma unroll 1
-    for (; c < NC; ++c) {
-        const int stg = c & 1;
-        unsigned char* st = sm + stg * P::STAGE;
-        const int64_t chunk = cbase + c;
-        if (issuer) {
-            if (wr_states) {  // chunk-start state -> saved boundary states, by TMA
-                tma_store_3d(&tm_st, sm + P::S_OP, 0, (int)(chunk * kD), v0 / 8);
-                bulk_commit();
-            }
-            const bool okt = mbar_wait(&tbar[stg], (c >> 1) & 1, err, 8);
-            if (okt) {
-                // [X; Y] = [W; Q] S0^T in one M=128 MMA chain
-                const uint64_t dWQ = sdesc(smem_u32(st + P::OFF_WQ), 16, 1024, SW_128B);
+        for (; c < NC; ++c) {
+            const int stg = c % NS;
+            unsigned char* st = sm + stg * P::STAGE;
+            if (mma_issuer) {
+                ok = mbar_wait(&tbar[stg], (c / NS) & 1, err, 8) && ok;
+                if (ok) {
+                    // [X; Y] = [W; Q] S0^T in one M=128 MMA chain
+                    const uint64_t dWQ = sdesc(smem_u32(st + P::OFF_WQ), 16, 1024, SW_128B);
 #pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2)
-                    mma_bf16_ss(tXY0 + (uint32_t)(stg * Vt), desc_add(dWQ, (s2 >> 2) * 16384 + (s2 & 3) * 32),
-                                desc_add(dS, s2 * 256), id, s2 > 0);
-                mma_commit(barXY);
+                    for (int s2 = 0; s2 < 8; ++s2)
+                        mma_bf16_ss(tXY0 + (uint32_t)((c & 1) * Vt),
+                                    desc_add(dWQ, (s2 >> 2) * 16384 + (s2 & 3) * 32), desc_add(dS, s2 * 256), id,
+                                    s2 > 0);
+                    mma_commit(barXY);
+                    xy_last = c;
+                }
             }
-        }
-        const float GC = GC_n;
-        const float gC = expf(GC);
-        const float Gr = Gr_n;
-        const float gr = expf(Gr), er = expf(GC - Gr);
-        if (c + 1 < NC) {
-            GC_n = G[(chunk + 1) * kC + kC - 1];
-            Gr_n = G[(chunk + 1) * kC + r];
-        }
-        if (!urow && c > 0) output_epilogue(c - 1, ok);  // overlaps this chunk's first MMAs
-        gr_prev = gr;
-        if (urow) {
-            ok = mbar_wait(&tbar[stg], (c >> 1) & 1, err, 8) && ok;  // Ut slice is read below
-            ok = mbar_wait(barXY, c & 1, err, 16) && ok;
             __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 1: U and Uh written, X / Y read
+            if (!ok) break;
             fence_after_sync();
-            // U = Ut - X, Uh = e_r U  (row r, columns cb .. cb+HV)
-            float xg[HV];
-            if constexpr (HV == 8) {
-                uint32_t w16[16];
-                tmem_ld16(tXY0 + (uint32_t)(stg * Vt) + lanebase, w16);
-                tmem_wait_ld(w16);
+            if (mma_issuer) {
+                const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 8192, 1024, SW_128B);
+                // rows 0-63 of this A are the K_1 block (unused rows), rows 64-127 are Mqk
+                const uint64_t dM = sdesc(smem_u32(st + P::OFF_K + 8192), 16, 1024, SW_128B);
+                // S1^T update first (critical), then the output term
 #pragma unroll
-                for (int j = 0; j < 8; ++j) xg[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
-            } else {
-                tmem_cols<HV>(tXY0 + (uint32_t)(stg * Vt) + lanebase + cb, xg);
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_bf16_ss(tS, desc_add(dK, s2 * 2048), desc_add(dUh, s2 * 256), idmn, s2 > 0);
+                mma_commit(barS);
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_bf16_ss(tO, desc_add(dM, s2 * 32), desc_add(dU, s2 * 256), id, s2 > 0);
+                mma_commit(barO);
+                o_last = c;
             }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 2: the state operand S1^T written
+            if (!ok) break;
+            fence_after_sync();
+        }
+    } else if (tma_warp) {
+#pragma unroll 1
+        for (; c < NC; ++c) {
+            if (tma_issuer) {
+                if (wr_states) {  // chunk-start state -> saved boundary states
+                    tma_store_3d(&tm_st, sm + P::S_OP, 0, (int)((cbase + c) * kD), v0 / 8);
+                    bulk_commit();
+                }
+                // chunk c + NS - 1 into the stage chunk c - 1 used, once its last
+                // MMAs (the output term) have read it
+                if (ok && issued < NC) {
+                    if (c > 0) ok = mbar_wait(barO, (c - 1) & 1, err, 64) && ok;
+                    if (ok) issue_loads(issued++);
+                }
+                bulk_wait_read0();  // the states store has read S0^T (rewritten after barrier 1)
+            }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 1
+            if (!ok) break;
+            fence_after_sync();
+            if (tma_issuer) {
+                if (c > 0 && wr_o) {  // output tile of the previous chunk
+                    tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + c - 1) * kC, v0 / 8, h, b);
+                    bulk_commit();
+                }
+                bulk_wait_read0();  // the output store has read the O tile (rewritten next chunk)
+            }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 2
+            if (!ok) break;
+            fence_after_sync();
+        }
+    } else {
+#pragma unroll 1
+        for (; c < NC; ++c) {
+            const int stg = c % NS;
+            unsigned char* st = sm + stg * P::STAGE;
+            const int64_t chunk = cbase + c;
+            const float GC = GC_n;
+            const float gC = expf(GC);
+            const float Gr = Gr_n;
+            const float gr = expf(Gr), er = expf(GC - Gr);
+            if (c + 1 < NC) {
+                GC_n = G[(chunk + 1) * kC + kC - 1];
+                Gr_n = G[(chunk + 1) * kC + r];
+            }
+            if (!urow && c > 0) output_epilogue(c - 1, ok);  // overlaps this chunk's first MMAs
+            gr_prev = gr;
+            if (urow) {
+                ok = mbar_wait(&tbar[stg], (c / NS) & 1, err, 8) && ok;  // Ut slice is read below
+                ok = mbar_wait(barXY, c & 1, err, 16) && ok;
+                __syncwarp();
+                fence_after_sync();
+                // U = Ut - X, Uh = e_r U  (row r, columns cb .. cb+HV)
+                float xg[HV];
+                if constexpr (HV == 8) {
+                    uint32_t w16[16];
+                    tmem_ld16(tXY0 + (uint32_t)((c & 1) * Vt) + lanebase, w16);
+                    tmem_wait_ld(w16);
 #pragma unroll
-            for (int g = 0; g < HV / 8; ++g) {
-                const int gg = cb / 8 + g;
-                const uint4 uq = *(const uint4*)(st + P::OFF_UT + gg * 1024 + r * 16);
-                const uint32_t uw4[4] = {uq.x, uq.y, uq.z, uq.w};
-                float u[8], uh[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {  // ut_w = 1 gives exactly Ut - X
-                    u[2 * e] = fmaf(ut_w, bf_lo(uw4[e]), -xg[8 * g + 2 * e]);
-                    u[2 * e + 1] = fmaf(ut_w, bf_hi(uw4[e]), -xg[8 * g + 2 * e + 1]);
+                    for (int j = 0; j < 8; ++j) xg[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
+                } else {
+                    tmem_cols<HV>(tXY0 + (uint32_t)((c & 1) * Vt) + lanebase + cb, xg);
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) uh[j] = er * u[j];
-                // MN-major, no swizzle: element (v, r) at (v/8)*1024 + r*16 + (v%8)*2
-                *(uint4*)(sm + P::U_OP + gg * 1024 + r * 16) =
-                    make_uint4(pack_bf16(u[0], u[1]), pack_bf16(u[2], u[3]), pack_bf16(u[4], u[5]), pack_bf16(u[6], u[7]));
-                *(uint4*)(sm + P::UH_OP + gg * 1024 + r * 16) =
-                    make_uint4(pack_bf16(uh[0], uh[1]), pack_bf16(uh[2], uh[3]), pack_bf16(uh[4], uh[5]), pack_bf16(uh[6], uh[7]));
+                for (int g = 0; g < HV / 8; ++g) {
+                    const int gg = cb / 8 + g;
+                    const uint4 uq = *(const uint4*)(st + P::OFF_UT + gg * 1024 + r * 16);
+                    const uint32_t uw4[4] = {uq.x, uq.y, uq.z, uq.w};
+                    float u[8], uh[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {  // ut_w = 1 gives exactly Ut - X
+                        u[2 * e] = fmaf(ut_w, bf_lo(uw4[e]), -xg[8 * g + 2 * e]);
+                        u[2 * e + 1] = fmaf(ut_w, bf_hi(uw4[e]), -xg[8 * g + 2 * e + 1]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) uh[j] = er * u[j];
+                    // MN-major, no swizzle: element (v, r) at (v/8)*1024 + r*16 + (v%8)*2
+                    *(uint4*)(sm + P::U_OP + gg * 1024 + r * 16) = make_uint4(
+                        pack_bf16(u[0], u[1]), pack_bf16(u[2], u[3]), pack_bf16(u[4], u[5]), pack_bf16(u[6], u[7]));
+                    *(uint4*)(sm + P::UH_OP + gg * 1024 + r * 16) =
+                        make_uint4(pack_bf16(uh[0], uh[1]), pack_bf16(uh[2], uh[3]), pack_bf16(uh[4], uh[5]),
+                                   pack_bf16(uh[6], uh[7]));
+                }
             }
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        if (issuer) bulk_wait_read0();  // the states store no longer reads S0^T
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        fence_after_sync();
-        if (issuer) {
-            if (c > 0 && wr_o) {  // output tile of the previous chunk
-                tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + c - 1) * kC, v0 / 8, h, b);
-                bulk_commit();
+            fence_proxy_async();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 1
+            if (!ok) break;
+            fence_after_sync();
+            ok = mbar_wait(barS, c & 1, err, 32) && ok;
+            __syncwarp();
+            fence_after_sync();
+            // S1^T = gamma_C S0^T + K^T Uh
+            {
+                float sv[HV];
+                if constexpr (HV == 8) {
+                    uint32_t w16[16];
+                    tmem_ld16(tS + lanebase, w16);
+                    tmem_wait_ld(w16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sv[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
+                } else {
+                    tmem_cols<HV>(tS + lanebase + cb, sv);
+                }
+#pragma unroll
+                for (int j = 0; j < HV; ++j) s[j] = gC * s[j] + sv[j];
             }
-            const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 8192, 1024, SW_128B);
-            // rows 0-63 of this A are the K_1 block (unused rows), rows 64-127 are Mqk
-            const uint64_t dM = sdesc(smem_u32(st + P::OFF_K + 8192), 16, 1024, SW_128B);
-            // S1^T update first (critical), then the output term
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2)
-                mma_bf16_ss(tS, desc_add(dK, s2 * 2048), desc_add(dUh, s2 * 256), idmn, s2 > 0);
-            mma_commit(barS);
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2)
-                mma_bf16_ss(tO, desc_add(dM, s2 * 32), desc_add(dU, s2 * 256), id, s2 > 0);
-            mma_commit(barO);
+            write_state_operand();
+            fence_proxy_async();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 2
+            if (!ok) break;
+            fence_after_sync();
         }
-        ok = mbar_wait(barS, c & 1, err, 32) && ok;
-        __syncwarp();
-        fence_after_sync();
-        // S1^T = gamma_C S0^T + K^T Uh
-        {
-            float sv[HV];
-            if constexpr (HV == 8) {
-                uint32_t w16[16];
-                tmem_ld16(tS + lanebase, w16);
-                tmem_wait_ld(w16);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) sv[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
-            } else {
-                tmem_cols<HV>(tS + lanebase + cb, sv);
-            }
-#pragma unroll
-            for (int j = 0; j < HV; ++j) s[j] = gC * s[j] + sv[j];
-        }
-        write_state_operand();
-        fence_proxy_async();
-        fence_before_sync();
-        if (issuer) bulk_wait_read0();  // the output store no longer reads the O tile
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        fence_after_sync();
     }
+    // `ok` is the value of the last block-wide vote here, the same in every thread
     if (ok && NC > 0) {
-        if (!urow) output_epilogue(NC - 1, ok);
+        if (epi && !urow) output_epilogue(NC - 1, ok);
         fence_proxy_async();
         fence_before_sync();
         ok = __syncthreads_and(ok);
-        if (issuer && ok && wr_o) {
+        if (tma_issuer && ok && wr_o) {
             tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + NC - 1) * kC, v0 / 8, h, b);
             bulk_commit();
         }
     }
-    if (ok && s_out) {
+    if (ok && s_out && epi) {
 #pragma unroll
-        for (int j = 0; j < HV; ++j) s_out[(sidx * d.V + v0 + cb + j) * kD + k] = s[j];
+        for (int j = 0; j < HV; ++j)
+            if ((kD % Vt == 0) || v0 + cb + j < kD) s_out[(sidx * d.V + v0 + cb + j) * kD + k] = s[j];
     }
-    if (issuer) {
-        if (!ok) {
-            // drain what may still be in flight (bounded) before leaving
-            for (int cc = c; cc < NC && cc < c + 2; ++cc) mbar_wait(&tbar[cc & 1], (cc >> 1) & 1, nullptr, 0);
-            mbar_wait(barO, (c > 0 ? c - 1 : 0) & 1, nullptr, 0);
-        }
+    if (tma_issuer) {
+        // on an error, the loads still in flight (bounded waits) before leaving
+        if (!ok)
+            for (int cc = c; cc < issued; ++cc) mbar_wait(&tbar[cc % NS], (cc / NS) & 1, nullptr, 0);
         bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
+    }
+    if (mma_issuer && !ok) {  // the MMAs still in flight, before the TMEM is freed
+        if (xy_last >= 0) mbar_wait(barXY, xy_last & 1, nullptr, 0);
+        if (o_last >= 0) mbar_wait(barO, o_last & 1, nullptr, 0);
     }
     __syncwarp();
     fence_before_sync();
@@ -800,9 +894,9 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     if (e != cudaSuccess) return e;
     const int mode = sq ? sq->mode : 0;
     const int nseq = sq ? sq->nseq : d.B;
-    dim3 grid(kD / Vt, d.H, mode == 1 ? 2 * nseq : nseq);
+    dim3 grid((kD + Vt - 1) / Vt, d.H, mode == 1 ? 2 * nseq : nseq);
     const bool tr_only = mode == 2;
-    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, (o != nullptr && !tr_only),
+    kern<<<grid, 320, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, (o != nullptr && !tr_only),
                                      (states != nullptr && !tr_only), sq ? sq->chunk_off : nullptr, nseq, mode,
                                      sq ? sq->trans : nullptr, tb.err);
     return cudaGetLastError();
@@ -814,10 +908,11 @@ bool tc_fwd_supported(const Dims& d, InType ty) {
     return ty == InType::BF16 && d.K == kD && d.V == kD && d.C == kC;
 }
 
+// The narrowest V-slice whose CTAs (one per slice and stream) fit one wave.
 int tc_scan_vt(int64_t streams) {
     const int64_t sms = sm_count();
-    for (int vt : {16, 32, 64})
-        if (streams * (kD / vt) <= sms) return vt;
+    for (int vt : {16, 32, 48, 64})
+        if (streams * ((kD + vt - 1) / vt) <= sms) return vt;
     return 64;
 }
 
@@ -843,6 +938,7 @@ cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, cons
     switch (tc_scan_vt(streams)) {
         case 16: return launch_scan_vt<16>(d, q, k, tb, s0, o, sT, states, st, sq);
         case 32: return launch_scan_vt<32>(d, q, k, tb, s0, o, sT, states, st, sq);
+        case 48: return launch_scan_vt<48>(d, q, k, tb, s0, o, sT, states, st, sq);
         default: return launch_scan_vt<64>(d, q, k, tb, s0, o, sT, states, st, sq);
     }
 }

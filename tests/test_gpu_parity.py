@@ -209,6 +209,17 @@ def test_slow_decay_long_range(oracle_mod, dtype, K, V, C):
     compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), dtype)
 
 
+@pytest.mark.parametrize("B,H", [(7, 6), (5, 9)])
+def test_tc_scan_48_column_slices(oracle_mod, B, H):
+    """39 to 50 streams run the scans in 48-column V-slices (three per stream,
+    the third reaching past V = 128 into zero columns): forward and backward
+    against the oracle on every stream, slow decay so the states carry."""
+    w = custom(B=B, T=200, H=H, K=128, V=128, chunk=64, dtype="bf16", seed=650 + B * H, init_std=0.3,
+               dfinal_std=0.05, alpha_lo=0.97)
+    inp = make_inputs(w)
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16")
+
+
 def test_tc_error_flag_stays_clear():
     """The tensor-core kernels' bounded waits never give up in a normal run: the
     error word at the start of the caller's workspace stays 0."""
