@@ -145,6 +145,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Waits until every committed bulk store but the most recent group has finished
+// reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Waits until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

@@ -164,22 +164,26 @@ __device__ __forceinline__ float warp_colsum16(float (&v)[16]) {
 // ============================================================ reverse scan
 template <int Vt>
 struct BScan {
+    // TMA stages: three (more lead) where they fit, up to 48-column slices
+    static constexpr int NS = Vt <= 48 ? 3 : 2;
     // stage: Mqk 8K | K_0 | K_1 | Q_0 | Q_1 | W_0 | W_1 (8K each) | dO slice [Vt/8][64][8]
     static constexpr int OFF_M = 0, OFF_K = 8192, OFF_Q = 24576, OFF_W = 40960, OFF_DO = 57344;
-    static constexpr int STAGE = 57344 + kC * Vt * 2;
-    static constexpr int DS_OP = 2 * STAGE;            // dS1^T [Vt/8][128 k][8], MN-major, no swizzle
+    static constexpr int STAGE = 57344 + kC * Vt * 2;   // a multiple of 1024 (swizzled operands)
+    static constexpr int DS_OP = NS * STAGE;            // dS1^T [Vt/8][128 k][8], MN-major, no swizzle
     static constexpr int GDO_OP = DS_OP + kD * Vt * 2;  // gamma dO, two buffers [Vt/8][64][8]
-    static constexpr int DU_OP = GDO_OP + 2 * kC * Vt * 2;
-    static constexpr int BAR = DU_OP + kC * Vt * 2;
+    static constexpr int DU_OP = GDO_OP + 2 * kC * Vt * 2;  // dU of iteration it in buffer it & 1
+    static constexpr int BAR = DU_OP + 2 * kC * Vt * 2;  // tma[NS], bar1, bar2, then the TMEM slot at +48
     static constexpr size_t SMEM = BAR + 64 + 1024;
     static constexpr uint32_t TMEM_COLS = (3 * Vt <= 64) ? 64 : (3 * Vt <= 128 ? 128 : 256);
 };
 
-// 256 threads; warps w and w+4 split the columns of TMEM lanes 32*(w%4) ...
-// Lanes 0-63: rows of dU (critical); lanes 64-127 prepare the next chunk's
-// gamma dO operand; all lanes update dS^T (rows k).
+// 320 threads: warps 0-7 run the epilogues, warp 8 issues the MMAs and warp 9 the
+// TMA copies (lane 0 of each).  Warps w and w+4 (w < 4) split the columns of TMEM
+// lanes 32*w ..  Lanes 0-63: rows of dU (critical); lanes 64-127 prepare the next
+// chunk's gamma dO operand; all lanes update dS^T (rows k).  The three roles run
+// separate loops with the same two block-wide barriers per chunk.
 template <int Vt>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(320, 1)
 scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dU,
@@ -187,18 +191,20 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             float* ds0, const int* __restrict__ chunk_off, int* err) {
     using P = BScan<Vt>;
     constexpr int HV = Vt / 2;
+    constexpr int NS = P::NS;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     uint64_t* tbar = (uint64_t*)(sm + P::BAR);
-    uint64_t* bar1 = tbar + 2;
-    uint64_t* bar2 = tbar + 3;
-    uint32_t* tslot = (uint32_t*)(sm + P::BAR + 32);
+    uint64_t* bar1 = tbar + NS;
+    uint64_t* bar2 = tbar + NS + 1;
+    uint32_t* tslot = (uint32_t*)(sm + P::BAR + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int sub = warp & 3, half = warp >> 2;
+    const bool mma_warp = warp == 8, tma_warp = warp == 9, epi = warp < 8;
+    const bool mma_issuer = tid == 256, tma_issuer = tid == 288;
+    const int sub = warp & 3, half = (warp >> 2) & 1;
     const int lanerow = 32 * sub + lane;
     const int cb = half * HV;
-    const bool issuer = tid == 96;
     const bool urow = sub < 2;
     const int r = urow ? lanerow : lanerow - 64;
     const int v0 = blockIdx.x * Vt, h = blockIdx.y;
@@ -215,10 +221,12 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     const int64_t cbase = ((int64_t)b * d.H + h) * d.NC + c0;  // global index of chunk c = 0
 
+    // Iteration it (chunk NC-1-it) into stage it % NS (the n-th use of a stage
+    // completes phase n & 1).
     auto issue_loads = [&](int it) {
         const int c = NC - 1 - it;
-        unsigned char* st = sm + (it & 1) * P::STAGE;
-        uint64_t* bar = &tbar[it & 1];
+        unsigned char* st = sm + (it % NS) * P::STAGE;
+        uint64_t* bar = &tbar[it % NS];
         const int row = (int)((cbase + c) * kC);
         const int t0 = (c0 + c) * kC;
         mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
@@ -231,11 +239,11 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tma_load_5d(st + P::OFF_DO, &tm_do, bar, 0, t0, v0 / 8, h, b);
     };
 
-    if (issuer) {
-        for (int i = 0; i < 4; ++i) mbar_init(&tbar[i], 1);
+    int issued = 0;  // iterations whose loads were issued (TMA issuer)
+    if (tma_issuer) {
+        for (int i = 0; i < NS + 2; ++i) mbar_init(&tbar[i], 1);
         fence_mbar_init();
-        if (NC > 0) issue_loads(0);
-        if (NC > 1) issue_loads(1);
+        for (; issued < NS && issued < NC; ++issued) issue_loads(issued);
     }
     if (warp == 0) {
         tmem_alloc(tslot, P::TMEM_COLS);
@@ -246,23 +254,23 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
     for (int j = 0; j < HV; ++j) {
         const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
-        ds[j] = (dsT && ((kD % Vt == 0) || v < kD)) ? dsT[(sidx * d.V + v) * kD + k] : 0.f;
+        ds[j] = (epi && dsT && ((kD % Vt == 0) || v < kD)) ? dsT[(sidx * d.V + v) * kD + k] : 0.f;
     }
     auto write_ds_operand = [&]() {
 #pragma unroll
         for (int g = 0; g < HV / 8; ++g)
             *(uint4*)(sm + P::DS_OP + (cb / 8 + g) * 2048 + k * 16) = pack8(&ds[8 * g]);
     };
-    write_ds_operand();
+    if (epi) write_ds_operand();
     // G of a chunk is fetched one chunk ahead.
-    float GC_n = NC > 0 ? G[(cbase + NC - 1) * kC + kC - 1] : 0.f;
-    float Gr_n = NC > 0 ? G[(cbase + NC - 1) * kC + r] : 0.f;
-    // gamma dO operand (buffer it2 & 1) of the chunk held in stage it2 & 1; rows of
-    // lanes 64-127; uses gamma_r = exp(Gr_n) of that chunk.
+    float GC_n = (NC > 0 && epi) ? G[(cbase + NC - 1) * kC + kC - 1] : 0.f;
+    float Gr_n = (NC > 0 && epi) ? G[(cbase + NC - 1) * kC + r] : 0.f;
+    // gamma dO operand (buffer it2 & 1) of iteration it2's chunk, from its stage;
+    // rows of lanes 64-127; uses gamma_r = exp(Gr_n) of that chunk.
     auto write_gdo_operand = [&](int it2, bool& okk) {
-        okk = mbar_wait(&tbar[it2 & 1], (it2 >> 1) & 1, err, 8) && okk;
+        okk = mbar_wait(&tbar[it2 % NS], (it2 / NS) & 1, err, 8) && okk;
         const float gr = expf(Gr_n);
-        const unsigned char* dsrc = sm + (it2 & 1) * P::STAGE + P::OFF_DO;
+        const unsigned char* dsrc = sm + (it2 % NS) * P::STAGE + P::OFF_DO;
         unsigned char* ddst = sm + P::GDO_OP + (it2 & 1) * (kC * Vt * 2);
 #pragma unroll
         for (int g = 0; g < HV / 8; ++g) {
@@ -279,7 +287,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     };
     bool ok = true;
-    if (!urow && NC > 0) write_gdo_operand(0, ok);
+    if (epi && !urow && NC > 0) write_gdo_operand(0, ok);
     fence_proxy_async();
     fence_before_sync();
     ok = __syncthreads_and(ok);
@@ -288,131 +296,179 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t tA = tmem, tB = tmem + Vt, tCc = tmem + 2 * Vt;
     const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
     const uint64_t dDS = sdesc(smem_u32(sm + P::DS_OP), 128, 2048, SW_NONE);
-    const uint64_t dDU = sdesc(smem_u32(sm + P::DU_OP), 128, 1024, SW_NONE);
     const uint32_t idn = idesc_bf16(128, Vt, false, true);
     const uint32_t idm = idesc_bf16(128, Vt, true, true);
     const uint32_t idneg = idesc_bf16(128, Vt, true, true, true);  // -W^T dU
 
     int it = 0;
+    int b1_last = -1, b2_last = -1;  // last iterations committed to bar1 / bar2 (MMA issuer)
+    if (mma_warp) {
 #pragma unroll 1
-    for (; ok && it < NC; ++it) {
-        const int c = NC - 1 - it;
-        const int stg = it & 1;
-        unsigned char* st = sm + stg * P::STAGE;
-        const int64_t chunk = cbase + c;
-        const float GC = GC_n;
-        const float gC = expf(GC);
-        const float er = expf(GC - Gr_n);
-        if (issuer) {
-            // the gradient of this chunk's end state, for the chunk-local gradients
-            tma_store_3d(&tm_dS1, sm + P::DS_OP, 0, (int)(chunk * kD), v0 / 8);
-            bulk_commit();
-            const bool okt = mbar_wait(&tbar[stg], (it >> 1) & 1, err, 8);
-            if (okt) {
-                // rows 64-127 of the first two A operands are neighbouring tiles (unused)
-                const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 16, 1024, SW_128B);
-                const uint64_t dM = sdesc(smem_u32(st + P::OFF_M), 8192, 1024, SW_128B);
-                const uint64_t dQ = sdesc(smem_u32(st + P::OFF_Q), 8192, 1024, SW_128B);
-                const uint64_t dDO = sdesc(smem_u32(st + P::OFF_DO), 128, 1024, SW_NONE);
-                const uint64_t dG = sdesc(smem_u32(sm + P::GDO_OP + stg * (kC * Vt * 2)), 128, 1024, SW_NONE);
+        for (; ok && it < NC; ++it) {
+            const int stg = it % NS;
+            unsigned char* st = sm + stg * P::STAGE;
+            if (mma_issuer) {
+                ok = mbar_wait(&tbar[stg], (it / NS) & 1, err, 8) && ok;
+                if (ok) {
+                    // rows 64-127 of the first two A operands are neighbouring tiles (unused)
+                    const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 16, 1024, SW_128B);
+                    const uint64_t dM = sdesc(smem_u32(st + P::OFF_M), 8192, 1024, SW_128B);
+                    const uint64_t dQ = sdesc(smem_u32(st + P::OFF_Q), 8192, 1024, SW_128B);
+                    const uint64_t dDO = sdesc(smem_u32(st + P::OFF_DO), 128, 1024, SW_NONE);
+                    const uint64_t dG =
+                        sdesc(smem_u32(sm + P::GDO_OP + (it & 1) * (kC * Vt * 2)), 128, 1024, SW_NONE);
 #pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2)
-                    mma_bf16_ss(tB, desc_add(dK, (s2 >> 2) * 8192 + (s2 & 3) * 32), desc_add(dDS, s2 * 256), idn,
-                                s2 > 0);
+                    for (int s2 = 0; s2 < 8; ++s2)
+                        mma_bf16_ss(tB, desc_add(dK, (s2 >> 2) * 8192 + (s2 & 3) * 32), desc_add(dDS, s2 * 256),
+                                    idn, s2 > 0);
 #pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2)
-                    mma_bf16_ss(tA, desc_add(dM, s2 * 2048), desc_add(dDO, s2 * 256), idm, s2 > 0);
-                mma_commit(bar1);
+                    for (int s2 = 0; s2 < 4; ++s2)
+                        mma_bf16_ss(tA, desc_add(dM, s2 * 2048), desc_add(dDO, s2 * 256), idm, s2 > 0);
+                    mma_commit(bar1);
+                    b1_last = it;
 #pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2)
-                    mma_bf16_ss(tCc, desc_add(dQ, s2 * 2048), desc_add(dG, s2 * 256), idm, s2 > 0);
+                    for (int s2 = 0; s2 < 4; ++s2)
+                        mma_bf16_ss(tCc, desc_add(dQ, s2 * 2048), desc_add(dG, s2 * 256), idm, s2 > 0);
+                }
             }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 1: dU and the next gamma dO written
+            if (!ok) break;
+            fence_after_sync();
+            if (mma_issuer) {
+                const uint64_t dW = sdesc(smem_u32(st + P::OFF_W), 8192, 1024, SW_128B);
+                const uint64_t dDU = sdesc(smem_u32(sm + P::DU_OP + (it & 1) * (kC * Vt * 2)), 128, 1024, SW_NONE);
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_bf16_ss(tCc, desc_add(dW, s2 * 2048), desc_add(dDU, s2 * 256), idneg, 1u);
+                mma_commit(bar2);
+                b2_last = it;
+            }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 2: dS^T written
+            if (!ok) break;
+            fence_after_sync();
         }
-        if (c > 0) {
-            GC_n = G[(chunk - 1) * kC + kC - 1];
-            Gr_n = G[(chunk - 1) * kC + r];
+    } else if (tma_warp) {
+#pragma unroll 1
+        for (; ok && it < NC; ++it) {
+            const int64_t chunk = cbase + (NC - 1 - it);
+            if (tma_issuer) {
+                // the gradient of this chunk's end state, for the chunk-local gradients
+                tma_store_3d(&tm_dS1, sm + P::DS_OP, 0, (int)(chunk * kD), v0 / 8);
+                bulk_commit();
+                bulk_wait_read0();  // it has read dS1^T (rewritten after barrier 1)
+            }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 1
+            if (!ok) break;
+            fence_after_sync();
+            if (tma_issuer) {
+                tma_store_3d(&tm_dU, sm + P::DU_OP + (it & 1) * (kC * Vt * 2), 0, (int)(chunk * kC), v0 / 8);
+                bulk_commit();
+                // iteration it + NS into this iteration's stage once its MMAs are done
+                if (ok && issued < NC) {
+                    ok = mbar_wait(bar2, it & 1, err, 32) && ok;
+                    if (ok) issue_loads(issued++);
+                }
+                bulk_wait_read1();  // the dU store of the previous iteration has read its buffer
+            }
+            __syncwarp();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 2
+            if (!ok) break;
+            fence_after_sync();
         }
-        if (urow) {
-            ok = mbar_wait(bar1, it & 1, err, 16) && ok;
+    } else {
+#pragma unroll 1
+        for (; ok && it < NC; ++it) {
+            const int c = NC - 1 - it;
+            const int64_t chunk = cbase + c;
+            const float GC = GC_n;
+            const float gC = expf(GC);
+            const float er = expf(GC - Gr_n);
+            if (c > 0) {
+                GC_n = G[(chunk - 1) * kC + kC - 1];
+                Gr_n = G[(chunk - 1) * kC + r];
+            }
+            if (urow) {
+                ok = mbar_wait(bar1, it & 1, err, 16) && ok;
+                __syncwarp();
+                fence_after_sync();
+                // dU = Mqk^T dO + e_r (K dS1^T)  (row r, columns cb .. cb+HV)
+                float a[HV], bb[HV];
+                if constexpr (HV == 8) {
+                    uint32_t wa[16], wb[16];
+                    tmem_ld16(tA + lanebase, wa);
+                    tmem_ld16(tB + lanebase, wb);
+                    tmem_wait_ld(wa);
+                    tmem_wait_ld(wb);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        a[j] = __uint_as_float(half ? wa[8 + j] : wa[j]);
+                        bb[j] = __uint_as_float(half ? wb[8 + j] : wb[j]);
+                    }
+                } else {
+                    tmem_cols2<HV>(tA + lanebase + cb, tB + lanebase + cb, a, bb);
+                }
+                unsigned char* du = sm + P::DU_OP + (it & 1) * (kC * Vt * 2);
+#pragma unroll
+                for (int g = 0; g < HV / 8; ++g) {
+                    float u[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) u[j] = a[8 * g + j] + er * bb[8 * g + j];
+                    *(uint4*)(du + (cb / 8 + g) * 1024 + r * 16) = pack8(u);
+                }
+            } else if (c > 0) {
+                write_gdo_operand(it + 1, ok);  // operand of the next chunk (c - 1)
+            }
+            fence_proxy_async();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 1
+            if (!ok) break;
+            fence_after_sync();
+            ok = mbar_wait(bar2, it & 1, err, 32) && ok;
             __syncwarp();
             fence_after_sync();
-            // dU = Mqk^T dO + e_r (K dS1^T)  (row r, columns cb .. cb+HV)
-            float a[HV], bb[HV];
-            if constexpr (HV == 8) {
-                uint32_t wa[16], wb[16];
-                tmem_ld16(tA + lanebase, wa);
-                tmem_ld16(tB + lanebase, wb);
-                tmem_wait_ld(wa);
-                tmem_wait_ld(wb);
+            {
+                float x[HV];
+                if constexpr (HV == 8) {
+                    uint32_t w16[16];
+                    tmem_ld16(tCc + lanebase, w16);
+                    tmem_wait_ld(w16);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    a[j] = __uint_as_float(half ? wa[8 + j] : wa[j]);
-                    bb[j] = __uint_as_float(half ? wb[8 + j] : wb[j]);
+                    for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
+                } else {
+                    tmem_cols<HV>(tCc + lanebase + cb, x);
                 }
-            } else {
-                tmem_cols2<HV>(tA + lanebase + cb, tB + lanebase + cb, a, bb);
+#pragma unroll
+                for (int j = 0; j < HV; ++j) ds[j] = gC * ds[j] + x[j];
             }
-#pragma unroll
-            for (int g = 0; g < HV / 8; ++g) {
-                float u[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) u[j] = a[8 * g + j] + er * bb[8 * g + j];
-                *(uint4*)(sm + P::DU_OP + (cb / 8 + g) * 1024 + r * 16) = pack8(u);
-            }
-        } else if (c > 0) {
-            write_gdo_operand(it + 1, ok);  // operand of the next chunk (c - 1)
+            write_ds_operand();
+            fence_proxy_async();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);  // 2
+            if (!ok) break;
+            fence_after_sync();
         }
-        fence_proxy_async();
-        fence_before_sync();
-        if (issuer) bulk_wait_read0();  // the dS1 store no longer reads dS1^T
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        fence_after_sync();
-        if (issuer) {
-            tma_store_3d(&tm_dU, sm + P::DU_OP, 0, (int)(chunk * kC), v0 / 8);
-            bulk_commit();
-            const uint64_t dW = sdesc(smem_u32(st + P::OFF_W), 8192, 1024, SW_128B);
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2)
-                mma_bf16_ss(tCc, desc_add(dW, s2 * 2048), desc_add(dDU, s2 * 256), idneg, 1u);
-            mma_commit(bar2);
-        }
-        ok = mbar_wait(bar2, it & 1, err, 32) && ok;
-        __syncwarp();
-        fence_after_sync();
-        if (issuer && ok && it + 2 < NC) issue_loads(it + 2);
-        __syncwarp();
-        {
-            float x[HV];
-            if constexpr (HV == 8) {
-                uint32_t w16[16];
-                tmem_ld16(tCc + lanebase, w16);
-                tmem_wait_ld(w16);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(half ? w16[8 + j] : w16[j]);
-            } else {
-                tmem_cols<HV>(tCc + lanebase + cb, x);
-            }
-#pragma unroll
-            for (int j = 0; j < HV; ++j) ds[j] = gC * ds[j] + x[j];
-        }
-        write_ds_operand();
-        fence_proxy_async();
-        fence_before_sync();
-        if (issuer) bulk_wait_read0();  // the dU store no longer reads the dU tile
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-        fence_after_sync();
     }
-    if (ok && ds0) {
+    if (ok && ds0 && epi) {
 #pragma unroll
         for (int j = 0; j < HV; ++j)
             if ((kD % Vt == 0) || v0 + cb + j < kD) ds0[(sidx * d.V + v0 + cb + j) * kD + k] = ds[j];
     }
-    if (issuer) {
+    if (tma_issuer) {
+        // on an error, the loads still in flight (bounded waits) before leaving
         if (!ok)
-            for (int i2 = it; i2 < NC && i2 < it + 2; ++i2) mbar_wait(&tbar[i2 & 1], (i2 >> 1) & 1, nullptr, 0);
+            for (int i2 = it; i2 < issued; ++i2) mbar_wait(&tbar[i2 % NS], (i2 / NS) & 1, nullptr, 0);
         bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
+    }
+    if (mma_issuer && !ok) {  // the MMAs still in flight, before the TMEM is freed
+        if (b1_last >= 0) mbar_wait(bar1, b1_last & 1, nullptr, 0);
+        if (b2_last >= 0) mbar_wait(bar2, b2_last & 1, nullptr, 0);
     }
     __syncwarp();
     fence_before_sync();
@@ -1165,7 +1221,7 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((kD + Vt - 1) / Vt, d.H, sq ? sq->nseq : d.B);
-    kern<<<grid, 256, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0,
+    kern<<<grid, 320, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0,
                                      sq ? sq->chunk_off : nullptr, tb.err);
     return cudaGetLastError();
 }

@@ -434,8 +434,8 @@ struct ScanPlan {
     static constexpr int S_OP = NS * STAGE;          // S0^T [Vt/8][128 k][8] (MN-major, no swizzle)
     static constexpr int U_OP = S_OP + kD * Vt * 2;  // U  [Vt/8][64 tok][8]
     static constexpr int UH_OP = U_OP + kC * Vt * 2; // Uh
-    static constexpr int O_OP = UH_OP + kC * Vt * 2; // output tile, same layout
-    static constexpr int BAR = O_OP + kC * Vt * 2;   // tma[NS], XY, S, O, then the TMEM slot at +48
+    static constexpr int O_OP = UH_OP + kC * Vt * 2; // output tiles of chunk c in buffer c & 1, same layout
+    static constexpr int BAR = O_OP + 2 * kC * Vt * 2;  // tma[NS], XY, S, O, then the TMEM slot at +48
     static constexpr int END = BAR + 64;
     static constexpr size_t SMEM = END + 1024;
     // TMEM: [X;Y] (two buffers), O2, DS, each Vt columns
@@ -669,7 +669,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             float f[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] = gr_prev * y[8 * g + j] + ov[8 * g + j];
-            *(uint4*)(sm + P::O_OP + (cb / 8 + g) * 1024 + r * 16) =
+            *(uint4*)(sm + P::O_OP + (cc & 1) * (kC * Vt * 2) + (cb / 8 + g) * 1024 + r * 16) =
                 make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                            pack_bf16(f[6], f[7]));
         }
@@ -746,10 +746,13 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             fence_after_sync();
             if (tma_issuer) {
                 if (c > 0 && wr_o) {  // output tile of the previous chunk
-                    tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + c - 1) * kC, v0 / 8, h, b);
+                    tma_store_5d(&tm_o, sm + P::O_OP + ((c - 1) & 1) * (kC * Vt * 2), 0, (c0 + c - 1) * kC,
+                                 v0 / 8, h, b);
                     bulk_commit();
                 }
-                bulk_wait_read0();  // the output store has read the O tile (rewritten next chunk)
+                // the store issued a chunk earlier has read its tile, which the
+                // next output epilogue rewrites
+                bulk_wait_read1();
             }
             __syncwarp();
             fence_before_sync();
@@ -848,7 +851,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_before_sync();
         ok = __syncthreads_and(ok);
         if (tma_issuer && ok && wr_o) {
-            tma_store_5d(&tm_o, sm + P::O_OP, 0, (c0 + NC - 1) * kC, v0 / 8, h, b);
+            tma_store_5d(&tm_o, sm + P::O_OP + ((NC - 1) & 1) * (kC * Vt * 2), 0, (c0 + NC - 1) * kC, v0 / 8, h,
+                         b);
             bulk_commit();
         }
     }
