@@ -523,6 +523,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const bool urow = sub < 2;
     const int r = urow ? lanerow : lanerow - 64;
     const int64_t nchunks = d.NS() * d.NC;
+    // the thread that issues the MMAs and the TMA stores: lane 0 of warp 2, whose
+    // lanes (TMEM rows 64-95) fetch no U~ / Mqk rows before phase 1
+    constexpr int kQkIssuer = 64;
 
     auto decode = [&](int64_t ch, int& b, int& h, int& c) {
         c = (int)(ch % d.NC);
@@ -560,7 +563,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // warp 3 keeps the next chunk's G (2 tokens per lane) in registers
     float2 gnext = make_float2(0.f, 0.f);
     if (warp == 3 && first < nchunks) gnext = *(const float2*)(G + first * kC + 2 * lane);
-    if (tid == 0) {
+    if (tid == kQkIssuer) {
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         if (first < nchunks) {
@@ -611,7 +614,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int q = 0; q < 4; ++q) mqv[q] = mp[q];
         }
         // ---- phase 1 (K over k): [X; Y] = [W; Q] S0^T, Z = [K; -] dS1^T  (M=128, N=128)
-        if (tid == 0) {
+        if (tid == kQkIssuer) {
             ok = mbar_wait(&bars[0], ph, err, 1) && ok;
             ok = mbar_wait(&bars[1], ph, err, 1) && ok;
             if (ok) {
@@ -630,7 +633,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // dO and S0 tiles are read by every thread
         ok = mbar_wait(&bars[2], ph, err, 2) && ok;
-        if (tid == 0) bulk_wait_read0();  // the previous chunk's stores from the U / EU tiles are done
+        if (tid == kQkIssuer) bulk_wait_read0();  // the previous chunk's stores from the U / EU tiles are done
         __syncthreads();  // Gs / gs
         fence_after_sync();
         const float GC = Gs[63], gC = gs[63];
@@ -676,7 +679,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_after_sync();
         // ---- phase 2 (K over v): dMqk = [dO; -] U^T (N=64), S0^T [dO; dU]^T (N=128),
         //      dK^T = dS1^T (eU)^T (N=64)   (M=128)
-        if (tid == 0 && ok) {
+        if (tid == kQkIssuer && ok) {
             const uint32_t id = idesc_bf16(128, 64, false, false);
             const uint32_t id128 = idesc_bf16(128, 128, false, false);
             const uint64_t ddo = sdesc(sDO, 16, 1024, SW_128B), du = sdesc(sU, 16, 1024, SW_128B);
@@ -709,7 +712,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_after_sync();
         // W, dU, dO, S0^T, dS1^T are free: request the next chunk's
         __syncthreads();  // every thread is past its reads of those tiles
-        if (tid == 0 && ok && ch + gridDim.x < nchunks) load_A(ch + gridDim.x);
+        // issued from warp 3 (output rows), which has the lighter epilogue in this phase
+        if (tid == 96 && ok && ch + gridDim.x < nchunks) load_A(ch + gridDim.x);
         {
             if (urow) {  // dMqk row r, columns half*32 .. +32 -> E1 row/column sums, dQK
                 const int cb = half * 32;
@@ -756,7 +760,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ok = __syncthreads_and(ok);
         fence_after_sync();
         // ---- phase 3 (K over tokens): dQ2^T = K^T dQK^T;  dK^T += Q^T dQK  (M=128, N=64)
-        if (tid == 0 && ok) {
+        if (tid == kQkIssuer && ok) {
             for (int j = 0; j < 2; ++j) tma_store_2d(&tm_dWt, sm + qk::EU + j * 8192, 0, krow0 + 64 * j);
             bulk_commit();
             const uint32_t idq = idesc_bf16(128, 64, true, false);
@@ -797,9 +801,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (ok) ok = mbar_wait(&bars[4], ph, err, 8);
         __syncwarp();
         fence_after_sync();
-        if (tid == 0) bulk_wait_read0();  // the previous dq store no longer reads the dq tile
+        if (tid == kQkIssuer) bulk_wait_read0();  // the previous dq store no longer reads the dq tile
         __syncthreads();                  // Q, K, dQK free; dq tile writable
-        if (tid == 0 && ok && ch + gridDim.x < nchunks) load_B(ch + gridDim.x);
+        if (tid == 96 && ok && ch + gridDim.x < nchunks) load_B(ch + gridDim.x);
         {
             const int cb = half * 32;
             unsigned char* dqt = sm + qk::DQ;
@@ -827,7 +831,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        if (tid == 0 && ok) {
+        if (tid == kQkIssuer && ok) {
             for (int j = 0; j < 2; ++j) {
                 tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
                 tma_store_2d(&tm_dKp, sm + qk::U + j * 8192, 0, krow0 + 64 * j);
@@ -836,7 +840,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         if (!ok) break;
     }
-    if (tid == 0) {
+    if (tid == kQkIssuer) {
         if (!ok) {  // prefetches of the next chunk may still be in flight (bounded waits)
             mbar_wait(&bars[0], (n + 1) & 1, nullptr, 0);
             mbar_wait(&bars[1], (n + 1) & 1, nullptr, 0);
