@@ -359,6 +359,14 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // the gradient of this chunk's end state, for the chunk-local gradients
                 tma_store_3d(&tm_dS1, sm + P::DS_OP, 0, (int)(chunk * kD), v0 / 8);
                 bulk_commit();
+                // With three stages, iteration it - 1 + NS goes into the stage of
+                // iteration it - 1 here, where this warp idles (its MMAs are done:
+                // bar2 of it - 1 was waited before the previous barrier 2); it is
+                // first read by the gamma dO operand during iteration it + 1.
+                if (NS >= 3 && ok && it > 0 && issued < NC) {
+                    ok = mbar_wait(bar2, (it - 1) & 1, err, 32) && ok;
+                    if (ok) issue_loads(issued++);
+                }
                 bulk_wait_read0();  // it has read dS1^T (rewritten after barrier 1)
             }
             __syncwarp();
@@ -369,8 +377,9 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (tma_issuer) {
                 tma_store_3d(&tm_dU, sm + P::DU_OP + (it & 1) * (kC * Vt * 2), 0, (int)(chunk * kC), v0 / 8);
                 bulk_commit();
-                // iteration it + NS into this iteration's stage once its MMAs are done
-                if (ok && issued < NC) {
+                // with two stages, iteration it + NS into this iteration's stage as
+                // soon as its MMAs are done (its gamma dO operand is read next iteration)
+                if (NS < 3 && ok && issued < NC) {
                     ok = mbar_wait(bar2, it & 1, err, 32) && ok;
                     if (ok) issue_loads(issued++);
                 }
