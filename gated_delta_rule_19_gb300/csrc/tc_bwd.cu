@@ -638,6 +638,15 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                 s2 > 0);
                 }
                 mma_commit(&bars[2]);
+                // S0^T [dO; dU]^T (N=128) reads only loaded tiles: issued now, it runs
+                // during epilogue 1 (phase 2's commit covers it)
+                const uint32_t id128 = idesc_bf16(128, 128, false, false);
+                const uint64_t ds0k = sdesc(sS0, 16, 1024, SW_128B), ddok = sdesc(sDO, 16, 1024, SW_128B);
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    const uint32_t o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
+                    mma_bf16_ss(tQW, desc_add(ds0k, o128), desc_add(ddok, o128), id128, s2 > 0);
+                }
             }
         }
         ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // dO and S0 tiles are read by every thread
@@ -686,19 +695,16 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        // ---- phase 2 (K over v): dMqk = [dO; -] U^T (N=64), S0^T [dO; dU]^T (N=128),
-        //      dK^T = dS1^T (eU)^T (N=64)   (M=128)
+        // ---- phase 2 (K over v): dMqk = [dO; -] U^T (N=64), dK^T = dS1^T (eU)^T (N=64)
+        //      (M=128); S0^T [dO; dU]^T was issued with phase 1
         if (tid == kQkIssuer && ok) {
             const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint32_t id128 = idesc_bf16(128, 128, false, false);
             const uint64_t ddo = sdesc(sDO, 16, 1024, SW_128B), du = sdesc(sU, 16, 1024, SW_128B);
-            const uint64_t ds0 = sdesc(sS0, 16, 1024, SW_128B);
             const uint64_t dds1 = sdesc(sDS1, 16, 1024, SW_128B), deu = sdesc(sEU, 16, 1024, SW_128B);
 #pragma unroll
             for (int s2 = 0; s2 < 8; ++s2) {
                 const uint32_t o64 = (s2 >> 2) * 8192 + (s2 & 3) * 32, o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
                 mma_bf16_ss(tDM, desc_add(ddo, o128), desc_add(du, o64), id, s2 > 0);
-                mma_bf16_ss(tQW, desc_add(ds0, o128), desc_add(ddo, o128), id128, s2 > 0);
                 mma_bf16_ss(tDK, desc_add(dds1, o128), desc_add(deu, o64), id, s2 > 0);
             }
             mma_commit(&bars[3]);
