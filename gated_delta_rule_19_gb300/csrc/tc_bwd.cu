@@ -1051,13 +1051,21 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     fence_before_sync();
     ok = __syncthreads_and(ok);
     fence_after_sync();
-    // ---- phase 2: Y = dT T^T  (M=128, K over tokens)
+    // ---- phase 2: Y = dT T^T  (M=128, K over tokens); then dV = T2^T dU (N=128,
+    // tokens on rows 64-127: T2 and dU are ready and Qm / P, whose columns it
+    // takes, were read before the barrier), which runs during the Y epilogue
+    // and is covered by phase 3's commit
     if (tid == 0 && ok) {
         const uint32_t id = idesc_bf16(128, 64, false, false);
         const uint64_t ddt = sdesc(sDT, 16, 1024, SW_128B), dt = sdesc(sT, 16, 1024, SW_128B);
 #pragma unroll
         for (int s2 = 0; s2 < 4; ++s2) mma_bf16_ss(tY, desc_add(ddt, s2 * 32), desc_add(dt, s2 * 32), id, s2 > 0);
         mma_commit(&bars[1]);
+        const uint32_t idv = idesc_bf16(128, 128, true, true);
+        const uint64_t dt2m = sdesc(sT2 - 8192, 8192, 1024, SW_128B), dum = sdesc(sDU, 8192, 1024, SW_128B);
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2)
+            mma_bf16_ss(tDV, desc_add(dt2m, s2 * 2048), desc_add(dum, s2 * 2048), idv, s2 > 0);
     }
     if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
     __syncwarp();
@@ -1072,17 +1080,13 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     fence_before_sync();
     ok = __syncthreads_and(ok);
     fence_after_sync();
-    // ---- phase 3: dA = -T^T Y (N=64, rows 0-63), dV = T2^T dU (N=128, tokens on rows 64-127)
+    // ---- phase 3: dA = -T^T Y (N=64, rows 0-63); its commit also covers dV
     if (tid == 0 && ok) {
         const uint32_t ida = idesc_bf16(128, 64, true, true, true);
-        const uint32_t idv = idesc_bf16(128, 128, true, true);
         const uint64_t dtm = sdesc(sT, 8192, 1024, SW_128B), dym = sdesc(sY, 8192, 1024, SW_128B);
-        const uint64_t dt2m = sdesc(sT2 - 8192, 8192, 1024, SW_128B), dum = sdesc(sDU, 8192, 1024, SW_128B);
 #pragma unroll
-        for (int s2 = 0; s2 < 4; ++s2) {
+        for (int s2 = 0; s2 < 4; ++s2)
             mma_bf16_ss(tDA, desc_add(dtm, s2 * 2048), desc_add(dym, s2 * 2048), ida, s2 > 0);
-            mma_bf16_ss(tDV, desc_add(dt2m, s2 * 2048), desc_add(dum, s2 * 2048), idv, s2 > 0);
-        }
         mma_commit(&bars[1]);
     }
     if (ok) ok = mbar_wait(&bars[1], 0, err, 8);
