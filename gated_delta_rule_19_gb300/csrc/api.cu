@@ -677,7 +677,7 @@ uint32_t one_bits(const gdn_problem* p) { return p->dtype == GDN_BF16 ? 0x3F80u 
 // The padded layout: packed -> laid out (gather) or back (scatter) for one tensor
 // of `width` bytes per (token, head).  `merge` (row moves only) is ORed into the
 // error word.
-cudaError_t varlen_move(const VarlenPlan& L, const gdn_problem* p, int64_t total, const int32_t* cu, char* ws,
+cudaError_t varlen_move(const VarlenPlan& L, int64_t total, const int32_t* cu, char* ws,
                         int width, const void* src, void* dst, uint32_t fill, bool scatter, const int* merge,
                         cudaStream_t cs) {
     int* err = (int*)ws;
@@ -786,12 +786,12 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu
     const int width[5] = {kb, kb, vb, (int)es, (int)es};
     const uint32_t fill[5] = {0u, 0u, 0u, one_bits(p), 0u};
     for (int i = 0; i < 5 && e == cudaSuccess; ++i)
-        e = varlen_move(L, p, total, cu_seqlens, ws, width[i], src[i], ws + dst[i], fill[i], false, nullptr, cs);
+        e = varlen_move(L, total, cu_seqlens, ws, width[i], src[i], ws + dst[i], fill[i], false, nullptr, cs);
     if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
     st = gdn_fwd(p, ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.b, initial_state, ws + L.o, final_state, saved,
                  ws + L.inner, L.q - L.inner, stream);
     if (st != GDN_OK) return st;
-    e = varlen_move(L, p, total, cu_seqlens, ws, vb, ws + L.o, o, 0u, true, nullptr, cs);
+    e = varlen_move(L, total, cu_seqlens, ws, vb, ws + L.o, o, 0u, true, nullptr, cs);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
 }
 
@@ -895,7 +895,7 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
     const int width[6] = {kb, kb, vb, vb, (int)es, (int)es};
     const uint32_t fill[6] = {0u, 0u, 0u, 0u, one_bits(p), 0u};
     for (int i = 0; i < 6 && e == cudaSuccess; ++i)
-        e = varlen_move(L, p, total, cu_seqlens, ws, width[i], src[i], ws + dst[i], fill[i], false, nullptr, cs);
+        e = varlen_move(L, total, cu_seqlens, ws, width[i], src[i], ws + dst[i], fill[i], false, nullptr, cs);
     if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
     st = gdn_bwd(p, ws + L.q, ws + L.k, ws + L.v, ws + L.a, ws + L.b, initial_state, saved, ws + L.d_o,
                  d_final_state, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db, d_initial_state,
@@ -905,7 +905,7 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
     void* gdst[5] = {dq, dk, dv, dalpha, dbeta};
     const int gw[5] = {kb, kb, vb, (int)es, (int)es};
     for (int i = 0; i < 5 && e == cudaSuccess; ++i)
-        e = varlen_move(L, p, total, cu_seqlens, ws, gw[i], ws + gsrc[i], gdst[i], 0u, true, nullptr, cs);
+        e = varlen_move(L, total, cu_seqlens, ws, gw[i], ws + gsrc[i], gdst[i], 0u, true, nullptr, cs);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
 }
 
