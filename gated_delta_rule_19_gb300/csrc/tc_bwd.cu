@@ -497,15 +497,15 @@ constexpr int U = 147456, EU = 163840;   // [64 x 128]
 constexpr int DQK = 180224;              // [64 x 64]
 constexpr int DQ = 188416;               // dq output tile [64 x 128]
 constexpr int E1 = 204800;               // fp32 [64][65]
-constexpr int VEC = E1 + 64 * 65 * 4;    // Gs gs eRp[2] dG1p[2] rE1 cE1 (8 x 64) + red (256)
-constexpr int BAR = VEC + (8 * 64 + 256) * 4;
+constexpr int VEC = E1 + 64 * 65 * 4;    // Gs gs eRp[4] dG1p[4] rE1 cE1 (12 x 64) + red (512)
+constexpr int BAR = VEC + (12 * 64 + 512) * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
 }  // namespace qk
 
-// Persistent: CTA i handles chunks i, i + gridDim.x, ...  256 threads; warps w and
-// w+4 split the columns of TMEM lanes 32*(w%4) ..  The next chunk's tiles are
-// requested as soon as their buffers are free (after phase 2 / phase 3).
-__global__ void __launch_bounds__(256, 1)
+// Persistent: CTA i handles chunks i, i + gridDim.x, ...  512 threads; warps w,
+// w+4, w+8 and w+12 split the columns of TMEM lanes 32*(w%4) ..  The next chunk's
+// tiles are requested as soon as their buffers are free (after phase 2 / phase 3).
+__global__ void __launch_bounds__(512, 1)
 grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_W,
            const __grid_constant__ CUtensorMap tm_dU, const __grid_constant__ CUtensorMap tm_S0,
@@ -518,16 +518,18 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     float* E1f = (float*)(sm + qk::E1);
     float* Gs = (float*)(sm + qk::VEC);
     float* gs = Gs + 64;
-    float* eRp = gs + 64;    // [2][64]
-    float* dG1p = eRp + 128; // [2][64]
-    float* rE1 = dG1p + 128;
+    float* eRp = gs + 64;    // [4 column quarters][64]
+    float* dG1p = eRp + 256; // [4][64]
+    float* rE1 = dG1p + 256;
     float* cE1 = rE1 + 64;
-    float* red = cE1 + 64;   // 256
+    float* red = cE1 + 64;   // 512
     uint64_t* bars = (uint64_t*)(sm + qk::BAR);  // [0] loads A, [1] loads B, [2..4] MMA phases
     uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 48);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int sub = warp & 3, half = warp >> 2;
+    // 16 warps: warp w reaches TMEM lanes 32*(w%4) ..; the four warps of a lane
+    // quarter split the columns of every epilogue (qtr = w / 4)
+    const int sub = warp & 3, qtr = warp >> 2;
     const int lanerow = 32 * sub + lane;
     const bool urow = sub < 2;
     const int r = urow ? lanerow : lanerow - 64;
@@ -613,14 +615,14 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (ch + gridDim.x < nchunks) gnext = *(const float2*)(G + (ch + gridDim.x) * kC + 2 * lane);
         }
         // rows of Ut (64 columns) and Mqk (32 columns) this thread needs, fetched early
-        uint4 utv[8], mqv[4];
+        uint4 utv[4], mqv[2];
         if (urow) {
-            const uint4* up = (const uint4*)(Ut + ((int64_t)row0 + r) * kD + half * 64);
+            const uint4* up = (const uint4*)(Ut + ((int64_t)row0 + r) * kD + qtr * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) utv[q] = up[q];
-            const uint4* mp = (const uint4*)(Mqk + ((int64_t)row0 + r) * kC + half * 32);
+            for (int q = 0; q < 4; ++q) utv[q] = up[q];
+            const uint4* mp = (const uint4*)(Mqk + ((int64_t)row0 + r) * kC + qtr * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) mqv[q] = mp[q];
+            for (int q = 0; q < 2; ++q) mqv[q] = mp[q];
         }
         // ---- phase 1 (K over k): [X; Y] = [W; Q] S0^T, Z = [K; -] dS1^T  (M=128, N=128)
         if (tid == kQkIssuer) {
@@ -657,10 +659,10 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float GC = Gs[63], gC = gs[63];
         const float Gr = Gs[r], er = expf(GC - Gr);
         {
-            const int cb = half * 64;
+            const int cb = qtr * 32;
             float acc = 0.f;
 #pragma unroll
-            for (int c0 = cb; c0 < cb + 64; c0 += 16) {
+            for (int c0 = cb; c0 < cb + 32; c0 += 16) {
                 if (urow) {
                     float x[16], z[16], u[16], eu[16];
                     tmem_load16f2(tXY + lanebase + c0, tZ + lanebase + c0, x, z);
@@ -688,8 +690,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int j = 0; j < 8; ++j) acc += dd[j] * y[j] + de[j] * y[8 + j];
                 }
             }
-            if (urow) eRp[half * 64 + r] = acc;
-            else dG1p[half * 64 + r] = acc;
+            if (urow) eRp[qtr * 64 + r] = acc;
+            else dG1p[qtr * 64 + r] = acc;
         }
         fence_proxy_async();
         fence_before_sync();
@@ -714,8 +716,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint4* bq = (const uint4*)(sm + qk::DS1) + tid;
             float acc = 0.f;
 #pragma unroll 4
-            for (int i = 0; i < 8; ++i) {
-                const uint4 x = a[i * 256], y = bq[i * 256];
+            for (int i = 0; i < 4; ++i) {
+                const uint4 x = a[i * 512], y = bq[i * 512];
                 const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc += bf_lo(xw[e]) * bf_lo(yw[e]) + bf_hi(xw[e]) * bf_hi(yw[e]);
@@ -730,12 +732,12 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // issued from warp 3 (output rows), which has the lighter epilogue in this phase
         if (tid == 96 && ok && ch + gridDim.x < nchunks) load_A(ch + gridDim.x);
         {
-            if (urow) {  // dMqk row r, columns half*32 .. +32 -> E1 row/column sums, dQK
-                const int cb = half * 32;
-                float e1[32];
+            if (urow) {  // dMqk row r, columns qtr*16 .. +16 -> E1 row/column sums, dQK
+                const int cb = qtr * 16;
+                float e1[16];
                 float rsum = 0.f;
 #pragma unroll
-                for (int c0 = 0; c0 < 32; c0 += 16) {
+                for (int c0 = 0; c0 < 16; c0 += 16) {
                     float dm[16], dq[16];
                     tmem_load16f(tDM + lanebase + cb + c0, dm);
                     const uint4 ma = mqv[c0 / 8], mb = mqv[c0 / 8 + 1];
@@ -750,25 +752,21 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                     tile_put16(sm + qk::DQK, 64, r, cb + c0, dq);
                 }
-                // row sums (this half of the columns) and column sums (these 32 rows)
-                E1f[half * 64 + r] = rsum;
-                E1f[128 + (sub * 2 + half) * 32 + lane] = warp_colsum32(e1);
+                // row sums (this quarter of the columns) and column sums (these 32 rows)
+                E1f[qtr * 64 + r] = rsum;
+                const float csum = warp_colsum16(e1);
+                if (lane < 16) E1f[256 + (sub * 4 + qtr) * 16 + lane] = csum;
             }
-            // dW^T row k (= lanerow), columns half*32 .. +32 -> [128 x 64] tile in the EU
+            // dW^T row k (= lanerow), columns qtr*16 .. +16 -> [128 x 64] tile in the EU
             // slot (dead once phase 2 is done), stored to scratch by TMA
-            const int cb = half * 32;
+            const int cb = qtr * 16;
             unsigned char* wt = sm + qk::EU + (lanerow >> 6) * 8192;
-            float w[16], w2[16];
-            tmem_load16f2(tDW + lanebase + cb, tDW + lanebase + cb + 16, w, w2);
+            float w[16];
+            tmem_load16f(tDW + lanebase + cb, w);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                w[j] = -w[j];
-                w2[j] = -w2[j];
-            }
+            for (int j = 0; j < 16; ++j) w[j] = -w[j];
             *(uint4*)(wt + sw128_off(lanerow & 63, cb)) = pack8(w);
             *(uint4*)(wt + sw128_off(lanerow & 63, cb + 8)) = pack8(w + 8);
-            *(uint4*)(wt + sw128_off(lanerow & 63, cb + 16)) = pack8(w2);
-            *(uint4*)(wt + sw128_off(lanerow & 63, cb + 24)) = pack8(w2 + 8);
         }
         fence_proxy_async();
         fence_before_sync();
@@ -791,17 +789,18 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mma_commit(&bars[4]);
         }
         if (tid < 64) {
-            // E1f[0..127]: row sums per column half; E1f[128 + (sub*2+half)*32 + col]:
-            // column sums over rows 32*sub .. +31 of columns half*32 + col
-            rE1[tid] = E1f[tid] + E1f[64 + tid];
-            const int hh = tid >> 5, col = tid & 31;
-            cE1[tid] = E1f[128 + (0 * 2 + hh) * 32 + col] + E1f[128 + (1 * 2 + hh) * 32 + col];
+            // E1f[q*64 + row]: row sums over column quarter q; E1f[256 + (sub*4+q)*16 +
+            // col]: column sums over rows 32*sub .. +31 of column q*16 + col
+            rE1[tid] = E1f[tid] + E1f[64 + tid] + E1f[128 + tid] + E1f[192 + tid];
+            const int qq = tid >> 4, col = tid & 15;
+            cE1[tid] = E1f[256 + (0 * 4 + qq) * 16 + col] + E1f[256 + (1 * 4 + qq) * 16 + col];
         } else if (warp == 2) {
             float ip = 0.f;
-            for (int i = lane; i < 256; i += 32) ip += red[i];
+            for (int i = lane; i < 512; i += 32) ip += red[i];
             // sum_i exp(G_C - G_i) eR_i over the chunk's 64 tokens
-            float es = expf(GC - Gs[lane]) * (eRp[lane] + eRp[64 + lane]) +
-                       expf(GC - Gs[32 + lane]) * (eRp[32 + lane] + eRp[96 + lane]);
+            const float eR0 = eRp[lane] + eRp[64 + lane] + eRp[128 + lane] + eRp[192 + lane];
+            const float eR1 = eRp[32 + lane] + eRp[96 + lane] + eRp[160 + lane] + eRp[224 + lane];
+            float es = expf(GC - Gs[lane]) * eR0 + expf(GC - Gs[32 + lane]) * eR1;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 ip += __shfl_xor_sync(0xffffffffu, ip, off);
@@ -820,11 +819,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         __syncthreads();                  // Q, K, dQK free; dq tile writable
         if (tid == 96 && ok && ch + gridDim.x < nchunks) load_B(ch + gridDim.x);
         {
-            const int cb = half * 32;
+            const int cb = qtr * 16;
             unsigned char* dqt = sm + qk::DQ;
             unsigned char* kt = sm + qk::U + (lanerow >> 6) * 8192;  // U is dead after phase 2
 #pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
+            for (int c0 = 0; c0 < 16; c0 += 16) {
                 float q1[16], q2[16], kk[16];
                 tmem_load16f3(tQ1 + lanebase + cb + c0, tQ2 + lanebase + cb + c0, tDK + lanebase + cb + c0, q1,
                               q2, kk);
@@ -837,8 +836,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
         if (tid < 64) {
-            const float eR = eRp[tid] + eRp[64 + tid];
-            float g = gs[tid] * (dG1p[tid] + dG1p[64 + tid]) + rE1[tid] - cE1[tid] - expf(GC - Gs[tid]) * eR;
+            const float eR = eRp[tid] + eRp[64 + tid] + eRp[128 + tid] + eRp[192 + tid];
+            const float dG1 = dG1p[tid] + dG1p[64 + tid] + dG1p[128 + tid] + dG1p[192 + tid];
+            float g = gs[tid] * dG1 + rE1[tid] - cE1[tid] - expf(GC - Gs[tid]) * eR;
             if (tid == 63) g += gC * red[0] + red[1];
             dGp[(int64_t)row0 + tid] = g;
         }
@@ -1277,7 +1277,7 @@ cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;
     dim3 grid((unsigned)std::min<int64_t>(nchunks, sm_count()));
-    grad_qk_tc<<<grid, 256, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, mdKp, mdWt, tb.Ut, tb.Mqk,
+    grad_qk_tc<<<grid, 512, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, mdKp, mdWt, tb.Ut, tb.Mqk,
                                             tb.G, bb.dGp, tb.err);
     return cudaGetLastError();
 }
