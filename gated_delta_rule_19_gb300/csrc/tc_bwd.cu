@@ -504,7 +504,7 @@ constexpr size_t SMEM = BAR + 64 + 1024;
 
 // Persistent: CTA i handles chunks i, i + gridDim.x, ...  512 threads; warps w,
 // w+4, w+8 and w+12 split the columns of TMEM lanes 32*(w%4) ..  The next chunk's
-// tiles are requested as soon as their buffers are free (after phase 2 / phase 3).
+// tiles are requested as soon as their buffers are free (after phase 1, 2 and 3).
 __global__ void __launch_bounds__(512, 1)
 grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_W,
@@ -523,8 +523,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     float* rE1 = dG1p + 256;
     float* cE1 = rE1 + 64;
     float* red = cE1 + 64;   // 512
-    uint64_t* bars = (uint64_t*)(sm + qk::BAR);  // [0] loads A, [1] loads B, [2..4] MMA phases
-    uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 48);
+    // [0] loads A1, [1] loads B, [2..4] MMA phases, [5] loads A2, [6] S0^T [dO; dU]^T
+    uint64_t* bars = (uint64_t*)(sm + qk::BAR);
+    uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 56);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // 16 warps: warp w reaches TMEM lanes 32*(w%4) ..; the four warps of a lane
@@ -544,20 +545,27 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         h = (int)(bh % d.H);
         b = (int)(bh / d.H);
     };
-    // group A: W, dU, dO, S0^T, dS1^T (free after phase 2); group B: Q, K (after phase 3)
-    auto load_A = [&](int64_t ch) {
-        int b, h, c;
-        decode(ch, b, h, c);
+    // group A1: W, dU, S0^T (free once phase 1's MMAs are done and <dS1, S0> is
+    // formed); A2: dO, dS1^T (free after phase 2); B: Q, K (free after phase 3)
+    auto load_A1 = [&](int64_t ch) {
         const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
-        mbar_arrive_expect_tx(&bars[0], 14 * 8192);
+        mbar_arrive_expect_tx(&bars[0], 8 * 8192);
         for (int j = 0; j < 2; ++j) {
             tma_load_2d(sm + qk::WQ + j * 16384, &tm_W, &bars[0], 64 * j, row0);
-            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[0], 64 * j, h, c * kC, b);
             tma_load_2d(sm + qk::DU + j * 16384, &tm_dU, &bars[0], 64 * j, row0);
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < 2; ++i)
                 tma_load_2d(sm + qk::S0 + j * 16384 + i * 8192, &tm_S0, &bars[0], 64 * j, krow0 + 64 * i);
-                tma_load_2d(sm + qk::DS1 + j * 16384 + i * 8192, &tm_dS1, &bars[0], 64 * j, krow0 + 64 * i);
-            }
+        }
+    };
+    auto load_A2 = [&](int64_t ch) {
+        int b, h, c;
+        decode(ch, b, h, c);
+        const int krow0 = (int)(ch * kD);
+        mbar_arrive_expect_tx(&bars[5], 6 * 8192);
+        for (int j = 0; j < 2; ++j) {
+            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[5], 64 * j, h, c * kC, b);
+            for (int i = 0; i < 2; ++i)
+                tma_load_2d(sm + qk::DS1 + j * 16384 + i * 8192, &tm_dS1, &bars[5], 64 * j, krow0 + 64 * i);
         }
     };
     auto load_B = [&](int64_t ch) {
@@ -575,10 +583,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     float2 gnext = make_float2(0.f, 0.f);
     if (warp == 3 && first < nchunks) gnext = *(const float2*)(G + first * kC + 2 * lane);
     if (tid == kQkIssuer) {
-        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         if (first < nchunks) {
-            load_A(first);
+            load_A1(first);
+            load_A2(first);
             load_B(first);
         }
     }
@@ -627,6 +636,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // ---- phase 1 (K over k): [X; Y] = [W; Q] S0^T, Z = [K; -] dS1^T  (M=128, N=128)
         if (tid == kQkIssuer) {
             ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[5], ph, err, 1) && ok;
             ok = mbar_wait(&bars[1], ph, err, 1) && ok;
             if (ok) {
                 const uint32_t id = idesc_bf16(128, 128, false, true);
@@ -641,7 +651,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
                 mma_commit(&bars[2]);
                 // S0^T [dO; dU]^T (N=128) reads only loaded tiles: issued now, it runs
-                // during epilogue 1 (phase 2's commit covers it)
+                // during epilogue 1 (its own commit frees W, dU, S0^T for the next chunk)
                 const uint32_t id128 = idesc_bf16(128, 128, false, false);
                 const uint64_t ds0k = sdesc(sS0, 16, 1024, SW_128B), ddok = sdesc(sDO, 16, 1024, SW_128B);
 #pragma unroll
@@ -649,13 +659,34 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const uint32_t o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
                     mma_bf16_ss(tQW, desc_add(ds0k, o128), desc_add(ddok, o128), id128, s2 > 0);
                 }
+                mma_commit(&bars[6]);
             }
         }
-        ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // dO and S0 tiles are read by every thread
+        ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // S0 (read below)
+        ok = mbar_wait(&bars[5], ph, err, 1) && ok;  // dO and dS1
+        {   // <dS1, S0> over the chunk (both tiles share one layout), coalesced, while
+            // phase 1's MMAs run
+            const uint4* a = (const uint4*)(sm + qk::S0) + tid;
+            const uint4* bq = (const uint4*)(sm + qk::DS1) + tid;
+            float acc = 0.f;
+#pragma unroll 4
+            for (int i = 0; i < 4; ++i) {
+                const uint4 x = a[i * 512], y = bq[i * 512];
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc += bf_lo(xw[e]) * bf_lo(yw[e]) + bf_hi(xw[e]) * bf_hi(yw[e]);
+            }
+            red[tid] = acc;
+        }
         ok = mbar_wait(&bars[2], ph, err, 2) && ok;
         if (tid == kQkIssuer) bulk_wait_read0();  // the previous chunk's stores from the U / EU tiles are done
-        __syncthreads();  // Gs / gs
+        __syncthreads();  // Gs / gs; every thread is past its reads of S0^T
         fence_after_sync();
+        // W, dU, S0^T are free once S0^T [dO; dU]^T is done: request the next chunk's
+        if (tid == 96 && ok && ch + gridDim.x < nchunks) {
+            ok = mbar_wait(&bars[6], ph, err, 2);
+            if (ok) load_A1(ch + gridDim.x);
+        }
         const float GC = Gs[63], gC = gs[63];
         const float Gr = Gs[r], er = expf(GC - Gr);
         {
@@ -711,26 +742,13 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             mma_commit(&bars[3]);
         }
-        {   // <dS1, S0> over the chunk (both tiles share one layout), coalesced
-            const uint4* a = (const uint4*)(sm + qk::S0) + tid;
-            const uint4* bq = (const uint4*)(sm + qk::DS1) + tid;
-            float acc = 0.f;
-#pragma unroll 4
-            for (int i = 0; i < 4; ++i) {
-                const uint4 x = a[i * 512], y = bq[i * 512];
-                const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc += bf_lo(xw[e]) * bf_lo(yw[e]) + bf_hi(xw[e]) * bf_hi(yw[e]);
-            }
-            red[tid] = acc;
-        }
         if (ok) ok = mbar_wait(&bars[3], ph, err, 4);
         __syncwarp();
         fence_after_sync();
-        // W, dU, dO, S0^T, dS1^T are free: request the next chunk's
+        // dO, dS1^T are free: request the next chunk's
         __syncthreads();  // every thread is past its reads of those tiles
         // issued from warp 3 (output rows), which has the lighter epilogue in this phase
-        if (tid == 96 && ok && ch + gridDim.x < nchunks) load_A(ch + gridDim.x);
+        if (tid == 96 && ok && ch + gridDim.x < nchunks) load_A2(ch + gridDim.x);
         {
             if (urow) {  // dMqk row r, columns qtr*16 .. +16 -> E1 row/column sums, dQK
                 const int cb = qtr * 16;
@@ -858,6 +876,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (tid == kQkIssuer) {
         if (!ok) {  // prefetches of the next chunk may still be in flight (bounded waits)
             mbar_wait(&bars[0], (n + 1) & 1, nullptr, 0);
+            mbar_wait(&bars[5], (n + 1) & 1, nullptr, 0);
             mbar_wait(&bars[1], (n + 1) & 1, nullptr, 0);
         }
         bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
