@@ -26,6 +26,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "gdn_internal.h"
@@ -163,22 +164,29 @@ __device__ void solve_unit_lower_64(const float* A, float* Tf, float* X) {
 // Shared-memory plan of prep_fwd_tc (offsets from a 1024-aligned base).  The Gram
 // MMA reads [K_0; Q_0] and [K_1; Q_1] as M=128 K-major operands (rows 64-127 of a
 // K-major tile lie 8 KB after rows 0-63); the W / Ut MMA reads K_0, K_1, V_0, V_1
-// as one N=256 MN-major operand (64-wide blocks 16 KB apart).
+// as one N=256 MN-major operand (64-wide blocks 16 KB apart).  W and Ut are staged
+// for their stores in the fp32 T and A regions, dead by then, so that the input
+// slots can take the next chunk's tiles as soon as the MMAs reading them are done.
 constexpr int P_K0 = 0, P_Q0 = 8192, P_K1 = 16384, P_Q1 = 24576;
-constexpr int P_V0 = 32768, P_M = 40960;  // V_1 at P_V0 + 16384; P_M: the Mqk output tile
-constexpr int P_AF = 57344;                             // fp32 A [64][kAS], dead before T1 / T2 exist
-constexpr int P_T1 = 65536, P_T2 = 73728;               // [T1; T2]: one M=128 K-major operand
-constexpr int P_TF = 81920;                             // fp32 T [64][kAS]
-constexpr int P_X = P_Q0;                               // fp32 [32][kXS] scratch, Q_0 is dead by then
-constexpr int P_VEC = P_TF + 64 * kAS * 4;              // G (log2 units), gamma, beta
+constexpr int P_V0 = 32768, P_M = 40960;   // V_1 at P_V0 + 16384; P_M: the Mqk output tile
+constexpr int P_AF = 57344;                // fp32 A [64][kAS], dead before T1 / T2 exist
+constexpr int P_T1 = 65536, P_T2 = 73728;  // [T1; T2]: one M=128 K-major operand
+constexpr int P_TF = 81920;                // fp32 T [64][kAS]
+constexpr int P_US = P_AF, P_WS = P_TF;    // Ut / W output tiles [64 x 128] (two 8 KB halves)
+constexpr int P_X = P_TF + 64 * kAS * 4;   // fp32 [32][kXS] solve scratch
+constexpr int P_VEC = P_X + 32 * kXS * 4;  // G (log2 units), gamma, beta
 constexpr int P_BAR = P_VEC + 3 * 64 * 4;
 constexpr int P_END = P_BAR + 64;
 constexpr size_t kPrepSmem = P_END + 1024;
 static_assert(P_AF + 64 * kAS * 4 <= P_T2 + 8192, "A overlaps only T1 / T2");
-static_assert(32 * kXS * 4 <= 8192, "solve scratch fits the Q_0 slot");
+static_assert(P_WS + 16384 <= P_X && P_US + 16384 <= P_T2 + 8192, "output tiles fit the dead regions");
+static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
-// One CTA per chunk, 256 threads, two CTAs per SM.  Warps w and w+4 read the same
-// TMEM lane quarter (w % 4) and split its columns.
+// Persistent, two CTAs per SM, 256 threads: CTA i takes chunks i, i + gridDim.x, ...
+// Warps w and w+4 read the same TMEM lane quarter (w % 4) and split its columns.
+// A chunk's Q tiles are replaced by the next chunk's once the Gram MMA is done, its
+// K and V tiles once the W / Ut MMA is done (both requested by thread 128, whose
+// warp has no Gram epilogue work); warp 2 keeps the next chunk's gates in registers.
 __global__ void __launch_bounds__(256, 2)
 prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_W,
@@ -192,35 +200,42 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     float* G2s = (float*)(sm + P_VEC);  // within-chunk cumsum of log2(alpha)
     float* gs = G2s + 64;               // gamma = alpha_1 ... alpha_r
     float* bs = gs + 64;
-    uint64_t* bars = (uint64_t*)(sm + P_BAR);  // [0] TMA, [1] MMA
-    uint32_t* tslot = (uint32_t*)(sm + P_BAR + 16);
+    uint64_t* bars = (uint64_t*)(sm + P_BAR);  // [0] Q loads, [1] K, V loads, [2] Gram MMA, [3] W / Ut MMA
+    uint32_t* tslot = (uint32_t*)(sm + P_BAR + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = warp & 3, half = warp >> 2;
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int t0 = c * kC;
-    const int64_t chunk = ((int64_t)b * d.H + h) * d.NC + c;
-    const int row0 = (int)(chunk * kC);
+    const int64_t nchunks = d.NS() * d.NC;
+    constexpr int kLoader = 128;
 
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bars[0], 6 * 8192);
+    // chunk index = (b * H + h) * NC + c
+    auto decode = [&](int64_t ch, int& b, int& h, int& t0) {
+        t0 = (int)(ch % d.NC) * kC;
+        const int64_t bh = ch / d.NC;
+        h = (int)(bh % d.H);
+        b = (int)(bh / d.H);
+    };
+    auto load_q = [&](int64_t ch) {
+        int b, h, t0;
+        decode(ch, b, h, t0);
+        mbar_arrive_expect_tx(&bars[0], 2 * 8192);
+        for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_Q0 + j * 16384, &tm_q, &bars[0], 64 * j, h, t0, b);
+    };
+    auto load_kv = [&](int64_t ch) {
+        int b, h, t0;
+        decode(ch, b, h, t0);
+        mbar_arrive_expect_tx(&bars[1], 4 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + P_K0 + j * 16384, &tm_k, &bars[0], 64 * j, h, t0, b);
-            tma_load_4d(sm + P_Q0 + j * 16384, &tm_q, &bars[0], 64 * j, h, t0, b);
-            tma_load_4d(sm + P_V0 + j * 16384, &tm_v, &bars[0], 64 * j, h, t0, b);
+            tma_load_4d(sm + P_K0 + j * 16384, &tm_k, &bars[1], 64 * j, h, t0, b);
+            tma_load_4d(sm + P_V0 + j * 16384, &tm_v, &bars[1], 64 * j, h, t0, b);
         }
-    }
-    if (warp == 1) {
-        tmem_alloc(tslot, 256);
-        tmem_relinquish();
-    }
-    // warp 2: gates of tokens 2 lane, 2 lane + 1, loaded now and used once the Gram MMA
-    // is issued; padding (alpha = 1, beta = 0) leaves the state unchanged
+    };
+    // warp 2: gates of tokens 2 lane, 2 lane + 1 of a chunk; padding (alpha = 1,
+    // beta = 0) leaves the state unchanged
     bf16 ga[2], gb[2];
-    if (warp == 2) {
+    auto load_gates = [&](int64_t ch) {
+        int b, h, t0;
+        decode(ch, b, h, t0);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * lane + e;
@@ -232,193 +247,243 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 gb[e] = beta[gi];
             }
         }
+    };
+
+    const int64_t first = blockIdx.x;
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        if (first < nchunks) {
+            load_q(first);
+            load_kv(first);
+        }
     }
+    if (warp == 1) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
+    if (warp == 2 && first < nchunks) load_gates(first);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
     bool ok = true;
-    if (tid == 0) {
-        ok = mbar_wait(&bars[0], 0, err, 1);
-        if (ok) {
-            // [K; Q] K^T = [K K^T ; Q K^T] into columns 0-63 (M=128, N=64, K over k)
-            const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint32_t base = smem_u32(sm + P_K0);
+    int n = 0;
+    int nq = first < nchunks ? 1 : 0, nkv = nq;  // load batches issued (thread kLoader's count)
+    int g_last = -1, w_last = -1;               // chunks whose MMAs were issued (thread 0)
+#pragma unroll 1
+    for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
+        const int ph = n & 1;
+        const int64_t nxt = ch + gridDim.x;
+        const bool has_next = nxt < nchunks;
+        const int row0 = (int)(ch * kC);
+        if (tid == 0) {
+            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[1], ph, err, 1) && ok;
+            if (ok) {
+                // [K; Q] K^T = [K K^T ; Q K^T] into columns 0-63 (M=128, N=64, K over k)
+                const uint32_t id = idesc_bf16(128, 64, false, false);
+                const uint32_t base = smem_u32(sm + P_K0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t a = base + (s >> 2) * 16384 + (s & 3) * 32;
-                mma_bf16_ss(tmem, sdesc(a, 16, 1024, SW_128B), sdesc(a, 16, 1024, SW_128B), id, s > 0);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t a = base + (s >> 2) * 16384 + (s & 3) * 32;
+                    mma_bf16_ss(tmem, sdesc(a, 16, 1024, SW_128B), sdesc(a, 16, 1024, SW_128B), id, s > 0);
+                }
+                mma_commit(&bars[2]);
+                g_last = n;
             }
-            mma_commit(&bars[1]);
+            bulk_wait_read0();  // the previous chunk's stores have read the A, T and Mqk tiles
         }
-    }
-    if (warp == 2) {
-        const float l[2] = {log2f(__bfloat162float(ga[0])), log2f(__bfloat162float(ga[1]))};
-        const float pair = l[0] + l[1];
-        float incl = pair;
+        if (warp == 2) {
+            const float l[2] = {log2f(__bfloat162float(ga[0])), log2f(__bfloat162float(ga[1]))};
+            const float pair = l[0] + l[1];
+            float incl = pair;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const float g0 = incl - pair + l[0], g1 = incl;
+            G2s[2 * lane] = g0;
+            G2s[2 * lane + 1] = g1;
+            gs[2 * lane] = exp2f(g0);
+            gs[2 * lane + 1] = exp2f(g1);
+            bs[2 * lane] = __bfloat162float(gb[0]);
+            bs[2 * lane + 1] = __bfloat162float(gb[1]);
+            constexpr float kLn2 = 0.693147180559945309f;
+            *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
+            if (has_next) load_gates(nxt);  // consumed next iteration
         }
-        const float g0 = incl - pair + l[0], g1 = incl;
-        G2s[2 * lane] = g0;
-        G2s[2 * lane + 1] = g1;
-        gs[2 * lane] = exp2f(g0);
-        gs[2 * lane + 1] = exp2f(g1);
-        bs[2 * lane] = __bfloat162float(gb[0]);
-        bs[2 * lane + 1] = __bfloat162float(gb[1]);
-        constexpr float kLn2 = 0.693147180559945309f;
-        *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
-    }
-    __syncthreads();  // gates visible
-    ok = mbar_wait(&bars[1], 0, err, 2) && ok;
-    __syncwarp();
-    fence_after_sync();
-    // Gram epilogue: lanes 0-63 hold rows of K K^T -> A (fp32), lanes 64-127 rows of
-    // Q K^T -> Mqk (bf16 tile); this warp takes columns cb .. cb+31.
-    {
-        const int rr = 32 * (sub & 1) + lane;
-        const int cb = 32 * half;
-        const bool any = cb <= 32 * (sub & 1) + 31;  // warp-uniform: some column on or below the diagonal
-        const float G2r = G2s[rr];
-        if (sub < 2) {
-            if (any) {
-                uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + cb, v);
-                tmem_wait_ld(v);
-                const float br = bs[rr];
-                float* arow = Af + rr * kAS + cb;
+        __syncthreads();  // gates visible; the output tiles are writable
+        ok = mbar_wait(&bars[2], ph, err, 2) && ok;
+        __syncwarp();
+        fence_after_sync();
+        if (tid == kLoader && ok && has_next) {  // the Q tiles are free
+            load_q(nxt);
+            ++nq;
+        }
+        // Gram epilogue: lanes 0-63 hold rows of K K^T -> A (fp32), lanes 64-127 rows of
+        // Q K^T -> Mqk (bf16 tile); this warp takes columns cb .. cb+31.
+        {
+            const int rr = 32 * (sub & 1) + lane;
+            const int cb = 32 * half;
+            const bool any = cb <= 32 * (sub & 1) + 31;  // warp-uniform: some column on or below the diagonal
+            const float G2r = G2s[rr];
+            if (sub < 2) {
+                if (any) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + cb, v);
+                    tmem_wait_ld(v);
+                    const float br = bs[rr];
+                    float* arow = Af + rr * kAS + cb;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float f[4];
+                    for (int q = 0; q < 8; ++q) {
+                        float f[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = cb + 4 * q + e;
-                        f[e] = (i < rr) ? br * exp2f(G2r - G2s[i]) * __uint_as_float(v[4 * q + e]) : 0.f;
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = cb + 4 * q + e;
+                            f[e] = (i < rr) ? br * exp2f(G2r - G2s[i]) * __uint_as_float(v[4 * q + e]) : 0.f;
+                        }
+                        *(float4*)(arow + 4 * q) = make_float4(f[0], f[1], f[2], f[3]);
                     }
-                    *(float4*)(arow + 4 * q) = make_float4(f[0], f[1], f[2], f[3]);
+                }
+            } else {
+                unsigned char* mt = sm + P_M;
+                if (any) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + cb, v);
+                    tmem_wait_ld(v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = cb + 8 * q + 2 * e;
+                            const float m0 = (i <= rr) ? exp2f(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
+                            const float m1 =
+                                (i + 1 <= rr) ? exp2f(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f;
+                            pk[e] = pack_bf16(m0, m1);
+                        }
+                        *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-        } else {
-            unsigned char* mt = sm + P_M;
-            if (any) {
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0) {
+            tma_store_2d(&tm_M, sm + P_M, 0, row0);
+            bulk_commit();
+        }
+        solve_unit_lower_64(Af, Tf, (float*)(sm + P_X));  // ends with __syncthreads
+        // B operands of W / Ut: T1 = T diag(beta gamma), T2 = T diag(beta), bf16 K-major
+        // [r][i], zero above the diagonal; T itself to global memory when asked for.
+        {
+            const int r = tid >> 2, i0 = (tid & 3) * 16;
+            const float* trow = Tf + r * kAS + i0;
+            uint32_t p0[8], p1[8], p2[8];
+#pragma unroll
+            for (int e4 = 0; e4 < 16; e4 += 4) {
+                const float4 t4 = *(const float4*)(trow + e4);
+                float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (i0 + e4 + e > r) tv[e] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int i = i0 + e4 + e;
+                    const float b0 = bs[i], b1 = bs[i + 1];
+                    p0[(e4 + e) >> 1] = pack_bf16(tv[e], tv[e + 1]);
+                    p1[(e4 + e) >> 1] = pack_bf16(tv[e] * b0 * gs[i], tv[e + 1] * b1 * gs[i + 1]);
+                    p2[(e4 + e) >> 1] = pack_bf16(tv[e] * b0, tv[e + 1] * b1);
+                }
+            }
+            if (Tout) {
+                uint4* tg = (uint4*)(Tout + ((int64_t)row0 + r) * kC + i0);
+                tg[0] = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+                tg[1] = make_uint4(p0[4], p0[5], p0[6], p0[7]);
+            }
+            *(uint4*)(sm + P_T1 + sw128_off(r, i0)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+            *(uint4*)(sm + P_T1 + sw128_off(r, i0 + 8)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
+            *(uint4*)(sm + P_T2 + sw128_off(r, i0)) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+            *(uint4*)(sm + P_T2 + sw128_off(r, i0 + 8)) = make_uint4(p2[4], p2[5], p2[6], p2[7]);
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        if (tid == 0 && ok) {
+            // [T1; T2] [K | V] (M=128, N=256, K over tokens): rows 0-63 of columns 0-127
+            // are W = T1 K, rows 64-127 of columns 128-255 are Ut = T2 V.
+            const uint32_t id = idesc_bf16(128, 256, false, true);
+            const uint64_t da = sdesc(smem_u32(sm + P_T1), 16, 1024, SW_128B);
+            const uint64_t db = sdesc(smem_u32(sm + P_K0), 16384, 1024, SW_128B);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) mma_bf16_ss(tmem, desc_add(da, s * 32), desc_add(db, s * 2048), id, s > 0);
+            mma_commit(&bars[3]);
+            w_last = n;
+        }
+        if (ok) ok = mbar_wait(&bars[3], ph, err, 4);
+        __syncwarp();
+        fence_after_sync();
+        if (tid == kLoader && ok && has_next) {  // the K and V tiles are free
+            load_kv(nxt);
+            ++nkv;
+        }
+        // Epilogue: row rr of W (lanes 0-63) or Ut (lanes 64-127), 64 columns per warp,
+        // into the dead T (W) and A (Ut) regions as 128B-swizzled K-major tiles.
+        {
+            const int rr = 32 * (sub & 1) + lane;
+            const bool isw = sub < 2;
+            unsigned char* dst = sm + (isw ? P_WS : P_US) + half * 8192;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * sub) << 16) + (isw ? 0 : 128) + 64 * half;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
                 uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * sub) << 16) + cb, v);
+                tmem_ld32(taddr + 32 * g, v);
                 tmem_wait_ld(v);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t pk[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = cb + 8 * q + 2 * e;
-                        const float m0 = (i <= rr) ? exp2f(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
-                        const float m1 =
-                            (i + 1 <= rr) ? exp2f(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f;
-                        pk[e] = pack_bf16(m0, m1);
-                    }
-                    *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    for (int e = 0; e < 4; ++e)
+                        pk[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]), __uint_as_float(v[8 * q + 2 * e + 1]));
+                    *(uint4*)(dst + sw128_off(rr, 32 * g + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-        tma_store_2d(&tm_M, sm + P_M, 0, row0);
-        bulk_commit();
-    }
-    solve_unit_lower_64(Af, Tf, (float*)(sm + P_X));  // ends with __syncthreads
-    // B operands of W / Ut: T1 = T diag(beta gamma), T2 = T diag(beta), bf16 K-major
-    // [r][i], zero above the diagonal; T itself to global memory when asked for.
-    {
-        const int r = tid >> 2, i0 = (tid & 3) * 16;
-        const float* trow = Tf + r * kAS + i0;
-        uint32_t p0[8], p1[8], p2[8];
-#pragma unroll
-        for (int e4 = 0; e4 < 16; e4 += 4) {
-            const float4 t4 = *(const float4*)(trow + e4);
-            float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (i0 + e4 + e > r) tv[e] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                const int i = i0 + e4 + e;
-                const float b0 = bs[i], b1 = bs[i + 1];
-                p0[(e4 + e) >> 1] = pack_bf16(tv[e], tv[e + 1]);
-                p1[(e4 + e) >> 1] = pack_bf16(tv[e] * b0 * gs[i], tv[e + 1] * b1 * gs[i + 1]);
-                p2[(e4 + e) >> 1] = pack_bf16(tv[e] * b0, tv[e + 1] * b1);
-            }
-        }
-        if (Tout) {
-            uint4* tg = (uint4*)(Tout + ((int64_t)row0 + r) * kC + i0);
-            tg[0] = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            tg[1] = make_uint4(p0[4], p0[5], p0[6], p0[7]);
-        }
-        *(uint4*)(sm + P_T1 + sw128_off(r, i0)) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-        *(uint4*)(sm + P_T1 + sw128_off(r, i0 + 8)) = make_uint4(p1[4], p1[5], p1[6], p1[7]);
-        *(uint4*)(sm + P_T2 + sw128_off(r, i0)) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
-        *(uint4*)(sm + P_T2 + sw128_off(r, i0 + 8)) = make_uint4(p2[4], p2[5], p2[6], p2[7]);
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    if (tid == 0 && ok) {
-        // [T1; T2] [K | V] (M=128, N=256, K over tokens): rows 0-63 of columns 0-127
-        // are W = T1 K, rows 64-127 of columns 128-255 are Ut = T2 V.
-        const uint32_t id = idesc_bf16(128, 256, false, true);
-        const uint64_t da = sdesc(smem_u32(sm + P_T1), 16, 1024, SW_128B);
-        const uint64_t db = sdesc(smem_u32(sm + P_K0), 16384, 1024, SW_128B);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) mma_bf16_ss(tmem, desc_add(da, s * 32), desc_add(db, s * 2048), id, s > 0);
-        mma_commit(&bars[1]);
-    }
-    if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
-    __syncwarp();
-    fence_after_sync();
-    // Epilogue: row rr of W (lanes 0-63) or Ut (lanes 64-127), 64 columns per warp,
-    // into the dead Q (W) and K (Ut) slots as 128B-swizzled K-major tiles.
-    {
-        const int rr = 32 * (sub & 1) + lane;
-        const bool isw = sub < 2;
-        unsigned char* dst = sm + (isw ? (half ? P_Q1 : P_Q0) : (half ? P_K1 : P_K0));
-        const uint32_t taddr = tmem + ((uint32_t)(32 * sub) << 16) + (isw ? 0 : 128) + 64 * half;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            uint32_t v[32];
-            tmem_ld32(taddr + 32 * g, v);
-            tmem_wait_ld(v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    pk[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]), __uint_as_float(v[8 * q + 2 * e + 1]));
-                *(uint4*)(dst + sw128_off(rr, 32 * g + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-        }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        if (ok) {
-            tma_store_2d(&tm_W, sm + P_Q0, 0, row0);
-            tma_store_2d(&tm_W, sm + P_Q1, 64, row0);
-            tma_store_2d(&tm_U, sm + P_K0, 0, row0);
-            tma_store_2d(&tm_U, sm + P_K1, 64, row0);
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        if (tid == 0 && ok) {
+            tma_store_2d(&tm_W, sm + P_WS, 0, row0);
+            tma_store_2d(&tm_W, sm + P_WS + 8192, 64, row0);
+            tma_store_2d(&tm_U, sm + P_US, 0, row0);
+            tma_store_2d(&tm_U, sm + P_US + 8192, 64, row0);
             bulk_commit();
         }
-        bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
+        if (!ok) break;
     }
+    if (!ok) {  // bounded waits for what is still in flight before the CTA leaves
+        if (tid == kLoader) {
+            for (int i = n; i < nq; ++i) mbar_wait(&bars[0], i & 1, nullptr, 0);
+            for (int i = n; i < nkv; ++i) mbar_wait(&bars[1], i & 1, nullptr, 0);
+        }
+        if (tid == 0) {
+            if (g_last == n) mbar_wait(&bars[2], n & 1, nullptr, 0);
+            if (w_last == n) mbar_wait(&bars[3], n & 1, nullptr, 0);
+        }
+    }
+    if (tid == 0) bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     __syncwarp();
+    fence_before_sync();
+    __syncthreads();
     fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
@@ -930,7 +995,8 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prep_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid(d.NC, d.H, d.B);
+    const int64_t nchunks = d.NS() * d.NC;
+    dim3 grid((unsigned)std::min<int64_t>(nchunks, 2 * sm_count()));
     prep_fwd_tc<<<grid, 256, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
                                               tb.G, tb.T, tb.err);
     return cudaGetLastError();
