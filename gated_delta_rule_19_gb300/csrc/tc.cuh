@@ -19,6 +19,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 2^x by the PTX instruction ex2.approx.ftz.f32: a hardware approximation (relative
+// error about 2^-22 per the PTX ISA) that flushes subnormal results to zero.  For
+// the decay factors exp2(G_r - G_i) <= 1 of the chunk matrices, where a factor
+// below 2^-126 is negligible.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

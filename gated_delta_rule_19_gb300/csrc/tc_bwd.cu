@@ -1122,7 +1122,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int bc = cb + c0 + j;
-                const float gam = (bc < r) ? expf(Ga - Gs[bc]) : 0.f;
+                const float gam = (bc < r) ? __expf(Ga - Gs[bc]) : 0.f;
                 const float m = gam * da[j];
                 b3 += m * kk[j];
                 ev[j] = ba * m;

@@ -342,7 +342,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i = cb + 4 * q + e;
-                            f[e] = (i < rr) ? br * exp2f(G2r - G2s[i]) * __uint_as_float(v[4 * q + e]) : 0.f;
+                            f[e] = (i < rr) ? br * fast_exp2(G2r - G2s[i]) * __uint_as_float(v[4 * q + e]) : 0.f;
                         }
                         *(float4*)(arow + 4 * q) = make_float4(f[0], f[1], f[2], f[3]);
                     }
@@ -359,9 +359,9 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i = cb + 8 * q + 2 * e;
-                            const float m0 = (i <= rr) ? exp2f(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
+                            const float m0 = (i <= rr) ? fast_exp2(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
                             const float m1 =
-                                (i + 1 <= rr) ? exp2f(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f;
+                                (i + 1 <= rr) ? fast_exp2(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f;
                             pk[e] = pack_bf16(m0, m1);
                         }
                         *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
