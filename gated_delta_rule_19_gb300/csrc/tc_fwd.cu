@@ -200,8 +200,9 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     float* G2s = (float*)(sm + P_VEC);  // within-chunk cumsum of log2(alpha)
     float* gs = G2s + 64;               // gamma = alpha_1 ... alpha_r
     float* bs = gs + 64;
-    uint64_t* bars = (uint64_t*)(sm + P_BAR);  // [0] Q loads, [1] K, V loads, [2] Gram MMA, [3] W / Ut MMA
-    uint32_t* tslot = (uint32_t*)(sm + P_BAR + 32);
+    // [0] Q loads, [1] K loads, [2] Gram MMA, [3] W / Ut MMA, [4] V loads
+    uint64_t* bars = (uint64_t*)(sm + P_BAR);
+    uint32_t* tslot = (uint32_t*)(sm + P_BAR + 40);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = warp & 3, half = warp >> 2;
@@ -221,14 +222,14 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_arrive_expect_tx(&bars[0], 2 * 8192);
         for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_Q0 + j * 16384, &tm_q, &bars[0], 64 * j, h, t0, b);
     };
+    // K first: the next Gram MMA waits for it, V only for the W / Ut MMA
     auto load_kv = [&](int64_t ch) {
         int b, h, t0;
         decode(ch, b, h, t0);
-        mbar_arrive_expect_tx(&bars[1], 4 * 8192);
-        for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + P_K0 + j * 16384, &tm_k, &bars[1], 64 * j, h, t0, b);
-            tma_load_4d(sm + P_V0 + j * 16384, &tm_v, &bars[1], 64 * j, h, t0, b);
-        }
+        mbar_arrive_expect_tx(&bars[1], 2 * 8192);
+        for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_K0 + j * 16384, &tm_k, &bars[1], 64 * j, h, t0, b);
+        mbar_arrive_expect_tx(&bars[4], 2 * 8192);
+        for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_V0 + j * 16384, &tm_v, &bars[4], 64 * j, h, t0, b);
     };
     // warp 2: gates of tokens 2 lane, 2 lane + 1 of a chunk; padding (alpha = 1,
     // beta = 0) leaves the state unchanged
@@ -251,7 +252,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     const int64_t first = blockIdx.x;
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         if (first < nchunks) {
             load_q(first);
@@ -417,6 +418,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
+        if (tid == 0) ok = mbar_wait(&bars[4], ph, err, 1) && ok;
         if (tid == 0 && ok) {
             // [T1; T2] [K | V] (M=128, N=256, K over tokens): rows 0-63 of columns 0-127
             // are W = T1 K, rows 64-127 of columns 128-255 are Ut = T2 V.
@@ -473,7 +475,10 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (!ok) {  // bounded waits for what is still in flight before the CTA leaves
         if (tid == kLoader) {
             for (int i = n; i < nq; ++i) mbar_wait(&bars[0], i & 1, nullptr, 0);
-            for (int i = n; i < nkv; ++i) mbar_wait(&bars[1], i & 1, nullptr, 0);
+            for (int i = n; i < nkv; ++i) {
+                mbar_wait(&bars[1], i & 1, nullptr, 0);
+                mbar_wait(&bars[4], i & 1, nullptr, 0);
+            }
         }
         if (tid == 0) {
             if (g_last == n) mbar_wait(&bars[2], n & 1, nullptr, 0);
