@@ -300,7 +300,7 @@ gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
         Carver sv{(char*)saved};
         carve_tc_saved(d, sv, &states, &tb);
     }
-    cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
+    cudaError_t e = cudaMemsetAsync(tb.err, 0, gdn::kErrWords * sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
     e = timed(gdn::KID_PREP_TC, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
@@ -359,7 +359,7 @@ gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
     SplitBufs sb{};
     if (split) carve_split(d, *sp, cv, &sb);
     const int npieces = split ? sp->nseq * sp->P : 0;
-    cudaError_t e = cudaMemsetAsync(tb.err, 0, sizeof(int), cs);
+    cudaError_t e = cudaMemsetAsync(tb.err, 0, gdn::kErrWords * sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
     if (split) {
         e = timed(gdn::KID_SPLIT_COMBINE, cs, [&] {

@@ -175,6 +175,10 @@ cudaError_t launch_combine_bwd(int S, int P, int H, const float* dsT, const floa
 // tensors to and from the padded [S, T, H, width] layout.  `merge` (optional) is
 // ORed into `err` once.
 constexpr int kVarlenBadOffsets = 1 << 30;  // error-word bit: invalid cu_seqlens
+// Work counters of the persistent kernels, in the error-flag area of the workspace
+// (64 ints, the first 32 reset at the start of every call): chunks handed out
+// beyond each CTA's first one.
+constexpr int kSchedPrep = 16, kSchedQk = 17, kSchedWy = 18, kErrWords = 32;
 cudaError_t launch_varlen_rows(const Dims& d, int64_t total, const int32_t* cu, int width_bytes, const void* src,
                                void* dst, uint32_t fill, bool scatter, int* err, const int* merge, cudaStream_t st);
 cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu, int elem_bytes, const void* src,

@@ -896,8 +896,9 @@ constexpr int T1 = 73728, T2 = 81920, DT = 90112, Y = 98304;  // [64 x 64]
 constexpr int E = DT;      // dT is dead once Y is formed
 constexpr int ID = Y;      // identity [64 x 64], written once Y has been read
 constexpr int KP = V;      // dK partial [128 x 64], loaded once V has been read
-constexpr int DV = DU;     // outputs [64 x 128] into dead input slots
-constexpr int DK = K;
+constexpr int DV = DU;     // outputs [64 x 128] into dead slots
+constexpr int DK = DT;     // dT / E and Y / ID: dead once phase 4's MMA is done, not
+                           // rewritten before the next chunk's first MMA completes
 constexpr int VEC = Y + 8192;  // per-token and partial-sum vectors
 constexpr int NVEC = 15 * 64;
 constexpr int BAR = VEC + NVEC * 4;
@@ -905,13 +906,19 @@ constexpr size_t SMEM = BAR + 64 + 1024;
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 // the M=128 operands whose rows 0-63 are not used read the 8 KB before their tile
 static_assert(T1 - 8192 == T && T2 - 8192 == T1 && E - 8192 == T2 && ID - 8192 == DT, "tile order");
+static_assert(DK + 16384 == VEC, "the dK tile spans the dT and Y tiles");
 }  // namespace wy
 
-// One CTA per chunk, 256 threads, two CTAs per SM (each one's epilogues overlap
-// the other's MMAs and loads).  Warps w and w+4 reach TMEM lanes 32*(w%4) and
-// split columns.  Rows of the 64 x 64 products land in lanes 0-63 (threads with
-// warp % 4 < 2); dV and dK are formed with tokens on lanes 64-127 and 128
-// columns, so the other half of the threads writes them as whole rows.
+// Persistent, two CTAs per SM (each one's epilogues overlap the other's MMAs and
+// loads), 256 threads: CTA i starts with chunk i and takes further chunks from a
+// work counter (lane 0 of warp 3 claims each one a chunk ahead), so that faster SMs
+// take more chunks.  Warps w and w+4
+// reach TMEM lanes 32*(w%4) and split columns.  Rows of the 64 x 64 products land
+// in lanes 0-63 (threads with warp % 4 < 2); dV and dK are formed with tokens on
+// lanes 64-127 and 128 columns, so the other half of the threads writes them as
+// whole rows.  dK is staged in the dT and Y tiles, so every input slot is free once
+// phase 4's MMA is done: the next chunk's tiles are requested then, and warp 3
+// reads the next chunk's per-token values into registers a chunk ahead.
 __global__ void __launch_bounds__(256, 2)
 grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_dWt, const __grid_constant__ CUtensorMap tm_dU,
@@ -934,6 +941,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     float* cE2 = vec + 832;     // [2][64]
     uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0] loads, [1] MMA, [2] dK partial
     uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 32);
+    int* s_next = (int*)(sm + wy::BAR + 40);  // the chunk after this one
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = warp & 3, half = warp >> 2;
@@ -941,16 +949,18 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const bool urow = sub < 2;
     const int r = urow ? lanerow : lanerow - 64;  // row of the 64-row results (both sides)
     const int cb = half * 32;                     // this warp's 32 columns of a 64-column result
-    const int64_t ch = blockIdx.x;
-    const int c = (int)(ch % d.NC);
-    const int h = (int)((ch / d.NC) % d.H);
-    const int b = (int)(ch / d.NC / d.H);
-    const int t0 = c * kC;
-    const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
+    const int64_t nchunks = d.NS() * d.NC;
 
-    if (tid == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
+    // chunk index = (b * H + h) * NC + c
+    auto decode = [&](int64_t ch, int& b, int& h, int& t0) {
+        t0 = (int)(ch % d.NC) * kC;
+        h = (int)((ch / d.NC) % d.H);
+        b = (int)(ch / d.NC / d.H);
+    };
+    auto load_inputs = [&](int64_t ch) {
+        int b, h, t0;
+        decode(ch, b, h, t0);
+        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
         mbar_arrive_expect_tx(&bars[0], 9 * 8192);
         for (int j = 0; j < 2; ++j) {
             tma_load_4d(sm + wy::K + j * 8192, &tm_k, &bars[0], 64 * j, h, t0, b);
@@ -959,30 +969,44 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             tma_load_2d(sm + wy::DWT + j * 8192, &tm_dWt, &bars[0], 0, krow0 + 64 * j);
         }
         tma_load_2d(sm + wy::T, &tm_T, &bars[0], 0, row0);
+    };
+    // warp 3: G, the dG partial and the gates of tokens 2 lane, 2 lane + 1 of a chunk
+    // (padding: alpha = 1, beta = 0), held in registers until the chunk starts
+    float2 gv = make_float2(0.f, 0.f), qv = gv;
+    bf16 ga[2], gb[2];
+    auto load_vec = [&](int64_t ch) {
+        int b, h, t0;
+        decode(ch, b, h, t0);
+        const int64_t row0 = ch * kC;
+        gv = *(const float2*)(G + row0 + 2 * lane);
+        qv = *(const float2*)(dGp + row0 + 2 * lane);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = t0 + 2 * lane + e;
+            ga[e] = __float2bfloat16_rn(1.f);
+            gb[e] = __float2bfloat16_rn(0.f);
+            if (t < d.T) {
+                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
+                ga[e] = alpha[gi];
+                gb[e] = beta[gi];
+            }
+        }
+    };
+
+    const int64_t first = blockIdx.x;
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        if (first < nchunks) load_inputs(first);
     }
     if (warp == 1) {
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
-    if (warp == 3) {
-        const float2 gv = *(const float2*)(G + (int64_t)row0 + 2 * lane);
-        const float2 qv = *(const float2*)(dGp + (int64_t)row0 + 2 * lane);
-        const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int p = 2 * lane + e, t = t0 + p;
-            float a = 1.f, be = 0.f;  // padding: alpha = 1, beta = 0
-            if (t < d.T) {
-                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-                a = __bfloat162float(alpha[gi]);
-                be = __bfloat162float(beta[gi]);
-            }
-            Gs[p] = g2[e];
-            gs[p] = expf(g2[e]);
-            bs[p] = be;
-            as_[p] = a;
-            dGq[p] = q2[e];
-        }
+    int claimed = 0;  // lane 0 of warp 3: the next chunk, claimed a chunk ahead
+    if (warp == 3 && first < nchunks) {
+        load_vec(first);
+        if (lane == 0) claimed = (int)gridDim.x + atomicAdd(err + kSchedWy, 1);
     }
     fence_before_sync();
     __syncthreads();
@@ -999,249 +1023,308 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const uint32_t sY = smem_u32(sm + wy::Y), sE = smem_u32(sm + wy::E), sID = smem_u32(sm + wy::ID);
     const uint32_t sKP = smem_u32(sm + wy::KP);
 
-    bool ok = mbar_wait(&bars[0], 0, err, 1);
-    // ---- phase 1: Qm = dW K^T (K over k), P = dU V^T (K over v), KK = K K^T   (M=128: rows 64-127 unused)
-    if (tid == 0 && ok) {
-        const uint32_t idq = idesc_bf16(128, 64, true, false);
-        const uint32_t id = idesc_bf16(128, 64, false, false);
-        const uint64_t ddw = sdesc(sDWT, 16384, 1024, SW_128B);
-        const uint64_t dk = sdesc(sK, 16, 1024, SW_128B), du = sdesc(sDU, 16, 1024, SW_128B);
-        const uint64_t dv = sdesc(sV, 16, 1024, SW_128B);
-#pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
-            const uint32_t o = (s2 >> 2) * 8192 + (s2 & 3) * 32;
-            mma_bf16_ss(tQm, desc_add(ddw, s2 * 2048), desc_add(dk, o), idq, s2 > 0);
-            mma_bf16_ss(tP, desc_add(du, o), desc_add(dv, o), id, s2 > 0);
-            mma_bf16_ss(tKK, desc_add(dk, o), desc_add(dk, o), id, s2 > 0);
-        }
-        mma_commit(&bars[1]);
-    }
-    if (!urow) {
-        // T1 = T diag(beta gamma), T2 = T diag(beta): rows r, this half of the columns
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float f[8], f1[8], f2[8];
-            tile_get8(sm + wy::T, 64, r, cb + 8 * q, f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int cc = cb + 8 * q + j;
-                f2[j] = f[j] * bs[cc];
-                f1[j] = f2[j] * gs[cc];
+
+    bool ok = true;
+    int n = 0;
+    // thread 0, this chunk: bit 0 the next chunk's inputs requested, bit 1 the dK
+    // partial requested, bits 2+ MMA commits
+    int trk = 0;
+    int64_t nxt = first;
+#pragma unroll 1
+    for (int64_t ch = first; ch < nchunks; ch = nxt, ++n) {
+        const int ph = n & 1;
+        int b, h, t0;
+        decode(ch, b, h, t0);
+        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
+        trk = 0;
+        if (warp == 3) {
+            const int nx = __shfl_sync(0xffffffffu, claimed, 0);
+            if (lane == 0) {
+                *s_next = nx;
+                if (nx < nchunks) claimed = (int)gridDim.x + atomicAdd(err + kSchedWy, 1);
             }
-            *(uint4*)(sm + wy::T1 + tile_off(64, r, cb + 8 * q)) = pack8(f1);
-            *(uint4*)(sm + wy::T2 + tile_off(64, r, cb + 8 * q)) = pack8(f2);
-        }
-    }
-    ok = mbar_wait(&bars[1], 0, err, 2) && ok;
-    __syncwarp();
-    fence_after_sync();
-    // V is dead: bring in the dK partial of the first gradient kernel for phase 4
-    if (tid == 0 && ok) {
-        mbar_arrive_expect_tx(&bars[2], 2 * 8192);
-        for (int j = 0; j < 2; ++j) tma_load_2d(sm + wy::KP + j * 8192, &tm_dKp, &bars[2], 0, krow0 + 64 * j);
-    }
-    if (urow) {
-        // rows s = r: column sums of T (P + Qm diag(gamma)) and T Qm over this warp's 32
-        // rows; dT (strictly lower) for the Y product
+            const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y};
 #pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-            float qm[16], p[16], t8a[8], t8b[8], dt[16], c1[16], c2[16];
-            tmem_load16f2(tQm + lanebase + cb + c0, tP + lanebase + cb + c0, qm, p);
-            tile_get8(sm + wy::T, 64, r, cb + c0, t8a);
-            tile_get8(sm + wy::T, 64, r, cb + c0 + 8, t8b);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int rc = cb + c0 + j;
-                const float tsr = j < 8 ? t8a[j] : t8b[j - 8];
-                const float pv = p[j] + gs[rc] * qm[j];
-                c1[j] = tsr * pv;
-                c2[j] = tsr * qm[j];
-                dt[j] = (rc < r) ? bs[rc] * pv : 0.f;
+            for (int e = 0; e < 2; ++e) {
+                const int p = 2 * lane + e;
+                Gs[p] = g2[e];
+                gs[p] = expf(g2[e]);
+                bs[p] = __bfloat162float(gb[e]);
+                as_[p] = __bfloat162float(ga[e]);
+                dGq[p] = q2[e];
             }
-            tile_put16(sm + wy::DT, 64, r, cb + c0, dt);
-            const float s1 = warp_colsum16(c1), s2 = warp_colsum16(c2);
-            if (lane < 16) {
-                cB12[sub * 64 + cb + c0 + lane] = s1;
-                cGw[sub * 64 + cb + c0 + lane] = s2;
-            }
+            if (nx < nchunks) load_vec(nx);  // used next iteration
         }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    // ---- phase 2: Y = dT T^T  (M=128, K over tokens); then dV = T2^T dU (N=128,
-    // tokens on rows 64-127: T2 and dU are ready and Qm / P, whose columns it
-    // takes, were read before the barrier), which runs during the Y epilogue
-    // and is covered by phase 3's commit
-    if (tid == 0 && ok) {
-        const uint32_t id = idesc_bf16(128, 64, false, false);
-        const uint64_t ddt = sdesc(sDT, 16, 1024, SW_128B), dt = sdesc(sT, 16, 1024, SW_128B);
+        __syncthreads();  // per-token values and the next chunk's index visible
+        fence_after_sync();
+        nxt = *s_next;
+        const bool has_next = nxt < nchunks;
+        ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+        // ---- phase 1: Qm = dW K^T (K over k), P = dU V^T (K over v), KK = K K^T   (M=128: rows 64-127 unused)
+        if (tid == 0 && ok) {
+            const uint32_t idq = idesc_bf16(128, 64, true, false);
+            const uint32_t id = idesc_bf16(128, 64, false, false);
+            const uint64_t ddw = sdesc(sDWT, 16384, 1024, SW_128B);
+            const uint64_t dk = sdesc(sK, 16, 1024, SW_128B), du = sdesc(sDU, 16, 1024, SW_128B);
+            const uint64_t dv = sdesc(sV, 16, 1024, SW_128B);
 #pragma unroll
-        for (int s2 = 0; s2 < 4; ++s2) mma_bf16_ss(tY, desc_add(ddt, s2 * 32), desc_add(dt, s2 * 32), id, s2 > 0);
-        mma_commit(&bars[1]);
-        const uint32_t idv = idesc_bf16(128, 128, true, true);
-        const uint64_t dt2m = sdesc(sT2 - 8192, 8192, 1024, SW_128B), dum = sdesc(sDU, 8192, 1024, SW_128B);
-#pragma unroll
-        for (int s2 = 0; s2 < 4; ++s2)
-            mma_bf16_ss(tDV, desc_add(dt2m, s2 * 2048), desc_add(dum, s2 * 2048), idv, s2 > 0);
-    }
-    if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
-    __syncwarp();
-    fence_after_sync();
-    if (urow) {
-        float y[16], y2[16];
-        tmem_load16f2(tY + lanebase + cb, tY + lanebase + cb + 16, y, y2);
-        tile_put16(sm + wy::Y, 64, r, cb, y);
-        tile_put16(sm + wy::Y, 64, r, cb + 16, y2);
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    // ---- phase 3: dA = -T^T Y (N=64, rows 0-63); its commit also covers dV
-    if (tid == 0 && ok) {
-        const uint32_t ida = idesc_bf16(128, 64, true, true, true);
-        const uint64_t dtm = sdesc(sT, 8192, 1024, SW_128B), dym = sdesc(sY, 8192, 1024, SW_128B);
-#pragma unroll
-        for (int s2 = 0; s2 < 4; ++s2)
-            mma_bf16_ss(tDA, desc_add(dtm, s2 * 2048), desc_add(dym, s2 * 2048), ida, s2 > 0);
-        mma_commit(&bars[1]);
-    }
-    if (ok) ok = mbar_wait(&bars[1], 0, err, 8);
-    __syncwarp();
-    fence_after_sync();
-    if (urow) {
-        // rows a = r: dbeta3, E = beta_a Gam .* dA (strictly lower) -> E tile, E2 = E .* KK
-        const float Ga = Gs[r], ba = bs[r];
-        float b3 = 0.f, re2 = 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-            float da[16], kk[16], ev[16], e2[16];
-            tmem_load16f2(tDA + lanebase + cb + c0, tKK + lanebase + cb + c0, da, kk);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int bc = cb + c0 + j;
-                const float gam = (bc < r) ? __expf(Ga - Gs[bc]) : 0.f;
-                const float m = gam * da[j];
-                b3 += m * kk[j];
-                ev[j] = ba * m;
-                e2[j] = ev[j] * kk[j];
-                re2 += e2[j];
+            for (int s2 = 0; s2 < 8; ++s2) {
+                const uint32_t o = (s2 >> 2) * 8192 + (s2 & 3) * 32;
+                mma_bf16_ss(tQm, desc_add(ddw, s2 * 2048), desc_add(dk, o), idq, s2 > 0);
+                mma_bf16_ss(tP, desc_add(du, o), desc_add(dv, o), id, s2 > 0);
+                mma_bf16_ss(tKK, desc_add(dk, o), desc_add(dk, o), id, s2 > 0);
             }
-            tile_put16(sm + wy::E, 64, r, cb + c0, ev);
-            const float s3 = warp_colsum16(e2);
-            if (lane < 16) cE2[sub * 64 + cb + c0 + lane] = s3;
-        }
-        dB3p[half * 64 + r] = b3;
-        rE2p[half * 64 + r] = re2;
-        // the identity for adding the dK partial by an MMA (Y is dead)
-        if (half == 0) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = (8 * q + j == r) ? 1.f : 0.f;
-                *(uint4*)(sm + wy::ID + sw128_off(r, 8 * q)) = pack8(f);
-            }
-        }
-    } else {
-        // dV row a = r (token), columns 64*half .. +64 -> dv tile (dU is dead)
-        unsigned char* dvt = sm + wy::DV + half * 8192;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            float x[32];
-            tmem_cols<32>(tDV + lanebase + 64 * half + 32 * g, x);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) *(uint4*)(dvt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
-        }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    // ---- phase 4: dK = T1^T dW + E K + E^T K + dK_partial (N=128, tokens on rows 64-127)
-    if (tid == 0 && ok) {
-        for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
-        bulk_commit();
-        ok = mbar_wait(&bars[2], 0, err, 16);
-        if (ok) {
-            const uint32_t id_mk = idesc_bf16(128, 128, true, false);   // A MN-major, B K-major
-            const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
-            const uint32_t id_mm = idesc_bf16(128, 128, true, true);
-            const uint32_t id_kk = idesc_bf16(128, 128, false, false);
-            const uint64_t dt1m = sdesc(sT1 - 8192, 8192, 1024, SW_128B), ddw = sdesc(sDWT, 16, 1024, SW_128B);
-            const uint64_t dek = sdesc(sE - 8192, 16, 1024, SW_128B), dem = sdesc(sE - 8192, 8192, 1024, SW_128B);
-            const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
-            const uint64_t did = sdesc(sID - 8192, 16, 1024, SW_128B), dkp = sdesc(sKP, 16, 1024, SW_128B);
-#pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                mma_bf16_ss(tDK, desc_add(dt1m, s2 * 2048), desc_add(ddw, s2 * 32), id_mk, s2 > 0);
-                mma_bf16_ss(tDK, desc_add(dek, s2 * 32), desc_add(dkm, s2 * 2048), id_km, 1u);
-                mma_bf16_ss(tDK, desc_add(dem, s2 * 2048), desc_add(dkm, s2 * 2048), id_mm, 1u);
-                mma_bf16_ss(tDK, desc_add(did, s2 * 32), desc_add(dkp, s2 * 32), id_kk, 1u);
-            }
+            // the previous chunk's dK store has read the dT / Y tiles before anyone
+            // sees this commit (dT is written after it)
+            bulk_wait_read0();
             mma_commit(&bars[1]);
+            trk += 4;
         }
-    }
-    if (warp == 1) {
-        // dG, dlog alpha = reverse within-chunk cumsum (lane l holds positions 63-2l and
-        // 62-2l), dalpha = dlog alpha / alpha, dbeta = dbeta12 + dbeta3
-        auto dg = [&](int p) {
-            return dGq[p] + bs[p] * gs[p] * (cGw[p] + cGw[64 + p]) + (rE2p[p] + rE2p[64 + p]) -
-                   (cE2[p] + cE2[64 + p]);
-        };
-        const int p1 = 63 - 2 * lane, p0 = 62 - 2 * lane;
-        const float g1 = dg(p1), g0 = dg(p0);
-        const float pair = g1 + g0;
-        float incl = pair;
+        if (!urow) {
+            // T1 = T diag(beta gamma), T2 = T diag(beta): rows r, this half of the columns
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        const float run1 = incl - pair + g1, run0 = run1 + g0;
-        const int pos[2] = {p1, p0};
-        const float run[2] = {run1, run0};
+            for (int q = 0; q < 4; ++q) {
+                float f[8], f1[8], f2[8];
+                tile_get8(sm + wy::T, 64, r, cb + 8 * q, f);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int t = t0 + pos[e];
-            if (t < d.T) {
-                const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
-                const int p = pos[e];
-                dalpha[gi] = __float2bfloat16_rn(run[e] / as_[p]);
-                dbeta[gi] = __float2bfloat16_rn(cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p]);
+                for (int j = 0; j < 8; ++j) {
+                    const int cc = cb + 8 * q + j;
+                    f2[j] = f[j] * bs[cc];
+                    f1[j] = f2[j] * gs[cc];
+                }
+                *(uint4*)(sm + wy::T1 + tile_off(64, r, cb + 8 * q)) = pack8(f1);
+                *(uint4*)(sm + wy::T2 + tile_off(64, r, cb + 8 * q)) = pack8(f2);
             }
         }
-    }
-    ok = __syncthreads_and(ok);  // the issuer's load wait is every thread's
-    if (ok) ok = mbar_wait(&bars[1], 1, err, 16);
-    __syncwarp();
-    fence_after_sync();
-    if (!urow) {
-        // dK row a = r (token), columns 64*half .. +64 -> dk tile (K is dead)
-        unsigned char* dkt = sm + wy::DK + half * 8192;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            float x[32];
-            tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) *(uint4*)(dkt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
+        ok = mbar_wait(&bars[1], 0, err, 2) && ok;
+        __syncwarp();
+        fence_after_sync();
+        // V is dead: bring in the dK partial of the first gradient kernel for phase 4
+        if (tid == 0 && ok) {
+            mbar_arrive_expect_tx(&bars[2], 2 * 8192);
+            for (int j = 0; j < 2; ++j) tma_load_2d(sm + wy::KP + j * 8192, &tm_dKp, &bars[2], 0, krow0 + 64 * j);
+            trk |= 2;
         }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(ok);
-    fence_after_sync();
-    if (tid == 0) {
-        if (ok) {
+        if (urow) {
+            // rows s = r: column sums of T (P + Qm diag(gamma)) and T Qm over this warp's 32
+            // rows; dT (strictly lower) for the Y product
+#pragma unroll
+            for (int c0 = 0; c0 < 32; c0 += 16) {
+                float qm[16], p[16], t8a[8], t8b[8], dt[16], c1[16], c2[16];
+                tmem_load16f2(tQm + lanebase + cb + c0, tP + lanebase + cb + c0, qm, p);
+                tile_get8(sm + wy::T, 64, r, cb + c0, t8a);
+                tile_get8(sm + wy::T, 64, r, cb + c0 + 8, t8b);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int rc = cb + c0 + j;
+                    const float tsr = j < 8 ? t8a[j] : t8b[j - 8];
+                    const float pv = p[j] + gs[rc] * qm[j];
+                    c1[j] = tsr * pv;
+                    c2[j] = tsr * qm[j];
+                    dt[j] = (rc < r) ? bs[rc] * pv : 0.f;
+                }
+                tile_put16(sm + wy::DT, 64, r, cb + c0, dt);
+                const float s1 = warp_colsum16(c1), s2 = warp_colsum16(c2);
+                if (lane < 16) {
+                    cB12[sub * 64 + cb + c0 + lane] = s1;
+                    cGw[sub * 64 + cb + c0 + lane] = s2;
+                }
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        // ---- phase 2: Y = dT T^T  (M=128, K over tokens); then dV = T2^T dU (N=128,
+        // tokens on rows 64-127: T2 and dU are ready and Qm / P, whose columns it
+        // takes, were read before the barrier), which runs during the Y epilogue
+        // and is covered by phase 3's commit
+        if (tid == 0 && ok) {
+            const uint32_t id = idesc_bf16(128, 64, false, false);
+            const uint64_t ddt = sdesc(sDT, 16, 1024, SW_128B), dt = sdesc(sT, 16, 1024, SW_128B);
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) mma_bf16_ss(tY, desc_add(ddt, s2 * 32), desc_add(dt, s2 * 32), id, s2 > 0);
+            mma_commit(&bars[1]);
+            trk += 4;
+            const uint32_t idv = idesc_bf16(128, 128, true, true);
+            const uint64_t dt2m = sdesc(sT2 - 8192, 8192, 1024, SW_128B), dum = sdesc(sDU, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+                mma_bf16_ss(tDV, desc_add(dt2m, s2 * 2048), desc_add(dum, s2 * 2048), idv, s2 > 0);
+        }
+        if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
+        __syncwarp();
+        fence_after_sync();
+        if (urow) {
+            float y[16], y2[16];
+            tmem_load16f2(tY + lanebase + cb, tY + lanebase + cb + 16, y, y2);
+            tile_put16(sm + wy::Y, 64, r, cb, y);
+            tile_put16(sm + wy::Y, 64, r, cb + 16, y2);
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        // ---- phase 3: dA = -T^T Y (N=64, rows 0-63); its commit also covers dV
+        if (tid == 0 && ok) {
+            const uint32_t ida = idesc_bf16(128, 64, true, true, true);
+            const uint64_t dtm = sdesc(sT, 8192, 1024, SW_128B), dym = sdesc(sY, 8192, 1024, SW_128B);
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+                mma_bf16_ss(tDA, desc_add(dtm, s2 * 2048), desc_add(dym, s2 * 2048), ida, s2 > 0);
+            mma_commit(&bars[1]);
+            trk += 4;
+        }
+        if (ok) ok = mbar_wait(&bars[1], 0, err, 8);
+        __syncwarp();
+        fence_after_sync();
+        if (urow) {
+            // rows a = r: dbeta3, E = beta_a Gam .* dA (strictly lower) -> E tile, E2 = E .* KK
+            const float Ga = Gs[r], ba = bs[r];
+            float b3 = 0.f, re2 = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < 32; c0 += 16) {
+                float da[16], kk[16], ev[16], e2[16];
+                tmem_load16f2(tDA + lanebase + cb + c0, tKK + lanebase + cb + c0, da, kk);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int bc = cb + c0 + j;
+                    const float gam = (bc < r) ? __expf(Ga - Gs[bc]) : 0.f;
+                    const float m = gam * da[j];
+                    b3 += m * kk[j];
+                    ev[j] = ba * m;
+                    e2[j] = ev[j] * kk[j];
+                    re2 += e2[j];
+                }
+                tile_put16(sm + wy::E, 64, r, cb + c0, ev);
+                const float s3 = warp_colsum16(e2);
+                if (lane < 16) cE2[sub * 64 + cb + c0 + lane] = s3;
+            }
+            dB3p[half * 64 + r] = b3;
+            rE2p[half * 64 + r] = re2;
+            // the identity for adding the dK partial by an MMA (Y is dead)
+            if (half == 0) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float f[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = (8 * q + j == r) ? 1.f : 0.f;
+                    *(uint4*)(sm + wy::ID + sw128_off(r, 8 * q)) = pack8(f);
+                }
+            }
+        } else {
+            // dV row a = r (token), columns 64*half .. +64 -> dv tile (dU is dead)
+            unsigned char* dvt = sm + wy::DV + half * 8192;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                float x[32];
+                tmem_cols<32>(tDV + lanebase + 64 * half + 32 * g, x);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) *(uint4*)(dvt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        // ---- phase 4: dK = T1^T dW + E K + E^T K + dK_partial (N=128, tokens on rows 64-127)
+        if (tid == 0 && ok) {
+            for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
+            bulk_commit();
+            ok = mbar_wait(&bars[2], ph, err, 16);
+            if (ok) {
+                const uint32_t id_mk = idesc_bf16(128, 128, true, false);   // A MN-major, B K-major
+                const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
+                const uint32_t id_mm = idesc_bf16(128, 128, true, true);
+                const uint32_t id_kk = idesc_bf16(128, 128, false, false);
+                const uint64_t dt1m = sdesc(sT1 - 8192, 8192, 1024, SW_128B), ddw = sdesc(sDWT, 16, 1024, SW_128B);
+                const uint64_t dek = sdesc(sE - 8192, 16, 1024, SW_128B), dem = sdesc(sE - 8192, 8192, 1024, SW_128B);
+                const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
+                const uint64_t did = sdesc(sID - 8192, 16, 1024, SW_128B), dkp = sdesc(sKP, 16, 1024, SW_128B);
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2) {
+                    mma_bf16_ss(tDK, desc_add(dt1m, s2 * 2048), desc_add(ddw, s2 * 32), id_mk, s2 > 0);
+                    mma_bf16_ss(tDK, desc_add(dek, s2 * 32), desc_add(dkm, s2 * 2048), id_km, 1u);
+                    mma_bf16_ss(tDK, desc_add(dem, s2 * 2048), desc_add(dkm, s2 * 2048), id_mm, 1u);
+                    mma_bf16_ss(tDK, desc_add(did, s2 * 32), desc_add(dkp, s2 * 32), id_kk, 1u);
+                }
+                mma_commit(&bars[1]);
+                trk += 4;
+            }
+        }
+        if (warp == 1) {
+            // dG, dlog alpha = reverse within-chunk cumsum (lane l holds positions 63-2l and
+            // 62-2l), dalpha = dlog alpha / alpha, dbeta = dbeta12 + dbeta3
+            auto dg = [&](int p) {
+                return dGq[p] + bs[p] * gs[p] * (cGw[p] + cGw[64 + p]) + (rE2p[p] + rE2p[64 + p]) -
+                       (cE2[p] + cE2[64 + p]);
+            };
+            const int p1 = 63 - 2 * lane, p0 = 62 - 2 * lane;
+            const float g1 = dg(p1), g0 = dg(p0);
+            const float pair = g1 + g0;
+            float incl = pair;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const float run1 = incl - pair + g1, run0 = run1 + g0;
+            const int pos[2] = {p1, p0};
+            const float run[2] = {run1, run0};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = t0 + pos[e];
+                if (t < d.T) {
+                    const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
+                    const int p = pos[e];
+                    dalpha[gi] = __float2bfloat16_rn(run[e] / as_[p]);
+                    dbeta[gi] = __float2bfloat16_rn(cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p]);
+                }
+            }
+        }
+        ok = __syncthreads_and(ok);  // the issuer's load wait is every thread's
+        if (ok) ok = mbar_wait(&bars[1], 1, err, 16);
+        __syncwarp();
+        fence_after_sync();
+        // every input slot is free (the dV store has read the dU slot): the next chunk's
+        if (tid == 0 && ok && has_next) {
+            bulk_wait_read0();
+            load_inputs(nxt);
+            trk |= 1;
+        }
+        if (!urow) {
+            // dK row a = r (token), columns 64*half .. +64 -> dk tile (dT / E and Y / ID are dead)
+            unsigned char* dkt = sm + wy::DK + half * 8192;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                float x[32];
+                tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) *(uint4*)(dkt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
+            }
+        }
+        fence_proxy_async();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);
+        fence_after_sync();
+        if (tid == 0 && ok) {
             for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
         }
-        if (!ok) mbar_wait(&bars[2], 0, nullptr, 0);  // the dK partial load may still be in flight
+        if (!ok) break;
+    }
+    if (tid == 0) {
+        if (!ok) {  // bounded waits for the copies and MMAs still in flight
+            mbar_wait(&bars[0], n & 1, nullptr, 0);
+            if (trk & 1) mbar_wait(&bars[0], (n + 1) & 1, nullptr, 0);
+            if (trk & 2) mbar_wait(&bars[2], n & 1, nullptr, 0);
+            if (trk >= 4) mbar_wait(&bars[1], ((trk >> 2) - 1) & 1, nullptr, 0);  // 4 commits per chunk
+        }
         bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
     __syncwarp();
+    fence_before_sync();
+    __syncthreads();
     fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
@@ -1314,7 +1397,7 @@ cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(grad_wy_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wy::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(d.NS() * d.NC));
+    dim3 grid((unsigned)std::min<int64_t>(d.NS() * d.NC, 2 * sm_count()));
     grad_wy_tc<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp, (const bf16*)alpha,
                                             (const bf16*)beta, tb.G, bb.dGp, (bf16*)dalpha, (bf16*)dbeta, tb.err);
     return cudaGetLastError();
