@@ -502,7 +502,8 @@ constexpr int BAR = VEC + (12 * 64 + 512) * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
 }  // namespace qk
 
-// Persistent: CTA i handles chunks i, i + gridDim.x, ...  512 threads; warps w,
+// Persistent: CTA i starts with chunk i and takes further chunks from a work
+// counter, so that faster SMs take more chunks.  512 threads; warps w,
 // w+4, w+8 and w+12 split the columns of TMEM lanes 32*(w%4) ..  The next chunk's
 // tiles are requested as soon as their buffers are free (after phase 1, 2 and 3).
 __global__ void __launch_bounds__(512, 1)
@@ -526,6 +527,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // [0] loads A1, [1] loads B, [2..4] MMA phases, [5] loads A2, [6] S0^T [dO; dU]^T
     uint64_t* bars = (uint64_t*)(sm + qk::BAR);
     uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 56);
+    int* s_next = (int*)(sm + qk::BAR + 60);  // the chunk after this one
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // 16 warps: warp w reaches TMEM lanes 32*(w%4) ..; the four warps of a lane
@@ -581,7 +583,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int64_t first = blockIdx.x;
     // warp 3 keeps the next chunk's G (2 tokens per lane) in registers
     float2 gnext = make_float2(0.f, 0.f);
-    if (warp == 3 && first < nchunks) gnext = *(const float2*)(G + first * kC + 2 * lane);
+    int claimed = 0;  // lane 0 of warp 3: the next chunk, claimed from the work counter a chunk ahead
+    if (warp == 3 && first < nchunks) {
+        gnext = *(const float2*)(G + first * kC + 2 * lane);
+        if (lane == 0) claimed = (int)gridDim.x + atomicAdd(err + kSchedQk, 1);
+    }
     if (tid == kQkIssuer) {
         for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -609,19 +615,25 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     bool ok = true;
     int n = 0;
+    int64_t nxt = first;
 #pragma unroll 1
-    for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
+    for (int64_t ch = first; ch < nchunks; ch = nxt, ++n) {
         int b, h, c;
         decode(ch, b, h, c);
         const int t0 = c * kC;
         const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
         const int ph = n & 1;
         if (warp == 3) {
+            const int nx = __shfl_sync(0xffffffffu, claimed, 0);
+            if (lane == 0) {
+                *s_next = nx;
+                if (nx < nchunks) claimed = (int)gridDim.x + atomicAdd(err + kSchedQk, 1);
+            }
             Gs[2 * lane] = gnext.x;
             Gs[2 * lane + 1] = gnext.y;
             gs[2 * lane] = expf(gnext.x);
             gs[2 * lane + 1] = expf(gnext.y);
-            if (ch + gridDim.x < nchunks) gnext = *(const float2*)(G + (ch + gridDim.x) * kC + 2 * lane);
+            if (nx < nchunks) gnext = *(const float2*)(G + (int64_t)nx * kC + 2 * lane);
         }
         // rows of Ut (64 columns) and Mqk (32 columns) this thread needs, fetched early
         uint4 utv[4], mqv[2];
@@ -680,12 +692,14 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         ok = mbar_wait(&bars[2], ph, err, 2) && ok;
         if (tid == kQkIssuer) bulk_wait_read0();  // the previous chunk's stores from the U / EU tiles are done
-        __syncthreads();  // Gs / gs; every thread is past its reads of S0^T
+        __syncthreads();  // Gs / gs, the next chunk's index; every thread is past its reads of S0^T
         fence_after_sync();
+        nxt = *s_next;
+        const bool has_next = nxt < nchunks;
         // W, dU, S0^T are free once S0^T [dO; dU]^T is done: request the next chunk's
-        if (tid == 96 && ok && ch + gridDim.x < nchunks) {
+        if (tid == 96 && ok && has_next) {
             ok = mbar_wait(&bars[6], ph, err, 2);
-            if (ok) load_A1(ch + gridDim.x);
+            if (ok) load_A1(nxt);
         }
         const float GC = Gs[63], gC = gs[63];
         const float Gr = Gs[r], er = expf(GC - Gr);
@@ -748,7 +762,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // dO, dS1^T are free: request the next chunk's
         __syncthreads();  // every thread is past its reads of those tiles
         // issued from warp 3 (output rows), which has the lighter epilogue in this phase
-        if (tid == 96 && ok && ch + gridDim.x < nchunks) load_A2(ch + gridDim.x);
+        if (tid == 96 && ok && has_next) load_A2(nxt);
         {
             if (urow) {  // dMqk row r, columns qtr*16 .. +16 -> E1 row/column sums, dQK
                 const int cb = qtr * 16;
@@ -835,7 +849,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_after_sync();
         if (tid == kQkIssuer) bulk_wait_read0();  // the previous dq store no longer reads the dq tile
         __syncthreads();                  // Q, K, dQK free; dq tile writable
-        if (tid == 96 && ok && ch + gridDim.x < nchunks) load_B(ch + gridDim.x);
+        if (tid == 96 && ok && has_next) load_B(nxt);
         {
             const int cb = qtr * 16;
             unsigned char* dqt = sm + qk::DQ;
