@@ -174,7 +174,8 @@ struct BScan {
     static constexpr int DU_OP = GDO_OP + 2 * kC * Vt * 2;  // dU of iteration it in buffer it & 1
     static constexpr int BAR = DU_OP + 2 * kC * Vt * 2;  // tma[NS], bar1, bar2, then the TMEM slot at +48
     static constexpr size_t SMEM = BAR + 64 + 1024;
-    static constexpr uint32_t TMEM_COLS = (3 * Vt <= 64) ? 64 : (3 * Vt <= 128 ? 128 : 256);
+    // tA (two buffers), tB, tCc
+    static constexpr uint32_t TMEM_COLS = (4 * Vt <= 64) ? 64 : (4 * Vt <= 128 ? 128 : 256);
 };
 
 // 320 threads: warps 0-7 run the epilogues, warp 8 issues the MMAs and warp 9 the
@@ -293,7 +294,9 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     ok = __syncthreads_and(ok);
     fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tA = tmem, tB = tmem + Vt, tCc = tmem + 2 * Vt;
+    // Mqk^T dO of iteration it in buffer it & 1 (the second at column 3 Vt)
+    const uint32_t tB = tmem + Vt, tCc = tmem + 2 * Vt;
+    auto tA_of = [&](int it2) { return tmem + (uint32_t)((it2 & 1) * 3 * Vt); };
     const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
     const uint64_t dDS = sdesc(smem_u32(sm + P::DS_OP), 128, 2048, SW_NONE);
     const uint32_t idn = idesc_bf16(128, Vt, false, true);
@@ -302,6 +305,16 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     int it = 0;
     int b1_last = -1, b2_last = -1;  // last iterations committed to bar1 / bar2 (MMA issuer)
+    bool a_ahead = false;            // Mqk^T dO of iteration it issued during the previous one
+    // Mqk^T dO (off the chunk-to-chunk chain) of iteration it2 from its stage
+    auto issue_tA = [&](int it2) {
+        unsigned char* st2 = sm + (it2 % NS) * P::STAGE;
+        const uint64_t dM = sdesc(smem_u32(st2 + P::OFF_M), 8192, 1024, SW_128B);
+        const uint64_t dDO = sdesc(smem_u32(st2 + P::OFF_DO), 128, 1024, SW_NONE);
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2)
+            mma_bf16_ss(tA_of(it2), desc_add(dM, s2 * 2048), desc_add(dDO, s2 * 256), idm, s2 > 0);
+    };
     if (mma_warp) {
 #pragma unroll 1
         for (; ok && it < NC; ++it) {
@@ -312,18 +325,14 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (ok) {
                     // rows 64-127 of the first two A operands are neighbouring tiles (unused)
                     const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 16, 1024, SW_128B);
-                    const uint64_t dM = sdesc(smem_u32(st + P::OFF_M), 8192, 1024, SW_128B);
                     const uint64_t dQ = sdesc(smem_u32(st + P::OFF_Q), 8192, 1024, SW_128B);
-                    const uint64_t dDO = sdesc(smem_u32(st + P::OFF_DO), 128, 1024, SW_NONE);
                     const uint64_t dG =
                         sdesc(smem_u32(sm + P::GDO_OP + (it & 1) * (kC * Vt * 2)), 128, 1024, SW_NONE);
+                    if (!a_ahead) issue_tA(it);
 #pragma unroll
                     for (int s2 = 0; s2 < 8; ++s2)
                         mma_bf16_ss(tB, desc_add(dK, (s2 >> 2) * 8192 + (s2 & 3) * 32), desc_add(dDS, s2 * 256),
                                     idn, s2 > 0);
-#pragma unroll
-                    for (int s2 = 0; s2 < 4; ++s2)
-                        mma_bf16_ss(tA, desc_add(dM, s2 * 2048), desc_add(dDO, s2 * 256), idm, s2 > 0);
                     mma_commit(bar1);
                     b1_last = it;
 #pragma unroll
@@ -344,6 +353,10 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     mma_bf16_ss(tCc, desc_add(dW, s2 * 2048), desc_add(dDU, s2 * 256), idneg, 1u);
                 mma_commit(bar2);
                 b2_last = it;
+                // the next iteration's Mqk^T dO now if its tiles are in (never waits: with
+                // two stages they are requested only after bar2), covered by its bar1
+                a_ahead = it + 1 < NC && mbar_test_wait(&tbar[(it + 1) % NS], ((it + 1) / NS) & 1);
+                if (a_ahead) issue_tA(it + 1);
             }
             __syncwarp();
             fence_before_sync();
@@ -411,7 +424,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 float a[HV], bb[HV];
                 if constexpr (HV == 8) {
                     uint32_t wa[16], wb[16];
-                    tmem_ld16(tA + lanebase, wa);
+                    tmem_ld16(tA_of(it) + lanebase, wa);
                     tmem_ld16(tB + lanebase, wb);
                     tmem_wait_ld(wa);
                     tmem_wait_ld(wb);
@@ -421,7 +434,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         bb[j] = __uint_as_float(half ? wb[8 + j] : wb[j]);
                     }
                 } else {
-                    tmem_cols2<HV>(tA + lanebase + cb, tB + lanebase + cb, a, bb);
+                    tmem_cols2<HV>(tA_of(it) + lanebase + cb, tB + lanebase + cb, a, bb);
                 }
                 unsigned char* du = sm + P::DU_OP + (it & 1) * (kC * Vt * 2);
 #pragma unroll
@@ -477,6 +490,10 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     if (mma_issuer && !ok) {  // the MMAs still in flight, before the TMEM is freed
         if (b1_last >= 0) mbar_wait(bar1, b1_last & 1, nullptr, 0);
+        if (a_ahead) {  // uncommitted MMAs of the next iteration
+            mma_commit(bar1);
+            mbar_wait(bar1, (b1_last + 1) & 1, nullptr, 0);
+        }
         if (b2_last >= 0) mbar_wait(bar2, b2_last & 1, nullptr, 0);
     }
     __syncwarp();
