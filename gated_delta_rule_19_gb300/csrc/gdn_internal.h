@@ -178,7 +178,7 @@ constexpr int kVarlenBadOffsets = 1 << 30;  // error-word bit: invalid cu_seqlen
 // Work counters of the persistent kernels, in the error-flag area of the workspace
 // (64 ints, the first 32 reset at the start of every call): chunks handed out
 // beyond each CTA's first one.
-constexpr int kSchedPrep = 16, kSchedQk = 17, kSchedWy = 18, kErrWords = 32;
+constexpr int kSchedQk = 17, kSchedWy = 18, kErrWords = 32;
 cudaError_t launch_varlen_rows(const Dims& d, int64_t total, const int32_t* cu, int width_bytes, const void* src,
                                void* dst, uint32_t fill, bool scatter, int* err, const int* merge, cudaStream_t st);
 cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu, int elem_bytes, const void* src,

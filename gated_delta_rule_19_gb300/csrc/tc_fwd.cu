@@ -182,9 +182,8 @@ static_assert(P_AF + 64 * kAS * 4 <= P_T2 + 8192, "A overlaps only T1 / T2");
 static_assert(P_WS + 16384 <= P_X && P_US + 16384 <= P_T2 + 8192, "output tiles fit the dead regions");
 static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
-// Persistent, two CTAs per SM, 256 threads: CTA i starts with chunk i and takes
-// further chunks from a work counter (lane 0 of warp 2 claims each one a chunk ahead),
-// so that faster SMs take more chunks.  Warps w and w+4 read the same TMEM lane quarter (w % 4) and split its columns.
+// Persistent, two CTAs per SM, 256 threads: CTA i takes chunks i, i + gridDim.x, ...
+// Warps w and w+4 read the same TMEM lane quarter (w % 4) and split its columns.
 // A chunk's Q tiles are replaced by the next chunk's once the Gram MMA is done, its
 // K and V tiles once the W / Ut MMA is done (both requested by thread 128, whose
 // warp has no Gram epilogue work); warp 2 keeps the next chunk's gates in registers.
@@ -204,7 +203,6 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // [0] Q loads, [1] K loads, [2] Gram MMA, [3] W / Ut MMA, [4] V loads
     uint64_t* bars = (uint64_t*)(sm + P_BAR);
     uint32_t* tslot = (uint32_t*)(sm + P_BAR + 40);
-    int* s_next = (int*)(sm + P_BAR + 48);  // the chunk after this one
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sub = warp & 3, half = warp >> 2;
@@ -265,11 +263,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
-    int claimed = 0;  // lane 0 of warp 2: the next chunk, claimed a chunk ahead
-    if (warp == 2 && first < nchunks) {
-        load_gates(first);
-        if (lane == 0) claimed = (int)gridDim.x + atomicAdd(err + kSchedPrep, 1);
-    }
+    if (warp == 2 && first < nchunks) load_gates(first);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -278,10 +272,11 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     int n = 0;
     int nq = first < nchunks ? 1 : 0, nkv = nq;  // load batches issued (thread kLoader's count)
     int g_last = -1, w_last = -1;               // chunks whose MMAs were issued (thread 0)
-    int64_t nxt = first;
 #pragma unroll 1
-    for (int64_t ch = first; ch < nchunks; ch = nxt, ++n) {
+    for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
         const int ph = n & 1;
+        const int64_t nxt = ch + gridDim.x;
+        const bool has_next = nxt < nchunks;
         const int row0 = (int)(ch * kC);
         if (tid == 0) {
             ok = mbar_wait(&bars[0], ph, err, 1) && ok;
@@ -301,11 +296,6 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             bulk_wait_read0();  // the previous chunk's stores have read the A, T and Mqk tiles
         }
         if (warp == 2) {
-            const int nx = __shfl_sync(0xffffffffu, claimed, 0);
-            if (lane == 0) {
-                *s_next = nx;
-                if (nx < nchunks) claimed = (int)gridDim.x + atomicAdd(err + kSchedPrep, 1);
-            }
             const float l[2] = {log2f(__bfloat162float(ga[0])), log2f(__bfloat162float(ga[1]))};
             const float pair = l[0] + l[1];
             float incl = pair;
@@ -323,11 +313,9 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             bs[2 * lane + 1] = __bfloat162float(gb[1]);
             constexpr float kLn2 = 0.693147180559945309f;
             *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
-            if (nx < nchunks) load_gates(nx);  // consumed next iteration
+            if (has_next) load_gates(nxt);  // consumed next iteration
         }
-        __syncthreads();  // gates and the next chunk's index visible; the output tiles are writable
-        nxt = *s_next;
-        const bool has_next = nxt < nchunks;
+        __syncthreads();  // gates visible; the output tiles are writable
         ok = mbar_wait(&bars[2], ph, err, 2) && ok;
         __syncwarp();
         fence_after_sync();
