@@ -634,7 +634,7 @@ gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan
             so += round_up(bytes);
             return o;
         };
-        L->s_off = stake(((size_t)d.B + 1) * sizeof(int));
+        L->s_off = stake(((size_t)2 * d.B + 1) * sizeof(int));  // chunk_off [B+1], order [B]
         L->s_q = stake(BTH * q.K * es);
         L->s_k = stake(BTH * q.K * es);
         L->s_v = stake(BTH * q.V * es);
@@ -651,7 +651,7 @@ gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan
         off += round_up(bytes);
         return o;
     };
-    L->off = take(((size_t)d.B + 1) * sizeof(int));
+    L->off = take(((size_t)2 * d.B + 1) * sizeof(int));  // chunk_off [B+1], order [B]
     L->inner = take(inner_bytes);
     L->q = take(BTH * q.K * es);
     L->k = take(BTH * q.K * es);
@@ -755,7 +755,8 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu
         char* lb = in + (saved ? L.s_b : L.b);
         const gdn::Dims& fd = L.pd;
         e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
-            return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, off, (int*)ws, cs);
+            return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, off, off + S + 1,
+                                              (int*)ws, cs);
         });
         gdn::FlatMoves m{5, {q, k, v, alpha, beta}, {lq, lk, lv, la, lb},
                          {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)(p->H * es), (int)(p->H * es)},
@@ -766,7 +767,8 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu
                                                cs);
             });
         if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
-        const gdn::SeqMap sq{off, S};
+        // longest sequences first; the longest has at most ceil(max_len / C) chunks
+        const gdn::SeqMap sq{off, S, 0, nullptr, off + S + 1, (int)((p->T + fd.C - 1) / fd.C)};
         SplitCfg sp;
         sp.P = L.pieces;
         sp.nseq = S;
@@ -853,7 +855,7 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
         } else {
             e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
                 return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, (int*)(ws + L.off),
-                                                  (int*)ws, cs);
+                                                  (int*)(ws + L.off) + S + 1, (int*)ws, cs);
             });
             m = gdn::FlatMoves{6,
                                {q, k, v, d_o, alpha, beta},
@@ -869,7 +871,8 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
                                                cs);
             });
         if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
-        const gdn::SeqMap sq{off, S};
+        // longest sequences first; the longest has at most ceil(max_len / C) chunks
+        const gdn::SeqMap sq{off, S, 0, nullptr, off + S + 1, (int)((p->T + fd.C - 1) / fd.C)};
         SplitCfg sp;
         sp.P = L.pieces;
         sp.nseq = S;

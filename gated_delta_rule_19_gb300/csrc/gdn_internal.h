@@ -161,8 +161,16 @@ struct SeqMap {
     int nseq;
     int mode = 0;
     float* trans = nullptr;  // [nseq * H, K, K] fp32, slot s*H + h
+    // device int32 [nseq], or NULL: the sequence that grid row z runs (longest
+    // first, so that the longest chains start in the first wave); mode 0 only
+    const int* order = nullptr;
+    // chunks of the longest sequence, or 0 if not known (mode 0 only)
+    int max_nc = 0;
 };
 int tc_scan_vt(int64_t streams);
+// The slice width for a scan over dims d with sequence map sq (or NULL) and
+// `streams` CTA rows of one slice each.
+int tc_scan_vt_for(const Dims& d, const SeqMap* sq, int64_t streams);
 
 // Within-call sequence split (split.cu): piece offsets, and the chains of the
 // pieces' affine maps forward (states) and backward (state gradients).
@@ -185,10 +193,11 @@ cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu,
                                 void* dst, uint32_t fill, bool scatter, int* err, cudaStream_t st);
 // The flat chunk layout (SeqMap): chunk_off from cu (one block; lengths above
 // max_len or invalid pairs count as empty and set the error bit; the offsets
-// never pass nc_max), then rows and single elements to (gather) and from
+// never pass nc_max) and, when `order` is not NULL, the sequences by chunk count,
+// longest first (0 .. S-1 above 1024 sequences), then rows and single elements to (gather) and from
 // (scatter) the flat [H rows of nc_max*C tokens] layout.
 cudaError_t launch_varlen_offsets(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* cu,
-                                  int* chunk_off, int* err, cudaStream_t st);
+                                  int* chunk_off, int* order, int* err, cudaStream_t st);
 // Up to 8 tensors moved by one launch; row_bytes = H * (bytes per token and head),
 // a multiple of 16 or, for the gates, H * 2 or H * 4 with elem_bytes 2 or 4.
 struct FlatMoves {

@@ -189,7 +189,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dU,
             const __grid_constant__ CUtensorMap tm_dS1, const float* __restrict__ G, const float* dsT,
-            float* ds0, const int* __restrict__ chunk_off, int* err) {
+            float* ds0, const int* __restrict__ chunk_off, const int* __restrict__ order, int* err) {
     using P = BScan<Vt>;
     constexpr int HV = Vt / 2;
     constexpr int NS = P::NS;
@@ -213,11 +213,13 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // packed sequences (chunk_off) the data is one row of chunks per head (B = 1):
     // sequence s = blockIdx.z runs chunks chunk_off[s+1]-1 .. chunk_off[s] of it,
     // with the state gradients in slot s*H + h.  c below counts this CTA's chunks.
-    int b = blockIdx.z, c0 = 0, NC = d.NC;
-    const int64_t sidx = (int64_t)blockIdx.z * d.H + h;  // state slot
+    // `order` (or NULL) maps grid row z to the sequence it runs.
+    const int zs = order ? order[blockIdx.z] : (int)blockIdx.z;
+    int b = zs, c0 = 0, NC = d.NC;
+    const int64_t sidx = (int64_t)zs * d.H + h;  // state slot
     if (chunk_off) {
-        c0 = chunk_off[blockIdx.z];
-        NC = chunk_off[blockIdx.z + 1] - c0;
+        c0 = chunk_off[zs];
+        NC = chunk_off[zs + 1] - c0;
         b = 0;
     }
     const int64_t cbase = ((int64_t)b * d.H + h) * d.NC + c0;  // global index of chunk c = 0
@@ -1378,7 +1380,8 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
     if (e != cudaSuccess) return e;
     dim3 grid((kD + Vt - 1) / Vt, d.H, sq ? sq->nseq : d.B);
     kern<<<grid, 320, P::SMEM, st>>>(d, mq, mk, mW, mM, mdo, mdU, mdS1, tb.G, dsT, ds0,
-                                     sq ? sq->chunk_off : nullptr, tb.err);
+                                     sq ? sq->chunk_off : nullptr, (sq && sq->mode == 0) ? sq->order : nullptr,
+                                     tb.err);
     return cudaGetLastError();
 }
 
@@ -1387,7 +1390,7 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
 cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
                                const float* dsT, const TcBwdBufs& bb, float* ds0, cudaStream_t st,
                                const SeqMap* sq) {
-    switch (tc_scan_vt(sq ? (int64_t)sq->nseq * d.H : d.NS())) {
+    switch (tc_scan_vt_for(d, sq, sq ? (int64_t)sq->nseq * d.H : d.NS())) {
         case 16: return launch_scan_bwd_vt<16>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
         case 32: return launch_scan_bwd_vt<32>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);
         case 48: return launch_scan_bwd_vt<48>(d, q, k, d_o, tb, dsT, bb, ds0, st, sq);

@@ -606,7 +606,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_Ut, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_st, const float* __restrict__ G, const float* s0,
             float* sT, int write_o, int write_states, const int* __restrict__ chunk_off, int nseq, int tmode,
-            float* trans, int* err) {
+            float* trans, const int* __restrict__ order, int* err) {
     using P = ScanPlan<Vt>;
     constexpr int HV = Vt / 2;  // columns per thread
     constexpr int NS = P::NS;
@@ -630,13 +630,15 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // sequence s = blockIdx.z runs chunks chunk_off[s] .. chunk_off[s+1]-1 of it
     // and keeps its state in slot s*H + h.  c below counts this CTA's chunks.
     // A transition CTA (tmode) starts from S0 = I, reads U~ as 0 and writes its
-    // final state, the product of its chunks' maps, to `trans`.
+    // final state, the product of its chunks' maps, to `trans`.  `order` (or NULL)
+    // maps grid row z to the sequence it runs.
     int b = blockIdx.z, c0 = 0, NC = d.NC;
     bool tr = tmode == 2;
     if (tmode == 1 && b >= nseq) {
         tr = true;
         b -= nseq;
     }
+    if (order) b = order[b];
     const int64_t sidx = (int64_t)b * d.H + h;  // state slot
     if (chunk_off) {
         c0 = chunk_off[b];
@@ -972,7 +974,7 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     const bool tr_only = mode == 2;
     kern<<<grid, 320, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, (o != nullptr && !tr_only),
                                      (states != nullptr && !tr_only), sq ? sq->chunk_off : nullptr, nseq, mode,
-                                     sq ? sq->trans : nullptr, tb.err);
+                                     sq ? sq->trans : nullptr, (sq && mode == 0) ? sq->order : nullptr, tb.err);
     return cudaGetLastError();
 }
 
@@ -988,6 +990,30 @@ int tc_scan_vt(int64_t streams) {
     for (int vt : {16, 32, 48, 64})
         if (streams * ((kD + vt - 1) / vt) <= sms) return vt;
     return 64;
+}
+
+// Packed sequences of unequal length: the CTAs do not finish together, so the
+// waves interleave and the scan takes about max(longest chain, chunk-slices per
+// SM) chunks, each at a cost that grows with the slice width (measured on GB300
+// at about 2.1K, 2.4K, 2.75K and 3.2K cycles per chunk for 16, 32, 48 and 64
+// columns); the longest sequences start first (SeqMap::order).
+int tc_scan_vt_for(const Dims& d, const SeqMap* sq, int64_t streams) {
+    if (!sq || sq->mode != 0 || sq->max_nc <= 0) return tc_scan_vt(streams);
+    const double sms = (double)sm_count();
+    const int vts[4] = {16, 32, 48, 64};
+    const double cost[4] = {2.1, 2.4, 2.75, 3.2};
+    int best = 64;
+    double best_t = 0.0;
+    for (int i = 0; i < 4; ++i) {
+        const int slices = (kD + vts[i] - 1) / vts[i];
+        const double work = (double)d.NC * d.H * slices / sms;  // flat chunk rows bound the total
+        const double t = cost[i] * (work > sq->max_nc ? work : (double)sq->max_nc);
+        if (i == 0 || t < best_t) {
+            best = vts[i];
+            best_t = t;
+        }
+    }
+    return best;
 }
 
 cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v, const void* alpha,
@@ -1010,7 +1036,7 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb, const float* s0,
                                void* o, float* sT, __nv_bfloat16* states, cudaStream_t st, const SeqMap* sq) {
     const int64_t streams = sq ? (int64_t)sq->nseq * d.H * (sq->mode == 1 ? 2 : 1) : d.NS();
-    switch (tc_scan_vt(streams)) {
+    switch (tc_scan_vt_for(d, sq, streams)) {
         case 16: return launch_scan_vt<16>(d, q, k, tb, s0, o, sT, states, st, sq);
         case 32: return launch_scan_vt<32>(d, q, k, tb, s0, o, sT, states, st, sq);
         case 48: return launch_scan_vt<48>(d, q, k, tb, s0, o, sT, states, st, sq);

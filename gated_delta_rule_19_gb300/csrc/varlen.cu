@@ -82,9 +82,13 @@ __global__ void elems_kernel(int S, int T, int H, int64_t total, const int32_t* 
 // ------------------------------------------------ flat chunk layout (SeqMap)
 // chunk_off[s] = sum over j < s of ceil(len_j / C), capped at nc_max.  One block;
 // thread i sums a contiguous run of sequences, then the block scans the sums.
+// order (when not NULL) lists the sequences by chunk count, longest first (ties by
+// index), when S <= 1024 (each thread ranks its sequence against all others), and
+// 0 .. S-1 otherwise.
 __global__ void offsets_kernel(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* __restrict__ cu,
-                               int* __restrict__ chunk_off, int* err) {
+                               int* __restrict__ chunk_off, int* __restrict__ order, int* err) {
     __shared__ int64_t part[1024];
+    __shared__ int cnt[1024];
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (S + nt - 1) / nt;
     const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
@@ -105,15 +109,29 @@ __global__ void offsets_kernel(int S, int64_t total, int max_len, int C, int nc_
     }
     int64_t run = tid ? part[tid - 1] : 0;
     for (int s = s0; s < s1; ++s) {
-        chunk_off[s] = (int)min(run, (int64_t)nc_max);
+        const int a = (int)min(run, (int64_t)nc_max);
+        chunk_off[s] = a;
         int64_t start;
         int len;
         seq_span(cu, s, total, max_len, start, len, nullptr);
         run += (len + C - 1) / C;
+        if (S <= 1024) cnt[s] = (int)min(run, (int64_t)nc_max) - a;  // chunks of s as laid out
     }
     if (tid == nt - 1) {
         chunk_off[S] = (int)min(part[nt - 1], (int64_t)nc_max);
         if (part[nt - 1] > nc_max || cu[0] != 0 || (int64_t)cu[S] != total) atomicOr(err, kVarlenBadOffsets);
+    }
+    if (!order) return;
+    if (S > 1024) {
+        for (int s = tid; s < S; s += nt) order[s] = s;
+        return;
+    }
+    __syncthreads();
+    if (tid < S) {  // one sequence per thread (nt >= S)
+        const int n = cnt[tid];
+        int rank = 0;
+        for (int j = 0; j < S; ++j) rank += (cnt[j] > n) || (cnt[j] == n && j < tid);
+        order[rank] = tid;
     }
 }
 
@@ -243,10 +261,10 @@ cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu,
 }
 
 cudaError_t launch_varlen_offsets(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* cu,
-                                  int* chunk_off, int* err, cudaStream_t st) {
+                                  int* chunk_off, int* order, int* err, cudaStream_t st) {
     int nt = 32;  // a power of two for the block scan
     while (nt < 1024 && nt < S) nt <<= 1;
-    offsets_kernel<<<1, nt, 0, st>>>(S, total, max_len, C, nc_max, cu, chunk_off, err);
+    offsets_kernel<<<1, nt, 0, st>>>(S, total, max_len, C, nc_max, cu, chunk_off, order, err);
     return cudaGetLastError();
 }
 
