@@ -68,6 +68,12 @@ CASES = [
     ([5, 17, 33, 0, 48], 3, 32, 32, 16, "f32"),
     ([70, 9, 100], 1, 16, 64, 32, "f32"),
     ([129, 2], 2, 128, 128, 64, "f32"),
+    # the longest sequence last and equal chunk counts: the scans run the
+    # sequences longest first, through a permutation of the grid rows
+    ([64, 300, 1, 700, 128, 128, 0, 1500], 3, 128, 128, 64, "bf16"),
+    # one long sequence among short ones: the slice width follows the longest
+    # chain (16-column slices)
+    ([3000, 10, 10], 2, 128, 128, 64, "bf16"),
 ]
 
 
