@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step, prologue, varlen and sequence-split lines")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step, prologue, varlen, sequence-split and per-config lines")
     return ap.parse_args()
 
 
@@ -542,6 +542,81 @@ def measure_split(gdn, dev, stream, args, world):
                                         "dq": rel(outs["split"][1], outs["unsplit"][1])}}
 
 
+def measure_configs(gdn, dev, stream, args, world):
+    """Throughput on every workload config at this N: the forward (a streaming
+    config runs its calls in sequence, each passing its final state to the next)
+    and, where the config trains, gdn_fwd(saved) + gdn_bwd; inputs resident, the
+    median of three windows of K steps; fractions against path_roofline's bound."""
+    peaks = load_peaks()
+    res = {}
+    for name, w in WORKLOADS.items():
+        inp = make_inputs(w)
+        d = {n: (t.to(dev) if t is not None else None) for n, t in inp.items()}
+        Tc = w.T // w.calls
+        if w.calls > 1 and w.B != 1:
+            raise SystemExit(f"{name}: a streaming config runs with B = 1")
+
+        def part(t, i):  # the i-th call's tokens (contiguous: B = 1 when calls > 1)
+            return None if t is None else t[:, i * Tc:(i + 1) * Tc]
+
+        p = gdn.make_problem(w.B, Tc, w.H, w.K, w.V, w.chunk, d["q"].dtype)
+        ws_f = torch.empty(max(gdn.gdn_fwd_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(max(gdn.gdn_bwd_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+        saved = torch.empty(max(gdn.gdn_saved_bytes(p), 1), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(d["v"])
+        states = [torch.empty(w.B, w.H, w.V, w.K, dtype=torch.float32, device=dev) for _ in range(2)]
+        grads = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+                 torch.empty_like(d["alpha"]), torch.empty_like(d["beta"]))
+        ds0 = torch.empty_like(states[0])
+
+        def fwd():
+            s_in = d["initial_state"]
+            for i in range(w.calls):
+                out_state = states[i & 1]
+                gdn.gdn_fwd(part(d["q"], i), part(d["k"], i), part(d["v"], i), part(d["alpha"], i),
+                            part(d["beta"], i), s_in, chunk=w.chunk, o=part(o, i), final_state=out_state,
+                            workspace=ws_f)
+                s_in = out_state
+
+        def train():
+            a_in = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"])
+            gdn.gdn_fwd(*a_in, chunk=w.chunk, o=o, final_state=states[0], saved=saved, workspace=ws_f)
+            gdn.gdn_bwd(*a_in, d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk, grads=grads,
+                        d_initial_state=ds0, workspace=ws_b)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            wins = []
+            for _ in range(3):
+                barrier(world)
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                wins.append(e0.elapsed_time(e1) / args.steps)
+            return max_over_ranks(statistics.median(wins), world, dev)
+
+        fwd_ms = timed(fwd)
+        train_ms = timed(train) if (w.backward and w.calls == 1) else None
+        rl = path_roofline(w, peaks, train_ms or fwd_ms, fwd_ms)
+        entry = {"dtype": w.dtype, "calls": w.calls,
+                 "fwd": {"ms_per_step": fwd_ms, "token_heads_per_s": world * w.token_heads / (fwd_ms / 1e3),
+                         "frac_of_bound": rl["fwd_frac"]}}
+        if train_ms is not None:
+            entry["fwd_bwd"] = {"ms_per_step": train_ms,
+                                "token_heads_per_s": world * w.token_heads / (train_ms / 1e3),
+                                "frac_of_bound": rl["frac"], "tc_peak_frac": rl["tc_peak_frac"]}
+        res[name] = entry
+        del d, ws_f, ws_b, saved, o, states, grads, ds0
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gdn(args, world, rank, local):
     from gated_delta_rule_19_gb300 import _build, gdn
 
@@ -745,6 +820,7 @@ def run_gdn(args, world, rank, local):
     prologue = None if args.no_decode else measure_prologue(gdn, dev, stream, args, world, w)
     varlen = None if args.no_decode else measure_varlen(gdn, dev, stream, args, world, ms_max, w.token_heads)
     split = None if args.no_decode else measure_split(gdn, dev, stream, args, world)
+    configs = None if args.no_decode else measure_configs(gdn, dev, stream, args, world)
 
     if rank != 0:
         return
@@ -780,6 +856,7 @@ def run_gdn(args, world, rank, local):
         "prologue": prologue,
         "varlen": varlen,
         "sequence_split": split,
+        "configs": configs,
         "gpu_launches": launches,
         "clocks": clk,
     }

@@ -698,7 +698,15 @@ cudaError_t set_smem(F* kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-int pick_vt(const Dims& d) { return d.V < 32 ? d.V : 32; }
+// The scans' V-slice: 32 columns (or V), halved down to 4 while the CTAs (one
+// per slice and stream) would leave SMs idle; each slice's chunk loop reads the
+// same per-chunk tiles, so narrower slices trade L2 reads for parallelism.
+int pick_vt(const Dims& d) {
+    int vt = d.V < 32 ? d.V : 32;
+    const int64_t streams = (int64_t)d.B * d.H, sms = sm_count();
+    while (vt > 4 && streams * (d.V / vt) < sms) vt /= 2;
+    return vt;
+}
 
 }  // namespace
 
