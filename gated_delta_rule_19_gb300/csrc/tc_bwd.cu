@@ -10,14 +10,14 @@
 //     dS0^T = gamma_C dS1^T + Q^T diag(gamma) dO - W^T dU
 //   writes dU and dS1 (bf16) per chunk and d(initial state).
 //
-// grad_qk_tc (one CTA per chunk): U = Ut - W S0^T, then
+// grad_qk_tc (chunk-parallel; persistent, one CTA per SM): U = Ut - W S0^T, then
 //     dMqk = dO U^T,   dQK = Gam .* lower(dMqk)
 //     dQ^T = S0^T (diag(gamma) dO)^T + K^T dQK^T                 -> dq
 //     dK^T (part) = dS1^T (diag(e) U)^T + Q^T dQK                -> scratch
 //     dW^T = -S0^T dU^T                                          -> scratch
 //     dG (part): gamma in O, Gam in Mqk, exp(G_C - G) in Khat, gamma_C in S1.
 //
-// grad_wy_tc (one CTA per chunk), through T = (I + A)^-1:
+// grad_wy_tc (chunk-parallel; persistent, two CTAs per SM), through T = (I + A)^-1:
 //     Qm = dW K^T,  P = dU V^T,  dT = strict_lower(diag(beta)(P + Qm diag(gamma)))^T-wise
 //     dA = strict_lower(-T^T (dT T^T)),  E = diag(beta)(Gam .* dA)
 //     dV^T = dU^T T diag(beta)                                   -> dv

@@ -1,25 +1,28 @@
 // tc_fwd.cu -- tensor-core (tcgen05 + TMA) forward for bf16 inputs, K = V = 128,
 // chunk 64.
 //
-// prep_fwd_tc (one CTA per chunk, chunk-parallel; "Sparse Delta Memory: layer and
-// kernels", "What the layer computes", Phase 1 and Solve):
-//   TMA loads of the chunk's K, Q, V tiles (128B-swizzled, K-major);
+// prep_fwd_tc (chunk-parallel; persistent, two CTAs per SM; "Sparse Delta Memory:
+// layer and kernels", "What the layer computes", Phase 1 and Solve):
+//   TMA loads of the chunk's K, Q, V tiles (128B-swizzled, K-major), the next
+//   chunk's requested as the current one's MMAs release them;
 //   one M=128 MMA gives [K;Q] K^T = [K K^T ; Q K^T] in TMEM;
 //   A = strict_lower(beta_r Gam_ri (K K^T)_ri) -> fp32 solve T = (I + A)^-1
 //   (16x16 diagonal blocks in registers, off-diagonal blocks in shared memory);
 //   Mqk = lower(Gam .* Q K^T) -> bf16;
-//   W^T = K^T (T diag(beta gamma))^T and Ut^T = V^T (T diag(beta))^T as M=128
-//   MMAs with K and V read MN-major from the same tiles;
+//   T1 = T diag(beta gamma), T2 = T diag(beta) (bf16), then one M=128, N=256 MMA
+//   [T1; T2] [K | V] whose rows 0-63 of columns 0-127 are W = T1 K and rows 64-127
+//   of columns 128-255 are Ut = T2 V (K and V read MN-major from their tiles);
 //   W, Ut, Mqk leave through TMA stores as bf16 [rows = chunk*64 + r][...].
 //
 // scan_fwd_tc (one CTA per (V-slice of Vt rows, head, batch); Phase 2):
 //   the state slice S^T [K=128, Vt] lives in registers (fp32, thread k = row k) and
 //   as a bf16 MMA operand in shared memory; per chunk
-//     Y = Q S0^T, X = W S0^T          (M=64 MMAs)
+//     [X; Y] = [W; Q] S0^T            (one M=128 MMA)
 //     U = Ut - X,  Uh = diag(exp(G_C - G)) U
-//     O = diag(gamma) Y + Mqk U       (M=64 MMA)
-//     S1^T = gamma_C S0^T + K^T Uh    (M=128 MMA)
-//   with the next chunk's Q, W, K, Mqk tiles prefetched by TMA (two stages).
+//     S1^T = gamma_C S0^T + K^T Uh    (M=128 MMA, on the chunk-to-chunk chain)
+//     O = diag(gamma) Y + Mqk U       (M=128 MMA, rows 64-127)
+//   with warps 0-7 on the epilogues, warp 8 issuing the MMAs and warp 9 the TMA
+//   copies, and the next chunks' tiles prefetched NS stages ahead.
 //
 // Every wait is bounded (2 s); a wait that gives up raises the error flag, and
 // the block leaves its loop together (block-wide vote) after draining its copies.
