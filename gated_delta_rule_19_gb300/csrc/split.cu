@@ -14,7 +14,7 @@
 // combine_bwd chains those from the last piece back.
 //
 // States are [V, K] fp32 (V = K = 128 on the tensor-core path), slot
-// (s*P + j)*H + h for piece j of sequence s; combine kernels run 16 rows of one
+// (s*P + j)*H + h for piece j of sequence s; combine kernels run 4 rows of one
 // (sequence, head) per CTA, rows being independent.
 
 #include <cuda_runtime.h>
@@ -25,7 +25,7 @@ namespace gdn {
 namespace {
 
 constexpr int kN = 128;    // K = V on the tensor-core path
-constexpr int kRows = 16;  // state rows per CTA
+constexpr int kRows = 4;   // state rows per CTA
 constexpr int kTS = kN + 1;  // padded row of the staged transition
 
 // piece_off[s*P + j] = first chunk of piece j of sequence s: its chunks
@@ -44,51 +44,67 @@ __global__ void pieces_kernel(int S, int P, int nc, const int* __restrict__ chun
     }
 }
 
-// Forward chain: thread (column k = tid & 127, rows 8*(tid >> 7) ..) of the CTA's
-// 16 rows; trans is read straight from global memory (coalesced along k).
+// Forward chain: thread (column k = tid & 127, rows 2*(tid >> 7) ..) of the CTA's
+// kRows rows.  trans_j is staged in shared memory per piece; the next piece's is
+// read into registers (16 float4 per thread) while this one's products run, so a
+// step costs one round trip to L2 instead of one per row of trans_j.  Each output
+// sums over m in order, as a plain row-times-matrix product.
 __global__ void __launch_bounds__(256) combine_fwd_kernel(int P, int H, const float* __restrict__ s0,
                                                           const float* __restrict__ R,
                                                           const float* __restrict__ trans, float* __restrict__ s_in,
                                                           float* __restrict__ sT) {
-    __shared__ float cur[kRows][kN];
+    extern __shared__ float smf[];
+    float* tt = smf;              // [kN][kN]: trans_j
+    float* cur = smf + kN * kN;   // [kRows][kN]
     const int rb = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-    const int tid = threadIdx.x, k = tid & (kN - 1), r0 = (tid >> 7) * 8;
+    const int tid = threadIdx.x, k = tid & (kN - 1), r0 = (tid >> 7) * 2;
     const int64_t seq_slot = (int64_t)s * H + h;
-    float acc[8];
+    float4 pre[16];
+    auto load_t = [&](int j) {
+        const float4* src = (const float4*)(trans + (((int64_t)s * P + j) * H + h) * kN * kN);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+        for (int q = 0; q < 16; ++q) pre[q] = src[tid + 256 * q];
+    };
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
         const int v = rb * kRows + r0 + i;
-        cur[r0 + i][k] = s0 ? s0[(seq_slot * kN + v) * kN + k] : 0.f;
+        cur[(r0 + i) * kN + k] = s0 ? s0[(seq_slot * kN + v) * kN + k] : 0.f;
     }
-    __syncthreads();
+    if (P > 0) load_t(0);
     for (int j = 0; j < P; ++j) {
         const int64_t slot = ((int64_t)s * P + j) * H + h;
-        const float* tj = trans + slot * kN * kN;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int q = 0; q < 16; ++q) ((float4*)tt)[tid + 256 * q] = pre[q];
+        __syncthreads();  // trans_j and the rows of S_in(j) in place
+        if (j + 1 < P) load_t(j + 1);
+        float acc[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
             const int v = rb * kRows + r0 + i;
-            s_in[(slot * kN + v) * kN + k] = cur[r0 + i][k];
+            s_in[(slot * kN + v) * kN + k] = cur[(r0 + i) * kN + k];
             acc[i] = R[(slot * kN + v) * kN + k];
         }
-#pragma unroll 4
+#pragma unroll 8
         for (int m = 0; m < kN; ++m) {
-            const float t = tj[m * kN + k];
+            const float t = tt[m * kN + k];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(cur[r0 + i][m], t, acc[i]);
+            for (int i = 0; i < 2; ++i) acc[i] = fmaf(cur[(r0 + i) * kN + m], t, acc[i]);
         }
-        __syncthreads();
+        __syncthreads();  // every read of tt and cur done
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cur[r0 + i][k] = acc[i];
-        __syncthreads();
+        for (int i = 0; i < 2; ++i) cur[(r0 + i) * kN + k] = acc[i];
     }
+    __syncthreads();
     if (sT) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sT[(seq_slot * kN + rb * kRows + r0 + i) * kN + k] = cur[r0 + i][k];
+        for (int i = 0; i < 2; ++i) sT[(seq_slot * kN + rb * kRows + r0 + i) * kN + k] = cur[(r0 + i) * kN + k];
     }
 }
 
 // Reverse chain: G <- G P_j + D_j from the last piece back, P_j[m][k] =
-// trans_j[k][m]; trans_j is staged transposed (padded rows) per piece.
+// trans_j[k][m]; trans_j is staged transposed (padded rows) per piece, the next
+// piece's read into registers (coalesced, 64 per thread) during this one's
+// products.
 __global__ void __launch_bounds__(256) combine_bwd_kernel(int P, int H, const float* __restrict__ dsT,
                                                           const float* __restrict__ D,
                                                           const float* __restrict__ trans,
@@ -97,42 +113,50 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int P, int H, const fl
     float* tt = smf;               // [kN][kTS]: tt[m][k] = trans_j[k][m]
     float* cur = smf + kN * kTS;   // [kRows][kN]
     const int rb = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-    const int tid = threadIdx.x, k = tid & (kN - 1), r0 = (tid >> 7) * 8;
+    const int tid = threadIdx.x, k = tid & (kN - 1), r0 = (tid >> 7) * 2;
     const int64_t seq_slot = (int64_t)s * H + h;
-    float acc[8];
+    float pre[64];
+    auto load_t = [&](int j) {
+        const float* src = trans + (((int64_t)s * P + j) * H + h) * kN * kN;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+        for (int q = 0; q < 64; ++q) pre[q] = src[tid + 256 * q];
+    };
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
         const int v = rb * kRows + r0 + i;
         cur[(r0 + i) * kN + k] = dsT ? dsT[(seq_slot * kN + v) * kN + k] : 0.f;
     }
+    if (P > 0) load_t(P - 1);
     for (int j = P - 1; j >= 0; --j) {
         const int64_t slot = ((int64_t)s * P + j) * H + h;
-        const float* tj = trans + slot * kN * kN;
-        for (int e = tid; e < kN * kN; e += blockDim.x) {  // read rows of trans_j, write columns of tt
-            const int row = e / kN, col = e % kN;
-            tt[col * kTS + row] = tj[e];
+#pragma unroll
+        for (int q = 0; q < 64; ++q) {  // element e = row * kN + col of trans_j -> tt[col][row]
+            const int e = tid + 256 * q;
+            tt[(e & (kN - 1)) * kTS + (e >> 7)] = pre[q];
         }
         __syncthreads();
+        if (j > 0) load_t(j - 1);
+        float acc[2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 2; ++i) {
             const int v = rb * kRows + r0 + i;
             ds_out[(slot * kN + v) * kN + k] = cur[(r0 + i) * kN + k];
             acc[i] = D[(slot * kN + v) * kN + k];
         }
-#pragma unroll 4
+#pragma unroll 8
         for (int m = 0; m < kN; ++m) {
             const float p = tt[m * kTS + k];  // P_j[m][k]
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(cur[(r0 + i) * kN + m], p, acc[i]);
+            for (int i = 0; i < 2; ++i) acc[i] = fmaf(cur[(r0 + i) * kN + m], p, acc[i]);
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cur[(r0 + i) * kN + k] = acc[i];
-        __syncthreads();
+        for (int i = 0; i < 2; ++i) cur[(r0 + i) * kN + k] = acc[i];
     }
+    __syncthreads();
     if (ds0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ds0[(seq_slot * kN + rb * kRows + r0 + i) * kN + k] = cur[(r0 + i) * kN + k];
+        for (int i = 0; i < 2; ++i) ds0[(seq_slot * kN + rb * kRows + r0 + i) * kN + k] = cur[(r0 + i) * kN + k];
     }
 }
 
@@ -147,7 +171,10 @@ cudaError_t launch_split_pieces(int S, int P, int nc, const int* chunk_off, int*
 cudaError_t launch_combine_fwd(int S, int P, int H, const float* s0, const float* R, const float* trans, float* s_in,
                                float* sT, cudaStream_t st) {
     if (S * H == 0) return cudaSuccess;
-    combine_fwd_kernel<<<dim3(kN / kRows, H, S), 256, 0, st>>>(P, H, s0, R, trans, s_in, sT);
+    const int smem = (kN * kN + kRows * kN) * (int)sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(combine_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    combine_fwd_kernel<<<dim3(kN / kRows, H, S), 256, smem, st>>>(P, H, s0, R, trans, s_in, sT);
     return cudaGetLastError();
 }
 
