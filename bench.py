@@ -814,7 +814,7 @@ def run_gdn(args, world, rank, local):
                "pipeline": "uploads and downloads on two copy streams overlap adjacent steps' compute",
                "results_match_resident_run": ok_e2e}
 
-    # ---- the decode step (a survey "next" row): one token per call, the state
+    # ---- the decode step: one token per call, the state
     # carried in place between calls
     decode = None if args.no_decode else measure_decode(gdn, dev, stream, args, world)
     prologue = None if args.no_decode else measure_prologue(gdn, dev, stream, args, world, w)
