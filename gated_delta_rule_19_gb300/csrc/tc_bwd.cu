@@ -632,6 +632,24 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t sS0 = smem_u32(sm + qk::S0), sDS1 = smem_u32(sm + qk::DS1);
     const uint32_t sU = smem_u32(sm + qk::U), sEU = smem_u32(sm + qk::EU), sDQK = smem_u32(sm + qk::DQK);
 
+    // rows of Ut (this quarter's 32 columns) and Mqk (16 columns) of row r of a
+    // chunk, read a chunk ahead: each set is reloaded for the next chunk as soon as
+    // its epilogue has used it
+    uint4 utv[4], mqv[2];
+    auto load_ut = [&](int64_t c2) {
+        const uint4* up = (const uint4*)(Ut + (c2 * kC + r) * kD + qtr * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) utv[q] = up[q];
+    };
+    auto load_mq = [&](int64_t c2) {
+        const uint4* mp = (const uint4*)(Mqk + (c2 * kC + r) * kC + qtr * 16);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) mqv[q] = mp[q];
+    };
+    if (urow && first < nchunks) {
+        load_ut(first);
+        load_mq(first);
+    }
     bool ok = true;
     int n = 0;
     int64_t nxt = first;
@@ -653,16 +671,6 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             gs[2 * lane] = expf(gnext.x);
             gs[2 * lane + 1] = expf(gnext.y);
             if (nx < nchunks) gnext = *(const float2*)(G + (int64_t)nx * kC + 2 * lane);
-        }
-        // rows of Ut (64 columns) and Mqk (32 columns) this thread needs, fetched early
-        uint4 utv[4], mqv[2];
-        if (urow) {
-            const uint4* up = (const uint4*)(Ut + ((int64_t)row0 + r) * kD + qtr * 32);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) utv[q] = up[q];
-            const uint4* mp = (const uint4*)(Mqk + ((int64_t)row0 + r) * kC + qtr * 16);
-#pragma unroll
-            for (int q = 0; q < 2; ++q) mqv[q] = mp[q];
         }
         // ---- phase 1 (K over k): [X; Y] = [W; Q] S0^T, Z = [K; -] dS1^T  (M=128, N=128)
         if (tid == kQkIssuer) {
@@ -757,6 +765,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (urow) eRp[qtr * 64 + r] = acc;
             else dG1p[qtr * 64 + r] = acc;
         }
+        if (urow && has_next) load_ut(nxt);
         fence_proxy_async();
         fence_before_sync();
         ok = __syncthreads_and(ok);
@@ -807,6 +816,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 E1f[qtr * 64 + r] = rsum;
                 const float csum = warp_colsum16(e1);
                 if (lane < 16) E1f[256 + (sub * 4 + qtr) * 16 + lane] = csum;
+                if (has_next) load_mq(nxt);
             }
             // dW^T row k (= lanerow), columns qtr*16 .. +16 -> [128 x 64] tile in the EU
             // slot (dead once phase 2 is done), stored to scratch by TMA
