@@ -214,7 +214,7 @@ const char* const kKernelNames[gdn::KID_COUNT] = {
     "prep_fwd_tc", "scan_fwd_tc", "prep_fwd_tc(bwd)", "scan_fwd_tc(state-only)",
     "scan_bwd_tc", "grad_qk_tc", "grad_wy_tc", "decode_kernel", "prologue_fwd_kernel",
     "prologue_bwd_kernel", "varlen_offsets", "varlen_gather", "varlen_scatter", "scan_fwd_tc(split pass 1)",
-    "scan_bwd_tc(split pass 1)", "scan_fwd_tc(transitions)", "split_combine"};
+    "scan_bwd_tc(split pass 1)", "scan_fwd_tc(transitions)", "split_combine", "count_nonfinite_kernel"};
 
 template <typename F>
 cudaError_t timed(int kid, cudaStream_t st, F&& launch) {
@@ -991,6 +991,22 @@ gdn_status gdn_decode(const gdn_problem* p, const void* q, const void* k, const 
         return gdn::launch_decode(d, ty, q, k, v, alpha, beta, state, o, cs);
     });
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "decode kernel");
+}
+
+gdn_status gdn_count_nonfinite(const void* x, int64_t n, gdn_dtype dtype, int64_t* count, void* stream) {
+    g_err[0] = 0;
+    if (n < 0) return fail(GDN_ERR_INVALID_ARG, "n=%lld is negative", (long long)n);
+    if (dtype != GDN_F32 && dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "dtype %d is not GDN_F32 or GDN_BF16", (int)dtype);
+    if (!count) return fail(GDN_ERR_INVALID_ARG, "count is NULL");
+    if (((uintptr_t)count) % 8 != 0) return fail(GDN_ERR_INVALID_ARG, "count is not 8-byte aligned");
+    if (n > 0 && !x) return fail(GDN_ERR_INVALID_ARG, "x is NULL");
+    if (x && ((uintptr_t)x) % 16 != 0) return fail(GDN_ERR_INVALID_ARG, "x is not 16-byte aligned");
+    if (n == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const gdn::InType ty = dtype == GDN_BF16 ? gdn::InType::BF16 : gdn::InType::F32;
+    cudaError_t e = timed(gdn::KID_COUNT_NONFINITE, cs, [&] { return gdn::launch_count_nonfinite(x, n, ty, count, cs); });
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "non-finite count kernel");
 }
 
 gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,

@@ -106,6 +106,7 @@ enum KernelId {
     KID_SPLIT_BWD_P1,    // scan_bwd_tc, split pass 1 (zero-start state gradients of the pieces)
     KID_SPLIT_TRANS,     // scan_fwd_tc, transitions only (backward with saved)
     KID_SPLIT_COMBINE,   // pieces_kernel, combine_fwd_kernel, combine_bwd_kernel
+    KID_COUNT_NONFINITE, // count_nonfinite_kernel
     KID_COUNT
 };
 
@@ -220,6 +221,8 @@ cudaError_t launch_prologue_bwd(const Dims& d, InType ty, const void* qr, const 
 
 // Recurrent step over the call's tokens, state [B,H,V,K] fp32 updated in place
 // (decode.cu).
+// Adds to *count (device) the number of NaN / inf elements of x[0 .. n-1] (check.cu).
+cudaError_t launch_count_nonfinite(const void* x, int64_t n, InType ty, int64_t* count, cudaStream_t st);
 cudaError_t launch_decode(const Dims& d, InType ty, const void* q, const void* k, const void* v,
                           const void* alpha, const void* beta, float* state, void* o, cudaStream_t st);
 

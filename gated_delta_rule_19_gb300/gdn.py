@@ -74,6 +74,8 @@ def load_library():
     lib.gdn_varlen_fwd.restype = ctypes.c_int
     lib.gdn_varlen_bwd.argtypes = [P, ctypes.c_int64] + [_vp] * 17 + [ctypes.c_size_t, _vp]
     lib.gdn_varlen_bwd.restype = ctypes.c_int
+    lib.gdn_count_nonfinite.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, _vp, _vp]
+    lib.gdn_count_nonfinite.restype = ctypes.c_int
     lib.gdn_set_sequence_split.argtypes = [ctypes.c_int]
     lib.gdn_set_sequence_split.restype = ctypes.c_int
     lib.gdn_get_sequence_split.restype = ctypes.c_int
@@ -97,7 +99,7 @@ EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_works
             "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode",
             "gdn_prologue_fwd", "gdn_prologue_bwd", "gdn_varlen_fwd_workspace_bytes",
             "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_saved_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd",
-            "gdn_set_sequence_split", "gdn_get_sequence_split")
+            "gdn_set_sequence_split", "gdn_get_sequence_split", "gdn_count_nonfinite")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -258,6 +260,25 @@ def gdn_bwd(q, k, v, alpha, beta, initial_state, d_o, d_final_state=None, *, sav
                      _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
     _check(st)
     return dq, dk, dv, da, db, d_initial_state
+
+
+def gdn_count_nonfinite(t, count=None, *, stream=None):
+    """Adds the number of NaN / inf elements of the contiguous CUDA tensor ``t``
+    (float32 or bfloat16) to ``count`` (a CUDA int64 tensor of one element;
+    a new zero one when None) without synchronising, and returns ``count``."""
+    lib = load_library()
+    dev = t.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "t must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise GdnError(GDN_ERR_INVALID_ARG, "t must be contiguous")
+    if count is None:
+        count = torch.zeros(1, dtype=torch.int64, device=dev)
+    if count.dtype != torch.int64 or count.device != dev or count.numel() < 1:
+        raise GdnError(GDN_ERR_INVALID_ARG, "count must be an int64 tensor on t's device")
+    _check(lib.gdn_count_nonfinite(_ptr(t), t.numel(), _dtype_code(t.dtype), _ptr(count),
+                                   _stream_handle(dev, stream)))
+    return count
 
 
 def gdn_set_sequence_split(pieces: int) -> None:

@@ -284,6 +284,20 @@ gdn_status gdn_decode(const gdn_problem* p, const void* q, const void* k, const 
                       const void* alpha, const void* beta, float* state, void* o, void* stream);
 
 /*
+ * gdn_count_nonfinite -- adds to *count the number of elements of x[0 .. n-1]
+ * that are NaN or +-inf: a device-side check of inputs or results (for example,
+ * the outputs of gdn_fwd after suspect inputs).  It does not synchronise: the
+ * caller reads *count after synchronising `stream`.
+ *   x      device tensor of n elements in `dtype` (GDN_F32 or GDN_BF16),
+ *          16-byte aligned; may be NULL when n = 0.
+ *   count  device int64, 8-byte aligned, required, owned by the caller (who
+ *          zeroes it before the first call; calls accumulate).
+ * Errors (negative n, unsupported dtype, NULL or misaligned pointers) are
+ * returned before any launch.  Allocates nothing; asynchronous on `stream`.
+ */
+gdn_status gdn_count_nonfinite(const void* x, int64_t n, gdn_dtype dtype, int64_t* count, void* stream);
+
+/*
  * Optional launch timer, for benchmarks.  While started, every kernel launch of
  * gdn_fwd/gdn_bwd is bracketed by two CUDA events recorded on the call's stream
  * (up to `capacity` launches; later launches are not timed).  The events are

@@ -239,3 +239,17 @@ def test_sequence_split_policy(lib):
         assert h.gdn_fwd_workspace_bytes(ctypes.byref(ragged)) == w5
     finally:
         h.gdn_set_sequence_split(0)
+
+
+def test_count_nonfinite_rejects_bad_arguments(lib):
+    """Rejections return before any launch (and n = 0 launches nothing)."""
+    h = lib.load_library()
+    OK, INVALID, UNSUPPORTED = 0, 1, 2
+    x, c = ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 20))
+    assert h.gdn_count_nonfinite(x, -1, 0, c, None) == INVALID
+    assert h.gdn_count_nonfinite(x, 10, 7, c, None) == UNSUPPORTED
+    assert h.gdn_count_nonfinite(x, 10, 0, None, None) == INVALID
+    assert h.gdn_count_nonfinite(x, 10, 0, ctypes.c_void_p(FAKE + 4), None) == INVALID  # count misaligned
+    assert h.gdn_count_nonfinite(None, 10, 1, c, None) == INVALID
+    assert h.gdn_count_nonfinite(ctypes.c_void_p(FAKE + 8), 10, 1, c, None) == INVALID  # x misaligned
+    assert h.gdn_count_nonfinite(None, 0, 1, c, None) == OK
