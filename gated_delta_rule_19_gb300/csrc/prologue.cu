@@ -7,10 +7,10 @@
 // and the chain rule back to the raw tensors:
 //   dx = r (dy - y (y . dy)) with r = (x . x + eps)^(-1/2), y = x r;
 //   da = -dalpha alpha (1 - alpha),  db = dbeta beta (1 - beta).
-// Rows (b, t, h) are independent: one warp handles four rows, lane l holds K/32
-// consecutive elements of each (one vector load), the row sums are butterfly
-// reductions, and the first four lanes compute the four rows' gates.  Both
-// kernels are bound by their HBM traffic.
+// Rows (b, t, h) are independent.  Each lane owns one 16-byte piece of a row (a
+// row spans K * size / 16 neighbouring lanes), the row sums are butterfly
+// reductions over those lanes, and the gates of a tile's rows are read and
+// written directly, one tile ahead.  Both kernels are bound by their HBM traffic.
 
 #include <cuda_bf16.h>
 
@@ -20,7 +20,6 @@ namespace gdn {
 namespace {
 
 constexpr float kEps = 1e-6f;
-constexpr int kR = 4;  // rows per warp
 
 template <int N>
 __device__ __forceinline__ void ldv(const float* p, float* f) {
@@ -36,7 +35,12 @@ __device__ __forceinline__ void ldv(const float* p, float* f) {
 }
 template <int N>
 __device__ __forceinline__ void ldv(const __nv_bfloat16* p, float* f) {
-    if constexpr (N == 4) {
+    if constexpr (N == 8) {
+        const uint4 x = *(const uint4*)p;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[2 * e] = __uint_as_float(w[e] << 16), f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    } else if constexpr (N == 4) {
         const uint2 x = *(const uint2*)p;
         f[0] = __uint_as_float(x.x << 16), f[1] = __uint_as_float(x.x & 0xffff0000u);
         f[2] = __uint_as_float(x.y << 16), f[3] = __uint_as_float(x.y & 0xffff0000u);
@@ -63,7 +67,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 template <int N>
 __device__ __forceinline__ void stv(__nv_bfloat16* p, const float* f) {
-    if constexpr (N == 4) {
+    if constexpr (N == 8) {
+        *(uint4*)p = make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+    } else if constexpr (N == 4) {
         *(uint2*)p = make_uint2(pack2(f[0], f[1]), pack2(f[2], f[3]));
     } else if constexpr (N == 2) {
         *(uint32_t*)p = pack2(f[0], f[1]);
@@ -81,151 +87,244 @@ __device__ __forceinline__ void st1(__nv_bfloat16* p, float x) { *p = __float2bf
 __device__ __forceinline__ float gate_alpha(float a) { return 1.f / (1.f + expf(a)); }
 __device__ __forceinline__ float gate_beta(float b) { return 1.f / (1.f + expf(-b)); }
 
-template <int M>
-__device__ __forceinline__ void warp_sum(float (&v)[M]) {
+// Sums over aligned groups of L lanes (L a power of two, at most 32).
+template <int L, int M>
+__device__ __forceinline__ void group_sum(float (&v)[M]) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
+    for (int off = L / 2; off > 0; off >>= 1)
 #pragma unroll
         for (int j = 0; j < M; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], off);
 }
 
-template <typename Tin, int KPL>
-__global__ void __launch_bounds__(256)
-prologue_fwd_kernel(int64_t N, int K, const Tin* __restrict__ qr, const Tin* __restrict__ kr,
-                    const Tin* __restrict__ a, const Tin* __restrict__ b, Tin* __restrict__ q, Tin* __restrict__ k,
-                    Tin* __restrict__ alpha, Tin* __restrict__ beta) {
-    const int lane = threadIdx.x & 31;
-    const int64_t n0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kR;
-    if (n0 >= N) return;  // whole warps leave together
-    const int c0 = lane * KPL;
-    const bool live = c0 < K;
-    float xq[kR][KPL], xk[kR][KPL];
+
+// Persistent kernels that stream the rows through shared memory: a tile holds TR
+// rows of every input (8 KB per tensor for any K and dtype: two passes of the
+// 256 threads, one 16-byte vector per lane, L = K / VPL lanes per row); cp.async
+// brings tiles (stages - 1) ahead, so the bytes in flight do not depend on
+// registers.  Rows past N are copied from row N - 1 and never stored.  A thread
+// reads back exactly the 16-byte pieces it copied (piece tid + 256 p in pass p),
+// so its own cp.async.wait_group orders everything: no block barrier.
+// Stages of the ring: the forward's tiles hold two tensors, the backward's four.
+constexpr int kStagesFwd = 5, kStagesBwd = 3;
+
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <typename Tin, int K>
+struct Pipe {
+    static constexpr int ROWB = K * (int)sizeof(Tin);  // bytes per row
+    static constexpr int VPL = 16 / (int)sizeof(Tin);  // elements per lane
+    static constexpr int L = ROWB / 16;                // lanes per row
+    static constexpr int RPP = 256 / L;                // rows per pass
+    static constexpr int TR = 2 * RPP;                 // rows per tile
+    static constexpr int TILEB = TR * ROWB;            // bytes per tensor and tile (8192)
+    static_assert(L >= 1 && L <= 32 && TR <= 256, "a row within one warp; a tile's gates one per thread");
+};
+
+// Tile `tile` of the NIN tensors `src` into stage `stg` (2 x NIN 16-byte copies per thread).
+template <typename Tin, int K, int NIN>
+__device__ __forceinline__ void issue_tile(unsigned char* sm, int stg, int64_t tile, int64_t N,
+                                           const Tin* const (&src)[NIN]) {
+    using G = Pipe<Tin, K>;
+    const int tid = threadIdx.x;
 #pragma unroll
-    for (int r = 0; r < kR; ++r) {
-        const int64_t n = n0 + r;
-        if (live && n < N) {
-            ldv<KPL>(qr + n * K + c0, xq[r]);
-            ldv<KPL>(kr + n * K + c0, xk[r]);
-        } else {
+    for (int t = 0; t < NIN; ++t) {
 #pragma unroll
-            for (int i = 0; i < KPL; ++i) xq[r][i] = xk[r][i] = 0.f;
+        for (int h = 0; h < 2; ++h) {
+            const int c = tid + 256 * h;  // 16-byte chunk of the tile
+            const int r = c / G::L;
+            int64_t n = tile * G::TR + r;
+            if (n > N - 1) n = N - 1;
+            cp16(sm + (stg * NIN + t) * G::TILEB + c * 16,
+                 (const unsigned char*)src[t] + n * G::ROWB + (c % G::L) * 16);
         }
-    }
-    float red[2 * kR];
-#pragma unroll
-    for (int r = 0; r < kR; ++r) {
-        float sq = 0.f, sk = 0.f;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            sq = fmaf(xq[r][i], xq[r][i], sq);
-            sk = fmaf(xk[r][i], xk[r][i], sk);
-        }
-        red[2 * r] = sq;
-        red[2 * r + 1] = sk;
-    }
-    warp_sum(red);
-#pragma unroll
-    for (int r = 0; r < kR; ++r) {
-        const int64_t n = n0 + r;
-        if (!live || n >= N) continue;
-        const float rq = rsqrtf(red[2 * r] + kEps), rk = rsqrtf(red[2 * r + 1] + kEps);
-        float yq[KPL], yk[KPL];
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            yq[i] = xq[r][i] * rq;
-            yk[i] = xk[r][i] * rk;
-        }
-        stv<KPL>(q + n * K + c0, yq);
-        stv<KPL>(k + n * K + c0, yk);
-    }
-    if (lane < kR && n0 + lane < N) {
-        const int64_t n = n0 + lane;
-        st1(alpha + n, gate_alpha(ld1(a + n)));
-        st1(beta + n, gate_beta(ld1(b + n)));
     }
 }
 
-template <typename Tin, int KPL>
-__global__ void __launch_bounds__(256)
-prologue_bwd_kernel(int64_t N, int K, const Tin* __restrict__ qr, const Tin* __restrict__ kr,
-                    const Tin* __restrict__ a, const Tin* __restrict__ b, const Tin* __restrict__ dq,
-                    const Tin* __restrict__ dk, const Tin* __restrict__ dalpha, const Tin* __restrict__ dbeta,
-                    Tin* __restrict__ dqr, Tin* __restrict__ dkr, Tin* __restrict__ da, Tin* __restrict__ db) {
-    const int lane = threadIdx.x & 31;
-    const int64_t n0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kR;
-    if (n0 >= N) return;
-    const int c0 = lane * KPL;
-    const bool live = c0 < K;
-    float xq[kR][KPL], xk[kR][KPL], gq[kR][KPL], gk[kR][KPL];
-#pragma unroll
-    for (int r = 0; r < kR; ++r) {
-        const int64_t n = n0 + r;
-        if (live && n < N) {
-            ldv<KPL>(qr + n * K + c0, xq[r]);
-            ldv<KPL>(kr + n * K + c0, xk[r]);
-            ldv<KPL>(dq + n * K + c0, gq[r]);
-            ldv<KPL>(dk + n * K + c0, gk[r]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < KPL; ++i) xq[r][i] = xk[r][i] = gq[r][i] = gk[r][i] = 0.f;
-        }
+template <typename Tin, int K>
+__global__ void __launch_bounds__(256, 2)
+prologue_fwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict__ kr, const Tin* __restrict__ a,
+                  const Tin* __restrict__ b, Tin* __restrict__ q, Tin* __restrict__ k, Tin* __restrict__ alpha,
+                  Tin* __restrict__ beta) {
+    using G = Pipe<Tin, K>;
+    extern __shared__ __align__(16) unsigned char psm[];
+    const int tid = threadIdx.x, sub = tid / G::L, c0 = (tid % G::L) * G::VPL;
+    const int64_t ntiles = (N + G::TR - 1) / G::TR;
+    const Tin* const src[2] = {qr, kr};
+    constexpr int kStages = kStagesFwd;
+    // gate logits of the next tile are read one tile ahead (thread tid: row tid)
+    const bool grow = tid < G::TR;
+    auto gates_in = [&](int64_t t, float& x, float& y) {
+        const int64_t n = t * G::TR + tid;
+        if (grow && t < ntiles && n < N) x = ld1(a + n), y = ld1(b + n);
+    };
+    float ga = 0.f, gb = 0.f;
+    gates_in(blockIdx.x, ga, gb);
+    for (int i = 0; i < kStages - 1; ++i) {
+        const int64_t t = blockIdx.x + (int64_t)i * gridDim.x;
+        if (t < ntiles) issue_tile<Tin, K, 2>(psm, i, t, N, src);
+        cp_commit();
     }
-    // per row: x.x and x.dy for q and k
-    float red[4 * kR];
+    int j = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        cp_wait_one_pending();  // this tile's pieces have landed
+        const int64_t nt = tile + (int64_t)(kStages - 1) * gridDim.x;
+        if (nt < ntiles) issue_tile<Tin, K, 2>(psm, (j + kStages - 1) % kStages, nt, N, src);
+        cp_commit();
+        float ga_n = 0.f, gb_n = 0.f;
+        gates_in(tile + gridDim.x, ga_n, gb_n);
+        const unsigned char* st = psm + (j % kStages) * 2 * G::TILEB;
 #pragma unroll
-    for (int r = 0; r < kR; ++r) {
-        float sq = 0.f, sk = 0.f, pq = 0.f, pk = 0.f;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int r = pass * G::RPP + sub;
+            const int64_t n = tile * G::TR + r;
+            float xq[G::VPL], xk[G::VPL];
+            ldv<G::VPL>((const Tin*)(st + r * G::ROWB) + c0, xq);
+            ldv<G::VPL>((const Tin*)(st + G::TILEB + r * G::ROWB) + c0, xk);
+            float red[2] = {0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            sq = fmaf(xq[r][i], xq[r][i], sq);
-            sk = fmaf(xk[r][i], xk[r][i], sk);
-            pq = fmaf(xq[r][i], gq[r][i], pq);
-            pk = fmaf(xk[r][i], gk[r][i], pk);
+            for (int i = 0; i < G::VPL; ++i) {
+                red[0] = fmaf(xq[i], xq[i], red[0]);
+                red[1] = fmaf(xk[i], xk[i], red[1]);
+            }
+            group_sum<G::L>(red);
+            if (n < N) {
+                const float rq = rsqrtf(red[0] + kEps), rk = rsqrtf(red[1] + kEps);
+#pragma unroll
+                for (int i = 0; i < G::VPL; ++i) {
+                    xq[i] *= rq;
+                    xk[i] *= rk;
+                }
+                stv<G::VPL>(q + n * K + c0, xq);
+                stv<G::VPL>(k + n * K + c0, xk);
+            }
         }
-        red[4 * r] = sq, red[4 * r + 1] = sk, red[4 * r + 2] = pq, red[4 * r + 3] = pk;
-    }
-    warp_sum(red);
-#pragma unroll
-    for (int r = 0; r < kR; ++r) {
-        const int64_t n = n0 + r;
-        if (!live || n >= N) continue;
-        // dx = r dy - x r^3 (x . dy)
-        const float rq = rsqrtf(red[4 * r] + kEps), rk = rsqrtf(red[4 * r + 1] + kEps);
-        const float cq = rq * rq * rq * red[4 * r + 2], ck = rk * rk * rk * red[4 * r + 3];
-        float oq[KPL], ok2[KPL];
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            oq[i] = rq * gq[r][i] - cq * xq[r][i];
-            ok2[i] = rk * gk[r][i] - ck * xk[r][i];
+        if (grow && tile * G::TR + tid < N) {
+            const int64_t n = tile * G::TR + tid;
+            st1(alpha + n, gate_alpha(ga));
+            st1(beta + n, gate_beta(gb));
         }
-        stv<KPL>(dqr + n * K + c0, oq);
-        stv<KPL>(dkr + n * K + c0, ok2);
-    }
-    if (lane < kR && n0 + lane < N) {
-        const int64_t n = n0 + lane;
-        const float al = gate_alpha(ld1(a + n)), be = gate_beta(ld1(b + n));
-        st1(da + n, -ld1(dalpha + n) * al * (1.f - al));
-        st1(db + n, ld1(dbeta + n) * be * (1.f - be));
+        ga = ga_n, gb = gb_n;
     }
 }
 
-template <typename Tin, int KPL>
-cudaError_t launch_fwd_k(int64_t N, int K, const void* qr, const void* kr, const void* a, const void* b, void* q,
-                         void* k, void* alpha, void* beta, cudaStream_t st) {
-    const int64_t blocks = (N + 8 * kR - 1) / (8 * kR);
-    prologue_fwd_kernel<Tin, KPL><<<(unsigned)blocks, 256, 0, st>>>(
-        N, K, (const Tin*)qr, (const Tin*)kr, (const Tin*)a, (const Tin*)b, (Tin*)q, (Tin*)k, (Tin*)alpha,
-        (Tin*)beta);
+template <typename Tin, int K>
+__global__ void __launch_bounds__(256, 2)
+prologue_bwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict__ kr, const Tin* __restrict__ a,
+                  const Tin* __restrict__ b, const Tin* __restrict__ dq, const Tin* __restrict__ dk,
+                  const Tin* __restrict__ dalpha, const Tin* __restrict__ dbeta, Tin* __restrict__ dqr,
+                  Tin* __restrict__ dkr, Tin* __restrict__ da, Tin* __restrict__ db) {
+    using G = Pipe<Tin, K>;
+    extern __shared__ __align__(16) unsigned char psm[];
+    const int tid = threadIdx.x, sub = tid / G::L, c0 = (tid % G::L) * G::VPL;
+    const int64_t ntiles = (N + G::TR - 1) / G::TR;
+    const Tin* const src[4] = {qr, kr, dq, dk};
+    constexpr int kStages = kStagesBwd;
+    const bool grow = tid < G::TR;
+    auto gates_in = [&](int64_t t, float (&x)[4]) {
+        const int64_t n = t * G::TR + tid;
+        if (grow && t < ntiles && n < N) x[0] = ld1(a + n), x[1] = ld1(b + n), x[2] = ld1(dalpha + n), x[3] = ld1(dbeta + n);
+    };
+    float gv[4] = {0.f, 0.f, 0.f, 0.f};
+    gates_in(blockIdx.x, gv);
+    for (int i = 0; i < kStages - 1; ++i) {
+        const int64_t t = blockIdx.x + (int64_t)i * gridDim.x;
+        if (t < ntiles) issue_tile<Tin, K, 4>(psm, i, t, N, src);
+        cp_commit();
+    }
+    int j = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        cp_wait_one_pending();
+        const int64_t nt = tile + (int64_t)(kStages - 1) * gridDim.x;
+        if (nt < ntiles) issue_tile<Tin, K, 4>(psm, (j + kStages - 1) % kStages, nt, N, src);
+        cp_commit();
+        float gv_n[4] = {0.f, 0.f, 0.f, 0.f};
+        gates_in(tile + gridDim.x, gv_n);
+        const unsigned char* st = psm + (j % kStages) * 4 * G::TILEB;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int r = pass * G::RPP + sub;
+            const int64_t n = tile * G::TR + r;
+            float xq[G::VPL], xk[G::VPL], gq[G::VPL], gk[G::VPL];
+            ldv<G::VPL>((const Tin*)(st + r * G::ROWB) + c0, xq);
+            ldv<G::VPL>((const Tin*)(st + G::TILEB + r * G::ROWB) + c0, xk);
+            ldv<G::VPL>((const Tin*)(st + 2 * G::TILEB + r * G::ROWB) + c0, gq);
+            ldv<G::VPL>((const Tin*)(st + 3 * G::TILEB + r * G::ROWB) + c0, gk);
+            // x.x and x.dy for q and k
+            float red[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < G::VPL; ++i) {
+                red[0] = fmaf(xq[i], xq[i], red[0]);
+                red[1] = fmaf(xk[i], xk[i], red[1]);
+                red[2] = fmaf(xq[i], gq[i], red[2]);
+                red[3] = fmaf(xk[i], gk[i], red[3]);
+            }
+            group_sum<G::L>(red);
+            if (n < N) {
+                // dx = r dy - x r^3 (x . dy)
+                const float rq = rsqrtf(red[0] + kEps), rk = rsqrtf(red[1] + kEps);
+                const float cq = rq * rq * rq * red[2], ck = rk * rk * rk * red[3];
+#pragma unroll
+                for (int i = 0; i < G::VPL; ++i) {
+                    gq[i] = rq * gq[i] - cq * xq[i];
+                    gk[i] = rk * gk[i] - ck * xk[i];
+                }
+                stv<G::VPL>(dqr + n * K + c0, gq);
+                stv<G::VPL>(dkr + n * K + c0, gk);
+            }
+        }
+        if (grow && tile * G::TR + tid < N) {
+            const int64_t n = tile * G::TR + tid;
+            const float al = gate_alpha(gv[0]), be = gate_beta(gv[1]);
+            st1(da + n, -gv[2] * al * (1.f - al));
+            st1(db + n, gv[3] * be * (1.f - be));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) gv[i] = gv_n[i];
+    }
+}
+
+// Grid: the resident CTAs of every SM (at most the number of tiles).
+template <typename KernelT>
+int64_t pipe_grid(KernelT kern, size_t smem, int64_t ntiles, cudaError_t& e) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int per_sm = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t g = (int64_t)per_sm * sm_count();
+    return g < ntiles ? g : ntiles;
+}
+
+template <typename Tin, int K>
+cudaError_t launch_fwd_k(int64_t N, const void* qr, const void* kr, const void* a, const void* b, void* q, void* k,
+                         void* alpha, void* beta, cudaStream_t st) {
+    using G = Pipe<Tin, K>;
+    const size_t smem = (size_t)kStagesFwd * 2 * G::TILEB;
+    cudaError_t e;
+    const int64_t grid = pipe_grid(prologue_fwd_kernel<Tin, K>, smem, (N + G::TR - 1) / G::TR, e);
+    if (e != cudaSuccess) return e;
+    prologue_fwd_kernel<Tin, K><<<(unsigned)grid, 256, smem, st>>>(N, (const Tin*)qr, (const Tin*)kr, (const Tin*)a,
+                                                                 (const Tin*)b, (Tin*)q, (Tin*)k, (Tin*)alpha,
+                                                                 (Tin*)beta);
     return cudaGetLastError();
 }
 
-template <typename Tin, int KPL>
-cudaError_t launch_bwd_k(int64_t N, int K, const void* qr, const void* kr, const void* a, const void* b,
-                         const void* dq, const void* dk, const void* dalpha, const void* dbeta, void* dqr, void* dkr,
-                         void* da, void* db, cudaStream_t st) {
-    const int64_t blocks = (N + 8 * kR - 1) / (8 * kR);
-    prologue_bwd_kernel<Tin, KPL><<<(unsigned)blocks, 256, 0, st>>>(
-        N, K, (const Tin*)qr, (const Tin*)kr, (const Tin*)a, (const Tin*)b, (const Tin*)dq, (const Tin*)dk,
+template <typename Tin, int K>
+cudaError_t launch_bwd_k(int64_t N, const void* qr, const void* kr, const void* a, const void* b, const void* dq,
+                         const void* dk, const void* dalpha, const void* dbeta, void* dqr, void* dkr, void* da,
+                         void* db, cudaStream_t st) {
+    using G = Pipe<Tin, K>;
+    const size_t smem = (size_t)kStagesBwd * 4 * G::TILEB;
+    cudaError_t e;
+    const int64_t grid = pipe_grid(prologue_bwd_kernel<Tin, K>, smem, (N + G::TR - 1) / G::TR, e);
+    if (e != cudaSuccess) return e;
+    prologue_bwd_kernel<Tin, K><<<(unsigned)grid, 256, smem, st>>>(
+        N, (const Tin*)qr, (const Tin*)kr, (const Tin*)a, (const Tin*)b, (const Tin*)dq, (const Tin*)dk,
         (const Tin*)dalpha, (const Tin*)dbeta, (Tin*)dqr, (Tin*)dkr, (Tin*)da, (Tin*)db);
     return cudaGetLastError();
 }
@@ -234,10 +333,10 @@ template <typename Tin>
 cudaError_t fwd_t(int64_t N, int K, const void* qr, const void* kr, const void* a, const void* b, void* q, void* k,
                   void* alpha, void* beta, cudaStream_t st) {
     switch (K) {
-        case 16:
-        case 32: return launch_fwd_k<Tin, 1>(N, K, qr, kr, a, b, q, k, alpha, beta, st);
-        case 64: return launch_fwd_k<Tin, 2>(N, K, qr, kr, a, b, q, k, alpha, beta, st);
-        default: return launch_fwd_k<Tin, 4>(N, K, qr, kr, a, b, q, k, alpha, beta, st);
+        case 16: return launch_fwd_k<Tin, 16>(N, qr, kr, a, b, q, k, alpha, beta, st);
+        case 32: return launch_fwd_k<Tin, 32>(N, qr, kr, a, b, q, k, alpha, beta, st);
+        case 64: return launch_fwd_k<Tin, 64>(N, qr, kr, a, b, q, k, alpha, beta, st);
+        default: return launch_fwd_k<Tin, 128>(N, qr, kr, a, b, q, k, alpha, beta, st);
     }
 }
 
@@ -246,10 +345,10 @@ cudaError_t bwd_t(int64_t N, int K, const void* qr, const void* kr, const void* 
                   const void* dk, const void* dalpha, const void* dbeta, void* dqr, void* dkr, void* da, void* db,
                   cudaStream_t st) {
     switch (K) {
-        case 16:
-        case 32: return launch_bwd_k<Tin, 1>(N, K, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
-        case 64: return launch_bwd_k<Tin, 2>(N, K, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
-        default: return launch_bwd_k<Tin, 4>(N, K, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
+        case 16: return launch_bwd_k<Tin, 16>(N, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
+        case 32: return launch_bwd_k<Tin, 32>(N, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
+        case 64: return launch_bwd_k<Tin, 64>(N, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
+        default: return launch_bwd_k<Tin, 128>(N, qr, kr, a, b, dq, dk, dalpha, dbeta, dqr, dkr, da, db, st);
     }
 }
 
