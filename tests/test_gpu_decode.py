@@ -45,6 +45,9 @@ def _decode(inp, calls=1):
     (1, 3, 4, 16, 16, "f32"),
     (2, 16, 2, 32, 128, "bf16"),
     (1, 7, 1, 128, 64, "f32"),
+    # more 8-row units (64 * 8 * 16 = 8192) than the persistent grid has warps
+    (64, 2, 8, 128, 128, "bf16"),
+    (40, 3, 9, 64, 64, "f32"),
 ])
 def test_decode_matches_oracle(oracle_mod, B, T, H, K, V, dtype):
     w = custom(B=B, T=T, H=H, K=K, V=V, chunk=64, dtype=dtype, seed=900 + T + K, init_std=0.5)

@@ -33,8 +33,14 @@ def _check(got, ref, lim, names):
     assert all(e <= lim for e in bad.values()), bad
 
 
+# Row tiles are 8 KB per tensor (16 to 256 rows, by K and dtype) and each CTA of
+# the persistent grid walks several of them: the cases cover every K and dtype,
+# ragged last tiles, and (the last two) more tiles than the grid has CTAs.
 @pytest.mark.parametrize("B,T,H,K,dtype", [(2, 33, 3, 128, "f32"), (1, 17, 2, 64, "bf16"),
-                                           (3, 5, 4, 16, "f32"), (2, 64, 6, 128, "bf16")])
+                                           (3, 5, 4, 16, "f32"), (2, 64, 6, 128, "bf16"),
+                                           (1, 1000, 3, 32, "bf16"), (2, 777, 5, 16, "bf16"),
+                                           (1, 50, 7, 64, "f32"), (1, 300, 3, 32, "f32"),
+                                           (4, 4099, 6, 128, "bf16"), (3, 4097, 5, 32, "f32")])
 def test_prologue_matches_oracle(pro, B, T, H, K, dtype):
     x = make_prologue_inputs(B, T, H, K, dtype, seed=B * 100 + T + K)
     d = {n: t.cuda() for n, t in x.items()}
