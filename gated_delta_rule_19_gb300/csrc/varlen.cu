@@ -173,14 +173,15 @@ __device__ __forceinline__ void move_run(const U* __restrict__ src, U* __restric
         for (int k = nvalid + tid; k < ntotal; k += nt) dst[k] = fill;
 }
 
-// Block per flat chunk c: the sequence s owning it (chunk_off[s] <= c <
-// chunk_off[s+1]) has n = min(C, len - j*C) valid rows there, j = c - chunk_off[s],
-// at packed rows start + j*C ...  Both sides are contiguous runs of rows, so each
-// tensor is one copy of n rows plus (gather) C - n rows of fill.
+// Block per flat chunk c and tensor t = blockIdx.y (so that the work spreads evenly
+// over the SMs): the sequence s owning chunk c (chunk_off[s] <= c < chunk_off[s+1])
+// has n = min(C, len - j*C) valid rows there, j = c - chunk_off[s], at packed rows
+// start + j*C ...  Both sides are contiguous runs of rows, so the tensor is one
+// copy of n rows plus (gather) C - n rows of fill.
 __global__ void flat_move_kernel(FlatMoves m, int S, int C, int nc_max, int64_t total,
                                  const int32_t* __restrict__ cu, const int* __restrict__ chunk_off, int dir,
                                  const int* merge, int* err) {
-    if (merge && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, *merge);
+    if (merge && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(err, *merge);
     __shared__ int64_t sh_row;
     __shared__ int sh_n;
     for (int c = blockIdx.x; c < nc_max; c += gridDim.x) {
@@ -201,28 +202,27 @@ __global__ void flat_move_kernel(FlatMoves m, int S, int C, int nc_max, int64_t 
         __syncthreads();
         const int n = sh_n;
         const int64_t prow = sh_row;
-        if (dir == 0 || n > 0) {
-            for (int t = 0; t < m.n; ++t) {
-                const int rb = m.row_bytes[t], eb = m.elem_bytes[t];
-                const int per_row = rb / eb;
-                const int64_t fo = (int64_t)c * C * per_row, po = prow * per_row;
-                const int nv = n * per_row, nall = C * per_row;
-                const char* sb = (const char*)m.src[t];
-                char* db = (char*)m.dst[t];
-                const uint32_t f = m.fill[t];
-                if (eb == 16) {
-                    const uint4* sp = (const uint4*)sb + (dir == 0 ? po : fo);
-                    uint4* dp = (uint4*)db + (dir == 0 ? fo : po);
-                    move_run<uint4>(sp, dp, nv, nall, make_uint4(f, f, f, f), dir == 0);
-                } else if (eb == 4) {
-                    const uint32_t* sp = (const uint32_t*)sb + (dir == 0 ? po : fo);
-                    uint32_t* dp = (uint32_t*)db + (dir == 0 ? fo : po);
-                    move_run<uint32_t>(sp, dp, nv, nall, f, dir == 0);
-                } else {
-                    const uint16_t* sp = (const uint16_t*)sb + (dir == 0 ? po : fo);
-                    uint16_t* dp = (uint16_t*)db + (dir == 0 ? fo : po);
-                    move_run<uint16_t>(sp, dp, nv, nall, (uint16_t)f, dir == 0);
-                }
+        if ((dir == 0 || n > 0) && (int)blockIdx.y < m.n) {
+            const int t = blockIdx.y;
+            const int rb = m.row_bytes[t], eb = m.elem_bytes[t];
+            const int per_row = rb / eb;
+            const int64_t fo = (int64_t)c * C * per_row, po = prow * per_row;
+            const int nv = n * per_row, nall = C * per_row;
+            const char* sb = (const char*)m.src[t];
+            char* db = (char*)m.dst[t];
+            const uint32_t f = m.fill[t];
+            if (eb == 16) {
+                const uint4* sp = (const uint4*)sb + (dir == 0 ? po : fo);
+                uint4* dp = (uint4*)db + (dir == 0 ? fo : po);
+                move_run<uint4>(sp, dp, nv, nall, make_uint4(f, f, f, f), dir == 0);
+            } else if (eb == 4) {
+                const uint32_t* sp = (const uint32_t*)sb + (dir == 0 ? po : fo);
+                uint32_t* dp = (uint32_t*)db + (dir == 0 ? fo : po);
+                move_run<uint32_t>(sp, dp, nv, nall, f, dir == 0);
+            } else {
+                const uint16_t* sp = (const uint16_t*)sb + (dir == 0 ? po : fo);
+                uint16_t* dp = (uint16_t*)db + (dir == 0 ? fo : po);
+                move_run<uint16_t>(sp, dp, nv, nall, (uint16_t)f, dir == 0);
             }
         }
         __syncthreads();  // sh_n / sh_row are rewritten for the next chunk
@@ -277,7 +277,8 @@ cudaError_t launch_varlen_flat(const FlatMoves& m, int S, int C, int nc_max, int
     if (m.n < 0 || m.n > 8) return cudaErrorInvalidValue;
     const int64_t cap = (int64_t)sm_count() * 8;
     const unsigned grid = (unsigned)max((int64_t)1, min((int64_t)nc_max, cap));
-    flat_move_kernel<<<grid, 256, 0, st>>>(m, S, C, nc_max, total, cu, chunk_off, scatter ? 1 : 0, merge, err);
+    const dim3 g2(grid, (unsigned)(m.n > 0 ? m.n : 1));  // one row of blocks even with no tensor (merge)
+    flat_move_kernel<<<g2, 256, 0, st>>>(m, S, C, nc_max, total, cu, chunk_off, scatter ? 1 : 0, merge, err);
     return cudaGetLastError();
 }
 
