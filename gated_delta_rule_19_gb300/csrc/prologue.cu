@@ -105,7 +105,11 @@ __device__ __forceinline__ void group_sum(float (&v)[M]) {
 // reads back exactly the 16-byte pieces it copied (piece tid + 256 p in pass p),
 // so its own cp.async.wait_group orders everything: no block barrier.
 // Stages of the ring: the forward's tiles hold two tensors, the backward's four.
-constexpr int kStagesFwd = 5, kStagesBwd = 3;
+// More resident CTAs (four per SM forward, three backward) pay more than a deeper
+// ring: with two per SM and rings of five and three stages the kernels ran 12%
+// and 9% slower.
+constexpr int kStagesFwd = 3, kStagesBwd = 2;
+static_assert(kStagesFwd >= 2 && kStagesBwd >= 2, "a ring holds the current tile and the next");
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
@@ -113,7 +117,9 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
                  : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Waits until at most N of this thread's copy groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <typename Tin, int K>
 struct Pipe {
@@ -147,7 +153,7 @@ __device__ __forceinline__ void issue_tile(unsigned char* sm, int stg, int64_t t
 }
 
 template <typename Tin, int K>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 4)
 prologue_fwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict__ kr, const Tin* __restrict__ a,
                   const Tin* __restrict__ b, Tin* __restrict__ q, Tin* __restrict__ k, Tin* __restrict__ alpha,
                   Tin* __restrict__ beta) {
@@ -172,7 +178,7 @@ prologue_fwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict
     }
     int j = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
-        cp_wait_one_pending();  // this tile's pieces have landed
+        cp_wait<kStages - 2>();  // groups 0 .. j done: this tile's pieces have landed
         const int64_t nt = tile + (int64_t)(kStages - 1) * gridDim.x;
         if (nt < ntiles) issue_tile<Tin, K, 2>(psm, (j + kStages - 1) % kStages, nt, N, src);
         cp_commit();
@@ -214,7 +220,7 @@ prologue_fwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict
 }
 
 template <typename Tin, int K>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 3)
 prologue_bwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict__ kr, const Tin* __restrict__ a,
                   const Tin* __restrict__ b, const Tin* __restrict__ dq, const Tin* __restrict__ dk,
                   const Tin* __restrict__ dalpha, const Tin* __restrict__ dbeta, Tin* __restrict__ dqr,
@@ -239,7 +245,7 @@ prologue_bwd_kernel(int64_t N, const Tin* __restrict__ qr, const Tin* __restrict
     }
     int j = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
-        cp_wait_one_pending();
+        cp_wait<kStages - 2>();
         const int64_t nt = tile + (int64_t)(kStages - 1) * gridDim.x;
         if (nt < ntiles) issue_tile<Tin, K, 4>(psm, (j + kStages - 1) % kStages, nt, N, src);
         cp_commit();
