@@ -10,7 +10,7 @@ import torch
 
 from gated_delta_rule_19_gb300 import gdn
 from gated_delta_rule_19_gb300.inputs import custom, make_inputs, make_varlen_inputs
-from gdn_testutil import compare, gpu_run, oracle_run, rel_l2, to_np
+from gdn_testutil import compare, gpu_run, oracle_run, rel_l2, sample_gpu, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -136,3 +136,15 @@ def test_split_varlen_matches_oracle(oracle_mod):
     want["final_state"] = np.stack(ref_sT)
     want["d_initial_state"] = np.stack(ref_ds0)
     compare({n: to_np(x) for n, x in got.items()}, want, "bf16")
+
+
+def test_long_context_workload_sampled(oracle_mod):
+    """The long context the bench times (B=1, T=65536, H=4, K=V=128 bf16: 1024
+    chunks per stream), split automatically as the bench runs it; two of its four
+    streams against the oracle over the whole sequence, forward and backward."""
+    w = custom(B=1, T=65536, H=4, K=128, V=128, chunk=64, dtype="bf16", seed=7, init_std=0.1)
+    inp = make_inputs(w)
+    got, prof = _run_profiled(w, inp)
+    assert "scan_fwd_tc(split pass 1)" in prof and "scan_bwd_tc(split pass 1)" in prof, prof
+    streams = [(0, 0), (0, 3)]
+    compare(sample_gpu(got, streams), oracle_run(oracle_mod, inp, True, streams=streams), "bf16")

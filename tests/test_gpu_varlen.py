@@ -243,3 +243,34 @@ def test_reset_mask_matches_oracle(oracle_mod, dtype, K, chunk):
     ref.update(resets.bwd_resets(*args, reset.numpy(), npi["initial_state"], npi["d_o"], npi["d_final_state"]))
     compare(got, ref, dtype)
     assert np.all(got["d_initial_state"][1] == 0.0)  # row 1 was reset at t = 0
+
+
+def test_varlen_bench_workload_sampled(oracle_mod):
+    """The packed batch the bench times (32768 tokens in 17 sequences of
+    log-uniform lengths in [128, 8192], H=6, K=V=128, bf16), run whole in the
+    bench's launch configuration; its longest, shortest and median sequences
+    against the oracle."""
+    from gated_delta_rule_19_gb300.inputs import VARLEN_WORKLOADS, varlen_lengths
+
+    spec = VARLEN_WORKLOADS["varlen_bf16_T32768_H6_K128_V128"]
+    lengths = varlen_lengths(spec["total"], spec["lo"], spec["hi"], spec["seed"])
+    inp = make_varlen_inputs(lengths, spec["H"], spec["K"], spec["V"], spec["dtype"], seed=spec["seed"])
+    got = _run_varlen(_cuda(inp), 64)
+    tol = TOL["bf16"]
+    cu = inp["cu_seqlens"].tolist()
+    by_len = sorted(range(len(lengths)), key=lambda s: lengths[s])
+    bad = []
+    for s in (by_len[-1], by_len[0], by_len[len(by_len) // 2]):
+        ref = _oracle_seq(oracle_mod, inp, s)
+        a, e = cu[s], cu[s + 1]
+        for n in ("o",) + GRADS:
+            err = rel_l2(to_np(got[n][a:e]), ref[n])
+            if err > tol["out" if n == "o" else "grad"]:
+                bad.append(f"seq {s} (len {e - a}) {n}: {err:.2e}")
+        for n in ("final_state", "d_initial_state"):
+            if got.get(n) is None:
+                continue
+            err = rel_l2(to_np(got[n][s]), ref[n])
+            if err > tol["out" if n == "final_state" else "grad"]:
+                bad.append(f"seq {s} {n}: {err:.2e}")
+    assert not bad, "; ".join(bad)
