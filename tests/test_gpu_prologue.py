@@ -40,7 +40,8 @@ def _check(got, ref, lim, names):
                                            (3, 5, 4, 16, "f32"), (2, 64, 6, 128, "bf16"),
                                            (1, 1000, 3, 32, "bf16"), (2, 777, 5, 16, "bf16"),
                                            (1, 50, 7, 64, "f32"), (1, 300, 3, 32, "f32"),
-                                           (4, 4099, 6, 128, "bf16"), (3, 4097, 5, 32, "f32")])
+                                           (4, 4099, 6, 128, "bf16"), (3, 4097, 5, 32, "f32"),
+                                           (8, 4096, 6, 128, "bf16")])  # the bench's workload
 def test_prologue_matches_oracle(pro, B, T, H, K, dtype):
     x = make_prologue_inputs(B, T, H, K, dtype, seed=B * 100 + T + K)
     d = {n: t.cuda() for n, t in x.items()}
