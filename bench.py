@@ -660,7 +660,9 @@ def run_gdn(args, world, rank, local):
         oracle.build()
         threads = oracle.threads(0)
         streams = sample_streams(w, n_sample_streams(w, threads))
-        dt, ref = oracle_step(oracle, np_inputs(inp_cpu), streams, threads)
+        np_in = np_inputs(inp_cpu)
+        dt, ref = oracle_step(oracle, np_in, streams, threads)
+        dt1, _ = oracle_step(oracle, np_in, streams[:1], 1)  # one stream on one thread
         got = dict(o=o, final_state=sT, dq=grads[0], dk=grads[1], dv=grads[2],
                    dalpha=grads[3], dbeta=grads[4], d_initial_state=ds0)
         parity = {}
@@ -680,7 +682,9 @@ def run_gdn(args, world, rank, local):
         cpu = {"value": len(streams) * w.T / dt, "unit": UNIT, "cores": threads,
                "kind": "oracle",
                "sample": f"{len(streams)} of {w.B * w.H} (b,h) streams at full T={w.T}, "
-                         f"fwd+bwd float64, {dt:.2f} s"}
+                         f"fwd+bwd float64, {dt:.2f} s",
+               "single_thread": {"value": w.T / dt1, "unit": UNIT, "cores": 1,
+                                 "sample": f"1 (b,h) stream at full T={w.T}, fwd+bwd float64, {dt1:.2f} s"}}
 
     # ---- timed region: windows of exactly K fwd+bwd steps, inputs resident in
     # HBM, each bracketed by a barrier and a synchronize; the value is the median
