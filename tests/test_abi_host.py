@@ -253,3 +253,33 @@ def test_count_nonfinite_rejects_bad_arguments(lib):
     assert h.gdn_count_nonfinite(None, 10, 1, c, None) == INVALID
     assert h.gdn_count_nonfinite(ctypes.c_void_p(FAKE + 8), 10, 1, c, None) == INVALID  # x misaligned
     assert h.gdn_count_nonfinite(None, 0, 1, c, None) == OK
+
+
+def _prologue(lib, p, bwd=False, **over):
+    """gdn_prologue_fwd / _bwd on fake, disjoint, 16-byte aligned addresses (1 GB apart)."""
+    h = lib.load_library()
+    names = (("q_raw", "k_raw", "a", "b", "dq", "dk", "dalpha", "dbeta", "dq_raw", "dk_raw", "da", "db") if bwd
+             else ("q_raw", "k_raw", "a", "b", "q", "k", "alpha", "beta"))
+    args = {n: FAKE + (i << 30) for i, n in enumerate(names)}
+    args.update(over)
+    fn = h.gdn_prologue_bwd if bwd else h.gdn_prologue_fwd
+    return fn(ctypes.byref(p), *[ctypes.c_void_p(args[n]) for n in names], ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+def test_prologue_arguments_rejected_before_launch(lib, bwd):
+    INVALID, UNSUP = 1, 2
+    ok = lib.make_problem(2, 5, 3, 64, 64, 64, 1)
+    assert _prologue(lib, ok, bwd, q_raw=None) == INVALID
+    assert "q_raw is NULL" in lib.gdn_last_error()
+    assert _prologue(lib, ok, bwd, k_raw=FAKE + (1 << 30) + 8) == INVALID  # misaligned
+    out = "dq_raw" if bwd else "q"
+    assert _prologue(lib, ok, bwd, **{out: FAKE}) == INVALID  # an output on an input
+    assert "overlaps" in lib.gdn_last_error()
+    assert _prologue(lib, lib.make_problem(2, 5, 3, 24, 24, 64, 1), bwd) == UNSUP
+    # no rows: every pointer may be NULL and nothing launches
+    empty = lib.make_problem(2, 0, 3, 64, 64, 64, 1)
+    names = 12 if bwd else 8
+    h = lib.load_library()
+    fn = h.gdn_prologue_bwd if bwd else h.gdn_prologue_fwd
+    assert fn(ctypes.byref(empty), *([ctypes.c_void_p(None)] * names), ctypes.c_void_p(None)) == 0
