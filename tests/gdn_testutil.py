@@ -86,8 +86,75 @@ def sample_gpu(out: dict, streams):
     return res
 
 
-def compare(got: dict, ref: dict, dtype: str, names=None):
-    """Returns {name: rel_l2} and raises AssertionError listing failures."""
+# Tensors compared block by block as well as whole: token tensors [B,T,H,D] per
+# (b, chunk of tokens, h); per-token gate gradients [B,T,H] and states [B,H,V,K]
+# per (b, h).  A whole-tensor norm hides damage confined to one chunk or row
+# (one wrong row of 128 values in a 6M-element o moves it by about 5e-3).
+TOKEN_TENSORS = ("o", "dq", "dk", "dv", "dq_raw", "dk_raw", "q", "k")
+GATE_TENSORS = ("dalpha", "dbeta", "da", "db", "alpha", "beta")
+STATE_TENSORS = ("final_state", "d_initial_state")
+LOCAL_FACTOR = 2.0   # a block may be this many times the whole-tensor tolerance
+LOCAL_FLOOR = 0.1    # blocks normalised by at least this fraction of the RMS block norm
+
+
+def block_errors(x, ref, name: str, chunk: int = 64):
+    """Per-block relative L2 errors of x against ref, or None if the tensor has no
+    block structure here.  Returns (errors, block shape description)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if x.shape != ref.shape:
+        return None
+    if name in TOKEN_TENSORS and x.ndim == 4:
+        B, T, H, _ = x.shape
+        if T == 0:
+            return None
+        d2 = ((x - ref) ** 2).sum(-1)            # [B, T, H]
+        r2 = (ref ** 2).sum(-1)
+        starts = np.arange(0, T, chunk)
+        d2 = np.add.reduceat(d2, starts, axis=1)  # [B, NC, H]
+        r2 = np.add.reduceat(r2, starts, axis=1)
+        what = "(b, chunk, h)"
+    elif name in GATE_TENSORS and x.ndim == 3:
+        d2 = ((x - ref) ** 2).sum(1)             # [B, H]
+        r2 = (ref ** 2).sum(1)
+        what = "(b, h)"
+    elif name in STATE_TENSORS and x.ndim == 4:
+        d2 = ((x - ref) ** 2).sum((2, 3))        # [B, H]
+        r2 = (ref ** 2).sum((2, 3))
+        what = "(b, h)"
+    else:
+        return None
+    if d2.size == 0:
+        return None
+    rms = np.sqrt(r2.sum() / r2.size)
+    den = np.maximum(np.sqrt(r2), LOCAL_FLOOR * rms)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        err = np.where(den > 0, np.sqrt(d2) / np.where(den > 0, den, 1.0), np.sqrt(d2))
+    return err, what
+
+
+def local_failure(x, ref, name: str, lim: float, chunk: int = 64, packed: bool = False):
+    """None if every block of x is within LOCAL_FACTOR * lim of ref, else a
+    message naming the worst block.  packed: x is one sequence of a packed batch
+    ([T, H, ...], no batch axis)."""
+    if packed:
+        x, ref = np.asarray(x)[None], np.asarray(ref)[None]
+    be = block_errors(x, ref, name, chunk)
+    if be is None:
+        return None
+    err, what = be
+    worst = np.unravel_index(int(np.argmax(np.where(np.isnan(err), np.inf, err))), err.shape)
+    w = float(err[worst])
+    if w <= LOCAL_FACTOR * lim:
+        return None
+    return f"{name}: block {what}={tuple(int(i) for i in worst)} rel_l2={w:.3e} > {LOCAL_FACTOR * lim:.0e}"
+
+
+def compare(got: dict, ref: dict, dtype: str, names=None, chunk: int = 64):
+    """Returns {name: rel_l2} and raises AssertionError listing failures: a tensor
+    whose whole-tensor relative L2 exceeds its tolerance, or any block (see
+    block_errors) whose relative L2 exceeds LOCAL_FACTOR times it; the worst
+    block's index is named."""
     tol = TOL[dtype]
     errs, bad = {}, []
     for n in (names or ref.keys()):
@@ -98,9 +165,12 @@ def compare(got: dict, ref: dict, dtype: str, names=None):
         lim = tol["out"] if n in ("o", "final_state") else tol["grad"]
         if not (e <= lim):
             bad.append(f"{n}: rel_l2={e:.3e} > {lim:.0e}")
+        msg = local_failure(got[n], ref[n], n, lim, chunk)
+        if msg:
+            bad.append(msg)
     assert not bad, "; ".join(bad) + f" (all: {errs})"
     return errs
 
 
-__all__ = ["TOL", "rel_l2", "gpu_run", "oracle_run", "compare", "custom", "make_inputs",
+__all__ = ["TOL", "rel_l2", "gpu_run", "oracle_run", "compare", "block_errors", "local_failure", "custom", "make_inputs",
            "sample_gpu", "select_streams", "select_states", "to_np"]

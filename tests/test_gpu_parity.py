@@ -33,7 +33,7 @@ def _check_workload(oracle_mod, w, streams=None):
     ref = oracle_run(oracle_mod, inp, backward=w.backward, streams=streams)
     if streams is not None:
         got = sample_gpu(got, streams)
-    return compare(got, ref, w.dtype)
+    return compare(got, ref, w.dtype, chunk=w.chunk)
 
 
 def test_tiny_fp32_fwd_bwd(oracle_mod):
@@ -90,7 +90,7 @@ def test_chunk_sizes(oracle_mod, C, dtype):
     w = custom(B=2, T=192, H=2, K=32, V=64, chunk=C, dtype=dtype, seed=10 + C, init_std=0.1,
                dfinal_std=0.01)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), dtype)
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), dtype, chunk=w.chunk)
 
 
 @pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 130])
@@ -98,7 +98,7 @@ def test_ragged_lengths_fp32(oracle_mod, T):
     w = custom(B=1, T=T, H=3, K=16, V=32, chunk=64, dtype="f32", seed=T, init_std=0.1,
                dfinal_std=0.1)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "f32")
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "f32", chunk=w.chunk)
 
 
 @pytest.mark.parametrize("K,V", [(64, 128), (128, 32), (16, 128), (128, 16)])
@@ -106,7 +106,7 @@ def test_key_value_dims_differ_bf16(oracle_mod, K, V):
     w = custom(B=1, T=200, H=2, K=K, V=V, chunk=64, dtype="bf16", seed=K + V, init_std=0.1,
                dfinal_std=0.01)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16")
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16", chunk=w.chunk)
 
 
 @pytest.mark.parametrize("seed", [100, 101, 102])
@@ -114,7 +114,7 @@ def test_seeds_fp32_full_heads(oracle_mod, seed):
     w = custom(B=2, T=96, H=2, K=128, V=128, chunk=32, dtype="f32", seed=seed, init_std=0.1,
                dfinal_std=0.1)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "f32")
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "f32", chunk=w.chunk)
 
 
 def test_backward_recompute_equals_saved():
@@ -173,7 +173,7 @@ def test_tc_path_ragged_lengths(oracle_mod, T):
     w = custom(B=2, T=T, H=3, K=128, V=128, chunk=64, dtype="bf16", seed=300 + T, init_std=0.1,
                dfinal_std=0.01)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16")
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16", chunk=w.chunk)
 
 
 def test_tc_path_many_streams_multiple_waves(oracle_mod):
@@ -206,7 +206,7 @@ def test_slow_decay_long_range(oracle_mod, dtype, K, V, C):
     w = custom(B=2, T=1000, H=2, K=K, V=V, chunk=C, dtype=dtype, seed=600 + K + C, init_std=0.3, dfinal_std=0.05,
                alpha_lo=0.97)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), dtype)
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), dtype, chunk=w.chunk)
 
 
 @pytest.mark.parametrize("B,H", [(7, 6), (5, 9)])
@@ -217,7 +217,7 @@ def test_tc_scan_48_column_slices(oracle_mod, B, H):
     w = custom(B=B, T=200, H=H, K=128, V=128, chunk=64, dtype="bf16", seed=650 + B * H, init_std=0.3,
                dfinal_std=0.05, alpha_lo=0.97)
     inp = make_inputs(w)
-    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16")
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16", chunk=w.chunk)
 
 
 def test_tc_error_flag_stays_clear():

@@ -12,7 +12,7 @@ import torch
 
 from gated_delta_rule_19_gb300 import gdn
 from gated_delta_rule_19_gb300.inputs import custom, make_inputs, make_varlen_inputs
-from gdn_testutil import TOL, rel_l2, to_np
+from gdn_testutil import TOL, local_failure, rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -101,9 +101,13 @@ def test_varlen_matches_oracle_per_sequence(oracle_mod, lengths, H, K, V, chunk,
             # per sequence where the sequence has enough elements for a relative
             # norm to mean something; the packed tensors are compared as a whole
             if e - a >= 16:
+                lim = tol["out" if n == "o" else "grad"]
                 err = rel_l2(to_np(got[n][a:e]), ref[n])
-                if err > tol["out" if n == "o" else "grad"]:
+                if err > lim:
                     bad.append(f"seq {s} {n}: {err:.2e}")
+                msg = local_failure(to_np(got[n][a:e]), ref[n], n, lim, chunk, packed=True)
+                if msg:
+                    bad.append(f"seq {s} {msg}")
     for n in ("o",) + GRADS:
         err = rel_l2(to_np(got[n]), np.concatenate(ref_all[n], 0))
         if err > tol["out" if n == "o" else "grad"]:
@@ -264,9 +268,13 @@ def test_varlen_bench_workload_sampled(oracle_mod):
         ref = _oracle_seq(oracle_mod, inp, s)
         a, e = cu[s], cu[s + 1]
         for n in ("o",) + GRADS:
+            lim = tol["out" if n == "o" else "grad"]
             err = rel_l2(to_np(got[n][a:e]), ref[n])
-            if err > tol["out" if n == "o" else "grad"]:
+            if err > lim:
                 bad.append(f"seq {s} (len {e - a}) {n}: {err:.2e}")
+            msg = local_failure(to_np(got[n][a:e]), ref[n], n, lim, 64, packed=True)
+            if msg:
+                bad.append(f"seq {s} {msg}")
         for n in ("final_state", "d_initial_state"):
             if got.get(n) is None:
                 continue
