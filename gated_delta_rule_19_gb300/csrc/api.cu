@@ -300,6 +300,9 @@ gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
         Carver sv{(char*)saved};
         carve_tc_saved(d, sv, &states, &tb);
     }
+    // Clears the error word and the persistent kernels' work counters.  gdn_fwd_noalloc
+    // depends on this: its scratch array keeps the previous call's contents, and
+    // these are the only scratch words read before the call writes them.
     cudaError_t e = cudaMemsetAsync(tb.err, 0, gdn::kErrWords * sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
     e = timed(gdn::KID_PREP_TC, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });

@@ -13,13 +13,18 @@
 // The array is GDN_FWD_NOALLOC_SCRATCH_BYTES (32 MiB) on every device that loads
 // the library, held until the process exits.  Problems whose forward scratch
 // (gdn_fwd_workspace_bytes) is larger are rejected before anything is enqueued.
-// The first call on a device looks up the array's device address with
+// The array used is the current device's: the current device must be the one
+// that holds the tensors and runs the stream (checked against q).  The first
+// call on a device looks up the array's device address with
 // cudaGetSymbolAddress (with that device current); make that first call outside
 // any stream capture.  Every call on a device shares the one array, so calls
 // that overlap on the GPU (for example on two streams) race: order them on one
-// stream.  The kernels write every scratch element before reading it within a
-// call, so what an earlier call left there never matters and nothing needs to
-// be cleared.
+// stream.  The array keeps what the previous call left.  Two parts of the
+// scratch are read before a call writes them: the tensor-core path's error word
+// and the work counters of its persistent kernels, at the start of the scratch.
+// gdn_fwd clears both with a cudaMemsetAsync on the call's stream at the start
+// of every tensor-core forward (run_fwd_tc), and that clear is what makes the
+// reuse safe; every other scratch element is written before it is read.
 
 #include <cuda_runtime.h>
 
@@ -89,6 +94,23 @@ extern "C" gdn_status gdn_fwd_noalloc(const gdn_problem* p, const void* q, const
                  need, (size_t)GDN_FWD_NOALLOC_SCRATCH_BYTES);
         gdn::set_last_error(msg);
         return GDN_ERR_UNSUPPORTED;
+    }
+    // the array of the current device: q must live there
+    int dev = -1;
+    cudaPointerAttributes attr;
+    bool known = false;
+    if (q && cudaGetDevice(&dev) == cudaSuccess) {
+        known = cudaPointerGetAttributes(&attr, q) == cudaSuccess;
+        if (!known) cudaGetLastError();  // a failed query must not be reported by a later launch
+    }
+    if (known && attr.type == cudaMemoryTypeDevice && attr.device != dev) {
+        char msg[256];
+        snprintf(msg, sizeof(msg),
+                 "gdn_fwd_noalloc: q is on device %d but device %d is current; make the tensors' device "
+                 "current before the call",
+                 attr.device, dev);
+        gdn::set_last_error(msg);
+        return GDN_ERR_INVALID_ARG;
     }
     void* scratch = nullptr;
     gdn_status st = scratch_address(&scratch);

@@ -634,6 +634,10 @@ def gdn_decode(q, k, v, alpha, beta, state, *, o=None, stream=None):
     return o, state
 
 
+# Size of the fixed scratch array gdn_fwd_noalloc runs on (GDN_FWD_NOALLOC_SCRATCH_BYTES).
+GDN_FWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
 def gdn_fwd_noalloc(q, k, v, alpha, beta, initial_state, o, final_state=None, *,
                     chunk: int = 64, stream=None):
     """Forward through ``gdn_fwd_noalloc``: the same result as :func:`gdn_fwd`,
@@ -661,8 +665,9 @@ def gdn_fwd_noalloc(q, k, v, alpha, beta, initial_state, o, final_state=None, *,
         _need(t, n, s, dt, dev)
     _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
     _need(final_state, "final_state", (B, H, V, K), torch.float32, dev)
-    st = lib.gdn_fwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
-                             _ptr(beta), _ptr(initial_state), _ptr(o), _ptr(final_state),
-                             _stream_handle(dev, stream))
+    with torch.cuda.device(dev):  # the library uses the current device's array
+        st = lib.gdn_fwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                 _ptr(beta), _ptr(initial_state), _ptr(o), _ptr(final_state),
+                                 _stream_handle(dev, stream))
     _check(st)
     return o, final_state

@@ -142,13 +142,18 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
  *   - Problems whose gdn_fwd_workspace_bytes(p) exceeds that size are rejected
  *     with GDN_ERR_UNSUPPORTED before anything is enqueued (e.g. K=V=128,
  *     chunk 64 needs 80.25 KiB per (b, h, chunk), so B*H*ceil(T/64) <= 408).
+ *   - The array used is the current device's: make the device that holds the
+ *     tensors and runs `stream` current before the call.  A q on another
+ *     device is rejected with GDN_ERR_INVALID_ARG.
  *   - The first call on a device looks up the array's address there
- *     (cudaGetSymbolAddress, with the stream's device current): make that
- *     first call outside any stream capture.
+ *     (cudaGetSymbolAddress, with that device current): make that first call
+ *     outside any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; calls that overlap on the GPU (e.g. on two streams) race and
- *     corrupt each other's results, so order them on one stream.  Each call
- *     writes every scratch element before reading it, so nothing is cleared.
+ *     corrupt each other's results, so order them on one stream.  The only
+ *     scratch words a call reads before writing them (the tensor-core path's
+ *     error word and work counters) are cleared by a cudaMemsetAsync at the
+ *     start of each call; everything else is written before it is read.
  * Arguments are those of gdn_fwd without saved/workspace; `o` is required.
  */
 #define GDN_FWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

@@ -3,16 +3,20 @@
 cudaMalloc's device-wide synchronisation is not acceptable).  Its scratch is a
 fixed array inside the library instead of a caller-owned workspace.
 
-The test calls it through the C ABI twice in a row, on two different problems
-(so the second call runs on the scratch the first left behind), and checks each
-result against the ordinary gdn_fwd within the parity tolerance.  This file is
-named so that pytest collects it last."""
+The tests call it through the C ABI several times in a row on different
+problems, so every call after the first runs on the scratch an earlier call left
+behind: first the CUDA-core kernels (fp32 K=V=64, then fp32 K=128/V=32, chunk
+32), then the tensor-core kernels, which keep an error word and the work
+counters of their persistent kernels in the scratch (bf16 K=V=128, chunk 64:
+one problem with the within-call sequence split, one with a ragged tail chunk).
+The same kernels on the same inputs must give the same bits as gdn_fwd with its
+own workspace, so results are compared with torch.equal.  This file is named so
+that pytest collects it last."""
 import pytest
 import torch
 
 from gated_delta_rule_19_gb300 import gdn
 from gated_delta_rule_19_gb300.inputs import custom, make_inputs
-from gdn_testutil import TOL, rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -21,6 +25,9 @@ def _run_pair(w):
     from gated_delta_rule_19_gb300 import _build
 
     _build.build()
+    p = gdn.make_problem(w.B, w.T, w.H, w.K, w.V, w.chunk,
+                         torch.bfloat16 if w.dtype == "bf16" else torch.float32)
+    assert 0 < gdn.gdn_fwd_workspace_bytes(p) <= gdn.GDN_FWD_NOALLOC_SCRATCH_BYTES
     inp = make_inputs(w)
     d = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
     args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"])
@@ -29,18 +36,22 @@ def _run_pair(w):
     s = torch.full_like(s_ref, float("nan"))
     gdn.gdn_fwd_noalloc(*args, o, s, chunk=w.chunk)
     torch.cuda.synchronize()
-    tol = TOL[w.dtype]["out"]
-    assert rel_l2(to_np(o), to_np(o_ref)) <= tol
-    assert rel_l2(to_np(s), to_np(s_ref)) <= tol
+    assert torch.equal(o, o_ref)
+    assert torch.equal(s, s_ref)
 
 
-def test_fwd_noalloc_matches_fwd_two_calls_in_a_row():
+def test_fwd_noalloc_matches_fwd_calls_in_a_row():
     assert torch.cuda.is_available()
-    # first call: bf16, K=V=64, 128 chunks of scratch
-    _run_pair(custom(B=2, T=1024, H=4, K=64, V=64, chunk=64, dtype="bf16", seed=21,
+    # CUDA-core kernels: fp32 K=V=64 (128 chunks of scratch), then fp32 K=128/V=32
+    _run_pair(custom(B=2, T=1024, H=4, K=64, V=64, chunk=64, dtype="f32", seed=21,
                      init_std=0.1))
-    # second call: another shape and dtype on the scratch the first call left
     _run_pair(custom(B=1, T=300, H=3, K=128, V=32, chunk=32, dtype="f32", seed=22,
+                     init_std=0.1))
+    # tensor-core kernels on the scratch the CUDA-core calls left: four streams of
+    # 64 chunks (the within-call sequence split runs), then a ragged tail chunk
+    _run_pair(custom(B=1, T=4096, H=4, K=128, V=128, chunk=64, dtype="bf16", seed=23,
+                     init_std=0.1))
+    _run_pair(custom(B=2, T=2000, H=3, K=128, V=128, chunk=64, dtype="bf16", seed=24,
                      init_std=0.1))
 
 
