@@ -256,7 +256,9 @@ def path_roofline(w, peaks, ms, fwd_ms):
     does 2C(3K+2V)+6KV flops and moves 2(2K+2V)+4 bytes at bf16 (es(2K+2V)+2es in
     general); the backward 14KV+10CV+18CK+4C^2 flops and es(4K+3V)+4es bytes (reads
     q,k,v,dO,alpha,beta; writes dq,dk,dv,dalpha,dbeta).  The bound time is the larger
-    of flops / sustained bf16 peak and bytes / HBM copy bandwidth."""
+    of flops / burst bf16 peak and bytes / HBM copy bandwidth (the step is timed in
+    windows of about 10 ms, not in a seconds-long loop, so the burst figure is the
+    one that applies)."""
     C, K, V = w.chunk, w.K, w.V
     es = 2 if w.dtype == "bf16" else 4
     f_fwd = 2 * C * (3 * K + 2 * V) + 6 * K * V
@@ -265,12 +267,12 @@ def path_roofline(w, peaks, ms, fwd_ms):
     b_bwd = es * (4 * K + 3 * V) + 4 * es
     n = w.token_heads
     def bound_ms(f, b):
-        return 1e3 * max(f * n / (peaks["bf16_tflops_sustained"] * 1e12), b * n / (peaks["hbm_gbs"] * 1e9))
+        return 1e3 * max(f * n / (peaks["bf16_tflops"] * 1e12), b * n / (peaks["hbm_gbs"] * 1e9))
     step_ms = bound_ms(f_fwd + f_bwd, b_fwd + b_bwd)
     fwd_bound = bound_ms(f_fwd, b_fwd)
     return {"bound_ms": step_ms, "frac": step_ms / ms, "fwd_bound_ms": fwd_bound,
             "fwd_frac": fwd_bound / fwd_ms if fwd_ms else None,
-            "tc_peak_frac": (f_fwd + f_bwd) * n / (ms / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12),
+            "tc_peak_frac": (f_fwd + f_bwd) * n / (ms / 1e3) / (peaks["bf16_tflops"] * 1e12),
             "per_token_head": {"fwd_flops": f_fwd, "bwd_flops": f_bwd, "fwd_bytes": b_fwd, "bwd_bytes": b_bwd}}
 
 
@@ -302,23 +304,32 @@ def source_hash():
 
 
 def roofline(summary, w, peaks):
+    """One row per kernel: achieved = its algorithmic flops (or bytes) per launch
+    / its average launch time, against the burst bf16 peak (each kernel is timed
+    in windows of about 10 ms, not a seconds-long loop) or the HBM copy rate,
+    whichever bound is larger for its counts.  traffic_ratio = the DRAM bytes ncu
+    counted per launch / the kernel's algorithmic bytes per launch (its own
+    inputs and outputs of the path); well above 1 means scratch and re-reads."""
     units = w.token_heads
     rows = []
     for name, (n, ms) in summary.items():
         flops, byts = kernel_work(name, w)
         avg_s = ms / n / 1e3
-        t_f = flops * units / (peaks["bf16_tflops_sustained"] * 1e12)
+        t_f = flops * units / (peaks["bf16_tflops"] * 1e12)
         t_b = byts * units / (peaks["hbm_gbs"] * 1e9)
         if t_f >= t_b:
             ach = flops * units / avg_s / 1e12
-            row = dict(bound="tensor", achieved=ach, peak=peaks["bf16_tflops_sustained"],
+            row = dict(bound="tensor", achieved=ach, peak=peaks["bf16_tflops"],
                        unit="TFLOP/s")
         else:
             ach = byts * units / avg_s / 1e9
             row = dict(bound="hbm", achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s")
+        traffic = traffic_for(name)
+        alg_bytes = byts * units
         row.update(frac=row["achieved"] / row["peak"], kernel=name, launches=n,
-                   avg_ms=ms / n, share=0.0, traffic=traffic_for(name),
-                   peak_source=peaks["source"] + (" sustained bf16" if row["bound"] == "tensor"
+                   avg_ms=ms / n, share=0.0, traffic=traffic, algorithmic_bytes=alg_bytes,
+                   traffic_ratio=(traffic / alg_bytes) if (traffic and alg_bytes) else None,
+                   peak_source=peaks["source"] + (" burst bf16" if row["bound"] == "tensor"
                                                   else " hbm copy"))
         rows.append(row)
     tot = sum(r["avg_ms"] * r["launches"] for r in rows) or 1.0
@@ -833,7 +844,16 @@ def run_gdn(args, world, rank, local):
     dom = rows[0]
     rl = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     rl.update(kernel=dom["kernel"], avg_ms=dom["avg_ms"], share=dom["share"],
-              peak_source=dom["peak_source"])
+              peak_source=dom["peak_source"], traffic_ratio=dom["traffic_ratio"])
+    # the whole step's DRAM traffic (ncu, summed over its kernels) against the
+    # bytes the path itself must move
+    tr = [r["traffic"] for r in rows]
+    pr_step = path_roofline(w, peaks, ms_max, fwd_ms)
+    alg_step = (pr_step["per_token_head"]["fwd_bytes"] + pr_step["per_token_head"]["bwd_bytes"]) * w.token_heads
+    step_traffic = sum(tr) if tr and all(t is not None for t in tr) else None
+    pr_step["traffic"] = step_traffic
+    pr_step["algorithmic_bytes"] = alg_step
+    pr_step["traffic_ratio"] = (step_traffic / alg_step) if step_traffic else None
     value = world * w.token_heads / (ms_max / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -850,9 +870,9 @@ def run_gdn(args, world, rank, local):
         "fwd": {"value": world * w.token_heads / (fwd_ms / 1e3), "unit": UNIT,
                 "ms_per_step": fwd_ms},
         "roofline": rl,
-        "path_roofline": path_roofline(w, peaks, ms_max, fwd_ms),
+        "path_roofline": pr_step,
         "kernels": [{k: r[k] for k in ("kernel", "launches", "avg_ms", "share", "bound",
-                                       "achieved", "unit", "frac")} for r in rows],
+                                       "achieved", "unit", "frac", "traffic", "traffic_ratio")} for r in rows],
         "cpu_baseline": cpu,
         "parity_sampled": parity,
         "e2e": e2e,
