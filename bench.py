@@ -384,6 +384,92 @@ def measure_prologue(gdn, dev, stream, args, world, w):
             "max_unit_norm_error": norm_err}
 
 
+def measure_raw(gdn, dev, stream, args, world, w):
+    """The training step with its prologue on the training shape, two ways, from
+    raw q/k rows and gate logits (q_raw, k_raw ~ N(0, 3^2), logits ~ N(0, 2^2)):
+    folded into the kernels (gdn_fwd_raw(saved) + gdn_bwd_raw), and as separate
+    passes (gdn_prologue_fwd, gdn_fwd(saved), gdn_bwd, gdn_prologue_bwd).  Both
+    compute the same function; the check compares their outputs and raw-input
+    gradients (relative L2, they differ only in where alpha and beta are
+    rounded), and the oracle chain checks both in the tests."""
+    from gated_delta_rule_19_gb300.inputs import make_prologue_inputs
+
+    x = {n: t.to(dev) for n, t in make_prologue_inputs(w.B, w.T, w.H, w.K, w.dtype, seed=w.seed).items()}
+    r = make_inputs(w)
+    v, do = r["v"].to(dev), r["d_o"].to(dev)
+    s0 = r["initial_state"].to(dev) if r["initial_state"] is not None else None
+    dsT = r["d_final_state"].to(dev) if r["d_final_state"] is not None else None
+    raw_in = (x["q_raw"], x["k_raw"], v, x["a_logit"], x["b_logit"], s0)
+    p = gdn.make_problem(w.B, w.T, w.H, w.K, w.V, w.chunk, x["q_raw"].dtype)
+    sv_raw = torch.empty(gdn.gdn_raw_saved_bytes(p), dtype=torch.uint8, device=dev)
+    ws_raw = torch.empty(max(gdn.gdn_raw_fwd_workspace_bytes(p), gdn.gdn_raw_bwd_workspace_bytes(p)),
+                         dtype=torch.uint8, device=dev)
+    sv = torch.empty(gdn.gdn_saved_bytes(p), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(gdn.gdn_fwd_workspace_bytes(p), gdn.gdn_bwd_workspace_bytes(p)), dtype=torch.uint8,
+                     device=dev)
+    o1 = torch.empty_like(v)
+    g1 = tuple(torch.empty_like(t) for t in (x["q_raw"], x["k_raw"], v, x["a_logit"], x["b_logit"]))
+
+    def folded():
+        o, _, _ = gdn.gdn_fwd_raw(*raw_in, chunk=w.chunk, o=o1, final_state=False, saved=sv_raw, workspace=ws_raw)
+        return (o,) + gdn.gdn_bwd_raw(*raw_in, do, dsT, saved=sv_raw, chunk=w.chunk, grads=g1,
+                                      d_initial_state=False, workspace=ws_raw)[:5]
+
+    pro_f = tuple(torch.empty_like(t) for t in (x["q_raw"], x["k_raw"], x["a_logit"], x["b_logit"]))
+    pro_b = tuple(torch.empty_like(t) for t in (x["q_raw"], x["k_raw"], x["a_logit"], x["b_logit"]))
+    o2 = torch.empty_like(v)
+    g2 = tuple(torch.empty_like(t) for t in (x["q_raw"], x["k_raw"], v, x["a_logit"], x["b_logit"]))
+
+    def separate():
+        q, k, al, be = gdn.gdn_prologue_fwd(x["q_raw"], x["k_raw"], x["a_logit"], x["b_logit"], out=pro_f)
+        o, _, _ = gdn.gdn_fwd(q, k, v, al, be, s0, chunk=w.chunk, o=o2, final_state=False, saved=sv, workspace=ws)
+        dq, dk, dv, da, db, _ = gdn.gdn_bwd(q, k, v, al, be, s0, do, dsT, saved=sv, chunk=w.chunk, grads=g2,
+                                            d_initial_state=False, workspace=ws)
+        dqr, dkr, dar, dbr = gdn.gdn_prologue_bwd(x["q_raw"], x["k_raw"], x["a_logit"], x["b_logit"], dq, dk, da,
+                                                  db, out=pro_b)
+        return (o, dqr, dkr, dv, dar, dbr)
+
+    a, b = folded(), separate()
+    torch.cuda.synchronize(dev)
+    rel = lambda u, t: float((u.float() - t.float()).norm() / t.float().norm())
+    names = ("o", "dq_raw", "dk_raw", "dv", "da_logit", "db_logit")
+    agree = {n: rel(u, t) for n, u, t in zip(names, a, b)}
+
+    def timed(fn, n):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+
+    n = max(20, args.steps)
+    f_ms = timed(folded, n)
+    s_ms = timed(separate, n)
+
+    def split_of(fn, reps=5):  # the per-kernel split, outside the timed loops
+        gdn.gdn_profiler_start(32 * reps + 32)
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        gdn.gdn_profiler_stop()
+        return {k: round(t / reps * 1e3, 1) for k, (_, t) in gdn.gdn_profiler_summary().items()}
+
+    f_split, s_split = split_of(folded), split_of(separate)
+    return {"workload": w.name, "inputs": "raw q/k ~ N(0, 3^2), gate logits ~ N(0, 2^2)",
+            "folded": {"step": "gdn_fwd_raw(saved) + gdn_bwd_raw", "ms_per_step": f_ms,
+                       "token_heads_per_s": w.token_heads / (f_ms / 1e3), "us_per_step_by_kernel": f_split},
+            "separate": {"step": "gdn_prologue_fwd + gdn_fwd(saved) + gdn_bwd + gdn_prologue_bwd",
+                         "ms_per_step": s_ms, "token_heads_per_s": w.token_heads / (s_ms / 1e3),
+                         "us_per_step_by_kernel": s_split},
+            "speedup": s_ms / f_ms, "rel_l2_folded_vs_separate": agree}
+
+
 def measure_decode(gdn, dev, stream, args, world):
     """Times gdn_decode on the decode workload (256 sequences x 16 heads, one
     token, K=V=128 bf16): its 256 MB fp32 state is read and written once per
@@ -833,6 +919,7 @@ def run_gdn(args, world, rank, local):
     # carried in place between calls
     decode = None if args.no_decode else measure_decode(gdn, dev, stream, args, world)
     prologue = None if args.no_decode else measure_prologue(gdn, dev, stream, args, world, w)
+    raw = None if args.no_decode else measure_raw(gdn, dev, stream, args, world, w)
     varlen = None if args.no_decode else measure_varlen(gdn, dev, stream, args, world, ms_max, w.token_heads)
     split = None if args.no_decode else measure_split(gdn, dev, stream, args, world)
     configs = None if args.no_decode else measure_configs(gdn, dev, stream, args, world)
@@ -878,6 +965,7 @@ def run_gdn(args, world, rank, local):
         "e2e": e2e,
         "decode": decode,
         "prologue": prologue,
+        "prologue_folded": raw,
         "varlen": varlen,
         "sequence_split": split,
         "configs": configs,

@@ -84,13 +84,18 @@ size_t carve_chunk(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, bool with
     return cv.off;
 }
 
+// The tensor-core kernels keep K and V at 128 in their own buffers: a problem with
+// K or V = 64 is read through TMA boxes that fill the missing columns with zeros,
+// and every internal row is 128 wide (its extra columns hold zeros).
+constexpr size_t kTcD = 128;
+
 // Chunk results of the tensor-core path.  err is carved separately (it always
 // lives in the workspace, even when the chunk results live in `saved`).
 size_t carve_tc_chunk(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with_T) {
     const size_t rows = (size_t)d.NS() * d.NC * d.C;
     tb->G = cv.take<float>(rows);
-    tb->W = cv.take<__nv_bfloat16>(rows * d.K);
-    tb->Ut = cv.take<__nv_bfloat16>(rows * d.V);
+    tb->W = cv.take<__nv_bfloat16>(rows * kTcD);
+    tb->Ut = cv.take<__nv_bfloat16>(rows * kTcD);
     tb->Mqk = cv.take<__nv_bfloat16>(rows * d.C);
     tb->T = with_T ? cv.take<__nv_bfloat16>(rows * d.C) : nullptr;
     return cv.off;
@@ -99,7 +104,7 @@ size_t carve_tc_chunk(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with
 // `saved` of the tensor-core path: bf16 chunk-start states [chunks*K, V] followed
 // by the forward's chunk results (reused by the backward instead of recomputed).
 size_t carve_tc_saved(const gdn::Dims& d, Carver& cv, __nv_bfloat16** states, gdn::TcBufs* tb) {
-    *states = cv.take<__nv_bfloat16>((size_t)d.NS() * d.NC * d.K * d.V);
+    *states = cv.take<__nv_bfloat16>((size_t)d.NS() * d.NC * kTcD * kTcD);
     return carve_tc_chunk(d, cv, tb, true);
 }
 
@@ -107,8 +112,8 @@ size_t carve_tc(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, bool with_T = f
     const size_t rows = (size_t)d.NS() * d.NC * d.C;
     tb->err = cv.take<int>(64);
     tb->G = cv.take<float>(rows);
-    tb->W = cv.take<__nv_bfloat16>(rows * d.K);
-    tb->Ut = cv.take<__nv_bfloat16>(rows * d.V);
+    tb->W = cv.take<__nv_bfloat16>(rows * kTcD);
+    tb->Ut = cv.take<__nv_bfloat16>(rows * kTcD);
     tb->Mqk = cv.take<__nv_bfloat16>(rows * d.C);
     tb->T = with_T ? cv.take<__nv_bfloat16>(rows * d.C) : nullptr;
     return cv.off;
@@ -124,12 +129,12 @@ size_t carve_tc_bwd(const gdn::Dims& d, Carver& cv, gdn::TcBufs* tb, gdn::TcBwdB
     const bool need_states = need_recompute;
     const size_t nchunks = (size_t)d.NS() * d.NC;
     const size_t rows = nchunks * d.C;
-    bb->dU = cv.take<__nv_bfloat16>(rows * d.V);
-    bb->dS1 = cv.take<__nv_bfloat16>(nchunks * d.K * d.V);
-    bb->dKp = cv.take<__nv_bfloat16>(nchunks * d.K * d.C);
-    bb->dWt = cv.take<__nv_bfloat16>(nchunks * d.K * d.C);
+    bb->dU = cv.take<__nv_bfloat16>(rows * kTcD);
+    bb->dS1 = cv.take<__nv_bfloat16>(nchunks * kTcD * kTcD);
+    bb->dKp = cv.take<__nv_bfloat16>(nchunks * kTcD * d.C);
+    bb->dWt = cv.take<__nv_bfloat16>(nchunks * kTcD * d.C);
     bb->dGp = cv.take<float>(rows);
-    bb->states = need_states ? cv.take<__nv_bfloat16>(nchunks * d.K * d.V) : nullptr;
+    bb->states = need_states ? cv.take<__nv_bfloat16>(nchunks * kTcD * kTcD) : nullptr;
     return cv.off;
 }
 
@@ -274,6 +279,7 @@ SplitCfg dense_split(const gdn::Dims& d, gdn::Dims* fd) {
     *fd = d;
     SplitCfg sp;
     if (d.B != 1 && d.T % d.C != 0) return sp;
+    if (d.K != 128 || d.V != 128) return sp;  // the transitions are 128 x 128 maps
     const int P = split_pieces(d.NS(), d.NC, true);
     if (P < 2) return sp;
     fd->B = 1;
@@ -289,9 +295,18 @@ SplitCfg dense_split(const gdn::Dims& d, gdn::Dims* fd) {
 // workspace holds carve_tc(d) (then carve_split with a split) and `saved` (or
 // NULL) carve_tc_saved(d); `sq` (or NULL) runs packed sequences on the flat
 // chunk layout; `sp` (or NULL, or P = 1) splits every sequence into pieces.
+// With `raw` (gdn_fwd_raw), q, k are the raw rows and alpha, beta the gate logits:
+// the chunk kernel normalises q, k into raw->qn, raw->kn, which the scans read.
 gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* alpha,
                       const void* beta, const float* initial_state, void* o, float* final_state, void* saved,
-                      void* workspace, const gdn::SeqMap* sq, const SplitCfg* sp, cudaStream_t cs) {
+                      void* workspace, const gdn::SeqMap* sq, const SplitCfg* sp, cudaStream_t cs,
+                      const gdn::RawPrologue* raw = nullptr) {
+    const void* qp = q;  // the rows the chunk kernel reads
+    const void* kp = k;
+    if (raw && raw->on) {  // the scans read the normalised rows
+        q = raw->qn;
+        k = raw->kn;
+    }
     Carver cv{(char*)workspace};
     gdn::TcBufs tb;
     __nv_bfloat16* states = nullptr;
@@ -305,7 +320,7 @@ gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
     // these are the only scratch words read before the call writes them.
     cudaError_t e = cudaMemsetAsync(tb.err, 0, gdn::kErrWords * sizeof(int), cs);
     if (e != cudaSuccess) return cuda_fail(e, "error-flag reset");
-    e = timed(gdn::KID_PREP_TC, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
+    e = timed(gdn::KID_PREP_TC, cs, [&] { return gdn::launch_prep_tc(d, qp, kp, v, alpha, beta, tb, cs, raw); });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
     if (!sp || sp->P < 2) {
         e = timed(gdn::KID_SCAN_FWD_TC, cs, [&] {
@@ -340,11 +355,21 @@ gdn_status run_fwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
 
 // The tensor-core backward on dims d (same conventions as run_fwd_tc; the
 // workspace holds carve_tc_bwd(d), then carve_split with a split).
+// With `raw` (gdn_bwd_raw), q, k are the raw rows and alpha, beta the gate logits;
+// raw->qn, kn, rq, rk hold the normalised rows and reciprocal norms (written by
+// the forward into `saved`, or here by the chunk kernel when `saved` is NULL), and
+// dq, dk, dalpha, dbeta receive the gradients of the raw inputs.
 gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* alpha,
                       const void* beta, const float* initial_state, const void* saved, const void* d_o,
                       const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
                       float* d_initial_state, void* workspace, const gdn::SeqMap* sq, const SplitCfg* sp,
-                      cudaStream_t cs) {
+                      cudaStream_t cs, const gdn::RawPrologue* raw = nullptr) {
+    const void* qp = q;  // the rows the chunk kernel reads
+    const void* kp = k;
+    if (raw && raw->on) {
+        q = raw->qn;
+        k = raw->kn;
+    }
     Carver cv{(char*)workspace};
     gdn::TcBufs tb;
     gdn::TcBwdBufs tbb;
@@ -371,7 +396,7 @@ gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
         if (e != cudaSuccess) return cuda_fail(e, "split pieces");
     }
     if (!saved) {
-        e = timed(gdn::KID_PREP_TC_BWD, cs, [&] { return gdn::launch_prep_tc(d, q, k, v, alpha, beta, tb, cs); });
+        e = timed(gdn::KID_PREP_TC_BWD, cs, [&] { return gdn::launch_prep_tc(d, qp, kp, v, alpha, beta, tb, cs, raw); });
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core chunk kernel");
         if (!split) {
             e = timed(gdn::KID_STATE_TC, cs, [&] {
@@ -422,10 +447,10 @@ gdn_status run_bwd_tc(const gdn::Dims& d, const void* q, const void* k, const vo
             });
     }
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core reverse scan");
-    e = timed(gdn::KID_GRAD_QK_TC, cs, [&] { return gdn::launch_grad_qk_tc(d, q, k, d_o, tb, states, tbb, dq, cs); });
+    e = timed(gdn::KID_GRAD_QK_TC, cs, [&] { return gdn::launch_grad_qk_tc(d, q, k, d_o, tb, states, tbb, dq, cs, raw); });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (q, k)");
     e = timed(gdn::KID_GRAD_WY_TC, cs, [&] {
-        return gdn::launch_grad_wy_tc(d, k, v, alpha, beta, tb, tbb, dk, dv, dalpha, dbeta, cs);
+        return gdn::launch_grad_wy_tc(d, k, v, alpha, beta, tb, tbb, dk, dv, dalpha, dbeta, cs, raw);
     });
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core gradient kernel (WY)");
     return GDN_OK;
@@ -608,7 +633,7 @@ gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan
     const size_t BTH = (size_t)q.B * q.T * q.H;
     size_t inner_bytes = 0;
     Carver cv{nullptr};
-    L->pieces = L->flat ? split_pieces((int64_t)d.B * d.H, 0, false) : 1;
+    L->pieces = (L->flat && d.K == 128 && d.V == 128) ? split_pieces((int64_t)d.B * d.H, 0, false) : 1;
     if (q.NS() * q.NC > 0) {
         if (L->flat) {
             gdn::TcBufs tb;
@@ -1098,6 +1123,402 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
     });
     if (e != cudaSuccess) return cuda_fail(e, "chunk gradient kernel");
     return GDN_OK;
+}
+
+// ------------------------------------------------ the recurrence with its prologue
+
+}  // extern "C"
+
+namespace {
+
+// The normalised rows and reciprocal norms of the raw path on the tensor-core
+// kernels (q, k bf16 [B,T,H,K]; 1/|q_raw|, 1/|k_raw| fp32 [B,T,H]).
+size_t carve_raw(const gdn::Dims& d, Carver& cv, gdn::RawPrologue* rp) {
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    rp->on = 1;
+    rp->qn = cv.take<__nv_bfloat16>(BTH * d.K);
+    rp->kn = cv.take<__nv_bfloat16>(BTH * d.K);
+    rp->rq = cv.take<float>(BTH);
+    rp->rk = cv.take<float>(BTH);
+    return cv.off;
+}
+
+// The composed raw path (shapes outside the tensor-core kernels): the prologue's
+// outputs and, for the backward, the gradients of the recurrence's inputs, all
+// in the run dtype.
+struct ComposedBufs {
+    void *qn, *kn, *al, *be, *dqn, *dkn, *dal, *dbe;
+};
+size_t carve_composed(const gdn::Dims& d, size_t es, Carver& cv, ComposedBufs* c, bool bwd) {
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    *c = ComposedBufs{};
+    c->qn = cv.take<char>(BTH * d.K * es);
+    c->kn = cv.take<char>(BTH * d.K * es);
+    c->al = cv.take<char>(BTH * es);
+    c->be = cv.take<char>(BTH * es);
+    if (bwd) {
+        c->dqn = cv.take<char>(BTH * d.K * es);
+        c->dkn = cv.take<char>(BTH * d.K * es);
+        c->dal = cv.take<char>(BTH * es);
+        c->dbe = cv.take<char>(BTH * es);
+    }
+    return cv.off;
+}
+
+// Bytes in front of the ordinary workspace in a raw call's workspace.
+size_t raw_prefix(const gdn_problem* p, const gdn::Dims& d, bool bwd) {
+    Carver cv{nullptr};
+    if (gdn::tc_fwd_supported(d, in_type(p))) {
+        gdn::RawPrologue rp;
+        return carve_raw(d, cv, &rp);
+    }
+    ComposedBufs c;
+    return carve_composed(d, p->dtype == GDN_BF16 ? 2 : 4, cv, &c, bwd);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_raw_saved_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    if (!gdn::tc_fwd_supported(d, in_type(p))) return gdn_saved_bytes(p);
+    Carver cv{nullptr};
+    gdn::RawPrologue rp;
+    carve_raw(d, cv, &rp);
+    return cv.off + gdn_saved_bytes(p);
+}
+
+size_t gdn_raw_fwd_workspace_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK || d.NS() * d.NC == 0) return 0;
+    return raw_prefix(p, d, false) + gdn_fwd_workspace_bytes(p);
+}
+
+size_t gdn_raw_bwd_workspace_bytes(const gdn_problem* p) {
+    gdn::Dims d{};
+    if (check_problem(p, &d) != GDN_OK || d.NS() * d.NC == 0) return 0;
+    return raw_prefix(p, d, true) + gdn_bwd_workspace_bytes(p);
+}
+
+gdn_status gdn_fwd_raw(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* v,
+                       const void* a_logit, const void* b_logit, const float* initial_state, void* o,
+                       float* final_state, void* saved, void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (d.NS() * d.NC == 0)  // nothing to normalise: the state passes through
+        return gdn_fwd(p, q_raw, k_raw, v, a_logit, b_logit, initial_state, o, final_state, nullptr, nullptr, 0,
+                       stream);
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const size_t need = gdn_raw_fwd_workspace_bytes(p);
+    const Span ins[] = {{q_raw, BTH * d.K * es, "q_raw"},     {k_raw, BTH * d.K * es, "k_raw"},
+                        {v, BTH * d.V * es, "v"},             {a_logit, BTH * es, "a_logit"},
+                        {b_logit, BTH * es, "b_logit"},       {initial_state, nstate, "initial_state"}};
+    const Span outs[] = {{o, BTH * d.V * es, "o"},
+                         {final_state, nstate, "final_state"},
+                         {saved, gdn_raw_saved_bytes(p), "saved"},
+                         {workspace, need, "workspace"}};
+    for (int i = 0; i < 6; ++i)
+        if ((st = check_ptr(ins[i], i != 5)) != GDN_OK) return st;
+    for (int i = 0; i < 4; ++i)
+        if ((st = check_ptr(outs[i], i == 0 || i == 3)) != GDN_OK) return st;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    if ((st = check_overlaps(ins, 6, outs, 4, final_state, initial_state)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const gdn::InType ty = in_type(p);
+    const size_t pre = raw_prefix(p, d, false);
+    char* ws = (char*)workspace + pre;
+    if (gdn::tc_fwd_supported(d, ty)) {
+        gdn::RawPrologue rp;
+        Carver cv{(char*)(saved ? saved : workspace)};
+        carve_raw(d, cv, &rp);
+        void* tc_saved = saved ? (char*)saved + cv.off : nullptr;
+        gdn::Dims fd;
+        const SplitCfg sp = dense_split(d, &fd);
+        return run_fwd_tc(fd, q_raw, k_raw, v, a_logit, b_logit, initial_state, o, final_state, tc_saved, ws,
+                          nullptr, &sp, cs, &rp);
+    }
+    // other shapes: the prologue kernel, then the recurrence on its outputs
+    ComposedBufs c;
+    Carver cv{(char*)workspace};
+    carve_composed(d, es, cv, &c, false);
+    cudaError_t e = timed(gdn::KID_PROLOGUE_FWD, cs, [&] {
+        return gdn::launch_prologue_fwd(d, ty, q_raw, k_raw, a_logit, b_logit, c.qn, c.kn, c.al, c.be, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "prologue kernel");
+    return gdn_fwd(p, c.qn, c.kn, v, c.al, c.be, initial_state, o, final_state, saved, ws, workspace_bytes - pre,
+                   stream);
+}
+
+gdn_status gdn_bwd_raw(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* v,
+                       const void* a_logit, const void* b_logit, const float* initial_state, const void* saved,
+                       const void* d_o, const float* d_final_state, void* dq_raw, void* dk_raw, void* dv,
+                       void* da_logit, void* db_logit, float* d_initial_state, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn::Dims d{};
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (d.NS() * d.NC == 0)  // no tokens: d(initial state) = d(final state)
+        return gdn_bwd(p, q_raw, k_raw, v, a_logit, b_logit, initial_state, nullptr, d_o, d_final_state, dq_raw,
+                       dk_raw, dv, da_logit, db_logit, d_initial_state, nullptr, 0, stream);
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)d.B * d.T * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const size_t need = gdn_raw_bwd_workspace_bytes(p);
+    const Span ins[] = {{q_raw, BTH * d.K * es, "q_raw"},
+                        {k_raw, BTH * d.K * es, "k_raw"},
+                        {v, BTH * d.V * es, "v"},
+                        {a_logit, BTH * es, "a_logit"},
+                        {b_logit, BTH * es, "b_logit"},
+                        {initial_state, nstate, "initial_state"},
+                        {saved, gdn_raw_saved_bytes(p), "saved"},
+                        {d_o, BTH * d.V * es, "d_o"},
+                        {d_final_state, nstate, "d_final_state"}};
+    const Span outs[] = {{dq_raw, BTH * d.K * es, "dq_raw"},
+                         {dk_raw, BTH * d.K * es, "dk_raw"},
+                         {dv, BTH * d.V * es, "dv"},
+                         {da_logit, BTH * es, "da_logit"},
+                         {db_logit, BTH * es, "db_logit"},
+                         {d_initial_state, nstate, "d_initial_state"},
+                         {workspace, need, "workspace"}};
+    for (int i = 0; i < 9; ++i)
+        if ((st = check_ptr(ins[i], !(i == 5 || i == 6 || i == 8))) != GDN_OK) return st;
+    for (int i = 0; i < 7; ++i)
+        if ((st = check_ptr(outs[i], i != 5)) != GDN_OK) return st;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    if ((st = check_overlaps(ins, 9, outs, 7, d_initial_state, d_final_state)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const gdn::InType ty = in_type(p);
+    const size_t pre = raw_prefix(p, d, true);
+    char* ws = (char*)workspace + pre;
+    if (gdn::tc_fwd_supported(d, ty)) {
+        gdn::RawPrologue rp;
+        Carver cv{(char*)(saved ? const_cast<void*>(saved) : workspace)};
+        carve_raw(d, cv, &rp);
+        const void* tc_saved = saved ? (const char*)saved + cv.off : nullptr;
+        gdn::Dims fd;
+        const SplitCfg sp = dense_split(d, &fd);
+        return run_bwd_tc(fd, q_raw, k_raw, v, a_logit, b_logit, initial_state, tc_saved, d_o, d_final_state,
+                          dq_raw, dk_raw, dv, da_logit, db_logit, d_initial_state, ws, nullptr, &sp, cs, &rp);
+    }
+    // other shapes: the prologue again, the recurrence's backward, then the prologue's
+    ComposedBufs c;
+    Carver cv{(char*)workspace};
+    carve_composed(d, es, cv, &c, true);
+    cudaError_t e = timed(gdn::KID_PROLOGUE_FWD, cs, [&] {
+        return gdn::launch_prologue_fwd(d, ty, q_raw, k_raw, a_logit, b_logit, c.qn, c.kn, c.al, c.be, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "prologue kernel");
+    st = gdn_bwd(p, c.qn, c.kn, v, c.al, c.be, initial_state, saved, d_o, d_final_state, c.dqn, c.dkn, dv, c.dal,
+                 c.dbe, d_initial_state, ws, workspace_bytes - pre, stream);
+    if (st != GDN_OK) return st;
+    e = timed(gdn::KID_PROLOGUE_BWD, cs, [&] {
+        return gdn::launch_prologue_bwd(d, ty, q_raw, k_raw, a_logit, b_logit, c.dqn, c.dkn, c.dal, c.dbe, dq_raw,
+                                        dk_raw, da_logit, db_logit, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "prologue backward kernel");
+    return GDN_OK;
+}
+
+// ------------------------------------------------------------------ reset masks
+
+}  // extern "C"
+
+namespace {
+
+// The reset calls run gdn_varlen_* on the dense tensors (a packed batch of S_max
+// sequences over the B*T tokens); their own buffers follow the varlen workspace,
+// so the varlen error word stays the first int of the caller's workspace.
+struct ResetBufs {
+    int32_t *cu, *in_map, *fin_map, *last, *first_carry;
+    int* err;
+    float *s_in, *s_out;  // per-segment initial / final states or state gradients
+};
+size_t carve_reset(const gdn::Dims& d, int64_t S_max, Carver& cv, ResetBufs* r) {
+    r->cu = cv.take<int32_t>((size_t)S_max + 1);
+    r->in_map = cv.take<int32_t>((size_t)S_max);
+    r->fin_map = cv.take<int32_t>((size_t)S_max);
+    r->last = cv.take<int32_t>((size_t)d.B);
+    r->first_carry = cv.take<int32_t>((size_t)d.B);
+    r->err = cv.take<int>(1);
+    const size_t st = (size_t)S_max * d.H * d.V * d.K;
+    r->s_in = cv.take<float>(st);
+    r->s_out = cv.take<float>(st);
+    return cv.off;
+}
+
+// The packed problem the reset calls run: S_max sequences of at most T tokens.
+gdn_status reset_problem(const gdn_problem* p, int64_t S_max, gdn_problem* pv, gdn::Dims* d) {
+    gdn_status st = check_problem(p, d);
+    if (st != GDN_OK) return st;
+    if (d->B > 0 && d->T > 0 && (S_max < d->B || S_max > (int64_t)d->B * d->T))
+        return fail(GDN_ERR_INVALID_ARG, "max_segments=%lld must be in [B, B*T] = [%d, %lld]", (long long)S_max,
+                    d->B, (long long)d->B * d->T);
+    if (S_max > 65535) return fail(GDN_ERR_UNSUPPORTED, "max_segments=%lld exceeds 65535", (long long)S_max);
+    *pv = *p;
+    pv->B = S_max;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_reset_saved_bytes(const gdn_problem* p, int64_t max_segments) {
+    gdn_problem pv;
+    gdn::Dims d{};
+    if (reset_problem(p, max_segments, &pv, &d) != GDN_OK) return 0;
+    return gdn_varlen_saved_bytes(&pv, (int64_t)d.B * d.T);
+}
+
+static size_t reset_ws_bytes(const gdn_problem* p, int64_t max_segments, bool bwd) {
+    gdn_problem pv;
+    gdn::Dims d{};
+    if (reset_problem(p, max_segments, &pv, &d) != GDN_OK || d.NS() * d.NC == 0) return 0;
+    const int64_t total = (int64_t)d.B * d.T;
+    const size_t inner =
+        round_up(bwd ? gdn_varlen_bwd_workspace_bytes(&pv, total) : gdn_varlen_fwd_workspace_bytes(&pv, total));
+    Carver cv{nullptr};
+    ResetBufs r;
+    return inner + carve_reset(d, max_segments, cv, &r);
+}
+
+size_t gdn_reset_fwd_workspace_bytes(const gdn_problem* p, int64_t max_segments) {
+    return reset_ws_bytes(p, max_segments, false);
+}
+
+size_t gdn_reset_bwd_workspace_bytes(const gdn_problem* p, int64_t max_segments) {
+    return reset_ws_bytes(p, max_segments, true);
+}
+
+gdn_status gdn_reset_fwd(const gdn_problem* p, int64_t max_segments, const uint8_t* reset, const void* q,
+                         const void* k, const void* v, const void* alpha, const void* beta,
+                         const float* initial_state, void* o, float* final_state, void* saved, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn_problem pv;
+    gdn::Dims d{};
+    gdn_status st = reset_problem(p, max_segments, &pv, &d);
+    if (st != GDN_OK) return st;
+    if (d.NS() * d.NC == 0)  // no tokens: the state passes through, the mask is not read
+        return gdn_fwd(p, q, k, v, alpha, beta, initial_state, o, final_state, nullptr, nullptr, 0, stream);
+    const int64_t total = (int64_t)d.B * d.T;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)total * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const size_t need = gdn_reset_fwd_workspace_bytes(p, max_segments);
+    // every argument is checked here, before the first launch (the packed call checks again)
+    const Span ins[] = {{q, BTH * d.K * es, "q"},       {k, BTH * d.K * es, "k"},
+                        {v, BTH * d.V * es, "v"},       {alpha, BTH * es, "alpha"},
+                        {beta, BTH * es, "beta"},       {initial_state, nstate, "initial_state"},
+                        {reset, (size_t)total, "reset"}};
+    const Span outs[] = {{o, BTH * d.V * es, "o"},
+                         {final_state, nstate, "final_state"},
+                         {saved, gdn_reset_saved_bytes(p, max_segments), "saved"},
+                         {workspace, need, "workspace"}};
+    if (!reset) return fail(GDN_ERR_INVALID_ARG, "reset is NULL");
+    for (int i = 0; i < 6; ++i)
+        if ((st = check_ptr(ins[i], i != 5)) != GDN_OK) return st;
+    for (int i = 0; i < 4; ++i)
+        if ((st = check_ptr(outs[i], i == 0 || i == 3)) != GDN_OK) return st;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    if ((st = check_overlaps(ins, 7, outs, 4, final_state, initial_state)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const size_t inner = round_up(gdn_varlen_fwd_workspace_bytes(&pv, total));
+    Carver cv{(char*)workspace + inner};
+    ResetBufs r;
+    carve_reset(d, max_segments, cv, &r);
+    const int64_t row = (int64_t)d.H * d.V * d.K;
+    cudaError_t e = gdn::launch_reset_segments(d.B, d.T, reset, (int)max_segments, r.cu, r.in_map, r.fin_map, r.last,
+                                               r.first_carry, r.err, cs);
+    if (e == cudaSuccess)  // each row's initial state into its first segment (unless reset at t = 0)
+        e = gdn::launch_route_states((int)max_segments, row, r.in_map, initial_state, r.s_in, nullptr, nullptr, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "reset segments");
+    st = gdn_varlen_fwd(&pv, total, r.cu, q, k, v, alpha, beta, r.s_in, o, r.s_out, saved, workspace, inner,
+                        stream);
+    if (st != GDN_OK) return st;
+    // each row's final state from its last segment; the segment error joins the varlen word
+    e = gdn::launch_route_states(final_state ? d.B : 0, row, r.last, r.s_out, final_state, r.err, (int*)workspace,
+                                 cs);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "reset state routing");
+}
+
+gdn_status gdn_reset_bwd(const gdn_problem* p, int64_t max_segments, const uint8_t* reset, const void* q,
+                         const void* k, const void* v, const void* alpha, const void* beta,
+                         const float* initial_state, const void* saved, const void* d_o, const float* d_final_state,
+                         void* dq, void* dk, void* dv, void* dalpha, void* dbeta, float* d_initial_state,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    gdn_problem pv;
+    gdn::Dims d{};
+    gdn_status st = reset_problem(p, max_segments, &pv, &d);
+    if (st != GDN_OK) return st;
+    if (d.NS() * d.NC == 0)
+        return gdn_bwd(p, q, k, v, alpha, beta, initial_state, nullptr, d_o, d_final_state, dq, dk, dv, dalpha,
+                       dbeta, d_initial_state, nullptr, 0, stream);
+    const int64_t total = (int64_t)d.B * d.T;
+    const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
+    const size_t BTH = (size_t)total * d.H;
+    const size_t nstate = (size_t)d.NS() * d.V * d.K * sizeof(float);
+    const size_t need = gdn_reset_bwd_workspace_bytes(p, max_segments);
+    // every argument is checked here, before the first launch (the packed call checks again)
+    const Span ins[] = {{q, BTH * d.K * es, "q"},
+                        {k, BTH * d.K * es, "k"},
+                        {v, BTH * d.V * es, "v"},
+                        {alpha, BTH * es, "alpha"},
+                        {beta, BTH * es, "beta"},
+                        {initial_state, nstate, "initial_state"},
+                        {saved, gdn_reset_saved_bytes(p, max_segments), "saved"},
+                        {d_o, BTH * d.V * es, "d_o"},
+                        {d_final_state, nstate, "d_final_state"},
+                        {reset, (size_t)total, "reset"}};
+    const Span outs[] = {{dq, BTH * d.K * es, "dq"},
+                         {dk, BTH * d.K * es, "dk"},
+                         {dv, BTH * d.V * es, "dv"},
+                         {dalpha, BTH * es, "dalpha"},
+                         {dbeta, BTH * es, "dbeta"},
+                         {d_initial_state, nstate, "d_initial_state"},
+                         {workspace, need, "workspace"}};
+    if (!reset) return fail(GDN_ERR_INVALID_ARG, "reset is NULL");
+    for (int i = 0; i < 9; ++i)
+        if ((st = check_ptr(ins[i], !(i == 5 || i == 6 || i == 8))) != GDN_OK) return st;
+    for (int i = 0; i < 7; ++i)
+        if ((st = check_ptr(outs[i], i != 5)) != GDN_OK) return st;
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    if ((st = check_overlaps(ins, 10, outs, 7, d_initial_state, d_final_state)) != GDN_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const size_t inner = round_up(gdn_varlen_bwd_workspace_bytes(&pv, total));
+    Carver cv{(char*)workspace + inner};
+    ResetBufs r;
+    carve_reset(d, max_segments, cv, &r);
+    const int64_t row = (int64_t)d.H * d.V * d.K;
+    float* s_init = r.s_in;    // the segments' initial states
+    float* g_fin = r.s_out;    // the segments' final-state gradients, then their initial-state gradients
+    cudaError_t e = gdn::launch_reset_segments(d.B, d.T, reset, (int)max_segments, r.cu, r.in_map, r.fin_map, r.last,
+                                               r.first_carry, r.err, cs);
+    if (e == cudaSuccess)
+        e = gdn::launch_route_states((int)max_segments, row, r.in_map, initial_state, s_init, nullptr, nullptr, cs);
+    if (e == cudaSuccess)  // each row's final-state gradient into its last segment
+        e = gdn::launch_route_states((int)max_segments, row, r.fin_map, d_final_state, g_fin, nullptr, nullptr, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "reset segments");
+    // in place: d(initial state) of every segment over its d(final state)
+    st = gdn_varlen_bwd(&pv, total, r.cu, q, k, v, alpha, beta, s_init, saved, d_o, g_fin, dq, dk, dv, dalpha,
+                        dbeta, g_fin, workspace, inner, stream);
+    if (st != GDN_OK) return st;
+    // a row's d(initial state) from its first segment; zero if the row resets at t = 0
+    e = gdn::launch_route_states(d_initial_state ? d.B : 0, row, r.first_carry, g_fin, d_initial_state, r.err,
+                                 (int*)workspace, cs);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "reset state routing");
 }
 
 gdn_status gdn_set_sequence_split(int pieces) {

@@ -184,6 +184,17 @@ cudaError_t launch_combine_bwd(int S, int P, int H, const float* dsT, const floa
 // tensors to and from the padded [S, T, H, width] layout.  `merge` (optional) is
 // ORed into `err` once.
 constexpr int kVarlenBadOffsets = 1 << 30;  // error-word bit: invalid cu_seqlens
+constexpr int kResetTooManySegments = 1 << 29;  // error-word bit: more segments than max_segments
+// Reset masks (reset.cu): the segments of a dense [B, T] batch whose streams
+// restart at every set mask entry, and the routing of states between rows and
+// segments (see gdn_reset_fwd in include/gdn.h).
+cudaError_t launch_reset_segments(int B, int T, const uint8_t* reset, int S_max, int32_t* cu, int32_t* in_map,
+                                  int32_t* fin_map, int32_t* last, int32_t* first_carry, int* err,
+                                  cudaStream_t st);
+// out[r] = src[map[r]] for nrows rows of `row` floats (zeros where map < 0 or src
+// is NULL); ORs *merge_from into *merge_to first when both are given.
+cudaError_t launch_route_states(int nrows, int64_t row, const int32_t* map, const float* src, float* out,
+                                const int* merge_from, int* merge_to, cudaStream_t st);
 // Work counters of the persistent kernels, in the error-flag area of the workspace
 // (64 ints, the first 32 reset at the start of every call): chunks handed out
 // beyond each CTA's first one.
@@ -226,9 +237,24 @@ cudaError_t launch_count_nonfinite(const void* x, int64_t n, InType ty, int64_t*
 cudaError_t launch_decode(const Dims& d, InType ty, const void* q, const void* k, const void* v,
                           const void* alpha, const void* beta, float* state, void* o, cudaStream_t st);
 
+// The prologue in front of the recurrence, folded into the tensor-core kernels
+// (gdn_fwd_raw / gdn_bwd_raw): with `on`, q and k are the raw rows and alpha,
+// beta the gate logits a, b.  prep_fwd_tc normalises the q, k rows as they land
+// (x / sqrt(sum x^2 + 1e-6)), writes them to qn, kn ([B,T,H,K] bf16) and the
+// reciprocal norms to rq, rk ([B,T,H] fp32), and takes log alpha = -softplus(a),
+// beta = sigmoid(b); the backward turns the gradients of the normalised rows and
+// gates into those of the raw inputs.
+struct RawPrologue {
+    int on = 0;
+    __nv_bfloat16* qn = nullptr;
+    __nv_bfloat16* kn = nullptr;
+    float* rq = nullptr;
+    float* rk = nullptr;
+};
+
 cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v,
                            const void* alpha, const void* beta, const TcBufs& tb,
-                           cudaStream_t st);
+                           cudaStream_t st, const RawPrologue* raw = nullptr);
 cudaError_t launch_scan_fwd_tc(const Dims& d, const void* q, const void* k, const TcBufs& tb,
                                const float* s0, void* o, float* sT, __nv_bfloat16* states,
                                cudaStream_t st, const SeqMap* sq = nullptr);
@@ -238,9 +264,11 @@ cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, cons
                                float* ds0, cudaStream_t st, const SeqMap* sq = nullptr);
 cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const void* d_o,
                               const TcBufs& tb, const __nv_bfloat16* states,
-                              const TcBwdBufs& bb, void* dq, cudaStream_t st);
+                              const TcBwdBufs& bb, void* dq, cudaStream_t st,
+                              const RawPrologue* raw = nullptr);
 cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const void* alpha,
                               const void* beta, const TcBufs& tb, const TcBwdBufs& bb,
-                              void* dk, void* dv, void* dalpha, void* dbeta, cudaStream_t st);
+                              void* dk, void* dv, void* dalpha, void* dbeta, cudaStream_t st,
+                              const RawPrologue* raw = nullptr);
 
 }  // namespace gdn

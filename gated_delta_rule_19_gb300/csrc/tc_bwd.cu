@@ -257,7 +257,8 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
     for (int j = 0; j < HV; ++j) {
         const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
-        ds[j] = (epi && dsT && ((kD % Vt == 0) || v < kD)) ? dsT[(sidx * d.V + v) * kD + k] : 0.f;
+        // the caller's [V, K] gradient (K, V = 64 or 128); rows and columns past them are zero
+        ds[j] = (epi && dsT && v < d.V && k < d.K) ? dsT[(sidx * d.V + v) * d.K + k] : 0.f;
     }
     auto write_ds_operand = [&]() {
 #pragma unroll
@@ -482,7 +483,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (ok && ds0 && epi) {
 #pragma unroll
         for (int j = 0; j < HV; ++j)
-            if ((kD % Vt == 0) || v0 + cb + j < kD) ds0[(sidx * d.V + v0 + cb + j) * kD + k] = ds[j];
+            if (v0 + cb + j < d.V && k < d.K) ds0[(sidx * d.V + v0 + cb + j) * d.K + k] = ds[j];
     }
     if (tma_issuer) {
         // on an error, the loads still in flight (bounded waits) before leaving
@@ -507,58 +508,74 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 // ====================================================== chunk gradients (1)
 namespace qk {
-constexpr int WQ = 0;                  // [W_0 | Q_0 | W_1 | Q_1]: stacked [W;Q] and Q (MN-major)
-constexpr int K = 32768;               // [K_0 | K_1]
-constexpr int DO = 49152;              // [dO_0 | dU_0 | dO_1 | dU_1]: stacked [dO; dU] (N=128)
-constexpr int DU = DO + 8192;
-constexpr int S0 = 81920, DS1 = 114688;  // [128 x 128]
-constexpr int U = 147456, EU = 163840;   // [64 x 128]
-constexpr int DQK = 180224;              // [64 x 64]
-constexpr int DQ = 188416;               // dq output tile [64 x 128]
-constexpr int E1 = 204800;               // fp32 [64][65]
-constexpr int VEC = E1 + 64 * 65 * 4;    // Gs gs eRp[4] dG1p[4] rE1 cE1 (12 x 64) + red (512)
-constexpr int BAR = VEC + (12 * 64 + 512) * 4;
+// group A (free once phase 1's MMAs are done): U | [dO_0 | dU_0 | dO_1 | dU_1] | S0^T | dS1^T
+constexpr int U = 0;                   // [64 x 128]: U_0 | U_1
+constexpr int DO = 16384;              // stacked [dO; dU] (M / N = 128), column blocks 16 KB apart
+constexpr int S0 = 49152, DS1 = 81920; // [128 x 128], column blocks 16 KB apart
+// group B (free once phase 2's MMAs are done)
+constexpr int Q = 114688, K = 131072;  // [64 x 128]: two column blocks 8 KB apart
+// results
+constexpr int DQK = 147456;            // [64 x 64]
+constexpr int DWT = 155648;            // dW^T [128 x 64] (two 64-row halves)
+constexpr int DQ = 172032;             // dq [64 x 128]
+constexpr int DKP = 188416;            // dK^T part [128 x 64]
+constexpr int VEC = 204800;            // Gs gs | dG1p[4] eRp[4] rE1[4] | cE1[8][16] | red[512] | 8 | rqs | dotp[4]
+constexpr int NVEC = 2 * 64 + 3 * 256 + 128 + 512 + 8 + 64 + 256;
+constexpr int BAR = VEC + NVEC * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
+static_assert(SMEM <= 232448, "one CTA per SM");
 }  // namespace qk
 
-// Persistent: CTA i starts with chunk i and takes further chunks from a work
-// counter, so that faster SMs take more chunks.  512 threads; warps w,
-// w+4, w+8 and w+12 split the columns of TMEM lanes 32*(w%4) ..  The next chunk's
-// tiles are requested as soon as their buffers are free (after phase 1, 2 and 3).
+// Chunk gradients on the q side, from the forward's U (= U~ - W S0^T, saved by the
+// forward scan), the chunk-start state S0, and the reverse scan's dU and dS1:
+//   phase 1 (operands all loaded):
+//     S0^T [dO; dU]^T          -> dQ1^T = S0^T dO^T  and  -dW^T = S0^T dU^T  (N = 128)
+//     [dO; dU] U^T (rows 0-63) -> dMqk = dO U^T                               (N = 64)
+//     dS1^T U^T                -> dK'^T = (U dS1)^T                           (N = 64)
+//   epilogue 1: dQK = Gam .* lower(dMqk); dW^T out; the dG sums
+//     dG1_r = sum_k Q_rk dQ1_rk  (= sum_v dO_rv (Q S0^T)_rv, gamma in O),
+//     eR_r  = sum_k K_rk dK'_rk  (= sum_v U_rv (K dS1^T)_rv, exp(G_C - G) in Khat),
+//     E1 = dMqk .* Mqk row and column sums (Gam in Mqk), <dS1, S0> (gamma_C in S1)
+//   phase 2: dQ2^T = K^T dQK^T,  QK^T = Q^T dQK                               (N = 64)
+//   epilogue 2: dq = gamma dQ1 + dQ2; dK^T part = exp(G_C - G) dK'^T + Q^T dQK; dG part.
+// Persistent, 512 threads, one CTA per SM: CTA i starts with chunk i and takes
+// further chunks from a work counter.  Warps w, w+4, w+8, w+12 reach TMEM lanes
+// 32*(w%4) .. and split the columns of every epilogue.  Group A tiles of the next
+// chunk are requested as soon as phase 1's MMAs are done, group B after phase 2.
+template <bool kRaw>
 __global__ void __launch_bounds__(512, 1)
 grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_W,
+           const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_U,
            const __grid_constant__ CUtensorMap tm_dU, const __grid_constant__ CUtensorMap tm_S0,
            const __grid_constant__ CUtensorMap tm_dS1, const __grid_constant__ CUtensorMap tm_dq,
            const __grid_constant__ CUtensorMap tm_dKp, const __grid_constant__ CUtensorMap tm_dWt,
-           const bf16* __restrict__ Ut, const bf16* __restrict__ Mqk, const float* __restrict__ G,
-           float* __restrict__ dGp, int* err) {
+           const bf16* __restrict__ Mqk, const float* __restrict__ G, float* __restrict__ dGp, RawPrologue raw,
+           int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-    float* E1f = (float*)(sm + qk::E1);
     float* Gs = (float*)(sm + qk::VEC);
     float* gs = Gs + 64;
-    float* eRp = gs + 64;    // [4 column quarters][64]
-    float* dG1p = eRp + 256; // [4][64]
-    float* rE1 = dG1p + 256;
-    float* cE1 = rE1 + 64;
-    float* red = cE1 + 64;   // 512
-    // [0] loads A1, [1] loads B, [2..4] MMA phases, [5] loads A2, [6] S0^T [dO; dU]^T
+    float* dG1p = gs + 64;   // [4 lane quarters][64 tokens]
+    float* eRp = dG1p + 256; // [4][64]
+    float* rE1 = eRp + 256;  // [4 column quarters][64 rows]
+    float* cE1 = rE1 + 256;  // [2 row halves][4 column quarters][16]
+    float* red = cE1 + 128;  // 512
+    float* fin = red + 512;  // <dS1, S0>, sum_i e_i eR_i
+    float* rqs = fin + 8;    // raw prologue: 1 / |q_raw| of the chunk's tokens
+    float* dotp = rqs + 64;  // raw prologue: q.dq partial sums [4 lane quarters][64]
+    // [0] loads A, [1] loads B, [2] phase 1 MMAs, [3] phase 2 MMAs
     uint64_t* bars = (uint64_t*)(sm + qk::BAR);
-    uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 56);
-    int* s_next = (int*)(sm + qk::BAR + 60);  // the chunk after this one
+    uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 40);
+    int* s_next = (int*)(sm + qk::BAR + 44);  // the chunk after this one
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // 16 warps: warp w reaches TMEM lanes 32*(w%4) ..; the four warps of a lane
-    // quarter split the columns of every epilogue (qtr = w / 4)
     const int sub = warp & 3, qtr = warp >> 2;
-    const int lanerow = 32 * sub + lane;
-    const bool urow = sub < 2;
+    const int lanerow = 32 * sub + lane;  // TMEM lane: a row k of the [128 x .] products
+    const bool urow = sub < 2;            // lanes 0-63: rows of the [64 x 64] product
     const int r = urow ? lanerow : lanerow - 64;
+    const int cb = qtr * 16;              // this thread's 16 columns of a 64-column product
     const int64_t nchunks = d.NS() * d.NC;
-    // the thread that issues the MMAs and the TMA stores: lane 0 of warp 2, whose
-    // lanes (TMEM rows 64-95) fetch no U~ / Mqk rows before phase 1
-    constexpr int kQkIssuer = 64;
+    constexpr int kIssuer = 64;  // MMAs, loads and stores: lane 0 of warp 2
 
     auto decode = [&](int64_t ch, int& b, int& h, int& c) {
         c = (int)(ch % d.NC);
@@ -566,27 +583,19 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         h = (int)(bh % d.H);
         b = (int)(bh / d.H);
     };
-    // group A1: W, dU, S0^T (free once phase 1's MMAs are done and <dS1, S0> is
-    // formed); A2: dO, dS1^T (free after phase 2); B: Q, K (free after phase 3)
-    auto load_A1 = [&](int64_t ch) {
-        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
-        mbar_arrive_expect_tx(&bars[0], 8 * 8192);
-        for (int j = 0; j < 2; ++j) {
-            tma_load_2d(sm + qk::WQ + j * 16384, &tm_W, &bars[0], 64 * j, row0);
-            tma_load_2d(sm + qk::DU + j * 16384, &tm_dU, &bars[0], 64 * j, row0);
-            for (int i = 0; i < 2; ++i)
-                tma_load_2d(sm + qk::S0 + j * 16384 + i * 8192, &tm_S0, &bars[0], 64 * j, krow0 + 64 * i);
-        }
-    };
-    auto load_A2 = [&](int64_t ch) {
+    auto load_A = [&](int64_t ch) {
         int b, h, c;
         decode(ch, b, h, c);
-        const int krow0 = (int)(ch * kD);
-        mbar_arrive_expect_tx(&bars[5], 6 * 8192);
+        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
+        mbar_arrive_expect_tx(&bars[0], 14 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[5], 64 * j, h, c * kC, b);
-            for (int i = 0; i < 2; ++i)
-                tma_load_2d(sm + qk::DS1 + j * 16384 + i * 8192, &tm_dS1, &bars[5], 64 * j, krow0 + 64 * i);
+            tma_load_2d(sm + qk::U + j * 8192, &tm_U, &bars[0], 64 * j, row0);
+            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[0], 64 * j, h, c * kC, b);
+            tma_load_2d(sm + qk::DO + j * 16384 + 8192, &tm_dU, &bars[0], 64 * j, row0);
+            for (int i = 0; i < 2; ++i) {
+                tma_load_2d(sm + qk::S0 + j * 16384 + i * 8192, &tm_S0, &bars[0], 64 * j, krow0 + 64 * i);
+                tma_load_2d(sm + qk::DS1 + j * 16384 + i * 8192, &tm_dS1, &bars[0], 64 * j, krow0 + 64 * i);
+            }
         }
     };
     auto load_B = [&](int64_t ch) {
@@ -594,26 +603,38 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         decode(ch, b, h, c);
         mbar_arrive_expect_tx(&bars[1], 4 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + qk::WQ + j * 16384 + 8192, &tm_q, &bars[1], 64 * j, h, c * kC, b);
+            tma_load_4d(sm + qk::Q + j * 8192, &tm_q, &bars[1], 64 * j, h, c * kC, b);
             tma_load_4d(sm + qk::K + j * 8192, &tm_k, &bars[1], 64 * j, h, c * kC, b);
         }
     };
 
     const int64_t first = blockIdx.x;
     // warp 3 keeps the next chunk's G (2 tokens per lane) in registers
-    float2 gnext = make_float2(0.f, 0.f);
+    float2 gnext = make_float2(0.f, 0.f), rnext = gnext;
+    auto load_rq = [&](int64_t c2) {  // 1 / |q_raw| of tokens 2 lane, 2 lane + 1 (raw prologue)
+        int b2, h2, cc;
+        decode(c2, b2, h2, cc);
+        const int t = cc * kC + 2 * lane;
+        const int64_t gi = ((int64_t)b2 * d.T + t) * d.H + h2;
+        rnext.x = t < d.T ? raw.rq[gi] : 0.f;
+        rnext.y = t + 1 < d.T ? raw.rq[gi + d.H] : 0.f;
+    };
     int claimed = 0;  // lane 0 of warp 3: the next chunk, claimed from the work counter a chunk ahead
     if (warp == 3 && first < nchunks) {
         gnext = *(const float2*)(G + first * kC + 2 * lane);
+        if (kRaw) load_rq(first);
         if (lane == 0) claimed = (int)gridDim.x + atomicAdd(err + kSchedQk, 1);
     }
-    if (tid == kQkIssuer) {
-        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
+    // issued counts (thread kIssuer): load groups A and B, phase 1 and 2 commits;
+    // on an error the last of each is waited for (bounded) before the CTA leaves
+    int na = 0, nb = 0, n1 = 0, n2 = 0;
+    if (tid == kIssuer) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         if (first < nchunks) {
-            load_A1(first);
-            load_A2(first);
+            load_A(first);
             load_B(first);
+            na = nb = 1;
         }
     }
     if (warp == 0) {
@@ -625,31 +646,22 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t lanebase = (uint32_t)(sub * 32) << 16;
-    // tQW: columns 0-63 S0^T dO^T (dQ1^T), 64-127 S0^T dU^T (-dW^T)
-    const uint32_t tXY = tmem, tZ = tmem + 128, tDM = tmem + 256, tQW = tmem + 320, tQ1 = tQW, tDW = tQW + 64,
-                   tDK = tmem + 448, tQ2 = tmem + 0;
-    const uint32_t sWQ = smem_u32(sm + qk::WQ), sK = smem_u32(sm + qk::K), sDO = smem_u32(sm + qk::DO);
-    const uint32_t sS0 = smem_u32(sm + qk::S0), sDS1 = smem_u32(sm + qk::DS1);
-    const uint32_t sU = smem_u32(sm + qk::U), sEU = smem_u32(sm + qk::EU), sDQK = smem_u32(sm + qk::DQK);
+    // TMEM columns: dQ1^T 0-63 and -dW^T 64-127 (tQW), dMqk 128-191 (then dQ2^T),
+    // dK'^T 192-255, Q^T dQK 256-319
+    const uint32_t tQW = tmem, tQ1 = tmem, tDW = tmem + 64, tDM = tmem + 128, tQ2 = tmem + 128,
+                   tDK = tmem + 192, tQK = tmem + 256;
+    const uint32_t sU = smem_u32(sm + qk::U), sDO = smem_u32(sm + qk::DO), sS0 = smem_u32(sm + qk::S0);
+    const uint32_t sDS1 = smem_u32(sm + qk::DS1), sQ = smem_u32(sm + qk::Q), sK = smem_u32(sm + qk::K);
+    const uint32_t sDQK = smem_u32(sm + qk::DQK);
 
-    // rows of Ut (this quarter's 32 columns) and Mqk (16 columns) of row r of a
-    // chunk, read a chunk ahead: each set is reloaded for the next chunk as soon as
-    // its epilogue has used it
-    uint4 utv[4], mqv[2];
-    auto load_ut = [&](int64_t c2) {
-        const uint4* up = (const uint4*)(Ut + (c2 * kC + r) * kD + qtr * 32);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) utv[q] = up[q];
-    };
+    // rows of Mqk (this quarter's 16 columns) of row r, read a chunk ahead
+    uint4 mqv[2];
     auto load_mq = [&](int64_t c2) {
-        const uint4* mp = (const uint4*)(Mqk + (c2 * kC + r) * kC + qtr * 16);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) mqv[q] = mp[q];
+        const uint4* mp = (const uint4*)(Mqk + (c2 * kC + r) * kC + cb);
+        mqv[0] = mp[0];
+        mqv[1] = mp[1];
     };
-    if (urow && first < nchunks) {
-        load_ut(first);
-        load_mq(first);
-    }
+    if (urow && first < nchunks) load_mq(first);
     bool ok = true;
     int n = 0;
     int64_t nxt = first;
@@ -670,39 +682,33 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             Gs[2 * lane + 1] = gnext.y;
             gs[2 * lane] = expf(gnext.x);
             gs[2 * lane + 1] = expf(gnext.y);
-            if (nx < nchunks) gnext = *(const float2*)(G + (int64_t)nx * kC + 2 * lane);
-        }
-        // ---- phase 1 (K over k): [X; Y] = [W; Q] S0^T, Z = [K; -] dS1^T  (M=128, N=128)
-        if (tid == kQkIssuer) {
-            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
-            ok = mbar_wait(&bars[5], ph, err, 1) && ok;
-            ok = mbar_wait(&bars[1], ph, err, 1) && ok;
-            if (ok) {
-                const uint32_t id = idesc_bf16(128, 128, false, true);
-                const uint64_t dwq = sdesc(sWQ, 16, 1024, SW_128B), dk = sdesc(sK, 16, 1024, SW_128B);
-                const uint64_t ds0 = sdesc(sS0, 16384, 1024, SW_128B), dds1 = sdesc(sDS1, 16384, 1024, SW_128B);
-#pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) {
-                    mma_bf16_ss(tXY, desc_add(dwq, (s2 >> 2) * 16384 + (s2 & 3) * 32), desc_add(ds0, s2 * 2048), id,
-                                s2 > 0);
-                    mma_bf16_ss(tZ, desc_add(dk, (s2 >> 2) * 8192 + (s2 & 3) * 32), desc_add(dds1, s2 * 2048), id,
-                                s2 > 0);
-                }
-                mma_commit(&bars[2]);
-                // S0^T [dO; dU]^T (N=128) reads only loaded tiles: issued now, it runs
-                // during epilogue 1 (its own commit frees W, dU, S0^T for the next chunk)
-                const uint32_t id128 = idesc_bf16(128, 128, false, false);
-                const uint64_t ds0k = sdesc(sS0, 16, 1024, SW_128B), ddok = sdesc(sDO, 16, 1024, SW_128B);
-#pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) {
-                    const uint32_t o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-                    mma_bf16_ss(tQW, desc_add(ds0k, o128), desc_add(ddok, o128), id128, s2 > 0);
-                }
-                mma_commit(&bars[6]);
+            rqs[2 * lane] = rnext.x;
+            rqs[2 * lane + 1] = rnext.y;
+            if (nx < nchunks) {
+                gnext = *(const float2*)(G + (int64_t)nx * kC + 2 * lane);
+                if (kRaw) load_rq(nx);
             }
         }
-        ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // S0 (read below)
-        ok = mbar_wait(&bars[5], ph, err, 1) && ok;  // dO and dS1
+        // ---- phase 1 (K over v): S0^T [dO; dU]^T (N=128), [dO; dU] U^T and dS1^T U^T (N=64)
+        if (tid == kIssuer) {
+            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+            if (ok) {
+                const uint32_t id128 = idesc_bf16(128, 128, false, false);
+                const uint32_t id64 = idesc_bf16(128, 64, false, false);
+                const uint64_t ds0 = sdesc(sS0, 16, 1024, SW_128B), ddo = sdesc(sDO, 16, 1024, SW_128B);
+                const uint64_t dds1 = sdesc(sDS1, 16, 1024, SW_128B), du = sdesc(sU, 16, 1024, SW_128B);
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    const uint32_t o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32, o64 = (s2 >> 2) * 8192 + (s2 & 3) * 32;
+                    mma_bf16_ss(tQW, desc_add(ds0, o128), desc_add(ddo, o128), id128, s2 > 0);
+                    mma_bf16_ss(tDM, desc_add(ddo, o128), desc_add(du, o64), id64, s2 > 0);
+                    mma_bf16_ss(tDK, desc_add(dds1, o128), desc_add(du, o64), id64, s2 > 0);
+                }
+                mma_commit(&bars[2]);
+                ++n1;
+            }
+        }
+        ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // S0 and dS1 (read below)
         {   // <dS1, S0> over the chunk (both tiles share one layout), coalesced, while
             // phase 1's MMAs run
             const uint4* a = (const uint4*)(sm + qk::S0) + tid;
@@ -717,210 +723,203 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             red[tid] = acc;
         }
-        ok = mbar_wait(&bars[2], ph, err, 2) && ok;
-        if (tid == kQkIssuer) bulk_wait_read0();  // the previous chunk's stores from the U / EU tiles are done
-        __syncthreads();  // Gs / gs, the next chunk's index; every thread is past its reads of S0^T
-        fence_after_sync();
-        nxt = *s_next;
-        const bool has_next = nxt < nchunks;
-        // W, dU, S0^T are free once S0^T [dO; dU]^T is done: request the next chunk's
-        if (tid == 96 && ok && has_next) {
-            ok = mbar_wait(&bars[6], ph, err, 2);
-            if (ok) load_A1(nxt);
-        }
-        const float GC = Gs[63], gC = gs[63];
-        const float Gr = Gs[r], er = expf(GC - Gr);
-        {
-            const int cb = qtr * 32;
-            float acc = 0.f;
-#pragma unroll
-            for (int c0 = cb; c0 < cb + 32; c0 += 16) {
-                if (urow) {
-                    float x[16], z[16], u[16], eu[16];
-                    tmem_load16f2(tXY + lanebase + c0, tZ + lanebase + c0, x, z);
-                    const uint4 ua = utv[(c0 - cb) / 8], ub = utv[(c0 - cb) / 8 + 1];
-                    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        u[2 * j] = bf_lo(uw[j]) - x[2 * j];
-                        u[2 * j + 1] = bf_hi(uw[j]) - x[2 * j + 1];
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        eu[j] = er * u[j];
-                        acc += u[j] * z[j];
-                    }
-                    tile_put16(sm + qk::U, 64, r, c0, u);
-                    tile_put16(sm + qk::EU, 64, r, c0, eu);
-                } else {
-                    float y[16], dd[8], de[8];
-                    tmem_load16f(tXY + lanebase + c0, y);
-                    const unsigned char* dob = sm + qk::DO + (c0 >> 6) * 16384;
-                    tile_get8(dob, 64, r, c0 & 63, dd);
-                    tile_get8(dob, 64, r, (c0 & 63) + 8, de);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc += dd[j] * y[j] + de[j] * y[8 + j];
-                }
-            }
-            if (urow) eRp[qtr * 64 + r] = acc;
-            else dG1p[qtr * 64 + r] = acc;
-        }
-        if (urow && has_next) load_ut(nxt);
-        fence_proxy_async();
-        fence_before_sync();
-        ok = __syncthreads_and(ok);
-        fence_after_sync();
-        // ---- phase 2 (K over v): dMqk = [dO; -] U^T (N=64), dK^T = dS1^T (eU)^T (N=64)
-        //      (M=128); S0^T [dO; dU]^T was issued with phase 1
-        if (tid == kQkIssuer && ok) {
-            const uint32_t id = idesc_bf16(128, 64, false, false);
-            const uint64_t ddo = sdesc(sDO, 16, 1024, SW_128B), du = sdesc(sU, 16, 1024, SW_128B);
-            const uint64_t dds1 = sdesc(sDS1, 16, 1024, SW_128B), deu = sdesc(sEU, 16, 1024, SW_128B);
-#pragma unroll
-            for (int s2 = 0; s2 < 8; ++s2) {
-                const uint32_t o64 = (s2 >> 2) * 8192 + (s2 & 3) * 32, o128 = (s2 >> 2) * 16384 + (s2 & 3) * 32;
-                mma_bf16_ss(tDM, desc_add(ddo, o128), desc_add(du, o64), id, s2 > 0);
-                mma_bf16_ss(tDK, desc_add(dds1, o128), desc_add(deu, o64), id, s2 > 0);
-            }
-            mma_commit(&bars[3]);
-        }
-        if (ok) ok = mbar_wait(&bars[3], ph, err, 4);
+        if (ok) ok = mbar_wait(&bars[2], ph, err, 2);
         __syncwarp();
         fence_after_sync();
-        // dO, dS1^T are free: request the next chunk's
-        __syncthreads();  // every thread is past its reads of those tiles
-        // issued from warp 3 (output rows), which has the lighter epilogue in this phase
-        if (tid == 96 && ok && has_next) load_A2(nxt);
+        // the previous chunk's stores no longer read the result tiles (rewritten below)
+        if (tid == kIssuer) bulk_wait_read0();
+        fence_before_sync();
+        ok = __syncthreads_and(ok);  // Gs / gs, the next chunk's index; S0^T, dS1^T read
+        fence_after_sync();
+        if (!ok) break;
+        nxt = *s_next;
+        const bool has_next = nxt < nchunks;
+        // every group A tile is dead (phase 1's MMAs are done): the next chunk's
+        if (tid == kIssuer && has_next) {
+            load_A(nxt);
+            ++na;
+        }
+        ok = mbar_wait(&bars[1], ph, err, 1) && ok;  // Q, K (read by epilogue 1)
+        // ---- epilogue 1
         {
-            if (urow) {  // dMqk row r, columns qtr*16 .. +16 -> E1 row/column sums, dQK
-                const int cb = qtr * 16;
-                float e1[16];
+            const float Gr = Gs[r];
+            if (urow) {  // dMqk row r, columns cb .. cb+15 -> E1 row / column sums, dQK
+                float dm[16], e1[16], dq[16];
                 float rsum = 0.f;
+                tmem_load16f(tDM + lanebase + cb, dm);
+                const uint32_t mw[8] = {mqv[0].x, mqv[0].y, mqv[0].z, mqv[0].w,
+                                        mqv[1].x, mqv[1].y, mqv[1].z, mqv[1].w};
 #pragma unroll
-                for (int c0 = 0; c0 < 16; c0 += 16) {
-                    float dm[16], dq[16];
-                    tmem_load16f(tDM + lanebase + cb + c0, dm);
-                    const uint4 ma = mqv[c0 / 8], mb = mqv[c0 / 8 + 1];
-                    const uint32_t mw[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = cb + c0 + j;
-                        const float mq = (j & 1) ? bf_hi(mw[j >> 1]) : bf_lo(mw[j >> 1]);
-                        e1[c0 + j] = dm[j] * mq;
-                        rsum += e1[c0 + j];
-                        dq[j] = (i <= r) ? __expf(Gr - Gs[i]) * dm[j] : 0.f;
-                    }
-                    tile_put16(sm + qk::DQK, 64, r, cb + c0, dq);
+                for (int j = 0; j < 16; ++j) {
+                    const int i = cb + j;
+                    const float mq = (j & 1) ? bf_hi(mw[j >> 1]) : bf_lo(mw[j >> 1]);
+                    e1[j] = dm[j] * mq;
+                    rsum += e1[j];
+                    dq[j] = (i <= r) ? __expf(Gr - Gs[i]) * dm[j] : 0.f;
                 }
-                // row sums (this quarter of the columns) and column sums (these 32 rows)
-                E1f[qtr * 64 + r] = rsum;
+                tile_put16(sm + qk::DQK, 64, r, cb, dq);
+                rE1[qtr * 64 + r] = rsum;
                 const float csum = warp_colsum16(e1);
-                if (lane < 16) E1f[256 + (sub * 4 + qtr) * 16 + lane] = csum;
+                if (lane < 16) cE1[(sub * 4 + qtr) * 16 + lane] = csum;
                 if (has_next) load_mq(nxt);
             }
-            // dW^T row k (= lanerow), columns qtr*16 .. +16 -> [128 x 64] tile in the EU
-            // slot (dead once phase 2 is done), stored to scratch by TMA
-            const int cb = qtr * 16;
-            unsigned char* wt = sm + qk::EU + (lanerow >> 6) * 8192;
-            float w[16];
-            tmem_load16f(tDW + lanebase + cb, w);
+            const int k = lanerow;
+            // -dW^T row k, columns cb .. cb+15 -> the dW^T tile (stored to scratch by TMA)
+            {
+                float w[16];
+                tmem_load16f(tDW + lanebase + cb, w);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = -w[j];
-            *(uint4*)(wt + sw128_off(lanerow & 63, cb)) = pack8(w);
-            *(uint4*)(wt + sw128_off(lanerow & 63, cb + 8)) = pack8(w + 8);
+                for (int j = 0; j < 16; ++j) w[j] = -w[j];
+                unsigned char* wt = sm + qk::DWT + (k >> 6) * 8192;
+                *(uint4*)(wt + sw128_off(k & 63, cb)) = pack8(w);
+                *(uint4*)(wt + sw128_off(k & 63, cb + 8)) = pack8(w + 8);
+            }
+            // dG1_t = sum_k Q_tk dQ1_tk and eR_t = sum_k K_tk dK'_tk for this quarter's
+            // 16 tokens t: products over this warp's 32 rows k, then column sums
+            {
+                float q1[16], dk[16], pq[16], pk[16];
+                tmem_load16f2(tQ1 + lanebase + cb, tDK + lanebase + cb, q1, dk);
+                const unsigned char* qt = sm + qk::Q + (k >> 6) * 8192;
+                const unsigned char* kt = sm + qk::K + (k >> 6) * 8192;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t off = sw128_off(cb + j, k & 63);
+                    pq[j] = __bfloat162float(*(const bf16*)(qt + off)) * q1[j];
+                    pk[j] = __bfloat162float(*(const bf16*)(kt + off)) * dk[j];
+                }
+                const float sq = warp_colsum16(pq);
+                const float sk = warp_colsum16(pk);
+                if (lane < 16) {
+                    dG1p[sub * 64 + cb + lane] = sq;
+                    eRp[sub * 64 + cb + lane] = sk;
+                }
+            }
         }
         fence_proxy_async();
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        // ---- phase 3 (K over tokens): dQ2^T = K^T dQK^T;  dK^T += Q^T dQK  (M=128, N=64)
-        if (tid == kQkIssuer && ok) {
-            for (int j = 0; j < 2; ++j) tma_store_2d(&tm_dWt, sm + qk::EU + j * 8192, 0, krow0 + 64 * j);
+        if (!ok) break;
+        // ---- phase 2 (K over tokens): dQ2^T = K^T dQK^T;  Q^T dQK  (M=128, N=64)
+        if (tid == kIssuer) {
+            for (int j = 0; j < 2; ++j) tma_store_2d(&tm_dWt, sm + qk::DWT + j * 8192, 0, krow0 + 64 * j);
             bulk_commit();
             const uint32_t idq = idesc_bf16(128, 64, true, false);
             const uint32_t idk = idesc_bf16(128, 64, true, true);
-            const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B);
-            const uint64_t dqm = sdesc(sWQ + 8192, 16384, 1024, SW_128B);  // Q blocks 16 KB apart
+            const uint64_t dkm = sdesc(sK, 8192, 1024, SW_128B), dqm = sdesc(sQ, 8192, 1024, SW_128B);
             const uint64_t dqk = sdesc(sDQK, 16, 1024, SW_128B), dqkm = sdesc(sDQK, 8192, 1024, SW_128B);
 #pragma unroll
             for (int s2 = 0; s2 < 4; ++s2) {
                 mma_bf16_ss(tQ2, desc_add(dkm, s2 * 2048), desc_add(dqk, s2 * 32), idq, s2 > 0);
-                mma_bf16_ss(tDK, desc_add(dqm, s2 * 2048), desc_add(dqkm, s2 * 2048), idk, 1u);
+                mma_bf16_ss(tQK, desc_add(dqm, s2 * 2048), desc_add(dqkm, s2 * 2048), idk, s2 > 0);
             }
-            mma_commit(&bars[4]);
+            mma_commit(&bars[3]);
+            ++n2;
         }
-        if (tid < 64) {
-            // E1f[q*64 + row]: row sums over column quarter q; E1f[256 + (sub*4+q)*16 +
-            // col]: column sums over rows 32*sub .. +31 of column q*16 + col
-            rE1[tid] = E1f[tid] + E1f[64 + tid] + E1f[128 + tid] + E1f[192 + tid];
-            const int qq = tid >> 4, col = tid & 15;
-            cE1[tid] = E1f[256 + (0 * 4 + qq) * 16 + col] + E1f[256 + (1 * 4 + qq) * 16 + col];
-        } else if (warp == 2) {
+        // sums over the chunk while phase 2 runs: <dS1, S0> (warp 2) and
+        // sum_i exp(G_C - G_i) eR_i (warp 5)
+        if (warp == 2) {
             float ip = 0.f;
             for (int i = lane; i < 512; i += 32) ip += red[i];
-            // sum_i exp(G_C - G_i) eR_i over the chunk's 64 tokens
-            const float eR0 = eRp[lane] + eRp[64 + lane] + eRp[128 + lane] + eRp[192 + lane];
-            const float eR1 = eRp[32 + lane] + eRp[96 + lane] + eRp[160 + lane] + eRp[224 + lane];
-            float es = expf(GC - Gs[lane]) * eR0 + expf(GC - Gs[32 + lane]) * eR1;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                ip += __shfl_xor_sync(0xffffffffu, ip, off);
-                es += __shfl_xor_sync(0xffffffffu, es, off);
+            for (int off = 16; off > 0; off >>= 1) ip += __shfl_xor_sync(0xffffffffu, ip, off);
+            if (lane == 0) fin[0] = ip;
+        } else if (warp == 5) {
+            const float GC = Gs[63];
+            float es = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = lane + 32 * hh;
+                es += expf(GC - Gs[t]) * (eRp[t] + eRp[64 + t] + eRp[128 + t] + eRp[192 + t]);
             }
-            __syncwarp();
-            if (lane == 0) {  // read after the next barrier
-                red[0] = ip;
-                red[1] = es;
-            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) es += __shfl_xor_sync(0xffffffffu, es, off);
+            if (lane == 0) fin[1] = es;
         }
-        if (ok) ok = mbar_wait(&bars[4], ph, err, 8);
+        ok = mbar_wait(&bars[3], ph, err, 8) && ok;
         __syncwarp();
         fence_after_sync();
-        if (tid == kQkIssuer) bulk_wait_read0();  // the previous dq store no longer reads the dq tile
-        __syncthreads();                  // Q, K, dQK free; dq tile writable
-        if (tid == 96 && ok && has_next) load_B(nxt);
+        fence_before_sync();
+        ok = __syncthreads_and(ok);  // Q, K, dQK free; fin visible
+        fence_after_sync();
+        if (!ok) break;
+        if (tid == kIssuer && has_next) {
+            load_B(nxt);
+            ++nb;
+        }
+        // ---- epilogue 2: dq (transposed into the dq tile), the dK^T part, dG
         {
-            const int cb = qtr * 16;
+            const int k = lanerow;
+            const float GC = Gs[63];
+            float q1[16], q2[16];
+            tmem_load16f2(tQ1 + lanebase + cb, tQ2 + lanebase + cb, q1, q2);
             unsigned char* dqt = sm + qk::DQ;
-            unsigned char* kt = sm + qk::U + (lanerow >> 6) * 8192;  // U is dead after phase 2
 #pragma unroll
-            for (int c0 = 0; c0 < 16; c0 += 16) {
-                float q1[16], q2[16], kk[16];
-                tmem_load16f3(tQ1 + lanebase + cb + c0, tQ2 + lanebase + cb + c0, tDK + lanebase + cb + c0, q1,
-                              q2, kk);
+            for (int j = 0; j < 16; ++j) q1[j] = gs[cb + j] * q1[j] + q2[j];  // dq of the normalised row
+            if (kRaw) {
+                // dq_raw = (dq - q (q . dq)) / |q_raw|, q the normalised row (read from its
+                // global copy: the Q tile already holds the next chunk's); the dot over k
+                // is a column sum over TMEM lanes (this warp's 32, then the 4 quarters)
+                float qh[16], pr[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *(bf16*)(dqt + tile_off(64, cb + c0 + j, lanerow)) =
-                        __float2bfloat16_rn(gs[cb + c0 + j] * q1[j] + q2[j]);
-                *(uint4*)(kt + sw128_off(lanerow & 63, cb + c0)) = pack8(kk);
-                *(uint4*)(kt + sw128_off(lanerow & 63, cb + c0 + 8)) = pack8(kk + 8);
+                for (int j = 0; j < 16; ++j) {
+                    const int t = t0 + cb + j;
+                    qh[j] = (t < d.T && k < d.K)
+                                ? __bfloat162float(raw.qn[(((int64_t)b * d.T + t) * d.H + h) * d.K + k])
+                                : 0.f;
+                    pr[j] = qh[j] * q1[j];
+                }
+                const float sdot = warp_colsum16(pr);
+                if (lane < 16) dotp[sub * 64 + cb + lane] = sdot;
+                __syncthreads();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = cb + j;
+                    const float sd = dotp[t] + dotp[64 + t] + dotp[128 + t] + dotp[192 + t];
+                    q1[j] = rqs[t] * (q1[j] - qh[j] * sd);
+                }
             }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) *(bf16*)(dqt + tile_off(64, cb + j, k)) = __float2bfloat16_rn(q1[j]);
+            float dk[16], qkv[16];
+            tmem_load16f2(tDK + lanebase + cb, tQK + lanebase + cb, dk, qkv);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dk[j] = expf(GC - Gs[cb + j]) * dk[j] + qkv[j];
+            unsigned char* kp = sm + qk::DKP + (k >> 6) * 8192;
+            *(uint4*)(kp + sw128_off(k & 63, cb)) = pack8(dk);
+            *(uint4*)(kp + sw128_off(k & 63, cb + 8)) = pack8(dk + 8);
         }
         if (tid < 64) {
-            const float eR = eRp[tid] + eRp[64 + tid] + eRp[128 + tid] + eRp[192 + tid];
-            const float dG1 = dG1p[tid] + dG1p[64 + tid] + dG1p[128 + tid] + dG1p[192 + tid];
-            float g = gs[tid] * dG1 + rE1[tid] - cE1[tid] - expf(GC - Gs[tid]) * eR;
-            if (tid == 63) g += gC * red[0] + red[1];
-            dGp[(int64_t)row0 + tid] = g;
+            const int t = tid;
+            const float GC = Gs[63], gC = gs[63];
+            const float dG1 = dG1p[t] + dG1p[64 + t] + dG1p[128 + t] + dG1p[192 + t];
+            const float eR = eRp[t] + eRp[64 + t] + eRp[128 + t] + eRp[192 + t];
+            const float re = rE1[t] + rE1[64 + t] + rE1[128 + t] + rE1[192 + t];
+            const int qq = t >> 4, col = t & 15;
+            const float ce = cE1[(0 * 4 + qq) * 16 + col] + cE1[(1 * 4 + qq) * 16 + col];
+            float g = gs[t] * dG1 + re - ce - expf(GC - Gs[t]) * eR;
+            if (t == 63) g += gC * fin[0] + fin[1];
+            dGp[(int64_t)row0 + t] = g;
         }
         fence_proxy_async();
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        if (tid == kQkIssuer && ok) {
+        if (tid == kIssuer && ok) {
             for (int j = 0; j < 2; ++j) {
-                tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
-                tma_store_2d(&tm_dKp, sm + qk::U + j * 8192, 0, krow0 + 64 * j);
+                if (64 * j < d.K) tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
+                tma_store_2d(&tm_dKp, sm + qk::DKP + j * 8192, 0, krow0 + 64 * j);
             }
             bulk_commit();
         }
         if (!ok) break;
     }
-    if (tid == kQkIssuer) {
-        if (!ok) {  // prefetches of the next chunk may still be in flight (bounded waits)
-            mbar_wait(&bars[0], (n + 1) & 1, nullptr, 0);
-            mbar_wait(&bars[5], (n + 1) & 1, nullptr, 0);
-            mbar_wait(&bars[1], (n + 1) & 1, nullptr, 0);
+    if (tid == kIssuer) {
+        if (!ok) {  // the last loads and MMAs issued may still be in flight (bounded waits)
+            if (na > 0) mbar_wait(&bars[0], (na - 1) & 1, nullptr, 0);
+            if (nb > 0) mbar_wait(&bars[1], (nb - 1) & 1, nullptr, 0);
+            if (n1 > 0) mbar_wait(&bars[2], (n1 - 1) & 1, nullptr, 0);
+            if (n2 > 0) mbar_wait(&bars[3], (n2 - 1) & 1, nullptr, 0);
         }
         bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     }
@@ -943,7 +942,7 @@ constexpr int DV = DU;     // outputs [64 x 128] into dead slots
 constexpr int DK = DT;     // dT / E and Y / ID: dead once phase 4's MMA is done, not
                            // rewritten before the next chunk's first MMA completes
 constexpr int VEC = Y + 8192;  // per-token and partial-sum vectors
-constexpr int NVEC = 15 * 64;
+constexpr int NVEC = 19 * 64;  // 15 x 64, then (raw prologue) sigmoid(a), 1/|k_raw|, k.dk halves
 constexpr int BAR = VEC + NVEC * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
@@ -962,13 +961,15 @@ static_assert(DK + 16384 == VEC, "the dK tile spans the dT and Y tiles");
 // whole rows.  dK is staged in the dT and Y tiles, so every input slot is free once
 // phase 4's MMA is done: the next chunk's tiles are requested then, and warp 3
 // reads the next chunk's per-token values into registers a chunk ahead.
+template <bool kRaw>
 __global__ void __launch_bounds__(256, 2)
 grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_dWt, const __grid_constant__ CUtensorMap tm_dU,
            const __grid_constant__ CUtensorMap tm_T, const __grid_constant__ CUtensorMap tm_dk,
            const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dKp,
            const bf16* __restrict__ alpha, const bf16* __restrict__ beta, const float* __restrict__ G,
-           const float* __restrict__ dGp, bf16* __restrict__ dalpha, bf16* __restrict__ dbeta, int* err) {
+           const float* __restrict__ dGp, bf16* __restrict__ dalpha, bf16* __restrict__ dbeta, RawPrologue raw,
+           int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* vec = (float*)(sm + wy::VEC);
@@ -982,6 +983,9 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     float* dB3p = vec + 576;    // [2 column halves][64]
     float* rE2p = vec + 704;    // [2][64]
     float* cE2 = vec + 832;     // [2][64]
+    float* sas = vec + 960;     // raw prologue: sigmoid(a) = 1 - alpha
+    float* rks = vec + 1024;    // raw prologue: 1 / |k_raw|
+    float* kdot = vec + 1088;   // raw prologue: k.dk over each half of the columns [2][64]
     uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0] loads, [1] MMA, [2] dK partial
     uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 32);
     int* s_next = (int*)(sm + wy::BAR + 40);  // the chunk after this one
@@ -1015,7 +1019,8 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     };
     // warp 3: G, the dG partial and the gates of tokens 2 lane, 2 lane + 1 of a chunk
     // (padding: alpha = 1, beta = 0), held in registers until the chunk starts
-    float2 gv = make_float2(0.f, 0.f), qv = gv;
+    // (with the raw prologue: the gate logits, padding a = b = -inf, and 1 / |k_raw|)
+    float2 gv = make_float2(0.f, 0.f), qv = gv, kv = gv;
     bf16 ga[2], gb[2];
     auto load_vec = [&](int64_t ch) {
         int b, h, t0;
@@ -1023,17 +1028,20 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const int64_t row0 = ch * kC;
         gv = *(const float2*)(G + row0 + 2 * lane);
         qv = *(const float2*)(dGp + row0 + 2 * lane);
+        float kr[2] = {0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * lane + e;
-            ga[e] = __float2bfloat16_rn(1.f);
-            gb[e] = __float2bfloat16_rn(0.f);
+            ga[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 1.f);
+            gb[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 0.f);
             if (t < d.T) {
                 const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
                 ga[e] = alpha[gi];
                 gb[e] = beta[gi];
+                if (kRaw) kr[e] = raw.rk[gi];
             }
         }
+        kv = make_float2(kr[0], kr[1]);
     };
 
     const int64_t first = blockIdx.x;
@@ -1086,15 +1094,23 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 *s_next = nx;
                 if (nx < nchunks) claimed = (int)gridDim.x + atomicAdd(err + kSchedWy, 1);
             }
-            const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y};
+            const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y}, k2[2] = {kv.x, kv.y};
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int p = 2 * lane + e;
                 Gs[p] = g2[e];
                 gs[p] = expf(g2[e]);
-                bs[p] = __bfloat162float(gb[e]);
-                as_[p] = __bfloat162float(ga[e]);
                 dGq[p] = q2[e];
+                if (kRaw) {  // alpha = sigmoid(-a), beta = sigmoid(b)
+                    const float a = __bfloat162float(ga[e]), bl = __bfloat162float(gb[e]);
+                    as_[p] = 1.f / (1.f + expf(a));
+                    sas[p] = 1.f / (1.f + expf(-a));
+                    bs[p] = 1.f / (1.f + expf(-bl));
+                    rks[p] = k2[e];
+                } else {
+                    bs[p] = __bfloat162float(gb[e]);
+                    as_[p] = __bfloat162float(ga[e]);
+                }
             }
             if (nx < nchunks) load_vec(nx);  // used next iteration
         }
@@ -1272,7 +1288,8 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         fence_after_sync();
         // ---- phase 4: dK = T1^T dW + E K + E^T K + dK_partial (N=128, tokens on rows 64-127)
         if (tid == 0 && ok) {
-            for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
+            for (int j = 0; j < 2; ++j)
+                if (64 * j < d.V) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
             ok = mbar_wait(&bars[2], ph, err, 16);
             if (ok) {
@@ -1320,8 +1337,14 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 if (t < d.T) {
                     const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
                     const int p = pos[e];
-                    dalpha[gi] = __float2bfloat16_rn(run[e] / as_[p]);
-                    dbeta[gi] = __float2bfloat16_rn(cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p]);
+                    const float dbv = cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p];
+                    if (kRaw) {  // d log alpha / da = -sigmoid(a); d beta / db = beta (1 - beta)
+                        dalpha[gi] = __float2bfloat16_rn(-run[e] * sas[p]);
+                        dbeta[gi] = __float2bfloat16_rn(dbv * bs[p] * (1.f - bs[p]));
+                    } else {
+                        dalpha[gi] = __float2bfloat16_rn(run[e] / as_[p]);
+                        dbeta[gi] = __float2bfloat16_rn(dbv);
+                    }
                 }
             }
         }
@@ -1335,13 +1358,54 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             load_inputs(nxt);
             trk |= 1;
         }
+        // the normalised k row r, columns 64*half + 32*g .. +32 (raw prologue), from its
+        // global copy (the K tile takes the next chunk's)
+        auto krow32 = [&](int g, float* kk) {
+            const int t = t0 + r, c0 = 64 * half + 32 * g;
+            const bool in = t < d.T && c0 < d.K;
+            const uint4* kg = (const uint4*)(raw.kn + (((int64_t)b * d.T + (in ? t : 0)) * d.H + h) * d.K + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 x = in ? kg[q] : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    kk[8 * q + 2 * e] = bf_lo(w4[e]);
+                    kk[8 * q + 2 * e + 1] = bf_hi(w4[e]);
+                }
+            }
+        };
+        if (kRaw) {
+            // dk_raw = (dk - k (k . dk)) / |k_raw|: k . dk over this half of the columns
+            if (!urow) {
+                float part = 0.f;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    float x[32], kk[32];
+                    tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
+                    krow32(g, kk);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) part += x[j] * kk[j];
+                }
+                kdot[half * 64 + r] = part;
+            }
+            __syncthreads();
+        }
         if (!urow) {
             // dK row a = r (token), columns 64*half .. +64 -> dk tile (dT / E and Y / ID are dead)
             unsigned char* dkt = sm + wy::DK + half * 8192;
+            const float sd = kRaw ? kdot[r] + kdot[64 + r] : 0.f;
+            const float rr = kRaw ? rks[r] : 0.f;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 float x[32];
                 tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
+                if (kRaw) {
+                    float kk[32];
+                    krow32(g, kk);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = rr * (x[j] - kk[j] * sd);
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) *(uint4*)(dkt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);
             }
@@ -1351,7 +1415,8 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         ok = __syncthreads_and(ok);
         fence_after_sync();
         if (tid == 0 && ok) {
-            for (int j = 0; j < 2; ++j) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
+            for (int j = 0; j < 2; ++j)
+                if (64 * j < d.K) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
         }
         if (!ok) break;
@@ -1379,9 +1444,9 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
     using P = BScan<Vt>;
     CUtensorMap mq, mk, mW, mM, mdo, mdU, mdS1;
     const int64_t rows = d.NS() * d.NC * kC;
-    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
+    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, d.K) || !tmap_bthd(&mk, k, d.B, d.T, d.H, d.K) ||
         !tmap_rows(&mW, tb.W, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC) ||
-        !tmap_core8_bthd(&mdo, d_o, d.B, d.T, d.H, kD, Vt / 8) ||
+        !tmap_core8_bthd(&mdo, d_o, d.B, d.T, d.H, d.V, Vt / 8) ||
         !tmap_core8_rows(&mdU, bb.dU, rows, kD, kC, Vt / 8) ||
         !tmap_core8_rows(&mdS1, bb.dS1, d.NS() * d.NC * kD, kD, kD, Vt / 8))
         return cudaErrorInvalidValue;
@@ -1409,41 +1474,50 @@ cudaError_t launch_scan_bwd_tc(const Dims& d, const void* q, const void* k, cons
 }
 
 cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const void* d_o, const TcBufs& tb,
-                              const __nv_bfloat16* states, const TcBwdBufs& bb, void* dq, cudaStream_t st) {
-    CUtensorMap mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, mdKp, mdWt;
+                              const __nv_bfloat16* states, const TcBwdBufs& bb, void* dq, cudaStream_t st,
+                              const RawPrologue* rp) {
+    // tb.Ut holds U: the forward scan that wrote the chunk-start states wrote U over U~
+    CUtensorMap mq, mk, mdo, mU, mdU, mS0, mdS1, mdq, mdKp, mdWt;
     const int64_t rows = d.NS() * d.NC * kC;
     const int64_t krows = d.NS() * d.NC * kD;
-    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
-        !tmap_bthd(&mdo, d_o, d.B, d.T, d.H, kD) || !tmap_rows(&mW, tb.W, rows, kD) ||
+    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, d.K) || !tmap_bthd(&mk, k, d.B, d.T, d.H, d.K) ||
+        !tmap_bthd(&mdo, d_o, d.B, d.T, d.H, d.V) || !tmap_rows(&mU, tb.Ut, rows, kD) ||
         !tmap_rows(&mdU, bb.dU, rows, kD) || !tmap_rows(&mS0, states, krows, kD) ||
-        !tmap_rows(&mdS1, bb.dS1, krows, kD) || !tmap_bthd(&mdq, dq, d.B, d.T, d.H, kD) ||
+        !tmap_rows(&mdS1, bb.dS1, krows, kD) || !tmap_bthd(&mdq, dq, d.B, d.T, d.H, d.K) ||
         !tmap_rows(&mdKp, bb.dKp, krows, kC) || !tmap_rows(&mdWt, bb.dWt, krows, kC))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(grad_qk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::SMEM);
+    RawPrologue raw{};
+    if (rp && rp->on) raw = *rp;
+    auto kern = raw.on ? grad_qk_tc<true> : grad_qk_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::SMEM);
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;
     dim3 grid((unsigned)std::min<int64_t>(nchunks, sm_count()));
-    grad_qk_tc<<<grid, 512, qk::SMEM, st>>>(d, mq, mk, mdo, mW, mdU, mS0, mdS1, mdq, mdKp, mdWt, tb.Ut, tb.Mqk,
-                                            tb.G, bb.dGp, tb.err);
+    kern<<<grid, 512, qk::SMEM, st>>>(d, mq, mk, mdo, mU, mdU, mS0, mdS1, mdq, mdKp, mdWt, tb.Mqk, tb.G,
+                                            bb.dGp, raw, tb.err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const void* alpha, const void* beta,
                               const TcBufs& tb, const TcBwdBufs& bb, void* dk, void* dv, void* dalpha, void* dbeta,
-                              cudaStream_t st) {
+                              cudaStream_t st, const RawPrologue* rp) {
     CUtensorMap mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp;
     const int64_t rows = d.NS() * d.NC * kC;
     const int64_t krows = d.NS() * d.NC * kD;
-    if (!tmap_bthd(&mk, k, d.B, d.T, d.H, kD) || !tmap_bthd(&mv, v, d.B, d.T, d.H, kD) ||
+    if (!tmap_bthd(&mk, k, d.B, d.T, d.H, d.K) || !tmap_bthd(&mv, v, d.B, d.T, d.H, d.V) ||
         !tmap_rows(&mdWt, bb.dWt, krows, kC) || !tmap_rows(&mdU, bb.dU, rows, kD) ||
-        !tmap_rows(&mT, tb.T, rows, kC) || !tmap_bthd(&mdk, dk, d.B, d.T, d.H, kD) ||
-        !tmap_bthd(&mdv, dv, d.B, d.T, d.H, kD) || !tmap_rows(&mdKp, bb.dKp, krows, kC))
+        !tmap_rows(&mT, tb.T, rows, kC) || !tmap_bthd(&mdk, dk, d.B, d.T, d.H, d.K) ||
+        !tmap_bthd(&mdv, dv, d.B, d.T, d.H, d.V) || !tmap_rows(&mdKp, bb.dKp, krows, kC))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(grad_wy_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wy::SMEM);
+    RawPrologue raw{};
+    if (rp && rp->on) raw = *rp;
+    auto kern = raw.on ? grad_wy_tc<true> : grad_wy_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wy::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)std::min<int64_t>(d.NS() * d.NC, 2 * sm_count()));
-    grad_wy_tc<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp, (const bf16*)alpha,
-                                            (const bf16*)beta, tb.G, bb.dGp, (bf16*)dalpha, (bf16*)dbeta, tb.err);
+    kern<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp, (const bf16*)alpha,
+                                            (const bf16*)beta, tb.G, bb.dGp, (bf16*)dalpha, (bf16*)dbeta, raw,
+                                            tb.err);
     return cudaGetLastError();
 }
 

@@ -22,7 +22,9 @@
 //     S1^T = gamma_C S0^T + K^T Uh    (M=128 MMA, on the chunk-to-chunk chain)
 //     O = diag(gamma) Y + Mqk U       (M=128 MMA, rows 64-127)
 //   with warps 0-7 on the epilogues, warp 8 issuing the MMAs and warp 9 the TMA
-//   copies, and the next chunks' tiles prefetched NS stages ahead.
+//   copies, and the next chunks' tiles prefetched NS stages ahead.  A scan that
+//   writes the chunk-start states for the backward also writes U (bf16) in place
+//   over its U~ slice: the backward's chunk gradients read U, never U~.
 //
 // Every wait is bounded (2 s); a wait that gives up raises the error flag, and
 // the block leaves its loop together (block-wide vote) after draining its copies.
@@ -46,6 +48,9 @@ constexpr int kD = 128;  // K = V = 128
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNormEps = 1e-6f;  // q, k normalisation: x / sqrt(sum x^2 + eps)
 
 constexpr int kAS = 68;  // fp32 row stride of A and T in shared memory (16-byte aligned rows)
 constexpr int kXS = 36;  // fp32 row stride of the solve's scratch block
@@ -190,12 +195,14 @@ static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 // A chunk's Q tiles are replaced by the next chunk's once the Gram MMA is done, its
 // K and V tiles once the W / Ut MMA is done (both requested by thread 128, whose
 // warp has no Gram epilogue work); warp 2 keeps the next chunk's gates in registers.
+template <bool kRaw>
 __global__ void __launch_bounds__(256, 2)
 prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_W,
             const __grid_constant__ CUtensorMap tm_U, const __grid_constant__ CUtensorMap tm_M,
             const bf16* __restrict__ alpha, const bf16* __restrict__ beta, float* __restrict__ Gout,
-            bf16* __restrict__ Tout, int* err) {
+            bf16* __restrict__ Tout, RawPrologue raw, const __grid_constant__ CUtensorMap tm_qn,
+            const __grid_constant__ CUtensorMap tm_kn, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* Af = (float*)(sm + P_AF);
@@ -225,26 +232,31 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_arrive_expect_tx(&bars[0], 2 * 8192);
         for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_Q0 + j * 16384, &tm_q, &bars[0], 64 * j, h, t0, b);
     };
-    // K first: the next Gram MMA waits for it, V only for the W / Ut MMA
-    auto load_kv = [&](int64_t ch) {
+    // K (the next Gram MMA waits for it) and V (only the W / Ut MMA reads it)
+    auto load_k = [&](int64_t ch) {
         int b, h, t0;
         decode(ch, b, h, t0);
         mbar_arrive_expect_tx(&bars[1], 2 * 8192);
         for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_K0 + j * 16384, &tm_k, &bars[1], 64 * j, h, t0, b);
+    };
+    auto load_v = [&](int64_t ch) {
+        int b, h, t0;
+        decode(ch, b, h, t0);
         mbar_arrive_expect_tx(&bars[4], 2 * 8192);
         for (int j = 0; j < 2; ++j) tma_load_4d(sm + P_V0 + j * 16384, &tm_v, &bars[4], 64 * j, h, t0, b);
     };
     // warp 2: gates of tokens 2 lane, 2 lane + 1 of a chunk; padding (alpha = 1,
     // beta = 0) leaves the state unchanged
     bf16 ga[2], gb[2];
+    // (with kRaw the gate logits; padding a = b = -inf gives alpha = 1, beta = 0)
     auto load_gates = [&](int64_t ch) {
         int b, h, t0;
         decode(ch, b, h, t0);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * lane + e;
-            ga[e] = __float2bfloat16_rn(1.f);
-            gb[e] = __float2bfloat16_rn(0.f);
+            ga[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 1.f);
+            gb[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 0.f);
             if (t < d.T) {
                 const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
                 ga[e] = alpha[gi];
@@ -259,7 +271,8 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_mbar_init();
         if (first < nchunks) {
             load_q(first);
-            load_kv(first);
+            load_k(first);
+            load_v(first);
         }
     }
     if (warp == 1) {
@@ -273,7 +286,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t tmem = *tslot;
     bool ok = true;
     int n = 0;
-    int nq = first < nchunks ? 1 : 0, nkv = nq;  // load batches issued (thread kLoader's count)
+    int nq = first < nchunks ? 1 : 0, nk = nq, nv = nq;  // load batches issued (thread kLoader's count)
     int g_last = -1, w_last = -1;               // chunks whose MMAs were issued (thread 0)
 #pragma unroll 1
     for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
@@ -281,6 +294,53 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int64_t nxt = ch + gridDim.x;
         const bool has_next = nxt < nchunks;
         const int row0 = (int)(ch * kC);
+        if (kRaw) {
+            // Raw q, k rows to unit length as they land, before the Gram MMA reads them
+            // (q = q_raw (sum q_raw^2 + 1e-6)^-1/2, the same for k): thread pairs hold the
+            // two 64-column halves of one row of the K (threads 0-127) or Q tile.
+            int b, h, t0;
+            decode(ch, b, h, t0);
+            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[1], ph, err, 1) && ok;
+            {
+                const bool isq = tid >= 128;
+                const int rr = (tid >> 1) & 63, hf = tid & 1;
+                unsigned char* rowp = sm + (isq ? P_Q0 : P_K0) + hf * 16384 + rr * 128;
+                uint4 x[8];
+                float ss = 0.f;
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    x[p] = *(const uint4*)(rowp + p * 16);
+                    const uint32_t w4[4] = {x[p].x, x[p].y, x[p].z, x[p].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) ss += bf_lo(w4[e]) * bf_lo(w4[e]) + bf_hi(w4[e]) * bf_hi(w4[e]);
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                const float rn = rsqrtf(ss + kNormEps);
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const uint32_t w4[4] = {x[p].x, x[p].y, x[p].z, x[p].w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o4[e] = pack_bf16(rn * bf_lo(w4[e]), rn * bf_hi(w4[e]));
+                    *(uint4*)(rowp + p * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                }
+                if (hf == 0 && t0 + rr < d.T) (isq ? raw.rq : raw.rk)[((int64_t)b * d.T + t0 + rr) * d.H + h] = rn;
+            }
+            fence_proxy_async();
+            fence_before_sync();
+            ok = __syncthreads_and(ok);
+            fence_after_sync();
+            if (!ok) break;
+            if (tid == kLoader) {  // the normalised rows, for the scan and the backward
+                for (int j = 0; j < 2; ++j) {
+                    if (64 * j >= d.K) continue;
+                    tma_store_4d(&tm_qn, sm + P_Q0 + j * 16384, 64 * j, h, t0, b);
+                    tma_store_4d(&tm_kn, sm + P_K0 + j * 16384, 64 * j, h, t0, b);
+                }
+                bulk_commit();
+            }
+        }
         if (tid == 0) {
             ok = mbar_wait(&bars[0], ph, err, 1) && ok;
             ok = mbar_wait(&bars[1], ph, err, 1) && ok;
@@ -299,7 +359,20 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             bulk_wait_read0();  // the previous chunk's stores have read the A, T and Mqk tiles
         }
         if (warp == 2) {
-            const float l[2] = {log2f(__bfloat162float(ga[0])), log2f(__bfloat162float(ga[1]))};
+            // log2 alpha, beta; from the logits: log alpha = -softplus(a), beta = sigmoid(b)
+            float l[2], bv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (kRaw) {
+                    const float a = __bfloat162float(ga[e]), bl = __bfloat162float(gb[e]);
+                    const float sp = a > 0.f ? a + log1pf(expf(-a)) : log1pf(expf(a));
+                    l[e] = -sp * kLog2e;
+                    bv[e] = 1.f / (1.f + expf(-bl));
+                } else {
+                    l[e] = log2f(__bfloat162float(ga[e]));
+                    bv[e] = __bfloat162float(gb[e]);
+                }
+            }
             const float pair = l[0] + l[1];
             float incl = pair;
 #pragma unroll
@@ -312,8 +385,8 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             G2s[2 * lane + 1] = g1;
             gs[2 * lane] = exp2f(g0);
             gs[2 * lane + 1] = exp2f(g1);
-            bs[2 * lane] = __bfloat162float(gb[0]);
-            bs[2 * lane + 1] = __bfloat162float(gb[1]);
+            bs[2 * lane] = bv[0];
+            bs[2 * lane + 1] = bv[1];
             constexpr float kLn2 = 0.693147180559945309f;
             *(float2*)(Gout + (int64_t)row0 + 2 * lane) = make_float2(g0 * kLn2, g1 * kLn2);
             if (has_next) load_gates(nxt);  // consumed next iteration
@@ -323,6 +396,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         __syncwarp();
         fence_after_sync();
         if (tid == kLoader && ok && has_next) {  // the Q tiles are free
+            if (kRaw) bulk_wait_read0();  // the normalised rows' stores have read them
             load_q(nxt);
             ++nq;
         }
@@ -437,8 +511,10 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         __syncwarp();
         fence_after_sync();
         if (tid == kLoader && ok && has_next) {  // the K and V tiles are free
-            load_kv(nxt);
-            ++nkv;
+            load_k(nxt);
+            load_v(nxt);
+            ++nk;
+            ++nv;
         }
         // Epilogue: row rr of W (lanes 0-63) or Ut (lanes 64-127), 64 columns per warp,
         // into the dead T (W) and A (Ut) regions as 128B-swizzled K-major tiles.
@@ -478,17 +554,15 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (!ok) {  // bounded waits for what is still in flight before the CTA leaves
         if (tid == kLoader) {
             for (int i = n; i < nq; ++i) mbar_wait(&bars[0], i & 1, nullptr, 0);
-            for (int i = n; i < nkv; ++i) {
-                mbar_wait(&bars[1], i & 1, nullptr, 0);
-                mbar_wait(&bars[4], i & 1, nullptr, 0);
-            }
+            for (int i = n; i < nk; ++i) mbar_wait(&bars[1], i & 1, nullptr, 0);
+            for (int i = n; i < nv; ++i) mbar_wait(&bars[4], i & 1, nullptr, 0);
         }
         if (tid == 0) {
             if (g_last == n) mbar_wait(&bars[2], n & 1, nullptr, 0);
             if (w_last == n) mbar_wait(&bars[3], n & 1, nullptr, 0);
         }
     }
-    if (tid == 0) bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
+    if (tid == 0 || tid == kLoader) bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     __syncwarp();
     fence_before_sync();
     __syncthreads();
@@ -651,7 +725,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int64_t cbase = ((int64_t)b * d.H + h) * d.NC + c0;  // global index of chunk c = 0
     const float ut_w = tr ? 0.f : 1.f;
     float* const s_out = tr ? trans : sT;
-    const bool wr_o = write_o && !tr, wr_states = write_states && !tr;
+    // a slice wholly past the caller's V (V = 64) has no output columns
+    const bool wr_o = write_o && !tr && v0 < d.V, wr_states = write_states && !tr;
 
     // Chunk c's tiles into stage c % NS (the n-th use of a stage completes phase n & 1).
     auto issue_loads = [&](int c) {
@@ -685,8 +760,11 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
     for (int j = 0; j < HV; ++j) {
         const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
+        // the caller's state is [V, K] (K, V = 64 or 128); rows and columns past them are zero
         const bool vok = (kD % Vt == 0) || v < kD;
-        s[j] = (!epi || !vok) ? 0.f : (tr ? (v == k ? 1.f : 0.f) : (s0 ? s0[(sidx * d.V + v) * kD + k] : 0.f));
+        const bool uok = v < d.V && k < d.K;
+        s[j] = (!epi || !vok) ? 0.f
+                              : (tr ? (v == k ? 1.f : 0.f) : ((s0 && uok) ? s0[(sidx * d.V + v) * d.K + k] : 0.f));
     }
     auto write_state_operand = [&]() {
         // MN-major, no swizzle: element (v, k) at (v/8)*2048 + k*16 + (v%8)*2
@@ -820,14 +898,24 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (!ok) break;
             fence_after_sync();
             if (tma_issuer) {
+                // U of this chunk, in place over its U~ slice (read by this CTA only,
+                // and already consumed), for the backward's chunk gradients
+                if (wr_states) {
+                    tma_store_3d(&tm_Ut, sm + P::U_OP, 0, (int)((cbase + c) * kC), v0 / 8);
+                    bulk_commit();
+                }
                 if (c > 0 && wr_o) {  // output tile of the previous chunk
                     tma_store_5d(&tm_o, sm + P::O_OP + ((c - 1) & 1) * (kC * Vt * 2), 0, (c0 + c - 1) * kC,
                                  v0 / 8, h, b);
                     bulk_commit();
+                    // the store issued a chunk earlier has read its tile, which the
+                    // next output epilogue rewrites; so has the U store (older group)
+                    bulk_wait_read1();
+                } else {
+                    // the U store has read its tile, which the next U epilogue rewrites
+                    if (wr_states) bulk_wait_read0();
+                    else bulk_wait_read1();
                 }
-                // the store issued a chunk earlier has read its tile, which the
-                // next output epilogue rewrites
-                bulk_wait_read1();
             }
             __syncwarp();
             fence_before_sync();
@@ -934,7 +1022,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (ok && s_out && epi) {
 #pragma unroll
         for (int j = 0; j < HV; ++j)
-            if ((kD % Vt == 0) || v0 + cb + j < kD) s_out[(sidx * d.V + v0 + cb + j) * kD + k] = s[j];
+            if (v0 + cb + j < d.V && k < d.K) s_out[(sidx * d.V + v0 + cb + j) * d.K + k] = s[j];
     }
     if (tma_issuer) {
         // on an error, the loads still in flight (bounded waits) before leaving
@@ -959,13 +1047,13 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     using P = ScanPlan<Vt>;
     CUtensorMap mq, mk, mW, mM, mUt, mo, mst;
     const int64_t rows = d.NS() * d.NC * kC;
-    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
+    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, d.K) || !tmap_bthd(&mk, k, d.B, d.T, d.H, d.K) ||
         !tmap_rows(&mW, tb.W, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC) ||
         !tmap_core8_rows(&mUt, tb.Ut, rows, kD, kC, Vt / 8))
         return cudaErrorInvalidValue;
     memset(&mo, 0, sizeof(mo));
     memset(&mst, 0, sizeof(mst));
-    if (o && !tmap_core8_bthd(&mo, o, d.B, d.T, d.H, kD, Vt / 8)) return cudaErrorInvalidValue;
+    if (o && !tmap_core8_bthd(&mo, o, d.B, d.T, d.H, d.V, Vt / 8)) return cudaErrorInvalidValue;
     if (states && !tmap_core8_rows(&mst, states, d.NS() * d.NC * kD, kD, kD, Vt / 8))
         return cudaErrorInvalidValue;
     auto kern = scan_fwd_tc<Vt>;
@@ -983,8 +1071,11 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
 
 }  // namespace
 
+// bf16 with 64-token chunks and K, V of 64 or 128: the kernels work on 128 columns
+// and TMA fills the columns past a 64-wide K or V with zeros on every load (they
+// contribute nothing to any product) and clips them on every store.
 bool tc_fwd_supported(const Dims& d, InType ty) {
-    return ty == InType::BF16 && d.K == kD && d.V == kD && d.C == kC;
+    return ty == InType::BF16 && d.C == kC && (d.K == kD || d.K == 64) && (d.V == kD || d.V == 64);
 }
 
 // The narrowest V-slice whose CTAs (one per slice and stream) fit one wave.
@@ -1020,19 +1111,28 @@ int tc_scan_vt_for(const Dims& d, const SeqMap* sq, int64_t streams) {
 }
 
 cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v, const void* alpha,
-                           const void* beta, const TcBufs& tb, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mW, mU, mM;
+                           const void* beta, const TcBufs& tb, cudaStream_t st, const RawPrologue* rp) {
+    CUtensorMap mq, mk, mv, mW, mU, mM, mqn, mkn;
     const int64_t rows = d.NS() * d.NC * kC;
-    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, kD) || !tmap_bthd(&mk, k, d.B, d.T, d.H, kD) ||
-        !tmap_bthd(&mv, v, d.B, d.T, d.H, kD) || !tmap_rows(&mW, tb.W, rows, kD) ||
+    if (!tmap_bthd(&mq, q, d.B, d.T, d.H, d.K) || !tmap_bthd(&mk, k, d.B, d.T, d.H, d.K) ||
+        !tmap_bthd(&mv, v, d.B, d.T, d.H, d.V) || !tmap_rows(&mW, tb.W, rows, kD) ||
         !tmap_rows(&mU, tb.Ut, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prep_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    RawPrologue raw{};
+    memset(&mqn, 0, sizeof(mqn));
+    memset(&mkn, 0, sizeof(mkn));
+    if (rp && rp->on) {
+        raw = *rp;
+        if (!tmap_bthd(&mqn, raw.qn, d.B, d.T, d.H, d.K) || !tmap_bthd(&mkn, raw.kn, d.B, d.T, d.H, d.K))
+            return cudaErrorInvalidValue;
+    }
+    auto kern = raw.on ? prep_fwd_tc<true> : prep_fwd_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;
     dim3 grid((unsigned)std::min<int64_t>(nchunks, 2 * sm_count()));
-    prep_fwd_tc<<<grid, 256, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
-                                              tb.G, tb.T, tb.err);
+    kern<<<grid, 256, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
+                                              tb.G, tb.T, raw, mqn, mkn, tb.err);
     return cudaGetLastError();
 }
 

@@ -59,6 +59,20 @@ def load_library():
     lib.gdn_fwd.restype = ctypes.c_int
     lib.gdn_bwd.argtypes = [P] + [_vp] * 16 + [ctypes.c_size_t, _vp]
     lib.gdn_bwd.restype = ctypes.c_int
+    for fn in ("gdn_raw_saved_bytes", "gdn_raw_fwd_workspace_bytes", "gdn_raw_bwd_workspace_bytes"):
+        getattr(lib, fn).argtypes = [P]
+        getattr(lib, fn).restype = ctypes.c_size_t
+    lib.gdn_fwd_raw.argtypes = [P] + [_vp] * 10 + [ctypes.c_size_t, _vp]
+    lib.gdn_fwd_raw.restype = ctypes.c_int
+    lib.gdn_bwd_raw.argtypes = [P] + [_vp] * 16 + [ctypes.c_size_t, _vp]
+    lib.gdn_bwd_raw.restype = ctypes.c_int
+    for fn in ("gdn_reset_saved_bytes", "gdn_reset_fwd_workspace_bytes", "gdn_reset_bwd_workspace_bytes"):
+        getattr(lib, fn).argtypes = [P, ctypes.c_int64]
+        getattr(lib, fn).restype = ctypes.c_size_t
+    lib.gdn_reset_fwd.argtypes = [P, ctypes.c_int64] + [_vp] * 11 + [ctypes.c_size_t, _vp]
+    lib.gdn_reset_fwd.restype = ctypes.c_int
+    lib.gdn_reset_bwd.argtypes = [P, ctypes.c_int64] + [_vp] * 17 + [ctypes.c_size_t, _vp]
+    lib.gdn_reset_bwd.restype = ctypes.c_int
     lib.gdn_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
     lib.gdn_fwd_noalloc.restype = ctypes.c_int
     lib.gdn_decode.argtypes = [P] + [_vp] * 7 + [_vp]
@@ -258,6 +272,100 @@ def gdn_bwd(q, k, v, alpha, beta, initial_state, d_o, d_final_state=None, *, sav
                      _ptr(initial_state), _ptr(saved), _ptr(d_o), _ptr(d_final_state),
                      _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(db), _ptr(d_initial_state),
                      _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
+    _check(st)
+    return dq, dk, dv, da, db, d_initial_state
+
+
+def gdn_raw_saved_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_raw_saved_bytes(ctypes.byref(p)))
+
+
+def gdn_raw_fwd_workspace_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_raw_fwd_workspace_bytes(ctypes.byref(p)))
+
+
+def gdn_raw_bwd_workspace_bytes(p: gdn_problem) -> int:
+    return int(load_library().gdn_raw_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def gdn_fwd_raw(q_raw, k_raw, v, a_logit, b_logit, initial_state=None, *, chunk: int = 64, o=None,
+                final_state=True, saved=False, workspace=None, stream=None):
+    """The forward with its prologue folded in (``gdn_fwd_raw``): q_raw, k_raw are
+    normalised to unit length per row and the gates come from the logits
+    (alpha = exp(-softplus(a_logit)), beta = sigmoid(b_logit)).  Shapes and
+    arguments as :func:`gdn_fwd`; ``saved`` (True or a buffer of
+    gdn_raw_saved_bytes()) feeds :func:`gdn_bwd_raw`.  Returns
+    ``(o, final_state or None, saved or None)``."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    B, T, H, K = q_raw.shape
+    V = v.shape[-1]
+    dt = q_raw.dtype
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    for t, n, sh in ((q_raw, "q_raw", (B, T, H, K)), (k_raw, "k_raw", (B, T, H, K)), (v, "v", (B, T, H, V)),
+                     (a_logit, "a_logit", (B, T, H)), (b_logit, "b_logit", (B, T, H))):
+        _need(t, n, sh, dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=dt, device=dev)
+    _need(o, "o", (B, T, H, V), dt, dev)
+    if final_state is True:
+        final_state = torch.empty((B, H, V, K), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", (B, H, V, K), torch.float32, dev)
+    if saved is True:
+        saved = torch.empty(max(gdn_raw_saved_bytes(p), 1), dtype=torch.uint8, device=dev)
+    elif saved is False:
+        saved = None
+    if workspace is None:
+        workspace = torch.empty(max(gdn_raw_fwd_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_fwd_raw(ctypes.byref(p), _ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(a_logit), _ptr(b_logit),
+                         _ptr(initial_state), _ptr(o), _ptr(final_state), _ptr(saved), _ptr(workspace), ws_bytes,
+                         _stream_handle(dev, stream))
+    _check(st)
+    return o, final_state, saved
+
+
+def gdn_bwd_raw(q_raw, k_raw, v, a_logit, b_logit, initial_state, d_o, d_final_state=None, *, saved=None,
+                chunk: int = 64, grads=None, d_initial_state=True, workspace=None, stream=None):
+    """Backward of :func:`gdn_fwd_raw` (``gdn_bwd_raw``): the gradients with respect
+    to the raw inputs.  Returns ``(dq_raw, dk_raw, dv, da_logit, db_logit,
+    d_initial_state or None)``."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
+    B, T, H, K = q_raw.shape
+    V = v.shape[-1]
+    dt = q_raw.dtype
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    for t, n, sh in ((q_raw, "q_raw", (B, T, H, K)), (k_raw, "k_raw", (B, T, H, K)), (v, "v", (B, T, H, V)),
+                     (a_logit, "a_logit", (B, T, H)), (b_logit, "b_logit", (B, T, H)),
+                     (d_o, "d_o", (B, T, H, V))):
+        _need(t, n, sh, dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    _need(d_final_state, "d_final_state", (B, H, V, K), torch.float32, dev)
+    if saved is not None and saved.numel() * saved.element_size() < gdn_raw_saved_bytes(p):
+        raise GdnError(GDN_ERR_INVALID_ARG, "saved buffer is smaller than gdn_raw_saved_bytes()")
+    if grads is None:
+        grads = (torch.empty_like(q_raw), torch.empty_like(k_raw), torch.empty_like(v),
+                 torch.empty_like(a_logit), torch.empty_like(b_logit))
+    dq, dk, dv, da, db = grads
+    if d_initial_state is True:
+        d_initial_state = torch.empty((B, H, V, K), dtype=torch.float32, device=dev)
+    elif d_initial_state is False:
+        d_initial_state = None
+    if workspace is None:
+        workspace = torch.empty(max(gdn_raw_bwd_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_bwd_raw(ctypes.byref(p), _ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(a_logit), _ptr(b_logit),
+                         _ptr(initial_state), _ptr(saved), _ptr(d_o), _ptr(d_final_state), _ptr(dq), _ptr(dk),
+                         _ptr(dv), _ptr(da), _ptr(db), _ptr(d_initial_state), _ptr(workspace), ws_bytes,
+                         _stream_handle(dev, stream))
     _check(st)
     return dq, dk, dv, da, db, d_initial_state
 
@@ -515,93 +623,134 @@ def gdn_varlen_bwd(q, k, v, alpha, beta, cu_seqlens, max_len, initial_state, d_o
     return dq, dk, dv, da, db, d_initial_state
 
 
-class ResetSegments:
-    """A dense [B, T] batch with reset positions, as the packed sequences the
-    varlen calls run: a reset at (b, t) restarts row b's stream from the zero
-    state at token t, so every row splits into segments that start at t = 0 or
-    at a reset, laid back to back in the row-major token order of the batch.
-
-    ``cu_seqlens`` (int32 [S+1]) holds the segment offsets over the B*T tokens,
-    ``first`` / ``last`` (int64 [B]) the segment index of each row's first and
-    last segment, ``max_len`` the longest segment, ``carry`` (int64) the rows
-    without a reset at t = 0, whose first segment starts from the row's initial
-    state (a reset at t = 0 discards it).  Building it reads the mask once on the
-    host (the number of segments sizes the launch)."""
-
-    def __init__(self, reset):
-        if reset.dim() != 2:
-            raise GdnError(GDN_ERR_INVALID_ARG, "reset must be a [B, T] mask")
-        B, T = reset.shape
-        dev = reset.device
-        start = reset.to(torch.bool).clone()
-        if T:
-            start[:, 0] = True
-        pos = torch.nonzero(start.reshape(-1), as_tuple=False).reshape(-1)
-        self.B, self.T, self.S = B, T, int(pos.numel())
-        self.cu_seqlens = torch.cat([pos, torch.tensor([B * T], device=dev)]).to(torch.int32)
-        lens = self.cu_seqlens[1:] - self.cu_seqlens[:-1]
-        self.max_len = int(lens.max().item()) if self.S else 0
-        self.first = torch.nonzero(pos % max(T, 1) == 0, as_tuple=False).reshape(-1) if T else pos
-        self.last = torch.cat([self.first[1:] - 1, torch.tensor([self.S - 1], device=dev)]) if T else pos
-        self.carry = torch.nonzero(~reset[:, 0].to(torch.bool), as_tuple=False).reshape(-1) if T else pos
+RESET_TOO_MANY_SEGMENTS = 1 << 29  # bit of the reset calls' error word
 
 
-def _rows_to_segments(x, seg: ResetSegments, at, rows):
-    """Per-row states [B,H,V,K] -> per-segment states [S,H,V,K]: row rows[i]'s
-    state at segment at[i], zero elsewhere."""
-    if x is None:
-        return None
-    out = torch.zeros((seg.S,) + tuple(x.shape[1:]), dtype=x.dtype, device=x.device)
-    out.index_copy_(0, at, x.index_select(0, rows))
-    return out
+def _reset_mask(reset, B, T, dev):
+    if reset is None or tuple(reset.shape) != (B, T):
+        raise GdnError(GDN_ERR_INVALID_ARG, f"reset must be a [B, T] = [{B}, {T}] mask")
+    if reset.device != dev or reset.dtype not in (torch.bool, torch.uint8) or not reset.is_contiguous():
+        raise GdnError(GDN_ERR_INVALID_ARG, "reset must be a contiguous bool or uint8 tensor on the inputs' device")
+    return reset.view(torch.uint8) if reset.dtype == torch.bool else reset
 
 
-def _all_rows(seg):
-    return torch.arange(seg.B, device=seg.cu_seqlens.device)
+def reset_segment_count(reset) -> int:
+    """The number of segments of a [B, T] reset mask: B plus the resets at t >= 1
+    (one device-to-host read; pass ``max_segments`` to the reset calls instead
+    when a bound is known)."""
+    B, T = reset.shape
+    return int(B + (int(reset[:, 1:].to(torch.int64).sum().item()) if T > 1 else 0))
 
 
-def gdn_reset_fwd(q, k, v, alpha, beta, reset, initial_state=None, *, chunk: int = 64, segments=None,
-                  saved=False, check=False, stream=None):
+def _reset_error(workspace, stream, dev):
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    stream.synchronize()
+    word = int(workspace[:4].view(torch.int32).item())
+    if word & RESET_TOO_MANY_SEGMENTS:
+        raise GdnError(GDN_ERR_INVALID_ARG, "the reset mask has more segments than max_segments")
+    if word:
+        raise GdnError(GDN_ERR_CUDA, f"kernel error word {word:#x}")
+
+
+def gdn_reset_fwd(q, k, v, alpha, beta, reset, initial_state=None, *, max_segments=None, chunk: int = 64, o=None,
+                  final_state=True, saved=False, workspace=None, check=False, stream=None):
     """Forward over a dense batch (q, k [B,T,H,K]; v [B,T,H,V]; alpha, beta
     [B,T,H]) whose streams restart from the zero state at every position where
-    ``reset`` ([B,T] bool) is set.  initial_state [B,H,V,K] feeds each row's
-    first segment.  Returns ``(o [B,T,H,V], final_state [B,H,V,K], saved,
-    segments)``; pass ``segments`` and ``saved`` on to :func:`gdn_reset_bwd`."""
-    seg = segments if segments is not None else ResetSegments(reset)
+    ``reset`` ([B,T] bool or uint8, on the device) is set (``gdn_reset_fwd``: the
+    segments are built from the mask by the library's kernels).
+    ``max_segments`` bounds the number of segments (B plus the resets at t >= 1);
+    if None it is counted with one device-to-host read.  ``check=True``
+    synchronises and raises if the kernels found more segments than the bound.
+    Returns ``(o, final_state or None, saved or None, max_segments)``; pass
+    ``saved`` and ``max_segments`` on to :func:`gdn_reset_bwd`."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
     B, T, H, K = q.shape
     V = v.shape[-1]
-    if seg.S == 0:  # no tokens: the state passes through
-        sT = (initial_state.clone() if initial_state is not None
-              else torch.zeros(B, H, V, K, dtype=torch.float32, device=q.device))
-        return torch.empty(B, T, H, V, dtype=q.dtype, device=q.device), sT, None, seg
-    flat = lambda x: x.reshape((B * T,) + tuple(x.shape[2:]))
-    s0 = _rows_to_segments(initial_state, seg, seg.first.index_select(0, seg.carry), seg.carry)
-    o, sT, sv = gdn_varlen_fwd(flat(q), flat(k), flat(v), flat(alpha), flat(beta), seg.cu_seqlens, seg.max_len,
-                               s0, chunk=chunk, saved=saved, check=check, stream=stream)
-    return o.reshape(B, T, H, V), sT.index_select(0, seg.last), sv, seg
+    dt = q.dtype
+    mask = _reset_mask(reset, B, T, dev)
+    if max_segments is None:
+        max_segments = reset_segment_count(mask)
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    for t, n, sh in ((k, "k", (B, T, H, K)), (v, "v", (B, T, H, V)), (q, "q", (B, T, H, K)),
+                     (alpha, "alpha", (B, T, H)), (beta, "beta", (B, T, H))):
+        _need(t, n, sh, dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=dt, device=dev)
+    _need(o, "o", (B, T, H, V), dt, dev)
+    if final_state is True:
+        final_state = torch.empty((B, H, V, K), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", (B, H, V, K), torch.float32, dev)
+    if saved is True:
+        saved = torch.empty(max(int(lib.gdn_reset_saved_bytes(ctypes.byref(p), max_segments)), 1),
+                            dtype=torch.uint8, device=dev)
+    elif saved is False:
+        saved = None
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.gdn_reset_fwd_workspace_bytes(ctypes.byref(p), max_segments)), 4),
+                                dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_reset_fwd(ctypes.byref(p), int(max_segments), _ptr(mask), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                           _ptr(beta), _ptr(initial_state), _ptr(o), _ptr(final_state), _ptr(saved),
+                           _ptr(workspace), ws_bytes, _stream_handle(dev, stream))
+    _check(st)
+    if check and B * T * H:
+        _reset_error(workspace, stream, dev)
+    return o, final_state, saved, max_segments
 
 
-def gdn_reset_bwd(q, k, v, alpha, beta, reset, initial_state, d_o, d_final_state=None, *, chunk: int = 64,
-                  segments=None, saved=None, check=False, stream=None):
-    """Backward of :func:`gdn_reset_fwd`: returns ``(dq, dk, dv, dalpha, dbeta,
-    d_initial_state [B,H,V,K])``."""
-    seg = segments if segments is not None else ResetSegments(reset)
+def gdn_reset_bwd(q, k, v, alpha, beta, reset, initial_state, d_o, d_final_state=None, *, max_segments=None,
+                  saved=None, chunk: int = 64, grads=None, d_initial_state=True, workspace=None, check=False,
+                  stream=None):
+    """Backward of :func:`gdn_reset_fwd` (``gdn_reset_bwd``): returns ``(dq, dk, dv,
+    dalpha, dbeta, d_initial_state [B,H,V,K] or None)``; a row reset at t = 0
+    gets a zero d_initial_state."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise GdnError(GDN_ERR_INVALID_ARG, "inputs must be CUDA tensors")
     B, T, H, K = q.shape
     V = v.shape[-1]
-    if seg.S == 0:  # no tokens: d(initial state) = d(final state)
-        ds0 = (d_final_state.clone() if d_final_state is not None
-               else torch.zeros(B, H, V, K, dtype=torch.float32, device=q.device))
-        return tuple(torch.empty_like(t) for t in (q, k, v, alpha, beta)) + (ds0,)
-    flat = lambda x: x.reshape((B * T,) + tuple(x.shape[2:]))
-    s0 = _rows_to_segments(initial_state, seg, seg.first.index_select(0, seg.carry), seg.carry)
-    dsT = _rows_to_segments(d_final_state, seg, seg.last, _all_rows(seg))
-    g = gdn_varlen_bwd(flat(q), flat(k), flat(v), flat(alpha), flat(beta), seg.cu_seqlens, seg.max_len, s0,
-                       flat(d_o), dsT, saved=saved, chunk=chunk, check=check, stream=stream)
-    grads = tuple(x.reshape(t.shape) for x, t in zip(g[:5], (q, k, v, alpha, beta)))
-    # a row whose stream was reset at t = 0 does not depend on its initial state
-    ds0 = torch.zeros(B, H, V, K, dtype=torch.float32, device=q.device)
-    ds0.index_copy_(0, seg.carry, g[5].index_select(0, seg.first.index_select(0, seg.carry)))
-    return grads + (ds0,)
+    dt = q.dtype
+    mask = _reset_mask(reset, B, T, dev)
+    if max_segments is None:
+        max_segments = reset_segment_count(mask)
+    p = make_problem(B, T, H, K, V, chunk, dt)
+    for t, n, sh in ((k, "k", (B, T, H, K)), (v, "v", (B, T, H, V)), (q, "q", (B, T, H, K)),
+                     (alpha, "alpha", (B, T, H)), (beta, "beta", (B, T, H)), (d_o, "d_o", (B, T, H, V))):
+        _need(t, n, sh, dt, dev)
+    _need(initial_state, "initial_state", (B, H, V, K), torch.float32, dev)
+    _need(d_final_state, "d_final_state", (B, H, V, K), torch.float32, dev)
+    if saved is not None and saved.numel() * saved.element_size() < int(
+            lib.gdn_reset_saved_bytes(ctypes.byref(p), max_segments)):
+        raise GdnError(GDN_ERR_INVALID_ARG, "saved buffer is smaller than gdn_reset_saved_bytes()")
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(alpha),
+                 torch.empty_like(beta))
+    dq, dk, dv, da, db = grads
+    if d_initial_state is True:
+        d_initial_state = torch.empty((B, H, V, K), dtype=torch.float32, device=dev)
+    elif d_initial_state is False:
+        d_initial_state = None
+    _need(d_initial_state, "d_initial_state", (B, H, V, K), torch.float32, dev)
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.gdn_reset_bwd_workspace_bytes(ctypes.byref(p), max_segments)), 4),
+                                dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_reset_bwd(ctypes.byref(p), int(max_segments), _ptr(mask), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                           _ptr(beta), _ptr(initial_state), _ptr(saved), _ptr(d_o), _ptr(d_final_state), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(da), _ptr(db), _ptr(d_initial_state), _ptr(workspace), ws_bytes,
+                           _stream_handle(dev, stream))
+    _check(st)
+    if check and B * T * H:
+        _reset_error(workspace, stream, dev)
+    return dq, dk, dv, da, db, d_initial_state
 
 
 def gdn_decode(q, k, v, alpha, beta, state, *, o=None, stream=None):

@@ -187,6 +187,44 @@ gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void*
                             void* stream);
 
 /*
+ * The recurrence with its prologue folded in: gdn_fwd / gdn_bwd on raw rows and
+ * gate logits ("OpenGDN", Mixer: the mixer normalises q and k to unit L2 length
+ * and computes the per-head gates in front of the operator).  Per row (b, t, h),
+ * exactly as gdn_prologue_fwd:
+ *     q = q_raw / sqrt(sum_K q_raw^2 + 1e-6)   (the same for k)
+ *     alpha = exp(-softplus(a_logit)),  beta = sigmoid(b_logit)
+ * then gdn_fwd on (q, k, v, alpha, beta); gdn_bwd_raw returns the gradients with
+ * respect to q_raw, k_raw, v, a_logit, b_logit and the initial state of
+ *     L = sum dO . o + sum d_final_state . final_state.
+ * On the tensor-core kernels (bf16, chunk 64, K and V of 64 or 128) the prologue
+ * runs inside them: the chunk kernel normalises the rows as they arrive and takes
+ * log alpha = -softplus(a) directly in fp32, and the gradient kernels return the
+ * raw inputs' gradients, so neither direction makes a separate pass over q and k.
+ * Other shapes run the prologue kernel, then gdn_fwd / gdn_bwd, inside the call.
+ *
+ *   q_raw, k_raw, dq_raw, dk_raw  [B,T,H,K] p->dtype;  v, o, d_o, dv  [B,T,H,V];
+ *   a_logit, b_logit, da_logit, db_logit  [B,T,H];  states as for gdn_fwd.
+ *   saved      : NULL, or gdn_raw_saved_bytes(p) bytes (opaque): the normalised
+ *                rows, their reciprocal norms and the forward's chunk results,
+ *                for gdn_bwd_raw on the same inputs.
+ *   workspace  : gdn_raw_fwd_workspace_bytes(p) / gdn_raw_bwd_workspace_bytes(p)
+ *                bytes; scratch, contents undefined after the call.
+ * Pointer, aliasing and error rules are those of gdn_fwd / gdn_bwd (checked before
+ * any launch).  Allocates nothing, never synchronises; asynchronous on `stream`.
+ */
+size_t gdn_raw_saved_bytes(const gdn_problem* p);
+size_t gdn_raw_fwd_workspace_bytes(const gdn_problem* p);
+size_t gdn_raw_bwd_workspace_bytes(const gdn_problem* p);
+gdn_status gdn_fwd_raw(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* v,
+                       const void* a_logit, const void* b_logit, const float* initial_state, void* o,
+                       float* final_state, void* saved, void* workspace, size_t workspace_bytes, void* stream);
+gdn_status gdn_bwd_raw(const gdn_problem* p, const void* q_raw, const void* k_raw, const void* v,
+                       const void* a_logit, const void* b_logit, const float* initial_state, const void* saved,
+                       const void* d_o, const float* d_final_state, void* dq_raw, void* dk_raw, void* dv,
+                       void* da_logit, void* db_logit, float* d_initial_state, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * Packed variable-length batches.  "OpenGDN", Scope, lists ragged batches as not
  * supported; "Sparse Delta Memory: layer and kernels", What the layer computes,
  * masks the tokens past the end of a stream.  These calls run S = p->B
@@ -240,6 +278,52 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
                           const float* initial_state, const void* saved, const void* d_o,
                           const float* d_final_state, void* dq, void* dk, void* dv, void* dalpha, void* dbeta,
                           float* d_initial_state, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Dense batches with reset masks.  "OpenGDN", Scope, lists reset masks among the
+ * features it does not support, and no page gives a formula; this library reads
+ * a reset at (b, t) as clearing the state just before token t, so that the row's
+ * stream continues from the zero state at t (the recurrence with alpha_t = 0).
+ * Each row is then a run of segments starting at t = 0 or at a reset, and the
+ * calls run them as a packed batch (gdn_varlen_fwd / gdn_varlen_bwd) over the
+ * B*T tokens of the dense tensors as they lie in memory.  The segmentation and
+ * the routing of states between rows and segments are built on the device from
+ * the mask: nothing is read back to the host.
+ *
+ *   p             : B, T, H, K, V, chunk, dtype as for gdn_fwd; q, k, v, alpha,
+ *                   beta, o, d_o and the gradients [B,T,H,...] as there.
+ *   max_segments  : an upper bound on the number of segments (B plus the number
+ *                   of resets at t >= 1), in [B, B*T] and at most 65535.
+ *                   Buffers and launches are sized by it.  More segments than the
+ *                   bound set bit 29 of the int32 at the start of the workspace,
+ *                   and the results are then not valid.
+ *   reset         : uint8 [B, T] on the device, nonzero where the stream restarts
+ *                   before that token.  A reset at t = 0 discards the row's
+ *                   initial state (and its d_initial_state is 0).
+ *   initial_state, final_state, d_final_state, d_initial_state : float32
+ *                   [B,H,V,K] or NULL, per row, as for gdn_fwd / gdn_bwd.
+ *   saved         : NULL or gdn_reset_saved_bytes(p, max_segments) bytes, from
+ *                   gdn_reset_fwd for gdn_reset_bwd with the same inputs and mask.
+ *   workspace     : gdn_reset_fwd_workspace_bytes / gdn_reset_bwd_workspace_bytes;
+ *                   its first int32 is the error word of the packed calls (bit 30:
+ *                   invalid offsets, bits 1..64: a bounded wait gave up) with
+ *                   bit 29 added; it is 0 after a successful call.
+ * Errors are returned before any launch (a NULL mask, a bound outside its range,
+ * a workspace too small, overlaps).  Allocates nothing, never synchronises;
+ * asynchronous on `stream`.
+ */
+size_t gdn_reset_saved_bytes(const gdn_problem* p, int64_t max_segments);
+size_t gdn_reset_fwd_workspace_bytes(const gdn_problem* p, int64_t max_segments);
+size_t gdn_reset_bwd_workspace_bytes(const gdn_problem* p, int64_t max_segments);
+gdn_status gdn_reset_fwd(const gdn_problem* p, int64_t max_segments, const uint8_t* reset, const void* q,
+                         const void* k, const void* v, const void* alpha, const void* beta,
+                         const float* initial_state, void* o, float* final_state, void* saved, void* workspace,
+                         size_t workspace_bytes, void* stream);
+gdn_status gdn_reset_bwd(const gdn_problem* p, int64_t max_segments, const uint8_t* reset, const void* q,
+                         const void* k, const void* v, const void* alpha, const void* beta,
+                         const float* initial_state, const void* saved, const void* d_o, const float* d_final_state,
+                         void* dq, void* dk, void* dv, void* dalpha, void* dbeta, float* d_initial_state,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Within-call sequence split (two-level scan) of the tensor-core path.  The

@@ -62,12 +62,15 @@ def test_sizes(lib):
     p = lib.make_problem(8, 4096, 6, 128, 128, 64, 1)
     NC = 64
     # bf16 K=V=128 chunk 64 runs on tensor cores: bf16 boundary states followed by
-    # the forward's chunk results (G f32; W, Ut, Mqk, T bf16), each region 256-aligned
+    # the forward's chunk results (G f32; W, U, Mqk, T bf16), each region 256-aligned
     rows = 8 * 6 * NC * 64
     expect = 8 * 6 * NC * 128 * 128 * 2 + rows * 4 + rows * 128 * 2 * 2 + rows * 64 * 2 * 2
     assert lib.gdn_saved_bytes(p) == expect
+    # bf16 K=V=64 chunk 64 also runs on tensor cores, with the same 128-wide buffers
+    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 1)) == expect
     # other shapes keep float32 boundary states
-    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 1)) == 8 * 6 * NC * 64 * 64 * 4
+    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 32, 1)) == 8 * 6 * 128 * 64 * 64 * 4
+    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 0)) == 8 * 6 * NC * 64 * 64 * 4
     assert lib.gdn_fwd_workspace_bytes(p) > 0
     assert lib.gdn_bwd_workspace_bytes(p) > lib.gdn_fwd_workspace_bytes(p)
     # ragged T rounds up to whole chunks
@@ -283,3 +286,97 @@ def test_prologue_arguments_rejected_before_launch(lib, bwd):
     h = lib.load_library()
     fn = h.gdn_prologue_bwd if bwd else h.gdn_prologue_fwd
     assert fn(ctypes.byref(empty), *([ctypes.c_void_p(None)] * names), ctypes.c_void_p(None)) == 0
+
+
+def _raw(lib, p, bwd=False, **over):
+    """gdn_fwd_raw / gdn_bwd_raw on fake, disjoint, 16-byte aligned addresses."""
+    h = lib.load_library()
+    if bwd:
+        base = dict(q=0, k=1, v=2, a=3, b=4, s0=None, saved=None, do=5, dsT=None, dq=6, dk=7, dv=8, da=9,
+                    db=10, ds0=None, ws=11)
+        order = ("q", "k", "v", "a", "b", "s0", "saved", "do", "dsT", "dq", "dk", "dv", "da", "db", "ds0", "ws")
+        fn = h.gdn_bwd_raw
+    else:
+        base = dict(q=0, k=1, v=2, a=3, b=4, s0=None, o=5, sT=None, saved=None, ws=6)
+        order = ("q", "k", "v", "a", "b", "s0", "o", "sT", "saved", "ws")
+        fn = h.gdn_fwd_raw
+    args = {n: (None if x is None else FAKE + (x << 30)) for n, x in base.items()}
+    args["ws_bytes"] = 1 << 40
+    args.update(over)
+    vp = ctypes.c_void_p
+    return fn(ctypes.byref(p), *[vp(args[n]) for n in order], args["ws_bytes"], vp(None))
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+def test_raw_arguments_rejected_before_launch(lib, bwd):
+    INVALID, UNSUP, WS = 1, 2, 3
+    for p in (lib.make_problem(2, 100, 3, 128, 128, 64, 1),   # tensor-core kernels, prologue folded in
+              lib.make_problem(2, 100, 3, 64, 32, 32, 0)):    # prologue kernel, then the recurrence
+        assert _raw(lib, p, bwd, q=None) == INVALID
+        assert "q_raw is NULL" in lib.gdn_last_error()
+        assert _raw(lib, p, bwd, b=FAKE + (4 << 30) + 8) == INVALID
+        assert "aligned" in lib.gdn_last_error()
+        assert _raw(lib, p, bwd, ws_bytes=16) == WS
+        out = "dq" if bwd else "o"
+        assert _raw(lib, p, bwd, **{out: FAKE + 64}) == INVALID  # an output on q_raw
+        assert "overlaps" in lib.gdn_last_error()
+    assert _raw(lib, lib.make_problem(1, 8, 1, 24, 16, 16, 1), bwd) == UNSUP
+
+
+def test_raw_sizes(lib):
+    tc = lib.make_problem(8, 4096, 6, 128, 128, 64, 1)
+    BTH = 8 * 4096 * 6
+    # the normalised q, k rows (bf16) and their reciprocal norms (fp32), then gdn_fwd's saved
+    raw_part = 2 * BTH * 128 * 2 + 2 * BTH * 4
+    assert lib.gdn_raw_saved_bytes(tc) == raw_part + lib.gdn_saved_bytes(tc)
+    assert lib.gdn_raw_fwd_workspace_bytes(tc) == raw_part + lib.gdn_fwd_workspace_bytes(tc)
+    assert lib.gdn_raw_bwd_workspace_bytes(tc) == raw_part + lib.gdn_bwd_workspace_bytes(tc)
+    # other shapes keep gdn_fwd's saved; the workspace holds the prologue's outputs
+    # (and, backward, the recurrence's input gradients) in the run dtype
+    f = lib.make_problem(2, 100, 3, 64, 32, 32, 0)
+    BTH = 2 * 100 * 3
+    r = lambda x: (x + 255) // 256 * 256
+    fwd_part = 2 * r(BTH * 64 * 4) + 2 * r(BTH * 4)
+    assert lib.gdn_raw_saved_bytes(f) == lib.gdn_saved_bytes(f)
+    assert lib.gdn_raw_fwd_workspace_bytes(f) == fwd_part + lib.gdn_fwd_workspace_bytes(f)
+    assert lib.gdn_raw_bwd_workspace_bytes(f) == 2 * fwd_part + lib.gdn_bwd_workspace_bytes(f)
+    assert lib.gdn_raw_fwd_workspace_bytes(lib.make_problem(1, 8, 1, 24, 16, 16, 0)) == 0
+
+
+def _reset(lib, p, S_max, bwd=False, **over):
+    """gdn_reset_fwd / gdn_reset_bwd on fake, disjoint, 16-byte aligned addresses."""
+    h = lib.load_library()
+    if bwd:
+        base = dict(mask=12, q=0, k=1, v=2, a=3, b=4, s0=None, saved=None, do=5, dsT=None, dq=6, dk=7, dv=8, da=9,
+                    db=10, ds0=None, ws=11)
+        order = ("mask", "q", "k", "v", "a", "b", "s0", "saved", "do", "dsT", "dq", "dk", "dv", "da", "db", "ds0",
+                 "ws")
+        fn = h.gdn_reset_bwd
+    else:
+        base = dict(mask=12, q=0, k=1, v=2, a=3, b=4, s0=None, o=5, sT=None, saved=None, ws=6)
+        order = ("mask", "q", "k", "v", "a", "b", "s0", "o", "sT", "saved", "ws")
+        fn = h.gdn_reset_fwd
+    args = {n: (None if x is None else FAKE + (x << 30)) for n, x in base.items()}
+    args["ws_bytes"] = 1 << 40
+    args.update(over)
+    vp = ctypes.c_void_p
+    return fn(ctypes.byref(p), S_max, *[vp(args[n]) for n in order], args["ws_bytes"], vp(None))
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+def test_reset_arguments_rejected_before_launch(lib, bwd):
+    INVALID, WS = 1, 3
+    p = lib.make_problem(3, 100, 2, 128, 128, 64, 1)
+    assert _reset(lib, p, 6, bwd, mask=None) == INVALID
+    assert "reset is NULL" in lib.gdn_last_error()
+    assert _reset(lib, p, 2, bwd) == INVALID  # fewer than one segment per row
+    assert "max_segments" in lib.gdn_last_error()
+    assert _reset(lib, p, 301, bwd) == INVALID  # more than B*T
+    assert _reset(lib, p, 6, bwd, ws_bytes=64) == WS
+    assert _reset(lib, p, 6, bwd, q=None) == INVALID  # the packed call's own checks
+    h = lib.load_library()
+    size = h.gdn_reset_bwd_workspace_bytes if bwd else h.gdn_reset_fwd_workspace_bytes
+    assert size(ctypes.byref(p), 6) > 0
+    assert size(ctypes.byref(p), 2) == 0
+    assert h.gdn_reset_saved_bytes(ctypes.byref(p), 6) == h.gdn_varlen_saved_bytes(
+        ctypes.byref(lib.make_problem(6, 100, 2, 128, 128, 64, 1)), 300)

@@ -101,7 +101,9 @@ def test_ragged_lengths_fp32(oracle_mod, T):
     compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "f32", chunk=w.chunk)
 
 
-@pytest.mark.parametrize("K,V", [(64, 128), (128, 32), (16, 128), (128, 16)])
+# (64, 128) and (128, 64) run the tensor-core kernels (TMA fills the missing
+# columns with zeros); the others the CUDA-core kernels
+@pytest.mark.parametrize("K,V", [(64, 128), (128, 64), (128, 32), (16, 128), (128, 16)])
 def test_key_value_dims_differ_bf16(oracle_mod, K, V):
     w = custom(B=1, T=200, H=2, K=K, V=V, chunk=64, dtype="bf16", seed=K + V, init_std=0.1,
                dfinal_std=0.01)
@@ -197,7 +199,8 @@ def test_tc_backward_recompute_equals_saved():
         np.testing.assert_array_equal(a[n], b[n], err_msg=n)
 
 
-@pytest.mark.parametrize("dtype,K,V,C", [("bf16", 128, 128, 64), ("f32", 32, 64, 32), ("bf16", 64, 64, 64)])
+@pytest.mark.parametrize("dtype,K,V,C", [("bf16", 128, 128, 64), ("f32", 32, 64, 32), ("bf16", 64, 64, 64),
+                                         ("bf16", 64, 128, 64), ("bf16", 128, 64, 64)])
 def test_slow_decay_long_range(oracle_mod, dtype, K, V, C):
     """Gates in (0.97, 1): the state carries across many chunks (about 40% of it
     survives a 64-token chunk), so cross-chunk propagation, the initial state and
@@ -215,6 +218,18 @@ def test_tc_scan_48_column_slices(oracle_mod, B, H):
     the third reaching past V = 128 into zero columns): forward and backward
     against the oracle on every stream, slow decay so the states carry."""
     w = custom(B=B, T=200, H=H, K=128, V=128, chunk=64, dtype="bf16", seed=650 + B * H, init_std=0.3,
+               dfinal_std=0.05, alpha_lo=0.97)
+    inp = make_inputs(w)
+    compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16", chunk=w.chunk)
+
+
+@pytest.mark.parametrize("B,H", [(7, 6), (3, 20)])
+def test_tc_k64_slices_and_tail(oracle_mod, B, H):
+    """K = V = 64 on the tensor-core kernels with more streams than one wave of
+    48-column slices (the second slice of each stream reaches past V = 64 into
+    the zero columns) and a ragged tail chunk: forward and backward against the
+    oracle on every stream, slow decay so the states carry."""
+    w = custom(B=B, T=230, H=H, K=64, V=64, chunk=64, dtype="bf16", seed=660 + B * H, init_std=0.3,
                dfinal_std=0.05, alpha_lo=0.97)
     inp = make_inputs(w)
     compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "bf16", chunk=w.chunk)

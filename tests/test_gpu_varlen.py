@@ -233,12 +233,12 @@ def test_reset_mask_matches_oracle(oracle_mod, dtype, K, chunk):
         reset[b, t] = True
     d = {n: (t.cuda() if t is not None else None) for n, t in inp.items()}
     ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
-    o, sT, saved, seg = gdn.gdn_reset_fwd(*ins, reset.cuda(), d["initial_state"], chunk=chunk, saved=True,
-                                          check=True)
+    o, sT, saved, nseg = gdn.gdn_reset_fwd(*ins, reset.cuda(), d["initial_state"], chunk=chunk, saved=True,
+                                           check=True)
     g = gdn.gdn_reset_bwd(*ins, reset.cuda(), d["initial_state"], d["d_o"], d["d_final_state"], chunk=chunk,
-                          segments=seg, saved=saved, check=True)
+                          max_segments=nseg, saved=saved, check=True)
     torch.cuda.synchronize()
-    assert seg.S == B + 6
+    assert nseg == B + 6
     got = dict(o=to_np(o), final_state=to_np(sT), **{n: to_np(x) for n, x in zip(GRADS + ("d_initial_state",), g)})
     npi = {n: to_np(inp[n]) for n in ("q", "k", "v", "alpha", "beta", "initial_state", "d_o", "d_final_state")}
     args = [npi[n] for n in ("q", "k", "v", "alpha", "beta")]
@@ -247,6 +247,46 @@ def test_reset_mask_matches_oracle(oracle_mod, dtype, K, chunk):
     ref.update(resets.bwd_resets(*args, reset.numpy(), npi["initial_state"], npi["d_o"], npi["d_final_state"]))
     compare(got, ref, dtype)
     assert np.all(got["d_initial_state"][1] == 0.0)  # row 1 was reset at t = 0
+
+
+def _reset_case(dtype="bf16", K=128):
+    B, T, H = 3, 150, 2
+    w = custom(B=B, T=T, H=H, K=K, V=K, chunk=64, dtype=dtype, seed=48, init_std=0.3, dfinal_std=0.05,
+               alpha_lo=0.97)
+    d = {n: (t.cuda() if t is not None else None) for n, t in make_inputs(w).items()}
+    reset = torch.zeros(B, T, dtype=torch.bool)
+    for b, t in [(0, 5), (1, 0), (1, 64), (2, 149)]:
+        reset[b, t] = True
+    return d, reset.cuda()
+
+
+def test_reset_loose_bound_gives_the_same_bits():
+    """A bound above the true segment count (the mask has 3 + 3 segments) only
+    adds empty segments: identical outputs and gradients, no host read."""
+    d, reset = _reset_case()
+    ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
+    out = []
+    for bound in (6, 40):
+        o, sT, sv, _ = gdn.gdn_reset_fwd(*ins, reset, d["initial_state"], max_segments=bound, saved=True,
+                                         check=True)
+        g = gdn.gdn_reset_bwd(*ins, reset, d["initial_state"], d["d_o"], d["d_final_state"], max_segments=bound,
+                              saved=sv, check=True)
+        out.append((o, sT) + tuple(g))
+    torch.cuda.synchronize()
+    for a, b in zip(*out):
+        assert torch.equal(a, b)
+
+
+def test_reset_too_small_bound_is_reported():
+    """Fewer segments allowed than the mask has: the kernels flag it in the error
+    word (and stay within the buffers); check=True raises, and the context stays
+    usable."""
+    d, reset = _reset_case()
+    ins = [d[n] for n in ("q", "k", "v", "alpha", "beta")]
+    with pytest.raises(gdn.GdnError, match="more segments than max_segments"):
+        gdn.gdn_reset_fwd(*ins, reset, d["initial_state"], max_segments=4, check=True)
+    gdn.gdn_reset_fwd(*ins, reset, d["initial_state"], max_segments=6, check=True)
+    torch.cuda.synchronize()
 
 
 def test_varlen_bench_workload_sampled(oracle_mod):
