@@ -1142,6 +1142,8 @@ size_t carve_raw(const gdn::Dims& d, Carver& cv, gdn::RawPrologue* rp) {
     rp->rk = cv.take<float>(BTH);
     return cv.off;
 }
+// The backward's per-token kdot, in the workspace (after the raw buffers).
+float* carve_kdot(const gdn::Dims& d, Carver& cv) { return cv.take<float>((size_t)d.NS() * d.NC * d.C); }
 
 // The composed raw path (shapes outside the tensor-core kernels): the prologue's
 // outputs and, for the backward, the gradients of the recurrence's inputs, all
@@ -1170,7 +1172,9 @@ size_t raw_prefix(const gdn_problem* p, const gdn::Dims& d, bool bwd) {
     Carver cv{nullptr};
     if (gdn::tc_fwd_supported(d, in_type(p))) {
         gdn::RawPrologue rp;
-        return carve_raw(d, cv, &rp);
+        carve_raw(d, cv, &rp);
+        if (bwd) carve_kdot(d, cv);
+        return cv.off;
     }
     ComposedBufs c;
     return carve_composed(d, p->dtype == GDN_BF16 ? 2 : 4, cv, &c, bwd);
@@ -1304,6 +1308,10 @@ gdn_status gdn_bwd_raw(const gdn_problem* p, const void* q_raw, const void* k_ra
         Carver cv{(char*)(saved ? const_cast<void*>(saved) : workspace)};
         carve_raw(d, cv, &rp);
         const void* tc_saved = saved ? (const char*)saved + cv.off : nullptr;
+        Carver kv{(char*)workspace};  // kdot after the workspace's own raw buffers
+        gdn::RawPrologue unused;
+        carve_raw(d, kv, &unused);
+        rp.kdot = carve_kdot(d, kv);
         gdn::Dims fd;
         const SplitCfg sp = dense_split(d, &fd);
         return run_bwd_tc(fd, q_raw, k_raw, v, a_logit, b_logit, initial_state, tc_saved, d_o, d_final_state,

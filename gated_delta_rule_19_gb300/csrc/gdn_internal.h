@@ -244,12 +244,15 @@ cudaError_t launch_decode(const Dims& d, InType ty, const void* q, const void* k
 // reciprocal norms to rq, rk ([B,T,H] fp32), and takes log alpha = -softplus(a),
 // beta = sigmoid(b); the backward turns the gradients of the normalised rows and
 // gates into those of the raw inputs.
+//   kdot [rows] fp32: per token, k . (the dK part grad_qk_tc hands to grad_wy_tc),
+//        which grad_wy_tc needs for the chain rule through the k normalisation.
 struct RawPrologue {
     int on = 0;
     __nv_bfloat16* qn = nullptr;
     __nv_bfloat16* kn = nullptr;
     float* rq = nullptr;
     float* rk = nullptr;
+    float* kdot = nullptr;
 };
 
 cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v,

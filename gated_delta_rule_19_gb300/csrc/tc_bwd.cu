@@ -519,9 +519,11 @@ constexpr int DQK = 147456;            // [64 x 64]
 constexpr int DWT = 155648;            // dW^T [128 x 64] (two 64-row halves)
 constexpr int DQ = 172032;             // dq [64 x 128]
 constexpr int DKP = 188416;            // dK^T part [128 x 64]
-constexpr int VEC = 204800;            // Gs gs | dG1p[4] eRp[4] rE1[4] | cE1[8][16] | red[512] | 8 | rqs | dotp[4]
-constexpr int NVEC = 2 * 64 + 3 * 256 + 128 + 512 + 8 + 64 + 256;
-constexpr int BAR = VEC + NVEC * 4;
+constexpr int VEC = 204800;            // Gs gs | dG1p[4] eRp[4] rE1[4] | cE1[8][16] | red[512] | 8 | rqs
+constexpr int NVEC = 2 * 64 + 3 * 256 + 128 + 512 + 8 + 64;
+constexpr int DD = 212992;             // raw prologue: diag(-q . dq) [64 x 64], zero off the diagonal
+static_assert(VEC + NVEC * 4 <= DD, "vectors before the diagonal tile");
+constexpr int BAR = DD + 8192;
 constexpr size_t SMEM = BAR + 64 + 1024;
 static_assert(SMEM <= 232448, "one CTA per SM");
 }  // namespace qk
@@ -562,7 +564,6 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     float* red = cE1 + 128;  // 512
     float* fin = red + 512;  // <dS1, S0>, sum_i e_i eR_i
     float* rqs = fin + 8;    // raw prologue: 1 / |q_raw| of the chunk's tokens
-    float* dotp = rqs + 64;  // raw prologue: q.dq partial sums [4 lane quarters][64]
     // [0] loads A, [1] loads B, [2] phase 1 MMAs, [3] phase 2 MMAs
     uint64_t* bars = (uint64_t*)(sm + qk::BAR);
     uint32_t* tslot = (uint32_t*)(sm + qk::BAR + 40);
@@ -640,6 +641,10 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
+    }
+    if (kRaw) {  // the diagonal tile's zeros, written once
+        for (int i = tid; i < 512; i += 512) *(uint4*)(sm + qk::DD + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async();
     }
     fence_before_sync();
     __syncthreads();
@@ -800,6 +805,21 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ok = __syncthreads_and(ok);
         fence_after_sync();
         if (!ok) break;
+        if (kRaw && warp == kIssuer / 32) {
+            // The normalisation's chain rule needs q . dq per token, which epilogue 1
+            // already holds: q . dQ1 = dG1 and q . dQ2 = sum_t' dQK q.k = the row sum of
+            // dMqk .* Mqk (E1).  diag(-q . dq) goes on the diagonal tile, and phase 2
+            // adds Q^T diag(-q . dq) to dQ2^T (dq_raw = (dq - q (q . dq)) / |q_raw|).
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = lane + 32 * hh;
+                const float g1 = dG1p[t] + dG1p[64 + t] + dG1p[128 + t] + dG1p[192 + t];
+                const float e1 = rE1[t] + rE1[64 + t] + rE1[128 + t] + rE1[192 + t];
+                *(bf16*)(sm + qk::DD + sw128_off(t, t)) = __float2bfloat16_rn(-(gs[t] * g1 + e1));
+            }
+            fence_proxy_async();
+            __syncwarp();
+        }
         // ---- phase 2 (K over tokens): dQ2^T = K^T dQK^T;  Q^T dQK  (M=128, N=64)
         if (tid == kIssuer) {
             for (int j = 0; j < 2; ++j) tma_store_2d(&tm_dWt, sm + qk::DWT + j * 8192, 0, krow0 + 64 * j);
@@ -812,6 +832,12 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int s2 = 0; s2 < 4; ++s2) {
                 mma_bf16_ss(tQ2, desc_add(dkm, s2 * 2048), desc_add(dqk, s2 * 32), idq, s2 > 0);
                 mma_bf16_ss(tQK, desc_add(dqm, s2 * 2048), desc_add(dqkm, s2 * 2048), idk, s2 > 0);
+            }
+            if (kRaw) {  // dQ2^T += Q^T diag(-q . dq)
+                const uint64_t ddd = sdesc(smem_u32(sm + qk::DD), 16, 1024, SW_128B);
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2)
+                    mma_bf16_ss(tQ2, desc_add(dqm, s2 * 2048), desc_add(ddd, s2 * 32), idq, 1u);
             }
             mma_commit(&bars[3]);
             ++n2;
@@ -854,31 +880,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             float q1[16], q2[16];
             tmem_load16f2(tQ1 + lanebase + cb, tQ2 + lanebase + cb, q1, q2);
             unsigned char* dqt = sm + qk::DQ;
+            // dq of the normalised row; with the raw prologue dQ2 already carries
+            // -q (q . dq), so dq_raw is one scaling by 1 / |q_raw|
 #pragma unroll
-            for (int j = 0; j < 16; ++j) q1[j] = gs[cb + j] * q1[j] + q2[j];  // dq of the normalised row
-            if (kRaw) {
-                // dq_raw = (dq - q (q . dq)) / |q_raw|, q the normalised row (read from its
-                // global copy: the Q tile already holds the next chunk's); the dot over k
-                // is a column sum over TMEM lanes (this warp's 32, then the 4 quarters)
-                float qh[16], pr[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = t0 + cb + j;
-                    qh[j] = (t < d.T && k < d.K)
-                                ? __bfloat162float(raw.qn[(((int64_t)b * d.T + t) * d.H + h) * d.K + k])
-                                : 0.f;
-                    pr[j] = qh[j] * q1[j];
-                }
-                const float sdot = warp_colsum16(pr);
-                if (lane < 16) dotp[sub * 64 + cb + lane] = sdot;
-                __syncthreads();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = cb + j;
-                    const float sd = dotp[t] + dotp[64 + t] + dotp[128 + t] + dotp[192 + t];
-                    q1[j] = rqs[t] * (q1[j] - qh[j] * sd);
-                }
-            }
+            for (int j = 0; j < 16; ++j)
+                q1[j] = kRaw ? rqs[cb + j] * (gs[cb + j] * q1[j] + q2[j]) : gs[cb + j] * q1[j] + q2[j];
 #pragma unroll
             for (int j = 0; j < 16; ++j) *(bf16*)(dqt + tile_off(64, cb + j, k)) = __float2bfloat16_rn(q1[j]);
             float dk[16], qkv[16];
@@ -900,6 +906,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             float g = gs[t] * dG1 + re - ce - expf(GC - Gs[t]) * eR;
             if (t == 63) g += gC * fin[0] + fin[1];
             dGp[(int64_t)row0 + t] = g;
+            // k . (the dK part written here) = exp(G_C - G_t) eR_t + the column sum of E1
+            if (kRaw) raw.kdot[(int64_t)row0 + t] = expf(GC - Gs[t]) * eR + ce;
         }
         fence_proxy_async();
         fence_before_sync();
@@ -942,7 +950,7 @@ constexpr int DV = DU;     // outputs [64 x 128] into dead slots
 constexpr int DK = DT;     // dT / E and Y / ID: dead once phase 4's MMA is done, not
                            // rewritten before the next chunk's first MMA completes
 constexpr int VEC = Y + 8192;  // per-token and partial-sum vectors
-constexpr int NVEC = 19 * 64;  // 15 x 64, then (raw prologue) sigmoid(a), 1/|k_raw|, k.dk halves
+constexpr int NVEC = 18 * 64;  // 15 x 64, then (raw prologue) sigmoid(a), 1/|k_raw|, k . dK part
 constexpr int BAR = VEC + NVEC * 4;
 constexpr size_t SMEM = BAR + 64 + 1024;
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
@@ -985,7 +993,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     float* cE2 = vec + 832;     // [2][64]
     float* sas = vec + 960;     // raw prologue: sigmoid(a) = 1 - alpha
     float* rks = vec + 1024;    // raw prologue: 1 / |k_raw|
-    float* kdot = vec + 1088;   // raw prologue: k.dk over each half of the columns [2][64]
+    float* kds = vec + 1088;    // raw prologue: k . dK part (from grad_qk_tc)
     uint64_t* bars = (uint64_t*)(sm + wy::BAR);  // [0] loads, [1] MMA, [2] dK partial
     uint32_t* tslot = (uint32_t*)(sm + wy::BAR + 32);
     int* s_next = (int*)(sm + wy::BAR + 40);  // the chunk after this one
@@ -1020,7 +1028,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     // warp 3: G, the dG partial and the gates of tokens 2 lane, 2 lane + 1 of a chunk
     // (padding: alpha = 1, beta = 0), held in registers until the chunk starts
     // (with the raw prologue: the gate logits, padding a = b = -inf, and 1 / |k_raw|)
-    float2 gv = make_float2(0.f, 0.f), qv = gv, kv = gv;
+    float2 gv = make_float2(0.f, 0.f), qv = gv, kv = gv, dv2 = gv;
     bf16 ga[2], gb[2];
     auto load_vec = [&](int64_t ch) {
         int b, h, t0;
@@ -1028,6 +1036,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const int64_t row0 = ch * kC;
         gv = *(const float2*)(G + row0 + 2 * lane);
         qv = *(const float2*)(dGp + row0 + 2 * lane);
+        if (kRaw) dv2 = *(const float2*)(raw.kdot + row0 + 2 * lane);
         float kr[2] = {0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -1094,7 +1103,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 *s_next = nx;
                 if (nx < nchunks) claimed = (int)gridDim.x + atomicAdd(err + kSchedWy, 1);
             }
-            const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y}, k2[2] = {kv.x, kv.y};
+            const float g2[2] = {gv.x, gv.y}, q2[2] = {qv.x, qv.y}, k2[2] = {kv.x, kv.y}, kd2[2] = {dv2.x, dv2.y};
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int p = 2 * lane + e;
@@ -1107,6 +1116,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     sas[p] = 1.f / (1.f + expf(-a));
                     bs[p] = 1.f / (1.f + expf(-bl));
                     rks[p] = k2[e];
+                    kds[p] = kd2[e];
                 } else {
                     bs[p] = __bfloat162float(gb[e]);
                     as_[p] = __bfloat162float(ga[e]);
@@ -1261,7 +1271,8 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             }
             dB3p[half * 64 + r] = b3;
             rE2p[half * 64 + r] = re2;
-            // the identity for adding the dK partial by an MMA (Y is dead)
+            // the identity for adding the dK partial by an MMA (Y is dead); with the raw
+            // prologue also the zeros of diag(-k . dk) in the dead T2 tile
             if (half == 0) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -1270,6 +1281,9 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     for (int j = 0; j < 8; ++j) f[j] = (8 * q + j == r) ? 1.f : 0.f;
                     *(uint4*)(sm + wy::ID + sw128_off(r, 8 * q)) = pack8(f);
                 }
+            } else if (kRaw) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) *(uint4*)(sm + wy::T2 + sw128_off(r, 8 * q)) = make_uint4(0u, 0u, 0u, 0u);
             }
         } else {
             // dV row a = r (token), columns 64*half .. +64 -> dv tile (dU is dead)
@@ -1286,6 +1300,21 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
+        if (kRaw && warp == 0) {
+            // k . dk per token from sums this chunk already holds: k . dK part (grad_qk_tc),
+            // k . T1^T dW = beta gamma (column sum of T .* Qm), k . (E + E^T) K = row and
+            // column sums of E .* KK^T.  diag(-k . dk) on the diagonal tile; phase 4 adds
+            // diag(-k . dk) K, so dk_raw = (dk - k (k . dk)) / |k_raw| is one row scaling.
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int t = lane + 32 * hh;
+                const float sd = kds[t] + bs[t] * gs[t] * (cGw[t] + cGw[64 + t]) + (rE2p[t] + rE2p[64 + t]) +
+                                 (cE2[t] + cE2[64 + t]);
+                *(bf16*)(sm + wy::T2 + sw128_off(t, t)) = __float2bfloat16_rn(-sd);
+            }
+            fence_proxy_async();
+            __syncwarp();
+        }
         // ---- phase 4: dK = T1^T dW + E K + E^T K + dK_partial (N=128, tokens on rows 64-127)
         if (tid == 0 && ok) {
             for (int j = 0; j < 2; ++j)
@@ -1307,6 +1336,12 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     mma_bf16_ss(tDK, desc_add(dek, s2 * 32), desc_add(dkm, s2 * 2048), id_km, 1u);
                     mma_bf16_ss(tDK, desc_add(dem, s2 * 2048), desc_add(dkm, s2 * 2048), id_mm, 1u);
                     mma_bf16_ss(tDK, desc_add(did, s2 * 32), desc_add(dkp, s2 * 32), id_kk, 1u);
+                }
+                if (kRaw) {  // + diag(-k . dk) K (rows 0-63 of this A are the T1 tile, unused)
+                    const uint64_t dsk = sdesc(smem_u32(sm + wy::T2 - 8192), 16, 1024, SW_128B);
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2)
+                        mma_bf16_ss(tDK, desc_add(dsk, s2 * 32), desc_add(dkm, s2 * 2048), id_km, 1u);
                 }
                 mma_commit(&bars[1]);
                 trk += 4;
@@ -1358,53 +1393,17 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             load_inputs(nxt);
             trk |= 1;
         }
-        // the normalised k row r, columns 64*half + 32*g .. +32 (raw prologue), from its
-        // global copy (the K tile takes the next chunk's)
-        auto krow32 = [&](int g, float* kk) {
-            const int t = t0 + r, c0 = 64 * half + 32 * g;
-            const bool in = t < d.T && c0 < d.K;
-            const uint4* kg = (const uint4*)(raw.kn + (((int64_t)b * d.T + (in ? t : 0)) * d.H + h) * d.K + c0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 x = in ? kg[q] : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kk[8 * q + 2 * e] = bf_lo(w4[e]);
-                    kk[8 * q + 2 * e + 1] = bf_hi(w4[e]);
-                }
-            }
-        };
-        if (kRaw) {
-            // dk_raw = (dk - k (k . dk)) / |k_raw|: k . dk over this half of the columns
-            if (!urow) {
-                float part = 0.f;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    float x[32], kk[32];
-                    tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
-                    krow32(g, kk);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) part += x[j] * kk[j];
-                }
-                kdot[half * 64 + r] = part;
-            }
-            __syncthreads();
-        }
         if (!urow) {
             // dK row a = r (token), columns 64*half .. +64 -> dk tile (dT / E and Y / ID are dead)
             unsigned char* dkt = sm + wy::DK + half * 8192;
-            const float sd = kRaw ? kdot[r] + kdot[64 + r] : 0.f;
-            const float rr = kRaw ? rks[r] : 0.f;
+            const float rr = kRaw ? rks[r] : 1.f;  // dk_raw = (dk - k (k . dk)) / |k_raw|
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 float x[32];
                 tmem_cols<32>(tDK + lanebase + 64 * half + 32 * g, x);
                 if (kRaw) {
-                    float kk[32];
-                    krow32(g, kk);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = rr * (x[j] - kk[j] * sd);
+                    for (int j = 0; j < 32; ++j) x[j] *= rr;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) *(uint4*)(dkt + sw128_off(r, 32 * g + 8 * q)) = pack8(x + 8 * q);

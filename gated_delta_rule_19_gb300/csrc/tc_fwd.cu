@@ -201,8 +201,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_W,
             const __grid_constant__ CUtensorMap tm_U, const __grid_constant__ CUtensorMap tm_M,
             const bf16* __restrict__ alpha, const bf16* __restrict__ beta, float* __restrict__ Gout,
-            bf16* __restrict__ Tout, RawPrologue raw, const __grid_constant__ CUtensorMap tm_qn,
-            const __grid_constant__ CUtensorMap tm_kn, int* err) {
+            bf16* __restrict__ Tout, RawPrologue raw, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* Af = (float*)(sm + P_AF);
@@ -296,50 +295,46 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int row0 = (int)(ch * kC);
         if (kRaw) {
             // Raw q, k rows to unit length as they land, before the Gram MMA reads them
-            // (q = q_raw (sum q_raw^2 + 1e-6)^-1/2, the same for k): thread pairs hold the
-            // two 64-column halves of one row of the K (threads 0-127) or Q tile.
+            // (q = q_raw (sum q_raw^2 + 1e-6)^-1/2, the same for k): 16 consecutive lanes
+            // hold the 16-byte pieces of one row (both 64-column halves), so every access
+            // is conflict-free; rows 0-63 are the K tile's, 64-127 the Q tile's.
             int b, h, t0;
             decode(ch, b, h, t0);
             ok = mbar_wait(&bars[0], ph, err, 1) && ok;
             ok = mbar_wait(&bars[1], ph, err, 1) && ok;
-            {
-                const bool isq = tid >= 128;
-                const int rr = (tid >> 1) & 63, hf = tid & 1;
-                unsigned char* rowp = sm + (isq ? P_Q0 : P_K0) + hf * 16384 + rr * 128;
-                uint4 x[8];
+            const int pc = tid & 15, hf = pc >> 3, p = pc & 7;
+#pragma unroll 2
+            for (int it = 0; it < 8; ++it) {
+                const int rowid = it * 16 + (tid >> 4);
+                const bool isq = rowid >= 64;
+                const int rr = rowid & 63;
+                unsigned char* ptr = sm + (isq ? P_Q0 : P_K0) + hf * 16384 + rr * 128 + p * 16;
+                const uint4 x = *(const uint4*)ptr;
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
                 float ss = 0.f;
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    x[p] = *(const uint4*)(rowp + p * 16);
-                    const uint32_t w4[4] = {x[p].x, x[p].y, x[p].z, x[p].w};
+                for (int e = 0; e < 4; ++e) ss += bf_lo(w4[e]) * bf_lo(w4[e]) + bf_hi(w4[e]) * bf_hi(w4[e]);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) ss += bf_lo(w4[e]) * bf_lo(w4[e]) + bf_hi(w4[e]) * bf_hi(w4[e]);
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 const float rn = rsqrtf(ss + kNormEps);
+                uint32_t o4[4];
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const uint32_t w4[4] = {x[p].x, x[p].y, x[p].z, x[p].w};
-                    uint32_t o4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o4[e] = pack_bf16(rn * bf_lo(w4[e]), rn * bf_hi(w4[e]));
-                    *(uint4*)(rowp + p * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-                }
-                if (hf == 0 && t0 + rr < d.T) (isq ? raw.rq : raw.rk)[((int64_t)b * d.T + t0 + rr) * d.H + h] = rn;
+                for (int e = 0; e < 4; ++e) o4[e] = pack_bf16(rn * bf_lo(w4[e]), rn * bf_hi(w4[e]));
+                const uint4 y = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                *(uint4*)ptr = y;
+                // the normalised row's global copy, for the scan and the backward: smem piece
+                // p holds columns 8 (p ^ (rr % 8)) .. +8 of its 128B-swizzled half row
+                const int t = t0 + rr;
+                if (t < d.T && 64 * hf < d.K)
+                    *(uint4*)((isq ? raw.qn : raw.kn) + (((int64_t)b * d.T + t) * d.H + h) * d.K + 64 * hf +
+                              8 * (p ^ (rr & 7))) = y;
+                if (pc == 0 && t < d.T) (isq ? raw.rq : raw.rk)[((int64_t)b * d.T + t) * d.H + h] = rn;
             }
             fence_proxy_async();
             fence_before_sync();
             ok = __syncthreads_and(ok);
             fence_after_sync();
             if (!ok) break;
-            if (tid == kLoader) {  // the normalised rows, for the scan and the backward
-                for (int j = 0; j < 2; ++j) {
-                    if (64 * j >= d.K) continue;
-                    tma_store_4d(&tm_qn, sm + P_Q0 + j * 16384, 64 * j, h, t0, b);
-                    tma_store_4d(&tm_kn, sm + P_K0 + j * 16384, 64 * j, h, t0, b);
-                }
-                bulk_commit();
-            }
         }
         if (tid == 0) {
             ok = mbar_wait(&bars[0], ph, err, 1) && ok;
@@ -396,7 +391,6 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         __syncwarp();
         fence_after_sync();
         if (tid == kLoader && ok && has_next) {  // the Q tiles are free
-            if (kRaw) bulk_wait_read0();  // the normalised rows' stores have read them
             load_q(nxt);
             ++nq;
         }
@@ -562,7 +556,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (w_last == n) mbar_wait(&bars[3], n & 1, nullptr, 0);
         }
     }
-    if (tid == 0 || tid == kLoader) bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
+    if (tid == 0) bulk_wait_read0();  // stores have read their tiles; their writes complete on their own
     __syncwarp();
     fence_before_sync();
     __syncthreads();
@@ -1112,27 +1106,21 @@ int tc_scan_vt_for(const Dims& d, const SeqMap* sq, int64_t streams) {
 
 cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const void* v, const void* alpha,
                            const void* beta, const TcBufs& tb, cudaStream_t st, const RawPrologue* rp) {
-    CUtensorMap mq, mk, mv, mW, mU, mM, mqn, mkn;
+    CUtensorMap mq, mk, mv, mW, mU, mM;
     const int64_t rows = d.NS() * d.NC * kC;
     if (!tmap_bthd(&mq, q, d.B, d.T, d.H, d.K) || !tmap_bthd(&mk, k, d.B, d.T, d.H, d.K) ||
         !tmap_bthd(&mv, v, d.B, d.T, d.H, d.V) || !tmap_rows(&mW, tb.W, rows, kD) ||
         !tmap_rows(&mU, tb.Ut, rows, kD) || !tmap_rows(&mM, tb.Mqk, rows, kC))
         return cudaErrorInvalidValue;
     RawPrologue raw{};
-    memset(&mqn, 0, sizeof(mqn));
-    memset(&mkn, 0, sizeof(mkn));
-    if (rp && rp->on) {
-        raw = *rp;
-        if (!tmap_bthd(&mqn, raw.qn, d.B, d.T, d.H, d.K) || !tmap_bthd(&mkn, raw.kn, d.B, d.T, d.H, d.K))
-            return cudaErrorInvalidValue;
-    }
+    if (rp && rp->on) raw = *rp;
     auto kern = raw.on ? prep_fwd_tc<true> : prep_fwd_tc<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;
     dim3 grid((unsigned)std::min<int64_t>(nchunks, 2 * sm_count()));
     kern<<<grid, 256, kPrepSmem, st>>>(d, mq, mk, mv, mW, mU, mM, (const bf16*)alpha, (const bf16*)beta,
-                                              tb.G, tb.T, raw, mqn, mkn, tb.err);
+                                              tb.G, tb.T, raw, tb.err);
     return cudaGetLastError();
 }
 

@@ -517,9 +517,21 @@ def _varlen_problem(q, v, cu_seqlens, max_len, chunk):
         raise GdnError(GDN_ERR_INVALID_ARG, "cu_seqlens must be a 1-d int32 tensor of S+1 offsets")
     _need(cu_seqlens, "cu_seqlens", tuple(cu_seqlens.shape), torch.int32, q.device)
     S = cu_seqlens.numel() - 1
-    if max_len is None:  # one device-to-host read; pass max_len to avoid it
-        max_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if S > 0 else 0
+    if max_len is None:
+        if _flat_layout(q.dtype, K, V, chunk):
+            # the tensor-core kernels lay the sequences out back to back: the bound only
+            # checks the offsets and guides the scans' slice width, and the packed total
+            # bounds every length, so nothing is read back
+            max_len = total
+        else:  # the padded layout is sized by it: one device-to-host read (pass max_len to avoid it)
+            max_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if S > 0 else 0
     return make_problem(S, max_len, H, K, V, chunk, q.dtype), (total, S, H, K, V)
+
+
+def _flat_layout(dtype, K, V, chunk) -> bool:
+    """Whether the library runs this shape on its tensor-core kernels (bf16, 64-token
+    chunks, K and V of 64 or 128), whose packed calls use the flat chunk layout."""
+    return dtype == torch.bfloat16 and chunk == 64 and K in (64, 128) and V in (64, 128)
 
 
 def _varlen_error(workspace, stream, dev):
@@ -540,8 +552,9 @@ def gdn_varlen_fwd(q, k, v, alpha, beta, cu_seqlens, max_len=None, initial_state
 
     q, k [total,H,K]; v [total,H,V]; alpha, beta [total,H]; sequence s is rows
     ``cu_seqlens[s]:cu_seqlens[s+1]`` (int32 [S+1] on the device).  ``max_len``
-    bounds every length (computed from cu_seqlens with one device-to-host read
-    if None).  initial_state / final_state are float32 [S,H,V,K] as in
+    bounds every length; if None it is ``total`` on the tensor-core shapes (no
+    read back) and is computed from cu_seqlens with one device-to-host read on
+    the others, whose padded layout it sizes.  initial_state / final_state are float32 [S,H,V,K] as in
     :func:`gdn_fwd`.  ``check=True`` synchronises and raises if the kernels
     found cu_seqlens invalid.  Returns ``(o, final_state or None, saved or None)``;
     ``saved`` feeds :func:`gdn_varlen_bwd` with the same cu_seqlens and max_len.

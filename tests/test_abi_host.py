@@ -330,7 +330,8 @@ def test_raw_sizes(lib):
     raw_part = 2 * BTH * 128 * 2 + 2 * BTH * 4
     assert lib.gdn_raw_saved_bytes(tc) == raw_part + lib.gdn_saved_bytes(tc)
     assert lib.gdn_raw_fwd_workspace_bytes(tc) == raw_part + lib.gdn_fwd_workspace_bytes(tc)
-    assert lib.gdn_raw_bwd_workspace_bytes(tc) == raw_part + lib.gdn_bwd_workspace_bytes(tc)
+    # the backward also keeps one float per token for the k normalisation's chain rule
+    assert lib.gdn_raw_bwd_workspace_bytes(tc) == raw_part + BTH * 4 + lib.gdn_bwd_workspace_bytes(tc)
     # other shapes keep gdn_fwd's saved; the workspace holds the prologue's outputs
     # (and, backward, the recurrence's input gradients) in the run dtype
     f = lib.make_problem(2, 100, 3, 64, 32, 32, 0)
