@@ -16,6 +16,17 @@ namespace gdn {
 struct Dims {
     int B, T, H, K, V, C, NC;
     __host__ __device__ int64_t NS() const { return (int64_t)B * H; }
+    // The chunk (index (b * H + h) * NC + c) that work item wi of a chunk-parallel
+    // kernel takes: every stream's chunk c before any chunk c + 1, c ascending or
+    // descending, so that the next kernel meets first the chunks written last
+    // (still in L2).  NS() * NC for wi past the end.
+    __host__ __device__ int64_t chunk_of(int64_t wi, bool descending) const {
+        const int64_t n = NS() * NC;
+        if (wi >= n) return n;
+        int64_t c = wi / NS();
+        if (descending) c = NC - 1 - c;
+        return (wi % NS()) * NC + c;
+    }
 };
 
 // Per-chunk results of the chunk-parallel step (Phase 1 + solve + recompute),

@@ -264,7 +264,9 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     };
 
-    const int64_t first = blockIdx.x;
+    // chunks position-major, descending: the forward scan starts with every stream's
+    // chunk 0, which is then the last one written (still in L2)
+    const int64_t first = d.chunk_of(blockIdx.x, true);
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -288,9 +290,10 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     int nq = first < nchunks ? 1 : 0, nk = nq, nv = nq;  // load batches issued (thread kLoader's count)
     int g_last = -1, w_last = -1;               // chunks whose MMAs were issued (thread 0)
 #pragma unroll 1
-    for (int64_t ch = first; ch < nchunks; ch += gridDim.x, ++n) {
+    for (int64_t wi = blockIdx.x; wi < nchunks; wi += gridDim.x, ++n) {
         const int ph = n & 1;
-        const int64_t nxt = ch + gridDim.x;
+        const int64_t ch = d.chunk_of(wi, true);
+        const int64_t nxt = d.chunk_of(wi + gridDim.x, true);
         const bool has_next = nxt < nchunks;
         const int row0 = (int)(ch * kC);
         if (kRaw) {

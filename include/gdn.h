@@ -140,8 +140,10 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
  * memory: GDN_FWD_NOALLOC_SCRATCH_BYTES on every device that loads the library,
  * held until the process exits.  It calls no allocating routine.
  *   - Problems whose gdn_fwd_workspace_bytes(p) exceeds that size are rejected
- *     with GDN_ERR_UNSUPPORTED before anything is enqueued (e.g. K=V=128,
- *     chunk 64 needs 80.25 KiB per (b, h, chunk), so B*H*ceil(T/64) <= 408).
+ *     with GDN_ERR_UNSUPPORTED before anything is enqueued (e.g. bf16 with K, V
+ *     of 64 or 128 and chunk 64 needs 40.25 KiB per (b, h, chunk), so
+ *     B*H*ceil(T/64) <= 814, less when the within-call sequence split runs: it
+ *     adds 192 KiB per (sequence, piece, head)).
  *   - The array used is the current device's: make the device that holds the
  *     tensors and runs `stream` current before the call.  A q on another
  *     device is rejected with GDN_ERR_INVALID_ARG.
