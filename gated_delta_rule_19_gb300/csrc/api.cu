@@ -85,7 +85,7 @@ size_t carve_chunk(const gdn::Dims& d, Carver& cv, gdn::ChunkBufs* cb, bool with
 }
 
 // The tensor-core kernels keep K and V at 128 in their own buffers: a problem with
-// K or V = 64 is read through TMA boxes that fill the missing columns with zeros,
+// K or V below 128 is read through TMA boxes that fill the missing columns with zeros,
 // and every internal row is 128 wide (its extra columns hold zeros).
 constexpr size_t kTcD = 128;
 

@@ -257,7 +257,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
     for (int j = 0; j < HV; ++j) {
         const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
-        // the caller's [V, K] gradient (K, V = 64 or 128); rows and columns past them are zero
+        // the caller's [V, K] gradient (K, V <= 128); rows and columns past them are zero
         ds[j] = (epi && dsT && v < d.V && k < d.K) ? dsT[(sidx * d.V + v) * d.K + k] : 0.f;
     }
     auto write_ds_operand = [&]() {

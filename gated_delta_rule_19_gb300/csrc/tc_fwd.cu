@@ -328,9 +328,9 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // the normalised row's global copy, for the scan and the backward: smem piece
                 // p holds columns 8 (p ^ (rr % 8)) .. +8 of its 128B-swizzled half row
                 const int t = t0 + rr;
-                if (t < d.T && 64 * hf < d.K)
-                    *(uint4*)((isq ? raw.qn : raw.kn) + (((int64_t)b * d.T + t) * d.H + h) * d.K + 64 * hf +
-                              8 * (p ^ (rr & 7))) = y;
+                const int col = 64 * hf + 8 * (p ^ (rr & 7));  // K is a multiple of 8
+                if (t < d.T && col < d.K)
+                    *(uint4*)((isq ? raw.qn : raw.kn) + (((int64_t)b * d.T + t) * d.H + h) * d.K + col) = y;
                 if (pc == 0 && t < d.T) (isq ? raw.rq : raw.rk)[((int64_t)b * d.T + t) * d.H + h] = rn;
             }
             fence_proxy_async();
@@ -757,7 +757,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
     for (int j = 0; j < HV; ++j) {
         const int v = v0 + cb + j;  // a 48-wide slice runs past V = 128 (zero columns)
-        // the caller's state is [V, K] (K, V = 64 or 128); rows and columns past them are zero
+        // the caller's state is [V, K] (K, V <= 128); rows and columns past them are zero
         const bool vok = (kD % Vt == 0) || v < kD;
         const bool uok = v < d.V && k < d.K;
         s[j] = (!epi || !vok) ? 0.f
@@ -1068,11 +1068,12 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
 
 }  // namespace
 
-// bf16 with 64-token chunks and K, V of 64 or 128: the kernels work on 128 columns
-// and TMA fills the columns past a 64-wide K or V with zeros on every load (they
-// contribute nothing to any product) and clips them on every store.
+// bf16 with 64-token chunks and K, V of 16, 32, 64 or 128: the kernels work on 128
+// columns and TMA fills the columns past a narrower K or V with zeros on every load
+// (they contribute nothing to any product) and clips them on every store.
 bool tc_fwd_supported(const Dims& d, InType ty) {
-    return ty == InType::BF16 && d.C == kC && (d.K == kD || d.K == 64) && (d.V == kD || d.V == 64);
+    auto w = [](int x) { return x == 16 || x == 32 || x == 64 || x == kD; };
+    return ty == InType::BF16 && d.C == kC && w(d.K) && w(d.V);
 }
 
 // The narrowest V-slice whose CTAs (one per slice and stream) fit one wave.

@@ -530,8 +530,9 @@ def _varlen_problem(q, v, cu_seqlens, max_len, chunk):
 
 def _flat_layout(dtype, K, V, chunk) -> bool:
     """Whether the library runs this shape on its tensor-core kernels (bf16, 64-token
-    chunks, K and V of 64 or 128), whose packed calls use the flat chunk layout."""
-    return dtype == torch.bfloat16 and chunk == 64 and K in (64, 128) and V in (64, 128)
+    chunks, K and V of 16, 32, 64 or 128), whose packed calls use the flat chunk layout."""
+    dims = (16, 32, 64, 128)
+    return dtype == torch.bfloat16 and chunk == 64 and K in dims and V in dims
 
 
 def _varlen_error(workspace, stream, dev):

@@ -140,8 +140,8 @@ gdn_status gdn_bwd(const gdn_problem* p, const void* q, const void* k, const voi
  * memory: GDN_FWD_NOALLOC_SCRATCH_BYTES on every device that loads the library,
  * held until the process exits.  It calls no allocating routine.
  *   - Problems whose gdn_fwd_workspace_bytes(p) exceeds that size are rejected
- *     with GDN_ERR_UNSUPPORTED before anything is enqueued (e.g. bf16 with K, V
- *     of 64 or 128 and chunk 64 needs 40.25 KiB per (b, h, chunk), so
+ *     with GDN_ERR_UNSUPPORTED before anything is enqueued (e.g. bf16 with
+ *     chunk 64 needs 40.25 KiB per (b, h, chunk), so
  *     B*H*ceil(T/64) <= 814, less when the within-call sequence split runs: it
  *     adds 192 KiB per (sequence, piece, head)).
  *   - The array used is the current device's: make the device that holds the
@@ -198,7 +198,7 @@ gdn_status gdn_prologue_bwd(const gdn_problem* p, const void* q_raw, const void*
  * then gdn_fwd on (q, k, v, alpha, beta); gdn_bwd_raw returns the gradients with
  * respect to q_raw, k_raw, v, a_logit, b_logit and the initial state of
  *     L = sum dO . o + sum d_final_state . final_state.
- * On the tensor-core kernels (bf16, chunk 64, K and V of 64 or 128) the prologue
+ * On the tensor-core kernels (bf16, chunk 64, K and V of 16 to 128) the prologue
  * runs inside them: the chunk kernel normalises the rows as they arrive and takes
  * log alpha = -softplus(a) directly in fp32, and the gradient kernels return the
  * raw inputs' gradients, so neither direction makes a separate pass over q and k.

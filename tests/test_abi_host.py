@@ -68,6 +68,9 @@ def test_sizes(lib):
     assert lib.gdn_saved_bytes(p) == expect
     # bf16 K=V=64 chunk 64 also runs on tensor cores, with the same 128-wide buffers
     assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 1)) == expect
+    # and so do K, V of 16 or 32, in any combination
+    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 32, 16, 64, 1)) == expect
+    assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 16, 128, 64, 1)) == expect
     # other shapes keep float32 boundary states
     assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 32, 1)) == 8 * 6 * 128 * 64 * 64 * 4
     assert lib.gdn_saved_bytes(lib.make_problem(8, 4096, 6, 64, 64, 64, 0)) == 8 * 6 * NC * 64 * 64 * 4

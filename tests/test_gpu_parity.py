@@ -101,9 +101,10 @@ def test_ragged_lengths_fp32(oracle_mod, T):
     compare(gpu_run(w, inp, True), oracle_run(oracle_mod, inp, True), "f32", chunk=w.chunk)
 
 
-# (64, 128) and (128, 64) run the tensor-core kernels (TMA fills the missing
-# columns with zeros); the others the CUDA-core kernels
-@pytest.mark.parametrize("K,V", [(64, 128), (128, 64), (128, 32), (16, 128), (128, 16)])
+# all run the tensor-core kernels: TMA fills the columns past K or V with zeros
+# on every load and clips them on every store
+@pytest.mark.parametrize("K,V", [(64, 128), (128, 64), (128, 32), (16, 128), (128, 16), (32, 32),
+                                 (16, 64)])
 def test_key_value_dims_differ_bf16(oracle_mod, K, V):
     w = custom(B=1, T=200, H=2, K=K, V=V, chunk=64, dtype="bf16", seed=K + V, init_std=0.1,
                dfinal_std=0.01)

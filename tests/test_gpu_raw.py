@@ -66,16 +66,20 @@ def _gpu(x, r, C, saved=True):
 
 
 # (B, T, H, K, V, chunk, dtype, slow decay): tensor-core shapes with a ragged tail,
-# K or V of 64, the within-call sequence split (B = 1, four streams of 64 chunks),
-# slow decay; then shapes that run the prologue kernel and the CUDA-core kernels
+# K or V below 128 (rows of 32 columns: the normalised rows' copies are written
+# piece by piece), the within-call sequence split (B = 1, four streams of 64
+# chunks), slow decay; then shapes that run the prologue kernel and the CUDA-core
+# kernels
 CASES = [
     (2, 300, 3, 128, 128, 64, "bf16", False),
     (2, 500, 2, 128, 128, 64, "bf16", True),
     (2, 256, 3, 64, 64, 64, "bf16", True),
     (1, 200, 2, 64, 128, 64, "bf16", False),
+    (2, 130, 2, 32, 32, 64, "bf16", False),
+    (1, 150, 3, 16, 64, 64, "bf16", True),
     (1, 4096, 4, 128, 128, 64, "bf16", False),
     (1, 100, 2, 32, 64, 32, "f32", True),
-    (2, 130, 2, 32, 32, 64, "bf16", False),
+    (2, 130, 2, 32, 32, 32, "bf16", False),
 ]
 
 

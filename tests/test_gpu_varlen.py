@@ -56,11 +56,12 @@ def _oracle_seq(oracle_mod, inp, s):
                 **{n: g[n][0] for n in GRADS})
 
 
-# bf16 with K = V = 128 and chunk 64 runs the tensor-core kernels on the flat
-# chunk layout (each sequence starts a new chunk); other shapes pad to max_len.
+# bf16 with chunk 64 runs the tensor-core kernels on the flat chunk layout (each
+# sequence starts a new chunk); other shapes pad to max_len.
 CASES = [
     # lengths (one empty, ragged tails, exact chunks, several tiles), H, K, V, chunk, dtype
     ([1, 63, 64, 65, 200, 0, 130], 2, 64, 64, 64, "bf16"),
+    ([65, 0, 1, 128, 70], 2, 32, 16, 64, "bf16"),
     ([64, 1, 128, 191], 2, 128, 128, 64, "bf16"),
     ([1, 63, 64, 65, 200, 0, 130, 0], 2, 128, 128, 64, "bf16"),
     # 40 sequences x 4 heads: more (sequence, head) streams than one wave of SMs
