@@ -592,21 +592,29 @@ gdn_status gdn_fwd(const gdn_problem* p, const void* q, const void* k, const voi
 }
 
 // ---------------------------------------------------------------- varlen
-// Packed sequences run on one of two layouts inside the workspace:
-//  * flat (tensor-core path): one row of chunks per head (B = 1), every sequence
-//    starting a new chunk: nc_max = ceil(total / C) + S chunks bound the
-//    sum of ceil(len_s / C); the scans take a SeqMap;
-//  * padded (other shapes): [S, max_len] streams, gdn_fwd / gdn_bwd as they are.
-// Workspace: the error word, chunk_off, the inner workspace, the laid-out tensors.
+// Packed sequences run on one of two layouts:
+//  * flat (tensor-core path): the kernels read and write the packed tensors in
+//    place, one row of chunks per head (B = 1), every sequence starting a new
+//    chunk: nc_max = ceil(total / C) + S chunks bound the sum of ceil(len_s / C),
+//    and the chunk-token map (Dims::tok, len) gives each chunk's first packed
+//    token and its number of tokens; the scans take a SeqMap.  Workspace: the
+//    tensor-core workspace (its error word, word 0, is the call's), then
+//    chunk_off [S+1], order [S], tok [nc_max], len [nc_max] and an error int for
+//    the offsets; with `saved` the four arrays live there instead (the backward
+//    reuses them), followed by the chunk kernels' own results.
+//  * padded (other shapes): [S, max_len] streams laid out in the workspace (the
+//    error word, chunk_off, the inner workspace, the laid-out tensors), gdn_fwd /
+//    gdn_bwd as they are.
 namespace {
 struct VarlenPlan {
     bool flat;
     int pieces;    // within-call split of every sequence (flat layout; 1: none)
     gdn::Dims pd;  // the problem the chunk kernels run on
     size_t off, inner, q, k, v, a, b, o, d_o, dq, dk, dv, da, db, total;
-    // `saved` of the flat layout: chunk_off and the laid-out inputs (the backward
-    // reads them instead of gathering again), then the chunk kernels' own.
-    size_t s_off, s_q, s_k, s_v, s_a, s_b, s_tc, saved;
+    size_t nints;  // flat: ints at `off` (chunk_off, order, tok, len, the offsets' error)
+    // `saved` of the flat layout: chunk_off, order, tok, len, then the chunk
+    // kernels' own results
+    size_t s_off, s_tc, saved;
 };
 
 gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan* L) {
@@ -619,18 +627,18 @@ gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan
     *L = VarlenPlan{};
     L->flat = gdn::tc_fwd_supported(d, in_type(p));
     L->pd = d;
+    int64_t nc_max = 0;
     if (L->flat) {
-        const int64_t nc_max = (total + d.C - 1) / d.C + d.B;
+        nc_max = (total + d.C - 1) / d.C + d.B;
         if (nc_max * d.C > ((int64_t)1 << 30))
             return fail(GDN_ERR_UNSUPPORTED, "total=%lld with B=%d sequences exceeds 2^30 chunk rows",
                         (long long)total, d.B);
         L->pd.B = 1;
         L->pd.NC = (int)nc_max;
-        L->pd.T = (int)(nc_max * d.C);
+        L->pd.T = (int)total;  // the packed tensors the kernels read in place
     }
     const gdn::Dims& q = L->pd;
     const size_t es = p->dtype == GDN_BF16 ? 2 : 4;
-    const size_t BTH = (size_t)q.B * q.T * q.H;
     size_t inner_bytes = 0;
     Carver cv{nullptr};
     L->pieces = (L->flat && d.K == 128 && d.V == 128) ? split_pieces((int64_t)d.B * d.H, 0, false) : 1;
@@ -652,27 +660,21 @@ gdn_status varlen_plan(const gdn_problem* p, int64_t total, bool bwd, VarlenPlan
         }
     }
     if (L->flat) {
+        L->nints = (size_t)2 * d.B + 1 + (size_t)2 * nc_max + 1;
+        L->inner = 0;
+        L->off = round_up(inner_bytes > 0 ? inner_bytes : sizeof(int));
+        L->total = L->off + round_up(L->nints * sizeof(int));
         Carver sv{nullptr};
         __nv_bfloat16* states;
         gdn::TcBufs tb;
         const size_t tc = q.NS() * q.NC > 0 ? carve_tc_saved(q, sv, &states, &tb) : 0;
-        size_t so = 0;
-        auto stake = [&](size_t bytes) {
-            const size_t o = so;
-            so += round_up(bytes);
-            return o;
-        };
-        L->s_off = stake(((size_t)2 * d.B + 1) * sizeof(int));  // chunk_off [B+1], order [B]
-        L->s_q = stake(BTH * q.K * es);
-        L->s_k = stake(BTH * q.K * es);
-        L->s_v = stake(BTH * q.V * es);
-        L->s_a = stake(BTH * es);
-        L->s_b = stake(BTH * es);
-        L->s_tc = stake(tc);
-        L->saved = so;
-    } else {
-        L->saved = gdn_saved_bytes(p);
+        L->s_off = 0;
+        L->s_tc = round_up((L->nints - 1) * sizeof(int));
+        L->saved = L->s_tc + tc;
+        return GDN_OK;
     }
+    L->saved = gdn_saved_bytes(p);
+    const size_t BTH = (size_t)q.B * q.T * q.H;
     size_t off = kAlign;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -715,6 +717,49 @@ cudaError_t varlen_move(const VarlenPlan& L, int64_t total, const int32_t* cu, c
             return gdn::launch_varlen_rows(d, total, cu, width, src, dst, fill, scatter, err, merge, cs);
         return gdn::launch_varlen_elems(d, total, cu, width, src, dst, fill, scatter, err, cs);
     });
+}
+
+// The flat layout's maps: chunk_off, order, tok, len at `ints` (computed on the
+// device when `compute`, else read from the forward's `saved`), and the dims with
+// the chunk-token map.  The offsets' error int (in the workspace) is cleared and
+// set by the offsets kernel.
+struct FlatMaps {
+    gdn::Dims d;
+    gdn::SeqMap sq;
+};
+gdn_status flat_maps(const VarlenPlan& L, const gdn_problem* p, int64_t total, const int32_t* cu, char* ints_base,
+                     char* ws, bool compute, cudaStream_t cs, FlatMaps* fm) {
+    const int S = (int)p->B, nc = L.pd.NC;
+    int* ints = (int*)ints_base;
+    int* chunk_off = ints;
+    int* order = ints + S + 1;
+    int* tok = order + S;
+    int* len = tok + nc;
+    int* offerr = (int*)(ws + L.off) + (L.nints - 1);
+    fm->d = L.pd;
+    fm->d.tok = tok;
+    fm->d.len = len;
+    // longest sequences first; the longest has at most ceil(max_len / C) chunks
+    fm->sq = gdn::SeqMap{chunk_off, S, 0, nullptr, order, (int)((p->T + L.pd.C - 1) / L.pd.C)};
+    if (!compute) return GDN_OK;
+    cudaError_t e = cudaMemsetAsync(offerr, 0, sizeof(int), cs);
+    if (e == cudaSuccess)
+        e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
+            cudaError_t e2 = gdn::launch_varlen_offsets(S, total, (int)p->T, L.pd.C, nc, cu, chunk_off, order, offerr,
+                                                        cs);
+            if (e2 == cudaSuccess)
+                e2 = gdn::launch_varlen_chunk_tokens(S, total, L.pd.C, nc, cu, chunk_off, tok, len, cs);
+            return e2;
+        });
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen offsets");
+}
+
+// The offsets' error int joins the call's error word (word 0 of the workspace,
+// the tensor-core kernels' own), after the kernels have run.
+gdn_status flat_merge_error(const VarlenPlan& L, char* ws, cudaStream_t cs) {
+    const int* offerr = (const int*)(ws + L.off) + (L.nints - 1);
+    cudaError_t e = gdn::launch_route_states(0, 0, nullptr, nullptr, nullptr, offerr, (int*)ws, cs);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen error word");
 }
 
 gdn_status check_cu(const gdn_problem* p, const int32_t* cu) {
@@ -773,43 +818,26 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int64_t total, const int32_t* cu
     if (p->B * p->H == 0) return GDN_OK;
     const int S = (int)p->B, kb = (int)(p->K * es), vb = (int)(p->V * es);
     if (L.flat) {
-        // laid-out inputs and chunk_off go to `saved` when given (the backward reuses them)
-        char* in = saved ? (char*)saved : ws;
-        int* off = (int*)(saved ? in + L.s_off : ws + L.off);
-        char* lq = in + (saved ? L.s_q : L.q);
-        char* lk = in + (saved ? L.s_k : L.k);
-        char* lv = in + (saved ? L.s_v : L.v);
-        char* la = in + (saved ? L.s_a : L.a);
-        char* lb = in + (saved ? L.s_b : L.b);
-        const gdn::Dims& fd = L.pd;
-        e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
-            return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, off, off + S + 1,
-                                              (int*)ws, cs);
-        });
-        gdn::FlatMoves m{5, {q, k, v, alpha, beta}, {lq, lk, lv, la, lb},
-                         {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)(p->H * es), (int)(p->H * es)},
-                         {16, 16, 16, (int)es, (int)es}, {0u, 0u, 0u, one_bits(p), 0u}};
-        if (e == cudaSuccess)
-            e = timed(gdn::KID_VARLEN_GATHER, cs, [&] {
-                return gdn::launch_varlen_flat(m, S, fd.C, fd.NC, total, cu_seqlens, off, false, nullptr, (int*)ws,
-                                               cs);
-            });
-        if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
-        // longest sequences first; the longest has at most ceil(max_len / C) chunks
-        const gdn::SeqMap sq{off, S, 0, nullptr, off + S + 1, (int)((p->T + fd.C - 1) / fd.C)};
+        if (total == 0) {  // no tokens: every state passes through
+            if (final_state) {
+                e = initial_state ? cudaMemcpyAsync(final_state, initial_state, nstate, cudaMemcpyDeviceToDevice, cs)
+                                  : cudaMemsetAsync(final_state, 0, nstate, cs);
+                if (e != cudaSuccess) return cuda_fail(e, "state copy");
+            }
+            return GDN_OK;
+        }
+        FlatMaps fm;
+        if ((st = flat_maps(L, p, total, cu_seqlens, saved ? (char*)saved + L.s_off : ws + L.off, ws, true, cs, &fm)) !=
+            GDN_OK)
+            return st;
         SplitCfg sp;
         sp.P = L.pieces;
         sp.nseq = S;
-        sp.seq_off = off;
-        st = run_fwd_tc(fd, lq, lk, lv, la, lb, initial_state, ws + L.o, final_state,
-                        saved ? (char*)saved + L.s_tc : nullptr, ws + L.inner, &sq, &sp, cs);
+        sp.seq_off = fm.sq.chunk_off;
+        st = run_fwd_tc(fm.d, q, k, v, alpha, beta, initial_state, o, final_state,
+                        saved ? (char*)saved + L.s_tc : nullptr, ws + L.inner, &fm.sq, &sp, cs);
         if (st != GDN_OK) return st;
-        gdn::FlatMoves mo{1, {ws + L.o}, {o}, {(int)p->H * vb}, {16}, {0u}};
-        e = timed(gdn::KID_VARLEN_SCATTER, cs, [&] {
-            return gdn::launch_varlen_flat(mo, S, fd.C, fd.NC, total, cu_seqlens, off, true,
-                                           (const int*)(ws + L.inner), (int*)ws, cs);
-        });
-        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
+        return flat_merge_error(L, ws, cs);
     }
     const void* src[5] = {q, k, v, alpha, beta};
     const size_t dst[5] = {L.q, L.k, L.v, L.a, L.b};
@@ -869,57 +897,28 @@ gdn_status gdn_varlen_bwd(const gdn_problem* p, int64_t total, const int32_t* cu
     if (p->B * p->H == 0) return GDN_OK;
     const int S = (int)p->B, kb = (int)(p->K * es), vb = (int)(p->V * es);
     if (L.flat) {
-        const gdn::Dims& fd = L.pd;
-        const char* in = saved ? (const char*)saved : ws;
-        const int* off = (const int*)(saved ? in + L.s_off : ws + L.off);
-        const char* lq = in + (saved ? L.s_q : L.q);
-        const char* lk = in + (saved ? L.s_k : L.k);
-        const char* lv = in + (saved ? L.s_v : L.v);
-        const char* la = in + (saved ? L.s_a : L.a);
-        const char* lb = in + (saved ? L.s_b : L.b);
-        gdn::FlatMoves m{};
-        if (saved) {  // the forward laid out the inputs and the offsets: only d_o is new
-            m = gdn::FlatMoves{1, {d_o}, {ws + L.d_o}, {(int)p->H * vb}, {16}, {0u}};
-        } else {
-            e = timed(gdn::KID_VARLEN_OFFSETS, cs, [&] {
-                return gdn::launch_varlen_offsets(S, total, (int)p->T, fd.C, fd.NC, cu_seqlens, (int*)(ws + L.off),
-                                                  (int*)(ws + L.off) + S + 1, (int*)ws, cs);
-            });
-            m = gdn::FlatMoves{6,
-                               {q, k, v, d_o, alpha, beta},
-                               {ws + L.q, ws + L.k, ws + L.v, ws + L.d_o, ws + L.a, ws + L.b},
-                               {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)p->H * vb, (int)(p->H * es),
-                                (int)(p->H * es)},
-                               {16, 16, 16, 16, (int)es, (int)es},
-                               {0u, 0u, 0u, 0u, one_bits(p), 0u}};
+        if (total == 0) {  // no tokens: every state gradient passes through
+            if (d_initial_state) {
+                e = d_final_state
+                        ? cudaMemcpyAsync(d_initial_state, d_final_state, nstate, cudaMemcpyDeviceToDevice, cs)
+                        : cudaMemsetAsync(d_initial_state, 0, nstate, cs);
+                if (e != cudaSuccess) return cuda_fail(e, "state copy");
+            }
+            return GDN_OK;
         }
-        if (e == cudaSuccess)
-            e = timed(gdn::KID_VARLEN_GATHER, cs, [&] {
-                return gdn::launch_varlen_flat(m, S, fd.C, fd.NC, total, cu_seqlens, off, false, nullptr, (int*)ws,
-                                               cs);
-            });
-        if (e != cudaSuccess) return cuda_fail(e, "varlen gather");
-        // longest sequences first; the longest has at most ceil(max_len / C) chunks
-        const gdn::SeqMap sq{off, S, 0, nullptr, off + S + 1, (int)((p->T + fd.C - 1) / fd.C)};
+        // the forward's maps when `saved` is given, else computed here
+        FlatMaps fm;
+        char* ints = saved ? (char*)const_cast<void*>(saved) + L.s_off : ws + L.off;
+        if ((st = flat_maps(L, p, total, cu_seqlens, ints, ws, saved == nullptr, cs, &fm)) != GDN_OK) return st;
         SplitCfg sp;
         sp.P = L.pieces;
         sp.nseq = S;
-        sp.seq_off = off;
-        st = run_bwd_tc(fd, lq, lk, lv, la, lb, initial_state, saved ? (const char*)saved + L.s_tc : nullptr,
-                        ws + L.d_o, d_final_state, ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db,
-                        d_initial_state, ws + L.inner, &sq, &sp, cs);
+        sp.seq_off = fm.sq.chunk_off;
+        st = run_bwd_tc(fm.d, q, k, v, alpha, beta, initial_state, saved ? (const char*)saved + L.s_tc : nullptr,
+                        d_o, d_final_state, dq, dk, dv, dalpha, dbeta, d_initial_state, ws + L.inner, &fm.sq, &sp,
+                        cs);
         if (st != GDN_OK) return st;
-        gdn::FlatMoves mg{5,
-                          {ws + L.dq, ws + L.dk, ws + L.dv, ws + L.da, ws + L.db},
-                          {dq, dk, dv, dalpha, dbeta},
-                          {(int)p->H * kb, (int)p->H * kb, (int)p->H * vb, (int)(p->H * es), (int)(p->H * es)},
-                          {16, 16, 16, (int)es, (int)es},
-                          {0u, 0u, 0u, 0u, 0u}};
-        e = timed(gdn::KID_VARLEN_SCATTER, cs, [&] {
-            return gdn::launch_varlen_flat(mg, S, fd.C, fd.NC, total, cu_seqlens, off, true,
-                                           (const int*)(ws + L.inner), (int*)ws, cs);
-        });
-        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "varlen scatter");
+        return saved ? GDN_OK : flat_merge_error(L, ws, cs);
     }
     const void* src[6] = {q, k, v, d_o, alpha, beta};
     const size_t dst[6] = {L.q, L.k, L.v, L.d_o, L.a, L.b};

@@ -15,6 +15,12 @@ namespace gdn {
 // is done in int64.
 struct Dims {
     int B, T, H, K, V, C, NC;
+    // A packed batch read in place (B = 1, T = the packed token count, one row of
+    // chunks per head): chunk c of the row starts at packed token tok[c] and has
+    // len[c] <= C tokens of its sequence (device arrays of NC ints).  NULL for
+    // dense tensors, where chunk c starts at c * C.
+    const int* tok = nullptr;
+    const int* len = nullptr;
     __host__ __device__ int64_t NS() const { return (int64_t)B * H; }
     // The chunk (index (b * H + h) * NC + c) that work item wi of a chunk-parallel
     // kernel takes: every stream's chunk c before any chunk c + 1, c ascending or
@@ -28,6 +34,20 @@ struct Dims {
         return (wi % NS()) * NC + c;
     }
 };
+
+// First token of chunk c within its batch row, and its number of tokens, for
+// kernels compiled for dense tensors (kPacked false: tok, len unused) or for a
+// packed batch read in place (kPacked true).
+template <bool kPacked>
+__device__ __forceinline__ int chunk_tok(const Dims& d, int c) {
+    if constexpr (kPacked) return d.tok[c];
+    else return c * d.C;
+}
+template <bool kPacked>
+__device__ __forceinline__ int chunk_valid(const Dims& d, int c) {
+    if constexpr (kPacked) return d.len[c];
+    else return d.T - c * d.C < d.C ? d.T - c * d.C : d.C;
+}
 
 // Per-chunk results of the chunk-parallel step (Phase 1 + solve + recompute),
 // float32, indexed [stream][chunk][...]:
@@ -168,6 +188,11 @@ bool tc_fwd_supported(const Dims& d, InType ty);
 // within-call sequence split).  mode 0: the sequences only; 1: the sequences
 // (CTAs z < nseq) and their transitions (z >= nseq, final states to `trans`);
 // 2: the transitions only.
+// tok / len of Dims for the flat layout of a packed batch (one block per chunk
+// row entry; entries past the sequences get len 0).
+cudaError_t launch_varlen_chunk_tokens(int S, int64_t total, int C, int nc_max, const int32_t* cu,
+                                       const int* chunk_off, int* tok, int* len, cudaStream_t st);
+
 struct SeqMap {
     const int* chunk_off;  // device, int32 [nseq + 1]
     int nseq;

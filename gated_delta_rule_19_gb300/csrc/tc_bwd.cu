@@ -183,7 +183,7 @@ struct BScan {
 // lanes 32*w ..  Lanes 0-63: rows of dU (critical); lanes 64-127 prepare the next
 // chunk's gamma dO operand; all lanes update dS^T (rows k).  The three roles run
 // separate loops with the same two block-wide barriers per chunk.
-template <int Vt>
+template <int Vt, bool kPacked>
 __global__ void __launch_bounds__(320, 1)
 scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
@@ -231,7 +231,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         unsigned char* st = sm + (it % NS) * P::STAGE;
         uint64_t* bar = &tbar[it % NS];
         const int row = (int)((cbase + c) * kC);
-        const int t0 = (c0 + c) * kC;
+        const int t0 = chunk_tok<kPacked>(d, c0 + c);
         mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         tma_load_2d(st + P::OFF_M, &tm_M, bar, 0, row);
         for (int j = 0; j < 2; ++j) {
@@ -270,9 +270,12 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     float GC_n = (NC > 0 && epi) ? G[(cbase + NC - 1) * kC + kC - 1] : 0.f;
     float Gr_n = (NC > 0 && epi) ? G[(cbase + NC - 1) * kC + r] : 0.f;
     // gamma dO operand (buffer it2 & 1) of iteration it2's chunk, from its stage;
-    // rows of lanes 64-127; uses gamma_r = exp(Gr_n) of that chunk.
+    // rows of lanes 64-127; uses gamma_r = exp(Gr_n) of that chunk.  Rows past the
+    // chunk's tokens (a packed batch's ragged chunk reads the next sequence's dO)
+    // are zero.
     auto write_gdo_operand = [&](int it2, bool& okk) {
         okk = mbar_wait(&tbar[it2 % NS], (it2 / NS) & 1, err, 8) && okk;
+        const bool live = !kPacked || r < chunk_valid<true>(d, c0 + NC - 1 - it2);
         const float gr = expf(Gr_n);
         const unsigned char* dsrc = sm + (it2 % NS) * P::STAGE + P::OFF_DO;
         unsigned char* ddst = sm + P::GDO_OP + (it2 & 1) * (kC * Vt * 2);
@@ -284,8 +287,8 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             float f[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                f[2 * e] = gr * bf_lo(w4[e]);
-                f[2 * e + 1] = gr * bf_hi(w4[e]);
+                f[2 * e] = live ? gr * bf_lo(w4[e]) : 0.f;
+                f[2 * e + 1] = live ? gr * bf_hi(w4[e]) : 0.f;
             }
             *(uint4*)(ddst + gg * 1024 + r * 16) = pack8(f);
         }
@@ -544,7 +547,7 @@ static_assert(SMEM <= 232448, "one CTA per SM");
 // further chunks from a work counter.  Warps w, w+4, w+8, w+12 reach TMEM lanes
 // 32*(w%4) .. and split the columns of every epilogue.  Group A tiles of the next
 // chunk are requested as soon as phase 1's MMAs are done, group B after phase 2.
-template <bool kRaw>
+template <bool kRaw, bool kPacked>
 __global__ void __launch_bounds__(512, 1)
 grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_U,
@@ -552,7 +555,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
            const __grid_constant__ CUtensorMap tm_dS1, const __grid_constant__ CUtensorMap tm_dq,
            const __grid_constant__ CUtensorMap tm_dKp, const __grid_constant__ CUtensorMap tm_dWt,
            const bf16* __restrict__ Mqk, const float* __restrict__ G, float* __restrict__ dGp, RawPrologue raw,
-           int* err) {
+           bf16* __restrict__ dq_rows, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* Gs = (float*)(sm + qk::VEC);
@@ -591,7 +594,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_arrive_expect_tx(&bars[0], 14 * 8192);
         for (int j = 0; j < 2; ++j) {
             tma_load_2d(sm + qk::U + j * 8192, &tm_U, &bars[0], 64 * j, row0);
-            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[0], 64 * j, h, c * kC, b);
+            tma_load_4d(sm + qk::DO + j * 16384, &tm_do, &bars[0], 64 * j, h, chunk_tok<kPacked>(d, c), b);
             tma_load_2d(sm + qk::DO + j * 16384 + 8192, &tm_dU, &bars[0], 64 * j, row0);
             for (int i = 0; i < 2; ++i) {
                 tma_load_2d(sm + qk::S0 + j * 16384 + i * 8192, &tm_S0, &bars[0], 64 * j, krow0 + 64 * i);
@@ -604,8 +607,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         decode(ch, b, h, c);
         mbar_arrive_expect_tx(&bars[1], 4 * 8192);
         for (int j = 0; j < 2; ++j) {
-            tma_load_4d(sm + qk::Q + j * 8192, &tm_q, &bars[1], 64 * j, h, c * kC, b);
-            tma_load_4d(sm + qk::K + j * 8192, &tm_k, &bars[1], 64 * j, h, c * kC, b);
+            tma_load_4d(sm + qk::Q + j * 8192, &tm_q, &bars[1], 64 * j, h, chunk_tok<kPacked>(d, c), b);
+            tma_load_4d(sm + qk::K + j * 8192, &tm_k, &bars[1], 64 * j, h, chunk_tok<kPacked>(d, c), b);
         }
     };
 
@@ -674,7 +677,8 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     for (int64_t ch = first; ch < nchunks; ch = nxt, ++n) {
         int b, h, c;
         decode(ch, b, h, c);
-        const int t0 = c * kC;
+        const int t0 = chunk_tok<kPacked>(d, c);  // first token of the chunk
+        const int nv = kPacked ? chunk_valid<true>(d, c) : kC;  // its tokens (packed)
         const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
         const int ph = n & 1;
         if (warp == 3) {
@@ -760,7 +764,9 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const float mq = (j & 1) ? bf_hi(mw[j >> 1]) : bf_lo(mw[j >> 1]);
                     e1[j] = dm[j] * mq;
                     rsum += e1[j];
-                    dq[j] = (i <= r) ? __expf(Gr - Gs[i]) * dm[j] : 0.f;
+                    // rows past the chunk's tokens (a packed batch's ragged chunk reads
+                    // the next sequence's dO) are zero
+                    dq[j] = (i <= r && (!kPacked || r < nv)) ? __expf(Gr - Gs[i]) * dm[j] : 0.f;
                 }
                 tile_put16(sm + qk::DQK, 64, r, cb, dq);
                 rE1[qtr * 64 + r] = rsum;
@@ -903,7 +909,11 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const float re = rE1[t] + rE1[64 + t] + rE1[128 + t] + rE1[192 + t];
             const int qq = t >> 4, col = t & 15;
             const float ce = cE1[(0 * 4 + qq) * 16 + col] + cE1[(1 * 4 + qq) * 16 + col];
-            float g = gs[t] * dG1 + re - ce - expf(GC - Gs[t]) * eR;
+            // per-token terms only for the chunk's tokens (past them, dQ1 carries the
+            // next sequence's dO in a packed batch's ragged chunk); the chunk-level
+            // terms (gamma_C in S1, exp(G_C - G) in Khat) sit at position 63, from
+            // where the reverse cumsum carries them to every token of the chunk
+            float g = (!kPacked || t < nv) ? gs[t] * dG1 + re - ce - expf(GC - Gs[t]) * eR : 0.f;
             if (t == 63) g += gC * fin[0] + fin[1];
             dGp[(int64_t)row0 + t] = g;
             // k . (the dK part written here) = exp(G_C - G_t) eR_t + the column sum of E1
@@ -913,12 +923,25 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
+        const bool dq_tma = !kPacked || nv == kC;
         if (tid == kIssuer && ok) {
             for (int j = 0; j < 2; ++j) {
-                if (64 * j < d.K) tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
+                if (dq_tma && 64 * j < d.K) tma_store_4d(&tm_dq, sm + qk::DQ + j * 8192, 64 * j, h, t0, b);
                 tma_store_2d(&tm_dKp, sm + qk::DKP + j * 8192, 0, krow0 + 64 * j);
             }
             bulk_commit();
+        }
+        if constexpr (kPacked) {
+            if (!dq_tma && ok && warp == kIssuer / 32) {
+                // the last chunk of a packed sequence, fewer than 64 tokens: the valid
+                // rows of dq (the rows after them belong to the next sequence)
+                for (int i = lane; i < nv * (kD / 8); i += 32) {
+                    const int t = i / (kD / 8), k8 = 8 * (i % (kD / 8));
+                    if (k8 < d.K)
+                        *(uint4*)(dq_rows + ((int64_t)(t0 + t) * d.H + h) * d.K + k8) =
+                            *(const uint4*)(sm + qk::DQ + (k8 >> 6) * 8192 + sw128_off(t, k8 & 63));
+                }
+            }
         }
         if (!ok) break;
     }
@@ -969,7 +992,7 @@ static_assert(DK + 16384 == VEC, "the dK tile spans the dT and Y tiles");
 // whole rows.  dK is staged in the dT and Y tiles, so every input slot is free once
 // phase 4's MMA is done: the next chunk's tiles are requested then, and warp 3
 // reads the next chunk's per-token values into registers a chunk ahead.
-template <bool kRaw>
+template <bool kRaw, bool kPacked>
 __global__ void __launch_bounds__(256, 2)
 grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_dWt, const __grid_constant__ CUtensorMap tm_dU,
@@ -977,7 +1000,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
            const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dKp,
            const bf16* __restrict__ alpha, const bf16* __restrict__ beta, const float* __restrict__ G,
            const float* __restrict__ dGp, bf16* __restrict__ dalpha, bf16* __restrict__ dbeta, RawPrologue raw,
-           int* err) {
+           bf16* __restrict__ dk_rows, bf16* __restrict__ dv_rows, int* err) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     float* vec = (float*)(sm + wy::VEC);
@@ -1006,9 +1029,10 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int cb = half * 32;                     // this warp's 32 columns of a 64-column result
     const int64_t nchunks = d.NS() * d.NC;
 
-    // chunk index = (b * H + h) * NC + c
+    // chunk index = (b * H + h) * NC + c; its first token (a packed batch: from the
+    // chunk-token map)
     auto decode = [&](int64_t ch, int& b, int& h, int& t0) {
-        t0 = (int)(ch % d.NC) * kC;
+        t0 = chunk_tok<kPacked>(d, (int)(ch % d.NC));
         h = (int)((ch / d.NC) % d.H);
         b = (int)(ch / d.NC / d.H);
     };
@@ -1038,12 +1062,13 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         qv = *(const float2*)(dGp + row0 + 2 * lane);
         if (kRaw) dv2 = *(const float2*)(raw.kdot + row0 + 2 * lane);
         float kr[2] = {0.f, 0.f};
+        const int nv = chunk_valid<kPacked>(d, (int)(ch % d.NC));
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * lane + e;
             ga[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 1.f);
             gb[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 0.f);
-            if (t < d.T) {
+            if (kPacked ? 2 * lane + e < nv : t < d.T) {
                 const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
                 ga[e] = alpha[gi];
                 gb[e] = beta[gi];
@@ -1095,6 +1120,20 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const int ph = n & 1;
         int b, h, t0;
         decode(ch, b, h, t0);
+        const int nv = chunk_valid<kPacked>(d, (int)(ch % d.NC));  // tokens of the chunk
+        // a packed sequence's last chunk of fewer than 64 tokens: dk and dv rows are
+        // copied by warp 0 (the rows after them belong to the next sequence)
+        const bool out_tma = !kPacked || nv == kC;
+        auto copy_rows = [&](bf16* dst, int width, const unsigned char* tile) {
+            if constexpr (kPacked) {
+                for (int i = lane; i < nv * (kD / 8); i += 32) {
+                    const int t = i / (kD / 8), c8 = 8 * (i % (kD / 8));
+                    if (c8 < width)
+                        *(uint4*)(dst + ((int64_t)(t0 + t) * d.H + h) * width + c8) =
+                            *(const uint4*)(tile + (c8 >> 6) * 8192 + sw128_off(t, c8 & 63));
+                }
+            }
+        };
         const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
         trk = 0;
         if (warp == 3) {
@@ -1316,10 +1355,13 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             __syncwarp();
         }
         // ---- phase 4: dK = T1^T dW + E K + E^T K + dK_partial (N=128, tokens on rows 64-127)
+        if (!out_tma && warp == 0 && ok) copy_rows(dv_rows, d.V, sm + wy::DV);
         if (tid == 0 && ok) {
-            for (int j = 0; j < 2; ++j)
-                if (64 * j < d.V) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
-            bulk_commit();
+            if (out_tma) {
+                for (int j = 0; j < 2; ++j)
+                    if (64 * j < d.V) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
+                bulk_commit();
+            }
             ok = mbar_wait(&bars[2], ph, err, 16);
             if (ok) {
                 const uint32_t id_mk = idesc_bf16(128, 128, true, false);   // A MN-major, B K-major
@@ -1369,7 +1411,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int t = t0 + pos[e];
-                if (t < d.T) {
+                if (kPacked ? pos[e] < nv : t < d.T) {
                     const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
                     const int p = pos[e];
                     const float dbv = cB12[p] + cB12[64 + p] + dB3p[p] + dB3p[64 + p];
@@ -1413,11 +1455,12 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        if (tid == 0 && ok) {
+        if (tid == 0 && ok && out_tma) {
             for (int j = 0; j < 2; ++j)
                 if (64 * j < d.K) tma_store_4d(&tm_dk, sm + wy::DK + j * 8192, 64 * j, h, t0, b);
             bulk_commit();
         }
+        if (!out_tma && warp == 0 && ok) copy_rows(dk_rows, d.K, sm + wy::DK);
         if (!ok) break;
     }
     if (tid == 0) {
@@ -1449,7 +1492,7 @@ cudaError_t launch_scan_bwd_vt(const Dims& d, const void* q, const void* k, cons
         !tmap_core8_rows(&mdU, bb.dU, rows, kD, kC, Vt / 8) ||
         !tmap_core8_rows(&mdS1, bb.dS1, d.NS() * d.NC * kD, kD, kD, Vt / 8))
         return cudaErrorInvalidValue;
-    auto kern = scan_bwd_tc<Vt>;
+    auto kern = d.tok ? scan_bwd_tc<Vt, true> : scan_bwd_tc<Vt, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((kD + Vt - 1) / Vt, d.H, sq ? sq->nseq : d.B);
@@ -1487,13 +1530,13 @@ cudaError_t launch_grad_qk_tc(const Dims& d, const void* q, const void* k, const
         return cudaErrorInvalidValue;
     RawPrologue raw{};
     if (rp && rp->on) raw = *rp;
-    auto kern = raw.on ? grad_qk_tc<true> : grad_qk_tc<false>;
+    auto kern = d.tok ? grad_qk_tc<false, true> : (raw.on ? grad_qk_tc<true, false> : grad_qk_tc<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qk::SMEM);
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;
     dim3 grid((unsigned)std::min<int64_t>(nchunks, sm_count()));
     kern<<<grid, 512, qk::SMEM, st>>>(d, mq, mk, mdo, mU, mdU, mS0, mdS1, mdq, mdKp, mdWt, tb.Mqk, tb.G,
-                                            bb.dGp, raw, tb.err);
+                                            bb.dGp, raw, (bf16*)dq, tb.err);
     return cudaGetLastError();
 }
 
@@ -1510,13 +1553,13 @@ cudaError_t launch_grad_wy_tc(const Dims& d, const void* k, const void* v, const
         return cudaErrorInvalidValue;
     RawPrologue raw{};
     if (rp && rp->on) raw = *rp;
-    auto kern = raw.on ? grad_wy_tc<true> : grad_wy_tc<false>;
+    auto kern = d.tok ? grad_wy_tc<false, true> : (raw.on ? grad_wy_tc<true, false> : grad_wy_tc<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wy::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)std::min<int64_t>(d.NS() * d.NC, 2 * sm_count()));
     kern<<<grid, 256, wy::SMEM, st>>>(d, mk, mv, mdWt, mdU, mT, mdk, mdv, mdKp, (const bf16*)alpha,
                                             (const bf16*)beta, tb.G, bb.dGp, (bf16*)dalpha, (bf16*)dbeta, raw,
-                                            tb.err);
+                                            (bf16*)dk, (bf16*)dv, tb.err);
     return cudaGetLastError();
 }
 

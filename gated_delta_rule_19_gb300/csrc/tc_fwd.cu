@@ -195,7 +195,7 @@ static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 // A chunk's Q tiles are replaced by the next chunk's once the Gram MMA is done, its
 // K and V tiles once the W / Ut MMA is done (both requested by thread 128, whose
 // warp has no Gram epilogue work); warp 2 keeps the next chunk's gates in registers.
-template <bool kRaw>
+template <bool kRaw, bool kPacked>
 __global__ void __launch_bounds__(256, 2)
 prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_W,
@@ -218,9 +218,10 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int64_t nchunks = d.NS() * d.NC;
     constexpr int kLoader = 128;
 
-    // chunk index = (b * H + h) * NC + c
+    // chunk index = (b * H + h) * NC + c; its first token (a packed batch: from the
+    // chunk-token map)
     auto decode = [&](int64_t ch, int& b, int& h, int& t0) {
-        t0 = (int)(ch % d.NC) * kC;
+        t0 = chunk_tok<kPacked>(d, (int)(ch % d.NC));
         const int64_t bh = ch / d.NC;
         h = (int)(bh % d.H);
         b = (int)(bh / d.H);
@@ -251,12 +252,13 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     auto load_gates = [&](int64_t ch) {
         int b, h, t0;
         decode(ch, b, h, t0);
+        const int nv = chunk_valid<kPacked>(d, (int)(ch % d.NC));
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int t = t0 + 2 * lane + e;
             ga[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 1.f);
             gb[e] = __float2bfloat16_rn(kRaw ? -INFINITY : 0.f);
-            if (t < d.T) {
+            if (kPacked ? 2 * lane + e < nv : t < d.T) {
                 const int64_t gi = ((int64_t)b * d.T + t) * d.H + h;
                 ga[e] = alpha[gi];
                 gb[e] = beta[gi];
@@ -398,9 +400,12 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             ++nq;
         }
         // Gram epilogue: lanes 0-63 hold rows of K K^T -> A (fp32), lanes 64-127 rows of
-        // Q K^T -> Mqk (bf16 tile); this warp takes columns cb .. cb+31.
+        // Q K^T -> Mqk (bf16 tile); this warp takes columns cb .. cb+31.  Rows past the
+        // chunk's tokens (a packed batch's ragged chunk reads the next sequence's rows)
+        // are zero in Mqk; in A their beta is 0.
         {
             const int rr = 32 * (sub & 1) + lane;
+            const int nv_rows = kPacked ? chunk_valid<true>(d, (int)(ch % d.NC)) : kC;
             const int cb = 32 * half;
             const bool any = cb <= 32 * (sub & 1) + 31;  // warp-uniform: some column on or below the diagonal
             const float G2r = G2s[rr];
@@ -434,9 +439,12 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i = cb + 8 * q + 2 * e;
-                            const float m0 = (i <= rr) ? fast_exp2(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
-                            const float m1 =
-                                (i + 1 <= rr) ? fast_exp2(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f;
+                            const bool live = !kPacked || rr < nv_rows;
+                            const float m0 =
+                                (live && i <= rr) ? fast_exp2(G2r - G2s[i]) * __uint_as_float(v[8 * q + 2 * e]) : 0.f;
+                            const float m1 = (live && i + 1 <= rr)
+                                                 ? fast_exp2(G2r - G2s[i + 1]) * __uint_as_float(v[8 * q + 2 * e + 1])
+                                                 : 0.f;
                             pk[e] = pack_bf16(m0, m1);
                         }
                         *(uint4*)(mt + sw128_off(rr, cb + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -673,14 +681,14 @@ __device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, 
 // (rows of U), lanes 64-127 hold Y = Q S0^T and the output term; the state update
 // uses all 128 lanes (rows k).  The three roles run separate loops with the same
 // two block-wide barriers per chunk.
-template <int Vt>
+template <int Vt, bool kPacked>
 __global__ void __launch_bounds__(320, 1)
 scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_W, const __grid_constant__ CUtensorMap tm_M,
             const __grid_constant__ CUtensorMap tm_Ut, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_st, const float* __restrict__ G, const float* s0,
             float* sT, int write_o, int write_states, const int* __restrict__ chunk_off, int nseq, int tmode,
-            float* trans, const int* __restrict__ order, int* err) {
+            float* trans, const int* __restrict__ order, bf16* __restrict__ o_rows, int* err) {
     using P = ScanPlan<Vt>;
     constexpr int HV = Vt / 2;  // columns per thread
     constexpr int NS = P::NS;
@@ -729,7 +737,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     auto issue_loads = [&](int c) {
         unsigned char* st = sm + (c % NS) * P::STAGE;
         const int row = (int)((cbase + c) * kC);
-        const int t0 = (c0 + c) * kC;
+        const int t0 = chunk_tok<kPacked>(d, c0 + c);
         uint64_t* bar = &tbar[c % NS];
         mbar_arrive_expect_tx(bar, 7 * 8192 + kC * Vt * 2);
         for (int j = 0; j < 2; ++j) {
@@ -825,6 +833,31 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     };
 
+    // Output tile of chunk cc to o: one TMA store, except the last chunk of a packed
+    // sequence with fewer than 64 tokens, whose valid rows the TMA warp copies (the
+    // rows after them belong to the next sequence).  Called by the whole TMA warp.
+    auto store_o = [&](int cc) {
+        const unsigned char* tile = sm + P::O_OP + (cc & 1) * (kC * Vt * 2);
+        const int t0 = chunk_tok<kPacked>(d, c0 + cc);
+        if (!kPacked || chunk_valid<true>(d, c0 + cc) == kC) {
+            if (tma_issuer) {
+                tma_store_5d(&tm_o, tile, 0, t0, v0 / 8, h, b);
+                bulk_commit();
+            }
+            return;
+        }
+        if constexpr (kPacked) {
+            // core-matrix tile: 8 columns of row r at (group) * 1024 + r * 16
+            const int nv = chunk_valid<true>(d, c0 + cc);
+            for (int i = lane; i < nv * (Vt / 8); i += 32) {
+                const int r = i / (Vt / 8), g = i % (Vt / 8);
+                if (v0 + 8 * g < d.V)
+                    *(uint4*)(o_rows + ((int64_t)(t0 + r) * d.H + h) * d.V + v0 + 8 * g) =
+                        *(const uint4*)(tile + g * 1024 + r * 16);
+            }
+        }
+    };
+
     bool ok = true;
     int c = 0;
     int xy_last = -1, o_last = -1;  // last chunk whose [X;Y] / output MMAs were committed (MMA issuer)
@@ -901,17 +934,17 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tma_store_3d(&tm_Ut, sm + P::U_OP, 0, (int)((cbase + c) * kC), v0 / 8);
                     bulk_commit();
                 }
-                if (c > 0 && wr_o) {  // output tile of the previous chunk
-                    tma_store_5d(&tm_o, sm + P::O_OP + ((c - 1) & 1) * (kC * Vt * 2), 0, (c0 + c - 1) * kC,
-                                 v0 / 8, h, b);
-                    bulk_commit();
+            }
+            if (c > 0 && wr_o) store_o(c - 1);  // output tile of the previous chunk
+            if (tma_issuer) {
+                if (c > 0 && wr_o && (!kPacked || chunk_valid<true>(d, c0 + c - 1) == kC)) {
                     // the store issued a chunk earlier has read its tile, which the
                     // next output epilogue rewrites; so has the U store (older group)
                     bulk_wait_read1();
                 } else {
-                    // the U store has read its tile, which the next U epilogue rewrites
-                    if (wr_states) bulk_wait_read0();
-                    else bulk_wait_read1();
+                    // no output store this chunk (or rows copied by the warp): every
+                    // store so far has read its tile (the U tile is rewritten next)
+                    bulk_wait_read0();
                 }
             }
             __syncwarp();
@@ -1010,11 +1043,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_proxy_async();
         fence_before_sync();
         ok = __syncthreads_and(ok);
-        if (tma_issuer && ok && wr_o) {
-            tma_store_5d(&tm_o, sm + P::O_OP + ((NC - 1) & 1) * (kC * Vt * 2), 0, (c0 + NC - 1) * kC, v0 / 8, h,
-                         b);
-            bulk_commit();
-        }
+        if (tma_warp && ok && wr_o) store_o(NC - 1);
     }
     if (ok && s_out && epi) {
 #pragma unroll
@@ -1053,7 +1082,7 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     if (o && !tmap_core8_bthd(&mo, o, d.B, d.T, d.H, d.V, Vt / 8)) return cudaErrorInvalidValue;
     if (states && !tmap_core8_rows(&mst, states, d.NS() * d.NC * kD, kD, kD, Vt / 8))
         return cudaErrorInvalidValue;
-    auto kern = scan_fwd_tc<Vt>;
+    auto kern = d.tok ? scan_fwd_tc<Vt, true> : scan_fwd_tc<Vt, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::SMEM);
     if (e != cudaSuccess) return e;
     const int mode = sq ? sq->mode : 0;
@@ -1062,7 +1091,8 @@ cudaError_t launch_scan_vt(const Dims& d, const void* q, const void* k, const Tc
     const bool tr_only = mode == 2;
     kern<<<grid, 320, P::SMEM, st>>>(d, mq, mk, mW, mM, mUt, mo, mst, tb.G, s0, sT, (o != nullptr && !tr_only),
                                      (states != nullptr && !tr_only), sq ? sq->chunk_off : nullptr, nseq, mode,
-                                     sq ? sq->trans : nullptr, (sq && mode == 0) ? sq->order : nullptr, tb.err);
+                                     sq ? sq->trans : nullptr, (sq && mode == 0) ? sq->order : nullptr,
+                                     (bf16*)o, tb.err);
     return cudaGetLastError();
 }
 
@@ -1118,7 +1148,7 @@ cudaError_t launch_prep_tc(const Dims& d, const void* q, const void* k, const vo
         return cudaErrorInvalidValue;
     RawPrologue raw{};
     if (rp && rp->on) raw = *rp;
-    auto kern = raw.on ? prep_fwd_tc<true> : prep_fwd_tc<false>;
+    auto kern = d.tok ? prep_fwd_tc<false, true> : (raw.on ? prep_fwd_tc<true, false> : prep_fwd_tc<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     const int64_t nchunks = d.NS() * d.NC;

@@ -154,6 +154,27 @@ __device__ __forceinline__ int last_le(const int* a, int n, int64_t x) {
     return lo;
 }
 
+// tok[c] / len[c] for flat chunk c: the sequence s owning it (chunk_off[s] <= c <
+// chunk_off[s+1]) starts at packed row start_s, so chunk j = c - chunk_off[s] of it
+// starts at start_s + j*C with min(C, len_s - j*C) tokens.  Chunks past the last
+// sequence get tok 0, len 0.
+__global__ void chunk_tokens_kernel(int S, int64_t total, int C, int nc_max, const int32_t* __restrict__ cu,
+                                    const int* __restrict__ chunk_off, int* __restrict__ tok, int* __restrict__ len) {
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nc_max; c += gridDim.x * blockDim.x) {
+        int t = 0, n = 0;
+        if (S > 0 && c < chunk_off[S]) {
+            const int s = last_le(chunk_off, S, c);
+            int64_t start;
+            const int ls = flat_len(cu, chunk_off, s, total, C, start);
+            const int j = c - chunk_off[s];
+            n = (int)max((int64_t)0, min((int64_t)C, (int64_t)ls - (int64_t)j * C));
+            t = n > 0 ? (int)(start + (int64_t)j * C) : 0;
+        }
+        tok[c] = t;
+        len[c] = n;
+    }
+}
+
 // One contiguous run: `nvalid` units copied, then (gather only) `ntotal - nvalid`
 // units of fill.  Four independent loads in flight per thread.
 template <typename U>
@@ -265,6 +286,14 @@ cudaError_t launch_varlen_offsets(int S, int64_t total, int max_len, int C, int 
     int nt = 32;  // a power of two for the block scan
     while (nt < 1024 && nt < S) nt <<= 1;
     offsets_kernel<<<1, nt, 0, st>>>(S, total, max_len, C, nc_max, cu, chunk_off, order, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_chunk_tokens(int S, int64_t total, int C, int nc_max, const int32_t* cu,
+                                       const int* chunk_off, int* tok, int* len, cudaStream_t st) {
+    if (nc_max <= 0) return cudaSuccess;
+    const int grid = (nc_max + 255) / 256;
+    chunk_tokens_kernel<<<grid < 1024 ? grid : 1024, 256, 0, st>>>(S, total, C, nc_max, cu, chunk_off, tok, len);
     return cudaGetLastError();
 }
 
