@@ -130,9 +130,9 @@ enum KernelId {
     KID_DECODE,          // decode_kernel
     KID_PROLOGUE_FWD,    // prologue_fwd_kernel
     KID_PROLOGUE_BWD,    // prologue_bwd_kernel
-    KID_VARLEN_OFFSETS,  // offsets_kernel (chunk offsets of packed sequences)
-    KID_VARLEN_GATHER,   // flat_kernel / rows16_kernel / elems_kernel, packed -> laid out
-    KID_VARLEN_SCATTER,  // the same, laid out -> packed
+    KID_VARLEN_OFFSETS,  // offsets_kernel, chunk_tokens_kernel (chunk offsets and token map)
+    KID_VARLEN_GATHER,   // rows16_kernel / elems_kernel, packed -> padded layout
+    KID_VARLEN_SCATTER,  // the same, padded layout -> packed
     KID_SPLIT_FWD_P1,    // scan_fwd_tc, split pass 1 (zero-start states and transitions of the pieces)
     KID_SPLIT_BWD_P1,    // scan_bwd_tc, split pass 1 (zero-start state gradients of the pieces)
     KID_SPLIT_TRANS,     // scan_fwd_tc, transitions only (backward with saved)
@@ -242,22 +242,9 @@ cudaError_t launch_varlen_elems(const Dims& d, int64_t total, const int32_t* cu,
 // The flat chunk layout (SeqMap): chunk_off from cu (one block; lengths above
 // max_len or invalid pairs count as empty and set the error bit; the offsets
 // never pass nc_max) and, when `order` is not NULL, the sequences by chunk count,
-// longest first (0 .. S-1 above 1024 sequences), then rows and single elements to (gather) and from
-// (scatter) the flat [H rows of nc_max*C tokens] layout.
+// longest first (0 .. S-1 above 1024 sequences).
 cudaError_t launch_varlen_offsets(int S, int64_t total, int max_len, int C, int nc_max, const int32_t* cu,
                                   int* chunk_off, int* order, int* err, cudaStream_t st);
-// Up to 8 tensors moved by one launch; row_bytes = H * (bytes per token and head),
-// a multiple of 16 or, for the gates, H * 2 or H * 4 with elem_bytes 2 or 4.
-struct FlatMoves {
-    int n;
-    const void* src[8];
-    void* dst[8];
-    int row_bytes[8];
-    int elem_bytes[8];  // 16 for row tensors
-    uint32_t fill[8];
-};
-cudaError_t launch_varlen_flat(const FlatMoves& m, int S, int C, int nc_max, int64_t total, const int32_t* cu,
-                               const int* chunk_off, bool scatter, const int* merge, int* err, cudaStream_t st);
 
 // q/k L2 normalisation and gate activations, and their backward (prologue.cu).
 cudaError_t launch_prologue_fwd(const Dims& d, InType ty, const void* qr, const void* kr, const void* a,

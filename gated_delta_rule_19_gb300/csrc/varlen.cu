@@ -1,8 +1,11 @@
 // varlen.cu -- packed variable-length batches.  Sequence s occupies rows
-// cu[s] .. cu[s+1]-1 of the packed tensors [total, H, ...]; gather copies them
-// into the padded layout [S, T, H, ...] the chunk kernels run on, filling rows
-// t >= len_s with a pad value (zeros for q, k, v, dO; alpha = 1 and beta = 0,
-// which leave the state unchanged), and scatter copies the padded results back.
+// cu[s] .. cu[s+1]-1 of the packed tensors [total, H, ...].  For the tensor-core
+// kernels, which read and write the packed tensors in place: the chunk offsets
+// of the flat layout and each chunk's first packed row and length.  For the
+// other shapes: gather copies the sequences into the padded layout [S, T, H, ...]
+// the chunk kernels run on, filling rows t >= len_s with a pad value (zeros for
+// q, k, v, dO; alpha = 1 and beta = 0, which leave the state unchanged), and
+// scatter copies the padded results back.
 // cu is read on the device: an offset outside [0, total], a decreasing pair, or a
 // length above T marks the sequence as empty and sets kVarlenBadOffsets in the
 // error word, so no access leaves the buffers.
@@ -175,81 +178,6 @@ __global__ void chunk_tokens_kernel(int S, int64_t total, int C, int nc_max, con
     }
 }
 
-// One contiguous run: `nvalid` units copied, then (gather only) `ntotal - nvalid`
-// units of fill.  Four independent loads in flight per thread.
-template <typename U>
-__device__ __forceinline__ void move_run(const U* __restrict__ src, U* __restrict__ dst, int nvalid, int ntotal,
-                                         U fill, bool do_fill) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    int i = tid;
-    for (; i + 3 * nt < nvalid; i += 4 * nt) {
-        const U a = src[i], b = src[i + nt], c = src[i + 2 * nt], d = src[i + 3 * nt];
-        dst[i] = a;
-        dst[i + nt] = b;
-        dst[i + 2 * nt] = c;
-        dst[i + 3 * nt] = d;
-    }
-    for (; i < nvalid; i += nt) dst[i] = src[i];
-    if (do_fill)
-        for (int k = nvalid + tid; k < ntotal; k += nt) dst[k] = fill;
-}
-
-// Block per flat chunk c and tensor t = blockIdx.y (so that the work spreads evenly
-// over the SMs): the sequence s owning chunk c (chunk_off[s] <= c < chunk_off[s+1])
-// has n = min(C, len - j*C) valid rows there, j = c - chunk_off[s], at packed rows
-// start + j*C ...  Both sides are contiguous runs of rows, so the tensor is one
-// copy of n rows plus (gather) C - n rows of fill.
-__global__ void flat_move_kernel(FlatMoves m, int S, int C, int nc_max, int64_t total,
-                                 const int32_t* __restrict__ cu, const int* __restrict__ chunk_off, int dir,
-                                 const int* merge, int* err) {
-    if (merge && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(err, *merge);
-    __shared__ int64_t sh_row;
-    __shared__ int sh_n;
-    for (int c = blockIdx.x; c < nc_max; c += gridDim.x) {
-        if (threadIdx.x == 0) {
-            int n = 0;
-            int64_t prow = 0;
-            if (S > 0 && c < chunk_off[S]) {
-                const int s = last_le(chunk_off, S, c);
-                int64_t start;
-                const int len = flat_len(cu, chunk_off, s, total, C, start);
-                const int64_t j = c - chunk_off[s];
-                n = (int)max((int64_t)0, min((int64_t)C, (int64_t)len - j * C));
-                prow = start + j * C;
-            }
-            sh_n = n;
-            sh_row = prow;
-        }
-        __syncthreads();
-        const int n = sh_n;
-        const int64_t prow = sh_row;
-        if ((dir == 0 || n > 0) && (int)blockIdx.y < m.n) {
-            const int t = blockIdx.y;
-            const int rb = m.row_bytes[t], eb = m.elem_bytes[t];
-            const int per_row = rb / eb;
-            const int64_t fo = (int64_t)c * C * per_row, po = prow * per_row;
-            const int nv = n * per_row, nall = C * per_row;
-            const char* sb = (const char*)m.src[t];
-            char* db = (char*)m.dst[t];
-            const uint32_t f = m.fill[t];
-            if (eb == 16) {
-                const uint4* sp = (const uint4*)sb + (dir == 0 ? po : fo);
-                uint4* dp = (uint4*)db + (dir == 0 ? fo : po);
-                move_run<uint4>(sp, dp, nv, nall, make_uint4(f, f, f, f), dir == 0);
-            } else if (eb == 4) {
-                const uint32_t* sp = (const uint32_t*)sb + (dir == 0 ? po : fo);
-                uint32_t* dp = (uint32_t*)db + (dir == 0 ? fo : po);
-                move_run<uint32_t>(sp, dp, nv, nall, f, dir == 0);
-            } else {
-                const uint16_t* sp = (const uint16_t*)sb + (dir == 0 ? po : fo);
-                uint16_t* dp = (uint16_t*)db + (dir == 0 ? fo : po);
-                move_run<uint16_t>(sp, dp, nv, nall, (uint16_t)f, dir == 0);
-            }
-        }
-        __syncthreads();  // sh_n / sh_row are rewritten for the next chunk
-    }
-}
-
 unsigned grid_for(int64_t n) {
     const int64_t want = (n + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 16;
@@ -294,20 +222,6 @@ cudaError_t launch_varlen_chunk_tokens(int S, int64_t total, int C, int nc_max, 
     if (nc_max <= 0) return cudaSuccess;
     const int grid = (nc_max + 255) / 256;
     chunk_tokens_kernel<<<grid < 1024 ? grid : 1024, 256, 0, st>>>(S, total, C, nc_max, cu, chunk_off, tok, len);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_varlen_flat(const FlatMoves& m, int S, int C, int nc_max, int64_t total, const int32_t* cu,
-                               const int* chunk_off, bool scatter, const int* merge, int* err, cudaStream_t st) {
-    for (int t = 0; t < m.n; ++t)
-        if ((m.elem_bytes[t] != 16 && m.elem_bytes[t] != 4 && m.elem_bytes[t] != 2) ||
-            m.row_bytes[t] % m.elem_bytes[t] != 0)
-            return cudaErrorInvalidValue;
-    if (m.n < 0 || m.n > 8) return cudaErrorInvalidValue;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    const unsigned grid = (unsigned)max((int64_t)1, min((int64_t)nc_max, cap));
-    const dim3 g2(grid, (unsigned)(m.n > 0 ? m.n : 1));  // one row of blocks even with no tensor (merge)
-    flat_move_kernel<<<g2, 256, 0, st>>>(m, S, C, nc_max, total, cu, chunk_off, scatter ? 1 : 0, merge, err);
     return cudaGetLastError();
 }
 

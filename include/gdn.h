@@ -254,19 +254,23 @@ gdn_status gdn_bwd_raw(const gdn_problem* p, const void* q_raw, const void* k_ra
  *   saved        : NULL or gdn_varlen_saved_bytes(p, total) bytes, filled by
  *                  gdn_varlen_fwd and read by gdn_varlen_bwd with the same
  *                  inputs and cu_seqlens.  On the tensor-core path it also keeps
- *                  the laid-out inputs and the chunk offsets, so the backward
- *                  then lays out only d_o (and does not re-check cu_seqlens).
+ *                  the chunk offsets and each chunk's first token and length, so
+ *                  the backward does not recompute (or re-check) them.
  *   workspace    : gdn_varlen_fwd_workspace_bytes(p, total) /
  *                  gdn_varlen_bwd_workspace_bytes(p, total) bytes.
- * Method: the sequences are copied into a chunk layout inside the workspace,
- * the chunk kernels run on it, and the results are copied back.  Rows past a
- * sequence's end get q = k = v = 0, alpha = 1, beta = 0, which leave the state
- * unchanged and read nothing.  With bf16, K = V = 128 and chunk 64 (the
- * tensor-core path) each sequence starts a new chunk of one row of chunks per
- * head, and the scans run one stream per (sequence, head) over that
- * sequence's chunks: at most chunk-1 padded rows per sequence.  Other shapes
- * pad every sequence to T.  Host-side checks as for gdn_fwd; every pointer
- * 16-byte aligned except cu_seqlens (4 bytes); S <= 65535.
+ * Method, tensor-core path (bf16, chunk 64, K and V of 16 to 128): the kernels
+ * read and write the packed tensors in place.  Each sequence starts a new
+ * chunk of one row of chunks per head; a device table gives every chunk its
+ * first packed row and its number of rows (at most chunk - 1 padded rows per
+ * sequence).  Rows of a ragged last chunk past the sequence's end are read
+ * (they belong to the next sequence) but count as alpha = 1, beta = 0 and
+ * d_o = 0, which leaves the results unchanged, and are never written.  The
+ * scans run one stream per (sequence, head) over that sequence's chunks.
+ * Other shapes: the sequences are copied into [S, T] streams inside the
+ * workspace (padded rows q = k = v = 0, alpha = 1, beta = 0), gdn_fwd /
+ * gdn_bwd run on them, and the results are copied back.  Host-side checks as
+ * for gdn_fwd; every pointer 16-byte aligned except cu_seqlens (4 bytes);
+ * S <= 65535.
  */
 size_t gdn_varlen_fwd_workspace_bytes(const gdn_problem* p, int64_t total);
 size_t gdn_varlen_bwd_workspace_bytes(const gdn_problem* p, int64_t total);
