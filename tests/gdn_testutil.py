@@ -28,17 +28,33 @@ def to_np(t):
     return None if t is None else t.detach().float().cpu().double().numpy()
 
 
+def poisoned(like, shape=None, dtype=None):
+    """An output buffer filled with NaN, so that any element the kernels do not
+    write shows up in the comparison."""
+    return torch.full(like.shape if shape is None else shape, float("nan"),
+                      dtype=like.dtype if dtype is None else dtype, device=like.device)
+
+
 def gpu_run(w: Workload, inp: dict, backward: bool, saved_mode: str = "saved",
             device="cuda"):
-    """Runs the CUDA path.  Returns a dict of numpy float64 arrays."""
+    """Runs the CUDA path on NaN-filled outputs.  Returns a dict of numpy float64
+    arrays."""
     d = {n: (t.to(device) if t is not None else None) for n, t in inp.items()}
+    B, T, H, _ = d["q"].shape
+    V = d["v"].shape[-1]
+    K = d["q"].shape[-1]
     o, sT, saved = gdn.gdn_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"],
                                d["initial_state"], chunk=w.chunk,
+                               o=poisoned(d["v"]),
+                               final_state=poisoned(d["v"], (B, H, V, K), torch.float32),
                                saved=(backward and saved_mode == "saved"))
     out = dict(o=to_np(o), final_state=to_np(sT))
     if backward:
+        grads = (poisoned(d["q"]), poisoned(d["k"]), poisoned(d["v"]), poisoned(d["alpha"]),
+                 poisoned(d["beta"]))
         g = gdn.gdn_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"],
-                        d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk)
+                        d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk, grads=grads,
+                        d_initial_state=poisoned(d["v"], (B, H, V, K), torch.float32))
         for n, t in zip(("dq", "dk", "dv", "dalpha", "dbeta", "d_initial_state"), g):
             out[n] = to_np(t)
     torch.cuda.synchronize()
@@ -172,5 +188,5 @@ def compare(got: dict, ref: dict, dtype: str, names=None, chunk: int = 64):
     return errs
 
 
-__all__ = ["TOL", "rel_l2", "gpu_run", "oracle_run", "compare", "block_errors", "local_failure", "custom", "make_inputs",
+__all__ = ["TOL", "rel_l2", "gpu_run", "poisoned", "oracle_run", "compare", "block_errors", "local_failure", "custom", "make_inputs",
            "sample_gpu", "select_streams", "select_states", "to_np"]

@@ -12,7 +12,7 @@ import torch
 
 from gated_delta_rule_19_gb300 import gdn
 from gated_delta_rule_19_gb300.inputs import custom, make_inputs, make_prologue_inputs
-from gdn_testutil import compare, to_np
+from gdn_testutil import compare, poisoned, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -55,12 +55,14 @@ def _oracle(oracle_mod, pro, x, r):
 
 
 def _gpu(x, r, C, saved=True):
+    """Both calls on NaN-filled outputs (an element left unwritten shows up)."""
     d = {n: t.cuda() for n, t in x.items()}
     v, s0, do = r["v"].cuda(), r["initial_state"].cuda(), r["d_o"].cuda()
     dsT = r["d_final_state"].cuda() if r["d_final_state"] is not None else None
     args = (d["q_raw"], d["k_raw"], v, d["a_logit"], d["b_logit"], s0)
-    o, sT, sv = gdn.gdn_fwd_raw(*args, chunk=C, saved=saved)
-    g = gdn.gdn_bwd_raw(*args, do, dsT, saved=sv, chunk=C)
+    o, sT, sv = gdn.gdn_fwd_raw(*args, chunk=C, saved=saved, o=poisoned(v), final_state=poisoned(s0))
+    grads = tuple(poisoned(t) for t in (d["q_raw"], d["k_raw"], v, d["a_logit"], d["b_logit"]))
+    g = gdn.gdn_bwd_raw(*args, do, dsT, saved=sv, chunk=C, grads=grads, d_initial_state=poisoned(s0))
     torch.cuda.synchronize()
     return dict(o=o, final_state=sT, **dict(zip(("dq_raw", "dk_raw", "dv", "da", "db", "d_initial_state"), g)))
 

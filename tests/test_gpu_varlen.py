@@ -12,7 +12,7 @@ import torch
 
 from gated_delta_rule_19_gb300 import gdn
 from gated_delta_rule_19_gb300.inputs import custom, make_inputs, make_varlen_inputs
-from gdn_testutil import TOL, local_failure, rel_l2, to_np
+from gdn_testutil import TOL, local_failure, poisoned, rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -32,13 +32,22 @@ def _cuda(inp):
 
 
 def _run_varlen(d, chunk, max_len=None, backward=True):
+    """Both calls on NaN-filled outputs: a row the kernels skip (or a ragged chunk's
+    copy that misses one) shows up in the comparison."""
+    S = d["cu_seqlens"].numel() - 1
+    _, H, K = d["q"].shape
+    V = d["v"].shape[-1]
+    st_shape = (S, H, V, K)
     o, sT, saved = gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], max_len,
-                                      d["initial_state"], chunk=chunk, saved=backward, check=True)
+                                      d["initial_state"], chunk=chunk, saved=backward, check=True,
+                                      o=poisoned(d["v"]), final_state=poisoned(d["v"], st_shape, torch.float32))
     out = dict(o=o, final_state=sT)
     if backward:
+        grads = tuple(poisoned(d[n]) for n in ("q", "k", "v", "alpha", "beta"))
         g = gdn.gdn_varlen_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"], max_len,
                                d["initial_state"], d["d_o"], d["d_final_state"], saved=saved, chunk=chunk,
-                               check=True)
+                               check=True, grads=grads,
+                               d_initial_state=poisoned(d["v"], st_shape, torch.float32))
         out.update(zip(GRADS + ("d_initial_state",), g))
     torch.cuda.synchronize()
     return out
