@@ -81,9 +81,10 @@ struct BwdBufs {
 
 enum class InType { F32 = 0, BF16 = 1 };
 
-// Chunk results of the tensor-core forward (bf16 inputs, K = V = 128, chunk 64),
-// rows indexed chunk * 64 + r with chunk = stream * NC + c:
-//   W [rows, K], Ut [rows, V], Mqk [rows, 64] (bf16); G [rows] (fp32).
+// Chunk results of the tensor-core forward (bf16 inputs, chunk 64, K and V of 16
+// to 128), rows indexed chunk * 64 + r with chunk = stream * NC + c:
+//   W [rows, 128], Ut [rows, 128], Mqk [rows, 64] (bf16; columns past K or V hold
+//   zeros); G [rows] (fp32).
 // err: an int the kernels set (bitwise) when a bounded wait gives up.
 //   T [rows, 64] (bf16, (I + A)^-1; written only when non-null, for the backward).
 struct TcBufs {

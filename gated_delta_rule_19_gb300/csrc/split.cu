@@ -13,7 +13,7 @@
 // the transpose: dS_in = dS_out P + D, D the piece's dS_in from a zero dS_out;
 // combine_bwd chains those from the last piece back.
 //
-// States are [V, K] fp32 (V = K = 128 on the tensor-core path), slot
+// States are [V, K] fp32 with V = K = 128 (the split runs only for that shape), slot
 // (s*P + j)*H + h for piece j of sequence s; combine kernels run 4 rows of one
 // (sequence, head) per CTA, rows being independent.
 
@@ -24,7 +24,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kN = 128;    // K = V on the tensor-core path
+constexpr int kN = 128;    // K = V
 constexpr int kRows = 4;   // state rows per CTA
 constexpr int kTS = kN + 1;  // padded row of the staged transition
 

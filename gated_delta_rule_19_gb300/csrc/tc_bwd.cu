@@ -1,5 +1,5 @@
-// tc_bwd.cu -- tensor-core (tcgen05 + TMA) backward for bf16 inputs, K = V = 128,
-// chunk 64 ("Sparse Delta Memory: layer and kernels", "What the layer computes":
+// tc_bwd.cu -- tensor-core (tcgen05 + TMA) backward for bf16 inputs, chunk 64, K and
+// V of 16 to 128 ("Sparse Delta Memory: layer and kernels", "What the layer computes":
 // the backward walks the chunks in reverse; "OpenGDN", "Core operator
 // reference": the reverse keeps chunk-boundary states and recomputes the 64x64
 // systems).  Three kernels after the chunk recompute (prep_fwd_tc with T):

@@ -1,5 +1,6 @@
-// tc_fwd.cu -- tensor-core (tcgen05 + TMA) forward for bf16 inputs, K = V = 128,
-// chunk 64.
+// tc_fwd.cu -- tensor-core (tcgen05 + TMA) forward for bf16 inputs, chunk 64, K and V
+// of 16 to 128 (tiles and buffers 128 wide; TMA fills the columns past K or V with
+// zeros).  Dense tensors, or a packed batch read in place (kPacked).
 //
 // prep_fwd_tc (chunk-parallel; persistent, two CTAs per SM; "Sparse Delta Memory:
 // layer and kernels", "What the layer computes", Phase 1 and Solve):
@@ -44,7 +45,7 @@ using namespace tc;
 using bf16 = __nv_bfloat16;
 
 constexpr int kC = 64;
-constexpr int kD = 128;  // K = V = 128
+constexpr int kD = 128;  // tile width of K and V (narrower K, V: zero columns)
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }

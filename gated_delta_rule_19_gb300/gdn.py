@@ -519,7 +519,7 @@ def _varlen_problem(q, v, cu_seqlens, max_len, chunk):
     S = cu_seqlens.numel() - 1
     if max_len is None:
         if _flat_layout(q.dtype, K, V, chunk):
-            # the tensor-core kernels lay the sequences out back to back: the bound only
+            # the tensor-core kernels read the packed tensors in place: the bound only
             # checks the offsets and guides the scans' slice width, and the packed total
             # bounds every length, so nothing is read back
             max_len = total

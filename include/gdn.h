@@ -82,7 +82,7 @@ size_t gdn_fwd_workspace_bytes(const gdn_problem* p);
  * ceil(T / chunk) per stream ("OpenGDN", "Core operator reference": the reverse
  * keeps chunk boundaries instead of a token history).  Its contents are private
  * to gdn_fwd/gdn_bwd: float32 [B, H, NC, V, K] in general; on the tensor-core
- * path (bf16 inputs, K = V = 128, chunk 64) bf16 [B, H, NC, K, V] states (they only
+ * path (bf16 inputs, chunk 64) bf16 [B, H, NC, 128, 128] states (they only
  * feed bf16 tensor-core products) followed by the forward's per-chunk solve
  * results, which gdn_bwd then reuses instead of recomputing ("atomic_ops",
  * "Features": the backward reuses forward residuals). */
