@@ -4,6 +4,7 @@
 // the launch sequence on the caller's stream.  Nothing here allocates device
 // memory or synchronises.
 
+#include <limits.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -58,6 +59,13 @@ gdn_status check_problem(const gdn_problem* p, gdn::Dims* d, bool need_chunk = t
     d->V = (int)p->V;
     d->C = need_chunk ? p->chunk : 64;
     d->NC = (int)((p->T + d->C - 1) / d->C);
+    // The tensor-core kernels address their buffers by row with 32-bit TMA
+    // coordinates; the largest row is that of the last chunk's 128-row state, and a
+    // packed batch of B sequences has at most B (NC + 1) chunks per head.
+    if (p->dtype == GDN_BF16 && d->C == 64 &&
+        (int64_t)d->B * d->H * (d->NC + 1) * 128 > (int64_t)INT32_MAX)
+        return fail(GDN_ERR_UNSUPPORTED, "B*H*(ceil(T/64)+1)*128 = %lld exceeds 2^31-1 (32-bit row coordinates)",
+                    (long long)((int64_t)d->B * d->H * (d->NC + 1) * 128));
     return GDN_OK;
 }
 

@@ -35,7 +35,9 @@
  *
  * Requirements: B, H >= 0, T >= 0; K, V in {16, 32, 64, 128}; chunk in
  * {16, 32, 64}; every pointer 16-byte aligned; outputs must not overlap inputs
- * or each other.  T need not be a multiple of chunk (the tail chunk is padded
+ * or each other.  Size limits (GDN_ERR_UNSUPPORTED beyond them): B, H <= 65535,
+ * T <= 2^30, and for bf16 at chunk 64, which runs on the tensor-core kernels
+ * whose TMA row coordinates are 32-bit, B * H * (ceil(T/64) + 1) * 128 < 2^31.  T need not be a multiple of chunk (the tail chunk is padded
  * inside the kernels with alpha = 1, beta = 0, which leaves the state unchanged).
  */
 #ifndef GDN_H_
@@ -51,7 +53,7 @@ extern "C" {
 typedef enum {
     GDN_OK = 0,
     GDN_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size   */
-    GDN_ERR_UNSUPPORTED = 2, /* K, V, chunk or dtype outside the supported set  */
+    GDN_ERR_UNSUPPORTED = 2, /* K, V, chunk, dtype or a size outside the limits */
     GDN_ERR_WORKSPACE = 3,   /* workspace smaller than the *_workspace_bytes()  */
     GDN_ERR_CUDA = 4         /* a kernel launch failed (cudaGetLastError)        */
 } gdn_status;

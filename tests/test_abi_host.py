@@ -136,6 +136,16 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert _bwd(lib, ok, dk=FAKE + (6 << 30) + 256) == INVALID  # dk overlaps dq
     assert _bwd(lib, ok, dv=FAKE) == INVALID  # dv overlaps q
     assert _bwd(lib, lib.make_problem(1, 8, 1, 16, 256, 16, 1)) == UNSUP
+    # bf16 at chunk 64 runs on the tensor-core kernels, whose TMA row coordinates are
+    # 32-bit: B*H*(ceil(T/64)+1)*128 must stay below 2^31 (the same token count in
+    # float32 runs on the CUDA-core kernels, which index with 64 bits)
+    big = lib.make_problem(64, 1 << 18, 256, 16, 16, 64, 1)
+    assert _fwd(lib, big) == UNSUP
+    assert "32-bit" in lib.gdn_last_error()
+    assert lib.gdn_fwd_workspace_bytes(big) == 0
+    assert _fwd(lib, lib.make_problem(64, 1 << 18, 256, 16, 16, 64, 0), ws_bytes=16) == WS
+    edge = lib.make_problem(1, 64 * ((1 << 24) - 2), 1, 16, 16, 64, 1)  # (NC + 1) * 128 = 2^31 - 128
+    assert lib.gdn_fwd_workspace_bytes(edge) > 0
 
 
 def test_binding_refuses_cpu_tensors(lib):
