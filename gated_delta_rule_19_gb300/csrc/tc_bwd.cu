@@ -125,25 +125,6 @@ __device__ __forceinline__ void tmem_cols2(uint32_t ta, uint32_t tb, float* fa, 
     }
 }
 
-// Column sums of a 32 x 32 block held one row per lane: on entry lane l holds
-// v[0..31] (row l); on return lane l holds the sum over the 32 rows of column l.
-// Butterfly reduce-scatter, 31 shuffles.
-__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-        const bool upper = lane & w;
-#pragma unroll
-        for (int j = 0; j < w; ++j) {
-            // keep the half of the columns this lane is responsible for, send the other
-            const float send = upper ? v[j] : v[j + w];
-            const float keep = upper ? v[j + w] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-    }
-    return v[0];
-}
-
 // Column sums of a 32 x 16 block held one row per lane: on return lanes l and l+16
 // hold the sum over the 32 rows of column l % 16.  15 + 1 shuffles.
 __device__ __forceinline__ float warp_colsum16(float (&v)[16]) {
@@ -1134,7 +1115,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 }
             }
         };
-        const int row0 = (int)(ch * kC), krow0 = (int)(ch * kD);
+        const int krow0 = (int)(ch * kD);
         trk = 0;
         if (warp == 3) {
             const int nx = __shfl_sync(0xffffffffu, claimed, 0);

@@ -187,6 +187,7 @@ constexpr int P_VEC = P_X + 32 * kXS * 4;  // G (log2 units), gamma, beta
 constexpr int P_BAR = P_VEC + 3 * 64 * 4;
 constexpr int P_END = P_BAR + 64;
 constexpr size_t kPrepSmem = P_END + 1024;
+static_assert(P_K1 == P_K0 + 16384 && P_Q1 == P_Q0 + 16384, "64-column halves 16 KB apart");
 static_assert(P_AF + 64 * kAS * 4 <= P_T2 + 8192, "A overlaps only T1 / T2");
 static_assert(P_WS + 16384 <= P_X && P_US + 16384 <= P_T2 + 8192, "output tiles fit the dead regions");
 static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
