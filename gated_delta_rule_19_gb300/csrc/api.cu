@@ -35,6 +35,10 @@ bool supported_dim(int64_t x) { return x == 16 || x == 32 || x == 64 || x == 128
 
 // Checks the problem and fills Dims.  Returns GDN_OK or an error status.  With
 // need_chunk false the chunk field is not used (gdn_decode) and is not checked.
+// Limit of the tensor-core kernels' bounded waits for calls made from now on, in
+// nanoseconds (0: the kernels' default); see gdn_test_set_wait_limit.
+uint32_t g_wait_limit_ns = 0;
+
 gdn_status check_problem(const gdn_problem* p, gdn::Dims* d, bool need_chunk = true) {
     if (!p) return fail(GDN_ERR_INVALID_ARG, "problem pointer is NULL");
     if (p->B < 0 || p->T < 0 || p->H < 0)
@@ -59,6 +63,7 @@ gdn_status check_problem(const gdn_problem* p, gdn::Dims* d, bool need_chunk = t
     d->V = (int)p->V;
     d->C = need_chunk ? p->chunk : 64;
     d->NC = (int)((p->T + d->C - 1) / d->C);
+    d->wait_ns = g_wait_limit_ns;
     // The tensor-core kernels address their buffers by row with 32-bit TMA
     // coordinates; the largest row is that of the last chunk's 128-row state, and a
     // packed batch of B sequences has at most B (NC + 1) chunks per head.
@@ -488,6 +493,11 @@ const char* gdn_status_string(gdn_status s) {
 }
 
 const char* gdn_last_error(void) { return g_err; }
+
+gdn_status gdn_test_set_wait_limit(uint32_t ns) {
+    g_wait_limit_ns = ns;
+    return GDN_OK;
+}
 
 size_t gdn_fwd_workspace_bytes(const gdn_problem* p) {
     gdn::Dims d{};

@@ -21,6 +21,9 @@ struct Dims {
     // dense tensors, where chunk c starts at c * C.
     const int* tok = nullptr;
     const int* len = nullptr;
+    // Limit of the tensor-core kernels' bounded waits in nanoseconds (0: the default
+    // of 2 s); set by the test hook gdn_test_set_wait_limit.
+    uint32_t wait_ns = 0;
     __host__ __device__ int64_t NS() const { return (int64_t)B * H; }
     // The chunk (index (b * H + h) * NC + c) that work item wi of a chunk-parallel
     // kernel takes: every stream's chunk c before any chunk c + 1, c ascending or

@@ -72,14 +72,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, sets bit `code` in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+// Waits for the phase with the given parity to complete.  Gives up after limit_ns
+// (0: kWaitLimitNs), sets bit `code` in *err (if not NULL) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code,
+                                          uint32_t limit_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit = limit_ns ? limit_ns : kWaitLimitNs;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit) {
             if (err) atomicOr(err, code);
             return false;
         }

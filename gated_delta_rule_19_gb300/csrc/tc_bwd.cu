@@ -255,7 +255,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // chunk's tokens (a packed batch's ragged chunk reads the next sequence's dO)
     // are zero.
     auto write_gdo_operand = [&](int it2, bool& okk) {
-        okk = mbar_wait(&tbar[it2 % NS], (it2 / NS) & 1, err, 8) && okk;
+        okk = mbar_wait(&tbar[it2 % NS], (it2 / NS) & 1, err, 8, d.wait_ns) && okk;
         const bool live = !kPacked || r < chunk_valid<true>(d, c0 + NC - 1 - it2);
         const float gr = expf(Gr_n);
         const unsigned char* dsrc = sm + (it2 % NS) * P::STAGE + P::OFF_DO;
@@ -308,7 +308,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int stg = it % NS;
             unsigned char* st = sm + stg * P::STAGE;
             if (mma_issuer) {
-                ok = mbar_wait(&tbar[stg], (it / NS) & 1, err, 8) && ok;
+                ok = mbar_wait(&tbar[stg], (it / NS) & 1, err, 8, d.wait_ns) && ok;
                 if (ok) {
                     // rows 64-127 of the first two A operands are neighbouring tiles (unused)
                     const uint64_t dK = sdesc(smem_u32(st + P::OFF_K), 16, 1024, SW_128B);
@@ -364,7 +364,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // bar2 of it - 1 was waited before the previous barrier 2); it is
                 // first read by the gamma dO operand during iteration it + 1.
                 if (NS >= 3 && ok && it > 0 && issued < NC) {
-                    ok = mbar_wait(bar2, (it - 1) & 1, err, 32) && ok;
+                    ok = mbar_wait(bar2, (it - 1) & 1, err, 32, d.wait_ns) && ok;
                     if (ok) issue_loads(issued++);
                 }
                 bulk_wait_read0();  // it has read dS1^T (rewritten after barrier 1)
@@ -380,7 +380,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // with two stages, iteration it + NS into this iteration's stage as
                 // soon as its MMAs are done (its gamma dO operand is read next iteration)
                 if (NS < 3 && ok && issued < NC) {
-                    ok = mbar_wait(bar2, it & 1, err, 32) && ok;
+                    ok = mbar_wait(bar2, it & 1, err, 32, d.wait_ns) && ok;
                     if (ok) issue_loads(issued++);
                 }
                 bulk_wait_read1();  // the dU store of the previous iteration has read its buffer
@@ -404,7 +404,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 Gr_n = G[(chunk - 1) * kC + r];
             }
             if (urow) {
-                ok = mbar_wait(bar1, it & 1, err, 16) && ok;
+                ok = mbar_wait(bar1, it & 1, err, 16, d.wait_ns) && ok;
                 __syncwarp();
                 fence_after_sync();
                 // dU = Mqk^T dO + e_r (K dS1^T)  (row r, columns cb .. cb+HV)
@@ -439,7 +439,7 @@ scan_bwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             ok = __syncthreads_and(ok);  // 1
             if (!ok) break;
             fence_after_sync();
-            ok = mbar_wait(bar2, it & 1, err, 32) && ok;
+            ok = mbar_wait(bar2, it & 1, err, 32, d.wait_ns) && ok;
             __syncwarp();
             fence_after_sync();
             {
@@ -681,7 +681,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         // ---- phase 1 (K over v): S0^T [dO; dU]^T (N=128), [dO; dU] U^T and dS1^T U^T (N=64)
         if (tid == kIssuer) {
-            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[0], ph, err, 1, d.wait_ns) && ok;
             if (ok) {
                 const uint32_t id128 = idesc_bf16(128, 128, false, false);
                 const uint32_t id64 = idesc_bf16(128, 64, false, false);
@@ -698,7 +698,7 @@ grad_qk_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 ++n1;
             }
         }
-        ok = mbar_wait(&bars[0], ph, err, 1) && ok;  // S0 and dS1 (read below)
+        ok = mbar_wait(&bars[0], ph, err, 1, d.wait_ns) && ok;  // S0 and dS1 (read below)
         {   // <dS1, S0> over the chunk (both tiles share one layout), coalesced, while
             // phase 1's MMAs run
             const uint4* a = (const uint4*)(sm + qk::S0) + tid;
@@ -1148,7 +1148,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         fence_after_sync();
         nxt = *s_next;
         const bool has_next = nxt < nchunks;
-        ok = mbar_wait(&bars[0], ph, err, 1) && ok;
+        ok = mbar_wait(&bars[0], ph, err, 1, d.wait_ns) && ok;
         // ---- phase 1: Qm = dW K^T (K over k), P = dU V^T (K over v), KK = K K^T   (M=128: rows 64-127 unused)
         if (tid == 0 && ok) {
             const uint32_t idq = idesc_bf16(128, 64, true, false);
@@ -1185,7 +1185,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 *(uint4*)(sm + wy::T2 + tile_off(64, r, cb + 8 * q)) = pack8(f2);
             }
         }
-        ok = mbar_wait(&bars[1], 0, err, 2) && ok;
+        ok = mbar_wait(&bars[1], 0, err, 2, d.wait_ns) && ok;
         __syncwarp();
         fence_after_sync();
         // V is dead: bring in the dK partial of the first gradient kernel for phase 4
@@ -1241,7 +1241,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             for (int s2 = 0; s2 < 4; ++s2)
                 mma_bf16_ss(tDV, desc_add(dt2m, s2 * 2048), desc_add(dum, s2 * 2048), idv, s2 > 0);
         }
-        if (ok) ok = mbar_wait(&bars[1], 1, err, 4);
+        if (ok) ok = mbar_wait(&bars[1], 1, err, 4, d.wait_ns);
         __syncwarp();
         fence_after_sync();
         if (urow) {
@@ -1264,7 +1264,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             mma_commit(&bars[1]);
             trk += 4;
         }
-        if (ok) ok = mbar_wait(&bars[1], 0, err, 8);
+        if (ok) ok = mbar_wait(&bars[1], 0, err, 8, d.wait_ns);
         __syncwarp();
         fence_after_sync();
         if (urow) {
@@ -1343,7 +1343,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     if (64 * j < d.V) tma_store_4d(&tm_dv, sm + wy::DV + j * 8192, 64 * j, h, t0, b);
                 bulk_commit();
             }
-            ok = mbar_wait(&bars[2], ph, err, 16);
+            ok = mbar_wait(&bars[2], ph, err, 16, d.wait_ns);
             if (ok) {
                 const uint32_t id_mk = idesc_bf16(128, 128, true, false);   // A MN-major, B K-major
                 const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
@@ -1407,7 +1407,7 @@ grad_wy_tc(Dims d, const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             }
         }
         ok = __syncthreads_and(ok);  // the issuer's load wait is every thread's
-        if (ok) ok = mbar_wait(&bars[1], 1, err, 16);
+        if (ok) ok = mbar_wait(&bars[1], 1, err, 16, d.wait_ns);
         __syncwarp();
         fence_after_sync();
         // every input slot is free (the dV store has read the dU slot): the next chunk's

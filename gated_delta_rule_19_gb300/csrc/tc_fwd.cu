@@ -307,8 +307,8 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // is conflict-free; rows 0-63 are the K tile's, 64-127 the Q tile's.
             int b, h, t0;
             decode(ch, b, h, t0);
-            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
-            ok = mbar_wait(&bars[1], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[0], ph, err, 1, d.wait_ns) && ok;
+            ok = mbar_wait(&bars[1], ph, err, 1, d.wait_ns) && ok;
             const int pc = tid & 15, hf = pc >> 3, p = pc & 7;
 #pragma unroll 2
             for (int it = 0; it < 8; ++it) {
@@ -344,8 +344,8 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (!ok) break;
         }
         if (tid == 0) {
-            ok = mbar_wait(&bars[0], ph, err, 1) && ok;
-            ok = mbar_wait(&bars[1], ph, err, 1) && ok;
+            ok = mbar_wait(&bars[0], ph, err, 1, d.wait_ns) && ok;
+            ok = mbar_wait(&bars[1], ph, err, 1, d.wait_ns) && ok;
             if (ok) {
                 // [K; Q] K^T = [K K^T ; Q K^T] into columns 0-63 (M=128, N=64, K over k)
                 const uint32_t id = idesc_bf16(128, 64, false, false);
@@ -394,7 +394,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (has_next) load_gates(nxt);  // consumed next iteration
         }
         __syncthreads();  // gates visible; the output tiles are writable
-        ok = mbar_wait(&bars[2], ph, err, 2) && ok;
+        ok = mbar_wait(&bars[2], ph, err, 2, d.wait_ns) && ok;
         __syncwarp();
         fence_after_sync();
         if (tid == kLoader && ok && has_next) {  // the Q tiles are free
@@ -502,7 +502,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
         fence_before_sync();
         ok = __syncthreads_and(ok);
         fence_after_sync();
-        if (tid == 0) ok = mbar_wait(&bars[4], ph, err, 1) && ok;
+        if (tid == 0) ok = mbar_wait(&bars[4], ph, err, 1, d.wait_ns) && ok;
         if (tid == 0 && ok) {
             // [T1; T2] [K | V] (M=128, N=256, K over tokens): rows 0-63 of columns 0-127
             // are W = T1 K, rows 64-127 of columns 128-255 are Ut = T2 V.
@@ -514,7 +514,7 @@ prep_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mma_commit(&bars[3]);
             w_last = n;
         }
-        if (ok) ok = mbar_wait(&bars[3], ph, err, 4);
+        if (ok) ok = mbar_wait(&bars[3], ph, err, 4, d.wait_ns);
         __syncwarp();
         fence_after_sync();
         if (tid == kLoader && ok && has_next) {  // the K and V tiles are free
@@ -804,7 +804,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     // Output of chunk cc (threads on lanes 64-127): O = gamma Y + Mqk U.
     auto output_epilogue = [&](int cc, bool& okk) {
-        okk = mbar_wait(barO, cc & 1, err, 64) && okk;
+        okk = mbar_wait(barO, cc & 1, err, 64, d.wait_ns) && okk;
         __syncwarp();
         fence_after_sync();
         float y[HV], ov[HV];
@@ -869,7 +869,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int stg = c % NS;
             unsigned char* st = sm + stg * P::STAGE;
             if (mma_issuer) {
-                ok = mbar_wait(&tbar[stg], (c / NS) & 1, err, 8) && ok;
+                ok = mbar_wait(&tbar[stg], (c / NS) & 1, err, 8, d.wait_ns) && ok;
                 if (ok) {
                     // [X; Y] = [W; Q] S0^T in one M=128 MMA chain
                     const uint64_t dWQ = sdesc(smem_u32(st + P::OFF_WQ), 16, 1024, SW_128B);
@@ -919,7 +919,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // chunk c + NS - 1 into the stage chunk c - 1 used, once its last
                 // MMAs (the output term) have read it
                 if (ok && issued < NC) {
-                    if (c > 0) ok = mbar_wait(barO, (c - 1) & 1, err, 64) && ok;
+                    if (c > 0) ok = mbar_wait(barO, (c - 1) & 1, err, 64, d.wait_ns) && ok;
                     if (ok) issue_loads(issued++);
                 }
                 bulk_wait_read0();  // the states store has read S0^T (rewritten after barrier 1)
@@ -972,8 +972,8 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (!urow && c > 0) output_epilogue(c - 1, ok);  // overlaps this chunk's first MMAs
             gr_prev = gr;
             if (urow) {
-                ok = mbar_wait(&tbar[stg], (c / NS) & 1, err, 8) && ok;  // Ut slice is read below
-                ok = mbar_wait(barXY, c & 1, err, 16) && ok;
+                ok = mbar_wait(&tbar[stg], (c / NS) & 1, err, 8, d.wait_ns) && ok;  // Ut slice is read below
+                ok = mbar_wait(barXY, c & 1, err, 16, d.wait_ns) && ok;
                 __syncwarp();
                 fence_after_sync();
                 // U = Ut - X, Uh = e_r U  (row r, columns cb .. cb+HV)
@@ -1013,7 +1013,7 @@ scan_fwd_tc(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_const
             ok = __syncthreads_and(ok);  // 1
             if (!ok) break;
             fence_after_sync();
-            ok = mbar_wait(barS, c & 1, err, 32) && ok;
+            ok = mbar_wait(barS, c & 1, err, 32, d.wait_ns) && ok;
             __syncwarp();
             fence_after_sync();
             // S1^T = gamma_C S0^T + K^T Uh

@@ -92,6 +92,8 @@ def load_library():
     lib.gdn_count_nonfinite.restype = ctypes.c_int
     lib.gdn_set_sequence_split.argtypes = [ctypes.c_int]
     lib.gdn_set_sequence_split.restype = ctypes.c_int
+    lib.gdn_test_set_wait_limit.argtypes = [ctypes.c_uint32]
+    lib.gdn_test_set_wait_limit.restype = ctypes.c_int
     lib.gdn_get_sequence_split.restype = ctypes.c_int
     lib.gdn_num_kernels.restype = ctypes.c_int
     lib.gdn_kernel_name.argtypes = [ctypes.c_int]
@@ -113,7 +115,8 @@ EXPORTED = ("gdn_version", "gdn_status_string", "gdn_last_error", "gdn_fwd_works
             "gdn_profiler_summary", "gdn_profiler_release", "gdn_fwd_noalloc", "gdn_decode",
             "gdn_prologue_fwd", "gdn_prologue_bwd", "gdn_varlen_fwd_workspace_bytes",
             "gdn_varlen_bwd_workspace_bytes", "gdn_varlen_saved_bytes", "gdn_varlen_fwd", "gdn_varlen_bwd",
-            "gdn_set_sequence_split", "gdn_get_sequence_split", "gdn_count_nonfinite")
+            "gdn_set_sequence_split", "gdn_get_sequence_split", "gdn_count_nonfinite",
+            "gdn_test_set_wait_limit")
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -393,6 +396,12 @@ def gdn_set_sequence_split(pieces: int) -> None:
     """Within-call sequence split policy for the calls that follow: 0 automatic
     (default), 1 never, n >= 2 pieces per sequence (see include/gdn.h)."""
     _check(load_library().gdn_set_sequence_split(int(pieces)))
+
+
+def gdn_test_set_wait_limit(ns: int) -> None:
+    """Test hook: limit, in nanoseconds, of the tensor-core kernels' bounded waits
+    in the calls that follow (0 restores the default of 2 s); see include/gdn.h."""
+    _check(load_library().gdn_test_set_wait_limit(int(ns)))
 
 
 def gdn_get_sequence_split() -> int:

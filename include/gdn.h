@@ -395,6 +395,23 @@ gdn_status gdn_decode(const gdn_problem* p, const void* q, const void* k, const 
 gdn_status gdn_count_nonfinite(const void* x, int64_t n, gdn_dtype dtype, int64_t* count, void* stream);
 
 /*
+ * gdn_test_set_wait_limit -- test hook for the error path of the tensor-core
+ * kernels.  Every wait of those kernels on an mbarrier (a TMA copy or a
+ * tensor-core operation completing) gives up after a limit, 2 s by default: the
+ * kernel then sets a bit in the workspace's error word (its first int; the
+ * kernel-specific code is the bit), stops issuing work, waits with the default
+ * limit for the copies and tensor-core operations it already issued, frees its
+ * tensor memory and exits, so the CUDA context stays usable.  This call sets the
+ * limit, in nanoseconds, for the calls made after it (0 restores the default), of
+ * every such wait except those of the q-side gradient kernel for its tensor-core
+ * operations (that kernel takes it for its loads only).  With a limit of a few
+ * nanoseconds the first wait that does not succeed at once gives up: the call
+ * still returns GDN_OK, its error word is nonzero and its outputs are not valid.  Process-wide (it takes effect when a call's arguments
+ * are checked); not for production use.
+ */
+gdn_status gdn_test_set_wait_limit(uint32_t ns);
+
+/*
  * Optional launch timer, for benchmarks.  While started, every kernel launch of
  * gdn_fwd/gdn_bwd is bracketed by two CUDA events recorded on the call's stream
  * (up to `capacity` launches; later launches are not timed).  The events are

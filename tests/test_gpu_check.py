@@ -1,8 +1,11 @@
-"""GPU tests of gdn_count_nonfinite: the count equals torch's on tensors with NaN
-and +-inf planted at known places (fp32 and bf16, sizes with ragged tails),
-calls accumulate, n = 0 leaves the count alone, and a NaN in one head's input
-to gdn_fwd shows up in that head's outputs only (the (b, h) streams are
-independent)."""
+"""GPU tests of failure detection.  gdn_count_nonfinite: the count equals torch's
+on tensors with NaN and +-inf planted at known places (fp32 and bf16, sizes with
+ragged tails), calls accumulate, n = 0 leaves the count alone, and a NaN in one
+head's input to gdn_fwd shows up in that head's outputs only (the (b, h) streams
+are independent).  Bounded waits: with the wait limit cut to a few nanoseconds
+every tensor-core kernel of a forward and a backward call takes its error path,
+the calls report it in their error words, and the next calls, at the default
+limit, give the same bits as before (the context and the device stay usable)."""
 import pytest
 import torch
 
@@ -65,3 +68,35 @@ def test_nan_input_reaches_only_its_stream():
     o, sT = run()
     assert _count(o[:, :, 1]) > 0 and _count(sT[:, 1]) > 0
     assert _count(o[:, :, 0]) == 0 and _count(sT[:, 0]) == 0
+
+
+def _step(w, d, wsf, wsb):
+    args = (d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["initial_state"])
+    o, s_t, saved = gdn.gdn_fwd(*args, chunk=w.chunk, saved=True, workspace=wsf)
+    g = gdn.gdn_bwd(*args, d["d_o"], d["d_final_state"], saved=saved, chunk=w.chunk, workspace=wsb)
+    torch.cuda.synchronize()
+    words = [int(ws[:4].view(torch.int32).item()) for ws in (wsf, wsb)]
+    return [o, s_t] + [x for x in g if x is not None], words
+
+
+def test_bounded_waits_give_up_and_the_context_stays_usable():
+    # 2 x 6 streams of 16 chunks: the scans, prep and both gradient kernels run
+    w = custom(B=2, T=1000, H=6, K=128, V=128, chunk=64, dtype="bf16", seed=51, init_std=0.1,
+               dfinal_std=0.01)
+    d = {n: (t.cuda() if t is not None else None) for n, t in make_inputs(w).items()}
+    p = gdn.make_problem(w.B, w.T, w.H, w.K, w.V, w.chunk, torch.bfloat16)
+    wsf = torch.zeros(gdn.gdn_fwd_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    wsb = torch.zeros(gdn.gdn_bwd_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    ref, words = _step(w, d, wsf, wsb)
+    assert words == [0, 0]
+    try:
+        gdn.gdn_test_set_wait_limit(2)  # 2 ns: the first wait that does not succeed at once gives up
+        _, words = _step(w, d, wsf, wsb)
+    finally:
+        gdn.gdn_test_set_wait_limit(0)
+    assert words[0] != 0 and words[1] != 0, words
+    for _ in range(2):
+        got, words = _step(w, d, wsf, wsb)
+        assert words == [0, 0]
+        for i, (a, b) in enumerate(zip(ref, got)):
+            assert torch.equal(a, b), f"output {i} differs after the error path ran"
