@@ -10,7 +10,8 @@
 //     dS0^T = gamma_C dS1^T + Q^T diag(gamma) dO - W^T dU
 //   writes dU and dS1 (bf16) per chunk and d(initial state).
 //
-// grad_qk_tc (chunk-parallel; persistent, one CTA per SM): U = Ut - W S0^T, then
+// grad_qk_tc (chunk-parallel; persistent, one CTA per SM), from U = Ut - W S0^T as
+// the forward scan wrote it:
 //     dMqk = dO U^T,   dQK = Gam .* lower(dMqk)
 //     dQ^T = S0^T (diag(gamma) dO)^T + K^T dQK^T                 -> dq
 //     dK^T (part) = dS1^T (diag(e) U)^T + Q^T dQK                -> scratch
@@ -24,7 +25,8 @@
 //     dK^T = dK^T (part) + dW^T T diag(beta gamma) + K^T (E + E^T) -> dk
 //     dbeta, dG (rest), dlog alpha = reverse cumsum of dG, dalpha = dlog alpha / alpha.
 //
-// Every wait is bounded (2 s) and raises the error flag when it gives up.
+// Every wait is bounded (2 s unless a test sets a shorter limit) and raises the error
+// flag when it gives up.
 
 #include <algorithm>
 

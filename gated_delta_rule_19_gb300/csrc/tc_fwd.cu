@@ -27,8 +27,9 @@
 //   writes the chunk-start states for the backward also writes U (bf16) in place
 //   over its U~ slice: the backward's chunk gradients read U, never U~.
 //
-// Every wait is bounded (2 s); a wait that gives up raises the error flag, and
-// the block leaves its loop together (block-wide vote) after draining its copies.
+// Every wait is bounded (2 s unless a test sets a shorter limit); a wait that gives
+// up raises the error flag, and the block leaves its loop together (block-wide
+// vote) after draining its copies.
 
 #include <cudaTypedefs.h>
 
