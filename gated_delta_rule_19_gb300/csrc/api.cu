@@ -33,12 +33,13 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool supported_dim(int64_t x) { return x == 16 || x == 32 || x == 64 || x == 128; }
 
-// Checks the problem and fills Dims.  Returns GDN_OK or an error status.  With
-// need_chunk false the chunk field is not used (gdn_decode) and is not checked.
 // Limit of the tensor-core kernels' bounded waits for calls made from now on, in
 // nanoseconds (0: the kernels' default); see gdn_test_set_wait_limit.
 uint32_t g_wait_limit_ns = 0;
 
+// Checks the problem and fills Dims.  Returns GDN_OK or an error status.  With
+// need_chunk false the chunk field is not used (gdn_decode, the prologue) and is
+// not checked.
 gdn_status check_problem(const gdn_problem* p, gdn::Dims* d, bool need_chunk = true) {
     if (!p) return fail(GDN_ERR_INVALID_ARG, "problem pointer is NULL");
     if (p->B < 0 || p->T < 0 || p->H < 0)
@@ -67,7 +68,7 @@ gdn_status check_problem(const gdn_problem* p, gdn::Dims* d, bool need_chunk = t
     // The tensor-core kernels address their buffers by row with 32-bit TMA
     // coordinates; the largest row is that of the last chunk's 128-row state, and a
     // packed batch of B sequences has at most B (NC + 1) chunks per head.
-    if (p->dtype == GDN_BF16 && d->C == 64 &&
+    if (need_chunk && p->dtype == GDN_BF16 && d->C == 64 &&
         (int64_t)d->B * d->H * (d->NC + 1) * 128 > (int64_t)INT32_MAX)
         return fail(GDN_ERR_UNSUPPORTED, "B*H*(ceil(T/64)+1)*128 = %lld exceeds 2^31-1 (32-bit row coordinates)",
                     (long long)((int64_t)d->B * d->H * (d->NC + 1) * 128));
