@@ -44,6 +44,29 @@ def _dense_cases(n=60, seed=2024):
     return cases
 
 
+def _large_cases(seed=31337):
+    """Long streams with slow decay (the state carried across up to 47 chunks), and
+    batches of up to 320 streams (more scan CTAs than one wave of SMs)."""
+    rng = np.random.RandomState(seed)
+    cases = []
+    for i in range(12):
+        dtype = "bf16" if rng.rand() < 0.8 else "f32"
+        chunk = 64 if (dtype == "bf16" and rng.rand() < 0.8) else int(rng.choice([16, 32, 64]))
+        cases.append(dict(B=int(rng.randint(1, 3)), T=int(rng.randint(700, 3000)), H=int(rng.randint(1, 3)),
+                          K=int(rng.choice(DIMS)), V=int(rng.choice(DIMS)), chunk=chunk, dtype=dtype,
+                          seed=110000 + i, init_std=float(rng.choice([0.0, 0.3])),
+                          dfinal_std=float(rng.choice([0.0, 0.05])),
+                          alpha_lo=float(rng.choice([0.0, 0.99, 0.999, 0.9999]))))
+    for i in range(10):
+        dtype = "bf16" if rng.rand() < 0.8 else "f32"
+        chunk = 64 if (dtype == "bf16" and rng.rand() < 0.8) else int(rng.choice([16, 32, 64]))
+        cases.append(dict(B=int(rng.randint(8, 20)), T=int(rng.randint(1, 200)), H=int(rng.randint(8, 17)),
+                          K=int(rng.choice(DIMS)), V=int(rng.choice(DIMS)), chunk=chunk, dtype=dtype,
+                          seed=120000 + i, init_std=float(rng.choice([0.0, 0.3])),
+                          dfinal_std=float(rng.choice([0.0, 0.05])), alpha_lo=float(rng.choice([0.0, 0.97]))))
+    return cases
+
+
 def _varlen_cases(n=20, seed=4048):
     rng = np.random.RandomState(seed)
     cases = []
@@ -78,7 +101,7 @@ def pro():
     return prologue
 
 
-@pytest.mark.parametrize("case", _dense_cases(), ids=lambda c: "B{B}_T{T}_H{H}_K{K}_V{V}_C{chunk}_{dtype}".format(**c))
+@pytest.mark.parametrize("case", _dense_cases() + _large_cases(), ids=lambda c: "B{B}_T{T}_H{H}_K{K}_V{V}_C{chunk}_{dtype}".format(**c))
 def test_dense_random_shapes(oracle_mod, case):
     w = custom(**case)
     inp = make_inputs(w)
